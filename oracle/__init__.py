@@ -1,0 +1,292 @@
+"""CPU oracle for the block-quantised GEMV -- TEST INFRASTRUCTURE ONLY.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
+``bench.py`` may import this package.  It shares no code with the CUDA
+library: the arithmetic lives in ``oracle.c`` (plain C99, built here with gcc
+``-O2 -ffp-contract=off``) and in the numpy helpers below, which only write
+block fields into bytes (the inverse of the pages' layouts) and restate the
+IQ3 encoder of page 4 "iq3_pack.py" (function ``encode``) for round-trip
+tests.
+
+Every function is pinned by ``tests/test_oracle_pins.py``; no function here is
+"parity unpinned".
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "oracle.c")
+_BUILD = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_BUILD, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+QK = 256
+Q4K_BYTES = 144
+IQ3_BYTES = 98
+
+
+def build(force: bool = False) -> str:
+    """Compile oracle.c into oracle/_build/liboracle.so (gcc, OpenMP)."""
+    os.makedirs(_BUILD, exist_ok=True)
+    if (not force and os.path.exists(_LIB_PATH)
+            and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
+        return _LIB_PATH
+    tmp = _LIB_PATH + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-std=c99", "-O2", "-ffp-contract=off", "-fno-fast-math", "-fopenmp",
+           "-fPIC", "-shared", "-o", tmp, _SRC, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        lib = ctypes.CDLL(build())
+        u8p = ctypes.POINTER(ctypes.c_uint8)
+        f32p = ctypes.POINTER(ctypes.c_float)
+        f64p = ctypes.POINTER(ctypes.c_double)
+        i64p = ctypes.POINTER(ctypes.c_int64)
+        i64 = ctypes.c_int64
+        lib.oracle_f16_to_f32_array.argtypes = [ctypes.POINTER(ctypes.c_uint16), f32p, i64]
+        lib.oracle_q4k_scale_min.argtypes = [u8p, u8p, u8p]
+        lib.oracle_dequant_q4k.argtypes = [u8p, i64, i64, f32p]
+        lib.oracle_dequant_iq3.argtypes = [u8p, u8p, i64, i64, f32p]
+        lib.oracle_gemv_q4k.argtypes = [u8p, f32p, ctypes.c_int, i64, i64p, i64, f64p, f64p,
+                                        ctypes.c_int]
+        lib.oracle_gemv_iq3.argtypes = [u8p, u8p, f32p, ctypes.c_int, i64, i64p, i64, f64p,
+                                        f64p, ctypes.c_int]
+        lib.oracle_max_threads.restype = ctypes.c_int
+        _lib = lib
+        return lib
+
+
+def _ptr(a: np.ndarray, ctype):
+    return a.ctypes.data_as(ctypes.POINTER(ctype))
+
+
+def max_threads() -> int:
+    return int(_load().oracle_max_threads())
+
+
+# --------------------------------------------------------------- C oracle calls
+def f16_to_f32(h: np.ndarray) -> np.ndarray:
+    """fp16 bit patterns (uint16) -> fp32 values, IEEE definition."""
+    h = np.ascontiguousarray(h, dtype=np.uint16)
+    out = np.empty(h.shape, dtype=np.float32)
+    _load().oracle_f16_to_f32_array(_ptr(h, ctypes.c_uint16), _ptr(out, ctypes.c_float), h.size)
+    return out
+
+
+def q4k_scale_min(p12) -> tuple[np.ndarray, np.ndarray]:
+    """The 12 packed Q4_K bytes -> (sc[8], mn[8]) as uint8 (page 1 unpack)."""
+    p = np.ascontiguousarray(p12, dtype=np.uint8).reshape(12)
+    sc = np.empty(8, np.uint8)
+    mn = np.empty(8, np.uint8)
+    _load().oracle_q4k_scale_min(_ptr(p, ctypes.c_uint8), _ptr(sc, ctypes.c_uint8),
+                                 _ptr(mn, ctypes.c_uint8))
+    return sc, mn
+
+
+def _check_rows(W: np.ndarray, K: int, block_bytes: int) -> int:
+    if K % QK:
+        raise ValueError(f"K must be a multiple of {QK}")
+    W = np.asarray(W)
+    row = K // QK * block_bytes
+    if W.size % row:
+        raise ValueError("W size is not a whole number of rows")
+    return W.size // row
+
+
+def dequant_q4k(W: np.ndarray, K: int) -> np.ndarray:
+    """Q4_K bytes [N, K/256*144] -> fp32 [N, K]."""
+    W = np.ascontiguousarray(W, dtype=np.uint8)
+    N = _check_rows(W, K, Q4K_BYTES)
+    out = np.empty((N, K), dtype=np.float32)
+    _load().oracle_dequant_q4k(_ptr(W, ctypes.c_uint8), N, K, _ptr(out, ctypes.c_float))
+    return out
+
+
+def dequant_iq3(W: np.ndarray, grid: np.ndarray, K: int) -> np.ndarray:
+    """IQ3 bytes [N, K/256*98] + grid uint8 [256, 4] (doubled units) -> fp32 [N, K]."""
+    W = np.ascontiguousarray(W, dtype=np.uint8)
+    grid = np.ascontiguousarray(grid, dtype=np.uint8).reshape(256, 4)
+    N = _check_rows(W, K, IQ3_BYTES)
+    out = np.empty((N, K), dtype=np.float32)
+    _load().oracle_dequant_iq3(_ptr(W, ctypes.c_uint8), _ptr(grid, ctypes.c_uint8), N, K,
+                               _ptr(out, ctypes.c_float))
+    return out
+
+
+def _gemv(fmt, W, grid, X, rows, nthreads):
+    W = np.ascontiguousarray(W, dtype=np.uint8)
+    X = np.ascontiguousarray(X, dtype=np.float32)
+    if X.ndim == 1:
+        X = X[None, :]
+    M, K = X.shape
+    N = _check_rows(W, K, Q4K_BYTES if fmt == 0 else IQ3_BYTES)
+    if rows is None:
+        rows_arr = np.arange(N, dtype=np.int64)
+    else:
+        rows_arr = np.ascontiguousarray(rows, dtype=np.int64)
+        if rows_arr.size and (rows_arr.min() < 0 or rows_arr.max() >= N):
+            raise ValueError("row index out of range")
+    nr = rows_arr.size
+    Y = np.empty((M, nr), dtype=np.float64)
+    A = np.empty((M, nr), dtype=np.float64)
+    nt = max_threads() if nthreads is None else int(nthreads)
+    lib = _load()
+    if fmt == 0:
+        lib.oracle_gemv_q4k(_ptr(W, ctypes.c_uint8), _ptr(X, ctypes.c_float), M, K,
+                            _ptr(rows_arr, ctypes.c_int64), nr, _ptr(Y, ctypes.c_double),
+                            _ptr(A, ctypes.c_double), nt)
+    else:
+        g = np.ascontiguousarray(grid, dtype=np.uint8).reshape(256, 4)
+        lib.oracle_gemv_iq3(_ptr(W, ctypes.c_uint8), _ptr(g, ctypes.c_uint8),
+                            _ptr(X, ctypes.c_float), M, K, _ptr(rows_arr, ctypes.c_int64), nr,
+                            _ptr(Y, ctypes.c_double), _ptr(A, ctypes.c_double), nt)
+    return Y, A
+
+
+def gemv_q4k(W, X, rows=None, nthreads=None):
+    """(Y, A): fp64 y = X W^T and A = sum |w x| for the given rows of a Q4_K W."""
+    return _gemv(0, W, None, X, rows, nthreads)
+
+
+def gemv_iq3(W, grid, X, rows=None, nthreads=None):
+    """(Y, A): fp64 y = X W^T and A = sum |w x| for the given rows of an IQ3 W."""
+    return _gemv(1, W, grid, X, rows, nthreads)
+
+
+# ------------------------------------------------ block writers (tests only)
+def pack_q4k_scale_min(sc, mn) -> np.ndarray:
+    """Inverse of page 1's unpack: eight 6-bit scales and mins -> 12 bytes.
+
+    j < 4 go to the low six bits of bytes j (scale) and j+4 (min); j >= 4 put
+    their low nibbles in byte j+4 (scale low, min high) and their top two bits
+    in bits 6-7 of byte j-4 (scale) and byte j (min).
+    """
+    sc = [int(v) for v in sc]
+    mn = [int(v) for v in mn]
+    if len(sc) != 8 or len(mn) != 8 or max(sc + mn) > 63 or min(sc + mn) < 0:
+        raise ValueError("need eight 6-bit scales and eight 6-bit mins")
+    p = [0] * 12
+    for j in range(4):
+        p[j] |= sc[j]
+        p[j + 4] |= mn[j]
+    for j in range(4, 8):
+        p[j + 4] = (sc[j] & 15) | ((mn[j] & 15) << 4)
+        p[j - 4] |= (sc[j] >> 4) << 6
+        p[j] |= (mn[j] >> 4) << 6
+    return np.array(p, dtype=np.uint8)
+
+
+def _f16_le(v: float) -> np.ndarray:
+    return np.array([v], dtype="<f2").view(np.uint8)
+
+
+def q4k_block(d, dmin, sc, mn, qs) -> np.ndarray:
+    """Write one 144-byte Q4_K block from its fields (d, dmin as floats rounded to fp16)."""
+    blk = np.zeros(Q4K_BYTES, np.uint8)
+    blk[0:2] = _f16_le(d)
+    blk[2:4] = _f16_le(dmin)
+    blk[4:16] = pack_q4k_scale_min(sc, mn)
+    blk[16:144] = np.asarray(qs, dtype=np.uint8).reshape(128)
+    return blk
+
+
+def iq3_word(sign7s, code) -> int:
+    """Four 7-bit sign words and a 4-bit code -> the sub-block's uint32 (page 4 layout)."""
+    w = 0
+    for l, s in enumerate(sign7s):
+        if not 0 <= int(s) < 128:
+            raise ValueError("sign words are 7 bits")
+        w |= int(s) << (7 * l)
+    if not 0 <= int(code) < 16:
+        raise ValueError("code is 4 bits")
+    return w | (int(code) << 28)
+
+
+def iq3_block(idx, words, d) -> np.ndarray:
+    """Write one 98-byte IQ3 block: idx[64] bytes, words[8] uint32, d rounded to fp16."""
+    blk = np.zeros(IQ3_BYTES, np.uint8)
+    blk[0:64] = np.asarray(idx, dtype=np.uint8).reshape(64)
+    blk[64:96] = np.asarray(words, dtype="<u4").reshape(8).view(np.uint8)
+    blk[96:98] = _f16_le(d)
+    return blk
+
+
+# ------------------------------------------- IQ3 encoder (page 4, ``encode``)
+def _nearest_rows(q: np.ndarray, g: np.ndarray) -> np.ndarray:
+    """Nearest row of g [256, 4] (L2) for each row of q [n, 4]; lowest index on ties."""
+    d2 = ((q[:, None, :].astype(np.float64) - g[None, :, :].astype(np.float64)) ** 2).sum(-1)
+    return np.argmin(d2, axis=1)
+
+
+def iq3_encode(x: np.ndarray, grid: np.ndarray, force_d=None) -> np.ndarray:
+    """fp32 [R, K] -> IQ3 bytes [R, K/256*98], following page 4 ``encode``.
+
+    Steps per super-block: signs (zero counts as positive); in every 8-group
+    with an odd number of negatives flip the sign of the smallest magnitude
+    (first on ties); d = fp16(sqrt(mean(mag^2))/20 + 1e-12), used as stored;
+    for each 32-weight sub-block try codes 0..15 with db = d*(0.5+code)*0.5,
+    take the nearest grid row per 4 magnitudes of mag/db, and keep the code
+    with strictly smaller squared error.  ``force_d`` (one fp16-representable
+    value per row and super-block) replaces the computed d.
+    """
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    if x.ndim == 1:
+        x = x[None, :]
+    R, K = x.shape
+    if K % QK:
+        raise ValueError(f"K % {QK} != 0")
+    nsb = K // QK
+    g = np.ascontiguousarray(grid, dtype=np.uint8).reshape(256, 4).astype(np.float32) * np.float32(0.5)
+    out = np.zeros((R, nsb * IQ3_BYTES), np.uint8)
+    for r in range(R):
+        for sb in range(nsb):
+            blk = x[r, sb * QK:(sb + 1) * QK]
+            neg = blk < 0
+            mag = np.abs(blk)
+            neg8 = neg.reshape(32, 8).copy()
+            mag8 = mag.reshape(32, 8)
+            for grp in range(32):
+                if neg8[grp].sum() % 2 == 1:
+                    j = int(np.argmin(mag8[grp]))
+                    neg8[grp, j] = not neg8[grp, j]
+            neg = neg8.reshape(QK)
+            if force_d is None:
+                dd = np.sqrt(np.mean(mag * mag, dtype=np.float32)) / np.float32(20.0) + np.float32(1e-12)
+            else:
+                dd = np.float32(np.asarray(force_d, dtype=np.float64).reshape(R, nsb)[r, sb])
+            d16 = np.array([dd], dtype="<f2")
+            d = np.float32(d16.astype(np.float32)[0])
+            base = sb * IQ3_BYTES
+            out[r, base + 96:base + 98] = d16.view(np.uint8)
+            for ib in range(8):
+                m = mag[ib * 32:(ib + 1) * 32]
+                best = None
+                for code in range(16):
+                    db = np.float32(d * np.float32(0.5 + code) * np.float32(0.5))
+                    q = (m / np.float32(max(db, np.float32(1e-20)))).reshape(8, 4)
+                    idx = _nearest_rows(q, g)
+                    rec = g[idx].reshape(32) * db
+                    err = float(((rec.astype(np.float64) - m.astype(np.float64)) ** 2).sum())
+                    if best is None or err < best[0]:
+                        best = (err, idx, code)
+                _, idx, code = best
+                out[r, base + ib * 8:base + ib * 8 + 8] = idx.astype(np.uint8)
+                s = neg[ib * 32:(ib + 1) * 32].reshape(4, 8)
+                sevens = [int(sum(int(s[l, j]) << j for j in range(7))) for l in range(4)]
+                w = np.array([iq3_word(sevens, code)], dtype="<u4")
+                out[r, base + 64 + 4 * ib:base + 68 + 4 * ib] = w.view(np.uint8)
+    return out

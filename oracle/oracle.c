@@ -1,0 +1,234 @@
+/*
+ * CPU oracle for the block-quantised GEMV: TEST INFRASTRUCTURE ONLY.
+ *
+ * Only the tests, the smoke check and the bench's CPU-baseline leg load this
+ * library.  It shares no code, header or table with the CUDA library.
+ *
+ * Plain C99, built with -O2 -ffp-contract=off so that every float operation
+ * below is rounded exactly as written (no fused multiply-add).
+ *
+ * Sources (page title, section):
+ *   - Q4_K: page 1 "Rewriting picoLM in Python", function dequantize_q4_K
+ *     (block layout, the 6-bit scale/min unpack, the nibble-to-weight map).
+ *   - IQ3:  page 4 "iq3_pack.py" (colibri fmt=5), module docstring (layout,
+ *     value formula) and function decode (sign words, implied 8th sign,
+ *     sub-scale), function grid (the x0.5 applied to the published table).
+ *   - GEMV: page 1, model_forward / forward: matmul(out, x, W, n_in, n_out)
+ *     computes out = W x with one output per row of W.
+ *
+ * Pins: tests/test_oracle_pins.py checks every function here against
+ * hand-worked blocks (tests/golden/), exact closed forms, numpy's fp16
+ * conversion and math.fsum.
+ */
+#include <math.h>
+#include <stddef.h>
+#include <stdint.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+#define QK 256
+#define Q4K_BYTES 144
+#define IQ3_BYTES 98
+
+/* IEEE-754 binary16 -> binary32, exact, from the format's definition:
+ * sign 1 bit, exponent 5 bits (bias 15), fraction 10 bits; exponent 0 is
+ * zero/subnormal (value = fraction * 2^-24), exponent 31 is Inf/NaN. */
+float oracle_f16_to_f32(uint16_t h)
+{
+    uint32_t sign = (uint32_t)(h >> 15) & 1u;
+    uint32_t expo = (uint32_t)(h >> 10) & 31u;
+    uint32_t frac = (uint32_t)h & 1023u;
+    float v;
+    if (expo == 0) {
+        v = ldexpf((float)frac, -24);           /* exact: frac < 2^10 */
+    } else if (expo == 31) {
+        if (frac == 0) {
+            v = INFINITY;
+        } else {                                /* keep the payload bits */
+            uint32_t bits = 0x7f800000u | (frac << 13);
+            memcpy(&v, &bits, 4);
+        }
+    } else {
+        v = ldexpf((float)(1024u + frac), (int)expo - 25);
+    }
+    return sign ? -v : v;
+}
+
+void oracle_f16_to_f32_array(const uint16_t *h, float *out, int64_t n)
+{
+    for (int64_t i = 0; i < n; ++i)
+        out[i] = oracle_f16_to_f32(h[i]);
+}
+
+static uint16_t le16(const uint8_t *p) { return (uint16_t)(p[0] | (p[1] << 8)); }
+static uint32_t le32(const uint8_t *p)
+{
+    return (uint32_t)p[0] | ((uint32_t)p[1] << 8) | ((uint32_t)p[2] << 16) | ((uint32_t)p[3] << 24);
+}
+
+/* Page 1, dequantize_q4_K: the 12 packed bytes hold eight 6-bit scales and
+ * eight 6-bit mins.  j < 4: the low six bits of bytes j and j+4.  j >= 4: the
+ * low (scale) or high (min) nibble of byte j+4, with the top two bits of byte
+ * j-4 (scale) or byte j (min) above it. */
+void oracle_q4k_scale_min(const uint8_t p[12], uint8_t sc[8], uint8_t mn[8])
+{
+    for (int j = 0; j < 8; ++j) {
+        if (j < 4) {
+            sc[j] = (uint8_t)(p[j] & 63);
+            mn[j] = (uint8_t)(p[j + 4] & 63);
+        } else {
+            sc[j] = (uint8_t)((p[j + 4] & 0xF) | ((p[j - 4] >> 6) << 4));
+            mn[j] = (uint8_t)((p[j + 4] >> 4) | ((p[j] >> 6) << 4));
+        }
+    }
+}
+
+/* One Q4_K block (144 bytes) -> 256 fp32 weights, page 1 dequantize_q4_K.
+ * Byte 0-1 d, 2-3 dmin (fp16), 4-15 packed scales/mins, 16-143 qs.  qs is
+ * four groups of 32 bytes; in group g, byte l gives weight 64g+l from its low
+ * nibble (scale/min index 2g) and weight 64g+32+l from its high nibble
+ * (index 2g+1).  Each weight is (d*sc)*q - (dmin*mn), evaluated left to
+ * right in fp32 as the page's numpy expression does. */
+void oracle_dequant_q4k_block(const uint8_t *blk, float *out)
+{
+    float d = oracle_f16_to_f32(le16(blk + 0));
+    float dmin = oracle_f16_to_f32(le16(blk + 2));
+    uint8_t sc[8], mn[8];
+    oracle_q4k_scale_min(blk + 4, sc, mn);
+    const uint8_t *qs = blk + 16;
+    for (int g = 0; g < 4; ++g) {
+        for (int l = 0; l < 32; ++l) {
+            uint8_t q = qs[32 * g + l];
+            float lo = (float)(q & 0xF), hi = (float)(q >> 4);
+            float a0 = d * (float)sc[2 * g];
+            float a1 = a0 * lo;
+            float b0 = dmin * (float)mn[2 * g];
+            out[64 * g + l] = a1 - b0;
+            float c0 = d * (float)sc[2 * g + 1];
+            float c1 = c0 * hi;
+            float e0 = dmin * (float)mn[2 * g + 1];
+            out[64 * g + 32 + l] = c1 - e0;
+        }
+    }
+}
+
+/* One IQ3 super-block (98 bytes) -> 256 fp32 weights, page 4 decode.
+ * Bytes 0-63: one grid index per 4 weights; 64-95: eight little-endian u32,
+ * one per 32-weight sub-block ib: bits 7l..7l+6 are the sign bits of weights
+ * 8l..8l+6 of the sub-block (bit set => negative), the sign of weight 8l+7 is
+ * the XOR of those seven bits, bits 28-31 are the sub-scale code; 96-97: fp16
+ * d.  value = mag * sign * db with mag = grid_byte * 0.5 (fp32, page 4 grid())
+ * and db = d * (0.5 + code) * 0.5 (fp64, as numpy promotes it), rounded once
+ * to fp32 when stored. */
+void oracle_dequant_iq3_block(const uint8_t *blk, const uint8_t *grid, float *out)
+{
+    double d = (double)oracle_f16_to_f32(le16(blk + 96));
+    for (int ib = 0; ib < 8; ++ib) {
+        const uint8_t *idx = blk + 8 * ib;
+        uint32_t word = le32(blk + 64 + 4 * ib);
+        uint32_t code = (word >> 28) & 0xF;
+        double db = d * (0.5 + (double)code) * 0.5;
+        for (int l = 0; l < 4; ++l) {
+            uint32_t seven = (word >> (7 * l)) & 0x7F;
+            uint32_t par = 0;
+            for (int j = 0; j < 8; ++j) {
+                uint32_t neg;
+                if (j < 7) {
+                    neg = (seven >> j) & 1u;
+                    par ^= neg;
+                } else {
+                    neg = par;
+                }
+                int t = 8 * l + j;              /* weight within the sub-block */
+                uint8_t gidx = idx[t / 4];
+                float mag = (float)grid[4 * gidx + (t % 4)] * 0.5f;
+                float sgn = neg ? -1.0f : 1.0f;
+                float ms = mag * sgn;
+                out[32 * ib + t] = (float)((double)ms * db);
+            }
+        }
+    }
+}
+
+/* Whole rows: W is [N][K/256 blocks], out is [N][K] fp32. */
+void oracle_dequant_q4k(const uint8_t *W, int64_t N, int64_t K, float *out)
+{
+    int64_t nb = K / QK;
+    for (int64_t n = 0; n < N; ++n)
+        for (int64_t b = 0; b < nb; ++b)
+            oracle_dequant_q4k_block(W + (n * nb + b) * Q4K_BYTES, out + n * K + b * QK);
+}
+
+void oracle_dequant_iq3(const uint8_t *W, const uint8_t *grid, int64_t N, int64_t K, float *out)
+{
+    int64_t nb = K / QK;
+    for (int64_t n = 0; n < N; ++n)
+        for (int64_t b = 0; b < nb; ++b)
+            oracle_dequant_iq3_block(W + (n * nb + b) * IQ3_BYTES, grid, out + n * K + b * QK);
+}
+
+/* GEMV reference for selected rows.  Y[m][r] = sum_k (double)w[row][k] * (double)x[m][k],
+ * summed in k order in fp64; A[m][r] = sum_k |w*x| in fp64 (the scale of the
+ * tolerance).  rows == NULL means rows 0..nrows-1.  Y and A are [M][nrows].
+ * fmt 0 = Q4_K, 1 = IQ3.  Rows are independent; with nthreads > 1 they are
+ * split across OpenMP threads (each row's sum is still sequential). */
+static void gemv_rows(int fmt, const uint8_t *W, const uint8_t *grid, const float *X,
+                      int M, int64_t K, const int64_t *rows, int64_t nrows,
+                      double *Y, double *A, int nthreads)
+{
+    int64_t nb = K / QK;
+    int64_t bytes = fmt == 0 ? Q4K_BYTES : IQ3_BYTES;
+#ifdef _OPENMP
+    if (nthreads < 1) nthreads = 1;
+#pragma omp parallel for schedule(dynamic, 1) num_threads(nthreads)
+#endif
+    for (int64_t r = 0; r < nrows; ++r) {
+        float w[QK];
+        int64_t row = rows ? rows[r] : r;
+        for (int m = 0; m < M; ++m) {
+            Y[(int64_t)m * nrows + r] = 0.0;
+            A[(int64_t)m * nrows + r] = 0.0;
+        }
+        for (int64_t b = 0; b < nb; ++b) {
+            const uint8_t *blk = W + (row * nb + b) * bytes;
+            if (fmt == 0)
+                oracle_dequant_q4k_block(blk, w);
+            else
+                oracle_dequant_iq3_block(blk, grid, w);
+            for (int m = 0; m < M; ++m) {
+                const float *x = X + (int64_t)m * K + b * QK;
+                double y = Y[(int64_t)m * nrows + r], a = A[(int64_t)m * nrows + r];
+                for (int k = 0; k < QK; ++k) {
+                    double p = (double)w[k] * (double)x[k];
+                    y += p;
+                    a += fabs(p);
+                }
+                Y[(int64_t)m * nrows + r] = y;
+                A[(int64_t)m * nrows + r] = a;
+            }
+        }
+    }
+}
+
+void oracle_gemv_q4k(const uint8_t *W, const float *X, int M, int64_t K,
+                     const int64_t *rows, int64_t nrows, double *Y, double *A, int nthreads)
+{
+    gemv_rows(0, W, NULL, X, M, K, rows, nrows, Y, A, nthreads);
+}
+
+void oracle_gemv_iq3(const uint8_t *W, const uint8_t *grid, const float *X, int M, int64_t K,
+                     const int64_t *rows, int64_t nrows, double *Y, double *A, int nthreads)
+{
+    gemv_rows(1, W, grid, X, M, K, rows, nrows, Y, A, nthreads);
+}
+
+int oracle_max_threads(void)
+{
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
