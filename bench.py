@@ -1,0 +1,464 @@
+#!/usr/bin/env python3
+"""Benchmark of the fused-dequantisation GEMV path (one JSON line on rank 0).
+
+Headline workload: the TinyLlama-1.1B-shaped decode weight pass at M=1, Q4_K
+throughout: 22 layers x (q, k, v, o, gate, up, down) + the output projection,
+155 GEMVs, 581,861,376 weight bytes, seeded synthetic weights and x.  One
+step = one pass.  value = effective weight GB/s (weight bytes / step time,
+summed over ranks); tokens/s-equiv = passes per second.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload tinyllama|q4k_c0|iq3_c2|q4k_c3|q4k_c4a|q4k_c4b|iq3_c4a|iq3_c4b] [--M m]
+
+The timed region replays a CUDA graph of the pass K times between CUDA
+events on the launching stream; the graph also holds an event pair around
+every launch, which gives the per-launch kernel durations used for the
+roofline.  The pass reads 581 MB, more than the 126 MB L2, so every step
+streams from HBM; single-matrix workloads rotate over enough copies to
+exceed twice the L2.
+"""
+from __future__ import annotations
+
+import argparse
+import ctypes
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "effective weight GB/s (% of HBM peak) for Q4_K/IQ3 GEMV at M=1; tokens/s-equiv"
+Q4K_BYTES, IQ3_BYTES = 144, 98
+FALLBACK_HBM_GBS = 6800.0
+
+
+# ------------------------------------------------------------------ workloads
+def workload_spec(name: str, M: int):
+    """[(fmt, K, N)] GEMVs of one step, a description, and the token count."""
+    from block_quantised_weight_gb300 import synth
+    if name == "tinyllama":
+        mats = [("q4k", K, N) for (_l, _n, K, N) in synth.tinyllama_shapes()]
+        return mats, "TinyLlama-1.1B-shaped Q4_K decode weight pass (155 GEMVs)", 1
+    table = {
+        "q4k_c0": ("q4k", 2048, 2048), "iq3_c2": ("iq3", 4096, 14336), "q4k_c3": ("q4k", 4096, 11008),
+        "q4k_c4a": ("q4k", 8192, 28672), "q4k_c4b": ("q4k", 28672, 8192),
+        "iq3_c4a": ("iq3", 8192, 28672), "iq3_c4b": ("iq3", 28672, 8192),
+    }
+    fmt, K, N = table[name]
+    return [(fmt, K, N)], f"{fmt.upper()} GEMV K={K} N={N} M={M}", M
+
+
+def weight_bytes(fmt, K, N):
+    return N * (K // 256) * (Q4K_BYTES if fmt == "q4k" else IQ3_BYTES)
+
+
+def gen_mats(name, mats, M):
+    """Host arrays per GEMV: (fmt, K, N, W, grid, x)."""
+    import numpy as np
+    from block_quantised_weight_gb300 import synth
+    out = []
+    if name == "tinyllama":
+        for (_shape, rng), (fmt, K, N) in zip(synth.tinyllama_seeds(1), mats):
+            W = synth.gen_q4k(N, K, rng)
+            x = synth.gen_x(M, K, rng)
+            out.append((fmt, K, N, W, None, x))
+        return out
+    fmt, K, N = mats[0]
+    seed = {"q4k_c0": 0, "iq3_c2": 2, "q4k_c3": 3}.get(name, 4)
+    rng = np.random.default_rng(seed)
+    if fmt == "q4k":
+        W, grid = synth.gen_q4k(N, K, rng), None
+    else:
+        W, grid = synth.gen_iq3(N, K, rng)
+    x = synth.gen_x(M, K, rng)
+    out.append((fmt, K, N, W, grid, x))
+    return out
+
+
+# ------------------------------------------------------------------ helpers
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        rows = [l.split(",") for l in self.lines if l.count(",") >= 8]
+        if not rows:
+            return None
+        sm = [float(r[1]) for r in rows if r[1].strip().replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].strip().replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].strip() == "Active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+def cudart():
+    for name in ("libcudart.so.13", "libcudart.so.12", "libcudart.so"):
+        try:
+            return ctypes.CDLL(name)
+        except OSError:
+            continue
+    return None
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "block_quantised_weight_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        if f.endswith((".cu", ".cuh", ".h")):
+            h.update(open(os.path.join(csrc, f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(workload, M):
+    """DRAM bytes per launch of the dominant kernel from a committed ncu summary,
+    only if the kernel sources are unchanged since it was taken."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        d = json.load(open(p))
+        e = d.get(f"{workload}:M{M}")
+        if e and e.get("kernel_source_hash") == kernel_source_hash():
+            return e["dram_bytes_per_launch"]
+    except Exception:
+        pass
+    return None
+
+
+# ------------------------------------------------------------------ our arm
+def run_ours(args, rank, world, local_rank):
+    import numpy as np
+    import torch
+    import torch.distributed as dist
+    from block_quantised_weight_gb300 import build, qgemv
+
+    if rank == 0:
+        build.build()
+    if world > 1:
+        dist.barrier()
+    lib = qgemv.load()
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    mats, desc, M = workload_spec(args.workload, args.M)
+    host = gen_mats(args.workload, mats, M)
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    step_wbytes = sum(weight_bytes(f, K, N) for f, K, N in mats)
+    copies = 1
+    if step_wbytes < 2 * l2:
+        copies = int(np.ceil(2 * l2 / step_wbytes)) + 1
+
+    # device buffers: weights (rotated copies), x / y concatenated per pass
+    xs_host = np.concatenate([h[5].reshape(-1) for h in host]).astype(np.float32)
+    ys_len = sum(M * h[2] for h in host)
+    x_dev = torch.from_numpy(xs_host).to(dev)
+    y_dev = torch.empty(ys_len, dtype=torch.float32, device=dev)
+    launches = []   # per copy: list of (fn, args, wbytes, algo_bytes)
+    keep = []
+    for c in range(copies):
+        xo, yo = 0, 0
+        lst = []
+        for fmt, K, N, W, grid, x in host:
+            Wd = torch.from_numpy(W).to(dev)
+            gd = torch.from_numpy(grid).to(dev) if grid is not None else None
+            keep.append((Wd, gd))
+            xp = x_dev.data_ptr() + 4 * xo
+            yp = y_dev.data_ptr() + 4 * yo
+            wb = weight_bytes(fmt, K, N)
+            algo = wb + 4 * M * K + 4 * M * N
+            if fmt == "q4k":
+                lst.append((lib.qgemv_q4k, (Wd.data_ptr(), xp, yp, M, N, K), wb, algo))
+            else:
+                lst.append((lib.qgemv_iq3, (Wd.data_ptr(), gd.data_ptr(), xp, yp, M, N, K), wb, algo))
+            xo += M * K
+            yo += M * N
+        launches.append(lst)
+    flat = [l for lst in launches for l in lst]
+
+    stream = torch.cuda.Stream(device=dev)
+    sh = ctypes.c_void_p(stream.cuda_stream)
+
+    def run_pass(lst):
+        for fn, a, _wb, _ab in lst:
+            rc = fn(*a, sh)
+            if rc != 0:
+                raise RuntimeError(f"launch failed: {rc} {qgemv.strerror(rc)}")
+
+    with torch.cuda.stream(stream):
+        for _ in range(2):
+            for lst in launches:
+                run_pass(lst)
+    torch.cuda.synchronize(dev)
+    assert qgemv.qg_device_status() == 0
+
+    # graph of one step (all copies, so one replay = `copies` passes), with an
+    # external event pair around every launch for per-launch durations
+    rt = cudart()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in flat]
+    for a, b in ev:
+        a.record(stream)
+        b.record(stream)
+    torch.cuda.synchronize(dev)
+    per_launch_ok = rt is not None and hasattr(ev[0][0], "cuda_event")
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        cap = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+        for i, (fn, a, _wb, _ab) in enumerate(flat):
+            if per_launch_ok:
+                per_launch_ok = rt.cudaEventRecordWithFlags(ctypes.c_void_p(ev[i][0].cuda_event), cap, 1) == 0
+            rc = fn(*a, cap)
+            if rc != 0:
+                raise RuntimeError(f"capture launch failed: {rc}")
+            if per_launch_ok:
+                per_launch_ok = rt.cudaEventRecordWithFlags(ctypes.c_void_p(ev[i][1].cuda_event), cap, 1) == 0
+    passes_per_replay = copies
+
+    with torch.cuda.stream(stream):
+        for _ in range(max(args.warmup, 3)):
+            g.replay()
+    torch.cuda.synchronize(dev)
+
+    sampler = ClockSampler(local_rank) if rank == 0 else None
+    if sampler:
+        sampler.start()
+        time.sleep(0.3)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        t0.record(stream)
+        for _ in range(args.steps):
+            g.replay()
+        t1.record(stream)
+    torch.cuda.synchronize(dev)
+    if world > 1:
+        dist.barrier()
+    clocks = sampler.stop() if sampler else None
+    ms_total = t0.elapsed_time(t1)
+    durs = None
+    if per_launch_ok:
+        try:
+            durs = [a.elapsed_time(b) for a, b in ev]
+        except Exception:
+            durs = None
+    status = qgemv.qg_device_status()
+    if status != 0:
+        raise RuntimeError(f"device status {status}")
+
+    # e2e: host x in, host y out, every step, through the same C-ABI calls
+    xs_pin = torch.from_numpy(xs_host).pin_memory()
+    ys_pin = torch.empty(ys_len, dtype=torch.float32).pin_memory()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        for _ in range(2):
+            x_dev.copy_(xs_pin, non_blocking=True)
+            g.replay()
+            ys_pin.copy_(y_dev, non_blocking=True)
+    torch.cuda.synchronize(dev)
+    if world > 1:
+        dist.barrier()
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(args.steps):
+            x_dev.copy_(xs_pin, non_blocking=True)
+            g.replay()
+            ys_pin.copy_(y_dev, non_blocking=True)
+        e1.record(stream)
+    torch.cuda.synchronize(dev)
+    ms_e2e = e0.elapsed_time(e1)
+
+    # max over ranks
+    t = torch.tensor([ms_total, ms_e2e], dtype=torch.float64, device=dev)
+    if world > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    ms_total, ms_e2e = float(t[0]), float(t[1])
+    n_pass = args.steps * passes_per_replay
+    ms_step = ms_total / n_pass
+    value = world * step_wbytes * n_pass / (ms_total * 1e-3) / 1e9
+    e2e_value = world * step_wbytes * n_pass / (ms_e2e * 1e-3) / 1e9
+
+    peak, peak_kind = measured_peaks()
+    roof = None
+    if durs:
+        algo = sum(ab for _f, _a, _wb, ab in flat)
+        kern_ms = sum(durs)
+        achieved = algo / (kern_ms * 1e-3) / 1e9
+        roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                "frac": round(achieved / peak, 4), "traffic": profiled_traffic(args.workload, M),
+                "peak_kind": f"of {peak_kind}", "kernel": "qgemv_q4k gemv_kernel<Q4K,M=1>"
+                if mats[0][0] == "q4k" else "qgemv_iq3 gemv_kernel<IQ3>",
+                "launches_timed": len(durs), "kernel_ms_per_pass": round(kern_ms / passes_per_replay, 4),
+                "algorithmic_bytes_per_launch": round(algo / len(durs))}
+        by_shape = {}
+        for (fn, a, wb, ab), d in zip(flat, durs):
+            key = f"K{a[-1]}xN{a[-2]}"
+            e = by_shape.setdefault(key, [0, 0.0, 0])
+            e[0] += 1
+            e[1] += d
+            e[2] += ab
+        roof["per_shape"] = {k: {"launches": n, "us_per_launch": round(1e3 * t / n, 2),
+                                 "GBps": round(b / (t * 1e-3) / 1e9, 1)} for k, (n, t, b) in by_shape.items()}
+    return {
+        "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms_step, 4), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic (seeded numpy; shapes of the pages' models)",
+        "config": {"workload": desc, "M": M, "weight_bytes_per_step": step_wbytes,
+                   "l2": ("inputs larger than L2" if copies == 1 else
+                          f"rotates {copies} weight copies (> 2x L2)"),
+                   "graph": "CUDA graph of the step, replayed", "parallelism": f"replicas x{world}"},
+        "tokens_per_s_equiv": round(world * 1000.0 / ms_step, 1),
+        "pct_of_hbm_peak": round(100 * value / world / peak, 1),
+        "e2e": {"value": round(e2e_value, 1), "unit": "GB/s", "h2d_bytes_per_step": int(xs_host.nbytes),
+                "d2h_bytes_per_step": int(4 * ys_len),
+                "note": "pinned host x -> device, graph of C-ABI launches, device y -> pinned host, every step"},
+        "gpu_launches": len(flat) * args.steps,
+        "roofline": roof,
+        "clocks": clocks,
+    }
+
+
+# ------------------------------------------------------------------ oracle arm
+def oracle_sample_rate(workload, M, budget_s, threads=None):
+    """Oracle weight GB/s on a bounded sample of the workload (full rows)."""
+    import numpy as np
+
+    import oracle
+    mats, _desc, M = workload_spec(workload, M)
+    host = gen_mats(workload, mats[:7], M) if workload == "tinyllama" else gen_mats(workload, mats, M)
+    done_bytes, t_used, n = 0, 0.0, 0
+    nt = oracle.max_threads() if threads is None else threads
+    rows_cap = []
+    for fmt, K, N, W, grid, x in host:
+        rows_cap.append(min(N, max(64, int(4e6 // K))))
+    t_start = time.perf_counter()
+    while t_used < budget_s:
+        for (fmt, K, N, W, grid, x), nr in zip(host, rows_cap):
+            rows = np.arange(nr)
+            t0 = time.perf_counter()
+            if fmt == "q4k":
+                oracle.gemv_q4k(W[:nr], x, rows=rows, nthreads=nt)
+            else:
+                oracle.gemv_iq3(W[:nr], grid, x, rows=rows, nthreads=nt)
+            t_used += time.perf_counter() - t0
+            done_bytes += weight_bytes(fmt, K, nr)
+            n += 1
+            if t_used >= budget_s:
+                break
+    sample = ("first 7 matrices of the pass (layer 0), first rows of each" if workload == "tinyllama"
+              else "first rows of the matrix") + f", {n} matrix calls, {done_bytes / 1e6:.1f} MB"
+    return done_bytes / t_used / 1e9, nt, sample
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return None
+    mats, desc, M = workload_spec(args.workload, args.M)
+    step_budget = 2.0
+    for _ in range(args.warmup):
+        oracle_sample_rate(args.workload, args.M, 0.2)
+    t0 = time.perf_counter()
+    rates, nt, sample = [], 1, ""
+    for _ in range(args.steps):
+        r, nt, sample = oracle_sample_rate(args.workload, args.M, step_budget)
+        rates.append(r)
+    wall = time.perf_counter() - t0
+    value = statistics.median(rates)
+    step_wbytes = sum(weight_bytes(f, K, N) for f, K, N in mats)
+    ms_step = step_wbytes / (value * 1e9) * 1e3
+    return {
+        "impl": "reference", "metric": METRIC, "value": round(value, 3), "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 2), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": desc, "M": M, "weight_bytes_per_step": step_wbytes},
+        "cpu_baseline": {"value": round(value, 3), "unit": "GB/s", "cores": nt, "kind": "oracle",
+                         "sample": sample + f"; {step_budget:.0f} s of oracle time per step"},
+        "e2e": {"value": round(value, 3), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "wall_s": round(wall, 1),
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="tinyllama")
+    ap.add_argument("--M", type=int, default=1)
+    ap.add_argument("--cpu-baseline-s", type=float, default=12.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        out = run_reference(args, rank, world)
+        if out is not None:
+            print(json.dumps(out), flush=True)
+        return
+    import torch
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    out = run_ours(args, rank, world, local_rank)
+    if rank == 0:
+        r, nt, sample = oracle_sample_rate(args.workload, args.M, args.cpu_baseline_s)
+        out["cpu_baseline"] = {"value": round(r, 3), "unit": "GB/s", "cores": nt, "kind": "oracle",
+                               "sample": sample}
+        print(json.dumps(out), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

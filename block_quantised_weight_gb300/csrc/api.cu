@@ -1,0 +1,145 @@
+// C-ABI entry points of libqgemv.so (declared in include/qgemv.h).
+//
+// Every argument is checked on the host before anything is launched; no
+// exception crosses this boundary and nothing here aborts the process.
+#include <cstdint>
+
+#include "common.cuh"
+#include "launch.h"
+
+namespace {
+
+// Per-device status word: kernels OR qg::kStatus* bits into it.  Kernels get
+// its device address (cudaGetSymbolAddress, cached per device), never the
+// host-side symbol.
+__device__ unsigned qg_status_word;
+unsigned* g_status_ptr[64];
+
+unsigned* status_ptr() {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+    if (!g_status_ptr[dev]) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, qg_status_word) != cudaSuccess) return nullptr;
+        g_status_ptr[dev] = static_cast<unsigned*>(p);
+    }
+    return g_status_ptr[dev];
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool overlap(const void* a, int64_t abytes, const void* b, int64_t bbytes) {
+    const uintptr_t a0 = reinterpret_cast<uintptr_t>(a), b0 = reinterpret_cast<uintptr_t>(b);
+    return a0 < b0 + static_cast<uintptr_t>(bbytes) && b0 < a0 + static_cast<uintptr_t>(abytes);
+}
+
+// Shape checks shared by the GEMV entry points.  Sizes are bounded so that
+// every byte count below fits comfortably in int64.
+int check_gemv(const uint8_t* W, const uint8_t* grid, bool need_grid, const float* X, const float* Y, int M,
+               int64_t N, int64_t K, int block_bytes) {
+    if (!W || !X || !Y || (need_grid && !grid)) return QG_EINVAL;
+    if (M < 1 || M > QG_MAX_M || N <= 0 || K <= 0 || K % 256 != 0) return QG_EINVAL;
+    if (N > (int64_t(1) << 31) || K > (int64_t(1) << 31)) return QG_EINVAL;
+    if (!aligned16(W) || !aligned16(X) || !aligned16(Y) || (need_grid && !aligned16(grid))) return QG_EALIGN;
+    const int64_t wbytes = N * (K / 256) * block_bytes;
+    const int64_t ybytes = int64_t(M) * N * 4, xbytes = int64_t(M) * K * 4;
+    if (overlap(Y, ybytes, W, wbytes) || overlap(Y, ybytes, X, xbytes) || (need_grid && overlap(Y, ybytes, grid, 1024)))
+        return QG_EALIAS;
+    return QG_OK;
+}
+
+int check_dequant(const uint8_t* W, const uint8_t* grid, bool need_grid, const float* out, int64_t N, int64_t K,
+                  int block_bytes) {
+    if (!W || !out || (need_grid && !grid)) return QG_EINVAL;
+    if (N <= 0 || K <= 0 || K % 256 != 0 || N > (int64_t(1) << 31) || K > (int64_t(1) << 31)) return QG_EINVAL;
+    if (N * (K / 256) > (int64_t(1) << 33)) return QG_EINVAL;
+    if (!aligned16(W) || !aligned16(out) || (need_grid && !aligned16(grid))) return QG_EALIGN;
+    if (overlap(out, N * K * 4, W, N * (K / 256) * block_bytes) || (need_grid && overlap(out, N * K * 4, grid, 1024)))
+        return QG_EALIAS;
+    return QG_OK;
+}
+
+// Test-only: an mbarrier nobody arrives on; the bounded wait must give up.
+__global__ void bounded_wait_probe(unsigned* status) {
+    __shared__ uint64_t bar;
+    if (threadIdx.x == 0) {
+        qg::mbar_init(&bar, 1);
+        qg::fence_mbar_init();
+    }
+    __syncthreads();
+    qg::mbar_wait_bounded(&bar, 0, status, 20000000ull);  // 20 ms
+}
+
+}  // namespace
+
+extern "C" {
+
+int qgemv_q4k(const uint8_t* W, const float* X, float* Y, int M, int64_t N, int64_t K, cudaStream_t stream) {
+    int rc = check_gemv(W, nullptr, false, X, Y, M, N, K, 144);
+    if (rc != QG_OK) return rc;
+    unsigned* st = status_ptr();
+    if (!st) return QG_ECUDA;
+    return qg::launch_gemv_q4k(W, X, Y, M, N, K, stream, st);
+}
+
+int qgemv_iq3(const uint8_t* W, const uint8_t* grid, const float* X, float* Y, int M, int64_t N, int64_t K,
+              cudaStream_t stream) {
+    int rc = check_gemv(W, grid, true, X, Y, M, N, K, 98);
+    if (rc != QG_OK) return rc;
+    unsigned* st = status_ptr();
+    if (!st) return QG_ECUDA;
+    return qg::launch_gemv_iq3(W, grid, X, Y, M, N, K, stream, st);
+}
+
+int qgemm_q4k_batched(const uint8_t* W, const float* X, float* Y, int M, int64_t N, int64_t K, cudaStream_t stream) {
+    int rc = check_gemv(W, nullptr, false, X, Y, M, N, K, 144);
+    if (rc != QG_OK) return rc;
+    unsigned* st = status_ptr();
+    if (!st) return QG_ECUDA;
+    if (M < 16) return qg::launch_gemv_q4k(W, X, Y, M, N, K, stream, st);
+    return qg::launch_gemm_q4k_tc(W, X, Y, M, N, K, stream, st);
+}
+
+int qdequant_q4k(const uint8_t* W, float* out, int64_t N, int64_t K, cudaStream_t stream) {
+    int rc = check_dequant(W, nullptr, false, out, N, K, 144);
+    if (rc != QG_OK) return rc;
+    return qg::launch_dequant_q4k(W, out, N, K, stream);
+}
+
+int qdequant_iq3(const uint8_t* W, const uint8_t* grid, float* out, int64_t N, int64_t K, cudaStream_t stream) {
+    int rc = check_dequant(W, grid, true, out, N, K, 98);
+    if (rc != QG_OK) return rc;
+    return qg::launch_dequant_iq3(W, grid, out, N, K, stream);
+}
+
+int qg_device_status(cudaStream_t stream) {
+    if (cudaStreamSynchronize(stream) != cudaSuccess) return QG_ECUDA;
+    unsigned v = 0, zero = 0;
+    if (cudaMemcpyFromSymbol(&v, qg_status_word, sizeof(v)) != cudaSuccess) return QG_ECUDA;
+    if (v != 0 && cudaMemcpyToSymbol(qg_status_word, &zero, sizeof(zero)) != cudaSuccess) return QG_ECUDA;
+    if (v & qg::kStatusTimeout) return QG_ETIMEOUT;
+    if (v & qg::kStatusBounds) return QG_EBOUNDS;
+    return QG_OK;
+}
+
+int qg_test_bounded_wait(cudaStream_t stream) {
+    unsigned* st = status_ptr();
+    if (!st) return QG_ECUDA;
+    bounded_wait_probe<<<1, 32, 0, stream>>>(st);
+    return cudaGetLastError() == cudaSuccess ? QG_OK : QG_ECUDA;
+}
+
+const char* qg_strerror(int status) {
+    switch (status) {
+        case QG_OK: return "ok";
+        case QG_EINVAL: return "invalid argument (M, N, K or a null pointer)";
+        case QG_EALIGN: return "pointer not 16-byte aligned";
+        case QG_ECUDA: return "CUDA runtime or launch error";
+        case QG_ETIMEOUT: return "a bounded wait inside a kernel gave up";
+        case QG_EBOUNDS: return "an index check inside a kernel failed";
+        case QG_EALIAS: return "output overlaps an input";
+        default: return "unknown status";
+    }
+}
+
+}  // extern "C"

@@ -1,0 +1,21 @@
+// Host-side launchers shared between the translation units of libqgemv.
+// Arguments are validated by the C-ABI layer (api.cu) before these run.
+#pragma once
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "../../include/qgemv.h"
+
+namespace qg {
+
+int launch_gemv_q4k(const uint8_t* W, const float* X, float* Y, int M, int64_t N, int64_t K, cudaStream_t s,
+                    unsigned* status);
+int launch_gemv_iq3(const uint8_t* W, const uint8_t* grid, const float* X, float* Y, int M, int64_t N, int64_t K,
+                    cudaStream_t s, unsigned* status);
+int launch_dequant_q4k(const uint8_t* W, float* out, int64_t N, int64_t K, cudaStream_t s);
+int launch_dequant_iq3(const uint8_t* W, const uint8_t* grid, float* out, int64_t N, int64_t K, cudaStream_t s);
+// tcgen05 bf16 path, 16 <= M <= 32
+int launch_gemm_q4k_tc(const uint8_t* W, const float* X, float* Y, int M, int64_t N, int64_t K, cudaStream_t s,
+                       unsigned* status);
+
+}  // namespace qg

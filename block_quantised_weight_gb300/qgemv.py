@@ -1,0 +1,180 @@
+"""ctypes binding of libqgemv.so: argument marshalling only.
+
+Each function takes torch CUDA tensors, checks dtype/shape/contiguity, and
+calls the C entry point of the same name on the current torch stream (or the
+stream given).  Every step of the computation runs in the library's CUDA
+kernels; there is no CPU fallback: if the library is missing or a call fails,
+an exception is raised.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+from . import build as _build
+
+_lock = threading.Lock()
+_lib = None
+
+QG_OK = 0
+QG_EINVAL = -1
+QG_EALIGN = -2
+QG_ECUDA = -3
+QG_ETIMEOUT = -4
+QG_EBOUNDS = -5
+QG_EALIAS = -6
+QG_MAX_M = 32
+
+EXPORTS = ("qgemv_q4k", "qgemv_iq3", "qgemm_q4k_batched", "qdequant_q4k", "qdequant_iq3",
+           "qg_device_status", "qg_test_bounded_wait", "qg_strerror")
+
+
+class QGError(RuntimeError):
+    def __init__(self, fn: str, code: int):
+        self.code = code
+        super().__init__(f"{fn} failed: {code} ({strerror(code)})")
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def load():
+    """Load libqgemv.so (built in-tree by build.build()); raise if it is missing."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        path = _build.LIB
+        if not os.path.exists(path):
+            raise RuntimeError(f"libqgemv.so is not built ({path}); run block_quantised_weight_gb300.build.build()")
+        lib = ctypes.CDLL(path)
+        vp, i64, ci = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
+        sigs = {
+            "qgemv_q4k": [vp, vp, vp, ci, i64, i64, vp],
+            "qgemv_iq3": [vp, vp, vp, vp, ci, i64, i64, vp],
+            "qgemm_q4k_batched": [vp, vp, vp, ci, i64, i64, vp],
+            "qdequant_q4k": [vp, vp, i64, i64, vp],
+            "qdequant_iq3": [vp, vp, vp, i64, i64, vp],
+            "qg_device_status": [vp],
+            "qg_test_bounded_wait": [vp],
+            "qg_strerror": [ci],
+        }
+        for name, args in sigs.items():
+            f = getattr(lib, name)
+            f.argtypes = args
+            f.restype = ctypes.c_char_p if name == "qg_strerror" else ctypes.c_int
+        _lib = lib
+        return lib
+
+
+def strerror(code: int) -> str:
+    try:
+        return load().qg_strerror(int(code)).decode()
+    except Exception:  # library not loadable: still give a message
+        return "unknown"
+
+
+def _stream(stream):
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(int(stream.cuda_stream))
+
+
+def _check(fn, rc):
+    if rc != QG_OK:
+        raise QGError(fn, rc)
+
+
+def _req(t, dtype, name):
+    import torch
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def _xy(W, X, out, block_bytes):
+    import torch
+    _req(W, torch.uint8, "W")
+    _req(X, torch.float32, "X")
+    if X.dim() == 1:
+        X = X.view(1, -1)
+    M, K = X.shape
+    if K % 256:
+        raise ValueError("K must be a multiple of 256")
+    row = K // 256 * block_bytes
+    if W.numel() % row:
+        raise ValueError("W is not a whole number of rows for this K")
+    N = W.numel() // row
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.float32, device=X.device)
+    else:
+        _req(out, torch.float32, "out")
+        if out.numel() != M * N:
+            raise ValueError("out has the wrong size")
+    return X, out, M, N, K
+
+
+def qgemv_q4k(W, X, out=None, stream=None):
+    """Y[M, N] = X[M, K] @ dequant(W)^T for a Q4_K matrix W (uint8, N*K/256*144 bytes)."""
+    X, out, M, N, K = _xy(W, X, out, 144)
+    _check("qgemv_q4k", load().qgemv_q4k(W.data_ptr(), X.data_ptr(), out.data_ptr(), M, N, K, _stream(stream)))
+    return out
+
+
+def qgemv_iq3(W, grid, X, out=None, stream=None):
+    """Y[M, N] = X @ dequant(W)^T for an IQ3 matrix W with codebook grid (uint8 [256, 4], doubled units)."""
+    import torch
+    _req(grid, torch.uint8, "grid")
+    if grid.numel() != 1024:
+        raise ValueError("grid must hold 256 x 4 bytes")
+    X, out, M, N, K = _xy(W, X, out, 98)
+    _check("qgemv_iq3", load().qgemv_iq3(W.data_ptr(), grid.data_ptr(), X.data_ptr(), out.data_ptr(), M, N, K,
+                                         _stream(stream)))
+    return out
+
+
+def qgemm_q4k_batched(W, X, out=None, stream=None):
+    """Batched Q4_K GEMM: M < 16 on the fp32 FMA path, M >= 16 on tcgen05 (bf16 operands)."""
+    X, out, M, N, K = _xy(W, X, out, 144)
+    _check("qgemm_q4k_batched", load().qgemm_q4k_batched(W.data_ptr(), X.data_ptr(), out.data_ptr(), M, N, K,
+                                                         _stream(stream)))
+    return out
+
+
+def qdequant_q4k(W, K, out=None, stream=None):
+    """Test-only: fp32 [N, K] dequantisation of a Q4_K matrix."""
+    import torch
+    _req(W, torch.uint8, "W")
+    N = W.numel() // (K // 256 * 144)
+    if out is None:
+        out = torch.empty((N, K), dtype=torch.float32, device=W.device)
+    _check("qdequant_q4k", load().qdequant_q4k(W.data_ptr(), out.data_ptr(), N, K, _stream(stream)))
+    return out
+
+
+def qdequant_iq3(W, grid, K, out=None, stream=None):
+    """Test-only: fp32 [N, K] dequantisation of an IQ3 matrix."""
+    import torch
+    _req(W, torch.uint8, "W")
+    _req(grid, torch.uint8, "grid")
+    N = W.numel() // (K // 256 * 98)
+    if out is None:
+        out = torch.empty((N, K), dtype=torch.float32, device=W.device)
+    _check("qdequant_iq3", load().qdequant_iq3(W.data_ptr(), grid.data_ptr(), out.data_ptr(), N, K,
+                                               _stream(stream)))
+    return out
+
+
+def qg_device_status(stream=None) -> int:
+    """Synchronise the stream and return (and clear) the device status code."""
+    return int(load().qg_device_status(_stream(stream)))
+
+
+def qg_test_bounded_wait(stream=None) -> int:
+    return int(load().qg_test_bounded_wait(_stream(stream)))

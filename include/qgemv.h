@@ -1,0 +1,119 @@
+/*
+ * qgemv: fused-dequantisation GEMV over block-quantised weights (sm_103a).
+ *
+ * C ABI of libqgemv.so.  Plain pointers and sizes only.
+ *
+ * The operation (page 1 "Rewriting picoLM in Python", model_forward /
+ * forward: matmul(out, x, W, n_in, n_out, type) with one output per weight
+ * row) is
+ *
+ *     Y[m][n] = sum_k w[n][k] * X[m][k]      0 <= m < M, 0 <= n < N, 0 <= k < K
+ *
+ * where w is decoded on the fly from the quantised bytes and never stored.
+ *
+ * Layouts (all little-endian, no padding):
+ *   W  row n, then super-block b (256 weights each): byte offset (n*K/256 + b)*B
+ *      with B = 144 for Q4_K, 98 for IQ3.
+ *   X  [M][K] fp32, row-major.     Y  [M][N] fp32, row-major (written, not
+ *      accumulated): Y = X * W^T, the layout of torch.nn.functional.linear.
+ *
+ * Block formats:
+ *   Q4_K (page 1, dequantize_q4_K): fp16 d @0, fp16 dmin @2, 12 bytes of
+ *     packed 6-bit scales/mins @4 (fields j >= 4 straddle bytes), 128 nibble
+ *     bytes @16; weight = d*sc*q - dmin*mn.
+ *   IQ3 (page 4 "iq3_pack.py", fmt=5, module docstring and decode): 64 grid
+ *     index bytes @0, eight u32 @64 (per 32-weight sub-block: four 7-bit sign
+ *     words in bits 0-27, the 8th sign of each 8-group the XOR of its seven
+ *     stored signs, a 4-bit code in bits 28-31), fp16 d @96;
+ *     weight = d*(0.5+code)*0.5 * grid[idx][j]*0.5 * sign.
+ *
+ * Ownership: every pointer is caller-owned device memory; the library
+ * allocates nothing per call.  Calls are asynchronous on `stream` (0 = the
+ * legacy default stream).  Y must not overlap W, X or grid.
+ *
+ * Errors: functions return QG_OK (0) or a negative QG_E* code and never
+ * abort, throw or trap.  Argument errors are detected on the host before any
+ * launch.  Faults detected inside a kernel (a bounded wait that gave up) are
+ * latched in a per-device status word; qg_device_status reports and clears
+ * it.
+ */
+#ifndef QGEMV_H
+#define QGEMV_H
+
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define QG_OK 0
+#define QG_EINVAL (-1)    /* K % 256 != 0, M outside [1, 32], N <= 0, K <= 0, null pointer */
+#define QG_EALIGN (-2)    /* W, X, Y or grid not 16-byte aligned */
+#define QG_ECUDA (-3)     /* a CUDA runtime call or kernel launch failed */
+#define QG_ETIMEOUT (-4)  /* device: a bounded wait inside a kernel gave up */
+#define QG_EBOUNDS (-5)   /* device: an index check inside a kernel failed */
+#define QG_EALIAS (-6)    /* Y overlaps W, X or grid */
+
+#define QG_MAX_M 32
+
+#if defined(__GNUC__)
+#define QG_API __attribute__((visibility("default")))
+#else
+#define QG_API
+#endif
+
+/* Q4_K GEMV, fp32 FMA path, 1 <= M <= 32.
+ * Page 1 "Rewriting picoLM in Python", dequantize_q4_K (format) and
+ * model_forward's matmul (operation).
+ * W: N*K/256*144 bytes.  X: M*K floats.  Y: M*N floats (output).
+ * Numerics: |Y - exact| <= 1e-5 * sum_k |w*x| per element (fp32 FMA,
+ * sub-block-factored sums).  M > 8 is processed in groups of 8 tokens, each
+ * group streaming W once. */
+QG_API int qgemv_q4k(const uint8_t* W, const float* X, float* Y, int M, int64_t N, int64_t K, cudaStream_t stream);
+
+/* IQ3 (98-byte super-block) GEMV, fp32 FMA path, 1 <= M <= 32.
+ * Page 4 "iq3_pack.py", module docstring and decode (format); page 1
+ * model_forward's matmul (operation).
+ * grid: 256*4 bytes, the codebook in the published doubled units (the kernel
+ * applies the 0.5 of page 4's grid()).  Other arguments as qgemv_q4k.
+ * K/256 a multiple of 8 takes the bulk-copy path; other K take a slower
+ * byte-addressed path with identical results. */
+QG_API int qgemv_iq3(const uint8_t* W, const uint8_t* grid, const float* X, float* Y, int M, int64_t N, int64_t K,
+              cudaStream_t stream);
+
+/* Batched Q4_K GEMM for decode batches, 1 <= M <= 32.
+ * Same operation and layouts as qgemv_q4k.  M < 16 runs the fp32 FMA path
+ * (tolerance 1e-5 * sum|w*x|); M >= 16 dequantises W tiles to bf16 (round to
+ * nearest even) in shared memory and multiplies on the tcgen05 tensor cores
+ * with fp32 accumulation in tensor memory, X also rounded to bf16
+ * (tolerance 4e-3 * sum|w*x|). */
+QG_API int qgemm_q4k_batched(const uint8_t* W, const float* X, float* Y, int M, int64_t N, int64_t K, cudaStream_t stream);
+
+/* Test-only: dequantise a Q4_K matrix to fp32 out[N][K] (caller-owned device
+ * memory, N*K floats), bit-exact with page 1's fp32 evaluation order
+ * ((d*sc)*q - (dmin*mn), each operation rounded). */
+QG_API int qdequant_q4k(const uint8_t* W, float* out, int64_t N, int64_t K, cudaStream_t stream);
+
+/* Test-only: dequantise an IQ3 matrix to fp32 out[N][K]; every value is
+ * exact (at most 24 significant bits), hence bit-exact with page 4's decode. */
+QG_API int qdequant_iq3(const uint8_t* W, const uint8_t* grid, float* out, int64_t N, int64_t K, cudaStream_t stream);
+
+/* Synchronise `stream`, then return and clear the current device's status
+ * word: QG_OK, QG_ETIMEOUT or QG_EBOUNDS (QG_ECUDA if the sync failed). */
+QG_API int qg_device_status(cudaStream_t stream);
+
+/* Test-only fault check: launches a kernel whose mbarrier wait can never
+ * complete (nothing arrives on it); the wait gives up after a bounded number
+ * of polls, records QG_ETIMEOUT in the status word and the kernel returns.
+ * Never traps or hangs. */
+QG_API int qg_test_bounded_wait(cudaStream_t stream);
+
+/* Static description of a status code. */
+QG_API const char* qg_strerror(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* QGEMV_H */

@@ -1,0 +1,216 @@
+"""GPU parity: the CUDA path (called through the C ABI) against the CPU oracle.
+
+* qdequant_*: bit-exact (uint32 views equal) with the oracle's fp32 decode.
+* qgemv_* (fp32 FMA path): |y - y_ref| <= 1e-5 * sum_k |w*x| per element,
+  y_ref and sum|w*x| in fp64 from the oracle; rows with sum|w*x| = 0 exactly 0.
+* Full-size shapes of the workloads are checked on sampled rows, in the same
+  launch configuration the bench uses.
+"""
+import numpy as np
+import pytest
+
+import oracle
+from block_quantised_weight_gb300 import synth
+
+torch = pytest.importorskip("torch")
+
+pytestmark = pytest.mark.gpu
+
+TAU_FMA = 1e-5
+
+
+@pytest.fixture(scope="module")
+def q():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from block_quantised_weight_gb300 import build, qgemv
+    build.build()
+    qgemv.load()
+    return qgemv
+
+
+def dev(a):
+    return torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+
+def check_tol(y, Y, A, tau, what=""):
+    y = np.asarray(y, dtype=np.float64)
+    err = np.abs(y - Y)
+    bad = err > tau * A
+    if bad.any():
+        i = np.argwhere(bad)[0]
+        raise AssertionError(f"{what}: {bad.sum()} elements out of tolerance; first {tuple(i)}: "
+                             f"y={y[tuple(i)]!r} ref={Y[tuple(i)]!r} A={A[tuple(i)]!r} "
+                             f"ratio={err[tuple(i)] / max(A[tuple(i)], 1e-300):.3e}")
+    return float((err / np.maximum(A, 1e-300)).max())
+
+
+# ------------------------------------------------------------ dequant, exact
+@pytest.mark.parametrize("N,K", [(1, 256), (7, 768), (33, 2304), (64, 4096)])
+def test_dequant_q4k_bit_exact(q, N, K):
+    W = synth.gen_q4k(N, K, 100 + N)
+    ref = oracle.dequant_q4k(W, K)
+    got = q.qdequant_q4k(dev(W), K).cpu().numpy()
+    assert np.array_equal(got.view(np.uint32), ref.view(np.uint32))
+
+
+@pytest.mark.parametrize("N,K", [(1, 256), (5, 768), (33, 2304), (40, 4096)])
+def test_dequant_iq3_bit_exact(q, N, K):
+    W, grid = synth.gen_iq3(N, K, 200 + N)
+    ref = oracle.dequant_iq3(W, grid, K)
+    got = q.qdequant_iq3(dev(W), dev(grid), K).cpu().numpy()
+    assert np.array_equal(got.view(np.uint32), ref.view(np.uint32))
+
+
+def test_dequant_handworked_blocks(q, golden):
+    # the golden blocks go through the GPU decoder too
+    from tests.test_oracle_pins import _iq3_golden, _q4k_golden, _q4k_golden_block
+    kv, ws, _ = _q4k_golden(golden)
+    blk, _ = _q4k_golden_block(kv, "header")
+    got = q.qdequant_q4k(dev(blk), 256).cpu().numpy()[0]
+    for i, v in ws:
+        assert got[i] == np.float32(v)
+    grid, iblk, vals = _iq3_golden(golden)
+    goti = q.qdequant_iq3(dev(iblk), dev(grid), 256).cpu().numpy()[0]
+    for ib, v in vals.items():
+        assert goti[32 * ib:32 * ib + 32].tolist() == v
+
+
+# ------------------------------------------------------------ GEMV, small
+Q4K_SHAPES = [(1, 256), (31, 256), (33, 512), (100, 2304), (64, 2048), (257, 4096), (40, 5632)]
+
+
+@pytest.mark.parametrize("N,K", Q4K_SHAPES)
+@pytest.mark.parametrize("M", [1, 2, 3, 4, 8])
+def test_gemv_q4k_small(q, N, K, M):
+    W = synth.gen_q4k(N, K, 7 * N + K)
+    x = synth.gen_x(M, K, 3 + M)
+    Y, A = oracle.gemv_q4k(W, x)
+    y = q.qgemv_q4k(dev(W), dev(x)).cpu().numpy()
+    check_tol(y, Y, A, TAU_FMA, f"q4k N={N} K={K} M={M}")
+
+
+@pytest.mark.parametrize("M", [9, 16, 32])
+def test_gemv_q4k_many_tokens(q, M):
+    N, K = 70, 1024
+    W = synth.gen_q4k(N, K, 5)
+    x = synth.gen_x(M, K, 6)
+    Y, A = oracle.gemv_q4k(W, x)
+    check_tol(q.qgemv_q4k(dev(W), dev(x)).cpu().numpy(), Y, A, TAU_FMA, f"q4k M={M}")
+
+
+IQ3_SHAPES = [(1, 2048), (31, 2048), (33, 4096), (100, 2048), (70, 6144),
+              (5, 256), (33, 768), (40, 2304)]   # the last three: K/256 not a multiple of 8
+
+
+@pytest.mark.parametrize("N,K", IQ3_SHAPES)
+@pytest.mark.parametrize("M", [1, 2, 3, 4, 8])
+def test_gemv_iq3_small(q, N, K, M):
+    W, grid = synth.gen_iq3(N, K, 11 * N + K)
+    x = synth.gen_x(M, K, 4 + M)
+    Y, A = oracle.gemv_iq3(W, grid, x)
+    y = q.qgemv_iq3(dev(W), dev(grid), dev(x)).cpu().numpy()
+    check_tol(y, Y, A, TAU_FMA, f"iq3 N={N} K={K} M={M}")
+
+
+@pytest.mark.parametrize("M", [13, 32])
+def test_gemv_iq3_many_tokens(q, M):
+    N, K = 45, 2048
+    W, grid = synth.gen_iq3(N, K, 8)
+    x = synth.gen_x(M, K, 9)
+    Y, A = oracle.gemv_iq3(W, grid, x)
+    check_tol(q.qgemv_iq3(dev(W), dev(grid), dev(x)).cpu().numpy(), Y, A, TAU_FMA, f"iq3 M={M}")
+
+
+def test_zero_rows_are_exactly_zero(q):
+    N, K = 40, 2048
+    W = synth.gen_q4k(N, K, 1)
+    W[3] = 0          # d = dmin = 0 everywhere in the row
+    W[17, 0:144] = 0  # one zero block inside a live row
+    x = synth.gen_x(2, K, 2)
+    y = q.qgemv_q4k(dev(W), dev(x)).cpu().numpy()
+    assert (y[:, 3] == 0).all()
+    Wi, grid = synth.gen_iq3(N, K, 3)
+    Wi[5] = 0         # d = 0 everywhere
+    yi = q.qgemv_iq3(dev(Wi), dev(grid), dev(x)).cpu().numpy()
+    assert (yi[:, 5] == 0).all()
+
+
+def test_handworked_iq3_gemv(q, golden):
+    """The hand-worked IQ3 block dotted with a one-hot x gives its own values."""
+    from tests.test_oracle_pins import _iq3_golden
+    grid, blk, vals = _iq3_golden(golden)
+    W = np.tile(blk, 8)[None, :]              # one row of 8 identical blocks (K = 2048)
+    x = np.zeros((4, 2048), np.float32)
+    for m, k in enumerate([0, 7, 23, 32 + 5]):
+        x[m, k] = 1.0
+    y = q.qgemv_iq3(dev(W), dev(grid), dev(x)).cpu().numpy()[:, 0]
+    assert y.tolist() == [vals[0][0], vals[0][7], vals[0][23], vals[1][5]]
+
+
+# ------------------------------------------------------------ full-size shapes
+def sampled_rows(N, n=96, seed=0):
+    rng = np.random.default_rng(seed)
+    return np.unique(np.concatenate([[0, N - 1], rng.integers(0, N, n)]))
+
+
+@pytest.mark.parametrize("K,N,M", [(2048, 2048, 1), (4096, 11008, 1), (4096, 11008, 2), (4096, 11008, 4),
+                                   (4096, 11008, 8), (8192, 28672, 1), (8192, 28672, 8), (28672, 8192, 1),
+                                   (28672, 8192, 8)])
+def test_gemv_q4k_full_size_sampled(q, K, N, M):
+    W = synth.gen_q4k(N, K, K + N)
+    x = synth.gen_x(M, K, M)
+    rows = sampled_rows(N)
+    Y, A = oracle.gemv_q4k(W, x, rows=rows)
+    y = q.qgemv_q4k(dev(W), dev(x)).cpu().numpy()
+    check_tol(y[:, rows], Y, A, TAU_FMA, f"q4k full K={K} N={N} M={M}")
+    assert np.isfinite(y).all()
+
+
+@pytest.mark.parametrize("K,N,M", [(4096, 14336, 1), (8192, 28672, 1), (8192, 28672, 8), (28672, 8192, 1),
+                                   (28672, 8192, 8)])
+def test_gemv_iq3_full_size_sampled(q, K, N, M):
+    W, grid = synth.gen_iq3(N, K, K + N + 1)
+    x = synth.gen_x(M, K, M + 1)
+    rows = sampled_rows(N)
+    Y, A = oracle.gemv_iq3(W, grid, x, rows=rows)
+    y = q.qgemv_iq3(dev(W), dev(grid), dev(x)).cpu().numpy()
+    check_tol(y[:, rows], Y, A, TAU_FMA, f"iq3 full K={K} N={N} M={M}")
+    assert np.isfinite(y).all()
+
+
+def test_tinyllama_pass_sampled(q):
+    """Every one of the 155 matrices of the TinyLlama-shaped decode pass,
+    sampled rows, through the same entry point the bench times."""
+    for (layer, name, K, N), rng in synth.tinyllama_seeds(1):
+        W = synth.gen_q4k(N, K, rng)
+        x = synth.gen_x(1, K, rng)
+        rows = sampled_rows(N, 24, seed=layer)
+        Y, A = oracle.gemv_q4k(W, x, rows=rows)
+        y = q.qgemv_q4k(dev(W), dev(x)).cpu().numpy()
+        check_tol(y[:, rows], Y, A, TAU_FMA, f"tinyllama {layer}.{name}")
+
+
+# ------------------------------------------------------------ errors
+def test_bounded_wait_reports_timeout_and_context_survives(q):
+    assert q.qg_device_status() == q.QG_OK
+    assert q.qg_test_bounded_wait() == q.QG_OK
+    assert q.qg_device_status() == q.QG_ETIMEOUT
+    assert q.qg_device_status() == q.QG_OK   # cleared
+    W = synth.gen_q4k(8, 512, 0)
+    x = synth.gen_x(1, 512, 0)
+    Y, A = oracle.gemv_q4k(W, x)
+    check_tol(q.qgemv_q4k(dev(W), dev(x)).cpu().numpy(), Y, A, TAU_FMA, "after timeout")
+
+
+def test_binding_raises_on_bad_arguments(q):
+    W = dev(synth.gen_q4k(4, 512, 0))
+    x = torch.zeros((33, 512), device="cuda")
+    with pytest.raises(q.QGError) as e:
+        q.qgemv_q4k(W, x)
+    assert e.value.code == q.QG_EINVAL
+    with pytest.raises(TypeError):
+        q.qgemv_q4k(W.cpu(), x[:1])
+    y = torch.empty((1, 4), device="cuda")
+    rc = q.load().qgemv_q4k(W.data_ptr() + 4, x.data_ptr(), y.data_ptr(), 1, 4, 512, None)
+    assert rc == q.QG_EALIGN
