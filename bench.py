@@ -209,10 +209,11 @@ def run_ours(args, rank, world, local_rank):
             yp = y_dev.data_ptr() + 4 * yo
             wb = weight_bytes(fmt, K, N)
             algo = wb + 4 * M * K + 4 * M * N
+            fl = 0 if args.no_prefetch else qgemv.QG_PREFETCH_WEIGHTS
             if fmt == "q4k":
-                lst.append((lib.qgemv_q4k, (Wd.data_ptr(), xp, yp, M, N, K), wb, algo))
+                lst.append((lib.qgemv_q4k_ex, (Wd.data_ptr(), xp, yp, M, N, K, fl), wb, algo))
             else:
-                lst.append((lib.qgemv_iq3, (Wd.data_ptr(), gd.data_ptr(), xp, yp, M, N, K), wb, algo))
+                lst.append((lib.qgemv_iq3_ex, (Wd.data_ptr(), gd.data_ptr(), xp, yp, M, N, K, fl), wb, algo))
             xo += M * K
             yo += M * N
         launches.append(lst)
@@ -234,8 +235,10 @@ def run_ours(args, rank, world, local_rank):
     torch.cuda.synchronize(dev)
     assert qgemv.qg_device_status() == 0
 
-    # graph of one step (all copies, so one replay = `copies` passes), with an
-    # external event pair around every launch for per-launch durations
+    # graph of one step (all copies, so one replay = `copies` passes); a second,
+    # instrumented graph holds an external event pair around every launch for
+    # per-launch kernel durations (the event nodes serialise the launches, so
+    # it is replayed after the timed region, not inside it)
     rt = cudart()
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in flat]
     for a, b in ev:
@@ -246,14 +249,22 @@ def run_ours(args, rank, world, local_rank):
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g, stream=stream):
         cap = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
-        for i, (fn, a, _wb, _ab) in enumerate(flat):
-            if per_launch_ok:
-                per_launch_ok = rt.cudaEventRecordWithFlags(ctypes.c_void_p(ev[i][0].cuda_event), cap, 1) == 0
+        for fn, a, _wb, _ab in flat:
             rc = fn(*a, cap)
             if rc != 0:
                 raise RuntimeError(f"capture launch failed: {rc}")
-            if per_launch_ok:
-                per_launch_ok = rt.cudaEventRecordWithFlags(ctypes.c_void_p(ev[i][1].cuda_event), cap, 1) == 0
+    gi = torch.cuda.CUDAGraph()
+    if per_launch_ok:
+        with torch.cuda.graph(gi, stream=stream):
+            cap = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+            for i, (fn, a, _wb, _ab) in enumerate(flat):
+                if per_launch_ok:
+                    per_launch_ok = rt.cudaEventRecordWithFlags(ctypes.c_void_p(ev[i][0].cuda_event), cap, 1) == 0
+                rc = fn(*a, cap)
+                if rc != 0:
+                    raise RuntimeError(f"capture launch failed: {rc}")
+                if per_launch_ok:
+                    per_launch_ok = rt.cudaEventRecordWithFlags(ctypes.c_void_p(ev[i][1].cuda_event), cap, 1) == 0
     passes_per_replay = copies
 
     with torch.cuda.stream(stream):
@@ -283,6 +294,10 @@ def run_ours(args, rank, world, local_rank):
     durs = None
     if per_launch_ok:
         try:
+            with torch.cuda.stream(stream):
+                for _ in range(3):
+                    gi.replay()
+            torch.cuda.synchronize(dev)
             durs = [a.elapsed_time(b) for a, b in ev]
         except Exception:
             durs = None
@@ -334,10 +349,12 @@ def run_ours(args, rank, world, local_rank):
                 "peak_kind": f"of {peak_kind}", "kernel": "qgemv_q4k gemv_kernel<Q4K,M=1>"
                 if mats[0][0] == "q4k" else "qgemv_iq3 gemv_kernel<IQ3>",
                 "launches_timed": len(durs), "kernel_ms_per_pass": round(kern_ms / passes_per_replay, 4),
+                "durations": "CUDA events around each launch, instrumented replay of the same graph right after "
+                             "the timed region (launches serialised there)",
                 "algorithmic_bytes_per_launch": round(algo / len(durs))}
         by_shape = {}
         for (fn, a, wb, ab), d in zip(flat, durs):
-            key = f"K{a[-1]}xN{a[-2]}"
+            key = f"K{a[-2]}xN{a[-3]}"
             e = by_shape.setdefault(key, [0, 0.0, 0])
             e[0] += 1
             e[1] += d
@@ -351,7 +368,10 @@ def run_ours(args, rank, world, local_rank):
         "config": {"workload": desc, "M": M, "weight_bytes_per_step": step_wbytes,
                    "l2": ("inputs larger than L2" if copies == 1 else
                           f"rotates {copies} weight copies (> 2x L2)"),
-                   "graph": "CUDA graph of the step, replayed", "parallelism": f"replicas x{world}"},
+                   "graph": "CUDA graph of the step, replayed", "parallelism": f"replicas x{world}",
+                   "launch": ("stream-ordered" if args.no_prefetch else
+                              "programmatic dependent launch: each GEMV streams its first weight tiles while "
+                              "the previous one finishes and waits for it before reading x")},
         "tokens_per_s_equiv": round(world * 1000.0 / ms_step, 1),
         "pct_of_hbm_peak": round(100 * value / world / peak, 1),
         "e2e": {"value": round(e2e_value, 1), "unit": "GB/s", "h2d_bytes_per_step": int(xs_host.nbytes),
@@ -432,6 +452,7 @@ def main():
     ap.add_argument("--workload", default="tinyllama")
     ap.add_argument("--M", type=int, default=1)
     ap.add_argument("--cpu-baseline-s", type=float, default=12.0)
+    ap.add_argument("--no-prefetch", action="store_true", help="plain stream-ordered launches")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

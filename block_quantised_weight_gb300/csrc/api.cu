@@ -74,21 +74,33 @@ __global__ void bounded_wait_probe(unsigned* status) {
 
 extern "C" {
 
-int qgemv_q4k(const uint8_t* W, const float* X, float* Y, int M, int64_t N, int64_t K, cudaStream_t stream) {
+int qgemv_q4k_ex(const uint8_t* W, const float* X, float* Y, int M, int64_t N, int64_t K, unsigned flags,
+                 cudaStream_t stream) {
+    if (flags & ~static_cast<unsigned>(QG_PREFETCH_WEIGHTS)) return QG_EINVAL;
     int rc = check_gemv(W, nullptr, false, X, Y, M, N, K, 144);
     if (rc != QG_OK) return rc;
     unsigned* st = status_ptr();
     if (!st) return QG_ECUDA;
-    return qg::launch_gemv_q4k(W, X, Y, M, N, K, stream, st);
+    return qg::launch_gemv_q4k(W, X, Y, M, N, K, stream, st, flags);
 }
 
-int qgemv_iq3(const uint8_t* W, const uint8_t* grid, const float* X, float* Y, int M, int64_t N, int64_t K,
-              cudaStream_t stream) {
+int qgemv_q4k(const uint8_t* W, const float* X, float* Y, int M, int64_t N, int64_t K, cudaStream_t stream) {
+    return qgemv_q4k_ex(W, X, Y, M, N, K, 0u, stream);
+}
+
+int qgemv_iq3_ex(const uint8_t* W, const uint8_t* grid, const float* X, float* Y, int M, int64_t N, int64_t K,
+                 unsigned flags, cudaStream_t stream) {
+    if (flags & ~static_cast<unsigned>(QG_PREFETCH_WEIGHTS)) return QG_EINVAL;
     int rc = check_gemv(W, grid, true, X, Y, M, N, K, 98);
     if (rc != QG_OK) return rc;
     unsigned* st = status_ptr();
     if (!st) return QG_ECUDA;
-    return qg::launch_gemv_iq3(W, grid, X, Y, M, N, K, stream, st);
+    return qg::launch_gemv_iq3(W, grid, X, Y, M, N, K, stream, st, flags);
+}
+
+int qgemv_iq3(const uint8_t* W, const uint8_t* grid, const float* X, float* Y, int M, int64_t N, int64_t K,
+              cudaStream_t stream) {
+    return qgemv_iq3_ex(W, grid, X, Y, M, N, K, 0u, stream);
 }
 
 int qgemm_q4k_batched(const uint8_t* W, const float* X, float* Y, int M, int64_t N, int64_t K, cudaStream_t stream) {
@@ -96,7 +108,7 @@ int qgemm_q4k_batched(const uint8_t* W, const float* X, float* Y, int M, int64_t
     if (rc != QG_OK) return rc;
     unsigned* st = status_ptr();
     if (!st) return QG_ECUDA;
-    if (M < 16) return qg::launch_gemv_q4k(W, X, Y, M, N, K, stream, st);
+    if (M < 16) return qg::launch_gemv_q4k(W, X, Y, M, N, K, stream, st, 0u);
     return qg::launch_gemm_q4k_tc(W, X, Y, M, N, K, stream, st);
 }
 

@@ -130,6 +130,25 @@ __device__ __forceinline__ void ffma2(f2& acc, f2 a, f2 b) {
         : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
 }
 
+// Packed fp32x2 add: a += b element-wise.
+__device__ __forceinline__ void fadd2(f2& a, f2 b) {
+    asm("{\n\t.reg .b64 ra, rb;\n\t"
+        "mov.b64 ra, {%0, %1};\n\t"
+        "mov.b64 rb, {%2, %3};\n\t"
+        "add.rn.f32x2 ra, ra, rb;\n\t"
+        "mov.b64 {%0, %1}, ra;\n\t}"
+        : "+f"(a.x), "+f"(a.y)
+        : "f"(b.x), "f"(b.y));
+}
+
+// Both fp16 halves of a 32-bit register -> fp32 (exact).
+__device__ __forceinline__ f2 h2_to_f2(uint32_t h) {
+    f2 r;
+    asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %2;\n\tcvt.f32.f16 %0, lo;\n\tcvt.f32.f16 %1, hi;\n\t}"
+        : "=f"(r.x), "=f"(r.y) : "r"(h));
+    return r;
+}
+
 __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
     uint32_t r;
     asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(sel));

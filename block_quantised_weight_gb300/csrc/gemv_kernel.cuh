@@ -1,0 +1,497 @@
+// Fused-dequantisation GEMV over block-quantised weights, fp32 FMA path.
+//
+//   Y[m][n] = sum_k w[n][k] * X[m][k],   m < MT <= 8 tokens per launch
+//
+// w is never materialised: each consumer thread decodes one 256-weight
+// super-block in registers and dots it with x.  Formats:
+//   Q4_K  page 1 "Rewriting picoLM in Python", dequantize_q4_K
+//   IQ3   page 4 "iq3_pack.py" (fmt=5), module docstring and decode
+//
+// CTA = RG row groups x 8 consumer warps + 1 producer warp.
+//   * A tile is RG*32 consecutive rows; the CTA walks the tile's K range in
+//     chunks of 8 super-block columns ("units").
+//   * The producer warp posts, per unit, one cp.async.bulk per row (the row's
+//     8 blocks are contiguous in HBM) into a padded smem slot, plus one copy
+//     per token of the matching x slice, on the stage's `full` mbarrier.  It
+//     reuses a stage once all consumer warps have arrived on its `empty`
+//     mbarrier: no CTA-wide barrier in the steady state.
+//   * Consumer warp (rg, c): lane r decodes block (row rg*32 + r, column c).
+//     The 8 lanes of a quarter-warp read 8 different rows: the smem row
+//     stride is an odd multiple of 16 bytes, so the 16-byte loads are
+//     conflict-free; all 32 lanes read the same x (broadcast).
+//   * Per-row partial sums stay in registers across a tile's units and are
+//     reduced over the 8 column warps through a double-buffered smem array
+//     once per tile (one named barrier among the consumers).
+//
+// Q4_K arithmetic: for sub-block j,
+//   sum_l (d*sc_j*q_l - dmin*mn_j) * x_l = (d*sc_j) * sum_l q_l*x_l - (dmin*mn_j) * sum_l x_l
+// and sum_l x_l is computed once per (column, token) by the warp, shared by
+// its 32 rows.
+#pragma once
+#include <cuda_fp16.h>
+
+#include "common.cuh"
+
+namespace qg {
+
+constexpr int kRows = 32;        // rows per row group (one per lane)
+constexpr int kCols = 8;         // super-block columns per unit (one per consumer warp)
+constexpr int kMaxStages = 6;
+constexpr int kSmemPerSM = 233472;   // 228 KB per SM on sm_103
+constexpr int kSmemPerCTA = 232448;  // 227 KB max dynamic smem per CTA
+constexpr int kSmemReserve = 1024;   // per-CTA system reservation
+
+struct FmtQ4K {
+    static constexpr int kBytes = 144;
+    static constexpr int kRowStride = kCols * 144 + 16;  // 1168 = 73 * 16 (odd)
+    static constexpr bool kIQ3 = false;
+};
+struct FmtIQ3 {
+    static constexpr int kBytes = 98;
+    static constexpr int kRowStride = kCols * 98;  // 784 = 49 * 16 (odd)
+    static constexpr bool kIQ3 = true;
+};
+
+// IQ3 grid table in smem, lane-replicated so every gather is conflict-free:
+// for grid row i, lane L reads word 64*i + L (fp16 magnitudes 0,1) and word
+// 64*i + 32 + L (fp16 magnitudes 2,3).  64 KB, shared by all consumer warps.
+constexpr int kIQ3TableBytes = 256 * 64 * 4;
+
+__host__ __device__ constexpr int align_up(int v, int a) { return (v + a - 1) / a * a; }
+__host__ __device__ inline int64_t min64(int64_t a, int64_t b) { return a < b ? a : b; }
+
+struct Layout {
+    int full, empty, sx, red, table, stage0, stage_bytes, xoff, total;
+};
+
+// Dynamic smem layout of gemv_kernel<F, MT, XS, RG> with `stages` stages.
+__host__ __device__ inline Layout make_layout(bool iq3, int MT, bool xs, int RG, int stages, int row_stride) {
+    Layout L;
+    const int warps = RG * kCols;
+    L.full = 0;
+    L.empty = 8 * kMaxStages;
+    L.sx = 128;
+    L.red = L.sx + align_up(warps * MT * 8 * 4, 128);
+    L.table = L.red + align_up(2 * warps * MT * kRows * 4, 128);
+    L.stage0 = L.table + (iq3 ? kIQ3TableBytes : 0);
+    L.xoff = align_up(RG * kRows * row_stride, 128);
+    L.stage_bytes = L.xoff + (xs ? MT * kCols * 1024 : 0);
+    L.total = L.stage0 + stages * L.stage_bytes;
+    return L;
+}
+
+// ------------------------------------------------------------ Q4_K helpers
+// The 12 packed bytes (little-endian words P0, P1, P2) -> eight 6-bit scales
+// and mins, four per result word (byte k of sc03 = sc[k], of sc47 = sc[4+k]).
+// Page 1: j < 4 -> low six bits of byte j (scale) / j+4 (min); j >= 4 ->
+// low (scale) / high (min) nibble of byte j+4, with bits 6-7 of byte j-4
+// (scale) / byte j (min) as bits 4-5.
+__device__ __forceinline__ void q4k_scale_min_words(uint32_t P0, uint32_t P1, uint32_t P2, uint32_t& sc03,
+                                                    uint32_t& mn03, uint32_t& sc47, uint32_t& mn47) {
+    sc03 = P0 & 0x3F3F3F3Fu;
+    mn03 = P1 & 0x3F3F3F3Fu;
+    sc47 = (P2 & 0x0F0F0F0Fu) | ((P0 >> 2) & 0x30303030u);
+    mn47 = ((P2 >> 4) & 0x0F0F0F0Fu) | ((P1 >> 2) & 0x30303030u);
+}
+
+__device__ __forceinline__ float byte_f(uint32_t w, int k) { return static_cast<float>((w >> (8 * k)) & 0xFFu); }
+__device__ __forceinline__ float half_lo(uint32_t h) {
+    return __half2float(__ushort_as_half(static_cast<unsigned short>(h & 0xFFFFu)));
+}
+__device__ __forceinline__ float half_hi(uint32_t h) {
+    return __half2float(__ushort_as_half(static_cast<unsigned short>(h >> 16)));
+}
+
+// acc += a * b on two fp32 lanes: packed FMA or two scalar FMAs.
+template <bool PACKED>
+__device__ __forceinline__ void fma2(f2& acc, f2 a, f2 b) {
+    if constexpr (PACKED) {
+        ffma2(acc, a, b);
+    } else {
+        acc.x = fmaf(a.x, b.x, acc.x);
+        acc.y = fmaf(a.y, b.y, acc.y);
+    }
+}
+
+// One Q4_K super-block (144 bytes at blk, smem) against MT tokens of x.
+// sx[m*8 + j] = sum of x over sub-block j for token m.
+// Nibbles become exact fp32 through the fp16 magic 0x6400|q (= 1024 + q):
+// low nibbles give 1024+q, high nibbles (left in place) 1024+16q, and the
+// mixed f16->f32 add of -1024 yields q or 16q exactly; the 1/16 is folded
+// into the sub-block scale (exact, a power of two).
+template <int MT, bool PACKED, int CVT>
+__device__ __forceinline__ void q4k_block(const uint8_t* blk, const float* xb, int64_t xstride, const float* sx,
+                                          int M, float (&acc)[MT]) {
+    const uint4 h = *reinterpret_cast<const uint4*>(blk);
+    const float d = h2f(h.x), dmin = h2f(h.x >> 16);
+    uint32_t sc03, mn03, sc47, mn47;
+    q4k_scale_min_words(h.y, h.z, h.w, sc03, mn03, sc47, mn47);
+    float mt[MT];
+#pragma unroll
+    for (int m = 0; m < MT; ++m) mt[m] = 0.f;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        const float dmn = dmin * byte_f(j < 4 ? mn03 : mn47, j & 3);
+#pragma unroll
+        for (int m = 0; m < MT; ++m)
+            if (MT == 1 || m < M) mt[m] = fmaf(dmn, sx[m * 8 + j], mt[m]);
+    }
+#pragma unroll
+    for (int g = 0; g < 4; ++g) {
+        const uint32_t scw = g < 2 ? sc03 : sc47;
+        const float dl = d * byte_f(scw, (2 * g) & 3);
+        const float dh = d * byte_f(scw, (2 * g + 1) & 3) * 0.0625f;
+        f2 al[MT], ah[MT];
+#pragma unroll
+        for (int m = 0; m < MT; ++m) al[m] = ah[m] = f2{0.f, 0.f};
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+            const uint4 q = *reinterpret_cast<const uint4*>(blk + 16 + 32 * g + 16 * hh);
+            const uint32_t qv[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int kl = 64 * g + 16 * hh + 4 * e;  // weights kl..kl+3 (low), +32 (high)
+                if constexpr (CVT == 0) {
+                    const uint32_t v = qv[e], v8 = v >> 8;
+                    const uint32_t A = (v & 0x000F000Fu) | 0x64006400u;   // bytes 0,2 low nibbles
+                    const uint32_t C = (v8 & 0x000F000Fu) | 0x64006400u;  // bytes 1,3 low nibbles
+                    const uint32_t B = (v & 0x00F000F0u) | 0x64006400u;   // bytes 0,2 high nibbles (x16)
+                    const uint32_t D = (v8 & 0x00F000F0u) | 0x64006400u;  // bytes 1,3 high nibbles (x16)
+                    const f2 l01{add_f16_f32(A, -1024.f), add_f16_f32(C, -1024.f)};
+                    const f2 l23{add_f16hi_f32(A, -1024.f), add_f16hi_f32(C, -1024.f)};
+                    const f2 h01{add_f16_f32(B, -1024.f), add_f16_f32(D, -1024.f)};
+                    const f2 h23{add_f16hi_f32(B, -1024.f), add_f16hi_f32(D, -1024.f)};
+#pragma unroll
+                    for (int m = 0; m < MT; ++m) {
+                        if (MT == 1 || m < M) {
+                            const float4 xl = *reinterpret_cast<const float4*>(xb + m * xstride + kl);
+                            const float4 xh = *reinterpret_cast<const float4*>(xb + m * xstride + kl + 32);
+                            fma2<PACKED>(al[m], l01, f2{xl.x, xl.y});
+                            fma2<PACKED>(al[m], l23, f2{xl.z, xl.w});
+                            fma2<PACKED>(ah[m], h01, f2{xh.x, xh.y});
+                            fma2<PACKED>(ah[m], h23, f2{xh.z, xh.w});
+                        }
+                    }
+                } else {
+                    // fp32 magic in place: (bits & mask) | 0x4B000000 = 2^23 + c*q with
+                    // c = 1 (bits 0-3), 16 (4-7), 256 (8-11), 4096 (12-15); the packed
+                    // add of -2^23 leaves c*q exactly.  Pair (byte k, byte k+1) puts the
+                    // c=1 (or 16) terms in lane .x and the c=256 (or 4096) terms in .y.
+                    const uint32_t v = qv[e], u = v >> 16;
+                    const f2 mg{-8388608.f, -8388608.f};
+                    f2 l01{__uint_as_float((v & 0xFu) | 0x4B000000u), __uint_as_float((v & 0xF00u) | 0x4B000000u)};
+                    f2 l23{__uint_as_float((u & 0xFu) | 0x4B000000u), __uint_as_float((u & 0xF00u) | 0x4B000000u)};
+                    f2 h01{__uint_as_float((v & 0xF0u) | 0x4B000000u), __uint_as_float((v & 0xF000u) | 0x4B000000u)};
+                    f2 h23{__uint_as_float((u & 0xF0u) | 0x4B000000u), __uint_as_float((u & 0xF000u) | 0x4B000000u)};
+                    fadd2(l01, mg);
+                    fadd2(l23, mg);
+                    fadd2(h01, mg);
+                    fadd2(h23, mg);
+#pragma unroll
+                    for (int m = 0; m < MT; ++m) {
+                        if (MT == 1 || m < M) {
+                            const float4 xl = *reinterpret_cast<const float4*>(xb + m * xstride + kl);
+                            const float4 xh = *reinterpret_cast<const float4*>(xb + m * xstride + kl + 32);
+                            fma2<PACKED>(al[m], l01, f2{xl.x, xl.y});
+                            fma2<PACKED>(al[m], l23, f2{xl.z, xl.w});
+                            fma2<PACKED>(ah[m], h01, f2{xh.x, xh.y});
+                            fma2<PACKED>(ah[m], h23, f2{xh.z, xh.w});
+                        }
+                    }
+                }
+            }
+        }
+#pragma unroll
+        for (int m = 0; m < MT; ++m) {
+            if (MT == 1 || m < M) {
+                if constexpr (CVT == 0) {
+                    acc[m] = fmaf(dl, al[m].x + al[m].y, acc[m]);
+                    acc[m] = fmaf(dh, ah[m].x + ah[m].y, acc[m]);
+                } else {
+                    acc[m] = fmaf(dl, fmaf(al[m].y, 0.00390625f, al[m].x), acc[m]);
+                    acc[m] = fmaf(dh, fmaf(ah[m].y, 0.00390625f, ah[m].x), acc[m]);
+                }
+            }
+        }
+    }
+#pragma unroll
+    for (int m = 0; m < MT; ++m) acc[m] -= mt[m];
+}
+
+// Load the IQ3 super-block at byte COL*98 of a 16-byte aligned row chunk in
+// smem and realign it: v[i] = block bytes 4i..4i+3 (i < 24: the 64 index
+// bytes and the eight sign/scale words), d = the fp16 at block byte 96.
+// Only this small step is specialised per column; the decoder is shared.
+template <int COL>
+__device__ __forceinline__ void iq3_load_block(const uint8_t* rowp, uint32_t (&v)[24], uint32_t& dbits) {
+    constexpr int S0 = COL * 98, A0 = S0 & ~15, OFF = S0 - A0;
+    uint32_t w[28];
+#pragma unroll
+    for (int i = 0; i < 7; ++i) {
+        const uint4 t = *reinterpret_cast<const uint4*>(rowp + A0 + 16 * i);
+        w[4 * i] = t.x;
+        w[4 * i + 1] = t.y;
+        w[4 * i + 2] = t.z;
+        w[4 * i + 3] = t.w;
+    }
+#pragma unroll
+    for (int i = 0; i < 24; ++i) {
+        const int P = OFF + 4 * i;
+        v[i] = (P & 3) == 0 ? w[P >> 2] : __funnelshift_r(w[P >> 2], w[(P >> 2) + 1], 8 * (P & 3));
+    }
+    constexpr int PD = OFF + 96;
+    dbits = w[PD >> 2] >> (8 * (PD & 3));
+}
+
+// One IQ3 super-block (realigned: v, d) against MT tokens.
+// Each 4-weight group gathers its grid row from the lane-replicated fp16
+// table (exact magnitudes), flips signs in the fp16 domain (sign bits moved
+// to bits 15/31 by one multiply; the shifted copies of the sign byte never
+// overlap, so there are no carries), converts to fp32 and FMAs.  The
+// sub-block factor d*(0.5+code)*0.5 and the grid's 0.5 are applied once per
+// 32 weights (exact: at most 16 significant bits).
+template <int MT, bool PACKED>
+__device__ __forceinline__ void iq3_block(const uint32_t (&v)[24], uint32_t dbits, const uint32_t* tbl, uint32_t lane4,
+                                          const float* xb, int64_t xstride, int M, float (&acc)[MT]) {
+    const float d = h2f(dbits);
+    const uint8_t* tb = reinterpret_cast<const uint8_t*>(tbl);
+#pragma unroll
+    for (int ib = 0; ib < 8; ++ib) {
+        const uint32_t sw = v[16 + ib];
+        const float db = d * (static_cast<float>(sw >> 28) + 0.5f) * 0.25f;
+        f2 dot[MT];
+#pragma unroll
+        for (int m = 0; m < MT; ++m) dot[m] = f2{0.f, 0.f};
+#pragma unroll
+        for (int l = 0; l < 4; ++l) {
+            const uint32_t seven = (sw >> (7 * l)) & 0x7Fu;
+            const uint32_t s8 = seven | ((__popc(seven) & 1u) << 7);
+#pragma unroll
+            for (int hf = 0; hf < 2; ++hf) {
+                const int PI = 8 * ib + 2 * l + hf;  // grid index byte of weights 8l+4hf..+3
+                const uint32_t off =
+                    prmt(v[PI >> 2], lane4, 4u | (static_cast<uint32_t>(PI & 3) << 4) | (5u << 8) | (5u << 12));
+                const uint32_t* tp = reinterpret_cast<const uint32_t*>(tb + off);
+                uint32_t h01 = tp[0], h23 = tp[32];
+                const uint32_t k01 = hf ? ((1u << 11) + (1u << 26)) : ((1u << 15) + (1u << 30));
+                const uint32_t k23 = hf ? ((1u << 9) + (1u << 24)) : ((1u << 13) + (1u << 28));
+                h01 ^= (s8 * k01) & 0x80008000u;
+                h23 ^= (s8 * k23) & 0x80008000u;
+                const f2 w01 = h2_to_f2(h01);
+                const f2 w23 = h2_to_f2(h23);
+#pragma unroll
+                for (int m = 0; m < MT; ++m) {
+                    if (MT == 1 || m < M) {
+                        const float4 x = *reinterpret_cast<const float4*>(xb + m * xstride + 32 * ib + 8 * l + 4 * hf);
+                        fma2<PACKED>(dot[m], w01, f2{x.x, x.y});
+                        fma2<PACKED>(dot[m], w23, f2{x.z, x.w});
+                    }
+                }
+            }
+        }
+#pragma unroll
+        for (int m = 0; m < MT; ++m)
+            if (MT == 1 || m < M) acc[m] = fmaf(db, dot[m].x + dot[m].y, acc[m]);
+    }
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+    asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+// Launch flag: W and the grid are not written by the preceding kernel in the
+// stream, so they may be prefetched before the grid dependency is resolved.
+constexpr int kFlagPrefetchWeights = 1;
+
+__device__ __forceinline__ void grid_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+template <int N>
+__device__ __forceinline__ void named_barrier_sync(int id) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "n"(N) : "memory");
+}
+
+// ------------------------------------------------------------ the kernel
+// Threads: RG*8 consumer warps, then one producer warp.
+template <class F, int MT, bool XS, int RG, bool PACKED, int MINB, int CVT = 0>
+__global__ void __launch_bounds__(RG * kCols * 32 + 32, MINB)
+    gemv_kernel(const uint8_t* __restrict__ W, const uint8_t* __restrict__ grid, const float* __restrict__ X,
+                float* __restrict__ Y, int M, int64_t N, int64_t K, int stages, unsigned* status, int flags) {
+    constexpr int kWarps = RG * kCols;          // consumer warps
+    constexpr int kConsumerThreads = kWarps * 32;
+    constexpr int kTileRows = RG * kRows;
+    extern __shared__ __align__(128) uint8_t smem[];
+    const int nb = static_cast<int>(K / 256);
+    const int nchunks = (nb + kCols - 1) / kCols;
+    const int64_t ntiles = (N + kTileRows - 1) / kTileRows;
+    const Layout L = make_layout(F::kIQ3, MT, XS, RG, stages, F::kRowStride);
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.full);
+    uint64_t* empty = reinterpret_cast<uint64_t*>(smem + L.empty);
+    float* sxw = reinterpret_cast<float*>(smem + L.sx);
+    float* red = reinterpret_cast<float*>(smem + L.red);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t pitch = static_cast<int64_t>(nb) * F::kBytes;
+
+    // Programmatic dependent launch: let the next kernel in the stream get
+    // scheduled now.  Without the weight-prefetch flag, wait for the previous
+    // kernel before touching any global memory; with it, only W and the grid
+    // (weights, never written by the previous kernel) are read before the wait.
+    grid_launch_dependents();
+    const bool prefetch = (flags & kFlagPrefetchWeights) != 0;
+    if (!prefetch) grid_dependency_wait();
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < stages; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], kWarps);
+        }
+        fence_mbar_init();
+    }
+    if constexpr (F::kIQ3) {
+        // fp16 copies of the doubled-unit magnitudes (exact: bytes < 2048)
+        uint32_t* tbl = reinterpret_cast<uint32_t*>(smem + L.table);
+        for (int i = threadIdx.x; i < 256 * 32; i += blockDim.x) {
+            const int row = i >> 5, ln = i & 31;
+            const uint32_t g = *reinterpret_cast<const uint32_t*>(grid + 4 * row);
+            const __half2 a = __floats2half2_rn(byte_f(g, 0), byte_f(g, 1));
+            const __half2 b = __floats2half2_rn(byte_f(g, 2), byte_f(g, 3));
+            tbl[64 * row + ln] = *reinterpret_cast<const uint32_t*>(&a);
+            tbl[64 * row + 32 + ln] = *reinterpret_cast<const uint32_t*>(&b);
+        }
+    }
+    __syncthreads();
+
+    const int64_t my_tiles =
+        static_cast<int64_t>(blockIdx.x) < ntiles ? (ntiles - 1 - blockIdx.x) / gridDim.x + 1 : 0;
+    const int64_t U = my_tiles * nchunks;
+
+    if (warp == kWarps) {
+        // ---------------- producer warp
+        const uint64_t pol_w = policy_evict_first();
+        const uint64_t pol_x = policy_evict_last();
+        // unit u -> (stage, tile rows, chunk); post its copies (W and/or x)
+        auto post = [&](int64_t u, bool do_w, bool do_x, bool expect) {
+            const int s = static_cast<int>(u % stages);
+            const int c = static_cast<int>(u % nchunks);
+            const int64_t tile = blockIdx.x + (u / nchunks) * gridDim.x;
+            const int64_t row0 = tile * kTileRows;
+            const int rows = static_cast<int>(min64(kTileRows, N - row0));
+            const int kc = min(kCols, nb - c * kCols);
+            uint8_t* st = smem + L.stage0 + s * L.stage_bytes;
+            if (expect) {
+                const uint32_t bytes = rows * kc * F::kBytes + (XS ? M * kc * 1024 : 0);
+                if (lane == 0) mbar_arrive_expect_tx(&full[s], bytes);
+                __syncwarp();
+            }
+            if (do_w) {
+                const uint8_t* src = W + row0 * pitch + static_cast<int64_t>(c) * kCols * F::kBytes;
+                for (int r = lane; r < rows; r += 32)
+                    bulk_g2s(st + r * F::kRowStride, src + r * pitch, kc * F::kBytes, &full[s], pol_w);
+            }
+            if (XS && do_x && lane < M)
+                bulk_g2s(st + L.xoff + lane * kCols * 1024, X + lane * K + static_cast<int64_t>(c) * kCols * 256,
+                         kc * 1024, &full[s], pol_x);
+        };
+        int64_t u0 = 0;
+        if (prefetch) {
+            // weights of the first stages stream while the previous kernel runs
+            const int64_t pre = min64(stages, U);
+            for (int64_t u = 0; u < pre; ++u) post(u, true, false, true);
+            grid_dependency_wait();
+            for (int64_t u = 0; u < pre; ++u) post(u, false, true, false);
+            u0 = pre;
+        }
+        for (int64_t u = u0; u < U; ++u) {
+            const int s = static_cast<int>(u % stages);
+            if (u >= stages) mbar_wait_bounded(&empty[s], static_cast<uint32_t>(((u / stages) - 1) & 1), status);
+            post(u, true, true, true);
+        }
+        return;
+    }
+
+    // ---------------- consumer warps
+    if (prefetch) grid_dependency_wait();  // x and Y belong to the dependency chain
+    const int rg = warp / kCols, cw = warp % kCols;
+    float acc[MT];
+#pragma unroll
+    for (int m = 0; m < MT; ++m) acc[m] = 0.f;
+    const uint32_t lane4 = static_cast<uint32_t>(lane) * 4u;
+    int64_t tile_count = 0;
+
+    for (int64_t u = 0; u < U; ++u) {
+        const int s = static_cast<int>(u % stages);
+        const int c = static_cast<int>(u % nchunks);
+        const int64_t tile = blockIdx.x + (u / nchunks) * gridDim.x;
+        const int64_t row0 = tile * kTileRows;
+        const int rows = static_cast<int>(min64(kTileRows, N - row0));
+        const int kc = min(kCols, nb - c * kCols);
+        const uint8_t* st = smem + L.stage0 + s * L.stage_bytes;
+        const int r = rg * kRows + lane;  // row within the tile
+        mbar_wait_bounded(&full[s], static_cast<uint32_t>((u / stages) & 1), status);
+
+        if (cw < kc) {
+            const int64_t b = static_cast<int64_t>(c) * kCols + cw;  // super-block column
+            const float* xb = XS ? reinterpret_cast<const float*>(st + L.xoff) + cw * 256 : X + b * 256;
+            const int64_t xstride = XS ? kCols * 256 : K;
+            if constexpr (!F::kIQ3) {
+                float* sxp = sxw + warp * MT * 8;
+#pragma unroll
+                for (int m = 0; m < MT; ++m) {
+                    if (MT == 1 || m < M) {
+                        const float* xp = xb + m * xstride + (lane >> 2) * 32 + (lane & 3) * 8;
+                        const float4 a = *reinterpret_cast<const float4*>(xp);
+                        const float4 bb = *reinterpret_cast<const float4*>(xp + 4);
+                        float sm = ((a.x + a.y) + (a.z + a.w)) + ((bb.x + bb.y) + (bb.z + bb.w));
+                        sm += __shfl_xor_sync(0xffffffffu, sm, 1);
+                        sm += __shfl_xor_sync(0xffffffffu, sm, 2);
+                        if ((lane & 3) == 0) sxp[m * 8 + (lane >> 2)] = sm;
+                    }
+                }
+                __syncwarp();
+                if (r < rows) q4k_block<MT, PACKED, CVT>(st + r * F::kRowStride + cw * F::kBytes, xb, xstride, sxp, M, acc);
+            } else {
+                if (r < rows) {
+                    const uint8_t* rowp = st + r * F::kRowStride;
+                    const uint32_t* tbl = reinterpret_cast<const uint32_t*>(smem + L.table);
+                    uint32_t v[24], dbits;
+                    switch (cw) {
+                        case 0: iq3_load_block<0>(rowp, v, dbits); break;
+                        case 1: iq3_load_block<1>(rowp, v, dbits); break;
+                        case 2: iq3_load_block<2>(rowp, v, dbits); break;
+                        case 3: iq3_load_block<3>(rowp, v, dbits); break;
+                        case 4: iq3_load_block<4>(rowp, v, dbits); break;
+                        case 5: iq3_load_block<5>(rowp, v, dbits); break;
+                        case 6: iq3_load_block<6>(rowp, v, dbits); break;
+                        default: iq3_load_block<7>(rowp, v, dbits); break;
+                    }
+                    iq3_block<MT, PACKED>(v, dbits, tbl, lane4, xb, xstride, M, acc);
+                }
+            }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[s]);
+
+        if (c == nchunks - 1) {
+            // reduce the 8 column warps' partial sums of each row, write Y
+            float* rb = red + (tile_count & 1) * (kWarps * MT * kRows);
+#pragma unroll
+            for (int m = 0; m < MT; ++m) {
+                rb[(warp * MT + m) * kRows + lane] = acc[m];
+                acc[m] = 0.f;
+            }
+            named_barrier_sync<kConsumerThreads>(1);
+            for (int t = threadIdx.x; t < MT * kTileRows; t += kConsumerThreads) {
+                const int m = t / kTileRows, rr = t % kTileRows;
+                const int g = rr / kRows, ln = rr % kRows;
+                if ((MT == 1 || m < M) && rr < rows) {
+                    float sum = 0.f;
+#pragma unroll
+                    for (int w = 0; w < kCols; ++w) sum += rb[((g * kCols + w) * MT + m) * kRows + ln];
+                    Y[m * N + row0 + rr] = sum;
+                }
+            }
+            ++tile_count;
+        }
+    }
+}
+
+}  // namespace qg

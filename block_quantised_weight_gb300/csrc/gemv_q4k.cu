@@ -1,0 +1,25 @@
+// Q4_K GEMV launcher (fp32 FMA path).  Kernel: gemv_kernel.cuh.
+#include "launch_common.cuh"
+
+namespace qg {
+
+// M is split into groups of at most 8 tokens; each group streams W once.
+int launch_gemv_q4k(const uint8_t* W, const float* X, float* Y, int M, int64_t N, int64_t K, cudaStream_t s,
+                    unsigned* status, unsigned flags) {
+    const int dev = current_device();
+    if (dev < 0) return QG_ECUDA;
+    for (int m0 = 0; m0 < M; m0 += 8) {
+        const int mg = std::min(8, M - m0);
+        const float* Xg = X + static_cast<int64_t>(m0) * K;
+        float* Yg = Y + static_cast<int64_t>(m0) * N;
+        int rc;
+        if (mg == 1) rc = launch_gemv<FmtQ4K, 1, true, 1, true, 2>(W, nullptr, Xg, Yg, mg, N, K, s, status, dev, flags);
+        else if (mg == 2) rc = launch_gemv<FmtQ4K, 2, true, 1, true, 2>(W, nullptr, Xg, Yg, mg, N, K, s, status, dev, flags);
+        else if (mg <= 4) rc = launch_gemv<FmtQ4K, 4, true, 1, true, 1>(W, nullptr, Xg, Yg, mg, N, K, s, status, dev, flags);
+        else rc = launch_gemv<FmtQ4K, 8, false, 1, true, 1>(W, nullptr, Xg, Yg, mg, N, K, s, status, dev, flags);
+        if (rc != QG_OK) return rc;
+    }
+    return QG_OK;
+}
+
+}  // namespace qg

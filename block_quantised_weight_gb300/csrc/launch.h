@@ -9,9 +9,9 @@
 namespace qg {
 
 int launch_gemv_q4k(const uint8_t* W, const float* X, float* Y, int M, int64_t N, int64_t K, cudaStream_t s,
-                    unsigned* status);
+                    unsigned* status, unsigned flags);
 int launch_gemv_iq3(const uint8_t* W, const uint8_t* grid, const float* X, float* Y, int M, int64_t N, int64_t K,
-                    cudaStream_t s, unsigned* status);
+                    cudaStream_t s, unsigned* status, unsigned flags);
 int launch_dequant_q4k(const uint8_t* W, float* out, int64_t N, int64_t K, cudaStream_t s);
 int launch_dequant_iq3(const uint8_t* W, const uint8_t* grid, float* out, int64_t N, int64_t K, cudaStream_t s);
 // tcgen05 bf16 path, 16 <= M <= 32

@@ -1,0 +1,69 @@
+// Host-side helpers shared by the GEMV launchers.
+#pragma once
+#include <algorithm>
+
+#include "gemv_kernel.cuh"
+#include "launch.h"
+
+namespace qg {
+
+inline int current_device() {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return -1;
+    return dev;
+}
+
+inline int sm_count(int dev) {
+    static int cache[64];
+    if (dev < 0 || dev >= 64) return 0;
+    if (cache[dev] == 0) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+        cache[dev] = n;
+    }
+    return cache[dev];
+}
+
+// Launch gemv_kernel<F, MT, XS, RG, PACKED, MINB>: MINB CTAs per SM, as many
+// pipeline stages as fit in the per-CTA share of shared memory.
+template <class F, int MT, bool XS, int RG, bool PACKED, int MINB, int CVT = 0>
+int launch_gemv(const uint8_t* W, const uint8_t* grid, const float* X, float* Y, int M, int64_t N, int64_t K,
+                cudaStream_t s, unsigned* status, int dev, unsigned flags) {
+    static bool attr_done[64];
+    const int budget = std::min(kSmemPerCTA, kSmemPerSM / MINB - kSmemReserve);
+    const Layout L1 = make_layout(F::kIQ3, MT, XS, RG, 1, F::kRowStride);
+    const int stages = std::min(kMaxStages, (budget - L1.stage0) / L1.stage_bytes);
+    if (stages < 2) return QG_EINVAL;
+    const Layout L = make_layout(F::kIQ3, MT, XS, RG, stages, F::kRowStride);
+    auto kern = gemv_kernel<F, MT, XS, RG, PACKED, MINB, CVT>;
+    if (!attr_done[dev]) {
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L.total) != cudaSuccess)
+            return QG_ECUDA;
+        attr_done[dev] = true;
+    }
+    const int64_t ntiles = (N + RG * kRows - 1) / (RG * kRows);
+    const int sms = sm_count(dev);
+    if (sms <= 0) return QG_ECUDA;
+    const int grid_x = static_cast<int>(std::min<int64_t>(ntiles, static_cast<int64_t>(sms) * MINB));
+    const int kflags = (flags & QG_PREFETCH_WEIGHTS) ? kFlagPrefetchWeights : 0;
+    if (!(flags & QG_PREFETCH_WEIGHTS)) {
+        kern<<<grid_x, RG * kCols * 32 + 32, L.total, s>>>(W, grid, X, Y, M, N, K, stages, status, kflags);
+        return cudaGetLastError() == cudaSuccess ? QG_OK : QG_ECUDA;
+    }
+    // programmatic dependent launch: this grid may start before the previous
+    // kernel in the stream finishes; the kernel waits before reading x.
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid_x);
+    cfg.blockDim = dim3(RG * kCols * 32 + 32);
+    cfg.dynamicSmemBytes = L.total;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, kern, W, grid, X, Y, M, N, K, stages, status, kflags) != cudaSuccess) return QG_ECUDA;
+    return cudaGetLastError() == cudaSuccess ? QG_OK : QG_ECUDA;
+}
+
+}  // namespace qg

@@ -26,7 +26,9 @@ QG_EBOUNDS = -5
 QG_EALIAS = -6
 QG_MAX_M = 32
 
-EXPORTS = ("qgemv_q4k", "qgemv_iq3", "qgemm_q4k_batched", "qdequant_q4k", "qdequant_iq3",
+QG_PREFETCH_WEIGHTS = 1
+
+EXPORTS = ("qgemv_q4k", "qgemv_q4k_ex", "qgemv_iq3", "qgemv_iq3_ex", "qgemm_q4k_batched", "qdequant_q4k", "qdequant_iq3",
            "qg_device_status", "qg_test_bounded_wait", "qg_strerror")
 
 
@@ -53,7 +55,9 @@ def load():
         vp, i64, ci = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
         sigs = {
             "qgemv_q4k": [vp, vp, vp, ci, i64, i64, vp],
+            "qgemv_q4k_ex": [vp, vp, vp, ci, i64, i64, ctypes.c_uint, vp],
             "qgemv_iq3": [vp, vp, vp, vp, ci, i64, i64, vp],
+            "qgemv_iq3_ex": [vp, vp, vp, vp, ci, i64, i64, ctypes.c_uint, vp],
             "qgemm_q4k_batched": [vp, vp, vp, ci, i64, i64, vp],
             "qdequant_q4k": [vp, vp, i64, i64, vp],
             "qdequant_iq3": [vp, vp, vp, i64, i64, vp],
@@ -120,22 +124,29 @@ def _xy(W, X, out, block_bytes):
     return X, out, M, N, K
 
 
-def qgemv_q4k(W, X, out=None, stream=None):
-    """Y[M, N] = X[M, K] @ dequant(W)^T for a Q4_K matrix W (uint8, N*K/256*144 bytes)."""
+def qgemv_q4k(W, X, out=None, stream=None, flags=0):
+    """Y[M, N] = X[M, K] @ dequant(W)^T for a Q4_K matrix W (uint8, N*K/256*144 bytes).
+
+    flags=QG_PREFETCH_WEIGHTS calls qgemv_q4k_ex (programmatic dependent launch)."""
     X, out, M, N, K = _xy(W, X, out, 144)
-    _check("qgemv_q4k", load().qgemv_q4k(W.data_ptr(), X.data_ptr(), out.data_ptr(), M, N, K, _stream(stream)))
+    if flags:
+        rc = load().qgemv_q4k_ex(W.data_ptr(), X.data_ptr(), out.data_ptr(), M, N, K, flags, _stream(stream))
+        _check("qgemv_q4k_ex", rc)
+    else:
+        _check("qgemv_q4k", load().qgemv_q4k(W.data_ptr(), X.data_ptr(), out.data_ptr(), M, N, K, _stream(stream)))
     return out
 
 
-def qgemv_iq3(W, grid, X, out=None, stream=None):
+def qgemv_iq3(W, grid, X, out=None, stream=None, flags=0):
     """Y[M, N] = X @ dequant(W)^T for an IQ3 matrix W with codebook grid (uint8 [256, 4], doubled units)."""
     import torch
     _req(grid, torch.uint8, "grid")
     if grid.numel() != 1024:
         raise ValueError("grid must hold 256 x 4 bytes")
     X, out, M, N, K = _xy(W, X, out, 98)
-    _check("qgemv_iq3", load().qgemv_iq3(W.data_ptr(), grid.data_ptr(), X.data_ptr(), out.data_ptr(), M, N, K,
-                                         _stream(stream)))
+    rc = load().qgemv_iq3_ex(W.data_ptr(), grid.data_ptr(), X.data_ptr(), out.data_ptr(), M, N, K, flags,
+                             _stream(stream))
+    _check("qgemv_iq3_ex" if flags else "qgemv_iq3", rc)
     return out
 
 

@@ -57,6 +57,15 @@ extern "C" {
 
 #define QG_MAX_M 32
 
+/* Launch flag for the *_ex entry points.  QG_PREFETCH_WEIGHTS promises that W
+ * (and the IQ3 grid) are not written by the kernel that precedes this call in
+ * the stream.  The GEMV is then launched as a programmatic dependent launch:
+ * it may start while the preceding kernel is still running and stream its
+ * first weight tiles, and it waits for the preceding kernel to complete (all
+ * its memory visible) before it reads X or writes Y.  Without the flag the
+ * call is ordinary stream-ordered work. */
+#define QG_PREFETCH_WEIGHTS 1u
+
 #if defined(__GNUC__)
 #define QG_API __attribute__((visibility("default")))
 #else
@@ -72,6 +81,11 @@ extern "C" {
  * group streaming W once. */
 QG_API int qgemv_q4k(const uint8_t* W, const float* X, float* Y, int M, int64_t N, int64_t K, cudaStream_t stream);
 
+/* qgemv_q4k with launch flags (0 or QG_PREFETCH_WEIGHTS); other flag bits:
+ * QG_EINVAL. */
+QG_API int qgemv_q4k_ex(const uint8_t* W, const float* X, float* Y, int M, int64_t N, int64_t K, unsigned flags,
+                        cudaStream_t stream);
+
 /* IQ3 (98-byte super-block) GEMV, fp32 FMA path, 1 <= M <= 32.
  * Page 4 "iq3_pack.py", module docstring and decode (format); page 1
  * model_forward's matmul (operation).
@@ -81,6 +95,10 @@ QG_API int qgemv_q4k(const uint8_t* W, const float* X, float* Y, int M, int64_t 
  * byte-addressed path with identical results. */
 QG_API int qgemv_iq3(const uint8_t* W, const uint8_t* grid, const float* X, float* Y, int M, int64_t N, int64_t K,
               cudaStream_t stream);
+
+/* qgemv_iq3 with launch flags (0 or QG_PREFETCH_WEIGHTS). */
+QG_API int qgemv_iq3_ex(const uint8_t* W, const uint8_t* grid, const float* X, float* Y, int M, int64_t N, int64_t K,
+                        unsigned flags, cudaStream_t stream);
 
 /* Batched Q4_K GEMM for decode batches, 1 <= M <= 32.
  * Same operation and layouts as qgemv_q4k.  M < 16 runs the fp32 FMA path

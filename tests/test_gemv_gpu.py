@@ -214,3 +214,53 @@ def test_binding_raises_on_bad_arguments(q):
     y = torch.empty((1, 4), device="cuda")
     rc = q.load().qgemv_q4k(W.data_ptr() + 4, x.data_ptr(), y.data_ptr(), 1, 4, 512, None)
     assert rc == q.QG_EALIGN
+
+
+# ------------------------------------------------------------ dependent launch
+@pytest.mark.parametrize("fmt", ["q4k", "iq3"])
+def test_prefetch_flag_dependency_chain(q, fmt):
+    """x_{i+1} = y_i through six square GEMVs issued back to back on one stream.
+    With QG_PREFETCH_WEIGHTS each launch may start before its predecessor ends;
+    the results must equal the plain stream-ordered launches bit for bit and
+    match the oracle stage by stage."""
+    K = N = 2048
+    mats = []
+    for i in range(6):
+        if fmt == "q4k":
+            mats.append((dev(synth.gen_q4k(N, K, 300 + i)), None))
+        else:
+            W, grid = synth.gen_iq3(N, K, 400 + i)
+            mats.append((dev(W), dev(grid)))
+    x0 = dev(synth.gen_x(1, K, 7))
+
+    def chain(flags):
+        xs = [x0]
+        for W, g in mats:
+            if fmt == "q4k":
+                y = q.qgemv_q4k(W, xs[-1], flags=flags)
+            else:
+                y = q.qgemv_iq3(W, g, xs[-1], flags=flags)
+            xs.append(y / 32.0)   # keep magnitudes bounded (exact scaling)
+        torch.cuda.synchronize()
+        return xs
+
+    plain = chain(0)
+    fast = chain(q.QG_PREFETCH_WEIGHTS)
+    for a, b in zip(plain, fast):
+        assert torch.equal(a, b)
+    for i, (W, g) in enumerate(mats):
+        xin = plain[i].cpu().numpy().reshape(1, K)
+        Wh = W.cpu().numpy()
+        if fmt == "q4k":
+            Y, A = oracle.gemv_q4k(Wh, xin)
+        else:
+            Y, A = oracle.gemv_iq3(Wh, g.cpu().numpy(), xin)
+        check_tol(plain[i + 1].cpu().numpy() * 32.0, Y, A, TAU_FMA, f"chain stage {i}")
+    assert q.qg_device_status() == q.QG_OK
+
+
+def test_prefetch_flag_rejects_unknown_bits(q):
+    W = dev(synth.gen_q4k(4, 512, 0))
+    x = torch.zeros((1, 512), device="cuda")
+    y = torch.empty((1, 4), device="cuda")
+    assert q.load().qgemv_q4k_ex(W.data_ptr(), x.data_ptr(), y.data_ptr(), 1, 4, 512, 6, None) == q.QG_EINVAL
