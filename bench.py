@@ -210,7 +210,9 @@ def run_ours(args, rank, world, local_rank):
             wb = weight_bytes(fmt, K, N)
             algo = wb + 4 * M * K + 4 * M * N
             fl = 0 if args.no_prefetch else qgemv.QG_PREFETCH_WEIGHTS
-            if fmt == "q4k":
+            if fmt == "q4k" and M >= 16:
+                lst.append((lib.qgemm_q4k_batched, (Wd.data_ptr(), xp, yp, M, N, K), wb, algo))
+            elif fmt == "q4k":
                 lst.append((lib.qgemv_q4k_ex, (Wd.data_ptr(), xp, yp, M, N, K, fl), wb, algo))
             else:
                 lst.append((lib.qgemv_iq3_ex, (Wd.data_ptr(), gd.data_ptr(), xp, yp, M, N, K, fl), wb, algo))
@@ -354,7 +356,7 @@ def run_ours(args, rank, world, local_rank):
                 "algorithmic_bytes_per_launch": round(algo / len(durs))}
         by_shape = {}
         for (fn, a, wb, ab), d in zip(flat, durs):
-            key = f"K{a[-2]}xN{a[-3]}"
+            key = f"K{a[5]}xN{a[4]}" if len(a) == 6 else f"K{a[-2]}xN{a[-3]}"
             e = by_shape.setdefault(key, [0, 0.0, 0])
             e[0] += 1
             e[1] += d
