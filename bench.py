@@ -45,7 +45,7 @@ def workload_spec(name: str, M: int):
     from block_quantised_weight_gb300 import synth
     if name == "tinyllama":
         mats = [("q4k", K, N) for (_l, _n, K, N) in synth.tinyllama_shapes()]
-        return mats, "TinyLlama-1.1B-shaped Q4_K decode weight pass (155 GEMVs)", 1
+        return mats, "TinyLlama-1.1B-shaped Q4_K decode weight pass, M=1 (155 GEMVs, 581,861,376 weight bytes)", 1
     table = {
         "q4k_c0": ("q4k", 2048, 2048), "iq3_c2": ("iq3", 4096, 14336), "q4k_c3": ("q4k", 4096, 11008),
         "q4k_c4a": ("q4k", 8192, 28672), "q4k_c4b": ("q4k", 28672, 8192),
@@ -53,6 +53,19 @@ def workload_spec(name: str, M: int):
     }
     fmt, K, N = table[name]
     return [(fmt, K, N)], f"{fmt.upper()} GEMV K={K} N={N} M={M}", M
+
+
+def pass_groups(name, n, single):
+    """Index groups launched together.  TinyLlama pass: per layer (q, k, v),
+    (o), (gate, up), (down), then (output): 89 launches for 155 GEMVs."""
+    if name != "tinyllama" or single:
+        return [[i] for i in range(n)]
+    groups = []
+    for l in range(22):
+        b = 7 * l
+        groups += [[b, b + 1, b + 2], [b + 3], [b + 4, b + 5], [b + 6]]
+    groups.append([154])
+    return groups
 
 
 def weight_bytes(fmt, K, N):
@@ -191,33 +204,56 @@ def run_ours(args, rank, world, local_rank):
     if step_wbytes < 2 * l2:
         copies = int(np.ceil(2 * l2 / step_wbytes)) + 1
 
+    # launch groups: in the decode pass q/k/v read one activation vector and
+    # gate/up another, so each such set is one grouped launch (--single: one
+    # launch per matrix)
+    groups = pass_groups(args.workload, len(host), args.single)
     # device buffers: weights (rotated copies), x / y concatenated per pass
-    xs_host = np.concatenate([h[5].reshape(-1) for h in host]).astype(np.float32)
+    xs_host = np.concatenate([host[g[0]][5].reshape(-1) for g in groups]).astype(np.float32)
     ys_len = sum(M * h[2] for h in host)
     x_dev = torch.from_numpy(xs_host).to(dev)
     y_dev = torch.empty(ys_len, dtype=torch.float32, device=dev)
-    launches = []   # per copy: list of (fn, args, wbytes, algo_bytes)
+    launches = []   # per copy: list of (fn, args, wbytes, algo_bytes, label)
     keep = []
+    fl = 0 if args.no_prefetch else qgemv.QG_PREFETCH_WEIGHTS
     for c in range(copies):
         xo, yo = 0, 0
         lst = []
-        for fmt, K, N, W, grid, x in host:
-            Wd = torch.from_numpy(W).to(dev)
-            gd = torch.from_numpy(grid).to(dev) if grid is not None else None
-            keep.append((Wd, gd))
+        for grp in groups:
+            fmt, K = host[grp[0]][0], host[grp[0]][1]
             xp = x_dev.data_ptr() + 4 * xo
-            yp = y_dev.data_ptr() + 4 * yo
-            wb = weight_bytes(fmt, K, N)
-            algo = wb + 4 * M * K + 4 * M * N
-            fl = 0 if args.no_prefetch else qgemv.QG_PREFETCH_WEIGHTS
-            if fmt == "q4k" and M >= 16:
-                lst.append((lib.qgemm_q4k_batched, (Wd.data_ptr(), xp, yp, M, N, K), wb, algo))
+            Wp, Yp, Ns, gd = [], [], [], None
+            for i in grp:
+                _f, _K, N, W, grid, _x = host[i]
+                Wd = torch.from_numpy(W).to(dev)
+                keep.append(Wd)
+                if grid is not None:
+                    gd = torch.from_numpy(grid).to(dev)
+                    keep.append(gd)
+                Wp.append(Wd.data_ptr())
+                Yp.append(y_dev.data_ptr() + 4 * yo)
+                Ns.append(N)
+                yo += M * N
+            wb = sum(weight_bytes(fmt, K, N) for N in Ns)
+            algo = wb + 4 * M * K + 4 * M * sum(Ns)
+            label = f"K{K}xN" + "+".join(str(n) for n in Ns)
+            if len(grp) > 1:
+                Wa = (ctypes.c_void_p * len(grp))(*Wp)
+                Ya = (ctypes.c_void_p * len(grp))(*Yp)
+                Na = (ctypes.c_int64 * len(grp))(*Ns)
+                keep.append((Wa, Ya, Na))
+                if fmt == "q4k":
+                    lst.append((lib.qgemv_q4k_group, (Wa, Ya, Na, len(grp), xp, M, K, fl), wb, algo, label))
+                else:
+                    lst.append((lib.qgemv_iq3_group, (Wa, Ya, Na, len(grp), gd.data_ptr(), xp, M, K, fl), wb, algo,
+                                label))
+            elif fmt == "q4k" and M >= 16:
+                lst.append((lib.qgemm_q4k_batched, (Wp[0], xp, Yp[0], M, Ns[0], K), wb, algo, label))
             elif fmt == "q4k":
-                lst.append((lib.qgemv_q4k_ex, (Wd.data_ptr(), xp, yp, M, N, K, fl), wb, algo))
+                lst.append((lib.qgemv_q4k_ex, (Wp[0], xp, Yp[0], M, Ns[0], K, fl), wb, algo, label))
             else:
-                lst.append((lib.qgemv_iq3_ex, (Wd.data_ptr(), gd.data_ptr(), xp, yp, M, N, K, fl), wb, algo))
+                lst.append((lib.qgemv_iq3_ex, (Wp[0], gd.data_ptr(), xp, Yp[0], M, Ns[0], K, fl), wb, algo, label))
             xo += M * K
-            yo += M * N
         launches.append(lst)
     flat = [l for lst in launches for l in lst]
 
@@ -225,7 +261,7 @@ def run_ours(args, rank, world, local_rank):
     sh = ctypes.c_void_p(stream.cuda_stream)
 
     def run_pass(lst):
-        for fn, a, _wb, _ab in lst:
+        for fn, a, _wb, _ab, _lb in lst:
             rc = fn(*a, sh)
             if rc != 0:
                 raise RuntimeError(f"launch failed: {rc} {qgemv.strerror(rc)}")
@@ -251,7 +287,7 @@ def run_ours(args, rank, world, local_rank):
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g, stream=stream):
         cap = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
-        for fn, a, _wb, _ab in flat:
+        for fn, a, _wb, _ab, _lb in flat:
             rc = fn(*a, cap)
             if rc != 0:
                 raise RuntimeError(f"capture launch failed: {rc}")
@@ -259,7 +295,7 @@ def run_ours(args, rank, world, local_rank):
     if per_launch_ok:
         with torch.cuda.graph(gi, stream=stream):
             cap = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
-            for i, (fn, a, _wb, _ab) in enumerate(flat):
+            for i, (fn, a, _wb, _ab, _lb) in enumerate(flat):
                 if per_launch_ok:
                     per_launch_ok = rt.cudaEventRecordWithFlags(ctypes.c_void_p(ev[i][0].cuda_event), cap, 1) == 0
                 rc = fn(*a, cap)
@@ -343,7 +379,7 @@ def run_ours(args, rank, world, local_rank):
     peak, peak_kind = measured_peaks()
     roof = None
     if durs:
-        algo = sum(ab for _f, _a, _wb, ab in flat)
+        algo = sum(ab for _f, _a, _wb, ab, _lb in flat)
         kern_ms = sum(durs)
         achieved = algo / (kern_ms * 1e-3) / 1e9
         roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
@@ -355,8 +391,7 @@ def run_ours(args, rank, world, local_rank):
                              "the timed region (launches serialised there)",
                 "algorithmic_bytes_per_launch": round(algo / len(durs))}
         by_shape = {}
-        for (fn, a, wb, ab), d in zip(flat, durs):
-            key = f"K{a[5]}xN{a[4]}" if len(a) == 6 else f"K{a[-2]}xN{a[-3]}"
+        for (fn, a, wb, ab, key), d in zip(flat, durs):
             e = by_shape.setdefault(key, [0, 0.0, 0])
             e[0] += 1
             e[1] += d
@@ -368,6 +403,7 @@ def run_ours(args, rank, world, local_rank):
         "warmup": args.warmup, "ms_per_step": round(ms_step, 4), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32", "data": "synthetic (seeded numpy; shapes of the pages' models)",
         "config": {"workload": desc, "M": M, "weight_bytes_per_step": step_wbytes,
+                   "launches_per_step": len(flat) // copies,
                    "l2": ("inputs larger than L2" if copies == 1 else
                           f"rotates {copies} weight copies (> 2x L2)"),
                    "graph": "CUDA graph of the step, replayed", "parallelism": f"replicas x{world}",
@@ -379,7 +415,7 @@ def run_ours(args, rank, world, local_rank):
         "e2e": {"value": round(e2e_value, 1), "unit": "GB/s", "h2d_bytes_per_step": int(xs_host.nbytes),
                 "d2h_bytes_per_step": int(4 * ys_len),
                 "note": "pinned host x -> device, graph of C-ABI launches, device y -> pinned host, every step"},
-        "gpu_launches": len(flat) * args.steps,
+        "gpu_launches": len(flat) * args.steps * (1 if M <= 8 or M >= 16 else (M + 7) // 8),
         "roofline": roof,
         "clocks": clocks,
     }
@@ -455,6 +491,7 @@ def main():
     ap.add_argument("--M", type=int, default=1)
     ap.add_argument("--cpu-baseline-s", type=float, default=12.0)
     ap.add_argument("--no-prefetch", action="store_true", help="plain stream-ordered launches")
+    ap.add_argument("--single", action="store_true", help="one launch per matrix (no q/k/v, gate/up groups)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

@@ -103,6 +103,45 @@ int qgemv_iq3(const uint8_t* W, const uint8_t* grid, const float* X, float* Y, i
     return qgemv_iq3_ex(W, grid, X, Y, M, N, K, 0u, stream);
 }
 
+// Group checks: every matrix as a single GEMV, plus no Y[i] overlapping any
+// other matrix's W or Y.
+static int check_group(const uint8_t* const* W, float* const* Y, const int64_t* N, int count, const uint8_t* grid,
+                bool need_grid, const float* X, int M, int64_t K, int block_bytes) {
+    if (!W || !Y || !N || count < 1 || count > QG_MAX_GROUP) return QG_EINVAL;
+    for (int i = 0; i < count; ++i) {
+        const int rc = check_gemv(W[i], grid, need_grid, X, Y[i], M, N[i], K, block_bytes);
+        if (rc != QG_OK) return rc;
+    }
+    for (int i = 0; i < count; ++i)
+        for (int j = 0; j < count; ++j) {
+            if (i == j) continue;
+            if (overlap(Y[i], int64_t(M) * N[i] * 4, W[j], N[j] * (K / 256) * block_bytes) ||
+                overlap(Y[i], int64_t(M) * N[i] * 4, Y[j], int64_t(M) * N[j] * 4))
+                return QG_EALIAS;
+        }
+    return QG_OK;
+}
+
+int qgemv_q4k_group(const uint8_t* const* W, float* const* Y, const int64_t* N, int count, const float* X, int M,
+                    int64_t K, unsigned flags, cudaStream_t stream) {
+    if (flags & ~static_cast<unsigned>(QG_PREFETCH_WEIGHTS)) return QG_EINVAL;
+    int rc = check_group(W, Y, N, count, nullptr, false, X, M, K, 144);
+    if (rc != QG_OK) return rc;
+    unsigned* st = status_ptr();
+    if (!st) return QG_ECUDA;
+    return qg::launch_group_q4k(W, Y, N, count, X, M, K, stream, st, flags);
+}
+
+int qgemv_iq3_group(const uint8_t* const* W, float* const* Y, const int64_t* N, int count, const uint8_t* grid,
+                    const float* X, int M, int64_t K, unsigned flags, cudaStream_t stream) {
+    if (flags & ~static_cast<unsigned>(QG_PREFETCH_WEIGHTS)) return QG_EINVAL;
+    int rc = check_group(W, Y, N, count, grid, true, X, M, K, 98);
+    if (rc != QG_OK) return rc;
+    unsigned* st = status_ptr();
+    if (!st) return QG_ECUDA;
+    return qg::launch_group_iq3(W, Y, N, count, grid, X, M, K, stream, st, flags);
+}
+
 int qgemm_q4k_batched(const uint8_t* W, const float* X, float* Y, int M, int64_t N, int64_t K, cudaStream_t stream) {
     int rc = check_gemv(W, nullptr, false, X, Y, M, N, K, 144);
     if (rc != QG_OK) return rc;

@@ -58,34 +58,41 @@ __global__ void __launch_bounds__(256)
     }
 }
 
-int launch_gemv_iq3(const uint8_t* W, const uint8_t* grid, const float* X, float* Y, int M, int64_t N, int64_t K,
-                    cudaStream_t s, unsigned* status, unsigned flags) {
+int launch_group_iq3(const uint8_t* const* W, float* const* Y, const int64_t* N, int count, const uint8_t* grid,
+                     const float* X, int M, int64_t K, cudaStream_t s, unsigned* status, unsigned flags) {
     const int dev = current_device();
     if (dev < 0) return QG_ECUDA;
     const bool aligned = (K / 256) % 8 == 0;
     for (int m0 = 0; m0 < M; m0 += 8) {
         const int mg = std::min(8, M - m0);
         const float* Xg = X + static_cast<int64_t>(m0) * K;
-        float* Yg = Y + static_cast<int64_t>(m0) * N;
-        int rc;
+        int rc = QG_OK;
         if (!aligned) {
             const int sms = sm_count(dev);
             if (sms <= 0) return QG_ECUDA;
-            const int64_t blocks = std::min<int64_t>((N + 7) / 8, static_cast<int64_t>(sms) * 8);
-            gemv_iq3_bytes_kernel<<<static_cast<int>(blocks), 256, 0, s>>>(W, grid, Xg, Yg, mg, N, K);
-            rc = cudaGetLastError() == cudaSuccess ? QG_OK : QG_ECUDA;
+            for (int i = 0; i < count && rc == QG_OK; ++i) {
+                const int64_t blocks = std::min<int64_t>((N[i] + 7) / 8, static_cast<int64_t>(sms) * 8);
+                gemv_iq3_bytes_kernel<<<static_cast<int>(blocks), 256, 0, s>>>(W[i], grid, Xg, Y[i] + m0 * N[i], mg,
+                                                                                N[i], K);
+                rc = cudaGetLastError() == cudaSuccess ? QG_OK : QG_ECUDA;
+            }
         } else if (mg == 1) {
-            rc = launch_gemv<FmtIQ3, 1, true, 2, true, 1>(W, grid, Xg, Yg, mg, N, K, s, status, dev, flags);
+            rc = launch_gemv<FmtIQ3, 1, true, 2, true, 1>(W, Y, N, count, m0, grid, Xg, mg, K, s, status, dev, flags);
         } else if (mg == 2) {
-            rc = launch_gemv<FmtIQ3, 2, true, 2, true, 1>(W, grid, Xg, Yg, mg, N, K, s, status, dev, flags);
+            rc = launch_gemv<FmtIQ3, 2, true, 2, true, 1>(W, Y, N, count, m0, grid, Xg, mg, K, s, status, dev, flags);
         } else if (mg <= 4) {
-            rc = launch_gemv<FmtIQ3, 4, false, 1, true, 1>(W, grid, Xg, Yg, mg, N, K, s, status, dev, flags);
+            rc = launch_gemv<FmtIQ3, 4, false, 1, true, 1>(W, Y, N, count, m0, grid, Xg, mg, K, s, status, dev, flags);
         } else {
-            rc = launch_gemv<FmtIQ3, 8, false, 1, true, 1>(W, grid, Xg, Yg, mg, N, K, s, status, dev, flags);
+            rc = launch_gemv<FmtIQ3, 8, false, 1, true, 1>(W, Y, N, count, m0, grid, Xg, mg, K, s, status, dev, flags);
         }
         if (rc != QG_OK) return rc;
     }
     return QG_OK;
+}
+
+int launch_gemv_iq3(const uint8_t* W, const uint8_t* grid, const float* X, float* Y, int M, int64_t N, int64_t K,
+                    cudaStream_t s, unsigned* status, unsigned flags) {
+    return launch_group_iq3(&W, &Y, &N, 1, grid, X, M, K, s, status, flags);
 }
 
 }  // namespace qg

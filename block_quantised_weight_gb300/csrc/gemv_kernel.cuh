@@ -64,6 +64,27 @@ struct Layout {
     int full, empty, sx, red, table, stage0, stage_bytes, xoff, total;
 };
 
+// Up to kMaxGroup matrices that share X and K, processed by one launch.
+// Tiles are numbered across the group: matrix i owns tiles
+// [tile0[i], tile0[i+1]).
+constexpr int kMaxGroup = 4;
+struct Group {
+    const uint8_t* W[kMaxGroup];
+    float* Y[kMaxGroup];
+    int64_t N[kMaxGroup];
+    int64_t tile0[kMaxGroup + 1];
+    int count;
+};
+
+// Matrix that owns global tile `tile`.
+__device__ __forceinline__ int group_find(const Group& G, int64_t tile) {
+    int i = 0;
+#pragma unroll
+    for (int k = 1; k < kMaxGroup; ++k)
+        if (k < G.count && tile >= G.tile0[k]) i = k;
+    return i;
+}
+
 // Dynamic smem layout of gemv_kernel<F, MT, XS, RG> with `stages` stages.
 __host__ __device__ inline Layout make_layout(bool iq3, int MT, bool xs, int RG, int stages, int row_stride) {
     Layout L;
@@ -315,15 +336,15 @@ __device__ __forceinline__ void named_barrier_sync(int id) {
 // Threads: RG*8 consumer warps, then one producer warp.
 template <class F, int MT, bool XS, int RG, bool PACKED, int MINB, int CVT = 0>
 __global__ void __launch_bounds__(RG * kCols * 32 + 32, MINB)
-    gemv_kernel(const uint8_t* __restrict__ W, const uint8_t* __restrict__ grid, const float* __restrict__ X,
-                float* __restrict__ Y, int M, int64_t N, int64_t K, int stages, unsigned* status, int flags) {
+    gemv_kernel(const __grid_constant__ Group G, const uint8_t* __restrict__ grid, const float* __restrict__ X, int M,
+                int64_t K, int stages, unsigned* status, int flags) {
     constexpr int kWarps = RG * kCols;          // consumer warps
     constexpr int kConsumerThreads = kWarps * 32;
     constexpr int kTileRows = RG * kRows;
     extern __shared__ __align__(128) uint8_t smem[];
     const int nb = static_cast<int>(K / 256);
     const int nchunks = (nb + kCols - 1) / kCols;
-    const int64_t ntiles = (N + kTileRows - 1) / kTileRows;
+    const int64_t ntiles = G.tile0[G.count];
     const Layout L = make_layout(F::kIQ3, MT, XS, RG, stages, F::kRowStride);
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.full);
     uint64_t* empty = reinterpret_cast<uint64_t*>(smem + L.empty);
@@ -373,8 +394,9 @@ __global__ void __launch_bounds__(RG * kCols * 32 + 32, MINB)
             const int s = static_cast<int>(u % stages);
             const int c = static_cast<int>(u % nchunks);
             const int64_t tile = blockIdx.x + (u / nchunks) * gridDim.x;
-            const int64_t row0 = tile * kTileRows;
-            const int rows = static_cast<int>(min64(kTileRows, N - row0));
+            const int gi = group_find(G, tile);
+            const int64_t row0 = (tile - G.tile0[gi]) * kTileRows;
+            const int rows = static_cast<int>(min64(kTileRows, G.N[gi] - row0));
             const int kc = min(kCols, nb - c * kCols);
             uint8_t* st = smem + L.stage0 + s * L.stage_bytes;
             if (expect) {
@@ -383,7 +405,7 @@ __global__ void __launch_bounds__(RG * kCols * 32 + 32, MINB)
                 __syncwarp();
             }
             if (do_w) {
-                const uint8_t* src = W + row0 * pitch + static_cast<int64_t>(c) * kCols * F::kBytes;
+                const uint8_t* src = G.W[gi] + row0 * pitch + static_cast<int64_t>(c) * kCols * F::kBytes;
                 for (int r = lane; r < rows; r += 32)
                     bulk_g2s(st + r * F::kRowStride, src + r * pitch, kc * F::kBytes, &full[s], pol_w);
             }
@@ -421,8 +443,10 @@ __global__ void __launch_bounds__(RG * kCols * 32 + 32, MINB)
         const int s = static_cast<int>(u % stages);
         const int c = static_cast<int>(u % nchunks);
         const int64_t tile = blockIdx.x + (u / nchunks) * gridDim.x;
-        const int64_t row0 = tile * kTileRows;
-        const int rows = static_cast<int>(min64(kTileRows, N - row0));
+        const int gi = group_find(G, tile);
+        const int64_t row0 = (tile - G.tile0[gi]) * kTileRows;
+        const int64_t Ni = G.N[gi];
+        const int rows = static_cast<int>(min64(kTileRows, Ni - row0));
         const int kc = min(kCols, nb - c * kCols);
         const uint8_t* st = smem + L.stage0 + s * L.stage_bytes;
         const int r = rg * kRows + lane;  // row within the tile
@@ -486,7 +510,7 @@ __global__ void __launch_bounds__(RG * kCols * 32 + 32, MINB)
                     float sum = 0.f;
 #pragma unroll
                     for (int w = 0; w < kCols; ++w) sum += rb[((g * kCols + w) * MT + m) * kRows + ln];
-                    Y[m * N + row0 + rr] = sum;
+                    G.Y[gi][m * Ni + row0 + rr] = sum;
                 }
             }
             ++tile_count;

@@ -3,23 +3,32 @@
 
 namespace qg {
 
-// M is split into groups of at most 8 tokens; each group streams W once.
-int launch_gemv_q4k(const uint8_t* W, const float* X, float* Y, int M, int64_t N, int64_t K, cudaStream_t s,
-                    unsigned* status, unsigned flags) {
+// count matrices sharing X; M is split into groups of at most 8 tokens, each
+// group streaming W once.
+int launch_group_q4k(const uint8_t* const* W, float* const* Y, const int64_t* N, int count, const float* X, int M,
+                     int64_t K, cudaStream_t s, unsigned* status, unsigned flags) {
     const int dev = current_device();
     if (dev < 0) return QG_ECUDA;
     for (int m0 = 0; m0 < M; m0 += 8) {
         const int mg = std::min(8, M - m0);
         const float* Xg = X + static_cast<int64_t>(m0) * K;
-        float* Yg = Y + static_cast<int64_t>(m0) * N;
         int rc;
-        if (mg == 1) rc = launch_gemv<FmtQ4K, 1, true, 1, true, 2>(W, nullptr, Xg, Yg, mg, N, K, s, status, dev, flags);
-        else if (mg == 2) rc = launch_gemv<FmtQ4K, 2, true, 1, true, 2>(W, nullptr, Xg, Yg, mg, N, K, s, status, dev, flags);
-        else if (mg <= 4) rc = launch_gemv<FmtQ4K, 4, true, 1, true, 1>(W, nullptr, Xg, Yg, mg, N, K, s, status, dev, flags);
-        else rc = launch_gemv<FmtQ4K, 8, false, 1, true, 1>(W, nullptr, Xg, Yg, mg, N, K, s, status, dev, flags);
+        if (mg == 1)
+            rc = launch_gemv<FmtQ4K, 1, true, 1, true, 2>(W, Y, N, count, m0, nullptr, Xg, mg, K, s, status, dev, flags);
+        else if (mg == 2)
+            rc = launch_gemv<FmtQ4K, 2, true, 1, true, 2>(W, Y, N, count, m0, nullptr, Xg, mg, K, s, status, dev, flags);
+        else if (mg <= 4)
+            rc = launch_gemv<FmtQ4K, 4, true, 1, true, 1>(W, Y, N, count, m0, nullptr, Xg, mg, K, s, status, dev, flags);
+        else
+            rc = launch_gemv<FmtQ4K, 8, false, 1, true, 1>(W, Y, N, count, m0, nullptr, Xg, mg, K, s, status, dev, flags);
         if (rc != QG_OK) return rc;
     }
     return QG_OK;
+}
+
+int launch_gemv_q4k(const uint8_t* W, const float* X, float* Y, int M, int64_t N, int64_t K, cudaStream_t s,
+                    unsigned* status, unsigned flags) {
+    return launch_group_q4k(&W, &Y, &N, 1, X, M, K, s, status, flags);
 }
 
 }  // namespace qg

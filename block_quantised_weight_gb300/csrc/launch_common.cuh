@@ -24,11 +24,13 @@ inline int sm_count(int dev) {
     return cache[dev];
 }
 
-// Launch gemv_kernel<F, MT, XS, RG, PACKED, MINB>: MINB CTAs per SM, as many
-// pipeline stages as fit in the per-CTA share of shared memory.
+// Launch gemv_kernel<F, MT, XS, RG, PACKED, MINB> over `count` matrices that
+// share X (token offset m0 already applied to X; Y[i] + m0*N[i] here): MINB
+// CTAs per SM, as many pipeline stages as fit in the per-CTA share of shared
+// memory.
 template <class F, int MT, bool XS, int RG, bool PACKED, int MINB, int CVT = 0>
-int launch_gemv(const uint8_t* W, const uint8_t* grid, const float* X, float* Y, int M, int64_t N, int64_t K,
-                cudaStream_t s, unsigned* status, int dev, unsigned flags) {
+int launch_gemv(const uint8_t* const* W, float* const* Y, const int64_t* N, int count, int m0, const uint8_t* grid,
+                const float* X, int M, int64_t K, cudaStream_t s, unsigned* status, int dev, unsigned flags) {
     static bool attr_done[64];
     const int budget = std::min(kSmemPerCTA, kSmemPerSM / MINB - kSmemReserve);
     const Layout L1 = make_layout(F::kIQ3, MT, XS, RG, 1, F::kRowStride);
@@ -41,13 +43,22 @@ int launch_gemv(const uint8_t* W, const uint8_t* grid, const float* X, float* Y,
             return QG_ECUDA;
         attr_done[dev] = true;
     }
-    const int64_t ntiles = (N + RG * kRows - 1) / (RG * kRows);
+    Group G = {};
+    G.count = count;
+    G.tile0[0] = 0;
+    for (int i = 0; i < count; ++i) {
+        G.W[i] = W[i];
+        G.Y[i] = Y[i] + static_cast<int64_t>(m0) * N[i];
+        G.N[i] = N[i];
+        G.tile0[i + 1] = G.tile0[i] + (N[i] + RG * kRows - 1) / (RG * kRows);
+    }
+    const int64_t ntiles = G.tile0[count];
     const int sms = sm_count(dev);
     if (sms <= 0) return QG_ECUDA;
     const int grid_x = static_cast<int>(std::min<int64_t>(ntiles, static_cast<int64_t>(sms) * MINB));
     const int kflags = (flags & QG_PREFETCH_WEIGHTS) ? kFlagPrefetchWeights : 0;
     if (!(flags & QG_PREFETCH_WEIGHTS)) {
-        kern<<<grid_x, RG * kCols * 32 + 32, L.total, s>>>(W, grid, X, Y, M, N, K, stages, status, kflags);
+        kern<<<grid_x, RG * kCols * 32 + 32, L.total, s>>>(G, grid, X, M, K, stages, status, kflags);
         return cudaGetLastError() == cudaSuccess ? QG_OK : QG_ECUDA;
     }
     // programmatic dependent launch: this grid may start before the previous
@@ -62,7 +73,7 @@ int launch_gemv(const uint8_t* W, const uint8_t* grid, const float* X, float* Y,
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if (cudaLaunchKernelEx(&cfg, kern, W, grid, X, Y, M, N, K, stages, status, kflags) != cudaSuccess) return QG_ECUDA;
+    if (cudaLaunchKernelEx(&cfg, kern, G, grid, X, M, K, stages, status, kflags) != cudaSuccess) return QG_ECUDA;
     return cudaGetLastError() == cudaSuccess ? QG_OK : QG_ECUDA;
 }
 

@@ -25,10 +25,11 @@ QG_ETIMEOUT = -4
 QG_EBOUNDS = -5
 QG_EALIAS = -6
 QG_MAX_M = 32
+QG_MAX_GROUP = 4
 
 QG_PREFETCH_WEIGHTS = 1
 
-EXPORTS = ("qgemv_q4k", "qgemv_q4k_ex", "qgemv_iq3", "qgemv_iq3_ex", "qgemm_q4k_batched", "qdequant_q4k", "qdequant_iq3",
+EXPORTS = ("qgemv_q4k", "qgemv_q4k_ex", "qgemv_q4k_group", "qgemv_iq3", "qgemv_iq3_ex", "qgemv_iq3_group", "qgemm_q4k_batched", "qdequant_q4k", "qdequant_iq3",
            "qg_device_status", "qg_test_bounded_wait", "qg_strerror")
 
 
@@ -58,6 +59,8 @@ def load():
             "qgemv_q4k_ex": [vp, vp, vp, ci, i64, i64, ctypes.c_uint, vp],
             "qgemv_iq3": [vp, vp, vp, vp, ci, i64, i64, vp],
             "qgemv_iq3_ex": [vp, vp, vp, vp, ci, i64, i64, ctypes.c_uint, vp],
+            "qgemv_q4k_group": [vp, vp, vp, ci, vp, ci, i64, ctypes.c_uint, vp],
+            "qgemv_iq3_group": [vp, vp, vp, ci, vp, vp, ci, i64, ctypes.c_uint, vp],
             "qgemm_q4k_batched": [vp, vp, vp, ci, i64, i64, vp],
             "qdequant_q4k": [vp, vp, i64, i64, vp],
             "qdequant_iq3": [vp, vp, vp, i64, i64, vp],
@@ -148,6 +151,52 @@ def qgemv_iq3(W, grid, X, out=None, stream=None, flags=0):
                              _stream(stream))
     _check("qgemv_iq3_ex" if flags else "qgemv_iq3", rc)
     return out
+
+
+def group_arrays(Ws, Ys, Ns):
+    """Host arrays (kept alive by the caller) of device pointers and row counts."""
+    n = len(Ws)
+    Wa = (ctypes.c_void_p * n)(*[w.data_ptr() for w in Ws])
+    Ya = (ctypes.c_void_p * n)(*[y.data_ptr() for y in Ys])
+    Na = (ctypes.c_int64 * n)(*Ns)
+    return Wa, Ya, Na
+
+
+def qgemv_q4k_group(Ws, X, outs=None, stream=None, flags=0):
+    """[X @ dequant(W_i)^T for W_i in Ws] in one launch (all W_i share K)."""
+    import torch
+    Xv = X.view(1, -1) if X.dim() == 1 else X
+    M, K = Xv.shape
+    Ns = []
+    for W in Ws:
+        _req(W, torch.uint8, "W")
+        Ns.append(W.numel() // (K // 256 * 144))
+    if outs is None:
+        outs = [torch.empty((M, n), dtype=torch.float32, device=X.device) for n in Ns]
+    _req(Xv, torch.float32, "X")
+    Wa, Ya, Na = group_arrays(Ws, outs, Ns)
+    rc = load().qgemv_q4k_group(Wa, Ya, Na, len(Ws), Xv.data_ptr(), M, K, flags, _stream(stream))
+    _check("qgemv_q4k_group", rc)
+    return outs
+
+
+def qgemv_iq3_group(Ws, grid, X, outs=None, stream=None, flags=0):
+    """IQ3 counterpart of qgemv_q4k_group (one grid)."""
+    import torch
+    Xv = X.view(1, -1) if X.dim() == 1 else X
+    M, K = Xv.shape
+    Ns = []
+    for W in Ws:
+        _req(W, torch.uint8, "W")
+        Ns.append(W.numel() // (K // 256 * 98))
+    if outs is None:
+        outs = [torch.empty((M, n), dtype=torch.float32, device=X.device) for n in Ns]
+    _req(Xv, torch.float32, "X")
+    _req(grid, torch.uint8, "grid")
+    Wa, Ya, Na = group_arrays(Ws, outs, Ns)
+    rc = load().qgemv_iq3_group(Wa, Ya, Na, len(Ws), grid.data_ptr(), Xv.data_ptr(), M, K, flags, _stream(stream))
+    _check("qgemv_iq3_group", rc)
+    return outs
 
 
 def qgemm_q4k_batched(W, X, out=None, stream=None):

@@ -56,6 +56,7 @@ extern "C" {
 #define QG_EALIAS (-6)    /* Y overlaps W, X or grid */
 
 #define QG_MAX_M 32
+#define QG_MAX_GROUP 4
 
 /* Launch flag for the *_ex entry points.  QG_PREFETCH_WEIGHTS promises that W
  * (and the IQ3 grid) are not written by the kernel that precedes this call in
@@ -99,6 +100,22 @@ QG_API int qgemv_iq3(const uint8_t* W, const uint8_t* grid, const float* X, floa
 /* qgemv_iq3 with launch flags (0 or QG_PREFETCH_WEIGHTS). */
 QG_API int qgemv_iq3_ex(const uint8_t* W, const uint8_t* grid, const float* X, float* Y, int M, int64_t N, int64_t K,
                         unsigned flags, cudaStream_t stream);
+
+/* Several Q4_K GEMVs that read the same X (in a decode step: q, k and v of a
+ * layer read the attention-norm output; gate and up read the FFN-norm
+ * output) in one launch: Y[i] = X * dequant(W[i])^T for i < count,
+ * 1 <= count <= QG_MAX_GROUP.  W, Y and N are HOST arrays holding device
+ * pointers and row counts; Y[i] is [M][N[i]].  Same K for every matrix.
+ * Results are identical to count separate qgemv_q4k_ex calls.  Page 1
+ * "Rewriting picoLM in Python", model_forward (the q/k/v and gate/up
+ * matmuls of one layer consume the same normalised activation). */
+QG_API int qgemv_q4k_group(const uint8_t* const* W, float* const* Y, const int64_t* N, int count, const float* X,
+                           int M, int64_t K, unsigned flags, cudaStream_t stream);
+
+/* IQ3 counterpart of qgemv_q4k_group; one grid for all matrices. */
+QG_API int qgemv_iq3_group(const uint8_t* const* W, float* const* Y, const int64_t* N, int count,
+                           const uint8_t* grid, const float* X, int M, int64_t K, unsigned flags,
+                           cudaStream_t stream);
 
 /* Batched Q4_K GEMM for decode batches, 1 <= M <= 32.
  * Same operation and layouts as qgemv_q4k.  M < 16 runs the fp32 FMA path

@@ -80,3 +80,21 @@ def test_output_aliasing_rejected_on_host(lib):
     # Y right after X's M*K floats does not overlap: validation passes the
     # alias check (then needs a GPU, so only the codes above are asserted)
     assert lib.qdequant_q4k(W, W + 16, 4, 256, None) == qgemv.QG_EALIAS
+
+
+def test_group_arguments_rejected_on_host(lib):
+    import ctypes
+    W = (ctypes.c_void_p * 2)(A, A + 0x1000000)
+    Y = (ctypes.c_void_p * 2)(A + 0x2000000, A + 0x3000000)
+    N = (ctypes.c_int64 * 2)(64, 64)
+    X = A + 0x4000000
+    assert lib.qgemv_q4k_group(W, Y, N, 0, X, 1, 256, 0, None) == qgemv.QG_EINVAL
+    assert lib.qgemv_q4k_group(W, Y, N, 5, X, 1, 256, 0, None) == qgemv.QG_EINVAL
+    assert lib.qgemv_q4k_group(W, Y, N, 2, X, 1, 256, 8, None) == qgemv.QG_EINVAL
+    # Y[1] overlapping W[0]
+    Y2 = (ctypes.c_void_p * 2)(A + 0x2000000, A + 64)
+    assert lib.qgemv_q4k_group(W, Y2, N, 2, X, 1, 256, 0, None) == qgemv.QG_EALIAS
+    # Y[0] and Y[1] overlapping each other
+    Y3 = (ctypes.c_void_p * 2)(A + 0x2000000, A + 0x2000000 + 128)
+    assert lib.qgemv_q4k_group(W, Y3, N, 2, X, 1, 256, 0, None) == qgemv.QG_EALIAS
+    assert lib.qgemv_iq3_group(W, Y, N, 2, None, X, 1, 256, 0, None) == qgemv.QG_EINVAL

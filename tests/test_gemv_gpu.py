@@ -264,3 +264,39 @@ def test_prefetch_flag_rejects_unknown_bits(q):
     x = torch.zeros((1, 512), device="cuda")
     y = torch.empty((1, 4), device="cuda")
     assert q.load().qgemv_q4k_ex(W.data_ptr(), x.data_ptr(), y.data_ptr(), 1, 4, 512, 6, None) == q.QG_EINVAL
+
+
+# ------------------------------------------------------------ grouped launches
+@pytest.mark.parametrize("M", [1, 3, 9])
+def test_q4k_group_matches_single_calls(q, M):
+    """q, k, v of one TinyLlama layer (2048x2048, 256x2048, 256x2048) in one
+    launch, reading the same x: identical to three separate launches."""
+    K = 2048
+    Ws = [dev(synth.gen_q4k(N, K, 50 + N + i)) for i, N in enumerate((2048, 256, 256))]
+    x = dev(synth.gen_x(M, K, 11))
+    ys = q.qgemv_q4k_group(Ws, x)
+    for W, y in zip(Ws, ys):
+        assert torch.equal(y, q.qgemv_q4k(W, x))
+        Y, A = oracle.gemv_q4k(W.cpu().numpy(), x.cpu().numpy(), rows=np.arange(0, W.numel() // 1152, 7))
+        check_tol(y.cpu().numpy()[:, ::7], Y, A, TAU_FMA, "group")
+
+
+def test_q4k_group_with_prefetch_flag(q):
+    K = 2048
+    Ws = [dev(synth.gen_q4k(N, K, 70 + i)) for i, N in enumerate((5632, 5632))]
+    x = dev(synth.gen_x(1, K, 12))
+    a = q.qgemv_q4k_group(Ws, x, flags=q.QG_PREFETCH_WEIGHTS)
+    b = [q.qgemv_q4k(W, x) for W in Ws]
+    for u, v in zip(a, b):
+        assert torch.equal(u, v)
+
+
+@pytest.mark.parametrize("K", [2048, 768])
+def test_iq3_group_matches_single_calls(q, K):
+    grid = synth.gen_iq3_grid(3)
+    Ws = [dev(synth.gen_iq3(N, K, 80 + i, grid_seed=3)[0]) for i, N in enumerate((100, 64, 33))]
+    g = dev(grid)
+    x = dev(synth.gen_x(2, K, 13))
+    ys = q.qgemv_iq3_group(Ws, g, x)
+    for W, y in zip(Ws, ys):
+        assert torch.equal(y, q.qgemv_iq3(W, g, x))
