@@ -4,27 +4,39 @@
 //
 // Only here the path is a dense contraction: a 128-row tile of W is
 // dequantised (page 1 "Rewriting picoLM in Python", dequantize_q4_K:
-// (d*sc)*q - dmin*mn, one fp32 rounding) and rounded to bf16 (RN) in shared
-// memory; X is rounded to bf16 likewise; tcgen05.mma (kind::f16, bf16 x bf16,
-// fp32 accumulation in tensor memory) computes D[row][token] = W_tile X^T
-// (W rows on the MMA's M=128 side, tokens on its N=16/32 side).
+// (d*sc)*q - dmin*mn) into shared memory as bf16 (round to nearest even); X
+// is rounded to bf16 likewise; tcgen05.mma (kind::f16, bf16 x bf16, fp32
+// accumulation in tensor memory) computes D[row][token] = W_tile X^T (W rows
+// on the MMA's M=128 side, tokens on its N=16/32 side).
 //
-// CTA roles (192 threads):
-//   warps 0-3  dequantise W (thread t = tile row t) and X into the operand
-//              stage, then drain the accumulator (tcgen05.ld) into Y;
-//   warp 4     producer: cp.async.bulk of each row's 144-byte block and of
-//              the fp32 x slice into a double-buffered raw stage;
-//   warp 5     allocates tensor memory; lane 0 issues the MMAs and commits
+// CTA roles (320 threads):
+//   warps 0-7  dequantise W and X into the operand stages: warps 0-3 the
+//              first 128 k of each unit, warps 4-7 the second (thread =
+//              tile row); warps 0-3 then drain the accumulator (tcgen05.ld,
+//              warp w reads TMEM lanes 32w..32w+31) into Y;
+//   warp 8     producer: one 2D tensor-map TMA per unit for the 128 rows x
+//              144-byte block column of W and one for the x slice (fp32),
+//              into a double-buffered raw stage;
+//   warp 9     allocates tensor memory; lane 0 issues the MMAs and commits
 //              them to mbarriers.
 // Work: units (tile, k-block) in row-major order, split evenly over the grid
 // (stream-K); a CTA's run over one tile is a "segment" whose partial sums are
-// added into Y (zeroed first) with fp32 atomics.
+// added into Y (zeroed first) with fp32 atomics.  Each unit is dequantised
+// in two halves of 128 k into two operand stages, in parallel, and the MMAs
+// of one unit overlap the dequantisation of the next raw stage.
 //
-// Operand layout (no swizzle, K-major): 8-row x 16-byte core matrices;
-// core (row group i, k chunk j) at ((i * 32) + j) * 128 bytes, row r of the
-// core at +16 r.  Adjacent k chunks are 128 bytes apart, adjacent row groups
-// 4096 bytes apart.
+// Exact weights: with the fp16 magic h = 1024 + q, one fp16 FMA gives
+// h*sc - 1024*sc = q*sc exactly (at most 945: the fused product is rounded
+// once and the result is representable); a mixed f16 x f16 + f32 FMA then
+// gives d*(q*sc) - dmin*mn with a single rounding, the pages' fp32 value.
+//
+// Operand layout (no swizzle, K-major): 8-row x 16-byte core matrices; in a
+// half stage core (row group i, k chunk j) sits at ((i * 16) + j) * 128
+// bytes, row r of the core at +16 r: adjacent k chunks 128 bytes apart,
+// adjacent row groups 2048 bytes apart.
+#include <cuda.h>
 #include <cuda_bf16.h>
+#include <cudaTypedefs.h>
 
 #include <algorithm>
 
@@ -36,17 +48,19 @@ namespace tc {
 
 constexpr int kTileRows = 128;
 constexpr int kBlockBytes = 144;
-constexpr int kThreads = 192;
-constexpr int kRawW = kTileRows * kBlockBytes;     // 18432
+constexpr int kThreads = 320;  // 8 dequant warps, producer, MMA
+constexpr int kRawW = kTileRows * kBlockBytes;     // 18432: TMA box 144 x 128
 constexpr int kRawX = 32 * 1024;                    // up to 32 tokens x 256 fp32
 constexpr int kRawStage = kRawW + kRawX;            // 51200
-constexpr int kOpA = kTileRows * 256 * 2;           // 65536: 128 rows x 256 k bf16
-constexpr int kOpB = 32 * 256 * 2;                  // 16384: 32 tokens x 256 k bf16
+constexpr int kOpA = kTileRows * 128 * 2;           // 32768: 128 rows x 128 k bf16
+constexpr int kOpB = 32 * 128 * 2;                  // 8192: 32 tokens x 128 k bf16
+constexpr int kOpStage = kOpA + kOpB;               // 40960
 constexpr int kRaw0 = 1024;
-constexpr int kOpA0 = kRaw0 + 2 * kRawStage;        // 103424
-constexpr int kOpB0 = kOpA0 + kOpA;                 // 168960
-constexpr int kSmemTotal = kOpB0 + kOpB;            // 185344
+constexpr int kOp0 = kRaw0 + 2 * kRawStage;         // 103424
+constexpr int kSmemTotal = kOp0 + 2 * kOpStage;     // 185344
 constexpr int kTmemCols = 32;
+constexpr uint32_t kSBO = 16 * 128;                 // row-group stride in an operand stage
+constexpr uint32_t kLBO = 128;                      // k-chunk stride
 
 // smem descriptor for tcgen05.mma: start address, leading (k) and stride
 // (row group) byte offsets, descriptor version 1, no swizzle.
@@ -107,47 +121,72 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
     for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
 
-// Offset of the 16-byte chunk (row, k chunk j) in an operand buffer.
+// Offset of the 16-byte chunk (row, k chunk j < 16) in a half operand stage.
 __device__ __forceinline__ uint32_t op_off(int row, int j) {
-    return static_cast<uint32_t>((((row >> 3) * 32) + j) * 128 + (row & 7) * 16);
+    return static_cast<uint32_t>((((row >> 3) * 16) + j) * 128 + (row & 7) * 16);
 }
 
-// Thread t: W tile row t, one 256-weight block -> 32 chunks of 8 bf16.
-// Weights are formed exactly in fp32 ((d*sc)*q - dmin*mn with both products
-// exact, one rounding) and then rounded to bf16.
-__device__ __forceinline__ void dequant_row(const uint8_t* blk, uint8_t* opA, int t) {
+__device__ __forceinline__ uint32_t hfma2_u32(uint32_t a, uint32_t b, uint32_t c) {
+    uint32_t r;
+    asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(c));
+    return r;
+}
+
+// fp32 d*qs + c, with d the fp16 in the low half of dh and qs one half of qp.
+__device__ __forceinline__ float mfma_lo(uint32_t dh, uint32_t qp, float c) {
+    float r;
+    asm("{\n\t.reg .b16 a0, a1, b0, b1;\n\tmov.b32 {a0, a1}, %1;\n\tmov.b32 {b0, b1}, %2;\n\t"
+        "fma.rn.f32.f16 %0, a0, b0, %3;\n\t}" : "=f"(r) : "r"(dh), "r"(qp), "f"(c));
+    return r;
+}
+__device__ __forceinline__ float mfma_hi(uint32_t dh, uint32_t qp, float c) {
+    float r;
+    asm("{\n\t.reg .b16 a0, a1, b0, b1;\n\tmov.b32 {a0, a1}, %1;\n\tmov.b32 {b0, b1}, %2;\n\t"
+        "fma.rn.f32.f16 %0, a0, b1, %3;\n\t}" : "=f"(r) : "r"(dh), "r"(qp), "f"(c));
+    return r;
+}
+
+__device__ __forceinline__ uint32_t half2_bits(float a) {
+    const __half2 h = __floats2half2_rn(a, a);
+    return *reinterpret_cast<const uint32_t*>(&h);
+}
+
+// Thread t: half `half` (k 128*half .. +127) of the W tile row t -> 16 chunks
+// of 8 bf16 in the operand stage.
+__device__ __forceinline__ void dequant_half(const uint8_t* blk, uint8_t* opA, int t, int half) {
     const uint4 h = *reinterpret_cast<const uint4*>(blk);
-    const float d = h2f(h.x), dmin = h2f(h.x >> 16);
+    const uint32_t dbits = h.x & 0xFFFFu;
+    const float dmin = h2f(h.x >> 16);
     uint32_t sc03, mn03, sc47, mn47;
     q4k_scale_min_words(h.y, h.z, h.w, sc03, mn03, sc47, mn47);
+    const uint32_t scw = half == 0 ? sc03 : sc47, mnw = half == 0 ? mn03 : mn47;
 #pragma unroll
-    for (int g = 0; g < 4; ++g) {
-        const uint32_t scw = g < 2 ? sc03 : sc47, mnw = g < 2 ? mn03 : mn47;
-        const float dl = d * byte_f(scw, (2 * g) & 3), ml = dmin * byte_f(mnw, (2 * g) & 3);
-        const float dh = d * byte_f(scw, (2 * g + 1) & 3), mh = dmin * byte_f(mnw, (2 * g + 1) & 3);
+    for (int gg = 0; gg < 2; ++gg) {
+        const int g = 2 * half + gg;
+        const float sl = byte_f(scw, 2 * gg), sh = byte_f(scw, 2 * gg + 1);
+        const float ml = -(dmin * byte_f(mnw, 2 * gg)), mh = -(dmin * byte_f(mnw, 2 * gg + 1));
+        // (1024+q)*sl - 1024*sl = q*sl; (1024+16q)*(sh/16) - 64*sh = q*sh (all exact in fp16)
+        const uint32_t SL = half2_bits(sl), NL = half2_bits(-1024.f * sl);
+        const uint32_t SH = half2_bits(sh * 0.0625f), NH = half2_bits(-64.f * sh);
 #pragma unroll
         for (int hh = 0; hh < 2; ++hh) {
             const uint4 q = *reinterpret_cast<const uint4*>(blk + 16 + 32 * g + 16 * hh);
             const uint32_t qv[4] = {q.x, q.y, q.z, q.w};
-            uint32_t lo[8], hi[8];  // bf16x2 words: weights 2e, 2e+1 of the 16 low / high
+            uint32_t lo[8], hi[8];
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-                const uint32_t v = qv[e];
-                // bytes 4e..4e+3: nibbles as exact floats
-                float ql[4], qh[4];
-#pragma unroll
-                for (int b = 0; b < 4; ++b) {
-                    ql[b] = static_cast<float>((v >> (8 * b)) & 0xFu);
-                    qh[b] = static_cast<float>((v >> (8 * b + 4)) & 0xFu);
-                }
-                lo[2 * e] = pack_bf16(fmaf(dl, ql[0], -ml), fmaf(dl, ql[1], -ml));
-                lo[2 * e + 1] = pack_bf16(fmaf(dl, ql[2], -ml), fmaf(dl, ql[3], -ml));
-                hi[2 * e] = pack_bf16(fmaf(dh, qh[0], -mh), fmaf(dh, qh[1], -mh));
-                hi[2 * e + 1] = pack_bf16(fmaf(dh, qh[2], -mh), fmaf(dh, qh[3], -mh));
+                const uint32_t v = qv[e], v8 = v >> 8;
+                const uint32_t A = hfma2_u32((v & 0x000F000Fu) | 0x64006400u, SL, NL);   // q*sl, bytes 0,2
+                const uint32_t C = hfma2_u32((v8 & 0x000F000Fu) | 0x64006400u, SL, NL);  // bytes 1,3
+                const uint32_t B = hfma2_u32((v & 0x00F000F0u) | 0x64006400u, SH, NH);   // q*sh, bytes 0,2
+                const uint32_t D = hfma2_u32((v8 & 0x00F000F0u) | 0x64006400u, SH, NH);  // bytes 1,3
+                lo[2 * e] = pack_bf16(mfma_lo(dbits, A, ml), mfma_lo(dbits, C, ml));
+                lo[2 * e + 1] = pack_bf16(mfma_hi(dbits, A, ml), mfma_hi(dbits, C, ml));
+                hi[2 * e] = pack_bf16(mfma_lo(dbits, B, mh), mfma_lo(dbits, D, mh));
+                hi[2 * e + 1] = pack_bf16(mfma_hi(dbits, B, mh), mfma_hi(dbits, D, mh));
             }
-            // low nibbles: k = 64g + 16hh + 0..15 -> chunks 8g + 2hh, +1
-            // high nibbles: k = 64g + 32 + 16hh + 0..15 -> chunks 8g + 4 + 2hh, +1
-            const int jl = 8 * g + 2 * hh, jh = 8 * g + 4 + 2 * hh;
+            // low nibbles: k' = 64gg + 16hh + 0..15; high: k' + 32 (k' within the half)
+            const int jl = 8 * gg + 2 * hh, jh = 8 * gg + 4 + 2 * hh;
             *reinterpret_cast<uint4*>(opA + op_off(t, jl)) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
             *reinterpret_cast<uint4*>(opA + op_off(t, jl + 1)) = make_uint4(lo[4], lo[5], lo[6], lo[7]);
             *reinterpret_cast<uint4*>(opA + op_off(t, jh)) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
@@ -156,23 +195,29 @@ __device__ __forceinline__ void dequant_row(const uint8_t* blk, uint8_t* opA, in
     }
 }
 
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar,
+                                            uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%2, %3}], [%4], %5;"
+        ::"r"(smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar)),
+          "l"(policy) : "memory");
+}
+
 __global__ void __launch_bounds__(kThreads, 1)
-    gemm_q4k_tc_kernel(const uint8_t* __restrict__ W, const float* __restrict__ X, float* __restrict__ Y, int M,
-                       int64_t N, int64_t K, unsigned* status) {
+    gemm_q4k_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
+                       float* __restrict__ Y, int M, int64_t N, int64_t K, unsigned* status) {
     extern __shared__ __align__(1024) uint8_t smem[];
-    uint64_t* raw_full = reinterpret_cast<uint64_t*>(smem);       // [2]
-    uint64_t* raw_empty = raw_full + 2;                            // [2]
-    uint64_t* op_full = raw_full + 4;
-    uint64_t* op_empty = raw_full + 5;
-    uint64_t* acc_full = raw_full + 6;
-    uint64_t* acc_empty = raw_full + 7;
+    uint64_t* raw_full = reinterpret_cast<uint64_t*>(smem);  // [2]
+    uint64_t* raw_empty = raw_full + 2;                       // [2]
+    uint64_t* op_full = raw_full + 4;                         // [2]
+    uint64_t* op_empty = raw_full + 6;                        // [2]
+    uint64_t* acc_full = raw_full + 8;
+    uint64_t* acc_empty = raw_full + 9;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + 128);
-    uint8_t* opA = smem + kOpA0;
-    uint8_t* opB = smem + kOpB0;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int nb = static_cast<int>(K / 256);
-    const int64_t pitch = static_cast<int64_t>(nb) * kBlockBytes;
     const int64_t ntiles = (N + kTileRows - 1) / kTileRows;
     const int64_t U = ntiles * nb;
     const int64_t u_begin = U * blockIdx.x / gridDim.x;
@@ -182,15 +227,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (threadIdx.x == 0) {
         for (int i = 0; i < 2; ++i) {
             mbar_init(&raw_full[i], 1);
-            mbar_init(&raw_empty[i], 4);
+            mbar_init(&raw_empty[i], 8);
+            mbar_init(&op_full[i], 4);
+            mbar_init(&op_empty[i], 1);
         }
-        mbar_init(op_full, 4);
-        mbar_init(op_empty, 1);
         mbar_init(acc_full, 1);
         mbar_init(acc_empty, 4);
         fence_mbar_init();
     }
-    if (warp == 5) {
+    if (warp == 9) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
                      ::"r"(smem_u32(tmem_slot)), "r"(kTmemCols) : "memory");
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
@@ -200,59 +245,65 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
-    if (warp == 4) {
-        // ---------------- producer
-        const uint64_t pol_w = policy_evict_first();
-        const uint64_t pol_x = policy_evict_last();
-        for (int64_t u = u_begin; u < u_end; ++u) {
-            const int64_t i = u - u_begin;
-            const int s = static_cast<int>(i & 1);
-            if (i >= 2) mbar_wait_bounded(&raw_empty[s], static_cast<uint32_t>(((i >> 1) - 1) & 1), status);
-            const int64_t tile = u / nb;
-            const int kb = static_cast<int>(u % nb);
-            const int64_t row0 = tile * kTileRows;
-            const int rows = static_cast<int>(min64(kTileRows, N - row0));
-            uint8_t* raw = smem + kRaw0 + s * kRawStage;
-            if (lane == 0) mbar_arrive_expect_tx(&raw_full[s], rows * kBlockBytes + M * 1024);
-            __syncwarp();
-            const uint8_t* src = W + row0 * pitch + static_cast<int64_t>(kb) * kBlockBytes;
-            for (int r = lane; r < rows; r += 32)
-                bulk_g2s(raw + r * kBlockBytes, src + r * pitch, kBlockBytes, &raw_full[s], pol_w);
-            for (int m = lane; m < M; m += 32)
-                bulk_g2s(raw + kRawW + m * 1024, X + m * K + static_cast<int64_t>(kb) * 256, 1024, &raw_full[s],
-                         pol_x);
+    if (warp == 8) {
+        // ---------------- producer (one thread issues the tensor copies)
+        if (lane == 0) {
+            const uint64_t pol_w = policy_evict_first();
+            const uint64_t pol_x = policy_evict_last();
+            const uint32_t bytes = kRawW + M * 1024;
+            for (int64_t u = u_begin; u < u_end; ++u) {
+                const int64_t i = u - u_begin;
+                const int s = static_cast<int>(i & 1);
+                if (i >= 2) mbar_wait_bounded(&raw_empty[s], static_cast<uint32_t>(((i >> 1) - 1) & 1), status);
+                const int64_t tile = u / nb;
+                const int kb = static_cast<int>(u % nb);
+                uint8_t* raw = smem + kRaw0 + s * kRawStage;
+                mbar_arrive_expect_tx(&raw_full[s], bytes);
+                tma_load_2d(raw, &tmW, kb * kBlockBytes, static_cast<int>(tile * kTileRows), &raw_full[s], pol_w);
+                tma_load_2d(raw + kRawW, &tmX, kb * 256, 0, &raw_full[s], pol_x);
+            }
         }
-    } else if (warp == 5) {
+        __syncwarp();
+    } else if (warp == 9) {
         // ---------------- MMA issuer
         const uint32_t idesc = instr_desc(kTileRows, nmma);
-        const uint32_t a0 = smem_u32(opA), b0 = smem_u32(opB);
         int64_t seg = 0;
         for (int64_t u = u_begin; u < u_end; ++u) {
             const int64_t i = u - u_begin;
             const int kb = static_cast<int>(u % nb);
             const bool first = (u == u_begin) || kb == 0;
             const bool last = (u == u_end - 1) || kb == nb - 1;
-            mbar_wait_bounded(op_full, static_cast<uint32_t>(i & 1), status);
-            if (first && seg > 0) mbar_wait_bounded(acc_empty, static_cast<uint32_t>((seg - 1) & 1), status);
-            tc_fence_after();
-            if (lane == 0) {
+            for (int half = 0; half < 2; ++half) {
+                const int o = half;  // operand stage o holds half o of every unit
+                mbar_wait_bounded(&op_full[o], static_cast<uint32_t>(i & 1), status);
+                if (first && half == 0 && seg > 0)
+                    mbar_wait_bounded(acc_empty, static_cast<uint32_t>((seg - 1) & 1), status);
+                tc_fence_after();
+                if (lane == 0) {
+                    const uint32_t a0 = smem_u32(smem + kOp0 + o * kOpStage);
+                    const uint32_t b0 = a0 + kOpA;
 #pragma unroll
-                for (int ks = 0; ks < 16; ++ks) {
-                    const uint64_t ad = smem_desc(a0 + 256 * ks, 128, 4096);
-                    const uint64_t bd = smem_desc(b0 + 256 * ks, 128, 4096);
-                    mma_bf16(tmem, ad, bd, idesc, (first && ks == 0) ? 0u : 1u);
+                    for (int ks = 0; ks < 8; ++ks) {
+                        const uint64_t ad = smem_desc(a0 + 256 * ks, kLBO, kSBO);
+                        const uint64_t bd = smem_desc(b0 + 256 * ks, kLBO, kSBO);
+                        mma_bf16(tmem, ad, bd, idesc, (first && half == 0 && ks == 0) ? 0u : 1u);
+                    }
+                    mma_commit(&op_empty[o]);
+                    if (last && half == 1) mma_commit(acc_full);
                 }
-                mma_commit(op_empty);
-                if (last) mma_commit(acc_full);
+                __syncwarp();
             }
-            __syncwarp();
             if (last) ++seg;
         }
         // the last segment's accumulator must be drained before TMEM is freed
         if (seg > 0) mbar_wait_bounded(acc_empty, static_cast<uint32_t>((seg - 1) & 1), status);
     } else {
-        // ---------------- dequant + epilogue (warps 0-3, thread t = tile row t)
-        const int t = threadIdx.x;
+        // ---------------- dequant (warps 0-7) + epilogue (warps 0-3)
+        const int half = warp >> 2;         // which 128 k of the unit
+        const int t = threadIdx.x & 127;    // tile row
+        const int hw = warp & 3;            // warp within the half
+        uint8_t* opA = smem + kOp0 + half * kOpStage;
+        uint8_t* opB = opA + kOpA;
         int64_t seg = 0;
         for (int64_t u = u_begin; u < u_end; ++u) {
             const int64_t i = u - u_begin;
@@ -263,31 +314,30 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int64_t row0 = tile * kTileRows;
             const int rows = static_cast<int>(min64(kTileRows, N - row0));
             const uint8_t* raw = smem + kRaw0 + s * kRawStage;
-            mbar_wait_bounded(&raw_full[s], static_cast<uint32_t>((i >> 1) & 1), status);
-            if (i >= 1) mbar_wait_bounded(op_empty, static_cast<uint32_t>((i - 1) & 1), status);
-            if (t < rows) dequant_row(raw + t * kBlockBytes, opA, t);
-            // X slice -> bf16 operand: chunk c = (token m, k chunk j)
             const float* xr = reinterpret_cast<const float*>(raw + kRawW);
-            for (int c = t; c < M * 32; c += 128) {
-                const int m = c >> 5, j = c & 31;
-                const float4 a = *reinterpret_cast<const float4*>(xr + m * 256 + 8 * j);
-                const float4 b = *reinterpret_cast<const float4*>(xr + m * 256 + 8 * j + 4);
-                *reinterpret_cast<uint4*>(opB + op_off(m, j)) =
-                    make_uint4(pack_bf16(a.x, a.y), pack_bf16(a.z, a.w), pack_bf16(b.x, b.y), pack_bf16(b.z, b.w));
+            mbar_wait_bounded(&raw_full[s], static_cast<uint32_t>((i >> 1) & 1), status);
+            if (i >= 1) mbar_wait_bounded(&op_empty[half], static_cast<uint32_t>((i - 1) & 1), status);
+            dequant_half(raw + t * kBlockBytes, opA, t, half);  // rows past N: TMA zero fill, unused
+            for (int c = t; c < M * 16; c += 128) {
+                const int m = c >> 4, j = c & 15;
+                const float4 a = *reinterpret_cast<const float4*>(xr + m * 256 + 128 * half + 8 * j);
+                const float4 b = *reinterpret_cast<const float4*>(xr + m * 256 + 128 * half + 8 * j + 4);
+                *reinterpret_cast<uint4*>(opB + op_off(m, j)) = make_uint4(
+                    pack_bf16(a.x, a.y), pack_bf16(a.z, a.w), pack_bf16(b.x, b.y), pack_bf16(b.z, b.w));
             }
             fence_proxy_async_smem();  // generic-proxy stores -> visible to the tensor core
             __syncwarp();
             if (lane == 0) {
+                arrive(&op_full[half]);
                 arrive(&raw_empty[s]);
-                arrive(op_full);
             }
-            if (last) {
+            if (last && half == 0) {
                 mbar_wait_bounded(acc_full, static_cast<uint32_t>(seg & 1), status);
                 tc_fence_after();
                 float v[32];
-                tmem_ld32(tmem + (static_cast<uint32_t>(32 * warp) << 16), v);
-                const int64_t row = row0 + t;
+                tmem_ld32(tmem + (static_cast<uint32_t>(32 * hw) << 16), v);
                 if (t < rows) {
+                    const int64_t row = row0 + t;
 #pragma unroll
                     for (int m = 0; m < 32; ++m)
                         if (m < M) atomicAdd(&Y[m * N + row], v[m]);
@@ -295,18 +345,36 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) arrive(acc_empty);
-                ++seg;
             }
+            if (last) ++seg;
         }
     }
     __syncthreads();
-    if (warp == 5) {
+    if (warp == 9) {
         tc_fence_after();
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols) : "memory");
     }
 }
 
 }  // namespace tc
+
+namespace {
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (!fn) {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) !=
+                cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            return nullptr;
+        fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    }
+    return fn;
+}
+
+}  // namespace
 
 int launch_gemm_q4k_tc(const uint8_t* W, const float* X, float* Y, int M, int64_t N, int64_t K, cudaStream_t s,
                        unsigned* status) {
@@ -320,13 +388,38 @@ int launch_gemm_q4k_tc(const uint8_t* W, const float* X, float* Y, int M, int64_
             return QG_ECUDA;
         attr_done[dev] = true;
     }
+    auto encode = tensor_map_encoder();
+    if (!encode) return QG_ECUDA;
+    // W viewed as [N rows][pitch bytes]; box = one 144-byte block column x 128 rows
+    const uint64_t pitch = static_cast<uint64_t>(K / 256) * tc::kBlockBytes;
+    CUtensorMap tmW, tmX;
+    {
+        const cuuint64_t gdim[2] = {pitch, static_cast<cuuint64_t>(N)};
+        const cuuint64_t gstride[1] = {pitch};
+        const cuuint32_t box[2] = {static_cast<cuuint32_t>(tc::kBlockBytes), static_cast<cuuint32_t>(tc::kTileRows)};
+        const cuuint32_t estr[2] = {1, 1};
+        if (encode(&tmW, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(W), gdim, gstride, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return QG_ECUDA;
+    }
+    {   // X [M][K] fp32; box = 256 k x M tokens
+        const cuuint64_t gdim[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(M)};
+        const cuuint64_t gstride[1] = {static_cast<cuuint64_t>(K) * 4};
+        const cuuint32_t box[2] = {256, static_cast<cuuint32_t>(M)};
+        const cuuint32_t estr[2] = {1, 1};
+        if (encode(&tmX, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float*>(X), gdim, gstride, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return QG_ECUDA;
+    }
     int sms = 0;
     if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0)
         return QG_ECUDA;
     if (cudaMemsetAsync(Y, 0, static_cast<size_t>(M) * N * sizeof(float), s) != cudaSuccess) return QG_ECUDA;
     const int64_t units = ((N + tc::kTileRows - 1) / tc::kTileRows) * (K / 256);
     const int grid = static_cast<int>(std::min<int64_t>(units, sms));
-    tc::gemm_q4k_tc_kernel<<<grid, tc::kThreads, tc::kSmemTotal, s>>>(W, X, Y, M, N, K, status);
+    tc::gemm_q4k_tc_kernel<<<grid, tc::kThreads, tc::kSmemTotal, s>>>(tmW, tmX, Y, M, N, K, status);
     return cudaGetLastError() == cudaSuccess ? QG_OK : QG_ECUDA;
 }
 
