@@ -136,10 +136,11 @@ __device__ __forceinline__ void fma2(f2& acc, f2 a, f2 b) {
 
 // One Q4_K super-block (144 bytes at blk, smem) against MT tokens of x.
 // sx[m*8 + j] = sum of x over sub-block j for token m.
-// Nibbles become exact fp32 through the fp16 magic 0x6400|q (= 1024 + q):
-// low nibbles give 1024+q, high nibbles (left in place) 1024+16q, and the
-// mixed f16->f32 add of -1024 yields q or 16q exactly; the 1/16 is folded
-// into the sub-block scale (exact, a power of two).
+// Nibbles become exact fp32 without any arithmetic (CVT == 2, the default):
+// a nibble placed in the low bits of an fp16 is the subnormal q*2^-24 (high
+// nibbles left in place: 16q*2^-24), which cvt.f32.f16 turns into an exact
+// fp32; the powers of two are folded into the sub-block scales.  (CVT 0 and
+// 1 are the earlier fp16 / fp32 magic-offset forms, kept for comparison.)
 template <int MT, bool PACKED, int CVT>
 __device__ __forceinline__ void q4k_block(const uint8_t* blk, const float* xb, int64_t xstride, const float* sx,
                                           int M, float (&acc)[MT]) {
@@ -172,7 +173,29 @@ __device__ __forceinline__ void q4k_block(const uint8_t* blk, const float* xb, i
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
                 const int kl = 64 * g + 16 * hh + 4 * e;  // weights kl..kl+3 (low), +32 (high)
-                if constexpr (CVT == 0) {
+                if constexpr (CVT == 2) {
+                    // Nibbles as fp16 subnormals: half bits 0x000q (low nibble)
+                    // or 0x00q0 (high nibble, 16q) are exactly q*2^-24 and
+                    // q*2^-20; one cvt per half gives exact fp32.  PRMT pairs
+                    // bytes (0,1) and (2,3) so each pair meets x[kl..kl+1],
+                    // x[kl+2..kl+3]; the powers of two go into the scales.
+                    const uint32_t lo4 = qv[e] & 0x0F0F0F0Fu, hi4 = qv[e] & 0xF0F0F0F0u;
+                    const f2 l01 = h2_to_f2(prmt(lo4, 0u, 0x5140u));
+                    const f2 l23 = h2_to_f2(prmt(lo4, 0u, 0x5342u));
+                    const f2 h01 = h2_to_f2(prmt(hi4, 0u, 0x5140u));
+                    const f2 h23 = h2_to_f2(prmt(hi4, 0u, 0x5342u));
+#pragma unroll
+                    for (int m = 0; m < MT; ++m) {
+                        if (MT == 1 || m < M) {
+                            const float4 xl = *reinterpret_cast<const float4*>(xb + m * xstride + kl);
+                            const float4 xh = *reinterpret_cast<const float4*>(xb + m * xstride + kl + 32);
+                            fma2<PACKED>(al[m], l01, f2{xl.x, xl.y});
+                            fma2<PACKED>(al[m], l23, f2{xl.z, xl.w});
+                            fma2<PACKED>(ah[m], h01, f2{xh.x, xh.y});
+                            fma2<PACKED>(ah[m], h23, f2{xh.z, xh.w});
+                        }
+                    }
+                } else if constexpr (CVT == 0) {
                     const uint32_t v = qv[e], v8 = v >> 8;
                     const uint32_t A = (v & 0x000F000Fu) | 0x64006400u;   // bytes 0,2 low nibbles
                     const uint32_t C = (v8 & 0x000F000Fu) | 0x64006400u;  // bytes 1,3 low nibbles
@@ -225,7 +248,10 @@ __device__ __forceinline__ void q4k_block(const uint8_t* blk, const float* xb, i
 #pragma unroll
         for (int m = 0; m < MT; ++m) {
             if (MT == 1 || m < M) {
-                if constexpr (CVT == 0) {
+                if constexpr (CVT == 2) {
+                    acc[m] = fmaf(dl * 16777216.f, al[m].x + al[m].y, acc[m]);     // 2^24
+                    acc[m] = fmaf(dh * 16777216.f, ah[m].x + ah[m].y, acc[m]);     // dh has 1/16: 2^20 * 16
+                } else if constexpr (CVT == 0) {
                     acc[m] = fmaf(dl, al[m].x + al[m].y, acc[m]);
                     acc[m] = fmaf(dh, ah[m].x + ah[m].y, acc[m]);
                 } else {
@@ -334,7 +360,7 @@ __device__ __forceinline__ void named_barrier_sync(int id) {
 
 // ------------------------------------------------------------ the kernel
 // Threads: RG*8 consumer warps, then one producer warp.
-template <class F, int MT, bool XS, int RG, bool PACKED, int MINB, int CVT = 0>
+template <class F, int MT, bool XS, int RG, bool PACKED, int MINB, int CVT = 2>
 __global__ void __launch_bounds__(RG * kCols * 32 + 32, MINB)
     gemv_kernel(const __grid_constant__ Group G, const uint8_t* __restrict__ grid, const float* __restrict__ X, int M,
                 int64_t K, int stages, unsigned* status, int flags) {

@@ -28,7 +28,7 @@ inline int sm_count(int dev) {
 // share X (token offset m0 already applied to X; Y[i] + m0*N[i] here): MINB
 // CTAs per SM, as many pipeline stages as fit in the per-CTA share of shared
 // memory.
-template <class F, int MT, bool XS, int RG, bool PACKED, int MINB, int CVT = 0>
+template <class F, int MT, bool XS, int RG, bool PACKED, int MINB, int CVT = 2>
 int launch_gemv(const uint8_t* const* W, float* const* Y, const int64_t* N, int count, int m0, const uint8_t* grid,
                 const float* X, int M, int64_t K, cudaStream_t s, unsigned* status, int dev, unsigned flags) {
     static bool attr_done[64];
