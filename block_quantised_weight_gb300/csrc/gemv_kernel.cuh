@@ -413,45 +413,69 @@ __global__ void __launch_bounds__(RG * kCols * 32 + 32, MINB)
 
     if (warp == kWarps) {
         // ---------------- producer warp
+        // Unit bookkeeping is incremental (stage, chunk, tile): no division
+        // in the loop.
         const uint64_t pol_w = policy_evict_first();
         const uint64_t pol_x = policy_evict_last();
-        // unit u -> (stage, tile rows, chunk); post its copies (W and/or x)
-        auto post = [&](int64_t u, bool do_w, bool do_x, bool expect) {
-            const int s = static_cast<int>(u % stages);
-            const int c = static_cast<int>(u % nchunks);
-            const int64_t tile = blockIdx.x + (u / nchunks) * gridDim.x;
-            const int gi = group_find(G, tile);
-            const int64_t row0 = (tile - G.tile0[gi]) * kTileRows;
-            const int rows = static_cast<int>(min64(kTileRows, G.N[gi] - row0));
-            const int kc = min(kCols, nb - c * kCols);
-            uint8_t* st = smem + L.stage0 + s * L.stage_bytes;
+        struct Pos {
+            int s, c;
+            int64_t tile, row0;
+            int gi, rows;
+        };
+        auto first_pos = [&]() {
+            Pos p{0, 0, static_cast<int64_t>(blockIdx.x), 0, 0, 0};
+            p.gi = group_find(G, p.tile);
+            p.row0 = (p.tile - G.tile0[p.gi]) * kTileRows;
+            p.rows = static_cast<int>(min64(kTileRows, G.N[p.gi] - p.row0));
+            return p;
+        };
+        auto next_pos = [&](Pos& p) {
+            if (++p.s == stages) p.s = 0;
+            if (++p.c == nchunks) {
+                p.c = 0;
+                p.tile += gridDim.x;
+                if (p.tile < ntiles) {
+                    p.gi = group_find(G, p.tile);
+                    p.row0 = (p.tile - G.tile0[p.gi]) * kTileRows;
+                    p.rows = static_cast<int>(min64(kTileRows, G.N[p.gi] - p.row0));
+                }
+            }
+        };
+        auto post = [&](const Pos& p, bool do_w, bool do_x, bool expect) {
+            const int kc = min(kCols, nb - p.c * kCols);
+            uint8_t* st = smem + L.stage0 + p.s * L.stage_bytes;
             if (expect) {
-                const uint32_t bytes = rows * kc * F::kBytes + (XS ? M * kc * 1024 : 0);
-                if (lane == 0) mbar_arrive_expect_tx(&full[s], bytes);
+                const uint32_t bytes = p.rows * kc * F::kBytes + (XS ? M * kc * 1024 : 0);
+                if (lane == 0) mbar_arrive_expect_tx(&full[p.s], bytes);
                 __syncwarp();
             }
             if (do_w) {
-                const uint8_t* src = G.W[gi] + row0 * pitch + static_cast<int64_t>(c) * kCols * F::kBytes;
-                for (int r = lane; r < rows; r += 32)
-                    bulk_g2s(st + r * F::kRowStride, src + r * pitch, kc * F::kBytes, &full[s], pol_w);
+                const uint8_t* src = G.W[p.gi] + p.row0 * pitch + static_cast<int64_t>(p.c) * kCols * F::kBytes;
+                for (int r = lane; r < p.rows; r += 32)
+                    bulk_g2s(st + r * F::kRowStride, src + r * pitch, kc * F::kBytes, &full[p.s], pol_w);
             }
             if (XS && do_x && lane < M)
-                bulk_g2s(st + L.xoff + lane * kCols * 1024, X + lane * K + static_cast<int64_t>(c) * kCols * 256,
-                         kc * 1024, &full[s], pol_x);
+                bulk_g2s(st + L.xoff + lane * kCols * 1024, X + lane * K + static_cast<int64_t>(p.c) * kCols * 256,
+                         kc * 1024, &full[p.s], pol_x);
         };
+        Pos p = first_pos();
         int64_t u0 = 0;
         if (prefetch) {
             // weights of the first stages stream while the previous kernel runs
             const int64_t pre = min64(stages, U);
-            for (int64_t u = 0; u < pre; ++u) post(u, true, false, true);
+            Pos q = p;
+            for (int64_t u = 0; u < pre; ++u, next_pos(q)) post(q, true, false, true);
             grid_dependency_wait();
-            for (int64_t u = 0; u < pre; ++u) post(u, false, true, false);
+            for (int64_t u = 0; u < pre; ++u, next_pos(p)) post(p, false, true, false);
             u0 = pre;
         }
-        for (int64_t u = u0; u < U; ++u) {
-            const int s = static_cast<int>(u % stages);
-            if (u >= stages) mbar_wait_bounded(&empty[s], static_cast<uint32_t>(((u / stages) - 1) & 1), status);
-            post(u, true, true, true);
+        uint32_t round = 0;  // completed passes over the ring before unit u
+        for (int64_t u = 0; u < u0; ++u)
+            if (static_cast<int>(u % stages) == stages - 1) ++round;
+        for (int64_t u = u0; u < U; ++u, next_pos(p)) {
+            if (u >= stages) mbar_wait_bounded(&empty[p.s], (round - 1) & 1u, status);
+            post(p, true, true, true);
+            if (p.s == stages - 1) ++round;
         }
         return;
     }
@@ -465,18 +489,24 @@ __global__ void __launch_bounds__(RG * kCols * 32 + 32, MINB)
     const uint32_t lane4 = static_cast<uint32_t>(lane) * 4u;
     int64_t tile_count = 0;
 
+    int s = 0, c = 0;
+    uint32_t phase = 0;
+    int64_t tile = blockIdx.x;
+    int gi = 0;
+    int64_t row0 = 0, Ni = 0;
+    int rows = 0;
+    auto load_tile = [&]() {
+        gi = group_find(G, tile);
+        row0 = (tile - G.tile0[gi]) * kTileRows;
+        Ni = G.N[gi];
+        rows = static_cast<int>(min64(kTileRows, Ni - row0));
+    };
+    if (U > 0) load_tile();
     for (int64_t u = 0; u < U; ++u) {
-        const int s = static_cast<int>(u % stages);
-        const int c = static_cast<int>(u % nchunks);
-        const int64_t tile = blockIdx.x + (u / nchunks) * gridDim.x;
-        const int gi = group_find(G, tile);
-        const int64_t row0 = (tile - G.tile0[gi]) * kTileRows;
-        const int64_t Ni = G.N[gi];
-        const int rows = static_cast<int>(min64(kTileRows, Ni - row0));
         const int kc = min(kCols, nb - c * kCols);
         const uint8_t* st = smem + L.stage0 + s * L.stage_bytes;
         const int r = rg * kRows + lane;  // row within the tile
-        mbar_wait_bounded(&full[s], static_cast<uint32_t>((u / stages) & 1), status);
+        mbar_wait_bounded(&full[s], phase, status);
 
         if (cw < kc) {
             const int64_t b = static_cast<int64_t>(c) * kCols + cw;  // super-block column
@@ -540,6 +570,16 @@ __global__ void __launch_bounds__(RG * kCols * 32 + 32, MINB)
                 }
             }
             ++tile_count;
+        }
+        // advance (stage ring, chunk, tile) without division
+        if (++s == stages) {
+            s = 0;
+            phase ^= 1u;
+        }
+        if (++c == nchunks) {
+            c = 0;
+            tile += gridDim.x;
+            if (tile < ntiles) load_tile();
         }
     }
 }
