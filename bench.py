@@ -207,7 +207,7 @@ def run_ours(args, rank, world, local_rank):
     # launch groups: in the decode pass q/k/v read one activation vector and
     # gate/up another, so each such set is one grouped launch (--single: one
     # launch per matrix)
-    groups = pass_groups(args.workload, len(host), args.single)
+    groups = pass_groups(args.workload, len(host), args.mode == "single")
     # device buffers: weights (rotated copies), x / y concatenated per pass
     xs_host = np.concatenate([host[g[0]][5].reshape(-1) for g in groups]).astype(np.float32)
     ys_len = sum(M * h[2] for h in host)
@@ -254,6 +254,27 @@ def run_ours(args, rank, world, local_rank):
             else:
                 lst.append((lib.qgemv_iq3_ex, (Wp[0], gd.data_ptr(), xp, Yp[0], M, Ns[0], K, fl), wb, algo, label))
             xo += M * K
+        if args.mode == "pass" and args.workload == "tinyllama":
+            # the whole pass as one persistent launch: stage i reads its x only
+            # after stage i-1 has written all of its y
+            arr = (qgemv.QgStage * len(lst))()
+            for i, (fn, a, wb, ab, lb) in enumerate(lst):
+                st = arr[i]
+                if fn == lib.qgemv_q4k_group:
+                    Wa, Ya, Na, cnt, xp, _M, K, _fl = a
+                    st.count = cnt
+                    for j in range(cnt):
+                        st.W[j], st.Y[j], st.N[j] = Wa[j], Ya[j], Na[j]
+                else:
+                    Wp0, xp, yp0, _M, N0, K, _fl = a
+                    st.count = 1
+                    st.W[0], st.Y[0], st.N[0] = Wp0, yp0, N0
+                st.X = xp
+                st.K = K
+            sync = torch.zeros(len(lst) + 8, dtype=torch.int32, device=dev)
+            keep.append((arr, sync))
+            lst = [(lib.qgemv_q4k_pass, (arr, len(lst), M, sync.data_ptr()), sum(l[2] for l in lst),
+                    sum(l[3] for l in lst), f"pass({len(lst)} stages)")]
         launches.append(lst)
     flat = [l for lst in launches for l in lst]
 
@@ -407,7 +428,10 @@ def run_ours(args, rank, world, local_rank):
                    "l2": ("inputs larger than L2" if copies == 1 else
                           f"rotates {copies} weight copies (> 2x L2)"),
                    "graph": "CUDA graph of the step, replayed", "parallelism": f"replicas x{world}",
-                   "launch": ("stream-ordered" if args.no_prefetch else
+                   "launch": ("one persistent cooperative launch per pass (qgemv_q4k_pass); stage i reads x only "
+                              "after every CTA finished stage i-1; weights of later stages stream meanwhile"
+                              if args.mode == "pass" and args.workload == "tinyllama" else
+                              "stream-ordered" if args.no_prefetch else
                               "programmatic dependent launch: each GEMV streams its first weight tiles while "
                               "the previous one finishes and waits for it before reading x")},
         "tokens_per_s_equiv": round(world * 1000.0 / ms_step, 1),
@@ -416,6 +440,7 @@ def run_ours(args, rank, world, local_rank):
                 "d2h_bytes_per_step": int(4 * ys_len),
                 "note": "pinned host x -> device, graph of C-ABI launches, device y -> pinned host, every step"},
         "gpu_launches": len(flat) * args.steps * (1 if M <= 8 or M >= 16 else (M + 7) // 8),
+        "mode": args.mode,
         "roofline": roof,
         "clocks": clocks,
     }
@@ -491,7 +516,9 @@ def main():
     ap.add_argument("--M", type=int, default=1)
     ap.add_argument("--cpu-baseline-s", type=float, default=12.0)
     ap.add_argument("--no-prefetch", action="store_true", help="plain stream-ordered launches")
-    ap.add_argument("--single", action="store_true", help="one launch per matrix (no q/k/v, gate/up groups)")
+    ap.add_argument("--mode", choices=["pass", "group", "single"], default="group",
+                    help="decode pass as one persistent launch (pass), one launch per q/k/v or gate/up group "
+                         "(group), or one launch per matrix (single)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

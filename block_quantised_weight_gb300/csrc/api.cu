@@ -142,6 +142,23 @@ int qgemv_iq3_group(const uint8_t* const* W, float* const* Y, const int64_t* N, 
     return qg::launch_group_iq3(W, Y, N, count, grid, X, M, K, stream, st, flags);
 }
 
+int qgemv_q4k_pass(const qg_stage* stages, int nstages, int M, unsigned* sync, cudaStream_t stream) {
+    if (!stages || !sync || nstages < 1 || nstages > QG_MAX_PASS_STAGES || M < 1 || M > 4) return QG_EINVAL;
+    if (reinterpret_cast<uintptr_t>(sync) & 3u) return QG_EALIGN;
+    for (int i = 0; i < nstages; ++i) {
+        const qg_stage& q = stages[i];
+        const int rc = check_group(q.W, const_cast<float* const*>(q.Y), q.N, q.count, nullptr, false, q.X, M, q.K, 144);
+        if (rc != QG_OK) return rc;
+        for (int j = 0; j < q.count; ++j)
+            if (overlap(sync, 4 * int64_t(nstages), q.Y[j], int64_t(M) * q.N[j] * 4) ||
+                overlap(sync, 4 * int64_t(nstages), q.W[j], q.N[j] * (q.K / 256) * 144))
+                return QG_EALIAS;
+    }
+    unsigned* st = status_ptr();
+    if (!st) return QG_ECUDA;
+    return qg::launch_pass_q4k(stages, nstages, M, sync, stream, st);
+}
+
 int qgemm_q4k_batched(const uint8_t* W, const float* X, float* Y, int M, int64_t N, int64_t K, cudaStream_t stream) {
     int rc = check_gemv(W, nullptr, false, X, Y, M, N, K, 144);
     if (rc != QG_OK) return rc;

@@ -16,6 +16,7 @@ int launch_group_q4k(const uint8_t* const* W, float* const* Y, const int64_t* N,
                      int64_t K, cudaStream_t s, unsigned* status, unsigned flags);
 int launch_group_iq3(const uint8_t* const* W, float* const* Y, const int64_t* N, int count, const uint8_t* grid,
                      const float* X, int M, int64_t K, cudaStream_t s, unsigned* status, unsigned flags);
+int launch_pass_q4k(const qg_stage* stages, int nstages, int M, unsigned* sync, cudaStream_t s, unsigned* status);
 int launch_dequant_q4k(const uint8_t* W, float* out, int64_t N, int64_t K, cudaStream_t s);
 int launch_dequant_iq3(const uint8_t* W, const uint8_t* grid, float* out, int64_t N, int64_t K, cudaStream_t s);
 // tcgen05 bf16 path, 16 <= M <= 32

@@ -26,10 +26,16 @@ QG_EBOUNDS = -5
 QG_EALIAS = -6
 QG_MAX_M = 32
 QG_MAX_GROUP = 4
+QG_MAX_PASS_STAGES = 96
+
+
+class QgStage(ctypes.Structure):
+    _fields_ = [("W", ctypes.c_void_p * 4), ("Y", ctypes.c_void_p * 4), ("N", ctypes.c_int64 * 4),
+                ("count", ctypes.c_int), ("X", ctypes.c_void_p), ("K", ctypes.c_int64)]
 
 QG_PREFETCH_WEIGHTS = 1
 
-EXPORTS = ("qgemv_q4k", "qgemv_q4k_ex", "qgemv_q4k_group", "qgemv_iq3", "qgemv_iq3_ex", "qgemv_iq3_group", "qgemm_q4k_batched", "qdequant_q4k", "qdequant_iq3",
+EXPORTS = ("qgemv_q4k", "qgemv_q4k_ex", "qgemv_q4k_group", "qgemv_q4k_pass", "qgemv_iq3", "qgemv_iq3_ex", "qgemv_iq3_group", "qgemm_q4k_batched", "qdequant_q4k", "qdequant_iq3",
            "qg_device_status", "qg_test_bounded_wait", "qg_strerror")
 
 
@@ -61,6 +67,7 @@ def load():
             "qgemv_iq3_ex": [vp, vp, vp, vp, ci, i64, i64, ctypes.c_uint, vp],
             "qgemv_q4k_group": [vp, vp, vp, ci, vp, ci, i64, ctypes.c_uint, vp],
             "qgemv_iq3_group": [vp, vp, vp, ci, vp, vp, ci, i64, ctypes.c_uint, vp],
+            "qgemv_q4k_pass": [vp, ci, ci, vp, vp],
             "qgemm_q4k_batched": [vp, vp, vp, ci, i64, i64, vp],
             "qdequant_q4k": [vp, vp, i64, i64, vp],
             "qdequant_iq3": [vp, vp, vp, i64, i64, vp],
@@ -197,6 +204,35 @@ def qgemv_iq3_group(Ws, grid, X, outs=None, stream=None, flags=0):
     rc = load().qgemv_iq3_group(Wa, Ya, Na, len(Ws), grid.data_ptr(), Xv.data_ptr(), M, K, flags, _stream(stream))
     _check("qgemv_iq3_group", rc)
     return outs
+
+
+def pass_stages(stages):
+    """ctypes array of qg_stage from [(Ws, Ys, X)] (torch CUDA tensors)."""
+    arr = (QgStage * len(stages))()
+    for i, (Ws, Ys, X) in enumerate(stages):
+        Xv = X.view(1, -1) if X.dim() == 1 else X
+        K = Xv.shape[1]
+        st = arr[i]
+        st.count = len(Ws)
+        for j, (W, Y) in enumerate(zip(Ws, Ys)):
+            st.W[j] = W.data_ptr()
+            st.Y[j] = Y.data_ptr()
+            st.N[j] = W.numel() // (K // 256 * 144)
+        st.X = Xv.data_ptr()
+        st.K = K
+    return arr
+
+
+def qgemv_q4k_pass(stages, sync, M=1, stream=None):
+    """Run [(Ws, Ys, X)] stages as one persistent launch; sync: int32 CUDA tensor
+    with at least len(stages) elements (zeroed by the call)."""
+    import torch
+    _req(sync, torch.int32, "sync")
+    if sync.numel() < len(stages):
+        raise ValueError("sync needs one word per stage")
+    arr = pass_stages(stages)
+    rc = load().qgemv_q4k_pass(arr, len(stages), M, sync.data_ptr(), _stream(stream))
+    _check("qgemv_q4k_pass", rc)
 
 
 def qgemm_q4k_batched(W, X, out=None, stream=None):

@@ -117,6 +117,30 @@ QG_API int qgemv_iq3_group(const uint8_t* const* W, float* const* Y, const int64
                            const uint8_t* grid, const float* X, int M, int64_t K, unsigned flags,
                            cudaStream_t stream);
 
+/* One stage of a decode pass: a group of matrices reading the same X. */
+#define QG_MAX_PASS_STAGES 96
+typedef struct qg_stage {
+    const uint8_t* W[QG_MAX_GROUP]; /* device, Q4_K, [N[i]][K/256 blocks] */
+    float* Y[QG_MAX_GROUP];         /* device, [M][N[i]] */
+    int64_t N[QG_MAX_GROUP];
+    int count;                      /* 1..QG_MAX_GROUP */
+    const float* X;                 /* device, [M][K]; may be a Y of an earlier stage */
+    int64_t K;
+} qg_stage;
+
+/* A sequence of dependent Q4_K GEMV stages (a decode pass: per layer q/k/v,
+ * o, gate/up, down, then the output projection) in one persistent,
+ * cooperative launch.  Stage s reads its X only after every stage < s has
+ * written all of its Y, so X of a stage may be any Y of an earlier stage;
+ * the weights of later stages stream while earlier stages finish.
+ * Results are identical to qgemv_q4k_group per stage.  1 <= M <= 4,
+ * 1 <= nstages <= QG_MAX_PASS_STAGES.  `stages` is a host array.
+ * sync: caller-owned device memory of at least 4*nstages bytes (4-byte
+ * aligned) used for the stage completion counts; the call zeroes it on the
+ * stream; concurrent calls must not share it.  Page 1 "Rewriting picoLM in
+ * Python", model_forward (the per-layer matmul sequence). */
+QG_API int qgemv_q4k_pass(const qg_stage* stages, int nstages, int M, unsigned* sync, cudaStream_t stream);
+
 /* Batched Q4_K GEMM for decode batches, 1 <= M <= 32.
  * Same operation and layouts as qgemv_q4k.  M < 16 runs the fp32 FMA path
  * (tolerance 1e-5 * sum|w*x|); M >= 16 dequantises W tiles to bf16 (round to

@@ -300,3 +300,72 @@ def test_iq3_group_matches_single_calls(q, K):
     ys = q.qgemv_iq3_group(Ws, g, x)
     for W, y in zip(Ws, ys):
         assert torch.equal(y, q.qgemv_iq3(W, g, x))
+
+
+# ------------------------------------------------------------ persistent pass
+@pytest.mark.parametrize("M", [1, 2])
+def test_pass_kernel_dependent_stages(q, M):
+    """Stages whose X is the previous stage's Y, in one persistent launch:
+    identical to launching the groups one by one, and matching the oracle
+    stage by stage."""
+    rng = np.random.default_rng(40 + M)
+
+    def W(N, K):
+        return dev(synth.gen_q4k(N, K, rng))
+
+    x0 = dev(synth.gen_x(M, 512, 5))
+    A, B = W(512, 512), W(256, 512)
+    C = W(768, 512)
+    D = W(256, 768)
+    E, F = W(100, 256), W(64, 256)
+    yA, yB = torch.empty((M, 512), device="cuda"), torch.empty((M, 256), device="cuda")
+    yC = torch.empty((M, 768), device="cuda")
+    yD = torch.empty((M, 256), device="cuda")
+    yE, yF = torch.empty((M, 100), device="cuda"), torch.empty((M, 64), device="cuda")
+    stages = [([A, B], [yA, yB], x0), ([C], [yC], yA), ([D], [yD], yC), ([E, F], [yE, yF], yD)]
+    sync = torch.zeros(8, dtype=torch.int32, device="cuda")
+    for _ in range(2):   # twice: the sync words are re-zeroed by each call
+        for ys in (yA, yB, yC, yD, yE, yF):
+            ys.fill_(float("nan"))
+        q.qgemv_q4k_pass(stages, sync, M=M)
+        torch.cuda.synchronize()
+        ref = []
+        for Ws, Ys, X in stages:
+            ref.append(q.qgemv_q4k_group(Ws, X))
+        torch.cuda.synchronize()
+        for (Ws, Ys, X), r in zip(stages, ref):
+            for y, yr in zip(Ys, r):
+                assert torch.equal(y, yr)
+    for Ws, Ys, X in stages:
+        for Wt, y in zip(Ws, Ys):
+            Y, Aa = oracle.gemv_q4k(Wt.cpu().numpy(), X.cpu().numpy())
+            check_tol(y.cpu().numpy(), Y, Aa, TAU_FMA, "pass stage")
+    assert q.qg_device_status() == q.QG_OK
+
+
+def test_tinyllama_pass_kernel_matches_groups(q):
+    """The 89-stage TinyLlama pass (q/k/v and gate/up grouped) as one launch
+    equals the stage-by-stage grouped launches bit for bit."""
+    stages, ys_ref = [], []
+    mats = synth.tinyllama_seeds(1)
+    i = 0
+    while i < len(mats):
+        (layer, name, K, N), rng = mats[i]
+        take = 3 if name == "q" else 2 if name == "gate" else 1
+        Ws, Ys = [], []
+        x = None
+        for j in range(take):
+            (_l, _n, Kj, Nj), rj = mats[i + j]
+            Ws.append(dev(synth.gen_q4k(Nj, Kj, rj)))
+            xj = synth.gen_x(1, Kj, rj)
+            x = dev(xj) if x is None else x
+            Ys.append(torch.empty((1, Nj), device="cuda"))
+        stages.append((Ws, Ys, x))
+        i += take
+    assert len(stages) == 89
+    sync = torch.zeros(89, dtype=torch.int32, device="cuda")
+    q.qgemv_q4k_pass(stages, sync, M=1)
+    for Ws, Ys, X in stages:
+        for y, yr in zip(Ys, q.qgemv_q4k_group(Ws, X)):
+            assert torch.equal(y, yr)
+    assert q.qg_device_status() == q.QG_OK
