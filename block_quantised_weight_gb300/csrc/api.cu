@@ -3,6 +3,7 @@
 // Every argument is checked on the host before anything is launched; no
 // exception crosses this boundary and nothing here aborts the process.
 #include <cstdint>
+#include <mutex>
 
 #include "common.cuh"
 #include "launch.h"
@@ -24,6 +25,35 @@ unsigned* status_ptr() {
         g_status_ptr[dev] = static_cast<unsigned*>(p);
     }
     return g_status_ptr[dev];
+}
+
+}  // namespace
+
+// Scratch of qgemv_q4k_pass_noalloc: its per-stage completion counts.  A
+// fixed array in the library's own module, so that the entry point needs no
+// allocation; every device that loads the library holds it until exit.  In
+// host code `qg_noalloc_scratch` is a host-side stand-in for the symbol, not
+// a device address: kernels get the address from cudaGetSymbolAddress.
+static __device__ __align__(256) unsigned qg_noalloc_scratch[QG_NOALLOC_SCRATCH_WORDS];
+
+namespace {
+
+std::mutex g_noalloc_mu;
+unsigned* g_noalloc_ptr[64];
+
+// Set-up, once per device, with that device current: the device address of
+// qg_noalloc_scratch.
+int noalloc_scratch(unsigned** out) {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return QG_ECUDA;
+    std::lock_guard<std::mutex> lock(g_noalloc_mu);
+    if (!g_noalloc_ptr[dev]) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, qg_noalloc_scratch) != cudaSuccess || !p) return QG_ECUDA;
+        g_noalloc_ptr[dev] = static_cast<unsigned*>(p);
+    }
+    *out = g_noalloc_ptr[dev];
+    return QG_OK;
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -159,6 +189,23 @@ int qgemv_q4k_pass(const qg_stage* stages, int nstages, int M, unsigned* sync, c
     return qg::launch_pass_q4k(stages, nstages, M, sync, stream, st);
 }
 
+int qgemv_q4k_pass_noalloc(const qg_stage* stages, int nstages, int M, cudaStream_t stream) {
+    if (!stages || nstages < 1 || M < 1 || M > 4) return QG_EINVAL;
+    if (nstages > QG_NOALLOC_SCRATCH_WORDS) return QG_ESCRATCH;
+    for (int i = 0; i < nstages; ++i) {
+        const qg_stage& q = stages[i];
+        const int rc = check_group(q.W, const_cast<float* const*>(q.Y), q.N, q.count, nullptr, false, q.X, M, q.K, 144);
+        if (rc != QG_OK) return rc;
+    }
+    unsigned* st = status_ptr();
+    if (!st) return QG_ECUDA;
+    unsigned* scratch = nullptr;
+    const int rc = noalloc_scratch(&scratch);
+    if (rc != QG_OK) return rc;
+    // launch_pass_q4k zeroes scratch[0, nstages) on the stream, then launches.
+    return qg::launch_pass_q4k(stages, nstages, M, scratch, stream, st);
+}
+
 int qgemm_q4k_batched(const uint8_t* W, const float* X, float* Y, int M, int64_t N, int64_t K, cudaStream_t stream) {
     int rc = check_gemv(W, nullptr, false, X, Y, M, N, K, 144);
     if (rc != QG_OK) return rc;
@@ -206,6 +253,7 @@ const char* qg_strerror(int status) {
         case QG_ETIMEOUT: return "a bounded wait inside a kernel gave up";
         case QG_EBOUNDS: return "an index check inside a kernel failed";
         case QG_EALIAS: return "output overlaps an input";
+        case QG_ESCRATCH: return "more stages than the fixed scratch of qgemv_q4k_pass_noalloc holds";
         default: return "unknown status";
     }
 }

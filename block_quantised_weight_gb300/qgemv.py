@@ -24,9 +24,11 @@ QG_ECUDA = -3
 QG_ETIMEOUT = -4
 QG_EBOUNDS = -5
 QG_EALIAS = -6
+QG_ESCRATCH = -7
 QG_MAX_M = 32
 QG_MAX_GROUP = 4
 QG_MAX_PASS_STAGES = 96
+QG_NOALLOC_SCRATCH_WORDS = 96
 
 
 class QgStage(ctypes.Structure):
@@ -35,7 +37,7 @@ class QgStage(ctypes.Structure):
 
 QG_PREFETCH_WEIGHTS = 1
 
-EXPORTS = ("qgemv_q4k", "qgemv_q4k_ex", "qgemv_q4k_group", "qgemv_q4k_pass", "qgemv_iq3", "qgemv_iq3_ex", "qgemv_iq3_group", "qgemm_q4k_batched", "qdequant_q4k", "qdequant_iq3",
+EXPORTS = ("qgemv_q4k", "qgemv_q4k_ex", "qgemv_q4k_group", "qgemv_q4k_pass", "qgemv_q4k_pass_noalloc", "qgemv_iq3", "qgemv_iq3_ex", "qgemv_iq3_group", "qgemm_q4k_batched", "qdequant_q4k", "qdequant_iq3",
            "qg_device_status", "qg_test_bounded_wait", "qg_strerror")
 
 
@@ -68,6 +70,7 @@ def load():
             "qgemv_q4k_group": [vp, vp, vp, ci, vp, ci, i64, ctypes.c_uint, vp],
             "qgemv_iq3_group": [vp, vp, vp, ci, vp, vp, ci, i64, ctypes.c_uint, vp],
             "qgemv_q4k_pass": [vp, ci, ci, vp, vp],
+            "qgemv_q4k_pass_noalloc": [vp, ci, ci, vp],
             "qgemm_q4k_batched": [vp, vp, vp, ci, i64, i64, vp],
             "qdequant_q4k": [vp, vp, i64, i64, vp],
             "qdequant_iq3": [vp, vp, vp, i64, i64, vp],
@@ -233,6 +236,15 @@ def qgemv_q4k_pass(stages, sync, M=1, stream=None):
     arr = pass_stages(stages)
     rc = load().qgemv_q4k_pass(arr, len(stages), M, sync.data_ptr(), _stream(stream))
     _check("qgemv_q4k_pass", rc)
+
+
+def qgemv_q4k_pass_noalloc(stages, M=1, stream=None):
+    """qgemv_q4k_pass with the stage counts in the library's fixed scratch:
+    the call allocates nothing on the device.  Calls that overlap on the GPU
+    race on that scratch."""
+    arr = pass_stages(stages)
+    rc = load().qgemv_q4k_pass_noalloc(arr, len(stages), M, _stream(stream))
+    _check("qgemv_q4k_pass_noalloc", rc)
 
 
 def qgemm_q4k_batched(W, X, out=None, stream=None):

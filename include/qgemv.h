@@ -54,6 +54,7 @@ extern "C" {
 #define QG_ETIMEOUT (-4)  /* device: a bounded wait inside a kernel gave up */
 #define QG_EBOUNDS (-5)   /* device: an index check inside a kernel failed */
 #define QG_EALIAS (-6)    /* Y overlaps W, X or grid */
+#define QG_ESCRATCH (-7)  /* request larger than the fixed scratch of qgemv_q4k_pass_noalloc */
 
 #define QG_MAX_M 32
 #define QG_MAX_GROUP 4
@@ -140,6 +141,31 @@ typedef struct qg_stage {
  * stream; concurrent calls must not share it.  Page 1 "Rewriting picoLM in
  * Python", model_forward (the per-layer matmul sequence). */
 QG_API int qgemv_q4k_pass(const qg_stage* stages, int nstages, int M, unsigned* sync, cudaStream_t stream);
+
+/* qgemv_q4k_pass without any allocation: for callers that cannot call
+ * cudaMalloc.  Examples are a plugin that its host application hands only
+ * input and output buffers while the application's own pool owns the rest
+ * of device memory, and a decode loop that must not stall, since cudaMalloc
+ * and cudaFree may synchronise the device.  Such callers still pass all
+ * inputs and outputs; only the stage completion counts (the `sync` words of
+ * qgemv_q4k_pass) move into a fixed scratch array inside this library,
+ * QG_NOALLOC_SCRATCH_WORDS 32-bit words (384 bytes) that every GPU which
+ * loads the library holds until the process exits.  Everything else is as
+ * in qgemv_q4k_pass: same stages, same results, 1 <= M <= 4.
+ * nstages > QG_NOALLOC_SCRATCH_WORDS returns QG_ESCRATCH; nstages < 1,
+ * M outside [1, 4] or a null `stages` returns QG_EINVAL.
+ * The first call on a device, with that device current, looks up the
+ * scratch array's device address; make that first call before any stream
+ * capture.  The call allocates nothing: no cudaMalloc, no cudaFree, no
+ * allocating library routine.  Each call zeroes the counts it uses on the
+ * stream before its launch (the array keeps the previous call's contents).
+ * All calls on a device share the one array, so calls that overlap on the
+ * GPU (other streams, other host threads) race and give wrong results:
+ * order them on one stream or synchronise between them.
+ * The paper has no counterpart: this entry point exists only for callers
+ * that cannot allocate. */
+#define QG_NOALLOC_SCRATCH_WORDS 96
+QG_API int qgemv_q4k_pass_noalloc(const qg_stage* stages, int nstages, int M, cudaStream_t stream);
 
 /* Batched Q4_K GEMM for decode batches, 1 <= M <= 32.
  * Same operation and layouts as qgemv_q4k.  M < 16 runs the fp32 FMA path
