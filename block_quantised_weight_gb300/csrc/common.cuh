@@ -7,6 +7,7 @@
 // and lets the kernel run to its end.
 #pragma once
 #include <cstdint>
+#include <cuda.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
@@ -70,6 +71,17 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
     }
     atomicOr(status, kStatusTimeout);
     return false;
+}
+
+// 2D tiled TMA load (tensor map in param/const space) completing on `bar`.
+// x is the innermost coordinate: x * element size must be a multiple of 16.
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar,
+                                            uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%2, %3}], [%4], %5;"
+        ::"r"(smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar)),
+          "l"(policy) : "memory");
 }
 
 // L2 policy for data read exactly once (the weight stream).

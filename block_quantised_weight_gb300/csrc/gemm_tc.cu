@@ -42,6 +42,7 @@
 
 #include "gemv_kernel.cuh"
 #include "launch.h"
+#include "tensor_map.h"
 
 namespace qg {
 namespace tc {
@@ -195,14 +196,6 @@ __device__ __forceinline__ void dequant_half(const uint8_t* blk, uint8_t* opA, i
     }
 }
 
-__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar,
-                                            uint64_t policy) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
-        " [%0], [%1, {%2, %3}], [%4], %5;"
-        ::"r"(smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar)),
-          "l"(policy) : "memory");
-}
 
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_q4k_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
@@ -358,23 +351,6 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 }  // namespace tc
 
-namespace {
-
-PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    if (!fn) {
-        void* p = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) !=
-                cudaSuccess ||
-            q != cudaDriverEntryPointSuccess)
-            return nullptr;
-        fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-    }
-    return fn;
-}
-
-}  // namespace
 
 int launch_gemm_q4k_tc(const uint8_t* W, const float* X, float* Y, int M, int64_t N, int64_t K, cudaStream_t s,
                        unsigned* status) {

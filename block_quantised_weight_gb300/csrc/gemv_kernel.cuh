@@ -41,15 +41,28 @@ constexpr int kSmemPerSM = 233472;   // 228 KB per SM on sm_103
 constexpr int kSmemPerCTA = 232448;  // 227 KB max dynamic smem per CTA
 constexpr int kSmemReserve = 1024;   // per-CTA system reservation
 
+// Stage layouts.  Row-copy formats: one bulk copy per row chunk, each row in
+// its own slot (kRowStride apart).  FmtQ4KT: one 2D tensor-map TMA per
+// super-block column, landing as [tile rows][144 B] boxes (a unit is kCols
+// boxes); 144 B = 9 x 16 B, so eight lanes reading eight consecutive rows
+// with 16-byte loads hit eight distinct bank groups.
 struct FmtQ4K {
     static constexpr int kBytes = 144;
     static constexpr int kRowStride = kCols * 144 + 16;  // 1168 = 73 * 16 (odd)
     static constexpr bool kIQ3 = false;
+    static constexpr bool kTMA = false;
+};
+struct FmtQ4KT {
+    static constexpr int kBytes = 144;
+    static constexpr int kRowStride = kCols * 144;  // bytes per tile row per unit (kCols boxes of 144 B)
+    static constexpr bool kIQ3 = false;
+    static constexpr bool kTMA = true;
 };
 struct FmtIQ3 {
     static constexpr int kBytes = 98;
     static constexpr int kRowStride = kCols * 98;  // 784 = 49 * 16 (odd)
     static constexpr bool kIQ3 = true;
+    static constexpr bool kTMA = false;
 };
 
 // IQ3 grid table in smem, lane-replicated so every gather is conflict-free:
@@ -74,6 +87,12 @@ struct Group {
     int64_t N[kMaxGroup];
     int64_t tile0[kMaxGroup + 1];
     int count;
+};
+
+// Tensor maps of the group's matrices (FmtQ4KT): bytes [N][K/256*144], box
+// 144 B x tile rows.
+struct TMaps {
+    CUtensorMap m[kMaxGroup];
 };
 
 // Matrix that owns global tile `tile`.
@@ -131,6 +150,37 @@ __device__ __forceinline__ void fma2(f2& acc, f2 a, f2 b) {
     } else {
         acc.x = fmaf(a.x, b.x, acc.x);
         acc.y = fmaf(a.y, b.y, acc.y);
+    }
+}
+
+// Per-warp x preparation for one Q4_K super-block column (256 x values per
+// token, in smem): sx[m*8 + j] = sum of x over sub-block j (the dmin*mn
+// term's factor), and for CVT == 3 the x values are scaled in place by
+// 2^(88-c), c = 4*(high nibble) + 8*(odd byte), the bit offsets at which
+// q4k_block finds each nibble.  The scaling is exact for |x| < 2^40; larger
+// values overflow to inf.  Callers that write x in smem must fence it
+// against the next bulk copy into the same slot.
+template <int MT, int CVT>
+__device__ __forceinline__ void q4k_stage_x(float* xb, int64_t xstride, float* sx, int M, int lane) {
+#pragma unroll
+    for (int m = 0; m < MT; ++m) {
+        if (MT == 1 || m < M) {
+            float* xp = xb + m * xstride + (lane >> 2) * 32 + (lane & 3) * 8;
+            float4 a = *reinterpret_cast<const float4*>(xp);
+            float4 b = *reinterpret_cast<const float4*>(xp + 4);
+            float sm = ((a.x + a.y) + (a.z + a.w)) + ((b.x + b.y) + (b.z + b.w));
+            sm += __shfl_xor_sync(0xffffffffu, sm, 1);
+            sm += __shfl_xor_sync(0xffffffffu, sm, 2);
+            if ((lane & 3) == 0) sx[m * 8 + (lane >> 2)] = sm;
+            if constexpr (CVT == 3) {
+                const float se = ((lane >> 2) & 1) ? 0x1p84f : 0x1p88f;   // even byte
+                const float so = se * 0x1p-8f;                            // odd byte
+                a = make_float4(a.x * se, a.y * so, a.z * se, a.w * so);
+                b = make_float4(b.x * se, b.y * so, b.z * se, b.w * so);
+                *reinterpret_cast<float4*>(xp) = a;
+                *reinterpret_cast<float4*>(xp + 4) = b;
+            }
+        }
     }
 }
 
@@ -195,6 +245,29 @@ __device__ __forceinline__ void q4k_block(const uint8_t* blk, const float* xb, i
                             fma2<PACKED>(ah[m], h23, f2{xh.z, xh.w});
                         }
                     }
+                } else if constexpr (CVT == 3) {
+                    // Nibbles as fp32 subnormals, masked in place: v & 0xF is
+                    // q*2^-149, v & 0xF0 is q*2^-145, v & 0xF00 q*2^-141,
+                    // v & 0xF000 q*2^-137 (bytes 2, 3 the same from v >> 16).
+                    // x was pre-scaled by 2^(88-c) for the nibble's offset c
+                    // (q4k_stage_x), so every product is q*x*2^-61, a normal
+                    // fp32 for |q*x| >= 2^-65: the FMA rounds as usual.
+                    const uint32_t v = qv[e], u = v >> 16;
+                    const f2 l01{__uint_as_float(v & 0xFu), __uint_as_float(v & 0xF00u)};
+                    const f2 l23{__uint_as_float(u & 0xFu), __uint_as_float(u & 0xF00u)};
+                    const f2 h01{__uint_as_float(v & 0xF0u), __uint_as_float(v & 0xF000u)};
+                    const f2 h23{__uint_as_float(u & 0xF0u), __uint_as_float(u & 0xF000u)};
+#pragma unroll
+                    for (int m = 0; m < MT; ++m) {
+                        if (MT == 1 || m < M) {
+                            const float4 xl = *reinterpret_cast<const float4*>(xb + m * xstride + kl);
+                            const float4 xh = *reinterpret_cast<const float4*>(xb + m * xstride + kl + 32);
+                            fma2<PACKED>(al[m], l01, f2{xl.x, xl.y});
+                            fma2<PACKED>(al[m], l23, f2{xl.z, xl.w});
+                            fma2<PACKED>(ah[m], h01, f2{xh.x, xh.y});
+                            fma2<PACKED>(ah[m], h23, f2{xh.z, xh.w});
+                        }
+                    }
                 } else if constexpr (CVT == 0) {
                     const uint32_t v = qv[e], v8 = v >> 8;
                     const uint32_t A = (v & 0x000F000Fu) | 0x64006400u;   // bytes 0,2 low nibbles
@@ -248,7 +321,10 @@ __device__ __forceinline__ void q4k_block(const uint8_t* blk, const float* xb, i
 #pragma unroll
         for (int m = 0; m < MT; ++m) {
             if (MT == 1 || m < M) {
-                if constexpr (CVT == 2) {
+                if constexpr (CVT == 3) {
+                    acc[m] = fmaf(dl * 0x1p61f, al[m].x + al[m].y, acc[m]);
+                    acc[m] = fmaf(dh * 0x1p65f, ah[m].x + ah[m].y, acc[m]);        // dh has 1/16
+                } else if constexpr (CVT == 2) {
                     acc[m] = fmaf(dl * 16777216.f, al[m].x + al[m].y, acc[m]);     // 2^24
                     acc[m] = fmaf(dh * 16777216.f, ah[m].x + ah[m].y, acc[m]);     // dh has 1/16: 2^20 * 16
                 } else if constexpr (CVT == 0) {
@@ -263,6 +339,90 @@ __device__ __forceinline__ void q4k_block(const uint8_t* blk, const float* xb, i
     }
 #pragma unroll
     for (int m = 0; m < MT; ++m) acc[m] -= mt[m];
+}
+
+// R rows of one Q4_K super-block column against MT tokens, x shared: row j's
+// block is at blk + j*rstride (smem).  Same arithmetic as q4k_block with
+// CVT == 3 (x pre-scaled by q4k_stage_x); one x load serves R rows.
+template <int MT, int R>
+__device__ __forceinline__ void q4k_block_rows(const uint8_t* blk, int rstride, const float* xb, int64_t xstride,
+                                               const float* sx, int M, float (&acc)[R][MT]) {
+    float d[R], dmin[R];
+    uint32_t sc03[R], mn03[R], sc47[R], mn47[R];
+#pragma unroll
+    for (int j = 0; j < R; ++j) {
+        const uint4 h = *reinterpret_cast<const uint4*>(blk + j * rstride);
+        d[j] = h2f(h.x);
+        dmin[j] = h2f(h.x >> 16);
+        q4k_scale_min_words(h.y, h.z, h.w, sc03[j], mn03[j], sc47[j], mn47[j]);
+    }
+#pragma unroll
+    for (int j = 0; j < R; ++j) {
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            const float dmn = dmin[j] * byte_f(k < 4 ? mn03[j] : mn47[j], k & 3);
+#pragma unroll
+            for (int m = 0; m < MT; ++m)
+                if (MT == 1 || m < M) acc[j][m] = fmaf(-dmn, sx[m * 8 + k], acc[j][m]);
+        }
+    }
+#pragma unroll
+    for (int g = 0; g < 4; ++g) {
+        f2 al[R][MT], ah[R][MT];
+#pragma unroll
+        for (int j = 0; j < R; ++j)
+#pragma unroll
+            for (int m = 0; m < MT; ++m) al[j][m] = ah[j][m] = f2{0.f, 0.f};
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+            uint4 q[R];
+#pragma unroll
+            for (int j = 0; j < R; ++j) q[j] = *reinterpret_cast<const uint4*>(blk + j * rstride + 16 + 32 * g + 16 * hh);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int kl = 64 * g + 16 * hh + 4 * e;
+                float4 xl[MT], xh[MT];
+#pragma unroll
+                for (int m = 0; m < MT; ++m) {
+                    if (MT == 1 || m < M) {
+                        xl[m] = *reinterpret_cast<const float4*>(xb + m * xstride + kl);
+                        xh[m] = *reinterpret_cast<const float4*>(xb + m * xstride + kl + 32);
+                    }
+                }
+#pragma unroll
+                for (int j = 0; j < R; ++j) {
+                    const uint32_t v = e == 0 ? q[j].x : e == 1 ? q[j].y : e == 2 ? q[j].z : q[j].w;
+                    const uint32_t u = v >> 16;
+                    const f2 l01{__uint_as_float(v & 0xFu), __uint_as_float(v & 0xF00u)};
+                    const f2 l23{__uint_as_float(u & 0xFu), __uint_as_float(u & 0xF00u)};
+                    const f2 h01{__uint_as_float(v & 0xF0u), __uint_as_float(v & 0xF000u)};
+                    const f2 h23{__uint_as_float(u & 0xF0u), __uint_as_float(u & 0xF000u)};
+#pragma unroll
+                    for (int m = 0; m < MT; ++m) {
+                        if (MT == 1 || m < M) {
+                            ffma2(al[j][m], l01, f2{xl[m].x, xl[m].y});
+                            ffma2(al[j][m], l23, f2{xl[m].z, xl[m].w});
+                            ffma2(ah[j][m], h01, f2{xh[m].x, xh[m].y});
+                            ffma2(ah[j][m], h23, f2{xh[m].z, xh[m].w});
+                        }
+                    }
+                }
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < R; ++j) {
+            const uint32_t scw = g < 2 ? sc03[j] : sc47[j];
+            const float dl = d[j] * byte_f(scw, (2 * g) & 3) * 0x1p61f;
+            const float dh = d[j] * byte_f(scw, (2 * g + 1) & 3) * 0x1p61f;
+#pragma unroll
+            for (int m = 0; m < MT; ++m) {
+                if (MT == 1 || m < M) {
+                    acc[j][m] = fmaf(dl, al[j][m].x + al[j][m].y, acc[j][m]);
+                    acc[j][m] = fmaf(dh, ah[j][m].x + ah[j][m].y, acc[j][m]);
+                }
+            }
+        }
+    }
 }
 
 // Load the IQ3 super-block at byte COL*98 of a 16-byte aligned row chunk in
@@ -362,8 +522,8 @@ __device__ __forceinline__ void named_barrier_sync(int id) {
 // Threads: RG*8 consumer warps, then one producer warp.
 template <class F, int MT, bool XS, int RG, bool PACKED, int MINB, int CVT = 2>
 __global__ void __launch_bounds__(RG * kCols * 32 + 32, MINB)
-    gemv_kernel(const __grid_constant__ Group G, const uint8_t* __restrict__ grid, const float* __restrict__ X, int M,
-                int64_t K, int stages, unsigned* status, int flags) {
+    gemv_kernel(const __grid_constant__ Group G, const __grid_constant__ TMaps T, const uint8_t* __restrict__ grid,
+                const float* __restrict__ X, int M, int64_t K, int stages, unsigned* status, int flags) {
     constexpr int kWarps = RG * kCols;          // consumer warps
     constexpr int kConsumerThreads = kWarps * 32;
     constexpr int kTileRows = RG * kRows;
@@ -444,6 +604,19 @@ __global__ void __launch_bounds__(RG * kCols * 32 + 32, MINB)
         auto post = [&](const Pos& p, bool do_w, bool do_x, bool expect) {
             const int kc = min(kCols, nb - p.c * kCols);
             uint8_t* st = smem + L.stage0 + p.s * L.stage_bytes;
+            if constexpr (F::kTMA) {
+                // kc boxes of 144 B x kTileRows; rows past N arrive as zeros
+                // and count in full toward the transaction bytes.
+                constexpr uint32_t kBox = kTileRows * F::kBytes;
+                if (expect) {
+                    if (lane == 0) mbar_arrive_expect_tx(&full[p.s], kc * kBox + (XS ? M * kc * 1024 : 0));
+                    __syncwarp();
+                }
+                if (do_w && lane == 0)
+                    for (int b = 0; b < kc; ++b)
+                        tma_load_2d(st + b * kBox, &T.m[p.gi], (p.c * kCols + b) * F::kBytes,
+                                    static_cast<int>(p.row0), &full[p.s], pol_w);
+            } else {
             if (expect) {
                 const uint32_t bytes = p.rows * kc * F::kBytes + (XS ? M * kc * 1024 : 0);
                 if (lane == 0) mbar_arrive_expect_tx(&full[p.s], bytes);
@@ -453,6 +626,7 @@ __global__ void __launch_bounds__(RG * kCols * 32 + 32, MINB)
                 const uint8_t* src = G.W[p.gi] + p.row0 * pitch + static_cast<int64_t>(p.c) * kCols * F::kBytes;
                 for (int r = lane; r < p.rows; r += 32)
                     bulk_g2s(st + r * F::kRowStride, src + r * pitch, kc * F::kBytes, &full[p.s], pol_w);
+            }
             }
             if (XS && do_x && lane < M)
                 bulk_g2s(st + L.xoff + lane * kCols * 1024, X + lane * K + static_cast<int64_t>(p.c) * kCols * 256,
@@ -513,21 +687,14 @@ __global__ void __launch_bounds__(RG * kCols * 32 + 32, MINB)
             const float* xb = XS ? reinterpret_cast<const float*>(st + L.xoff) + cw * 256 : X + b * 256;
             const int64_t xstride = XS ? kCols * 256 : K;
             if constexpr (!F::kIQ3) {
+                static_assert(CVT != 3 || (XS && RG == 1), "in-place x scaling needs x in smem, one warp per column");
                 float* sxp = sxw + warp * MT * 8;
-#pragma unroll
-                for (int m = 0; m < MT; ++m) {
-                    if (MT == 1 || m < M) {
-                        const float* xp = xb + m * xstride + (lane >> 2) * 32 + (lane & 3) * 8;
-                        const float4 a = *reinterpret_cast<const float4*>(xp);
-                        const float4 bb = *reinterpret_cast<const float4*>(xp + 4);
-                        float sm = ((a.x + a.y) + (a.z + a.w)) + ((bb.x + bb.y) + (bb.z + bb.w));
-                        sm += __shfl_xor_sync(0xffffffffu, sm, 1);
-                        sm += __shfl_xor_sync(0xffffffffu, sm, 2);
-                        if ((lane & 3) == 0) sxp[m * 8 + (lane >> 2)] = sm;
-                    }
-                }
+                q4k_stage_x<MT, CVT>(const_cast<float*>(xb), xstride, sxp, M, lane);
                 __syncwarp();
-                if (r < rows) q4k_block<MT, PACKED, CVT>(st + r * F::kRowStride + cw * F::kBytes, xb, xstride, sxp, M, acc);
+                const uint8_t* blk = F::kTMA ? st + cw * (kTileRows * F::kBytes) + r * F::kBytes
+                                             : st + r * F::kRowStride + cw * F::kBytes;
+                if (r < rows) q4k_block<MT, PACKED, CVT>(blk, xb, xstride, sxp, M, acc);
+                if constexpr (CVT == 3) fence_proxy_async_smem();  // x was written: order it before the slot's next copy
             } else {
                 if (r < rows) {
                     const uint8_t* rowp = st + r * F::kRowStride;

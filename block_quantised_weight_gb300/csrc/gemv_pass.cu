@@ -166,21 +166,11 @@ __global__ void __launch_bounds__(kCols * 32 + 32, 2)
                         const float* xb = reinterpret_cast<const float*>(st + L.xoff) + cw * 256;
                         constexpr int64_t xstride = kCols * 256;
                         float* sxp = sxw + warp * MT * 8;
-#pragma unroll
-                        for (int m = 0; m < MT; ++m) {
-                            if (MT == 1 || m < M) {
-                                const float* xp = xb + m * xstride + (lane >> 2) * 32 + (lane & 3) * 8;
-                                const float4 a = *reinterpret_cast<const float4*>(xp);
-                                const float4 bb = *reinterpret_cast<const float4*>(xp + 4);
-                                float sm = ((a.x + a.y) + (a.z + a.w)) + ((bb.x + bb.y) + (bb.z + bb.w));
-                                sm += __shfl_xor_sync(0xffffffffu, sm, 1);
-                                sm += __shfl_xor_sync(0xffffffffu, sm, 2);
-                                if ((lane & 3) == 0) sxp[m * 8 + (lane >> 2)] = sm;
-                            }
-                        }
+                        q4k_stage_x<MT, 3>(const_cast<float*>(xb), xstride, sxp, M, lane);
                         __syncwarp();
                         if (lane < rows)
-                            q4k_block<MT, true, 2>(st + lane * F::kRowStride + cw * F::kBytes, xb, xstride, sxp, M, acc);
+                            q4k_block<MT, true, 3>(st + lane * F::kRowStride + cw * F::kBytes, xb, xstride, sxp, M, acc);
+                        fence_proxy_async_smem();  // x was written: order it before the slot's next copy
                     }
                     __syncwarp();
                     if (lane == 0) mbar_arrive(&empty[s]);

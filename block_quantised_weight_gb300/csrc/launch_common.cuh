@@ -4,6 +4,7 @@
 
 #include "gemv_kernel.cuh"
 #include "launch.h"
+#include "tensor_map.h"
 
 namespace qg {
 
@@ -52,13 +53,20 @@ int launch_gemv(const uint8_t* const* W, float* const* Y, const int64_t* N, int 
         G.N[i] = N[i];
         G.tile0[i + 1] = G.tile0[i] + (N[i] + RG * kRows - 1) / (RG * kRows);
     }
+    TMaps T = {};
+    if constexpr (F::kTMA) {
+        const uint64_t pitch = static_cast<uint64_t>(K / 256) * F::kBytes;
+        for (int i = 0; i < count; ++i)
+            if (!encode_byte_rows(&T.m[i], W[i], pitch, static_cast<uint64_t>(N[i]), F::kBytes, RG * kRows))
+                return QG_ECUDA;
+    }
     const int64_t ntiles = G.tile0[count];
     const int sms = sm_count(dev);
     if (sms <= 0) return QG_ECUDA;
     const int grid_x = static_cast<int>(std::min<int64_t>(ntiles, static_cast<int64_t>(sms) * MINB));
     const int kflags = (flags & QG_PREFETCH_WEIGHTS) ? kFlagPrefetchWeights : 0;
     if (!(flags & QG_PREFETCH_WEIGHTS)) {
-        kern<<<grid_x, RG * kCols * 32 + 32, L.total, s>>>(G, grid, X, M, K, stages, status, kflags);
+        kern<<<grid_x, RG * kCols * 32 + 32, L.total, s>>>(G, T, grid, X, M, K, stages, status, kflags);
         return cudaGetLastError() == cudaSuccess ? QG_OK : QG_ECUDA;
     }
     // programmatic dependent launch: this grid may start before the previous
@@ -73,7 +81,7 @@ int launch_gemv(const uint8_t* const* W, float* const* Y, const int64_t* N, int 
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if (cudaLaunchKernelEx(&cfg, kern, G, grid, X, M, K, stages, status, kflags) != cudaSuccess) return QG_ECUDA;
+    if (cudaLaunchKernelEx(&cfg, kern, G, T, grid, X, M, K, stages, status, kflags) != cudaSuccess) return QG_ECUDA;
     return cudaGetLastError() == cudaSuccess ? QG_OK : QG_ECUDA;
 }
 

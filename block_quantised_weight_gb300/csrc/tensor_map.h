@@ -1,0 +1,42 @@
+// Host-side construction of TMA tensor maps (cuTensorMapEncodeTiled, reached
+// through the runtime's driver entry-point query: no link against libcuda).
+#pragma once
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+namespace qg {
+
+inline PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (!fn) {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) !=
+                cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            return nullptr;
+        fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    }
+    return fn;
+}
+
+// A quantised matrix viewed as bytes [rows][pitch]; box = box_bytes x
+// box_rows, no swizzle, reads outside the matrix fill zeros.  pitch and the
+// base address must be multiples of 16.  Returns false if encoding fails.
+inline bool encode_byte_rows(CUtensorMap* map, const uint8_t* base, uint64_t pitch, uint64_t rows,
+                             uint32_t box_bytes, uint32_t box_rows) {
+    auto encode = tensor_map_encoder();
+    if (!encode) return false;
+    const cuuint64_t gdim[2] = {pitch, rows};
+    const cuuint64_t gstride[1] = {pitch};
+    const cuuint32_t box[2] = {box_bytes, box_rows};
+    const cuuint32_t estr[2] = {1, 1};
+    return encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(base), gdim, gstride, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace qg

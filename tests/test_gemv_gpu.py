@@ -369,3 +369,18 @@ def test_tinyllama_pass_kernel_matches_groups(q):
         for y, yr in zip(Ys, q.qgemv_q4k_group(Ws, X)):
             assert torch.equal(y, yr)
     assert q.qg_device_status() == q.QG_OK
+
+
+@pytest.mark.parametrize("scale", [2.0 ** 36, 2.0 ** -60])
+@pytest.mark.parametrize("M", [1, 4])
+def test_gemv_q4k_x_range(q, scale, M):
+    """The M <= 4 Q4_K path scales x by powers of two up to 2^88 in shared
+    memory, so |x| must stay below 2^40: activations from about 2^-60 up to
+    2^39 (gen_x draws |x| < 4 here, times 2^36) still meet the fp32 tolerance."""
+    N, K = 96, 2048
+    W = synth.gen_q4k(N, K, 31)
+    x = synth.gen_x(M, K, 32) * np.float32(scale)
+    Y, A = oracle.gemv_q4k(W, x)
+    y = q.qgemv_q4k(dev(W), dev(x)).cpu().numpy()
+    assert np.isfinite(y).all()
+    check_tol(y, Y, A, TAU_FMA, f"x scale {scale:g}, M={M}")
