@@ -425,6 +425,94 @@ __device__ __forceinline__ void q4k_block_rows(const uint8_t* blk, int rstride, 
     }
 }
 
+// Half of one Q4_K super-block column for two rows (CVT 4, x pre-scaled as
+// for CVT 3).  Lane L of a warp takes rows L&15 and (L&15)+16 of the tile and
+// half h = L>>4 of the block (sub-blocks 4h..4h+3, weights 128h..128h+127),
+// so every x load serves two rows; the two halves of a row meet with one
+// shuffle at the end of the tile.  blk: the row-(L&15) block in smem;
+// rstride: bytes from a row to the row 16 below.  The min term
+// dmin*mn*sum(x) is taken first, then the scaled sub-block sums.
+template <int MT>
+__device__ __forceinline__ void q4k_half2(const uint8_t* blk, int rstride, int h, const float* xb, int64_t xstride,
+                                          const float* sx, int M, float (&acc)[2][MT]) {
+    float d61[2];
+    uint32_t scw[2];
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+        const uint4 hd = *reinterpret_cast<const uint4*>(blk + j * rstride);
+        d61[j] = h2f(hd.x) * 0x1p61f;
+        const float dmin = h2f(hd.x >> 16);
+        // scales / mins of sub-blocks 4h..4h+3 (page 1 packing: j >= 4 straddles)
+        scw[j] = h ? ((hd.w & 0x0F0F0F0Fu) | ((hd.y >> 2) & 0x30303030u)) : (hd.y & 0x3F3F3F3Fu);
+        const uint32_t mnw = h ? (((hd.w >> 4) & 0x0F0F0F0Fu) | ((hd.z >> 2) & 0x30303030u)) : (hd.z & 0x3F3F3F3Fu);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const float dmn = dmin * byte_f(mnw, k);
+#pragma unroll
+            for (int m = 0; m < MT; ++m)
+                if (MT == 1 || m < M) acc[j][m] = fmaf(-dmn, sx[m * 8 + 4 * h + k], acc[j][m]);
+        }
+    }
+    const uint8_t* qb = blk + 16 + 64 * h;
+    const float* xq = xb + 128 * h;
+#pragma unroll
+    for (int g = 0; g < 2; ++g) {
+        f2 al[2][MT], ah[2][MT];
+#pragma unroll
+        for (int j = 0; j < 2; ++j)
+#pragma unroll
+            for (int m = 0; m < MT; ++m) al[j][m] = ah[j][m] = f2{0.f, 0.f};
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+            uint4 q[2];
+#pragma unroll
+            for (int j = 0; j < 2; ++j) q[j] = *reinterpret_cast<const uint4*>(qb + j * rstride + 32 * g + 16 * hh);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int kl = 64 * g + 16 * hh + 4 * e;  // weights kl..kl+3 (low nibbles), +32 (high)
+                float4 xl[MT], xh[MT];
+#pragma unroll
+                for (int m = 0; m < MT; ++m) {
+                    if (MT == 1 || m < M) {
+                        xl[m] = *reinterpret_cast<const float4*>(xq + m * xstride + kl);
+                        xh[m] = *reinterpret_cast<const float4*>(xq + m * xstride + kl + 32);
+                    }
+                }
+#pragma unroll
+                for (int j = 0; j < 2; ++j) {
+                    const uint32_t v = e == 0 ? q[j].x : e == 1 ? q[j].y : e == 2 ? q[j].z : q[j].w;
+                    const uint32_t u = v >> 16;
+                    const f2 l01{__uint_as_float(v & 0xFu), __uint_as_float(v & 0xF00u)};
+                    const f2 l23{__uint_as_float(u & 0xFu), __uint_as_float(u & 0xF00u)};
+                    const f2 h01{__uint_as_float(v & 0xF0u), __uint_as_float(v & 0xF000u)};
+                    const f2 h23{__uint_as_float(u & 0xF0u), __uint_as_float(u & 0xF000u)};
+#pragma unroll
+                    for (int m = 0; m < MT; ++m) {
+                        if (MT == 1 || m < M) {
+                            ffma2(al[j][m], l01, f2{xl[m].x, xl[m].y});
+                            ffma2(al[j][m], l23, f2{xl[m].z, xl[m].w});
+                            ffma2(ah[j][m], h01, f2{xh[m].x, xh[m].y});
+                            ffma2(ah[j][m], h23, f2{xh[m].z, xh[m].w});
+                        }
+                    }
+                }
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            const float dl = d61[j] * byte_f(scw[j], 2 * g);
+            const float dh = d61[j] * byte_f(scw[j], 2 * g + 1);
+#pragma unroll
+            for (int m = 0; m < MT; ++m) {
+                if (MT == 1 || m < M) {
+                    acc[j][m] = fmaf(dl, al[j][m].x + al[j][m].y, acc[j][m]);
+                    acc[j][m] = fmaf(dh, ah[j][m].x + ah[j][m].y, acc[j][m]);
+                }
+            }
+        }
+    }
+}
+
 // Load the IQ3 super-block at byte COL*98 of a 16-byte aligned row chunk in
 // smem and realign it: v[i] = block bytes 4i..4i+3 (i < 24: the 64 index
 // bytes and the eight sign/scale words), d = the fp16 at block byte 96.
@@ -657,9 +745,12 @@ __global__ void __launch_bounds__(RG * kCols * 32 + 32, MINB)
     // ---------------- consumer warps
     if (prefetch) grid_dependency_wait();  // x and Y belong to the dependency chain
     const int rg = warp / kCols, cw = warp % kCols;
+    // CVT 4: two rows per lane (acc2[j]: row (lane&15) + 16j, half lane>>4)
+    constexpr bool kHalf2 = (CVT == 4);
     float acc[MT];
+    float acc2[2][MT];
 #pragma unroll
-    for (int m = 0; m < MT; ++m) acc[m] = 0.f;
+    for (int m = 0; m < MT; ++m) acc[m] = acc2[0][m] = acc2[1][m] = 0.f;
     const uint32_t lane4 = static_cast<uint32_t>(lane) * 4u;
     int64_t tile_count = 0;
 
@@ -687,14 +778,20 @@ __global__ void __launch_bounds__(RG * kCols * 32 + 32, MINB)
             const float* xb = XS ? reinterpret_cast<const float*>(st + L.xoff) + cw * 256 : X + b * 256;
             const int64_t xstride = XS ? kCols * 256 : K;
             if constexpr (!F::kIQ3) {
-                static_assert(CVT != 3 || (XS && RG == 1), "in-place x scaling needs x in smem, one warp per column");
+                static_assert(CVT < 3 || (XS && RG == 1), "in-place x scaling needs x in smem, one warp per column");
+                static_assert(CVT != 4 || F::kTMA, "two-row decode reads the tensor-map layout");
                 float* sxp = sxw + warp * MT * 8;
-                q4k_stage_x<MT, CVT>(const_cast<float*>(xb), xstride, sxp, M, lane);
+                q4k_stage_x<MT, CVT == 4 ? 3 : CVT>(const_cast<float*>(xb), xstride, sxp, M, lane);
                 __syncwarp();
-                const uint8_t* blk = F::kTMA ? st + cw * (kTileRows * F::kBytes) + r * F::kBytes
-                                             : st + r * F::kRowStride + cw * F::kBytes;
-                if (r < rows) q4k_block<MT, PACKED, CVT>(blk, xb, xstride, sxp, M, acc);
-                if constexpr (CVT == 3) fence_proxy_async_smem();  // x was written: order it before the slot's next copy
+                if constexpr (kHalf2) {
+                    const uint8_t* blk = st + cw * (kTileRows * F::kBytes) + (lane & 15) * F::kBytes;
+                    q4k_half2<MT>(blk, 16 * F::kBytes, lane >> 4, xb, xstride, sxp, M, acc2);
+                } else {
+                    const uint8_t* blk = F::kTMA ? st + cw * (kTileRows * F::kBytes) + r * F::kBytes
+                                                 : st + r * F::kRowStride + cw * F::kBytes;
+                    if (r < rows) q4k_block<MT, PACKED, CVT>(blk, xb, xstride, sxp, M, acc);
+                }
+                if constexpr (CVT >= 3) fence_proxy_async_smem();  // x was written: order it before the slot's next copy
             } else {
                 if (r < rows) {
                     const uint8_t* rowp = st + r * F::kRowStride;
@@ -722,8 +819,16 @@ __global__ void __launch_bounds__(RG * kCols * 32 + 32, MINB)
             float* rb = red + (tile_count & 1) * (kWarps * MT * kRows);
 #pragma unroll
             for (int m = 0; m < MT; ++m) {
-                rb[(warp * MT + m) * kRows + lane] = acc[m];
-                acc[m] = 0.f;
+                if constexpr (kHalf2) {
+                    // lanes L and L^16 hold the two halves of rows L&15 and (L&15)+16
+                    const float s0 = acc2[0][m] + __shfl_xor_sync(0xffffffffu, acc2[0][m], 16);
+                    const float s1 = acc2[1][m] + __shfl_xor_sync(0xffffffffu, acc2[1][m], 16);
+                    rb[(warp * MT + m) * kRows + lane] = lane < 16 ? s0 : s1;
+                    acc2[0][m] = acc2[1][m] = 0.f;
+                } else {
+                    rb[(warp * MT + m) * kRows + lane] = acc[m];
+                    acc[m] = 0.f;
+                }
             }
             named_barrier_sync<kConsumerThreads>(1);
             for (int t = threadIdx.x; t < MT * kTileRows; t += kConsumerThreads) {

@@ -144,9 +144,9 @@ __global__ void __launch_bounds__(kCols * 32 + 32, 2)
     } else {
         // ---------------- consumer warps
         const int cw = warp;
-        float acc[MT];
+        float acc[2][MT];  // rows (lane&15) and (lane&15)+16, half lane>>4 of each block
 #pragma unroll
-        for (int m = 0; m < MT; ++m) acc[m] = 0.f;
+        for (int m = 0; m < MT; ++m) acc[0][m] = acc[1][m] = 0.f;
         int s = 0;
         uint32_t phase = 0;
         int64_t tile_count = 0;
@@ -168,8 +168,10 @@ __global__ void __launch_bounds__(kCols * 32 + 32, 2)
                         float* sxp = sxw + warp * MT * 8;
                         q4k_stage_x<MT, 3>(const_cast<float*>(xb), xstride, sxp, M, lane);
                         __syncwarp();
-                        if (lane < rows)
-                            q4k_block<MT, true, 3>(st + lane * F::kRowStride + cw * F::kBytes, xb, xstride, sxp, M, acc);
+                        // two rows per lane, half a block each (same arithmetic as the
+                        // single-launch GEMV; rows past the tile end are discarded)
+                        q4k_half2<MT>(st + (lane & 15) * F::kRowStride + cw * F::kBytes, 16 * F::kRowStride, lane >> 4,
+                                      xb, xstride, sxp, M, acc);
                         fence_proxy_async_smem();  // x was written: order it before the slot's next copy
                     }
                     __syncwarp();
@@ -178,8 +180,10 @@ __global__ void __launch_bounds__(kCols * 32 + 32, 2)
                         float* rb = red + (tile_count & 1) * (kWarps * MT * kRows);
 #pragma unroll
                         for (int m = 0; m < MT; ++m) {
-                            rb[(warp * MT + m) * kRows + lane] = acc[m];
-                            acc[m] = 0.f;
+                            const float s0 = acc[0][m] + __shfl_xor_sync(0xffffffffu, acc[0][m], 16);
+                            const float s1 = acc[1][m] + __shfl_xor_sync(0xffffffffu, acc[1][m], 16);
+                            rb[(warp * MT + m) * kRows + lane] = lane < 16 ? s0 : s1;
+                            acc[0][m] = acc[1][m] = 0.f;
                         }
                         named_barrier_sync<kConsumerThreads>(1);
                         for (int t = threadIdx.x; t < MT * kTileRows; t += kConsumerThreads) {
