@@ -46,23 +46,45 @@ constexpr int kSmemReserve = 1024;   // per-CTA system reservation
 // super-block column, landing as [tile rows][144 B] boxes (a unit is kCols
 // boxes); 144 B = 9 x 16 B, so eight lanes reading eight consecutive rows
 // with 16-byte loads hit eight distinct bank groups.
+// kCols of a format: super-block columns per unit = consumer warps per row
+// group.
+// Tensor-map formats load box kBoxBytes wide starting at the block's byte
+// offset rounded down to 16: Q4_K blocks (144 B = 9 x 16) start aligned; an
+// IQ3 block (98 B) starts 0..14 bytes into its 112-byte box.  112 B = 7 x 16
+// is also an odd multiple of 16, so rows stay conflict-free.
 struct FmtQ4K {
     static constexpr int kBytes = 144;
+    static constexpr int kCols = qg::kCols;
     static constexpr int kRowStride = kCols * 144 + 16;  // 1168 = 73 * 16 (odd)
     static constexpr bool kIQ3 = false;
     static constexpr bool kTMA = false;
+    static constexpr int kBoxBytes = 0;
 };
-struct FmtQ4KT {
+template <int C>
+struct FmtQ4KTc {
     static constexpr int kBytes = 144;
-    static constexpr int kRowStride = kCols * 144;  // bytes per tile row per unit (kCols boxes of 144 B)
+    static constexpr int kCols = C;
+    static constexpr int kRowStride = C * 144;  // bytes per tile row per unit (C boxes of 144 B)
     static constexpr bool kIQ3 = false;
     static constexpr bool kTMA = true;
+    static constexpr int kBoxBytes = 144;
 };
+using FmtQ4KT = FmtQ4KTc<kCols>;
 struct FmtIQ3 {
     static constexpr int kBytes = 98;
+    static constexpr int kCols = qg::kCols;
     static constexpr int kRowStride = kCols * 98;  // 784 = 49 * 16 (odd)
     static constexpr bool kIQ3 = true;
     static constexpr bool kTMA = false;
+    static constexpr int kBoxBytes = 0;
+};
+struct FmtIQ3T {
+    static constexpr int kBytes = 98;
+    static constexpr int kCols = qg::kCols;
+    static constexpr int kRowStride = kCols * 112;  // bytes per tile row per unit (kCols boxes of 112 B)
+    static constexpr bool kIQ3 = true;
+    static constexpr bool kTMA = true;
+    static constexpr int kBoxBytes = 112;
 };
 
 // IQ3 grid table in smem, lane-replicated so every gather is conflict-free:
@@ -105,9 +127,10 @@ __device__ __forceinline__ int group_find(const Group& G, int64_t tile) {
 }
 
 // Dynamic smem layout of gemv_kernel<F, MT, XS, RG> with `stages` stages.
-__host__ __device__ inline Layout make_layout(bool iq3, int MT, bool xs, int RG, int stages, int row_stride) {
+__host__ __device__ inline Layout make_layout(bool iq3, int MT, bool xs, int RG, int stages, int row_stride,
+                                              int cols = kCols) {
     Layout L;
-    const int warps = RG * kCols;
+    const int warps = RG * cols;
     L.full = 0;
     L.empty = 8 * kMaxStages;
     L.sx = 128;
@@ -115,7 +138,7 @@ __host__ __device__ inline Layout make_layout(bool iq3, int MT, bool xs, int RG,
     L.table = L.red + align_up(2 * warps * MT * kRows * 4, 128);
     L.stage0 = L.table + (iq3 ? kIQ3TableBytes : 0);
     L.xoff = align_up(RG * kRows * row_stride, 128);
-    L.stage_bytes = L.xoff + (xs ? MT * kCols * 1024 : 0);
+    L.stage_bytes = L.xoff + (xs ? MT * cols * 1024 : 0);
     L.total = L.stage0 + stages * L.stage_bytes;
     return L;
 }
@@ -609,17 +632,17 @@ __device__ __forceinline__ void named_barrier_sync(int id) {
 // ------------------------------------------------------------ the kernel
 // Threads: RG*8 consumer warps, then one producer warp.
 template <class F, int MT, bool XS, int RG, bool PACKED, int MINB, int CVT = 2>
-__global__ void __launch_bounds__(RG * kCols * 32 + 32, MINB)
+__global__ void __launch_bounds__(RG * F::kCols * 32 + 32, MINB)
     gemv_kernel(const __grid_constant__ Group G, const __grid_constant__ TMaps T, const uint8_t* __restrict__ grid,
                 const float* __restrict__ X, int M, int64_t K, int stages, unsigned* status, int flags) {
-    constexpr int kWarps = RG * kCols;          // consumer warps
+    constexpr int kWarps = RG * F::kCols;          // consumer warps
     constexpr int kConsumerThreads = kWarps * 32;
     constexpr int kTileRows = RG * kRows;
     extern __shared__ __align__(128) uint8_t smem[];
     const int nb = static_cast<int>(K / 256);
-    const int nchunks = (nb + kCols - 1) / kCols;
+    const int nchunks = (nb + F::kCols - 1) / F::kCols;
     const int64_t ntiles = G.tile0[G.count];
-    const Layout L = make_layout(F::kIQ3, MT, XS, RG, stages, F::kRowStride);
+    const Layout L = make_layout(F::kIQ3, MT, XS, RG, stages, F::kRowStride, F::kCols);
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.full);
     uint64_t* empty = reinterpret_cast<uint64_t*>(smem + L.empty);
     float* sxw = reinterpret_cast<float*>(smem + L.sx);
@@ -690,19 +713,20 @@ __global__ void __launch_bounds__(RG * kCols * 32 + 32, MINB)
             }
         };
         auto post = [&](const Pos& p, bool do_w, bool do_x, bool expect) {
-            const int kc = min(kCols, nb - p.c * kCols);
+            const int kc = min(F::kCols, nb - p.c * F::kCols);
             uint8_t* st = smem + L.stage0 + p.s * L.stage_bytes;
             if constexpr (F::kTMA) {
-                // kc boxes of 144 B x kTileRows; rows past N arrive as zeros
-                // and count in full toward the transaction bytes.
-                constexpr uint32_t kBox = kTileRows * F::kBytes;
+                // kc boxes of kBoxBytes x kTileRows; rows past N (and bytes past
+                // the row end) arrive as zeros and count in full toward the
+                // transaction bytes.
+                constexpr uint32_t kBox = kTileRows * F::kBoxBytes;
                 if (expect) {
                     if (lane == 0) mbar_arrive_expect_tx(&full[p.s], kc * kBox + (XS ? M * kc * 1024 : 0));
                     __syncwarp();
                 }
                 if (do_w && lane == 0)
                     for (int b = 0; b < kc; ++b)
-                        tma_load_2d(st + b * kBox, &T.m[p.gi], (p.c * kCols + b) * F::kBytes,
+                        tma_load_2d(st + b * kBox, &T.m[p.gi], ((p.c * F::kCols + b) * F::kBytes) & ~15,
                                     static_cast<int>(p.row0), &full[p.s], pol_w);
             } else {
             if (expect) {
@@ -711,13 +735,13 @@ __global__ void __launch_bounds__(RG * kCols * 32 + 32, MINB)
                 __syncwarp();
             }
             if (do_w) {
-                const uint8_t* src = G.W[p.gi] + p.row0 * pitch + static_cast<int64_t>(p.c) * kCols * F::kBytes;
+                const uint8_t* src = G.W[p.gi] + p.row0 * pitch + static_cast<int64_t>(p.c) * F::kCols * F::kBytes;
                 for (int r = lane; r < p.rows; r += 32)
                     bulk_g2s(st + r * F::kRowStride, src + r * pitch, kc * F::kBytes, &full[p.s], pol_w);
             }
             }
             if (XS && do_x && lane < M)
-                bulk_g2s(st + L.xoff + lane * kCols * 1024, X + lane * K + static_cast<int64_t>(p.c) * kCols * 256,
+                bulk_g2s(st + L.xoff + lane * F::kCols * 1024, X + lane * K + static_cast<int64_t>(p.c) * F::kCols * 256,
                          kc * 1024, &full[p.s], pol_x);
         };
         Pos p = first_pos();
@@ -744,7 +768,7 @@ __global__ void __launch_bounds__(RG * kCols * 32 + 32, MINB)
 
     // ---------------- consumer warps
     if (prefetch) grid_dependency_wait();  // x and Y belong to the dependency chain
-    const int rg = warp / kCols, cw = warp % kCols;
+    const int rg = warp / F::kCols, cw = warp % F::kCols;
     // CVT 4: two rows per lane (acc2[j]: row (lane&15) + 16j, half lane>>4)
     constexpr bool kHalf2 = (CVT == 4);
     float acc[MT];
@@ -768,15 +792,15 @@ __global__ void __launch_bounds__(RG * kCols * 32 + 32, MINB)
     };
     if (U > 0) load_tile();
     for (int64_t u = 0; u < U; ++u) {
-        const int kc = min(kCols, nb - c * kCols);
+        const int kc = min(F::kCols, nb - c * F::kCols);
         const uint8_t* st = smem + L.stage0 + s * L.stage_bytes;
         const int r = rg * kRows + lane;  // row within the tile
         mbar_wait_bounded(&full[s], phase, status);
 
         if (cw < kc) {
-            const int64_t b = static_cast<int64_t>(c) * kCols + cw;  // super-block column
+            const int64_t b = static_cast<int64_t>(c) * F::kCols + cw;  // super-block column
             const float* xb = XS ? reinterpret_cast<const float*>(st + L.xoff) + cw * 256 : X + b * 256;
-            const int64_t xstride = XS ? kCols * 256 : K;
+            const int64_t xstride = XS ? F::kCols * 256 : K;
             if constexpr (!F::kIQ3) {
                 static_assert(CVT < 3 || (XS && RG == 1), "in-place x scaling needs x in smem, one warp per column");
                 static_assert(CVT != 4 || F::kTMA, "two-row decode reads the tensor-map layout");
@@ -794,7 +818,12 @@ __global__ void __launch_bounds__(RG * kCols * 32 + 32, MINB)
                 if constexpr (CVT >= 3) fence_proxy_async_smem();  // x was written: order it before the slot's next copy
             } else {
                 if (r < rows) {
-                    const uint8_t* rowp = st + r * F::kRowStride;
+                    // row-copy layout: the row's kCols blocks back to back; TMA
+                    // layout: block cw's box, shifted so that rowp + (98*cw & ~15)
+                    // is the box row
+                    const uint8_t* rowp = F::kTMA ? st + cw * (kTileRows * F::kBoxBytes) + r * F::kBoxBytes -
+                                                        ((cw * F::kBytes) & ~15)
+                                                  : st + r * F::kRowStride;
                     const uint32_t* tbl = reinterpret_cast<const uint32_t*>(smem + L.table);
                     uint32_t v[24], dbits;
                     switch (cw) {
@@ -837,7 +866,7 @@ __global__ void __launch_bounds__(RG * kCols * 32 + 32, MINB)
                 if ((MT == 1 || m < M) && rr < rows) {
                     float sum = 0.f;
 #pragma unroll
-                    for (int w = 0; w < kCols; ++w) sum += rb[((g * kCols + w) * MT + m) * kRows + ln];
+                    for (int w = 0; w < F::kCols; ++w) sum += rb[((g * F::kCols + w) * MT + m) * kRows + ln];
                     G.Y[gi][m * Ni + row0 + rr] = sum;
                 }
             }

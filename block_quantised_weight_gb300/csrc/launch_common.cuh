@@ -34,10 +34,10 @@ int launch_gemv(const uint8_t* const* W, float* const* Y, const int64_t* N, int 
                 const float* X, int M, int64_t K, cudaStream_t s, unsigned* status, int dev, unsigned flags) {
     static bool attr_done[64];
     const int budget = std::min(kSmemPerCTA, kSmemPerSM / MINB - kSmemReserve);
-    const Layout L1 = make_layout(F::kIQ3, MT, XS, RG, 1, F::kRowStride);
+    const Layout L1 = make_layout(F::kIQ3, MT, XS, RG, 1, F::kRowStride, F::kCols);
     const int stages = std::min(kMaxStages, (budget - L1.stage0) / L1.stage_bytes);
     if (stages < 2) return QG_EINVAL;
-    const Layout L = make_layout(F::kIQ3, MT, XS, RG, stages, F::kRowStride);
+    const Layout L = make_layout(F::kIQ3, MT, XS, RG, stages, F::kRowStride, F::kCols);
     auto kern = gemv_kernel<F, MT, XS, RG, PACKED, MINB, CVT>;
     if (!attr_done[dev]) {
         if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L.total) != cudaSuccess)
@@ -57,7 +57,7 @@ int launch_gemv(const uint8_t* const* W, float* const* Y, const int64_t* N, int 
     if constexpr (F::kTMA) {
         const uint64_t pitch = static_cast<uint64_t>(K / 256) * F::kBytes;
         for (int i = 0; i < count; ++i)
-            if (!encode_byte_rows(&T.m[i], W[i], pitch, static_cast<uint64_t>(N[i]), F::kBytes, RG * kRows))
+            if (!encode_byte_rows(&T.m[i], W[i], pitch, static_cast<uint64_t>(N[i]), F::kBoxBytes, RG * kRows))
                 return QG_ECUDA;
     }
     const int64_t ntiles = G.tile0[count];
@@ -66,14 +66,14 @@ int launch_gemv(const uint8_t* const* W, float* const* Y, const int64_t* N, int 
     const int grid_x = static_cast<int>(std::min<int64_t>(ntiles, static_cast<int64_t>(sms) * MINB));
     const int kflags = (flags & QG_PREFETCH_WEIGHTS) ? kFlagPrefetchWeights : 0;
     if (!(flags & QG_PREFETCH_WEIGHTS)) {
-        kern<<<grid_x, RG * kCols * 32 + 32, L.total, s>>>(G, T, grid, X, M, K, stages, status, kflags);
+        kern<<<grid_x, RG * F::kCols * 32 + 32, L.total, s>>>(G, T, grid, X, M, K, stages, status, kflags);
         return cudaGetLastError() == cudaSuccess ? QG_OK : QG_ECUDA;
     }
     // programmatic dependent launch: this grid may start before the previous
     // kernel in the stream finishes; the kernel waits before reading x.
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid_x);
-    cfg.blockDim = dim3(RG * kCols * 32 + 32);
+    cfg.blockDim = dim3(RG * F::kCols * 32 + 32);
     cfg.dynamicSmemBytes = L.total;
     cfg.stream = s;
     cudaLaunchAttribute attr[1];
