@@ -80,7 +80,10 @@ extern "C" {
  * W: N*K/256*144 bytes.  X: M*K floats.  Y: M*N floats (output).
  * Numerics: |Y - exact| <= 1e-5 * sum_k |w*x| per element (fp32 FMA,
  * sub-block-factored sums).  M > 8 is processed in groups of 8 tokens, each
- * group streaming W once. */
+ * group streaming W once.  Range: for groups of up to 4 tokens the kernel
+ * scales x by powers of two up to 2^88 in shared memory, so every |x| must
+ * be below 2^40 (larger values give inf/NaN in Y); the same holds for
+ * qgemv_q4k_group and qgemv_q4k_pass. */
 QG_API int qgemv_q4k(const uint8_t* W, const float* X, float* Y, int M, int64_t N, int64_t K, cudaStream_t stream);
 
 /* qgemv_q4k with launch flags (0 or QG_PREFETCH_WEIGHTS); other flag bits:
