@@ -93,10 +93,14 @@ struct FmtIQ3T {
 constexpr int kIQ3TableBytes = 256 * 64 * 4;
 
 __host__ __device__ constexpr int align_up(int v, int a) { return (v + a - 1) / a * a; }
+
+// Split-K over a thread-block cluster: up to kMaxCluster CTAs share a tile,
+// one K chunk each, and meet in the first CTA's shared memory.
+constexpr int kMaxCluster = 8;
 __host__ __device__ inline int64_t min64(int64_t a, int64_t b) { return a < b ? a : b; }
 
 struct Layout {
-    int full, empty, sx, red, table, stage0, stage_bytes, xoff, total;
+    int full, empty, sx, red, cred, table, stage0, stage_bytes, xoff, total;
 };
 
 // Up to kMaxGroup matrices that share X and K, processed by one launch.
@@ -135,7 +139,8 @@ __host__ __device__ inline Layout make_layout(bool iq3, int MT, bool xs, int RG,
     L.empty = 8 * kMaxStages;
     L.sx = 128;
     L.red = L.sx + align_up(warps * MT * 8 * 4, 128);
-    L.table = L.red + align_up(2 * warps * MT * kRows * 4, 128);
+    L.cred = L.red + align_up(2 * warps * MT * kRows * 4, 128);
+    L.table = L.cred + align_up(kMaxCluster * MT * RG * kRows * 4, 128);
     L.stage0 = L.table + (iq3 ? kIQ3TableBytes : 0);
     L.xoff = align_up(RG * kRows * row_stride, 128);
     L.stage_bytes = L.xoff + (xs ? MT * cols * 1024 : 0);
@@ -620,6 +625,28 @@ __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
 // Launch flag: W and the grid are not written by the preceding kernel in the
 // stream, so they may be prefetched before the grid dependency is resolved.
 constexpr int kFlagPrefetchWeights = 1;
+// Launch flag bits 8-11: cluster size C > 1 (split-K over a cluster of C CTAs
+// per tile; the grid is ntiles * C, CTA rank r takes chunk r).
+constexpr int kFlagClusterShift = 8;
+
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+    asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_arrive_release() {
+    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory"); }
+// Store v at the same shared-memory offset as p in cluster CTA `rank`.
+__device__ __forceinline__ void st_cluster_f32(const void* p, uint32_t rank, float v) {
+    uint32_t a;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(a) : "r"(smem_u32(p)), "r"(rank));
+    asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(a), "f"(v) : "memory");
+}
 
 __device__ __forceinline__ void grid_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 __device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
@@ -678,9 +705,16 @@ __global__ void __launch_bounds__(RG * F::kCols * 32 + 32, MINB)
     }
     __syncthreads();
 
+    // Cluster split-K: this CTA takes chunk `crank` of tile blockIdx.x / csize.
+    const int csize = (flags >> kFlagClusterShift) & 15;
+    const bool clus = csize > 1;
+    const int crank = clus ? static_cast<int>(cluster_ctarank()) : 0;
+    const int64_t tile_first = clus ? blockIdx.x / csize : blockIdx.x;
+    if (clus) cluster_arrive_relaxed();  // phase 0: every CTA of the cluster has started
     const int64_t my_tiles =
-        static_cast<int64_t>(blockIdx.x) < ntiles ? (ntiles - 1 - blockIdx.x) / gridDim.x + 1 : 0;
-    const int64_t U = my_tiles * nchunks;
+        clus ? (tile_first < ntiles ? 1 : 0)
+             : (static_cast<int64_t>(blockIdx.x) < ntiles ? (ntiles - 1 - blockIdx.x) / gridDim.x + 1 : 0);
+    const int64_t U = clus ? my_tiles : my_tiles * nchunks;
 
     if (warp == kWarps) {
         // ---------------- producer warp
@@ -694,7 +728,7 @@ __global__ void __launch_bounds__(RG * F::kCols * 32 + 32, MINB)
             int gi, rows;
         };
         auto first_pos = [&]() {
-            Pos p{0, 0, static_cast<int64_t>(blockIdx.x), 0, 0, 0};
+            Pos p{0, crank, tile_first, 0, 0, 0};
             p.gi = group_find(G, p.tile);
             p.row0 = (p.tile - G.tile0[p.gi]) * kTileRows;
             p.rows = static_cast<int>(min64(kTileRows, G.N[p.gi] - p.row0));
@@ -763,6 +797,12 @@ __global__ void __launch_bounds__(RG * F::kCols * 32 + 32, MINB)
             post(p, true, true, true);
             if (p.s == stages - 1) ++round;
         }
+        if (clus) {  // the producer takes part in both cluster barrier phases
+            __syncwarp();
+            cluster_wait();
+            cluster_arrive_release();
+            cluster_wait();
+        }
         return;
     }
 
@@ -778,9 +818,9 @@ __global__ void __launch_bounds__(RG * F::kCols * 32 + 32, MINB)
     const uint32_t lane4 = static_cast<uint32_t>(lane) * 4u;
     int64_t tile_count = 0;
 
-    int s = 0, c = 0;
+    int s = 0, c = crank;
     uint32_t phase = 0;
-    int64_t tile = blockIdx.x;
+    int64_t tile = tile_first;
     int gi = 0;
     int64_t row0 = 0, Ni = 0;
     int rows = 0;
@@ -843,7 +883,7 @@ __global__ void __launch_bounds__(RG * F::kCols * 32 + 32, MINB)
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[s]);
 
-        if (c == nchunks - 1) {
+        if (clus || c == nchunks - 1) {
             // reduce the 8 column warps' partial sums of each row, write Y
             float* rb = red + (tile_count & 1) * (kWarps * MT * kRows);
 #pragma unroll
@@ -860,6 +900,34 @@ __global__ void __launch_bounds__(RG * F::kCols * 32 + 32, MINB)
                 }
             }
             named_barrier_sync<kConsumerThreads>(1);
+            if (clus) {
+                // this chunk's row sums -> slot crank of the first CTA; after the
+                // cluster barrier it adds the slots in rank order (deterministic)
+                float* cred = reinterpret_cast<float*>(smem + L.cred);
+                __syncwarp();
+                cluster_wait();  // phase 0: all CTAs of the cluster are running
+                for (int t = threadIdx.x; t < MT * kTileRows; t += kConsumerThreads) {
+                    const int m = t / kTileRows, rr = t % kTileRows;
+                    const int g = rr / kRows, ln = rr % kRows;
+                    float sum = 0.f;
+#pragma unroll
+                    for (int w = 0; w < F::kCols; ++w) sum += rb[((g * F::kCols + w) * MT + m) * kRows + ln];
+                    st_cluster_f32(cred + crank * MT * kTileRows + t, 0, sum);
+                }
+                __syncwarp();
+                cluster_arrive_release();
+                cluster_wait();
+                if (crank == 0) {
+                    for (int t = threadIdx.x; t < MT * kTileRows; t += kConsumerThreads) {
+                        const int m = t / kTileRows, rr = t % kTileRows;
+                        if ((MT == 1 || m < M) && rr < rows) {
+                            float sum = 0.f;
+                            for (int q = 0; q < csize; ++q) sum += cred[q * MT * kTileRows + t];
+                            G.Y[gi][m * Ni + row0 + rr] = sum;
+                        }
+                    }
+                }
+            } else {
             for (int t = threadIdx.x; t < MT * kTileRows; t += kConsumerThreads) {
                 const int m = t / kTileRows, rr = t % kTileRows;
                 const int g = rr / kRows, ln = rr % kRows;
@@ -869,6 +937,7 @@ __global__ void __launch_bounds__(RG * F::kCols * 32 + 32, MINB)
                     for (int w = 0; w < F::kCols; ++w) sum += rb[((g * F::kCols + w) * MT + m) * kRows + ln];
                     G.Y[gi][m * Ni + row0 + rr] = sum;
                 }
+            }
             }
             ++tile_count;
         }
@@ -882,6 +951,11 @@ __global__ void __launch_bounds__(RG * F::kCols * 32 + 32, MINB)
             tile += gridDim.x;
             if (tile < ntiles) load_tile();
         }
+    }
+    if (clus && U == 0) {  // no unit (never with grid = ntiles * C): still pass both phases
+        cluster_wait();
+        cluster_arrive_release();
+        cluster_wait();
     }
 }
 

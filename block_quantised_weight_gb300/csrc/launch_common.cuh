@@ -31,7 +31,8 @@ inline int sm_count(int dev) {
 // memory.
 template <class F, int MT, bool XS, int RG, bool PACKED, int MINB, int CVT = 2>
 int launch_gemv(const uint8_t* const* W, float* const* Y, const int64_t* N, int count, int m0, const uint8_t* grid,
-                const float* X, int M, int64_t K, cudaStream_t s, unsigned* status, int dev, unsigned flags) {
+                const float* X, int M, int64_t K, cudaStream_t s, unsigned* status, int dev, unsigned flags,
+                int csize = 1) {
     static bool attr_done[64];
     const int budget = std::min(kSmemPerCTA, kSmemPerSM / MINB - kSmemReserve);
     const Layout L1 = make_layout(F::kIQ3, MT, XS, RG, 1, F::kRowStride, F::kCols);
@@ -63,24 +64,40 @@ int launch_gemv(const uint8_t* const* W, float* const* Y, const int64_t* N, int 
     const int64_t ntiles = G.tile0[count];
     const int sms = sm_count(dev);
     if (sms <= 0) return QG_ECUDA;
-    const int grid_x = static_cast<int>(std::min<int64_t>(ntiles, static_cast<int64_t>(sms) * MINB));
-    const int kflags = (flags & QG_PREFETCH_WEIGHTS) ? kFlagPrefetchWeights : 0;
-    if (!(flags & QG_PREFETCH_WEIGHTS)) {
+    // csize > 1: one CTA per (tile, K chunk), the chunks of a tile in one
+    // cluster (the caller checks that the grid fits one wave).
+    const int grid_x = csize > 1 ? static_cast<int>(ntiles * csize)
+                                 : static_cast<int>(std::min<int64_t>(ntiles, static_cast<int64_t>(sms) * MINB));
+    const int kflags = ((flags & QG_PREFETCH_WEIGHTS) ? kFlagPrefetchWeights : 0) |
+                       (csize > 1 ? csize << kFlagClusterShift : 0);
+    if (!(flags & QG_PREFETCH_WEIGHTS) && csize <= 1) {
         kern<<<grid_x, RG * F::kCols * 32 + 32, L.total, s>>>(G, T, grid, X, M, K, stages, status, kflags);
         return cudaGetLastError() == cudaSuccess ? QG_OK : QG_ECUDA;
     }
-    // programmatic dependent launch: this grid may start before the previous
-    // kernel in the stream finishes; the kernel waits before reading x.
+    // programmatic dependent launch (this grid may start before the previous
+    // kernel in the stream finishes; the kernel waits before reading x) and/or
+    // a cluster launch
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid_x);
     cfg.blockDim = dim3(RG * F::kCols * 32 + 32);
     cfg.dynamicSmemBytes = L.total;
     cfg.stream = s;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchAttribute attr[2];
+    int na = 0;
+    if (flags & QG_PREFETCH_WEIGHTS) {
+        attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[na].val.programmaticStreamSerializationAllowed = 1;
+        ++na;
+    }
+    if (csize > 1) {
+        attr[na].id = cudaLaunchAttributeClusterDimension;
+        attr[na].val.clusterDim.x = csize;
+        attr[na].val.clusterDim.y = 1;
+        attr[na].val.clusterDim.z = 1;
+        ++na;
+    }
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = na;
     if (cudaLaunchKernelEx(&cfg, kern, G, T, grid, X, M, K, stages, status, kflags) != cudaSuccess) return QG_ECUDA;
     return cudaGetLastError() == cudaSuccess ? QG_OK : QG_ECUDA;
 }

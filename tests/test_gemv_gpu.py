@@ -345,7 +345,11 @@ def test_pass_kernel_dependent_stages(q, M):
 
 def test_tinyllama_pass_kernel_matches_groups(q):
     """The 89-stage TinyLlama pass (q/k/v and gate/up grouped) as one launch
-    equals the stage-by-stage grouped launches bit for bit."""
+    equals the stage-by-stage grouped launches: bit for bit where both add
+    the K chunks in the same order (one chunk, K = 2048); within twice the
+    fp32 tolerance where the grouped launch splits K over a cluster
+    (down projection, K = 5632, three chunks summed after their own
+    reductions)."""
     stages, ys_ref = [], []
     mats = synth.tinyllama_seeds(1)
     i = 0
@@ -366,8 +370,13 @@ def test_tinyllama_pass_kernel_matches_groups(q):
     sync = torch.zeros(89, dtype=torch.int32, device="cuda")
     q.qgemv_q4k_pass(stages, sync, M=1)
     for Ws, Ys, X in stages:
-        for y, yr in zip(Ys, q.qgemv_q4k_group(Ws, X)):
-            assert torch.equal(y, yr)
+        K = X.shape[-1]
+        for W, y, yr in zip(Ws, Ys, q.qgemv_q4k_group(Ws, X)):
+            if K <= 2048:
+                assert torch.equal(y, yr)
+            else:
+                scale = (q.qdequant_q4k(W, K).abs() @ X.reshape(1, K).abs().T).T  # sum|w*x|
+                assert bool(((y - yr).abs() <= 2 * TAU_FMA * scale).all())
     assert q.qg_device_status() == q.QG_OK
 
 
