@@ -77,9 +77,9 @@ int launch_group_iq3(const uint8_t* const* W, float* const* Y, const int64_t* N,
                 rc = cudaGetLastError() == cudaSuccess ? QG_OK : QG_ECUDA;
             }
         } else if (mg == 1) {
-            rc = launch_gemv<FmtIQ3T, 1, true, 2, true, 1>(W, Y, N, count, m0, grid, Xg, mg, K, s, status, dev, flags);
+            rc = launch_gemv<FmtIQ3T, 1, true, 2, true, 1, 4>(W, Y, N, count, m0, grid, Xg, mg, K, s, status, dev, flags);
         } else if (mg == 2) {
-            rc = launch_gemv<FmtIQ3T, 2, true, 2, true, 1>(W, Y, N, count, m0, grid, Xg, mg, K, s, status, dev, flags);
+            rc = launch_gemv<FmtIQ3T, 2, true, 1, true, 1, 4>(W, Y, N, count, m0, grid, Xg, mg, K, s, status, dev, flags);
         } else if (mg <= 4) {
             rc = launch_gemv<FmtIQ3T, 4, false, 1, true, 1>(W, Y, N, count, m0, grid, Xg, mg, K, s, status, dev, flags);
         } else {

@@ -87,10 +87,16 @@ struct FmtIQ3T {
     static constexpr int kBoxBytes = 112;
 };
 
-// IQ3 grid table in smem, lane-replicated so every gather is conflict-free:
-// for grid row i, lane L reads word 64*i + L (fp16 magnitudes 0,1) and word
-// 64*i + 32 + L (fp16 magnitudes 2,3).  64 KB, shared by all consumer warps.
-constexpr int kIQ3TableBytes = 256 * 64 * 4;
+// IQ3 tables in smem, shared by all consumer warps.
+// Grid: lane-replicated so every gather is conflict-free: for grid row i,
+// lane L reads the 8 bytes at 256*i + 8*L (fp16 magnitudes 0,1 then 2,3).
+// Signs: for each 7-bit sign field s7 one word T with the eight signs s8 (the
+// eighth = parity of the seven) placed so that (T << p) & 0x80008000 is the
+// sign mask of fp16 pair p (weights 2p, 2p+1): sign 2p at bit 15-p, sign
+// 2p+1 at bit 31-p.  Lane replicated: lane L reads word 32*s7 + L.
+constexpr int kIQ3GridBytes = 256 * 32 * 8;
+constexpr int kIQ3SignBytes = 128 * 32 * 4;
+constexpr int kIQ3TableBytes = kIQ3GridBytes + kIQ3SignBytes;
 
 __host__ __device__ constexpr int align_up(int v, int a) { return (v + a - 1) / a * a; }
 
@@ -566,18 +572,32 @@ __device__ __forceinline__ void iq3_load_block(const uint8_t* rowp, uint32_t (&v
     dbits = w[PD >> 2] >> (8 * (PD & 3));
 }
 
+// Sign word T of the sign field at bits 7l..7l+6 of sw (see kIQ3SignBytes);
+// lane4 = 4 * lane.
+__device__ __forceinline__ uint32_t iq3_signs(const uint8_t* sg, uint32_t sw, int l, uint32_t lane4) {
+    const uint32_t off = (l == 0 ? (sw << 7) : (sw >> (7 * l - 7))) & 0x3F80u;
+    return *reinterpret_cast<const uint32_t*>(sg + (off | lane4));
+}
+// fp16 pair p of the grid row, sign flipped by sign word T.
+__device__ __forceinline__ uint32_t iq3_flip(uint32_t g, uint32_t T, int p) { return g ^ ((T << p) & 0x80008000u); }
+
+// Grid row of the index byte `byte` of word w: 8 bytes (two fp16 pairs).
+__device__ __forceinline__ uint2 iq3_grid(const uint8_t* tb, uint32_t w, int byte, uint32_t lane8) {
+    const uint32_t off = prmt(w, lane8, 4u | (static_cast<uint32_t>(byte) << 4) | (5u << 8) | (5u << 12));
+    return *reinterpret_cast<const uint2*>(tb + off);
+}
+
 // One IQ3 super-block (realigned: v, d) against MT tokens.
 // Each 4-weight group gathers its grid row from the lane-replicated fp16
-// table (exact magnitudes), flips signs in the fp16 domain (sign bits moved
-// to bits 15/31 by one multiply; the shifted copies of the sign byte never
-// overlap, so there are no carries), converts to fp32 and FMAs.  The
-// sub-block factor d*(0.5+code)*0.5 and the grid's 0.5 are applied once per
-// 32 weights (exact: at most 16 significant bits).
+// table (exact magnitudes), flips signs in the fp16 domain with the masks of
+// the sign table (the implied eighth sign included), converts to fp32 and
+// FMAs.  The sub-block factor d*(0.5+code)*0.5 and the grid's 0.5 are
+// applied once per 32 weights (exact: at most 16 significant bits).
 template <int MT, bool PACKED>
-__device__ __forceinline__ void iq3_block(const uint32_t (&v)[24], uint32_t dbits, const uint32_t* tbl, uint32_t lane4,
-                                          const float* xb, int64_t xstride, int M, float (&acc)[MT]) {
+__device__ __forceinline__ void iq3_block(const uint32_t (&v)[24], uint32_t dbits, const uint8_t* tb, const uint8_t* sg,
+                                          uint32_t lane8, uint32_t lane4, const float* xb, int64_t xstride, int M,
+                                          float (&acc)[MT]) {
     const float d = h2f(dbits);
-    const uint8_t* tb = reinterpret_cast<const uint8_t*>(tbl);
 #pragma unroll
     for (int ib = 0; ib < 8; ++ib) {
         const uint32_t sw = v[16 + ib];
@@ -587,21 +607,13 @@ __device__ __forceinline__ void iq3_block(const uint32_t (&v)[24], uint32_t dbit
         for (int m = 0; m < MT; ++m) dot[m] = f2{0.f, 0.f};
 #pragma unroll
         for (int l = 0; l < 4; ++l) {
-            const uint32_t seven = (sw >> (7 * l)) & 0x7Fu;
-            const uint32_t s8 = seven | ((__popc(seven) & 1u) << 7);
+            const uint32_t T = iq3_signs(sg, sw, l, lane4);
 #pragma unroll
             for (int hf = 0; hf < 2; ++hf) {
                 const int PI = 8 * ib + 2 * l + hf;  // grid index byte of weights 8l+4hf..+3
-                const uint32_t off =
-                    prmt(v[PI >> 2], lane4, 4u | (static_cast<uint32_t>(PI & 3) << 4) | (5u << 8) | (5u << 12));
-                const uint32_t* tp = reinterpret_cast<const uint32_t*>(tb + off);
-                uint32_t h01 = tp[0], h23 = tp[32];
-                const uint32_t k01 = hf ? ((1u << 11) + (1u << 26)) : ((1u << 15) + (1u << 30));
-                const uint32_t k23 = hf ? ((1u << 9) + (1u << 24)) : ((1u << 13) + (1u << 28));
-                h01 ^= (s8 * k01) & 0x80008000u;
-                h23 ^= (s8 * k23) & 0x80008000u;
-                const f2 w01 = h2_to_f2(h01);
-                const f2 w23 = h2_to_f2(h23);
+                const uint2 g = iq3_grid(tb, v[PI >> 2], PI & 3, lane8);
+                const f2 w01 = h2_to_f2(iq3_flip(g.x, T, 2 * hf));
+                const f2 w23 = h2_to_f2(iq3_flip(g.y, T, 2 * hf + 1));
 #pragma unroll
                 for (int m = 0; m < MT; ++m) {
                     if (MT == 1 || m < M) {
@@ -615,6 +627,86 @@ __device__ __forceinline__ void iq3_block(const uint32_t (&v)[24], uint32_t dbit
 #pragma unroll
         for (int m = 0; m < MT; ++m)
             if (MT == 1 || m < M) acc[m] = fmaf(db, dot[m].x + dot[m].y, acc[m]);
+    }
+}
+
+// Half h of the IQ3 super-block of column COL from its 112-byte TMA box row
+// (the block starts (98*COL) mod 16 bytes in): vi = index bytes 32h..32h+31,
+// vs = sign/scale words 4h..4h+3, dbits = the fp16 d.
+template <int COL>
+__device__ __forceinline__ void iq3_load_half(const uint8_t* boxrow, int h, uint32_t (&vi)[8], uint32_t (&vs)[4],
+                                              uint32_t& dbits) {
+    constexpr int OFF = (COL * 98) & 15, W0 = OFF >> 2, SH = 8 * (OFF & 3);
+    uint32_t w[12];
+#pragma unroll
+    for (int i = 0; i < 3; ++i) {
+        const uint4 t = *reinterpret_cast<const uint4*>(boxrow + 32 * h + 16 * i);
+        w[4 * i] = t.x; w[4 * i + 1] = t.y; w[4 * i + 2] = t.z; w[4 * i + 3] = t.w;
+    }
+#pragma unroll
+    for (int i = 0; i < 8; ++i) vi[i] = SH ? __funnelshift_r(w[W0 + i], w[W0 + i + 1], SH) : w[W0 + i];
+    uint32_t u[8];
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+        const uint4 t = *reinterpret_cast<const uint4*>(boxrow + 64 + 16 * h + 16 * i);
+        u[4 * i] = t.x; u[4 * i + 1] = t.y; u[4 * i + 2] = t.z; u[4 * i + 3] = t.w;
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) vs[i] = SH ? __funnelshift_r(u[W0 + i], u[W0 + i + 1], SH) : u[W0 + i];
+    dbits = *reinterpret_cast<const uint32_t*>(boxrow + 96 + (OFF & ~3)) >> SH;
+}
+
+// Two rows (r, r+16), half h of an IQ3 super-block each, against MT tokens:
+// the layout of q4k_half2 (one x load serves both rows).  xq = x of the
+// block + 128h.
+template <int MT>
+__device__ __forceinline__ void iq3_half2(const uint32_t (&vi)[2][8], const uint32_t (&vs)[2][4], const uint32_t (&dbits)[2],
+                                          const uint8_t* tb, const uint8_t* sg, uint32_t lane8, uint32_t lane4,
+                                          const float* xq, int64_t xstride, int M, float (&acc)[2][MT]) {
+    float d[2];
+#pragma unroll
+    for (int r = 0; r < 2; ++r) d[r] = h2f(dbits[r]);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        f2 dot[2][MT];
+#pragma unroll
+        for (int r = 0; r < 2; ++r)
+#pragma unroll
+            for (int m = 0; m < MT; ++m) dot[r][m] = f2{0.f, 0.f};
+#pragma unroll
+        for (int l = 0; l < 4; ++l) {
+            uint32_t T[2];
+#pragma unroll
+            for (int r = 0; r < 2; ++r) T[r] = iq3_signs(sg, vs[r][j], l, lane4);
+#pragma unroll
+            for (int hf = 0; hf < 2; ++hf) {
+                const int PI = 8 * j + 2 * l + hf;  // index byte within the half
+                float4 x[MT];
+#pragma unroll
+                for (int m = 0; m < MT; ++m)
+                    if (MT == 1 || m < M) x[m] = *reinterpret_cast<const float4*>(xq + m * xstride + 32 * j + 8 * l + 4 * hf);
+#pragma unroll
+                for (int r = 0; r < 2; ++r) {
+                    const uint2 g = iq3_grid(tb, vi[r][PI >> 2], PI & 3, lane8);
+                    const f2 w01 = h2_to_f2(iq3_flip(g.x, T[r], 2 * hf));
+                    const f2 w23 = h2_to_f2(iq3_flip(g.y, T[r], 2 * hf + 1));
+#pragma unroll
+                    for (int m = 0; m < MT; ++m) {
+                        if (MT == 1 || m < M) {
+                            ffma2(dot[r][m], w01, f2{x[m].x, x[m].y});
+                            ffma2(dot[r][m], w23, f2{x[m].z, x[m].w});
+                        }
+                    }
+                }
+            }
+        }
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+            const float db = d[r] * (static_cast<float>(vs[r][j] >> 28) + 0.5f) * 0.25f;
+#pragma unroll
+            for (int m = 0; m < MT; ++m)
+                if (MT == 1 || m < M) acc[r][m] = fmaf(db, dot[r][m].x + dot[r][m].y, acc[r][m]);
+        }
     }
 }
 
@@ -695,12 +787,24 @@ __global__ void __launch_bounds__(RG * F::kCols * 32 + 32, MINB)
         // fp16 copies of the doubled-unit magnitudes (exact: bytes < 2048)
         uint32_t* tbl = reinterpret_cast<uint32_t*>(smem + L.table);
         for (int i = threadIdx.x; i < 256 * 32; i += blockDim.x) {
-            const int row = i >> 5, ln = i & 31;
+            const int row = i >> 5;
             const uint32_t g = *reinterpret_cast<const uint32_t*>(grid + 4 * row);
             const __half2 a = __floats2half2_rn(byte_f(g, 0), byte_f(g, 1));
             const __half2 b = __floats2half2_rn(byte_f(g, 2), byte_f(g, 3));
-            tbl[64 * row + ln] = *reinterpret_cast<const uint32_t*>(&a);
-            tbl[64 * row + 32 + ln] = *reinterpret_cast<const uint32_t*>(&b);
+            tbl[2 * i] = *reinterpret_cast<const uint32_t*>(&a);
+            tbl[2 * i + 1] = *reinterpret_cast<const uint32_t*>(&b);
+        }
+        // sign masks: s8 = the seven stored signs + their parity (page 4,
+        // decode); sign k goes to bit 15 (k even) or 31 (k odd) of pair k/2
+        uint32_t* sgt = reinterpret_cast<uint32_t*>(smem + L.table + kIQ3GridBytes);
+        for (int i = threadIdx.x; i < 128 * 32; i += blockDim.x) {
+            const uint32_t s7 = static_cast<uint32_t>(i) >> 5;
+            const uint32_t s8 = s7 | ((__popc(s7) & 1u) << 7);
+            uint32_t t = 0;
+#pragma unroll
+            for (int pr = 0; pr < 4; ++pr)
+                t |= (((s8 >> (2 * pr)) & 1u) << (15 - pr)) | (((s8 >> (2 * pr + 1)) & 1u) << (31 - pr));
+            sgt[i] = t;
         }
     }
     __syncthreads();
@@ -815,7 +919,7 @@ __global__ void __launch_bounds__(RG * F::kCols * 32 + 32, MINB)
     float acc2[2][MT];
 #pragma unroll
     for (int m = 0; m < MT; ++m) acc[m] = acc2[0][m] = acc2[1][m] = 0.f;
-    const uint32_t lane4 = static_cast<uint32_t>(lane) * 4u;
+    const uint32_t lane8 = static_cast<uint32_t>(lane) * 8u, lane4 = static_cast<uint32_t>(lane) * 4u;
     int64_t tile_count = 0;
 
     int s = 0, c = crank;
@@ -856,6 +960,29 @@ __global__ void __launch_bounds__(RG * F::kCols * 32 + 32, MINB)
                     if (r < rows) q4k_block<MT, PACKED, CVT>(blk, xb, xstride, sxp, M, acc);
                 }
                 if constexpr (CVT >= 3) fence_proxy_async_smem();  // x was written: order it before the slot's next copy
+            } else if constexpr (kHalf2) {
+                // two rows per lane, half a block each (TMA layout): rows
+                // rg*32 + (lane&15) and +16, half lane>>4
+                static_assert(F::kTMA, "two-row IQ3 decode reads the tensor-map layout");
+                const int hl = lane >> 4;
+                const uint8_t* box = st + cw * (kTileRows * F::kBoxBytes) + (rg * kRows + (lane & 15)) * F::kBoxBytes;
+                uint32_t vi[2][8], vs[2][4], dbits[2];
+                switch (cw) {
+#define QG_IQ3_HALF(C)                                                          \
+    case C:                                                                     \
+        iq3_load_half<C>(box, hl, vi[0], vs[0], dbits[0]);                      \
+        iq3_load_half<C>(box + 16 * F::kBoxBytes, hl, vi[1], vs[1], dbits[1]);  \
+        break;
+                    QG_IQ3_HALF(0) QG_IQ3_HALF(1) QG_IQ3_HALF(2) QG_IQ3_HALF(3)
+                    QG_IQ3_HALF(4) QG_IQ3_HALF(5) QG_IQ3_HALF(6)
+                    default:
+                        iq3_load_half<7>(box, hl, vi[0], vs[0], dbits[0]);
+                        iq3_load_half<7>(box + 16 * F::kBoxBytes, hl, vi[1], vs[1], dbits[1]);
+                        break;
+#undef QG_IQ3_HALF
+                }
+                const uint8_t* tb = smem + L.table;
+                iq3_half2<MT>(vi, vs, dbits, tb, tb + kIQ3GridBytes, lane8, lane4, xb + 128 * hl, xstride, M, acc2);
             } else {
                 if (r < rows) {
                     // row-copy layout: the row's kCols blocks back to back; TMA
@@ -864,7 +991,7 @@ __global__ void __launch_bounds__(RG * F::kCols * 32 + 32, MINB)
                     const uint8_t* rowp = F::kTMA ? st + cw * (kTileRows * F::kBoxBytes) + r * F::kBoxBytes -
                                                         ((cw * F::kBytes) & ~15)
                                                   : st + r * F::kRowStride;
-                    const uint32_t* tbl = reinterpret_cast<const uint32_t*>(smem + L.table);
+                    const uint8_t* tb = smem + L.table;
                     uint32_t v[24], dbits;
                     switch (cw) {
                         case 0: iq3_load_block<0>(rowp, v, dbits); break;
@@ -876,7 +1003,7 @@ __global__ void __launch_bounds__(RG * F::kCols * 32 + 32, MINB)
                         case 6: iq3_load_block<6>(rowp, v, dbits); break;
                         default: iq3_load_block<7>(rowp, v, dbits); break;
                     }
-                    iq3_block<MT, PACKED>(v, dbits, tbl, lane4, xb, xstride, M, acc);
+                    iq3_block<MT, PACKED>(v, dbits, tb, tb + kIQ3GridBytes, lane8, lane4, xb, xstride, M, acc);
                 }
             }
         }
