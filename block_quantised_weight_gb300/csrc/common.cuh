@@ -84,6 +84,11 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, i
           "l"(policy) : "memory");
 }
 
+// Fetch a tensor-map descriptor (kernel parameter space) ahead of its first use.
+__device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
 // L2 policy for data read exactly once (the weight stream).
 __device__ __forceinline__ uint64_t policy_evict_first() {
     uint64_t p;

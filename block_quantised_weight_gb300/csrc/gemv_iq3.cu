@@ -77,13 +77,13 @@ int launch_group_iq3(const uint8_t* const* W, float* const* Y, const int64_t* N,
                 rc = cudaGetLastError() == cudaSuccess ? QG_OK : QG_ECUDA;
             }
         } else if (mg == 1) {
-            rc = launch_gemv<FmtIQ3T, 1, true, 2, true, 1, 4>(W, Y, N, count, m0, grid, Xg, mg, K, s, status, dev, flags);
+            rc = launch_gemv<FmtIQ3T, 1, true, 2, 1>(W, Y, N, count, m0, grid, Xg, mg, K, s, status, dev, flags);
         } else if (mg == 2) {
-            rc = launch_gemv<FmtIQ3T, 2, true, 1, true, 1, 4>(W, Y, N, count, m0, grid, Xg, mg, K, s, status, dev, flags);
+            rc = launch_gemv<FmtIQ3T, 2, true, 1, 1>(W, Y, N, count, m0, grid, Xg, mg, K, s, status, dev, flags);
         } else if (mg <= 4) {
-            rc = launch_gemv<FmtIQ3T, 4, false, 1, true, 1>(W, Y, N, count, m0, grid, Xg, mg, K, s, status, dev, flags);
+            rc = launch_gemv<FmtIQ3T, 4, false, 1, 1>(W, Y, N, count, m0, grid, Xg, mg, K, s, status, dev, flags);
         } else {
-            rc = launch_gemv<FmtIQ3T, 8, false, 1, true, 1>(W, Y, N, count, m0, grid, Xg, mg, K, s, status, dev, flags);
+            rc = launch_gemv<FmtIQ3T, 8, false, 1, 1>(W, Y, N, count, m0, grid, Xg, mg, K, s, status, dev, flags);
         }
         if (rc != QG_OK) return rc;
     }

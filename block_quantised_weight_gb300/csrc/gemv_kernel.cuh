@@ -41,6 +41,16 @@ constexpr int kSmemPerSM = 233472;   // 228 KB per SM on sm_103
 constexpr int kSmemPerCTA = 232448;  // 227 KB max dynamic smem per CTA
 constexpr int kSmemReserve = 1024;   // per-CTA system reservation
 
+// x of one super-block column and token in a ring stage: two halves of 128
+// floats, half 1 starting F::kXH floats after half 0.  IQ3 pads (kXH =
+// kXHalf = 132): the 4-float gap puts the halves 16 bytes apart modulo the
+// 128-byte bank period, so the lanes of a two-row decode (lanes 0-15 on
+// half 0, 16-31 on half 1, reading the same offset in their half) load x
+// without a bank conflict.  Q4_K stages x contiguously (kXH = 128): there
+// the conflict costs less than the padded copy.
+constexpr int kXHalf = 132;
+constexpr int kXCol = 2 * kXHalf;  // padded floats per column and token (1056 bytes)
+
 // Stage layouts.  Row-copy formats: one bulk copy per row chunk, each row in
 // its own slot (kRowStride apart).  FmtQ4KT: one 2D tensor-map TMA per
 // super-block column, landing as [tile rows][144 B] boxes (a unit is kCols
@@ -59,6 +69,7 @@ struct FmtQ4K {
     static constexpr bool kIQ3 = false;
     static constexpr bool kTMA = false;
     static constexpr int kBoxBytes = 0;
+    static constexpr int kXH = 128;
 };
 template <int C>
 struct FmtQ4KTc {
@@ -68,16 +79,9 @@ struct FmtQ4KTc {
     static constexpr bool kIQ3 = false;
     static constexpr bool kTMA = true;
     static constexpr int kBoxBytes = 144;
+    static constexpr int kXH = 128;  // x staged contiguously (one bulk copy per token)
 };
 using FmtQ4KT = FmtQ4KTc<kCols>;
-struct FmtIQ3 {
-    static constexpr int kBytes = 98;
-    static constexpr int kCols = qg::kCols;
-    static constexpr int kRowStride = kCols * 98;  // 784 = 49 * 16 (odd)
-    static constexpr bool kIQ3 = true;
-    static constexpr bool kTMA = false;
-    static constexpr int kBoxBytes = 0;
-};
 struct FmtIQ3T {
     static constexpr int kBytes = 98;
     static constexpr int kCols = qg::kCols;
@@ -85,6 +89,7 @@ struct FmtIQ3T {
     static constexpr bool kIQ3 = true;
     static constexpr bool kTMA = true;
     static constexpr int kBoxBytes = 112;
+    static constexpr int kXH = kXHalf;  // x staged in the padded layout (one 2D box per token)
 };
 
 // IQ3 tables in smem, shared by all consumer warps.
@@ -97,6 +102,7 @@ struct FmtIQ3T {
 constexpr int kIQ3GridBytes = 256 * 32 * 8;
 constexpr int kIQ3SignBytes = 128 * 32 * 4;
 constexpr int kIQ3TableBytes = kIQ3GridBytes + kIQ3SignBytes;
+
 
 __host__ __device__ constexpr int align_up(int v, int a) { return (v + a - 1) / a * a; }
 
@@ -121,11 +127,14 @@ struct Group {
     int count;
 };
 
-// Tensor maps of the group's matrices (FmtQ4KT): bytes [N][K/256*144], box
-// 144 B x tile rows.
+// Tensor maps of the group's matrices: bytes [N][K/256*B], box kBoxBytes x
+// tile rows; and of X viewed as [M*K/128][128] fp32 with 132 x 16 boxes
+// (one box = the padded x of one unit's 8 columns for one token).
 struct TMaps {
     CUtensorMap m[kMaxGroup];
+    CUtensorMap xm;
 };
+constexpr uint32_t kXBoxBytes = 16 * kXHalf * 4;  // 8448
 
 // Matrix that owns global tile `tile`.
 __device__ __forceinline__ int group_find(const Group& G, int64_t tile) {
@@ -136,8 +145,10 @@ __device__ __forceinline__ int group_find(const Group& G, int64_t tile) {
     return i;
 }
 
-// Dynamic smem layout of gemv_kernel<F, MT, XS, RG> with `stages` stages.
-__host__ __device__ inline Layout make_layout(bool iq3, int MT, bool xs, int RG, int stages, int row_stride,
+// Dynamic smem layout of gemv_kernel<F, MT, XS, RG> with `stages` stages;
+// xh = F::kXH when x is staged with the weights, 0 when it is read from
+// global memory.
+__host__ __device__ inline Layout make_layout(bool iq3, int MT, int xh, int RG, int stages, int row_stride,
                                               int cols = kCols) {
     Layout L;
     const int warps = RG * cols;
@@ -149,7 +160,7 @@ __host__ __device__ inline Layout make_layout(bool iq3, int MT, bool xs, int RG,
     L.table = L.cred + align_up(kMaxCluster * MT * RG * kRows * 4, 128);
     L.stage0 = L.table + (iq3 ? kIQ3TableBytes : 0);
     L.xoff = align_up(RG * kRows * row_stride, 128);
-    L.stage_bytes = L.xoff + (xs ? MT * cols * 1024 : 0);
+    L.stage_bytes = L.xoff + MT * cols * 8 * xh;  // xh: F::kXH with x staged, else 0
     L.total = L.stage0 + stages * L.stage_bytes;
     return L;
 }
@@ -176,37 +187,27 @@ __device__ __forceinline__ float half_hi(uint32_t h) {
     return __half2float(__ushort_as_half(static_cast<unsigned short>(h >> 16)));
 }
 
-// acc += a * b on two fp32 lanes: packed FMA or two scalar FMAs.
-template <bool PACKED>
-__device__ __forceinline__ void fma2(f2& acc, f2 a, f2 b) {
-    if constexpr (PACKED) {
-        ffma2(acc, a, b);
-    } else {
-        acc.x = fmaf(a.x, b.x, acc.x);
-        acc.y = fmaf(a.y, b.y, acc.y);
-    }
-}
-
 // Per-warp x preparation for one Q4_K super-block column (256 x values per
-// token, in smem): sx[m*8 + j] = sum of x over sub-block j (the dmin*mn
-// term's factor), and for CVT == 3 the x values are scaled in place by
-// 2^(88-c), c = 4*(high nibble) + 8*(odd byte), the bit offsets at which
-// q4k_block finds each nibble.  The scaling is exact for |x| < 2^40; larger
-// values overflow to inf.  Callers that write x in smem must fence it
-// against the next bulk copy into the same slot.
-template <int MT, int CVT>
+// token; half 1, x[128..255], starts XH floats after half 0):
+// sx[m*8 + j] = sum of x over sub-block j (the dmin*mn term's factor), and
+// with SCALE the x values (in smem) are scaled in place by 2^(88-c),
+// c = 4*(high nibble) + 8*(odd byte), the bit offsets at which q4k_half2
+// finds each nibble.  The scaling is exact for |x| < 2^40; larger values
+// overflow to inf.  Callers that write x in smem must fence it against the
+// next bulk copy into the same slot.
+template <int MT, bool SCALE, int XH>
 __device__ __forceinline__ void q4k_stage_x(float* xb, int64_t xstride, float* sx, int M, int lane) {
 #pragma unroll
     for (int m = 0; m < MT; ++m) {
         if (MT == 1 || m < M) {
-            float* xp = xb + m * xstride + (lane >> 2) * 32 + (lane & 3) * 8;
+            float* xp = xb + m * xstride + (lane >> 4) * XH + ((lane >> 2) & 3) * 32 + (lane & 3) * 8;
             float4 a = *reinterpret_cast<const float4*>(xp);
             float4 b = *reinterpret_cast<const float4*>(xp + 4);
             float sm = ((a.x + a.y) + (a.z + a.w)) + ((b.x + b.y) + (b.z + b.w));
             sm += __shfl_xor_sync(0xffffffffu, sm, 1);
             sm += __shfl_xor_sync(0xffffffffu, sm, 2);
             if ((lane & 3) == 0) sx[m * 8 + (lane >> 2)] = sm;
-            if constexpr (CVT == 3) {
+            if constexpr (SCALE) {
                 const float se = ((lane >> 2) & 1) ? 0x1p84f : 0x1p88f;   // even byte
                 const float so = se * 0x1p-8f;                            // odd byte
                 a = make_float4(a.x * se, a.y * so, a.z * se, a.w * so);
@@ -220,12 +221,12 @@ __device__ __forceinline__ void q4k_stage_x(float* xb, int64_t xstride, float* s
 
 // One Q4_K super-block (144 bytes at blk, smem) against MT tokens of x.
 // sx[m*8 + j] = sum of x over sub-block j for token m.
-// Nibbles become exact fp32 without any arithmetic (CVT == 2, the default):
-// a nibble placed in the low bits of an fp16 is the subnormal q*2^-24 (high
-// nibbles left in place: 16q*2^-24), which cvt.f32.f16 turns into an exact
-// fp32; the powers of two are folded into the sub-block scales.  (CVT 0 and
-// 1 are the earlier fp16 / fp32 magic-offset forms, kept for comparison.)
-template <int MT, bool PACKED, int CVT>
+// Nibbles become exact fp32 without any arithmetic: a nibble placed in the
+// low bits of an fp16 is the subnormal q*2^-24 (high nibbles left in place:
+// 16q*2^-24), which cvt.f32.f16 turns into an exact fp32; the powers of two
+// are folded into the sub-block scales.  PRMT pairs bytes (0,1) and (2,3) so
+// each pair meets x[kl..kl+1], x[kl+2..kl+3].
+template <int MT>
 __device__ __forceinline__ void q4k_block(const uint8_t* blk, const float* xb, int64_t xstride, const float* sx,
                                           int M, float (&acc)[MT]) {
     const uint4 h = *reinterpret_cast<const uint4*>(blk);
@@ -257,97 +258,20 @@ __device__ __forceinline__ void q4k_block(const uint8_t* blk, const float* xb, i
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
                 const int kl = 64 * g + 16 * hh + 4 * e;  // weights kl..kl+3 (low), +32 (high)
-                if constexpr (CVT == 2) {
-                    // Nibbles as fp16 subnormals: half bits 0x000q (low nibble)
-                    // or 0x00q0 (high nibble, 16q) are exactly q*2^-24 and
-                    // q*2^-20; one cvt per half gives exact fp32.  PRMT pairs
-                    // bytes (0,1) and (2,3) so each pair meets x[kl..kl+1],
-                    // x[kl+2..kl+3]; the powers of two go into the scales.
-                    const uint32_t lo4 = qv[e] & 0x0F0F0F0Fu, hi4 = qv[e] & 0xF0F0F0F0u;
-                    const f2 l01 = h2_to_f2(prmt(lo4, 0u, 0x5140u));
-                    const f2 l23 = h2_to_f2(prmt(lo4, 0u, 0x5342u));
-                    const f2 h01 = h2_to_f2(prmt(hi4, 0u, 0x5140u));
-                    const f2 h23 = h2_to_f2(prmt(hi4, 0u, 0x5342u));
+                const uint32_t lo4 = qv[e] & 0x0F0F0F0Fu, hi4 = qv[e] & 0xF0F0F0F0u;
+                const f2 l01 = h2_to_f2(prmt(lo4, 0u, 0x5140u));
+                const f2 l23 = h2_to_f2(prmt(lo4, 0u, 0x5342u));
+                const f2 h01 = h2_to_f2(prmt(hi4, 0u, 0x5140u));
+                const f2 h23 = h2_to_f2(prmt(hi4, 0u, 0x5342u));
 #pragma unroll
-                    for (int m = 0; m < MT; ++m) {
-                        if (MT == 1 || m < M) {
-                            const float4 xl = *reinterpret_cast<const float4*>(xb + m * xstride + kl);
-                            const float4 xh = *reinterpret_cast<const float4*>(xb + m * xstride + kl + 32);
-                            fma2<PACKED>(al[m], l01, f2{xl.x, xl.y});
-                            fma2<PACKED>(al[m], l23, f2{xl.z, xl.w});
-                            fma2<PACKED>(ah[m], h01, f2{xh.x, xh.y});
-                            fma2<PACKED>(ah[m], h23, f2{xh.z, xh.w});
-                        }
-                    }
-                } else if constexpr (CVT == 3) {
-                    // Nibbles as fp32 subnormals, masked in place: v & 0xF is
-                    // q*2^-149, v & 0xF0 is q*2^-145, v & 0xF00 q*2^-141,
-                    // v & 0xF000 q*2^-137 (bytes 2, 3 the same from v >> 16).
-                    // x was pre-scaled by 2^(88-c) for the nibble's offset c
-                    // (q4k_stage_x), so every product is q*x*2^-61, a normal
-                    // fp32 for |q*x| >= 2^-65: the FMA rounds as usual.
-                    const uint32_t v = qv[e], u = v >> 16;
-                    const f2 l01{__uint_as_float(v & 0xFu), __uint_as_float(v & 0xF00u)};
-                    const f2 l23{__uint_as_float(u & 0xFu), __uint_as_float(u & 0xF00u)};
-                    const f2 h01{__uint_as_float(v & 0xF0u), __uint_as_float(v & 0xF000u)};
-                    const f2 h23{__uint_as_float(u & 0xF0u), __uint_as_float(u & 0xF000u)};
-#pragma unroll
-                    for (int m = 0; m < MT; ++m) {
-                        if (MT == 1 || m < M) {
-                            const float4 xl = *reinterpret_cast<const float4*>(xb + m * xstride + kl);
-                            const float4 xh = *reinterpret_cast<const float4*>(xb + m * xstride + kl + 32);
-                            fma2<PACKED>(al[m], l01, f2{xl.x, xl.y});
-                            fma2<PACKED>(al[m], l23, f2{xl.z, xl.w});
-                            fma2<PACKED>(ah[m], h01, f2{xh.x, xh.y});
-                            fma2<PACKED>(ah[m], h23, f2{xh.z, xh.w});
-                        }
-                    }
-                } else if constexpr (CVT == 0) {
-                    const uint32_t v = qv[e], v8 = v >> 8;
-                    const uint32_t A = (v & 0x000F000Fu) | 0x64006400u;   // bytes 0,2 low nibbles
-                    const uint32_t C = (v8 & 0x000F000Fu) | 0x64006400u;  // bytes 1,3 low nibbles
-                    const uint32_t B = (v & 0x00F000F0u) | 0x64006400u;   // bytes 0,2 high nibbles (x16)
-                    const uint32_t D = (v8 & 0x00F000F0u) | 0x64006400u;  // bytes 1,3 high nibbles (x16)
-                    const f2 l01{add_f16_f32(A, -1024.f), add_f16_f32(C, -1024.f)};
-                    const f2 l23{add_f16hi_f32(A, -1024.f), add_f16hi_f32(C, -1024.f)};
-                    const f2 h01{add_f16_f32(B, -1024.f), add_f16_f32(D, -1024.f)};
-                    const f2 h23{add_f16hi_f32(B, -1024.f), add_f16hi_f32(D, -1024.f)};
-#pragma unroll
-                    for (int m = 0; m < MT; ++m) {
-                        if (MT == 1 || m < M) {
-                            const float4 xl = *reinterpret_cast<const float4*>(xb + m * xstride + kl);
-                            const float4 xh = *reinterpret_cast<const float4*>(xb + m * xstride + kl + 32);
-                            fma2<PACKED>(al[m], l01, f2{xl.x, xl.y});
-                            fma2<PACKED>(al[m], l23, f2{xl.z, xl.w});
-                            fma2<PACKED>(ah[m], h01, f2{xh.x, xh.y});
-                            fma2<PACKED>(ah[m], h23, f2{xh.z, xh.w});
-                        }
-                    }
-                } else {
-                    // fp32 magic in place: (bits & mask) | 0x4B000000 = 2^23 + c*q with
-                    // c = 1 (bits 0-3), 16 (4-7), 256 (8-11), 4096 (12-15); the packed
-                    // add of -2^23 leaves c*q exactly.  Pair (byte k, byte k+1) puts the
-                    // c=1 (or 16) terms in lane .x and the c=256 (or 4096) terms in .y.
-                    const uint32_t v = qv[e], u = v >> 16;
-                    const f2 mg{-8388608.f, -8388608.f};
-                    f2 l01{__uint_as_float((v & 0xFu) | 0x4B000000u), __uint_as_float((v & 0xF00u) | 0x4B000000u)};
-                    f2 l23{__uint_as_float((u & 0xFu) | 0x4B000000u), __uint_as_float((u & 0xF00u) | 0x4B000000u)};
-                    f2 h01{__uint_as_float((v & 0xF0u) | 0x4B000000u), __uint_as_float((v & 0xF000u) | 0x4B000000u)};
-                    f2 h23{__uint_as_float((u & 0xF0u) | 0x4B000000u), __uint_as_float((u & 0xF000u) | 0x4B000000u)};
-                    fadd2(l01, mg);
-                    fadd2(l23, mg);
-                    fadd2(h01, mg);
-                    fadd2(h23, mg);
-#pragma unroll
-                    for (int m = 0; m < MT; ++m) {
-                        if (MT == 1 || m < M) {
-                            const float4 xl = *reinterpret_cast<const float4*>(xb + m * xstride + kl);
-                            const float4 xh = *reinterpret_cast<const float4*>(xb + m * xstride + kl + 32);
-                            fma2<PACKED>(al[m], l01, f2{xl.x, xl.y});
-                            fma2<PACKED>(al[m], l23, f2{xl.z, xl.w});
-                            fma2<PACKED>(ah[m], h01, f2{xh.x, xh.y});
-                            fma2<PACKED>(ah[m], h23, f2{xh.z, xh.w});
-                        }
+                for (int m = 0; m < MT; ++m) {
+                    if (MT == 1 || m < M) {
+                        const float4 xl = *reinterpret_cast<const float4*>(xb + m * xstride + kl);
+                        const float4 xh = *reinterpret_cast<const float4*>(xb + m * xstride + kl + 32);
+                        ffma2(al[m], l01, f2{xl.x, xl.y});
+                        ffma2(al[m], l23, f2{xl.z, xl.w});
+                        ffma2(ah[m], h01, f2{xh.x, xh.y});
+                        ffma2(ah[m], h23, f2{xh.z, xh.w});
                     }
                 }
             }
@@ -355,19 +279,8 @@ __device__ __forceinline__ void q4k_block(const uint8_t* blk, const float* xb, i
 #pragma unroll
         for (int m = 0; m < MT; ++m) {
             if (MT == 1 || m < M) {
-                if constexpr (CVT == 3) {
-                    acc[m] = fmaf(dl * 0x1p61f, al[m].x + al[m].y, acc[m]);
-                    acc[m] = fmaf(dh * 0x1p65f, ah[m].x + ah[m].y, acc[m]);        // dh has 1/16
-                } else if constexpr (CVT == 2) {
-                    acc[m] = fmaf(dl * 16777216.f, al[m].x + al[m].y, acc[m]);     // 2^24
-                    acc[m] = fmaf(dh * 16777216.f, ah[m].x + ah[m].y, acc[m]);     // dh has 1/16: 2^20 * 16
-                } else if constexpr (CVT == 0) {
-                    acc[m] = fmaf(dl, al[m].x + al[m].y, acc[m]);
-                    acc[m] = fmaf(dh, ah[m].x + ah[m].y, acc[m]);
-                } else {
-                    acc[m] = fmaf(dl, fmaf(al[m].y, 0.00390625f, al[m].x), acc[m]);
-                    acc[m] = fmaf(dh, fmaf(ah[m].y, 0.00390625f, ah[m].x), acc[m]);
-                }
+                acc[m] = fmaf(dl * 16777216.f, al[m].x + al[m].y, acc[m]);     // 2^24
+                acc[m] = fmaf(dh * 16777216.f, ah[m].x + ah[m].y, acc[m]);     // dh has 1/16: 2^20 * 16
             }
         }
     }
@@ -375,98 +288,14 @@ __device__ __forceinline__ void q4k_block(const uint8_t* blk, const float* xb, i
     for (int m = 0; m < MT; ++m) acc[m] -= mt[m];
 }
 
-// R rows of one Q4_K super-block column against MT tokens, x shared: row j's
-// block is at blk + j*rstride (smem).  Same arithmetic as q4k_block with
-// CVT == 3 (x pre-scaled by q4k_stage_x); one x load serves R rows.
-template <int MT, int R>
-__device__ __forceinline__ void q4k_block_rows(const uint8_t* blk, int rstride, const float* xb, int64_t xstride,
-                                               const float* sx, int M, float (&acc)[R][MT]) {
-    float d[R], dmin[R];
-    uint32_t sc03[R], mn03[R], sc47[R], mn47[R];
-#pragma unroll
-    for (int j = 0; j < R; ++j) {
-        const uint4 h = *reinterpret_cast<const uint4*>(blk + j * rstride);
-        d[j] = h2f(h.x);
-        dmin[j] = h2f(h.x >> 16);
-        q4k_scale_min_words(h.y, h.z, h.w, sc03[j], mn03[j], sc47[j], mn47[j]);
-    }
-#pragma unroll
-    for (int j = 0; j < R; ++j) {
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {
-            const float dmn = dmin[j] * byte_f(k < 4 ? mn03[j] : mn47[j], k & 3);
-#pragma unroll
-            for (int m = 0; m < MT; ++m)
-                if (MT == 1 || m < M) acc[j][m] = fmaf(-dmn, sx[m * 8 + k], acc[j][m]);
-        }
-    }
-#pragma unroll
-    for (int g = 0; g < 4; ++g) {
-        f2 al[R][MT], ah[R][MT];
-#pragma unroll
-        for (int j = 0; j < R; ++j)
-#pragma unroll
-            for (int m = 0; m < MT; ++m) al[j][m] = ah[j][m] = f2{0.f, 0.f};
-#pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
-            uint4 q[R];
-#pragma unroll
-            for (int j = 0; j < R; ++j) q[j] = *reinterpret_cast<const uint4*>(blk + j * rstride + 16 + 32 * g + 16 * hh);
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const int kl = 64 * g + 16 * hh + 4 * e;
-                float4 xl[MT], xh[MT];
-#pragma unroll
-                for (int m = 0; m < MT; ++m) {
-                    if (MT == 1 || m < M) {
-                        xl[m] = *reinterpret_cast<const float4*>(xb + m * xstride + kl);
-                        xh[m] = *reinterpret_cast<const float4*>(xb + m * xstride + kl + 32);
-                    }
-                }
-#pragma unroll
-                for (int j = 0; j < R; ++j) {
-                    const uint32_t v = e == 0 ? q[j].x : e == 1 ? q[j].y : e == 2 ? q[j].z : q[j].w;
-                    const uint32_t u = v >> 16;
-                    const f2 l01{__uint_as_float(v & 0xFu), __uint_as_float(v & 0xF00u)};
-                    const f2 l23{__uint_as_float(u & 0xFu), __uint_as_float(u & 0xF00u)};
-                    const f2 h01{__uint_as_float(v & 0xF0u), __uint_as_float(v & 0xF000u)};
-                    const f2 h23{__uint_as_float(u & 0xF0u), __uint_as_float(u & 0xF000u)};
-#pragma unroll
-                    for (int m = 0; m < MT; ++m) {
-                        if (MT == 1 || m < M) {
-                            ffma2(al[j][m], l01, f2{xl[m].x, xl[m].y});
-                            ffma2(al[j][m], l23, f2{xl[m].z, xl[m].w});
-                            ffma2(ah[j][m], h01, f2{xh[m].x, xh[m].y});
-                            ffma2(ah[j][m], h23, f2{xh[m].z, xh[m].w});
-                        }
-                    }
-                }
-            }
-        }
-#pragma unroll
-        for (int j = 0; j < R; ++j) {
-            const uint32_t scw = g < 2 ? sc03[j] : sc47[j];
-            const float dl = d[j] * byte_f(scw, (2 * g) & 3) * 0x1p61f;
-            const float dh = d[j] * byte_f(scw, (2 * g + 1) & 3) * 0x1p61f;
-#pragma unroll
-            for (int m = 0; m < MT; ++m) {
-                if (MT == 1 || m < M) {
-                    acc[j][m] = fmaf(dl, al[j][m].x + al[j][m].y, acc[j][m]);
-                    acc[j][m] = fmaf(dh, ah[j][m].x + ah[j][m].y, acc[j][m]);
-                }
-            }
-        }
-    }
-}
-
-// Half of one Q4_K super-block column for two rows (CVT 4, x pre-scaled as
-// for CVT 3).  Lane L of a warp takes rows L&15 and (L&15)+16 of the tile and
+// Half of one Q4_K super-block column for two rows (x pre-scaled by
+// q4k_stage_x with SCALE; half 1 of x XH floats after half 0).  Lane L of a warp takes rows L&15 and (L&15)+16 of the tile and
 // half h = L>>4 of the block (sub-blocks 4h..4h+3, weights 128h..128h+127),
 // so every x load serves two rows; the two halves of a row meet with one
 // shuffle at the end of the tile.  blk: the row-(L&15) block in smem;
 // rstride: bytes from a row to the row 16 below.  The min term
 // dmin*mn*sum(x) is taken first, then the scaled sub-block sums.
-template <int MT>
+template <int MT, int XH>
 __device__ __forceinline__ void q4k_half2(const uint8_t* blk, int rstride, int h, const float* xb, int64_t xstride,
                                           const float* sx, int M, float (&acc)[2][MT]) {
     float d61[2];
@@ -488,7 +317,7 @@ __device__ __forceinline__ void q4k_half2(const uint8_t* blk, int rstride, int h
         }
     }
     const uint8_t* qb = blk + 16 + 64 * h;
-    const float* xq = xb + 128 * h;
+    const float* xq = xb + XH * h;
 #pragma unroll
     for (int g = 0; g < 2; ++g) {
         f2 al[2][MT], ah[2][MT];
@@ -593,7 +422,7 @@ __device__ __forceinline__ uint2 iq3_grid(const uint8_t* tb, uint32_t w, int byt
 // the sign table (the implied eighth sign included), converts to fp32 and
 // FMAs.  The sub-block factor d*(0.5+code)*0.5 and the grid's 0.5 are
 // applied once per 32 weights (exact: at most 16 significant bits).
-template <int MT, bool PACKED>
+template <int MT>
 __device__ __forceinline__ void iq3_block(const uint32_t (&v)[24], uint32_t dbits, const uint8_t* tb, const uint8_t* sg,
                                           uint32_t lane8, uint32_t lane4, const float* xb, int64_t xstride, int M,
                                           float (&acc)[MT]) {
@@ -618,8 +447,8 @@ __device__ __forceinline__ void iq3_block(const uint32_t (&v)[24], uint32_t dbit
                 for (int m = 0; m < MT; ++m) {
                     if (MT == 1 || m < M) {
                         const float4 x = *reinterpret_cast<const float4*>(xb + m * xstride + 32 * ib + 8 * l + 4 * hf);
-                        fma2<PACKED>(dot[m], w01, f2{x.x, x.y});
-                        fma2<PACKED>(dot[m], w23, f2{x.z, x.w});
+                        ffma2(dot[m], w01, f2{x.x, x.y});
+                        ffma2(dot[m], w23, f2{x.z, x.w});
                     }
                 }
             }
@@ -750,7 +579,10 @@ __device__ __forceinline__ void named_barrier_sync(int id) {
 
 // ------------------------------------------------------------ the kernel
 // Threads: RG*8 consumer warps, then one producer warp.
-template <class F, int MT, bool XS, int RG, bool PACKED, int MINB, int CVT = 2>
+// XS: x staged in shared memory with each unit (padded layout above) and
+// the two-row decode (lane L: rows L&15 and (L&15)+16, half L>>4 of each
+// block); otherwise x read from global memory and one row per lane.
+template <class F, int MT, bool XS, int RG, int MINB>
 __global__ void __launch_bounds__(RG * F::kCols * 32 + 32, MINB)
     gemv_kernel(const __grid_constant__ Group G, const __grid_constant__ TMaps T, const uint8_t* __restrict__ grid,
                 const float* __restrict__ X, int M, int64_t K, int stages, unsigned* status, int flags) {
@@ -761,13 +593,16 @@ __global__ void __launch_bounds__(RG * F::kCols * 32 + 32, MINB)
     const int nb = static_cast<int>(K / 256);
     const int nchunks = (nb + F::kCols - 1) / F::kCols;
     const int64_t ntiles = G.tile0[G.count];
-    const Layout L = make_layout(F::kIQ3, MT, XS, RG, stages, F::kRowStride, F::kCols);
+    constexpr int XH = XS ? F::kXH : 0;  // floats from half 0 to half 1 of a staged x column
+    const Layout L = make_layout(F::kIQ3, MT, XH, RG, stages, F::kRowStride, F::kCols);
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.full);
     uint64_t* empty = reinterpret_cast<uint64_t*>(smem + L.empty);
     float* sxw = reinterpret_cast<float*>(smem + L.sx);
     float* red = reinterpret_cast<float*>(smem + L.red);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int64_t pitch = static_cast<int64_t>(nb) * F::kBytes;
+    static_assert(F::kTMA, "weights arrive through the format's tensor map");
+    static_assert(!XS || F::kCols == 8, "one x box holds 8 columns");
+    static_assert(!XS || F::kIQ3 || RG == 1, "in-place x scaling needs one warp per column");
 
     // Programmatic dependent launch: let the next kernel in the stream get
     // scheduled now.  Without the weight-prefetch flag, wait for the previous
@@ -826,6 +661,10 @@ __global__ void __launch_bounds__(RG * F::kCols * 32 + 32, MINB)
         // in the loop.
         const uint64_t pol_w = policy_evict_first();
         const uint64_t pol_x = policy_evict_last();
+        // bring the tensor-map descriptors in before the first copies (the x
+        // map's first use sits on the dependency chain)
+        if (lane < G.count) prefetch_tensormap(&T.m[lane]);
+        if (XH == kXHalf && lane == 31) prefetch_tensormap(&T.xm);
         struct Pos {
             int s, c;
             int64_t tile, row0;
@@ -853,34 +692,31 @@ __global__ void __launch_bounds__(RG * F::kCols * 32 + 32, MINB)
         auto post = [&](const Pos& p, bool do_w, bool do_x, bool expect) {
             const int kc = min(F::kCols, nb - p.c * F::kCols);
             uint8_t* st = smem + L.stage0 + p.s * L.stage_bytes;
-            if constexpr (F::kTMA) {
-                // kc boxes of kBoxBytes x kTileRows; rows past N (and bytes past
-                // the row end) arrive as zeros and count in full toward the
-                // transaction bytes.
-                constexpr uint32_t kBox = kTileRows * F::kBoxBytes;
-                if (expect) {
-                    if (lane == 0) mbar_arrive_expect_tx(&full[p.s], kc * kBox + (XS ? M * kc * 1024 : 0));
-                    __syncwarp();
-                }
-                if (do_w && lane == 0)
-                    for (int b = 0; b < kc; ++b)
-                        tma_load_2d(st + b * kBox, &T.m[p.gi], ((p.c * F::kCols + b) * F::kBytes) & ~15,
-                                    static_cast<int>(p.row0), &full[p.s], pol_w);
-            } else {
+            // kc boxes of kBoxBytes x kTileRows; rows past N (and bytes past
+            // the row end) arrive as zeros and count in full toward the
+            // transaction bytes.
+            constexpr uint32_t kBox = kTileRows * F::kBoxBytes;
+            // x, padded layout: one 132 x 16 box per token (the unit's 8
+            // columns as 16 padded halves; halves past the chunk are never
+            // read); contiguous layout: one bulk copy per token
+            constexpr bool kXBox = (XH == kXHalf);
             if (expect) {
-                const uint32_t bytes = p.rows * kc * F::kBytes + (XS ? M * kc * 1024 : 0);
-                if (lane == 0) mbar_arrive_expect_tx(&full[p.s], bytes);
+                if (lane == 0)
+                    mbar_arrive_expect_tx(&full[p.s], kc * kBox + (XS ? M * (kXBox ? kXBoxBytes : kc * 1024) : 0));
                 __syncwarp();
             }
-            if (do_w) {
-                const uint8_t* src = G.W[p.gi] + p.row0 * pitch + static_cast<int64_t>(p.c) * F::kCols * F::kBytes;
-                for (int r = lane; r < p.rows; r += 32)
-                    bulk_g2s(st + r * F::kRowStride, src + r * pitch, kc * F::kBytes, &full[p.s], pol_w);
+            if (do_w && lane == 0)
+                for (int b = 0; b < kc; ++b)
+                    tma_load_2d(st + b * kBox, &T.m[p.gi], ((p.c * F::kCols + b) * F::kBytes) & ~15,
+                                static_cast<int>(p.row0), &full[p.s], pol_w);
+            if (XS && do_x && lane < M) {
+                if constexpr (kXBox)
+                    tma_load_2d(st + L.xoff + lane * kXBoxBytes, &T.xm, 0,
+                                static_cast<int>((lane * K) / 128 + p.c * (2 * F::kCols)), &full[p.s], pol_x);
+                else
+                    bulk_g2s(st + L.xoff + lane * F::kCols * 1024,
+                             X + lane * K + static_cast<int64_t>(p.c) * F::kCols * 256, kc * 1024, &full[p.s], pol_x);
             }
-            }
-            if (XS && do_x && lane < M)
-                bulk_g2s(st + L.xoff + lane * F::kCols * 1024, X + lane * K + static_cast<int64_t>(p.c) * F::kCols * 256,
-                         kc * 1024, &full[p.s], pol_x);
         };
         Pos p = first_pos();
         int64_t u0 = 0;
@@ -913,8 +749,8 @@ __global__ void __launch_bounds__(RG * F::kCols * 32 + 32, MINB)
     // ---------------- consumer warps
     if (prefetch) grid_dependency_wait();  // x and Y belong to the dependency chain
     const int rg = warp / F::kCols, cw = warp % F::kCols;
-    // CVT 4: two rows per lane (acc2[j]: row (lane&15) + 16j, half lane>>4)
-    constexpr bool kHalf2 = (CVT == 4);
+    // XS: two rows per lane (acc2[j]: row (lane&15) + 16j, half lane>>4)
+    constexpr bool kHalf2 = XS;
     float acc[MT];
     float acc2[2][MT];
 #pragma unroll
@@ -943,27 +779,23 @@ __global__ void __launch_bounds__(RG * F::kCols * 32 + 32, MINB)
 
         if (cw < kc) {
             const int64_t b = static_cast<int64_t>(c) * F::kCols + cw;  // super-block column
-            const float* xb = XS ? reinterpret_cast<const float*>(st + L.xoff) + cw * 256 : X + b * 256;
-            const int64_t xstride = XS ? F::kCols * 256 : K;
+            const float* xb = XS ? reinterpret_cast<const float*>(st + L.xoff) + cw * 2 * XH : X + b * 256;
+            const int64_t xstride = XS ? F::kCols * 2 * XH : K;
             if constexpr (!F::kIQ3) {
-                static_assert(CVT < 3 || (XS && RG == 1), "in-place x scaling needs x in smem, one warp per column");
-                static_assert(CVT != 4 || F::kTMA, "two-row decode reads the tensor-map layout");
                 float* sxp = sxw + warp * MT * 8;
-                q4k_stage_x<MT, CVT == 4 ? 3 : CVT>(const_cast<float*>(xb), xstride, sxp, M, lane);
+                q4k_stage_x<MT, XS, XS ? XH : 128>(const_cast<float*>(xb), xstride, sxp, M, lane);
                 __syncwarp();
                 if constexpr (kHalf2) {
                     const uint8_t* blk = st + cw * (kTileRows * F::kBytes) + (lane & 15) * F::kBytes;
-                    q4k_half2<MT>(blk, 16 * F::kBytes, lane >> 4, xb, xstride, sxp, M, acc2);
+                    q4k_half2<MT, XH>(blk, 16 * F::kBytes, lane >> 4, xb, xstride, sxp, M, acc2);
+                    fence_proxy_async_smem();  // x was written: order it before the slot's next copy
                 } else {
-                    const uint8_t* blk = F::kTMA ? st + cw * (kTileRows * F::kBytes) + r * F::kBytes
-                                                 : st + r * F::kRowStride + cw * F::kBytes;
-                    if (r < rows) q4k_block<MT, PACKED, CVT>(blk, xb, xstride, sxp, M, acc);
+                    const uint8_t* blk = st + cw * (kTileRows * F::kBytes) + r * F::kBytes;
+                    if (r < rows) q4k_block<MT>(blk, xb, xstride, sxp, M, acc);
                 }
-                if constexpr (CVT >= 3) fence_proxy_async_smem();  // x was written: order it before the slot's next copy
             } else if constexpr (kHalf2) {
                 // two rows per lane, half a block each (TMA layout): rows
                 // rg*32 + (lane&15) and +16, half lane>>4
-                static_assert(F::kTMA, "two-row IQ3 decode reads the tensor-map layout");
                 const int hl = lane >> 4;
                 const uint8_t* box = st + cw * (kTileRows * F::kBoxBytes) + (rg * kRows + (lane & 15)) * F::kBoxBytes;
                 uint32_t vi[2][8], vs[2][4], dbits[2];
@@ -982,15 +814,13 @@ __global__ void __launch_bounds__(RG * F::kCols * 32 + 32, MINB)
 #undef QG_IQ3_HALF
                 }
                 const uint8_t* tb = smem + L.table;
-                iq3_half2<MT>(vi, vs, dbits, tb, tb + kIQ3GridBytes, lane8, lane4, xb + 128 * hl, xstride, M, acc2);
+                iq3_half2<MT>(vi, vs, dbits, tb, tb + kIQ3GridBytes, lane8, lane4, xb + XH * hl, xstride, M, acc2);
             } else {
                 if (r < rows) {
-                    // row-copy layout: the row's kCols blocks back to back; TMA
-                    // layout: block cw's box, shifted so that rowp + (98*cw & ~15)
+                    // block cw's box row, shifted so that rowp + (98*cw & ~15)
                     // is the box row
-                    const uint8_t* rowp = F::kTMA ? st + cw * (kTileRows * F::kBoxBytes) + r * F::kBoxBytes -
-                                                        ((cw * F::kBytes) & ~15)
-                                                  : st + r * F::kRowStride;
+                    const uint8_t* rowp =
+                        st + cw * (kTileRows * F::kBoxBytes) + r * F::kBoxBytes - ((cw * F::kBytes) & ~15);
                     const uint8_t* tb = smem + L.table;
                     uint32_t v[24], dbits;
                     switch (cw) {
@@ -1003,7 +833,7 @@ __global__ void __launch_bounds__(RG * F::kCols * 32 + 32, MINB)
                         case 6: iq3_load_block<6>(rowp, v, dbits); break;
                         default: iq3_load_block<7>(rowp, v, dbits); break;
                     }
-                    iq3_block<MT, PACKED>(v, dbits, tb, tb + kIQ3GridBytes, lane8, lane4, xb, xstride, M, acc);
+                    iq3_block<MT>(v, dbits, tb, tb + kIQ3GridBytes, lane8, lane4, xb, xstride, M, acc);
                 }
             }
         }

@@ -64,7 +64,7 @@ __global__ void __launch_bounds__(kCols * 32 + 32, 2)
     constexpr int kConsumerThreads = kWarps * 32;
     constexpr int kTileRows = kRows;
     extern __shared__ __align__(128) uint8_t smem[];
-    const Layout L = make_layout(false, MT, true, 1, stages, F::kRowStride);
+    const Layout L = make_layout(false, MT, F::kXH, 1, stages, F::kRowStride);
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.full);
     uint64_t* empty = reinterpret_cast<uint64_t*>(smem + L.empty);
     float* sxw = reinterpret_cast<float*>(smem + L.sx);
@@ -166,11 +166,11 @@ __global__ void __launch_bounds__(kCols * 32 + 32, 2)
                         const float* xb = reinterpret_cast<const float*>(st + L.xoff) + cw * 256;
                         constexpr int64_t xstride = kCols * 256;
                         float* sxp = sxw + warp * MT * 8;
-                        q4k_stage_x<MT, 3>(const_cast<float*>(xb), xstride, sxp, M, lane);
+                        q4k_stage_x<MT, true, 128>(const_cast<float*>(xb), xstride, sxp, M, lane);
                         __syncwarp();
                         // two rows per lane, half a block each (same arithmetic as the
                         // single-launch GEMV; rows past the tile end are discarded)
-                        q4k_half2<MT>(st + (lane & 15) * F::kRowStride + cw * F::kBytes, 16 * F::kRowStride, lane >> 4,
+                        q4k_half2<MT, 128>(st + (lane & 15) * F::kRowStride + cw * F::kBytes, 16 * F::kRowStride, lane >> 4,
                                       xb, xstride, sxp, M, acc);
                         fence_proxy_async_smem();  // x was written: order it before the slot's next copy
                     }
@@ -223,10 +223,10 @@ int launch_pass_t(const pass::Plan& plan, int M, unsigned* sync, cudaStream_t s,
     static bool attr_done[64];
     static int occ_cache[64];
     const int budget = kSmemPerSM / 2 - kSmemReserve;
-    const Layout L1 = make_layout(false, MT, true, 1, 1, FmtQ4K::kRowStride);
+    const Layout L1 = make_layout(false, MT, FmtQ4K::kXH, 1, 1, FmtQ4K::kRowStride);
     int stages = std::min(kMaxStages, (budget - L1.stage0) / L1.stage_bytes);
     if (stages < 2) return QG_EINVAL;
-    const Layout L = make_layout(false, MT, true, 1, stages, FmtQ4K::kRowStride);
+    const Layout L = make_layout(false, MT, FmtQ4K::kXH, 1, stages, FmtQ4K::kRowStride);
     auto kern = pass::gemv_pass_kernel<MT>;
     if (!attr_done[dev]) {
         if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L.total) != cudaSuccess)

@@ -24,18 +24,18 @@ int launch_group_q4k(const uint8_t* const* W, float* const* Y, const int64_t* N,
         const float* Xg = X + static_cast<int64_t>(m0) * K;
         int rc;
         if (mg == 1 && csize > 1)
-            rc = launch_gemv<FmtQ4KT, 1, true, 1, true, 2, 4>(W, Y, N, count, m0, nullptr, Xg, mg, K, s, status, dev, flags,
+            rc = launch_gemv<FmtQ4KT, 1, true, 1, 2>(W, Y, N, count, m0, nullptr, Xg, mg, K, s, status, dev, flags,
                                                               csize);
         else if (mg == 1 && few_tiles)  // one CTA per SM: a deeper ring prefetches every unit of a tile
-            rc = launch_gemv<FmtQ4KT, 1, true, 1, true, 1, 4>(W, Y, N, count, m0, nullptr, Xg, mg, K, s, status, dev, flags);
+            rc = launch_gemv<FmtQ4KT, 1, true, 1, 1>(W, Y, N, count, m0, nullptr, Xg, mg, K, s, status, dev, flags);
         else if (mg == 1)
-            rc = launch_gemv<FmtQ4KT, 1, true, 1, true, 2, 4>(W, Y, N, count, m0, nullptr, Xg, mg, K, s, status, dev, flags);
+            rc = launch_gemv<FmtQ4KT, 1, true, 1, 2>(W, Y, N, count, m0, nullptr, Xg, mg, K, s, status, dev, flags);
         else if (mg == 2)
-            rc = launch_gemv<FmtQ4KT, 2, true, 1, true, 2, 4>(W, Y, N, count, m0, nullptr, Xg, mg, K, s, status, dev, flags);
+            rc = launch_gemv<FmtQ4KT, 2, true, 1, 2>(W, Y, N, count, m0, nullptr, Xg, mg, K, s, status, dev, flags);
         else if (mg <= 4)
-            rc = launch_gemv<FmtQ4KT, 4, true, 1, true, 1, 4>(W, Y, N, count, m0, nullptr, Xg, mg, K, s, status, dev, flags);
+            rc = launch_gemv<FmtQ4KT, 4, true, 1, 1>(W, Y, N, count, m0, nullptr, Xg, mg, K, s, status, dev, flags);
         else
-            rc = launch_gemv<FmtQ4KT, 8, false, 1, true, 1>(W, Y, N, count, m0, nullptr, Xg, mg, K, s, status, dev, flags);
+            rc = launch_gemv<FmtQ4KT, 8, false, 1, 1>(W, Y, N, count, m0, nullptr, Xg, mg, K, s, status, dev, flags);
         if (rc != QG_OK) return rc;
     }
     return QG_OK;

@@ -25,21 +25,21 @@ inline int sm_count(int dev) {
     return cache[dev];
 }
 
-// Launch gemv_kernel<F, MT, XS, RG, PACKED, MINB> over `count` matrices that
+// Launch gemv_kernel<F, MT, XS, RG, MINB> over `count` matrices that
 // share X (token offset m0 already applied to X; Y[i] + m0*N[i] here): MINB
 // CTAs per SM, as many pipeline stages as fit in the per-CTA share of shared
 // memory.
-template <class F, int MT, bool XS, int RG, bool PACKED, int MINB, int CVT = 2>
+template <class F, int MT, bool XS, int RG, int MINB>
 int launch_gemv(const uint8_t* const* W, float* const* Y, const int64_t* N, int count, int m0, const uint8_t* grid,
                 const float* X, int M, int64_t K, cudaStream_t s, unsigned* status, int dev, unsigned flags,
                 int csize = 1) {
     static bool attr_done[64];
     const int budget = std::min(kSmemPerCTA, kSmemPerSM / MINB - kSmemReserve);
-    const Layout L1 = make_layout(F::kIQ3, MT, XS, RG, 1, F::kRowStride, F::kCols);
+    const Layout L1 = make_layout(F::kIQ3, MT, XS ? F::kXH : 0, RG, 1, F::kRowStride, F::kCols);
     const int stages = std::min(kMaxStages, (budget - L1.stage0) / L1.stage_bytes);
     if (stages < 2) return QG_EINVAL;
-    const Layout L = make_layout(F::kIQ3, MT, XS, RG, stages, F::kRowStride, F::kCols);
-    auto kern = gemv_kernel<F, MT, XS, RG, PACKED, MINB, CVT>;
+    const Layout L = make_layout(F::kIQ3, MT, XS ? F::kXH : 0, RG, stages, F::kRowStride, F::kCols);
+    auto kern = gemv_kernel<F, MT, XS, RG, MINB>;
     if (!attr_done[dev]) {
         if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L.total) != cudaSuccess)
             return QG_ECUDA;
@@ -55,12 +55,13 @@ int launch_gemv(const uint8_t* const* W, float* const* Y, const int64_t* N, int 
         G.tile0[i + 1] = G.tile0[i] + (N[i] + RG * kRows - 1) / (RG * kRows);
     }
     TMaps T = {};
-    if constexpr (F::kTMA) {
+    {
         const uint64_t pitch = static_cast<uint64_t>(K / 256) * F::kBytes;
         for (int i = 0; i < count; ++i)
             if (!encode_byte_rows(&T.m[i], W[i], pitch, static_cast<uint64_t>(N[i]), F::kBoxBytes, RG * kRows))
                 return QG_ECUDA;
     }
+    if (XS && F::kXH == kXHalf && !encode_x_halves(&T.xm, X, static_cast<uint64_t>(M) * static_cast<uint64_t>(K / 128))) return QG_ECUDA;
     const int64_t ntiles = G.tile0[count];
     const int sms = sm_count(dev);
     if (sms <= 0) return QG_ECUDA;

@@ -39,4 +39,21 @@ inline bool encode_byte_rows(CUtensorMap* map, const uint8_t* base, uint64_t pit
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Activations X [M][K] fp32 viewed as rows of 128 floats ([M*K/128][128]);
+// box = 132 floats x 16 rows.  The 4 floats past each 128-float row lie
+// outside the tensor and arrive as zeros, so one box lands as 16 row halves
+// 528 bytes apart: the padded per-column x layout of the GEMV stages.
+// X must be 16-byte aligned and K a multiple of 256.
+inline bool encode_x_halves(CUtensorMap* map, const float* X, uint64_t rows) {
+    auto encode = tensor_map_encoder();
+    if (!encode) return false;
+    const cuuint64_t gdim[2] = {128, rows};
+    const cuuint64_t gstride[1] = {512};
+    const cuuint32_t box[2] = {132, 16};
+    const cuuint32_t estr[2] = {1, 1};
+    return encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float*>(X), gdim, gstride, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 }  // namespace qg
