@@ -183,6 +183,70 @@ def profiled_traffic(workload, M):
 
 
 # ------------------------------------------------------------------ our arm
+def fused_step_launches(lib, qgemv, host, dev, keep):
+    """The TinyLlama-shaped decode step with its data flow on the device, every
+    GEMV fused (page 2 "Candle", Block::forward; page 1 model_forward): per
+    layer q/k/v = rmsnorm(x) W^T (one grouped launch), x += q Wo^T (q stands
+    in for the attention output, which is outside this library), gate/up =
+    rmsnorm(x) W^T (grouped), x += (silu(gate) * up) Wd^T; then logits =
+    rmsnorm(x) Wout^T.  89 launches, the weights of the plain pass; the norm
+    weights are seeded 1 + 0.1 N(0, 1).  Returns (launches, x, logits, x0)."""
+    import numpy as np
+    import torch
+    rng = np.random.default_rng(12345)
+    D = host[0][1]
+    mats = [torch.from_numpy(h[3]).to(dev) for h in host]
+    keep.extend(mats)
+    x0 = host[0][5].reshape(-1).astype(np.float32)
+    x = torch.from_numpy(x0.copy()).to(dev)
+    qkv = [torch.empty(h[2], dtype=torch.float32, device=dev) for h in host[0:3]]
+    gu = [torch.empty(h[2], dtype=torch.float32, device=dev) for h in host[4:6]]
+    logits = torch.empty(host[154][2], dtype=torch.float32, device=dev)
+    keep.extend([x, logits, *qkv, *gu])
+    fl = qgemv.QG_PREFETCH_WEIGHTS
+    lst = []
+
+    def fz(norm=None, up=None, res=None):
+        f = qgemv.fuse_struct(norm, 1e-5, up, (res,))
+        keep.append(f)
+        return ctypes.byref(f)
+
+    def norm_w():
+        g = torch.from_numpy((1.0 + 0.1 * rng.standard_normal(D)).astype(np.float32)).to(dev)
+        keep.append(g)
+        return g
+
+    for l in range(22):
+        b = 7 * l
+        ws = [mats[b + i] for i in range(7)]
+        Ns = [host[b + i][2] for i in range(7)]
+        Wa = (ctypes.c_void_p * 3)(*[w.data_ptr() for w in ws[0:3]])
+        Ya = (ctypes.c_void_p * 3)(*[t.data_ptr() for t in qkv])
+        Na = (ctypes.c_int64 * 3)(*Ns[0:3])
+        Wb = (ctypes.c_void_p * 2)(*[w.data_ptr() for w in ws[4:6]])
+        Yb = (ctypes.c_void_p * 2)(*[t.data_ptr() for t in gu])
+        Nb = (ctypes.c_int64 * 2)(*Ns[4:6])
+        keep.append((Wa, Ya, Na, Wb, Yb, Nb))
+        F = host[b + 4][2]
+        wq = sum(weight_bytes("q4k", D, n) for n in Ns[0:3])
+        lst.append((lib.qgemv_q4k_fused_group, (Wa, Ya, Na, 3, x.data_ptr(), 1, D, fz(norm=norm_w()), fl), wq,
+                    wq + 8 * D + 4 * sum(Ns[0:3]), "fused qkv+rmsnorm"))
+        wo = weight_bytes("q4k", D, D)
+        lst.append((lib.qgemv_q4k_fused, (ws[3].data_ptr(), qkv[0].data_ptr(), x.data_ptr(), 1, D, D,
+                                          fz(res=x), fl), wo, wo + 4 * D + 8 * D, "fused o+residual"))
+        wg = 2 * weight_bytes("q4k", D, F)
+        lst.append((lib.qgemv_q4k_fused_group, (Wb, Yb, Nb, 2, x.data_ptr(), 1, D, fz(norm=norm_w()), fl), wg,
+                    wg + 8 * D + 8 * F, "fused gate/up+rmsnorm"))
+        wd = weight_bytes("q4k", F, D)
+        lst.append((lib.qgemv_q4k_fused, (ws[6].data_ptr(), gu[0].data_ptr(), x.data_ptr(), 1, D, F,
+                                          fz(up=gu[1], res=x), fl), wd, wd + 8 * F + 8 * D, "fused down+swiglu+residual"))
+    V = host[154][2]
+    wv = weight_bytes("q4k", D, V)
+    lst.append((lib.qgemv_q4k_fused, (mats[154].data_ptr(), x.data_ptr(), logits.data_ptr(), 1, V, D,
+                                      fz(norm=norm_w()), fl), wv, wv + 8 * D + 4 * V, "fused output+rmsnorm"))
+    return lst, x, logits, x0
+
+
 def run_ours(args, rank, world, local_rank):
     import numpy as np
     import torch
@@ -211,12 +275,20 @@ def run_ours(args, rank, world, local_rank):
     # device buffers: weights (rotated copies), x / y concatenated per pass
     xs_host = np.concatenate([host[g[0]][5].reshape(-1) for g in groups]).astype(np.float32)
     ys_len = sum(M * h[2] for h in host)
-    x_dev = torch.from_numpy(xs_host).to(dev)
-    y_dev = torch.empty(ys_len, dtype=torch.float32, device=dev)
     launches = []   # per copy: list of (fn, args, wbytes, algo_bytes, label)
     keep = []
     fl = 0 if args.no_prefetch else qgemv.QG_PREFETCH_WEIGHTS
-    for c in range(copies):
+    fused = args.mode == "fused"
+    if fused:
+        if args.workload != "tinyllama" or M != 1:
+            raise SystemExit("--mode fused runs the TinyLlama-shaped decode step at M=1")
+        lst, x_dev, y_dev, xs_host = fused_step_launches(lib, qgemv, host, dev, keep)
+        ys_len = y_dev.numel()
+        launches.append(lst)
+    else:
+        x_dev = torch.from_numpy(xs_host).to(dev)
+        y_dev = torch.empty(ys_len, dtype=torch.float32, device=dev)
+    for c in range(0 if fused else copies):
         xo, yo = 0, 0
         lst = []
         for grp in groups:
@@ -409,6 +481,8 @@ def run_ours(args, rank, world, local_rank):
     achieved = (algo / len(flat)) / (avg_launch_ms * 1e-3) / 1e9
     if args.mode == "pass" and args.workload == "tinyllama":
         kname = "qgemv_q4k_pass gemv_pass_kernel"
+    elif fused:
+        kname = "qgemv_q4k_fused gemv_kernel<FmtQ4KT, FUSE>"
     elif mats[0][0] == "q4k":
         kname = ("qgemm_q4k_batched gemm_q4k_tc_kernel (tcgen05)" if M >= 16 else
                  "qgemv_q4k gemv_kernel<FmtQ4KT>")
@@ -444,6 +518,9 @@ def run_ours(args, rank, world, local_rank):
                    "launch": ("one persistent cooperative launch per pass (qgemv_q4k_pass); stage i reads x only "
                               "after every CTA finished stage i-1; weights of later stages stream meanwhile"
                               if args.mode == "pass" and args.workload == "tinyllama" else
+                              "decode step with its data flow on the device: fused RMSNorm / SwiGLU prologues "
+                              "and residual epilogues, each GEMV reading the previous one's output "
+                              "(programmatic dependent launch)" if fused else
                               "stream-ordered" if args.no_prefetch else
                               "programmatic dependent launch: each GEMV streams its first weight tiles while "
                               "the previous one finishes and waits for it before reading x")},
@@ -451,7 +528,9 @@ def run_ours(args, rank, world, local_rank):
         "pct_of_hbm_peak": round(100 * value / world / peak, 1),
         "e2e": {"value": round(e2e_value, 1), "unit": "GB/s", "h2d_bytes_per_step": int(xs_host.nbytes),
                 "d2h_bytes_per_step": int(4 * ys_len),
-                "note": "pinned host x -> device, graph of C-ABI launches, device y -> pinned host, every step"},
+                "note": ("pinned host x (the embedding row) -> device, graph of C-ABI launches, device logits -> "
+                         "pinned host, every step" if fused else
+                         "pinned host x -> device, graph of C-ABI launches, device y -> pinned host, every step")},
         "gpu_launches": len(flat) * args.steps * (1 if M <= 8 or M >= 16 else (M + 7) // 8),
         "mode": args.mode,
         "roofline": roof,
@@ -529,9 +608,10 @@ def main():
     ap.add_argument("--M", type=int, default=1)
     ap.add_argument("--cpu-baseline-s", type=float, default=12.0)
     ap.add_argument("--no-prefetch", action="store_true", help="plain stream-ordered launches")
-    ap.add_argument("--mode", choices=["pass", "group", "single"], default="group",
+    ap.add_argument("--mode", choices=["pass", "group", "single", "fused"], default="group",
                     help="decode pass as one persistent launch (pass), one launch per q/k/v or gate/up group "
-                         "(group), or one launch per matrix (single)")
+                         "(group), one launch per matrix (single), or the decode step with fused RMSNorm / "
+                         "SwiGLU / residual and its data flow on the device (fused)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

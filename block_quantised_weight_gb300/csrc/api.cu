@@ -6,6 +6,7 @@
 #include <mutex>
 
 #include "common.cuh"
+#include "gemv_kernel.cuh"
 #include "launch.h"
 
 namespace {
@@ -159,7 +160,63 @@ int qgemv_q4k_group(const uint8_t* const* W, float* const* Y, const int64_t* N, 
     if (rc != QG_OK) return rc;
     unsigned* st = status_ptr();
     if (!st) return QG_ECUDA;
-    return qg::launch_group_q4k(W, Y, N, count, X, M, K, stream, st, flags);
+    return qg::launch_group_q4k(W, Y, N, count, X, M, K, stream, st, flags, nullptr);
+}
+
+// Fused calls: the group checks, then the prologue operands and residuals.
+static int check_fuse(const qg_fuse* f, float* const* Y, const int64_t* N, int count, int M, int64_t K) {
+    if (!f) return QG_OK;
+    if (f->norm_weight && f->up) return QG_EINVAL;
+    if ((f->norm_weight || f->up) && M > 4) return QG_EINVAL;
+    if (f->norm_weight && !(f->norm_eps >= 0.f && f->norm_eps <= 3.0e38f)) return QG_EINVAL;
+    if ((f->norm_weight && !aligned16(f->norm_weight)) || (f->up && !aligned16(f->up))) return QG_EALIGN;
+    for (int i = 0; i < count; ++i) {
+        const int64_t yb = int64_t(M) * N[i] * 4;
+        if (f->residual[i] && !aligned16(f->residual[i])) return QG_EALIGN;
+        if ((f->norm_weight && overlap(Y[i], yb, f->norm_weight, K * 4)) ||
+            (f->up && overlap(Y[i], yb, f->up, int64_t(M) * K * 4)))
+            return QG_EALIAS;
+        for (int j = 0; j < count; ++j) {
+            const float* r = f->residual[j];
+            if (!r) continue;
+            // a residual may be its own matrix's output, exactly; nothing else
+            if (j == i ? (r != Y[i] && overlap(Y[i], yb, r, yb)) : overlap(Y[i], yb, r, int64_t(M) * N[j] * 4))
+                return QG_EALIAS;
+        }
+    }
+    return QG_OK;
+}
+
+static qg::Fuse to_fuse(const qg_fuse* f) {
+    qg::Fuse z = {};
+    if (f) {
+        z.g = f->norm_weight;
+        z.eps = f->norm_eps;
+        z.up = f->up;
+        for (int i = 0; i < QG_MAX_GROUP; ++i) z.R[i] = f->residual[i];
+    }
+    return z;
+}
+
+int qgemv_q4k_fused_group(const uint8_t* const* W, float* const* Y, const int64_t* N, int count, const float* X,
+                          int M, int64_t K, const qg_fuse* fuse, unsigned flags, cudaStream_t stream) {
+    if (flags & ~static_cast<unsigned>(QG_PREFETCH_WEIGHTS)) return QG_EINVAL;
+    int rc = check_group(W, Y, N, count, nullptr, false, X, M, K, 144);
+    if (rc != QG_OK) return rc;
+    rc = check_fuse(fuse, Y, N, count, M, K);
+    if (rc != QG_OK) return rc;
+    unsigned* st = status_ptr();
+    if (!st) return QG_ECUDA;
+    const qg::Fuse z = to_fuse(fuse);
+    return qg::launch_group_q4k_fused(W, Y, N, count, X, M, K, stream, st, flags, z);
+}
+
+int qgemv_q4k_fused(const uint8_t* W, const float* X, float* Y, int M, int64_t N, int64_t K, const qg_fuse* fuse,
+                    unsigned flags, cudaStream_t stream) {
+    if (fuse)
+        for (int i = 1; i < QG_MAX_GROUP; ++i)
+            if (fuse->residual[i]) return QG_EINVAL;
+    return qgemv_q4k_fused_group(&W, &Y, &N, 1, X, M, K, fuse, flags, stream);
 }
 
 int qgemv_iq3_group(const uint8_t* const* W, float* const* Y, const int64_t* N, int count, const uint8_t* grid,

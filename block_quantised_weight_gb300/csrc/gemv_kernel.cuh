@@ -112,7 +112,22 @@ constexpr int kMaxCluster = 8;
 __host__ __device__ inline int64_t min64(int64_t a, int64_t b) { return a < b ? a : b; }
 
 struct Layout {
-    int full, empty, sx, red, cred, table, stage0, stage_bytes, xoff, total;
+    int full, empty, sx, red, cred, ss, table, stage0, stage_bytes, xoff, aoff, total;
+};
+
+// Fused prologue / epilogue of a GEMV (page 2 "Candle", RmsNorm::forward
+// and Block::forward: h = rmsnorm(x) before q/k/v and gate/up,
+// down(silu(gate) * up), residual adds).  Kernel template FUSE selects the
+// prologue: 0 none, kFuseNorm x' = x * g / rms(x), kFuseSwiGLU
+// x' = silu(x) * up.  R[i] (residual of matrix i, [M][N[i]], may be Y[i]
+// itself) is added to the output when not null, with any FUSE.
+constexpr int kFuseNorm = 1;
+constexpr int kFuseSwiGLU = 2;
+struct Fuse {
+    const float* g;    // RMSNorm weight [K]
+    const float* up;   // SwiGLU up operand [M][K]
+    const float* R[4]; // residuals (one per matrix of the group), or null
+    float eps;         // RMSNorm epsilon
 };
 
 // Up to kMaxGroup matrices that share X and K, processed by one launch.
@@ -149,7 +164,7 @@ __device__ __forceinline__ int group_find(const Group& G, int64_t tile) {
 // xh = F::kXH when x is staged with the weights, 0 when it is read from
 // global memory.
 __host__ __device__ inline Layout make_layout(bool iq3, int MT, int xh, int RG, int stages, int row_stride,
-                                              int cols = kCols) {
+                                              int cols = kCols, int fuse = 0) {
     Layout L;
     const int warps = RG * cols;
     L.full = 0;
@@ -157,10 +172,14 @@ __host__ __device__ inline Layout make_layout(bool iq3, int MT, int xh, int RG, 
     L.sx = 128;
     L.red = L.sx + align_up(warps * MT * 8 * 4, 128);
     L.cred = L.red + align_up(2 * warps * MT * kRows * 4, 128);
-    L.table = L.cred + align_up(kMaxCluster * MT * RG * kRows * 4, 128);
+    L.ss = L.cred + align_up(kMaxCluster * MT * (RG * kRows + 1) * 4, 128);
+    L.table = L.ss + align_up(2 * warps * MT * 4, 128);
     L.stage0 = L.table + (iq3 ? kIQ3TableBytes : 0);
     L.xoff = align_up(RG * kRows * row_stride, 128);
-    L.stage_bytes = L.xoff + MT * cols * 8 * xh;  // xh: F::kXH with x staged, else 0
+    L.aoff = L.xoff + MT * cols * 8 * xh;  // xh: F::kXH with x staged, else 0
+    // prologue operands staged beside x: RMSNorm weight (shared by the
+    // tokens) or the SwiGLU up operand (per token), 1 KB per column
+    L.stage_bytes = L.aoff + (fuse == kFuseNorm ? cols * 1024 : fuse == kFuseSwiGLU ? MT * cols * 1024 : 0);
     L.total = L.stage0 + stages * L.stage_bytes;
     return L;
 }
@@ -187,22 +206,46 @@ __device__ __forceinline__ float half_hi(uint32_t h) {
     return __half2float(__ushort_as_half(static_cast<unsigned short>(h >> 16)));
 }
 
+// SiLU (page 2 "Candle", Block::forward's silu): z * sigmoid(z).
+__device__ __forceinline__ float silu(float z) { return z / (1.f + expf(-z)); }
+
 // Per-warp x preparation for one Q4_K super-block column (256 x values per
 // token; half 1, x[128..255], starts XH floats after half 0):
 // sx[m*8 + j] = sum of x over sub-block j (the dmin*mn term's factor), and
 // with SCALE the x values (in smem) are scaled in place by 2^(88-c),
 // c = 4*(high nibble) + 8*(odd byte), the bit offsets at which q4k_half2
 // finds each nibble.  The scaling is exact for |x| < 2^40; larger values
-// overflow to inf.  Callers that write x in smem must fence it against the
-// next bulk copy into the same slot.
-template <int MT, bool SCALE, int XH>
-__device__ __forceinline__ void q4k_stage_x(float* xb, int64_t xstride, float* sx, int M, int lane) {
+// overflow to inf.  With FUSE the prologue (kFuseNorm: x * g, sum of x^2
+// into ss; kFuseSwiGLU: silu(x) * up) is applied first, reading g or up at
+// ab (+ m * astride), laid out like x; sx and the scaling see the result.
+// Callers that write x in smem must fence it against the next bulk copy
+// into the same slot.
+template <int MT, bool SCALE, int XH, int FUSE = 0>
+__device__ __forceinline__ void q4k_stage_x(float* xb, int64_t xstride, const float* ab, int64_t astride, float* sx,
+                                            float (&ss)[MT], int M, int lane) {
 #pragma unroll
     for (int m = 0; m < MT; ++m) {
         if (MT == 1 || m < M) {
-            float* xp = xb + m * xstride + (lane >> 4) * XH + ((lane >> 2) & 3) * 32 + (lane & 3) * 8;
+            const int off = (lane >> 4) * XH + ((lane >> 2) & 3) * 32 + (lane & 3) * 8;
+            float* xp = xb + m * xstride + off;
             float4 a = *reinterpret_cast<const float4*>(xp);
             float4 b = *reinterpret_cast<const float4*>(xp + 4);
+            if constexpr (FUSE == kFuseNorm) {
+                // RMSNorm prologue: sum of squares of the raw x (1/rms is
+                // applied to the finished row sums), then x * g
+                ss[m] = fmaf(a.x, a.x, fmaf(a.y, a.y, fmaf(a.z, a.z, fmaf(a.w, a.w, ss[m]))));
+                ss[m] = fmaf(b.x, b.x, fmaf(b.y, b.y, fmaf(b.z, b.z, fmaf(b.w, b.w, ss[m]))));
+                const float4 ga = *reinterpret_cast<const float4*>(ab + off);
+                const float4 gb = *reinterpret_cast<const float4*>(ab + off + 4);
+                a = make_float4(a.x * ga.x, a.y * ga.y, a.z * ga.z, a.w * ga.w);
+                b = make_float4(b.x * gb.x, b.y * gb.y, b.z * gb.z, b.w * gb.w);
+            } else if constexpr (FUSE == kFuseSwiGLU) {
+                // SwiGLU prologue: silu(gate) * up, gate being x
+                const float4 ua = *reinterpret_cast<const float4*>(ab + m * astride + off);
+                const float4 ub = *reinterpret_cast<const float4*>(ab + m * astride + off + 4);
+                a = make_float4(silu(a.x) * ua.x, silu(a.y) * ua.y, silu(a.z) * ua.z, silu(a.w) * ua.w);
+                b = make_float4(silu(b.x) * ub.x, silu(b.y) * ub.y, silu(b.z) * ub.z, silu(b.w) * ub.w);
+            }
             float sm = ((a.x + a.y) + (a.z + a.w)) + ((b.x + b.y) + (b.z + b.w));
             sm += __shfl_xor_sync(0xffffffffu, sm, 1);
             sm += __shfl_xor_sync(0xffffffffu, sm, 2);
@@ -212,6 +255,8 @@ __device__ __forceinline__ void q4k_stage_x(float* xb, int64_t xstride, float* s
                 const float so = se * 0x1p-8f;                            // odd byte
                 a = make_float4(a.x * se, a.y * so, a.z * se, a.w * so);
                 b = make_float4(b.x * se, b.y * so, b.z * se, b.w * so);
+            }
+            if constexpr (SCALE || FUSE != 0) {
                 *reinterpret_cast<float4*>(xp) = a;
                 *reinterpret_cast<float4*>(xp + 4) = b;
             }
@@ -582,10 +627,11 @@ __device__ __forceinline__ void named_barrier_sync(int id) {
 // XS: x staged in shared memory with each unit (padded layout above) and
 // the two-row decode (lane L: rows L&15 and (L&15)+16, half L>>4 of each
 // block); otherwise x read from global memory and one row per lane.
-template <class F, int MT, bool XS, int RG, int MINB>
+template <class F, int MT, bool XS, int RG, int MINB, int FUSE = 0>
 __global__ void __launch_bounds__(RG * F::kCols * 32 + 32, MINB)
-    gemv_kernel(const __grid_constant__ Group G, const __grid_constant__ TMaps T, const uint8_t* __restrict__ grid,
-                const float* __restrict__ X, int M, int64_t K, int stages, unsigned* status, int flags) {
+    gemv_kernel(const __grid_constant__ Group G, const __grid_constant__ TMaps T, const __grid_constant__ Fuse Fz,
+                const uint8_t* __restrict__ grid, const float* __restrict__ X, int M, int64_t K, int stages,
+                unsigned* status, int flags) {
     constexpr int kWarps = RG * F::kCols;          // consumer warps
     constexpr int kConsumerThreads = kWarps * 32;
     constexpr int kTileRows = RG * kRows;
@@ -594,7 +640,8 @@ __global__ void __launch_bounds__(RG * F::kCols * 32 + 32, MINB)
     const int nchunks = (nb + F::kCols - 1) / F::kCols;
     const int64_t ntiles = G.tile0[G.count];
     constexpr int XH = XS ? F::kXH : 0;  // floats from half 0 to half 1 of a staged x column
-    const Layout L = make_layout(F::kIQ3, MT, XH, RG, stages, F::kRowStride, F::kCols);
+    const Layout L = make_layout(F::kIQ3, MT, XH, RG, stages, F::kRowStride, F::kCols, FUSE);
+    static_assert(FUSE == 0 || (XS && !F::kIQ3), "fused prologues run on the staged Q4_K path");
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.full);
     uint64_t* empty = reinterpret_cast<uint64_t*>(smem + L.empty);
     float* sxw = reinterpret_cast<float*>(smem + L.sx);
@@ -700,9 +747,12 @@ __global__ void __launch_bounds__(RG * F::kCols * 32 + 32, MINB)
             // columns as 16 padded halves; halves past the chunk are never
             // read); contiguous layout: one bulk copy per token
             constexpr bool kXBox = (XH == kXHalf);
+            constexpr int kAuxTokens = FUSE == kFuseSwiGLU ? 1 : 0;  // up: per token; g: once
             if (expect) {
+                const uint32_t aux = FUSE == 0 ? 0u : (kAuxTokens ? M : 1) * kc * 1024;
                 if (lane == 0)
-                    mbar_arrive_expect_tx(&full[p.s], kc * kBox + (XS ? M * (kXBox ? kXBoxBytes : kc * 1024) : 0));
+                    mbar_arrive_expect_tx(&full[p.s],
+                                          kc * kBox + (XS ? M * (kXBox ? kXBoxBytes : kc * 1024) : 0) + aux);
                 __syncwarp();
             }
             if (do_w && lane == 0)
@@ -716,6 +766,18 @@ __global__ void __launch_bounds__(RG * F::kCols * 32 + 32, MINB)
                 else
                     bulk_g2s(st + L.xoff + lane * F::kCols * 1024,
                              X + lane * K + static_cast<int64_t>(p.c) * F::kCols * 256, kc * 1024, &full[p.s], pol_x);
+            }
+            // prologue operand slices, laid out like x (they belong to the
+            // dependency chain, as x does)
+            if constexpr (FUSE == kFuseNorm) {
+                if (do_x && lane == 0)
+                    bulk_g2s(st + L.aoff, Fz.g + static_cast<int64_t>(p.c) * F::kCols * 256, kc * 1024, &full[p.s],
+                             pol_x);
+            } else if constexpr (FUSE == kFuseSwiGLU) {
+                if (do_x && lane < M)
+                    bulk_g2s(st + L.aoff + lane * F::kCols * 1024,
+                             Fz.up + lane * K + static_cast<int64_t>(p.c) * F::kCols * 256, kc * 1024, &full[p.s],
+                             pol_x);
             }
         };
         Pos p = first_pos();
@@ -753,8 +815,9 @@ __global__ void __launch_bounds__(RG * F::kCols * 32 + 32, MINB)
     constexpr bool kHalf2 = XS;
     float acc[MT];
     float acc2[2][MT];
+    float ss[MT];  // RMSNorm prologue: this lane's part of sum(x^2) over the tile's units
 #pragma unroll
-    for (int m = 0; m < MT; ++m) acc[m] = acc2[0][m] = acc2[1][m] = 0.f;
+    for (int m = 0; m < MT; ++m) acc[m] = acc2[0][m] = acc2[1][m] = ss[m] = 0.f;
     const uint32_t lane8 = static_cast<uint32_t>(lane) * 8u, lane4 = static_cast<uint32_t>(lane) * 4u;
     int64_t tile_count = 0;
 
@@ -783,7 +846,9 @@ __global__ void __launch_bounds__(RG * F::kCols * 32 + 32, MINB)
             const int64_t xstride = XS ? F::kCols * 2 * XH : K;
             if constexpr (!F::kIQ3) {
                 float* sxp = sxw + warp * MT * 8;
-                q4k_stage_x<MT, XS, XS ? XH : 128>(const_cast<float*>(xb), xstride, sxp, M, lane);
+                const float* ab = reinterpret_cast<const float*>(st + L.aoff) + cw * 256;
+                q4k_stage_x<MT, XS, XS ? XH : 128, FUSE>(const_cast<float*>(xb), xstride, ab, F::kCols * 256, sxp, ss,
+                                                         M, lane);
                 __syncwarp();
                 if constexpr (kHalf2) {
                     const uint8_t* blk = st + cw * (kTileRows * F::kBytes) + (lane & 15) * F::kBytes;
@@ -856,11 +921,33 @@ __global__ void __launch_bounds__(RG * F::kCols * 32 + 32, MINB)
                     acc[m] = 0.f;
                 }
             }
+            // RMSNorm prologue: each warp's sum of x^2 (its columns, all of
+            // the tile's chunks) per token
+            float* ssw = reinterpret_cast<float*>(smem + L.ss) + (tile_count & 1) * (kWarps * MT);
+            if constexpr (FUSE == kFuseNorm) {
+#pragma unroll
+                for (int m = 0; m < MT; ++m) {
+                    float t = ss[m];
+#pragma unroll
+                    for (int o = 16; o > 0; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
+                    if (lane == 0) ssw[warp * MT + m] = t;
+                    ss[m] = 0.f;
+                }
+            }
             named_barrier_sync<kConsumerThreads>(1);
+            // finished row sum -> output: times 1/rms(x) of the token, plus the residual
+            auto finish = [&](int m, int rr, float sum, float sumsq) {
+                if constexpr (FUSE == kFuseNorm) sum *= 1.f / sqrtf(sumsq / static_cast<float>(K) + Fz.eps);
+                const int64_t o = m * Ni + row0 + rr;
+                if (Fz.R[gi]) sum += Fz.R[gi][o];
+                G.Y[gi][o] = sum;
+            };
             if (clus) {
-                // this chunk's row sums -> slot crank of the first CTA; after the
-                // cluster barrier it adds the slots in rank order (deterministic)
+                // this chunk's row sums (and sum of x^2) -> slot crank of the
+                // first CTA; after the cluster barrier it adds the slots in
+                // rank order (deterministic)
                 float* cred = reinterpret_cast<float*>(smem + L.cred);
+                float* cssq = cred + kMaxCluster * MT * kTileRows;
                 __syncwarp();
                 cluster_wait();  // phase 0: all CTAs of the cluster are running
                 for (int t = threadIdx.x; t < MT * kTileRows; t += kConsumerThreads) {
@@ -871,6 +958,11 @@ __global__ void __launch_bounds__(RG * F::kCols * 32 + 32, MINB)
                     for (int w = 0; w < F::kCols; ++w) sum += rb[((g * F::kCols + w) * MT + m) * kRows + ln];
                     st_cluster_f32(cred + crank * MT * kTileRows + t, 0, sum);
                 }
+                if (FUSE == kFuseNorm && threadIdx.x < MT) {
+                    float q = 0.f;
+                    for (int w = 0; w < kWarps; ++w) q += ssw[w * MT + threadIdx.x];
+                    st_cluster_f32(cssq + crank * MT + threadIdx.x, 0, q);
+                }
                 __syncwarp();
                 cluster_arrive_release();
                 cluster_wait();
@@ -878,23 +970,27 @@ __global__ void __launch_bounds__(RG * F::kCols * 32 + 32, MINB)
                     for (int t = threadIdx.x; t < MT * kTileRows; t += kConsumerThreads) {
                         const int m = t / kTileRows, rr = t % kTileRows;
                         if ((MT == 1 || m < M) && rr < rows) {
-                            float sum = 0.f;
+                            float sum = 0.f, sq = 0.f;
                             for (int q = 0; q < csize; ++q) sum += cred[q * MT * kTileRows + t];
-                            G.Y[gi][m * Ni + row0 + rr] = sum;
+                            if (FUSE == kFuseNorm)
+                                for (int q = 0; q < csize; ++q) sq += cssq[q * MT + m];
+                            finish(m, rr, sum, sq);
                         }
                     }
                 }
             } else {
-            for (int t = threadIdx.x; t < MT * kTileRows; t += kConsumerThreads) {
-                const int m = t / kTileRows, rr = t % kTileRows;
-                const int g = rr / kRows, ln = rr % kRows;
-                if ((MT == 1 || m < M) && rr < rows) {
-                    float sum = 0.f;
+                for (int t = threadIdx.x; t < MT * kTileRows; t += kConsumerThreads) {
+                    const int m = t / kTileRows, rr = t % kTileRows;
+                    const int g = rr / kRows, ln = rr % kRows;
+                    if ((MT == 1 || m < M) && rr < rows) {
+                        float sum = 0.f, sq = 0.f;
 #pragma unroll
-                    for (int w = 0; w < F::kCols; ++w) sum += rb[((g * F::kCols + w) * MT + m) * kRows + ln];
-                    G.Y[gi][m * Ni + row0 + rr] = sum;
+                        for (int w = 0; w < F::kCols; ++w) sum += rb[((g * F::kCols + w) * MT + m) * kRows + ln];
+                        if (FUSE == kFuseNorm)
+                            for (int w = 0; w < kWarps; ++w) sq += ssw[w * MT + m];
+                        finish(m, rr, sum, sq);
+                    }
                 }
-            }
             }
             ++tile_count;
         }

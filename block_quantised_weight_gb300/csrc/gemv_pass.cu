@@ -166,7 +166,8 @@ __global__ void __launch_bounds__(kCols * 32 + 32, 2)
                         const float* xb = reinterpret_cast<const float*>(st + L.xoff) + cw * 256;
                         constexpr int64_t xstride = kCols * 256;
                         float* sxp = sxw + warp * MT * 8;
-                        q4k_stage_x<MT, true, 128>(const_cast<float*>(xb), xstride, sxp, M, lane);
+                        float ssq[MT];  // unused: no prologue here
+                        q4k_stage_x<MT, true, 128>(const_cast<float*>(xb), xstride, nullptr, 0, sxp, ssq, M, lane);
                         __syncwarp();
                         // two rows per lane, half a block each (same arithmetic as the
                         // single-launch GEMV; rows past the tile end are discarded)

@@ -1,49 +1,16 @@
-// Q4_K GEMV launcher (fp32 FMA path).  Kernel: gemv_kernel.cuh.
-#include "launch_common.cuh"
+// Q4_K GEMV launcher (fp32 FMA path), no prologue.  Dispatch: launch_q4k.cuh.
+#include "launch_q4k.cuh"
 
 namespace qg {
 
-// count matrices sharing X; M is split into groups of at most 8 tokens, each
-// group streaming W once.
 int launch_group_q4k(const uint8_t* const* W, float* const* Y, const int64_t* N, int count, const float* X, int M,
-                     int64_t K, cudaStream_t s, unsigned* status, unsigned flags) {
-    const int dev = current_device();
-    if (dev < 0) return QG_ECUDA;
-    // Launches with at most one 32-row tile per SM are latency-bound: run them
-    // one CTA per SM with the deepest ring that fits.
-    int64_t tiles = 0;
-    for (int i = 0; i < count; ++i) tiles += (N[i] + kRows - 1) / kRows;
-    const int sms = sm_count(dev);
-    const bool few_tiles = tiles <= sms;
-    // ... and when the tiles' K chunks fit one wave of two CTAs per SM, each
-    // chunk gets its own CTA, the chunks of a tile forming one cluster.
-    const int64_t nchunks = (K / 256 + kCols - 1) / kCols;
-    const int csize = (nchunks > 1 && nchunks <= kMaxCluster && tiles * nchunks <= 2 * sms) ? static_cast<int>(nchunks) : 1;
-    for (int m0 = 0; m0 < M; m0 += 8) {
-        const int mg = std::min(8, M - m0);
-        const float* Xg = X + static_cast<int64_t>(m0) * K;
-        int rc;
-        if (mg == 1 && csize > 1)
-            rc = launch_gemv<FmtQ4KT, 1, true, 1, 2>(W, Y, N, count, m0, nullptr, Xg, mg, K, s, status, dev, flags,
-                                                              csize);
-        else if (mg == 1 && few_tiles)  // one CTA per SM: a deeper ring prefetches every unit of a tile
-            rc = launch_gemv<FmtQ4KT, 1, true, 1, 1>(W, Y, N, count, m0, nullptr, Xg, mg, K, s, status, dev, flags);
-        else if (mg == 1)
-            rc = launch_gemv<FmtQ4KT, 1, true, 1, 2>(W, Y, N, count, m0, nullptr, Xg, mg, K, s, status, dev, flags);
-        else if (mg == 2)
-            rc = launch_gemv<FmtQ4KT, 2, true, 1, 2>(W, Y, N, count, m0, nullptr, Xg, mg, K, s, status, dev, flags);
-        else if (mg <= 4)
-            rc = launch_gemv<FmtQ4KT, 4, true, 1, 1>(W, Y, N, count, m0, nullptr, Xg, mg, K, s, status, dev, flags);
-        else
-            rc = launch_gemv<FmtQ4KT, 8, false, 1, 1>(W, Y, N, count, m0, nullptr, Xg, mg, K, s, status, dev, flags);
-        if (rc != QG_OK) return rc;
-    }
-    return QG_OK;
+                     int64_t K, cudaStream_t s, unsigned* status, unsigned flags, const Fuse* fz) {
+    return launch_group_q4k_t<0>(W, Y, N, count, X, M, K, s, status, flags, fz);
 }
 
 int launch_gemv_q4k(const uint8_t* W, const float* X, float* Y, int M, int64_t N, int64_t K, cudaStream_t s,
                     unsigned* status, unsigned flags) {
-    return launch_group_q4k(&W, &Y, &N, 1, X, M, K, s, status, flags);
+    return launch_group_q4k(&W, &Y, &N, 1, X, M, K, s, status, flags, nullptr);
 }
 
 }  // namespace qg

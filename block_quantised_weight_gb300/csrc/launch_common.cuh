@@ -29,22 +29,31 @@ inline int sm_count(int dev) {
 // share X (token offset m0 already applied to X; Y[i] + m0*N[i] here): MINB
 // CTAs per SM, as many pipeline stages as fit in the per-CTA share of shared
 // memory.
-template <class F, int MT, bool XS, int RG, int MINB>
+template <class F, int MT, bool XS, int RG, int MINB, int FUSE = 0>
 int launch_gemv(const uint8_t* const* W, float* const* Y, const int64_t* N, int count, int m0, const uint8_t* grid,
                 const float* X, int M, int64_t K, cudaStream_t s, unsigned* status, int dev, unsigned flags,
-                int csize = 1) {
+                int csize = 1, const Fuse* fz = nullptr) {
     static bool attr_done[64];
     const int budget = std::min(kSmemPerCTA, kSmemPerSM / MINB - kSmemReserve);
-    const Layout L1 = make_layout(F::kIQ3, MT, XS ? F::kXH : 0, RG, 1, F::kRowStride, F::kCols);
+    const Layout L1 = make_layout(F::kIQ3, MT, XS ? F::kXH : 0, RG, 1, F::kRowStride, F::kCols, FUSE);
     const int stages = std::min(kMaxStages, (budget - L1.stage0) / L1.stage_bytes);
     if (stages < 2) return QG_EINVAL;
-    const Layout L = make_layout(F::kIQ3, MT, XS ? F::kXH : 0, RG, stages, F::kRowStride, F::kCols);
-    auto kern = gemv_kernel<F, MT, XS, RG, MINB>;
+    const Layout L = make_layout(F::kIQ3, MT, XS ? F::kXH : 0, RG, stages, F::kRowStride, F::kCols, FUSE);
+    auto kern = gemv_kernel<F, MT, XS, RG, MINB, FUSE>;
     if (!attr_done[dev]) {
         if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L.total) != cudaSuccess)
             return QG_ECUDA;
         attr_done[dev] = true;
     }
+    // prologue operands and residuals (token offset m0 applied like X, Y)
+    Fuse Fz = {};
+    if (fz) {
+        Fz = *fz;
+        if (Fz.up) Fz.up += static_cast<int64_t>(m0) * K;
+        for (int i = 0; i < count; ++i)
+            if (Fz.R[i]) Fz.R[i] += static_cast<int64_t>(m0) * N[i];
+    }
+    for (int i = count; i < kMaxGroup; ++i) Fz.R[i] = nullptr;
     Group G = {};
     G.count = count;
     G.tile0[0] = 0;
@@ -72,7 +81,7 @@ int launch_gemv(const uint8_t* const* W, float* const* Y, const int64_t* N, int 
     const int kflags = ((flags & QG_PREFETCH_WEIGHTS) ? kFlagPrefetchWeights : 0) |
                        (csize > 1 ? csize << kFlagClusterShift : 0);
     if (!(flags & QG_PREFETCH_WEIGHTS) && csize <= 1) {
-        kern<<<grid_x, RG * F::kCols * 32 + 32, L.total, s>>>(G, T, grid, X, M, K, stages, status, kflags);
+        kern<<<grid_x, RG * F::kCols * 32 + 32, L.total, s>>>(G, T, Fz, grid, X, M, K, stages, status, kflags);
         return cudaGetLastError() == cudaSuccess ? QG_OK : QG_ECUDA;
     }
     // programmatic dependent launch (this grid may start before the previous
@@ -99,7 +108,8 @@ int launch_gemv(const uint8_t* const* W, float* const* Y, const int64_t* N, int 
     }
     cfg.attrs = attr;
     cfg.numAttrs = na;
-    if (cudaLaunchKernelEx(&cfg, kern, G, T, grid, X, M, K, stages, status, kflags) != cudaSuccess) return QG_ECUDA;
+    if (cudaLaunchKernelEx(&cfg, kern, G, T, Fz, grid, X, M, K, stages, status, kflags) != cudaSuccess)
+        return QG_ECUDA;
     return cudaGetLastError() == cudaSuccess ? QG_OK : QG_ECUDA;
 }
 

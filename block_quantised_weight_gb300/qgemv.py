@@ -35,9 +35,13 @@ class QgStage(ctypes.Structure):
     _fields_ = [("W", ctypes.c_void_p * 4), ("Y", ctypes.c_void_p * 4), ("N", ctypes.c_int64 * 4),
                 ("count", ctypes.c_int), ("X", ctypes.c_void_p), ("K", ctypes.c_int64)]
 
+class QgFuse(ctypes.Structure):
+    _fields_ = [("norm_weight", ctypes.c_void_p), ("norm_eps", ctypes.c_float), ("up", ctypes.c_void_p),
+                ("residual", ctypes.c_void_p * 4)]
+
 QG_PREFETCH_WEIGHTS = 1
 
-EXPORTS = ("qgemv_q4k", "qgemv_q4k_ex", "qgemv_q4k_group", "qgemv_q4k_pass", "qgemv_q4k_pass_noalloc", "qgemv_iq3", "qgemv_iq3_ex", "qgemv_iq3_group", "qgemm_q4k_batched", "qdequant_q4k", "qdequant_iq3",
+EXPORTS = ("qgemv_q4k", "qgemv_q4k_ex", "qgemv_q4k_group", "qgemv_q4k_fused", "qgemv_q4k_fused_group", "qgemv_q4k_pass", "qgemv_q4k_pass_noalloc", "qgemv_iq3", "qgemv_iq3_ex", "qgemv_iq3_group", "qgemm_q4k_batched", "qdequant_q4k", "qdequant_iq3",
            "qg_device_status", "qg_test_bounded_wait", "qg_strerror")
 
 
@@ -69,6 +73,8 @@ def load():
             "qgemv_iq3_ex": [vp, vp, vp, vp, ci, i64, i64, ctypes.c_uint, vp],
             "qgemv_q4k_group": [vp, vp, vp, ci, vp, ci, i64, ctypes.c_uint, vp],
             "qgemv_iq3_group": [vp, vp, vp, ci, vp, vp, ci, i64, ctypes.c_uint, vp],
+            "qgemv_q4k_fused": [vp, vp, vp, ci, i64, i64, vp, ctypes.c_uint, vp],
+            "qgemv_q4k_fused_group": [vp, vp, vp, ci, vp, ci, i64, vp, ctypes.c_uint, vp],
             "qgemv_q4k_pass": [vp, ci, ci, vp, vp],
             "qgemv_q4k_pass_noalloc": [vp, ci, ci, vp],
             "qgemm_q4k_batched": [vp, vp, vp, ci, i64, i64, vp],
@@ -206,6 +212,56 @@ def qgemv_iq3_group(Ws, grid, X, outs=None, stream=None, flags=0):
     Wa, Ya, Na = group_arrays(Ws, outs, Ns)
     rc = load().qgemv_iq3_group(Wa, Ya, Na, len(Ws), grid.data_ptr(), Xv.data_ptr(), M, K, flags, _stream(stream))
     _check("qgemv_iq3_group", rc)
+    return outs
+
+
+def fuse_struct(norm_weight=None, eps=0.0, up=None, residuals=()):
+    """qg_fuse from torch CUDA tensors (None disables an operand)."""
+    import torch
+    f = QgFuse()
+    if norm_weight is not None:
+        _req(norm_weight, torch.float32, "norm_weight")
+        f.norm_weight = norm_weight.data_ptr()
+    f.norm_eps = float(eps)
+    if up is not None:
+        _req(up, torch.float32, "up")
+        f.up = up.data_ptr()
+    for i, r in enumerate(residuals):
+        if r is not None:
+            _req(r, torch.float32, "residual")
+            f.residual[i] = r.data_ptr()
+    return f
+
+
+def qgemv_q4k_fused(W, X, out=None, norm_weight=None, eps=0.0, up=None, residual=None, stream=None, flags=0):
+    """Y = h @ dequant(W)^T (+ residual) with h = X, rmsnorm(X; norm_weight, eps)
+    or silu(X) * up (qgemv_q4k_fused).  residual may be `out` itself."""
+    X, out, M, N, K = _xy(W, X, out, 144)
+    f = fuse_struct(norm_weight, eps, up, (residual,))
+    rc = load().qgemv_q4k_fused(W.data_ptr(), X.data_ptr(), out.data_ptr(), M, N, K, ctypes.byref(f), flags,
+                                _stream(stream))
+    _check("qgemv_q4k_fused", rc)
+    return out
+
+
+def qgemv_q4k_fused_group(Ws, X, outs=None, norm_weight=None, eps=0.0, up=None, residuals=(), stream=None,
+                          flags=0):
+    """qgemv_q4k_group with a shared prologue and per-matrix residuals."""
+    import torch
+    Xv = X.view(1, -1) if X.dim() == 1 else X
+    M, K = Xv.shape
+    Ns = []
+    for W in Ws:
+        _req(W, torch.uint8, "W")
+        Ns.append(W.numel() // (K // 256 * 144))
+    if outs is None:
+        outs = [torch.empty((M, n), dtype=torch.float32, device=X.device) for n in Ns]
+    _req(Xv, torch.float32, "X")
+    Wa, Ya, Na = group_arrays(Ws, outs, Ns)
+    f = fuse_struct(norm_weight, eps, up, residuals)
+    rc = load().qgemv_q4k_fused_group(Wa, Ya, Na, len(Ws), Xv.data_ptr(), M, K, ctypes.byref(f), flags,
+                                      _stream(stream))
+    _check("qgemv_q4k_fused_group", rc)
     return outs
 
 

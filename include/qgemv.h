@@ -121,6 +121,42 @@ QG_API int qgemv_iq3_group(const uint8_t* const* W, float* const* Y, const int64
                            const uint8_t* grid, const float* X, int M, int64_t K, unsigned flags,
                            cudaStream_t stream);
 
+/* Fused prologue and epilogue of a Q4_K GEMV inside a decode step.
+ * Page 2 "Candle", RmsNorm::forward (x * (1/sqrt(mean(x^2) + eps)) * weight)
+ * and Block::forward (h = norm(x); x + attn(h); down(silu(gate(h)) * up(h));
+ * the residual adds); page 1 model_forward (rmsnorm before the q/k/v
+ * matmuls and before the output projection).  With h the GEMV input:
+ *   no prologue:   h = X
+ *   norm_weight:   h[m][k] = X[m][k] / sqrt(mean_k' X[m][k']^2 + norm_eps) * norm_weight[k]
+ *   up:            h[m][k] = silu(X[m][k]) * up[m][k],  silu(z) = z / (1 + exp(-z))
+ *   Y[i][m][n] = sum_k dequant(W[i])[n][k] * h[m][k]   (+ residual[i][m][n])
+ * All pointers device, 16-byte aligned, caller-owned; NULL disables an
+ * operand.  norm_weight [K] fp32; up [M][K] fp32; residual[i] [M][N[i]]
+ * fp32, which may be exactly Y[i] (in-place add) but must not otherwise
+ * overlap any Y.  At most one of norm_weight and up; with either, M <= 4.
+ * Numerics: |Y - exact| <= 1e-5 * sum_k |w*h| per element (h exact), plus
+ * the fp32 rounding of the residual add. */
+typedef struct qg_fuse {
+    const float* norm_weight;
+    float norm_eps;                      /* >= 0, finite */
+    const float* up;
+    const float* residual[QG_MAX_GROUP]; /* per matrix of a group; [0] for single calls */
+} qg_fuse;
+
+/* Q4_K GEMV with the prologue / epilogue of `fuse` (NULL: plain GEMV).
+ * Same arguments, layouts and flags as qgemv_q4k_ex; fuse->residual[i] for
+ * i >= 1 must be NULL.  Errors: QG_EINVAL for both prologues, a prologue
+ * with M > 4, a negative or non-finite norm_eps; QG_EALIGN; QG_EALIAS. */
+QG_API int qgemv_q4k_fused(const uint8_t* W, const float* X, float* Y, int M, int64_t N, int64_t K,
+                           const qg_fuse* fuse, unsigned flags, cudaStream_t stream);
+
+/* qgemv_q4k_group with the prologue / epilogue of `fuse` (the prologue is
+ * shared by the matrices, residual[i] belongs to matrix i).  In a decode
+ * step: q/k/v with the attention RMSNorm, gate/up with the FFN RMSNorm. */
+QG_API int qgemv_q4k_fused_group(const uint8_t* const* W, float* const* Y, const int64_t* N, int count,
+                                 const float* X, int M, int64_t K, const qg_fuse* fuse, unsigned flags,
+                                 cudaStream_t stream);
+
 /* One stage of a decode pass: a group of matrices reading the same X. */
 #define QG_MAX_PASS_STAGES 96
 typedef struct qg_stage {

@@ -167,6 +167,54 @@ def gemv_iq3(W, grid, X, rows=None, nthreads=None):
     return _gemv(1, W, grid, X, rows, nthreads)
 
 
+# ------------------------------------------------ decode-step prologues (fp64)
+def rmsnorm(x, weight, eps: float) -> np.ndarray:
+    """Page 2 "Candle", RmsNorm::forward (and the transformers snippet on the
+    same page): x * (1 / sqrt(mean(x^2) + eps)) * weight over the last axis,
+    evaluated in fp64."""
+    x = np.asarray(x, dtype=np.float64)
+    inv = 1.0 / np.sqrt(np.mean(x * x, axis=-1, keepdims=True) + float(eps))
+    return x * inv * np.asarray(weight, dtype=np.float64)
+
+
+def silu(z) -> np.ndarray:
+    """Page 2 "Candle", Block::forward's silu: z * sigmoid(z) = z / (1 + exp(-z)),
+    fp64 (exp(-z) overflowing to inf gives -0, the limit)."""
+    z = np.asarray(z, dtype=np.float64)
+    with np.errstate(over="ignore"):
+        return z / (1.0 + np.exp(-z))
+
+
+def swiglu(gate, up) -> np.ndarray:
+    """Page 2 "Candle", Block::forward: silu(gate(h)) * up(h), fp64."""
+    return silu(gate) * np.asarray(up, dtype=np.float64)
+
+
+def fused_gemv_q4k(W, X, norm_weight=None, eps: float = 0.0, up=None, residual=None):
+    """(Y, A) of a Q4_K GEMV inside a decode step, fp64: h = X, rmsnorm(X) or
+    silu(X) * up; Y = h W^T (+ residual); A = |h| |W|^T (the tolerance scale).
+    W is dequantised by the pinned C oracle (exact fp32 values), then the
+    products are taken by numpy's fp64 matmul."""
+    X = np.asarray(X, dtype=np.float32)
+    if X.ndim == 1:
+        X = X[None, :]
+    K = X.shape[1]
+    if norm_weight is not None and up is not None:
+        raise ValueError("at most one prologue")
+    if norm_weight is not None:
+        h = rmsnorm(X, norm_weight, eps)
+    elif up is not None:
+        h = swiglu(X, np.asarray(up, dtype=np.float32).reshape(X.shape))
+    else:
+        h = X.astype(np.float64)
+    Wd = dequant_q4k(W, K).astype(np.float64)
+    Y = h @ Wd.T
+    A = np.abs(h) @ np.abs(Wd).T
+    if residual is not None:
+        Y = Y + np.asarray(residual, dtype=np.float64).reshape(Y.shape)
+    return Y, A
+
+
 # ------------------------------------------------ block writers (tests only)
 def pack_q4k_scale_min(sc, mn) -> np.ndarray:
     """Inverse of page 1's unpack: eight 6-bit scales and mins -> 12 bytes.

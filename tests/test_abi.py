@@ -98,3 +98,35 @@ def test_group_arguments_rejected_on_host(lib):
     Y3 = (ctypes.c_void_p * 2)(A + 0x2000000, A + 0x2000000 + 128)
     assert lib.qgemv_q4k_group(W, Y3, N, 2, X, 1, 256, 0, None) == qgemv.QG_EALIAS
     assert lib.qgemv_iq3_group(W, Y, N, 2, None, X, 1, 256, 0, None) == qgemv.QG_EINVAL
+
+
+def test_fused_arguments_rejected_on_host(lib):
+    W, X, Y = A, A + 0x10000000, A + 0x20000000
+    g, up = A + 0x30000000, A + 0x40000000
+
+    def call(M=1, N=64, K=256, **kw):
+        f = qgemv.QgFuse()
+        f.norm_weight = kw.get("norm")
+        f.norm_eps = kw.get("eps", 1e-5)
+        f.up = kw.get("up")
+        for i, r in enumerate(kw.get("res", ())):
+            f.residual[i] = r
+        return lib.qgemv_q4k_fused(W, X, kw.get("Y", Y), M, N, K, ctypes.byref(f), 0, None)
+
+    assert call(norm=g, up=up) == qgemv.QG_EINVAL            # two prologues
+    assert call(M=5, norm=g) == qgemv.QG_EINVAL              # prologue needs M <= 4
+    assert call(M=5, up=up) == qgemv.QG_EINVAL
+    assert call(norm=g, eps=-1.0) == qgemv.QG_EINVAL
+    assert call(norm=g, eps=float("nan")) == qgemv.QG_EINVAL
+    assert call(norm=g + 4) == qgemv.QG_EALIGN
+    assert call(up=up + 8) == qgemv.QG_EALIGN
+    assert call(res=(Y + 4,)) == qgemv.QG_EALIGN
+    assert call(res=(Y + 16,)) == qgemv.QG_EALIAS             # partial overlap with Y
+    assert call(norm=Y + 64) == qgemv.QG_EALIAS
+    assert call(res=(None, Y)) == qgemv.QG_EINVAL             # single call: residual[0] only
+    Wg = (ctypes.c_void_p * 2)(A, A + 0x1000000)
+    Yg = (ctypes.c_void_p * 2)(A + 0x2000000, A + 0x3000000)
+    Ng = (ctypes.c_int64 * 2)(64, 64)
+    f = qgemv.QgFuse()
+    f.residual[0] = A + 0x3000000                             # matrix 0's residual is matrix 1's output
+    assert lib.qgemv_q4k_fused_group(Wg, Yg, Ng, 2, X, 1, 256, ctypes.byref(f), 0, None) == qgemv.QG_EALIAS

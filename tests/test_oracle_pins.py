@@ -343,3 +343,67 @@ def test_zero_rows_give_exact_zero():
     x = synth.gen_x(1, K, 2)
     Y, A = oracle.gemv_q4k(W, x)
     assert Y[0, 1] == 0.0 and A[0, 1] == 0.0
+
+
+# ------------------------------------------------- decode-step prologues
+def test_rmsnorm_worked_example():
+    """Page 2 "Candle", RmsNorm::forward on x = (3, 4): mean(x^2) = 12.5, so
+    the outputs are 3/sqrt(12.5) and 4/sqrt(12.5) (worked by hand:
+    0.8485281374238570, 1.1313708498984760), times the weight."""
+    h = oracle.rmsnorm(np.array([3.0, 4.0]), np.array([1.0, 1.0]), 0.0)
+    assert np.allclose(h, [0.8485281374238570, 1.1313708498984760], rtol=1e-15, atol=0)
+    h2 = oracle.rmsnorm(np.array([3.0, 4.0]), np.array([2.0, -0.5]), 0.0)
+    assert np.allclose(h2, [1.6970562748477140, -0.5656854249492380], rtol=1e-15, atol=0)
+    # eps enters under the root: x = (0, 0, 0, 2), eps = 1 -> 2 / sqrt(1 + 1)
+    h3 = oracle.rmsnorm(np.array([0.0, 0.0, 0.0, 2.0]), np.ones(4), 1.0)
+    assert np.allclose(h3, [0, 0, 0, 2 / math.sqrt(2.0)], rtol=1e-15, atol=0)
+
+
+def test_rmsnorm_invariants():
+    rng = np.random.default_rng(11)
+    x = rng.standard_normal((3, 64))
+    w = np.ones(64)
+    h = oracle.rmsnorm(x, w, 0.0)
+    assert np.allclose(np.mean(h * h, axis=-1), 1.0, rtol=1e-13)          # unit mean square
+    assert np.allclose(oracle.rmsnorm(7.5 * x, w, 0.0), h, rtol=1e-13)     # scale invariant
+    assert np.allclose(oracle.rmsnorm(np.full(8, -3.0), np.ones(8), 0.0), -1.0, rtol=1e-15)
+    g = rng.standard_normal(64)
+    assert np.allclose(oracle.rmsnorm(x, g, 0.0), h * g, rtol=1e-13)       # weight is elementwise
+    assert np.all(oracle.rmsnorm(np.zeros(16), np.ones(16), 1e-6) == 0.0)  # eps keeps zero finite
+
+
+def test_silu_closed_forms():
+    """silu(z) = z / (1 + exp(-z)): silu(0) = 0, silu(1) = e / (e + 1),
+    silu(z) - silu(-z) = z, silu(z) -> z for large z and -> 0 for very
+    negative z."""
+    assert oracle.silu(0.0) == 0.0
+    assert abs(oracle.silu(1.0) - math.e / (math.e + 1.0)) < 1e-16
+    z = np.linspace(-30, 30, 121)
+    assert np.allclose(oracle.silu(z) - oracle.silu(-z), z, rtol=0, atol=1e-13)
+    assert abs(oracle.silu(40.0) - 40.0) < 1e-14
+    assert oracle.silu(-800.0) == 0.0 and np.isfinite(oracle.silu(-800.0))
+    assert np.allclose(oracle.swiglu(z, 2.0 * z), 2.0 * z * oracle.silu(z), rtol=1e-15)
+
+
+def test_fused_gemv_reduces_to_the_plain_oracle():
+    """No prologue: the fp64 matmul of the C-dequantised W equals the C GEMV;
+    with a prologue, it equals the C GEMV of the fp32-rounded h within fp32
+    rounding of h; the residual is added exactly."""
+    K = 768
+    W = synth.gen_q4k(33, K, 21)
+    x = synth.gen_x(3, K, 22)
+    Y0, A0 = oracle.fused_gemv_q4k(W, x)
+    Yc, Ac = oracle.gemv_q4k(W, x)
+    assert np.allclose(Y0, Yc, rtol=0, atol=1e-12 * A0.max()) and np.allclose(A0, Ac, rtol=1e-12)
+    g = synth.gen_x(1, K, 23)[0]
+    h = oracle.rmsnorm(x, g, 1e-5)
+    Yn, An = oracle.fused_gemv_q4k(W, x, norm_weight=g, eps=1e-5)
+    Yh, _ = oracle.gemv_q4k(W, h.astype(np.float32))
+    assert np.all(np.abs(Yn - Yh) <= 2.0 ** -23 * An)
+    up = synth.gen_x(3, K, 24)
+    Ys, As = oracle.fused_gemv_q4k(W, x, up=up)
+    Yh2, _ = oracle.gemv_q4k(W, oracle.swiglu(x, up).astype(np.float32))
+    assert np.all(np.abs(Ys - Yh2) <= 2.0 ** -23 * As)
+    R = synth.gen_x(3, 33, 25)
+    Yr, _ = oracle.fused_gemv_q4k(W, x, up=up, residual=R)
+    assert np.array_equal(Yr, Ys + R.astype(np.float64))
