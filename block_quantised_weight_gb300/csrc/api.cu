@@ -272,6 +272,16 @@ int qgemm_q4k_batched(const uint8_t* W, const float* X, float* Y, int M, int64_t
     return qg::launch_gemm_q4k_tc(W, X, Y, M, N, K, stream, st);
 }
 
+int qgemm_iq3_batched(const uint8_t* W, const uint8_t* grid, const float* X, float* Y, int M, int64_t N, int64_t K,
+                      cudaStream_t stream) {
+    int rc = check_gemv(W, grid, true, X, Y, M, N, K, 98);
+    if (rc != QG_OK) return rc;
+    unsigned* st = status_ptr();
+    if (!st) return QG_ECUDA;
+    if (M < 16 || (K / 256) % 8 != 0) return qg::launch_gemv_iq3(W, grid, X, Y, M, N, K, stream, st, 0u);
+    return qg::launch_gemm_iq3_tc(W, grid, X, Y, M, N, K, stream, st);
+}
+
 int qdequant_q4k(const uint8_t* W, float* out, int64_t N, int64_t K, cudaStream_t stream) {
     int rc = check_dequant(W, nullptr, false, out, N, K, 144);
     if (rc != QG_OK) return rc;

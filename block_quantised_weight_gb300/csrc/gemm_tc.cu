@@ -1,10 +1,12 @@
-// Batched Q4_K GEMM on the tcgen05 tensor cores (16 <= M <= 32 tokens).
+// Batched Q4_K / IQ3 GEMM on the tcgen05 tensor cores (16 <= M <= 32 tokens).
 //
 //   Y[m][n] = sum_k w[n][k] * X[m][k]
 //
 // Only here the path is a dense contraction: a 128-row tile of W is
 // dequantised (page 1 "Rewriting picoLM in Python", dequantize_q4_K:
-// (d*sc)*q - dmin*mn) into shared memory as bf16 (round to nearest even); X
+// (d*sc)*q - dmin*mn; page 4 "iq3_pack.py", decode:
+// d*(0.5+code)*0.5 * grid*0.5 * sign) into shared memory as bf16 (round to
+// nearest even); X
 // is rounded to bf16 likewise; tcgen05.mma (kind::f16, bf16 x bf16, fp32
 // accumulation in tensor memory) computes D[row][token] = W_tile X^T (W rows
 // on the MMA's M=128 side, tokens on its N=16/32 side).
@@ -15,8 +17,10 @@
 //              tile row); warps 0-3 then drain the accumulator (tcgen05.ld,
 //              warp w reads TMEM lanes 32w..32w+31) into Y;
 //   warp 8     producer: one 2D tensor-map TMA per unit for the 128 rows x
-//              144-byte block column of W and one for the x slice (fp32),
-//              into a double-buffered raw stage;
+//              block column of W (Q4_K: 144 bytes; IQ3: the 112 bytes from
+//              the block's offset rounded down to 16, the block starting
+//              0..14 bytes in) and one for the x slice (fp32), into a
+//              double-buffered raw stage;
 //   warp 9     allocates tensor memory; lane 0 issues the MMAs and commits
 //              them to mbarriers.
 // Work: units (tile, k-block) in row-major order, split evenly over the grid
@@ -29,6 +33,9 @@
 // h*sc - 1024*sc = q*sc exactly (at most 945: the fused product is rounded
 // once and the result is representable); a mixed f16 x f16 + f32 FMA then
 // gives d*(q*sc) - dmin*mn with a single rounding, the pages' fp32 value.
+// IQ3 values have at most 24 significant bits: (grid byte) * (d*(0.5+code)
+// *0.25) is exact in fp32 (the grid's 0.5 folded into the sub-block factor),
+// so bf16 rounds the pages' exact value once.
 //
 // Operand layout (no swizzle, K-major): 8-row x 16-byte core matrices; in a
 // half stage core (row group i, k chunk j) sits at ((i * 16) + j) * 128
@@ -50,7 +57,8 @@ namespace tc {
 constexpr int kTileRows = 128;
 constexpr int kBlockBytes = 144;
 constexpr int kThreads = 320;  // 8 dequant warps, producer, MMA
-constexpr int kRawW = kTileRows * kBlockBytes;     // 18432: TMA box 144 x 128
+constexpr int kRawW = kTileRows * kBlockBytes;     // 18432: TMA box 144 x 128 (IQ3: 112 x 128)
+constexpr int kIQ3Box = 112;
 constexpr int kRawX = 32 * 1024;                    // up to 32 tokens x 256 fp32
 constexpr int kRawStage = kRawW + kRawX;            // 51200
 constexpr int kOpA = kTileRows * 128 * 2;           // 32768: 128 rows x 128 k bf16
@@ -58,7 +66,13 @@ constexpr int kOpB = 32 * 128 * 2;                  // 8192: 32 tokens x 128 k b
 constexpr int kOpStage = kOpA + kOpB;               // 40960
 constexpr int kRaw0 = 1024;
 constexpr int kOp0 = kRaw0 + 2 * kRawStage;         // 103424
-constexpr int kSmemTotal = kOp0 + 2 * kOpStage;     // 185344
+// IQ3: the grid as fp32, 8 copies: row i of copy c at (8i + c) * 16 bytes,
+// lane L reading copy L & 7, so the 8 lanes of a quarter warp gather from 8
+// distinct bank groups whatever their rows (32 KB).
+constexpr int kGrid0 = kOp0 + 2 * kOpStage;
+constexpr int kSign0 = kGrid0 + 32768;              // IQ3: sign-mask word per 7-bit sign field (512 B)
+constexpr int kSmemTotal = kGrid0;                  // 185344 (Q4_K)
+constexpr int kSmemTotalIQ3 = kSign0 + 512;
 constexpr int kTmemCols = 32;
 constexpr uint32_t kSBO = 16 * 128;                 // row-group stride in an operand stage
 constexpr uint32_t kLBO = 128;                      // k-chunk stride
@@ -196,10 +210,54 @@ __device__ __forceinline__ void dequant_half(const uint8_t* blk, uint8_t* opA, i
     }
 }
 
+// IQ3: thread t, half `half` (sub-blocks 4*half .. +3) of tile row t, the
+// block starting `off` bytes into the box row.  Fields are read as 32-bit
+// words at the aligned address below and funnel-shifted into place.  Signs
+// are applied to packed bf16 pairs: sgn[s7] holds the eight signs of a
+// 7-bit field (the eighth its parity) with sign 2p at bit 15-p and sign
+// 2p+1 at bit 31-p, so (T << p) & 0x80008000 flips pair p.
+__device__ __forceinline__ void dequant_half_iq3(const uint8_t* row, int off, const float4* grid4,
+                                                 const uint32_t* sgn, uint8_t* opA, int t, int half) {
+    const uint8_t* base = row + (off & ~3);
+    const uint32_t sh = 8u * static_cast<uint32_t>(off & 3);
+    auto word = [&](int b) {  // block bytes b..b+3 (b a multiple of 4)
+        const uint32_t lo = *reinterpret_cast<const uint32_t*>(base + b);
+        const uint32_t hi = *reinterpret_cast<const uint32_t*>(base + b + 4);
+        return __funnelshift_r(lo, hi, sh);
+    };
+    const float d = h2f(word(96));
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const int ib = 4 * half + j;
+        const uint32_t sw = word(64 + 4 * ib);
+        const float dbh = d * (static_cast<float>(sw >> 28) + 0.5f) * 0.25f;  // 0.5 * grid's 0.5
+        const uint32_t iw0 = word(8 * ib), iw1 = word(8 * ib + 4);
+#pragma unroll
+        for (int l = 0; l < 4; ++l) {
+            const uint32_t T = sgn[(sw >> (7 * l)) & 0x7Fu];
+            uint32_t packed[4];
+#pragma unroll
+            for (int hf = 0; hf < 2; ++hf) {
+                const int pi = 2 * l + hf;  // index byte within the sub-block
+                const uint32_t idx = ((pi < 4 ? iw0 : iw1) >> (8 * (pi & 3))) & 0xFFu;
+                const float4 g = grid4[8 * idx + (t & 7)];
+                // |w| = grid * dbh exactly, rounded once to bf16; the sign bits of
+                // pairs 2hf and 2hf+1 come from T
+                packed[2 * hf] = pack_bf16(g.x * dbh, g.y * dbh) ^ ((T << (2 * hf)) & 0x80008000u);
+                packed[2 * hf + 1] = pack_bf16(g.z * dbh, g.w * dbh) ^ ((T << (2 * hf + 1)) & 0x80008000u);
+            }
+            // weights 32j + 8l .. +7 of the half: chunk 4j + l
+            *reinterpret_cast<uint4*>(opA + op_off(t, 4 * j + l)) =
+                make_uint4(packed[0], packed[1], packed[2], packed[3]);
+        }
+    }
+}
 
+template <bool IQ3>
 __global__ void __launch_bounds__(kThreads, 1)
-    gemm_q4k_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
-                       float* __restrict__ Y, int M, int64_t N, int64_t K, unsigned* status) {
+    gemm_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
+                   const uint8_t* __restrict__ grid, float* __restrict__ Y, int M, int64_t N, int64_t K,
+                   unsigned* status) {
     extern __shared__ __align__(1024) uint8_t smem[];
     uint64_t* raw_full = reinterpret_cast<uint64_t*>(smem);  // [2]
     uint64_t* raw_empty = raw_full + 2;                       // [2]
@@ -228,6 +286,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(acc_empty, 4);
         fence_mbar_init();
     }
+    if constexpr (IQ3) {
+        // the grid bytes (doubled units) as fp32, one float4 per row
+        float* g = reinterpret_cast<float*>(smem + kGrid0);
+        for (int i = threadIdx.x; i < 8 * 1024; i += kThreads)  // i = (row * 8 + copy) * 4 + j
+            g[i] = static_cast<float>(grid[(i >> 5) * 4 + (i & 3)]);
+        // signs of each 7-bit field: the seven stored ones and their parity
+        // (page 4, decode), sign k at bit 15 - k/2 (k even) or 31 - k/2 (odd)
+        uint32_t* sg = reinterpret_cast<uint32_t*>(smem + kSign0);
+        for (int i = threadIdx.x; i < 128; i += kThreads) {
+            const uint32_t s8 = static_cast<uint32_t>(i) | ((__popc(i) & 1u) << 7);
+            uint32_t t = 0;
+            for (int pr = 0; pr < 4; ++pr)
+                t |= (((s8 >> (2 * pr)) & 1u) << (15 - pr)) | (((s8 >> (2 * pr + 1)) & 1u) << (31 - pr));
+            sg[i] = t;
+        }
+    }
     if (warp == 9) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
                      ::"r"(smem_u32(tmem_slot)), "r"(kTmemCols) : "memory");
@@ -243,7 +317,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) {
             const uint64_t pol_w = policy_evict_first();
             const uint64_t pol_x = policy_evict_last();
-            const uint32_t bytes = kRawW + M * 1024;
+            constexpr int kBoxBytes = IQ3 ? kIQ3Box : kBlockBytes;
+            const uint32_t bytes = kTileRows * kBoxBytes + M * 1024;
             for (int64_t u = u_begin; u < u_end; ++u) {
                 const int64_t i = u - u_begin;
                 const int s = static_cast<int>(i & 1);
@@ -252,7 +327,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int kb = static_cast<int>(u % nb);
                 uint8_t* raw = smem + kRaw0 + s * kRawStage;
                 mbar_arrive_expect_tx(&raw_full[s], bytes);
-                tma_load_2d(raw, &tmW, kb * kBlockBytes, static_cast<int>(tile * kTileRows), &raw_full[s], pol_w);
+                const int bx = IQ3 ? (kb * 98) & ~15 : kb * kBlockBytes;  // x * 1 byte: 16-byte aligned
+                tma_load_2d(raw, &tmW, bx, static_cast<int>(tile * kTileRows), &raw_full[s], pol_w);
                 tma_load_2d(raw + kRawW, &tmX, kb * 256, 0, &raw_full[s], pol_x);
             }
         }
@@ -310,7 +386,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float* xr = reinterpret_cast<const float*>(raw + kRawW);
             mbar_wait_bounded(&raw_full[s], static_cast<uint32_t>((i >> 1) & 1), status);
             if (i >= 1) mbar_wait_bounded(&op_empty[half], static_cast<uint32_t>((i - 1) & 1), status);
-            dequant_half(raw + t * kBlockBytes, opA, t, half);  // rows past N: TMA zero fill, unused
+            if constexpr (IQ3)  // rows past N: TMA zero fill, unused
+                dequant_half_iq3(raw + t * kIQ3Box, (kb * 98) & 15, reinterpret_cast<const float4*>(smem + kGrid0),
+                                 reinterpret_cast<const uint32_t*>(smem + kSign0), opA, t, half);
+            else
+                dequant_half(raw + t * kBlockBytes, opA, t, half);
             for (int c = t; c < M * 16; c += 128) {
                 const int m = c >> 4, j = c & 15;
                 const float4 a = *reinterpret_cast<const float4*>(xr + m * 256 + 128 * half + 8 * j);
@@ -352,34 +432,33 @@ __global__ void __launch_bounds__(kThreads, 1)
 }  // namespace tc
 
 
-int launch_gemm_q4k_tc(const uint8_t* W, const float* X, float* Y, int M, int64_t N, int64_t K, cudaStream_t s,
-                       unsigned* status) {
+namespace {
+
+// Both formats: W viewed as [N rows][pitch bytes] with a box of one block
+// column (Q4_K 144 bytes; IQ3 112 bytes) x 128 rows; X [M][K] fp32 with a
+// box of 256 k x M tokens.
+template <bool IQ3>
+int launch_tc(const uint8_t* W, const uint8_t* grid, const float* X, float* Y, int M, int64_t N, int64_t K,
+              cudaStream_t s, unsigned* status) {
     if (M < 16 || M > 32) return QG_EINVAL;
     static bool attr_done[64];
     int dev = -1;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return QG_ECUDA;
+    const int smem = IQ3 ? tc::kSmemTotalIQ3 : tc::kSmemTotal;
     if (!attr_done[dev]) {
-        if (cudaFuncSetAttribute(tc::gemm_q4k_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 tc::kSmemTotal) != cudaSuccess)
+        if (cudaFuncSetAttribute(tc::gemm_tc_kernel<IQ3>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
+            cudaSuccess)
             return QG_ECUDA;
         attr_done[dev] = true;
     }
     auto encode = tensor_map_encoder();
     if (!encode) return QG_ECUDA;
-    // W viewed as [N rows][pitch bytes]; box = one 144-byte block column x 128 rows
-    const uint64_t pitch = static_cast<uint64_t>(K / 256) * tc::kBlockBytes;
+    const uint64_t pitch = static_cast<uint64_t>(K / 256) * (IQ3 ? 98 : tc::kBlockBytes);
     CUtensorMap tmW, tmX;
+    if (!encode_byte_rows(&tmW, W, pitch, static_cast<uint64_t>(N), IQ3 ? tc::kIQ3Box : tc::kBlockBytes,
+                          tc::kTileRows))
+        return QG_ECUDA;
     {
-        const cuuint64_t gdim[2] = {pitch, static_cast<cuuint64_t>(N)};
-        const cuuint64_t gstride[1] = {pitch};
-        const cuuint32_t box[2] = {static_cast<cuuint32_t>(tc::kBlockBytes), static_cast<cuuint32_t>(tc::kTileRows)};
-        const cuuint32_t estr[2] = {1, 1};
-        if (encode(&tmW, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(W), gdim, gstride, box, estr,
-                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-            return QG_ECUDA;
-    }
-    {   // X [M][K] fp32; box = 256 k x M tokens
         const cuuint64_t gdim[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(M)};
         const cuuint64_t gstride[1] = {static_cast<cuuint64_t>(K) * 4};
         const cuuint32_t box[2] = {256, static_cast<cuuint32_t>(M)};
@@ -394,9 +473,23 @@ int launch_gemm_q4k_tc(const uint8_t* W, const float* X, float* Y, int M, int64_
         return QG_ECUDA;
     if (cudaMemsetAsync(Y, 0, static_cast<size_t>(M) * N * sizeof(float), s) != cudaSuccess) return QG_ECUDA;
     const int64_t units = ((N + tc::kTileRows - 1) / tc::kTileRows) * (K / 256);
-    const int grid = static_cast<int>(std::min<int64_t>(units, sms));
-    tc::gemm_q4k_tc_kernel<<<grid, tc::kThreads, tc::kSmemTotal, s>>>(tmW, tmX, Y, M, N, K, status);
+    const int gridx = static_cast<int>(std::min<int64_t>(units, sms));
+    tc::gemm_tc_kernel<IQ3><<<gridx, tc::kThreads, smem, s>>>(tmW, tmX, grid, Y, M, N, K, status);
     return cudaGetLastError() == cudaSuccess ? QG_OK : QG_ECUDA;
+}
+
+}  // namespace
+
+int launch_gemm_q4k_tc(const uint8_t* W, const float* X, float* Y, int M, int64_t N, int64_t K, cudaStream_t s,
+                       unsigned* status) {
+    return launch_tc<false>(W, nullptr, X, Y, M, N, K, s, status);
+}
+
+// IQ3 needs 16-byte aligned rows (K/256 a multiple of 8) for its tensor map.
+int launch_gemm_iq3_tc(const uint8_t* W, const uint8_t* grid, const float* X, float* Y, int M, int64_t N, int64_t K,
+                       cudaStream_t s, unsigned* status) {
+    if ((K / 256) % 8 != 0) return QG_EINVAL;
+    return launch_tc<true>(W, grid, X, Y, M, N, K, s, status);
 }
 
 }  // namespace qg

@@ -26,5 +26,7 @@ int launch_dequant_iq3(const uint8_t* W, const uint8_t* grid, float* out, int64_
 // tcgen05 bf16 path, 16 <= M <= 32
 int launch_gemm_q4k_tc(const uint8_t* W, const float* X, float* Y, int M, int64_t N, int64_t K, cudaStream_t s,
                        unsigned* status);
+int launch_gemm_iq3_tc(const uint8_t* W, const uint8_t* grid, const float* X, float* Y, int M, int64_t N, int64_t K,
+                       cudaStream_t s, unsigned* status);
 
 }  // namespace qg

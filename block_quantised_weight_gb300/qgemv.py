@@ -41,7 +41,7 @@ class QgFuse(ctypes.Structure):
 
 QG_PREFETCH_WEIGHTS = 1
 
-EXPORTS = ("qgemv_q4k", "qgemv_q4k_ex", "qgemv_q4k_group", "qgemv_q4k_fused", "qgemv_q4k_fused_group", "qgemv_q4k_pass", "qgemv_q4k_pass_noalloc", "qgemv_iq3", "qgemv_iq3_ex", "qgemv_iq3_group", "qgemm_q4k_batched", "qdequant_q4k", "qdequant_iq3",
+EXPORTS = ("qgemv_q4k", "qgemv_q4k_ex", "qgemv_q4k_group", "qgemv_q4k_fused", "qgemv_q4k_fused_group", "qgemv_q4k_pass", "qgemv_q4k_pass_noalloc", "qgemv_iq3", "qgemv_iq3_ex", "qgemv_iq3_group", "qgemm_q4k_batched", "qgemm_iq3_batched", "qdequant_q4k", "qdequant_iq3",
            "qg_device_status", "qg_test_bounded_wait", "qg_strerror")
 
 
@@ -78,6 +78,7 @@ def load():
             "qgemv_q4k_pass": [vp, ci, ci, vp, vp],
             "qgemv_q4k_pass_noalloc": [vp, ci, ci, vp],
             "qgemm_q4k_batched": [vp, vp, vp, ci, i64, i64, vp],
+            "qgemm_iq3_batched": [vp, vp, vp, vp, ci, i64, i64, vp],
             "qdequant_q4k": [vp, vp, i64, i64, vp],
             "qdequant_iq3": [vp, vp, vp, i64, i64, vp],
             "qg_device_status": [vp],
@@ -308,6 +309,16 @@ def qgemm_q4k_batched(W, X, out=None, stream=None):
     X, out, M, N, K = _xy(W, X, out, 144)
     _check("qgemm_q4k_batched", load().qgemm_q4k_batched(W.data_ptr(), X.data_ptr(), out.data_ptr(), M, N, K,
                                                          _stream(stream)))
+    return out
+
+
+def qgemm_iq3_batched(W, grid, X, out=None, stream=None):
+    """Batched IQ3 GEMM: M >= 16 (K/256 a multiple of 8) on tcgen05 (bf16 operands), else the FMA path."""
+    import torch
+    _req(grid, torch.uint8, "grid")
+    X, out, M, N, K = _xy(W, X, out, 98)
+    _check("qgemm_iq3_batched", load().qgemm_iq3_batched(W.data_ptr(), grid.data_ptr(), X.data_ptr(),
+                                                         out.data_ptr(), M, N, K, _stream(stream)))
     return out
 
 

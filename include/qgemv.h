@@ -214,6 +214,16 @@ QG_API int qgemv_q4k_pass_noalloc(const qg_stage* stages, int nstages, int M, cu
  * (tolerance 4e-3 * sum|w*x|). */
 QG_API int qgemm_q4k_batched(const uint8_t* W, const float* X, float* Y, int M, int64_t N, int64_t K, cudaStream_t stream);
 
+/* Batched IQ3 GEMM for decode batches, 1 <= M <= 32.  Same operation,
+ * layouts and grid as qgemv_iq3.  M >= 16 with K/256 a multiple of 8
+ * dequantises W tiles to bf16 (round to nearest even; every IQ3 value is
+ * exact in fp32 first, page 4 "iq3_pack.py", decode) in shared memory and
+ * multiplies on the tcgen05 tensor cores with fp32 accumulation in tensor
+ * memory, X also rounded to bf16 (tolerance 4e-3 * sum|w*x|); otherwise the
+ * fp32 FMA path of qgemv_iq3 (1e-5 * sum|w*x|). */
+QG_API int qgemm_iq3_batched(const uint8_t* W, const uint8_t* grid, const float* X, float* Y, int M, int64_t N,
+                             int64_t K, cudaStream_t stream);
+
 /* Test-only: dequantise a Q4_K matrix to fp32 out[N][K] (caller-owned device
  * memory, N*K floats), bit-exact with page 1's fp32 evaluation order
  * ((d*sc)*q - (dmin*mn), each operation rounded). */

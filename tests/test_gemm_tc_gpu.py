@@ -87,3 +87,41 @@ def test_tc_repeatable_within_tolerance(q):
     check(a, Y, A, TAU_TC, "run a")
     check(b, Y, A, TAU_TC, "run b")
     assert np.allclose(a, b, rtol=0, atol=1e-6 * A.max())
+
+
+# ------------------------------------------------------------------- IQ3
+@pytest.mark.parametrize("N,K,M", [(128, 2048, 16), (300, 2048, 17), (129, 4096, 32), (1000, 2048, 24),
+                                   (64, 6144, 31)])
+def test_tc_iq3_small(q, N, K, M):
+    """IQ3 through tcgen05: every 98-byte block starts 0..14 bytes into its
+    112-byte box (all offsets occur for K/256 >= 8)."""
+    W, grid = synth.gen_iq3(N, K, N + K + M)
+    x = synth.gen_x(M, K, M + 40)
+    Y, A = oracle.gemv_iq3(W, grid, x)
+    y = q.qgemm_iq3_batched(dev(W), dev(grid), dev(x)).cpu().numpy()
+    r = check(y, Y, A, TAU_TC, f"iq3 tc N={N} K={K} M={M}")
+    assert r > 1e-6
+
+
+@pytest.mark.parametrize("M,K", [(8, 2048), (15, 2048), (16, 768), (20, 2304)])
+def test_iq3_batched_fma_path(q, M, K):
+    """M < 16, or rows not 16-byte aligned (K/256 not a multiple of 8): the
+    fp32 FMA path and its 1e-5 bar."""
+    N = 150
+    W, grid = synth.gen_iq3(N, K, 50 + M)
+    x = synth.gen_x(M, K, 51)
+    Y, A = oracle.gemv_iq3(W, grid, x)
+    check(q.qgemm_iq3_batched(dev(W), dev(grid), dev(x)).cpu().numpy(), Y, A, TAU_FMA, f"iq3 batched M={M}")
+
+
+@pytest.mark.parametrize("K,N,M", [(8192, 28672, 16), (28672, 8192, 32)])
+def test_tc_iq3_full_size_sampled(q, K, N, M):
+    W, grid = synth.gen_iq3(N, K, K + N + 1)
+    x = synth.gen_x(M, K, M + 5)
+    rng = np.random.default_rng(2)
+    rows = np.unique(np.concatenate([[0, N - 1], rng.integers(0, N, 64)]))
+    Y, A = oracle.gemv_iq3(W, grid, x, rows=rows)
+    y = q.qgemm_iq3_batched(dev(W), dev(grid), dev(x)).cpu().numpy()
+    check(y[:, rows], Y, A, TAU_TC, f"iq3 tc full K={K} N={N} M={M}")
+    assert np.isfinite(y).all()
+    assert q.qg_device_status() == q.QG_OK
