@@ -134,6 +134,21 @@ int qgemv_iq3(const uint8_t* W, const uint8_t* grid, const float* X, float* Y, i
     return qgemv_iq3_ex(W, grid, X, Y, M, N, K, 0u, stream);
 }
 
+int qgemv_iq3xxs_ex(const uint8_t* W, const uint8_t* grid, const float* X, float* Y, int M, int64_t N, int64_t K,
+                    unsigned flags, cudaStream_t stream) {
+    if (flags & ~static_cast<unsigned>(QG_PREFETCH_WEIGHTS)) return QG_EINVAL;
+    int rc = check_gemv(W, grid, true, X, Y, M, N, K, 98);
+    if (rc != QG_OK) return rc;
+    unsigned* st = status_ptr();
+    if (!st) return QG_ECUDA;
+    return qg::launch_gemv_iq3xxs(W, grid, X, Y, M, N, K, stream, st, flags);
+}
+
+int qgemv_iq3xxs(const uint8_t* W, const uint8_t* grid, const float* X, float* Y, int M, int64_t N, int64_t K,
+                 cudaStream_t stream) {
+    return qgemv_iq3xxs_ex(W, grid, X, Y, M, N, K, 0u, stream);
+}
+
 // Group checks: every matrix as a single GEMV, plus no Y[i] overlapping any
 // other matrix's W or Y.
 static int check_group(const uint8_t* const* W, float* const* Y, const int64_t* N, int count, const uint8_t* grid,
@@ -292,6 +307,12 @@ int qdequant_iq3(const uint8_t* W, const uint8_t* grid, float* out, int64_t N, i
     int rc = check_dequant(W, grid, true, out, N, K, 98);
     if (rc != QG_OK) return rc;
     return qg::launch_dequant_iq3(W, grid, out, N, K, stream);
+}
+
+int qdequant_iq3xxs(const uint8_t* W, const uint8_t* grid, float* out, int64_t N, int64_t K, cudaStream_t stream) {
+    int rc = check_dequant(W, grid, true, out, N, K, 98);
+    if (rc != QG_OK) return rc;
+    return qg::launch_dequant_iq3xxs(W, grid, out, N, K, stream);
 }
 
 int qg_device_status(cudaStream_t stream) {

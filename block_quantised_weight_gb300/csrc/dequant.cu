@@ -27,6 +27,9 @@ __global__ void dequant_q4k_kernel(const uint8_t* __restrict__ W, float* __restr
     }
 }
 
+// Both IQ3 orders (FmtIQ3T: page 4; FmtIQ3XXST: page 3): every value has at
+// most 24 significant bits, so any evaluation order gives the exact value.
+template <class F>
 __global__ void dequant_iq3_kernel(const uint8_t* __restrict__ W, const uint8_t* __restrict__ grid,
                                    float* __restrict__ out, int64_t nblocks) {
     const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;  // (block, sub-block)
@@ -34,8 +37,8 @@ __global__ void dequant_iq3_kernel(const uint8_t* __restrict__ W, const uint8_t*
     const int64_t bi = i >> 3;
     const int ib = static_cast<int>(i & 7);
     const uint8_t* blk = W + bi * 98;
-    const float d = h2f(static_cast<uint32_t>(blk[96]) | (static_cast<uint32_t>(blk[97]) << 8));
-    const uint8_t* wp = blk + 64 + 4 * ib;
+    const float d = h2f(static_cast<uint32_t>(blk[F::kDOff]) | (static_cast<uint32_t>(blk[F::kDOff + 1]) << 8));
+    const uint8_t* wp = blk + F::kWordOff + 4 * ib;
     const uint32_t sw = static_cast<uint32_t>(wp[0]) | (static_cast<uint32_t>(wp[1]) << 8) |
                         (static_cast<uint32_t>(wp[2]) << 16) | (static_cast<uint32_t>(wp[3]) << 24);
     const float db = __fmul_rn(__fmul_rn(d, __fadd_rn(0.5f, static_cast<float>(sw >> 28))), 0.5f);
@@ -44,7 +47,9 @@ __global__ void dequant_iq3_kernel(const uint8_t* __restrict__ W, const uint8_t*
         const int l = t >> 3, j = t & 7;
         const uint32_t seven = (sw >> (7 * l)) & 0x7Fu;
         const uint32_t neg = j < 7 ? (seven >> j) & 1u : (__popc(seven) & 1u);
-        const float mag = __fmul_rn(static_cast<float>(grid[4 * blk[8 * ib + (t >> 2)] + (t & 3)]), 0.5f);
+        // page 4 halves the grid bytes (doubled units); page 3 uses them as they are
+        const float mag = __fmul_rn(static_cast<float>(grid[4 * blk[F::kIdxOff + 8 * ib + (t >> 2)] + (t & 3)]),
+                                    F::kGridScale);
         o[t] = __fmul_rn(neg ? -mag : mag, db);
     }
 }
@@ -59,7 +64,15 @@ int launch_dequant_q4k(const uint8_t* W, float* out, int64_t N, int64_t K, cudaS
 int launch_dequant_iq3(const uint8_t* W, const uint8_t* grid, float* out, int64_t N, int64_t K, cudaStream_t s) {
     const int64_t nblocks = N * (K / 256);
     const int64_t threads = nblocks * 8;
-    dequant_iq3_kernel<<<static_cast<unsigned>((threads + 255) / 256), 256, 0, s>>>(W, grid, out, nblocks);
+    dequant_iq3_kernel<FmtIQ3T><<<static_cast<unsigned>((threads + 255) / 256), 256, 0, s>>>(W, grid, out, nblocks);
+    return cudaGetLastError() == cudaSuccess ? QG_OK : QG_ECUDA;
+}
+
+int launch_dequant_iq3xxs(const uint8_t* W, const uint8_t* grid, float* out, int64_t N, int64_t K, cudaStream_t s) {
+    const int64_t nblocks = N * (K / 256);
+    const int64_t threads = nblocks * 8;
+    dequant_iq3_kernel<FmtIQ3XXST><<<static_cast<unsigned>((threads + 255) / 256), 256, 0, s>>>(W, grid, out,
+                                                                                              nblocks);
     return cudaGetLastError() == cudaSuccess ? QG_OK : QG_ECUDA;
 }
 

@@ -82,6 +82,13 @@ struct FmtQ4KTc {
     static constexpr int kXH = 128;  // x staged contiguously (one bulk copy per token)
 };
 using FmtQ4KT = FmtQ4KTc<kCols>;
+// IQ3 block layouts (98 bytes, same fields, two orders):
+//   FmtIQ3T    page 4 "iq3_pack.py": 64 index bytes @0, eight u32 @64, fp16 d
+//              @96; value = d*(0.5+code)*0.5 * grid*0.5 * sign
+//   FmtIQ3XXST page 3 (llama.cpp IQ3_XXS): fp16 d @0, 64 index bytes @2,
+//              eight u32 @66; value = d*(0.5+s)*0.5 * grid * sign
+// kDbScale folds the constant factors into the sub-block factor
+// d*(0.5+code)*kDbScale that multiplies the raw grid bytes.
 struct FmtIQ3T {
     static constexpr int kBytes = 98;
     static constexpr int kCols = qg::kCols;
@@ -90,6 +97,14 @@ struct FmtIQ3T {
     static constexpr bool kTMA = true;
     static constexpr int kBoxBytes = 112;
     static constexpr int kXH = kXHalf;  // x staged in the padded layout (one 2D box per token)
+    static constexpr int kIdxOff = 0, kWordOff = 64, kDOff = 96;
+    static constexpr float kDbScale = 0.25f;
+    static constexpr float kGridScale = 0.5f;  // the magnitude of a grid byte
+};
+struct FmtIQ3XXST : FmtIQ3T {
+    static constexpr int kIdxOff = 2, kWordOff = 66, kDOff = 0;
+    static constexpr float kDbScale = 0.5f;
+    static constexpr float kGridScale = 1.f;
 };
 
 // IQ3 tables in smem, shared by all consumer warps.
@@ -422,10 +437,11 @@ __device__ __forceinline__ void q4k_half2(const uint8_t* blk, int rstride, int h
 }
 
 // Load the IQ3 super-block at byte COL*98 of a 16-byte aligned row chunk in
-// smem and realign it: v[i] = block bytes 4i..4i+3 (i < 24: the 64 index
-// bytes and the eight sign/scale words), d = the fp16 at block byte 96.
-// Only this small step is specialised per column; the decoder is shared.
-template <int COL>
+// smem and realign it: v[i] = block bytes F::kIdxOff + 4i.. (i < 24: the 64
+// index bytes and the eight sign/scale words, contiguous in both orders),
+// d = the fp16 at block byte F::kDOff.  Only this small step is
+// specialised per column; the decoder is shared.
+template <class F, int COL>
 __device__ __forceinline__ void iq3_load_block(const uint8_t* rowp, uint32_t (&v)[24], uint32_t& dbits) {
     constexpr int S0 = COL * 98, A0 = S0 & ~15, OFF = S0 - A0;
     uint32_t w[28];
@@ -439,10 +455,10 @@ __device__ __forceinline__ void iq3_load_block(const uint8_t* rowp, uint32_t (&v
     }
 #pragma unroll
     for (int i = 0; i < 24; ++i) {
-        const int P = OFF + 4 * i;
+        const int P = OFF + F::kIdxOff + 4 * i;
         v[i] = (P & 3) == 0 ? w[P >> 2] : __funnelshift_r(w[P >> 2], w[(P >> 2) + 1], 8 * (P & 3));
     }
-    constexpr int PD = OFF + 96;
+    constexpr int PD = OFF + F::kDOff;
     dbits = w[PD >> 2] >> (8 * (PD & 3));
 }
 
@@ -467,7 +483,7 @@ __device__ __forceinline__ uint2 iq3_grid(const uint8_t* tb, uint32_t w, int byt
 // the sign table (the implied eighth sign included), converts to fp32 and
 // FMAs.  The sub-block factor d*(0.5+code)*0.5 and the grid's 0.5 are
 // applied once per 32 weights (exact: at most 16 significant bits).
-template <int MT>
+template <int MT, class F>
 __device__ __forceinline__ void iq3_block(const uint32_t (&v)[24], uint32_t dbits, const uint8_t* tb, const uint8_t* sg,
                                           uint32_t lane8, uint32_t lane4, const float* xb, int64_t xstride, int M,
                                           float (&acc)[MT]) {
@@ -475,7 +491,7 @@ __device__ __forceinline__ void iq3_block(const uint32_t (&v)[24], uint32_t dbit
 #pragma unroll
     for (int ib = 0; ib < 8; ++ib) {
         const uint32_t sw = v[16 + ib];
-        const float db = d * (static_cast<float>(sw >> 28) + 0.5f) * 0.25f;
+        const float db = d * (static_cast<float>(sw >> 28) + 0.5f) * F::kDbScale;
         f2 dot[MT];
 #pragma unroll
         for (int m = 0; m < MT; ++m) dot[m] = f2{0.f, 0.f};
@@ -506,11 +522,14 @@ __device__ __forceinline__ void iq3_block(const uint32_t (&v)[24], uint32_t dbit
 
 // Half h of the IQ3 super-block of column COL from its 112-byte TMA box row
 // (the block starts (98*COL) mod 16 bytes in): vi = index bytes 32h..32h+31,
-// vs = sign/scale words 4h..4h+3, dbits = the fp16 d.
-template <int COL>
+// vs = sign/scale words 4h..4h+3, dbits = the fp16 d (field offsets of F).
+template <class F, int COL>
 __device__ __forceinline__ void iq3_load_half(const uint8_t* boxrow, int h, uint32_t (&vi)[8], uint32_t (&vs)[4],
                                               uint32_t& dbits) {
-    constexpr int OFF = (COL * 98) & 15, W0 = OFF >> 2, SH = 8 * (OFF & 3);
+    constexpr int OFF = (COL * 98) & 15;
+    constexpr int OI = OFF + F::kIdxOff, W0 = OI >> 2, SH = 8 * (OI & 3);          // index bytes
+    constexpr int OW = OFF + F::kWordOff - 64, W0w = OW >> 2, SHw = 8 * (OW & 3);  // sign/scale words
+    constexpr int OD = OFF + F::kDOff;                                             // d
     uint32_t w[12];
 #pragma unroll
     for (int i = 0; i < 3; ++i) {
@@ -526,14 +545,14 @@ __device__ __forceinline__ void iq3_load_half(const uint8_t* boxrow, int h, uint
         u[4 * i] = t.x; u[4 * i + 1] = t.y; u[4 * i + 2] = t.z; u[4 * i + 3] = t.w;
     }
 #pragma unroll
-    for (int i = 0; i < 4; ++i) vs[i] = SH ? __funnelshift_r(u[W0 + i], u[W0 + i + 1], SH) : u[W0 + i];
-    dbits = *reinterpret_cast<const uint32_t*>(boxrow + 96 + (OFF & ~3)) >> SH;
+    for (int i = 0; i < 4; ++i) vs[i] = SHw ? __funnelshift_r(u[W0w + i], u[W0w + i + 1], SHw) : u[W0w + i];
+    dbits = *reinterpret_cast<const uint32_t*>(boxrow + (OD & ~3)) >> (8 * (OD & 3));
 }
 
 // Two rows (r, r+16), half h of an IQ3 super-block each, against MT tokens:
 // the layout of q4k_half2 (one x load serves both rows).  xq = x of the
 // block + 128h.
-template <int MT>
+template <int MT, class F>
 __device__ __forceinline__ void iq3_half2(const uint32_t (&vi)[2][8], const uint32_t (&vs)[2][4], const uint32_t (&dbits)[2],
                                           const uint8_t* tb, const uint8_t* sg, uint32_t lane8, uint32_t lane4,
                                           const float* xq, int64_t xstride, int M, float (&acc)[2][MT]) {
@@ -576,7 +595,7 @@ __device__ __forceinline__ void iq3_half2(const uint32_t (&vi)[2][8], const uint
         }
 #pragma unroll
         for (int r = 0; r < 2; ++r) {
-            const float db = d[r] * (static_cast<float>(vs[r][j] >> 28) + 0.5f) * 0.25f;
+            const float db = d[r] * (static_cast<float>(vs[r][j] >> 28) + 0.5f) * F::kDbScale;
 #pragma unroll
             for (int m = 0; m < MT; ++m)
                 if (MT == 1 || m < M) acc[r][m] = fmaf(db, dot[r][m].x + dot[r][m].y, acc[r][m]);
@@ -867,19 +886,19 @@ __global__ void __launch_bounds__(RG * F::kCols * 32 + 32, MINB)
                 switch (cw) {
 #define QG_IQ3_HALF(C)                                                          \
     case C:                                                                     \
-        iq3_load_half<C>(box, hl, vi[0], vs[0], dbits[0]);                      \
-        iq3_load_half<C>(box + 16 * F::kBoxBytes, hl, vi[1], vs[1], dbits[1]);  \
+        iq3_load_half<F, C>(box, hl, vi[0], vs[0], dbits[0]);                      \
+        iq3_load_half<F, C>(box + 16 * F::kBoxBytes, hl, vi[1], vs[1], dbits[1]);  \
         break;
                     QG_IQ3_HALF(0) QG_IQ3_HALF(1) QG_IQ3_HALF(2) QG_IQ3_HALF(3)
                     QG_IQ3_HALF(4) QG_IQ3_HALF(5) QG_IQ3_HALF(6)
                     default:
-                        iq3_load_half<7>(box, hl, vi[0], vs[0], dbits[0]);
-                        iq3_load_half<7>(box + 16 * F::kBoxBytes, hl, vi[1], vs[1], dbits[1]);
+                        iq3_load_half<F, 7>(box, hl, vi[0], vs[0], dbits[0]);
+                        iq3_load_half<F, 7>(box + 16 * F::kBoxBytes, hl, vi[1], vs[1], dbits[1]);
                         break;
 #undef QG_IQ3_HALF
                 }
                 const uint8_t* tb = smem + L.table;
-                iq3_half2<MT>(vi, vs, dbits, tb, tb + kIQ3GridBytes, lane8, lane4, xb + XH * hl, xstride, M, acc2);
+                iq3_half2<MT, F>(vi, vs, dbits, tb, tb + kIQ3GridBytes, lane8, lane4, xb + XH * hl, xstride, M, acc2);
             } else {
                 if (r < rows) {
                     // block cw's box row, shifted so that rowp + (98*cw & ~15)
@@ -889,16 +908,16 @@ __global__ void __launch_bounds__(RG * F::kCols * 32 + 32, MINB)
                     const uint8_t* tb = smem + L.table;
                     uint32_t v[24], dbits;
                     switch (cw) {
-                        case 0: iq3_load_block<0>(rowp, v, dbits); break;
-                        case 1: iq3_load_block<1>(rowp, v, dbits); break;
-                        case 2: iq3_load_block<2>(rowp, v, dbits); break;
-                        case 3: iq3_load_block<3>(rowp, v, dbits); break;
-                        case 4: iq3_load_block<4>(rowp, v, dbits); break;
-                        case 5: iq3_load_block<5>(rowp, v, dbits); break;
-                        case 6: iq3_load_block<6>(rowp, v, dbits); break;
-                        default: iq3_load_block<7>(rowp, v, dbits); break;
+                        case 0: iq3_load_block<F, 0>(rowp, v, dbits); break;
+                        case 1: iq3_load_block<F, 1>(rowp, v, dbits); break;
+                        case 2: iq3_load_block<F, 2>(rowp, v, dbits); break;
+                        case 3: iq3_load_block<F, 3>(rowp, v, dbits); break;
+                        case 4: iq3_load_block<F, 4>(rowp, v, dbits); break;
+                        case 5: iq3_load_block<F, 5>(rowp, v, dbits); break;
+                        case 6: iq3_load_block<F, 6>(rowp, v, dbits); break;
+                        default: iq3_load_block<F, 7>(rowp, v, dbits); break;
                     }
-                    iq3_block<MT>(v, dbits, tb, tb + kIQ3GridBytes, lane8, lane4, xb, xstride, M, acc);
+                    iq3_block<MT, F>(v, dbits, tb, tb + kIQ3GridBytes, lane8, lane4, xb, xstride, M, acc);
                 }
             }
         }

@@ -18,6 +18,9 @@ int launch_group_q4k(const uint8_t* const* W, float* const* Y, const int64_t* N,
 // RMSNorm / SwiGLU prologue (M <= 4) and residual epilogue, see gemv_kernel.cuh's Fuse
 int launch_group_q4k_fused(const uint8_t* const* W, float* const* Y, const int64_t* N, int count, const float* X,
                            int M, int64_t K, cudaStream_t s, unsigned* status, unsigned flags, const Fuse& fz);
+int launch_gemv_iq3xxs(const uint8_t* W, const uint8_t* grid, const float* X, float* Y, int M, int64_t N, int64_t K,
+                       cudaStream_t s, unsigned* status, unsigned flags);
+int launch_dequant_iq3xxs(const uint8_t* W, const uint8_t* grid, float* out, int64_t N, int64_t K, cudaStream_t s);
 int launch_group_iq3(const uint8_t* const* W, float* const* Y, const int64_t* N, int count, const uint8_t* grid,
                      const float* X, int M, int64_t K, cudaStream_t s, unsigned* status, unsigned flags);
 int launch_pass_q4k(const qg_stage* stages, int nstages, int M, unsigned* sync, cudaStream_t s, unsigned* status);

@@ -1,0 +1,99 @@
+// IQ3 GEMV dispatch (fp32 FMA path) for both block orders (page 4's and
+// page 3's IQ3_XXS), shared by their translation units.  Kernel:
+// gemv_kernel.cuh; rows whose byte offsets are not 16-byte aligned take the
+// byte-addressed kernel below.
+#pragma once
+#include "launch_common.cuh"
+
+namespace qg {
+
+
+// ------------------------------------------------ IQ3 rows not 16-byte aligned
+// When K/256 is not a multiple of 8 the 98-byte rows do not start on 16-byte
+// boundaries, which bulk copies require.  This path reads bytes straight
+// from global memory: one warp per row, lanes over super-blocks, the grid
+// staged in smem.  Correct for every K % 256 == 0; not tuned.
+template <class F>
+__global__ void __launch_bounds__(256)
+    gemv_iq3_bytes_kernel(const uint8_t* __restrict__ W, const uint8_t* __restrict__ grid, const float* __restrict__ X,
+                          float* __restrict__ Y, int M, int64_t N, int64_t K) {
+    __shared__ uint32_t g[256];
+    for (int i = threadIdx.x; i < 256; i += blockDim.x) g[i] = *reinterpret_cast<const uint32_t*>(grid + 4 * i);
+    __syncthreads();
+    const int nb = static_cast<int>(K / 256);
+    const int lane = threadIdx.x & 31;
+    const int64_t warps = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
+    for (int64_t row = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); row < N; row += warps) {
+        float acc[8];
+#pragma unroll
+        for (int m = 0; m < 8; ++m) acc[m] = 0.f;
+        for (int b = lane; b < nb; b += 32) {
+            const uint8_t* blk = W + (row * nb + b) * 98;
+            const float d = h2f(static_cast<uint32_t>(blk[F::kDOff]) | (static_cast<uint32_t>(blk[F::kDOff + 1]) << 8));
+            for (int ib = 0; ib < 8; ++ib) {
+                const uint8_t* wp = blk + F::kWordOff + 4 * ib;
+                const uint32_t sw = static_cast<uint32_t>(wp[0]) | (static_cast<uint32_t>(wp[1]) << 8) |
+                                    (static_cast<uint32_t>(wp[2]) << 16) | (static_cast<uint32_t>(wp[3]) << 24);
+                const float db = d * (static_cast<float>(sw >> 28) + 0.5f) * F::kDbScale;
+                float dot[8];
+#pragma unroll
+                for (int m = 0; m < 8; ++m) dot[m] = 0.f;
+                for (int t = 0; t < 32; ++t) {
+                    const int l = t >> 3, j = t & 7;
+                    const uint32_t seven = (sw >> (7 * l)) & 0x7Fu;
+                    const uint32_t neg = j < 7 ? (seven >> j) & 1u : (__popc(seven) & 1u);
+                    const float mag = byte_f(g[blk[F::kIdxOff + 8 * ib + (t >> 2)]], t & 3);
+                    const float wv = neg ? -mag : mag;
+                    const int64_t k = static_cast<int64_t>(b) * 256 + 32 * ib + t;
+#pragma unroll
+                    for (int m = 0; m < 8; ++m)
+                        if (m < M) dot[m] = fmaf(wv, X[m * K + k], dot[m]);
+                }
+#pragma unroll
+                for (int m = 0; m < 8; ++m) acc[m] = fmaf(db, dot[m], acc[m]);
+            }
+        }
+#pragma unroll
+        for (int m = 0; m < 8; ++m) {
+            float v = acc[m];
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+            if (lane == 0 && m < M) Y[m * N + row] = v;
+        }
+    }
+}
+
+template <class F>
+int launch_group_iq3_t(const uint8_t* const* W, float* const* Y, const int64_t* N, int count, const uint8_t* grid,
+                       const float* X, int M, int64_t K, cudaStream_t s, unsigned* status, unsigned flags) {
+    const int dev = current_device();
+    if (dev < 0) return QG_ECUDA;
+    const bool aligned = (K / 256) % 8 == 0;
+    for (int m0 = 0; m0 < M; m0 += 8) {
+        const int mg = std::min(8, M - m0);
+        const float* Xg = X + static_cast<int64_t>(m0) * K;
+        int rc = QG_OK;
+        if (!aligned) {
+            const int sms = sm_count(dev);
+            if (sms <= 0) return QG_ECUDA;
+            for (int i = 0; i < count && rc == QG_OK; ++i) {
+                const int64_t blocks = std::min<int64_t>((N[i] + 7) / 8, static_cast<int64_t>(sms) * 8);
+                gemv_iq3_bytes_kernel<F><<<static_cast<int>(blocks), 256, 0, s>>>(W[i], grid, Xg, Y[i] + m0 * N[i], mg,
+                                                                                N[i], K);
+                rc = cudaGetLastError() == cudaSuccess ? QG_OK : QG_ECUDA;
+            }
+        } else if (mg == 1) {
+            rc = launch_gemv<F, 1, true, 2, 1>(W, Y, N, count, m0, grid, Xg, mg, K, s, status, dev, flags);
+        } else if (mg == 2) {
+            rc = launch_gemv<F, 2, true, 1, 1>(W, Y, N, count, m0, grid, Xg, mg, K, s, status, dev, flags);
+        } else if (mg <= 4) {
+            rc = launch_gemv<F, 4, false, 1, 1>(W, Y, N, count, m0, grid, Xg, mg, K, s, status, dev, flags);
+        } else {
+            rc = launch_gemv<F, 8, false, 1, 1>(W, Y, N, count, m0, grid, Xg, mg, K, s, status, dev, flags);
+        }
+        if (rc != QG_OK) return rc;
+    }
+    return QG_OK;
+}
+
+}  // namespace qg

@@ -41,7 +41,7 @@ class QgFuse(ctypes.Structure):
 
 QG_PREFETCH_WEIGHTS = 1
 
-EXPORTS = ("qgemv_q4k", "qgemv_q4k_ex", "qgemv_q4k_group", "qgemv_q4k_fused", "qgemv_q4k_fused_group", "qgemv_q4k_pass", "qgemv_q4k_pass_noalloc", "qgemv_iq3", "qgemv_iq3_ex", "qgemv_iq3_group", "qgemm_q4k_batched", "qgemm_iq3_batched", "qdequant_q4k", "qdequant_iq3",
+EXPORTS = ("qgemv_q4k", "qgemv_q4k_ex", "qgemv_q4k_group", "qgemv_q4k_fused", "qgemv_q4k_fused_group", "qgemv_q4k_pass", "qgemv_q4k_pass_noalloc", "qgemv_iq3", "qgemv_iq3_ex", "qgemv_iq3_group", "qgemv_iq3xxs", "qgemv_iq3xxs_ex", "qdequant_iq3xxs", "qgemm_q4k_batched", "qgemm_iq3_batched", "qdequant_q4k", "qdequant_iq3",
            "qg_device_status", "qg_test_bounded_wait", "qg_strerror")
 
 
@@ -71,6 +71,9 @@ def load():
             "qgemv_q4k_ex": [vp, vp, vp, ci, i64, i64, ctypes.c_uint, vp],
             "qgemv_iq3": [vp, vp, vp, vp, ci, i64, i64, vp],
             "qgemv_iq3_ex": [vp, vp, vp, vp, ci, i64, i64, ctypes.c_uint, vp],
+            "qgemv_iq3xxs": [vp, vp, vp, vp, ci, i64, i64, vp],
+            "qgemv_iq3xxs_ex": [vp, vp, vp, vp, ci, i64, i64, ctypes.c_uint, vp],
+            "qdequant_iq3xxs": [vp, vp, vp, i64, i64, vp],
             "qgemv_q4k_group": [vp, vp, vp, ci, vp, ci, i64, ctypes.c_uint, vp],
             "qgemv_iq3_group": [vp, vp, vp, ci, vp, vp, ci, i64, ctypes.c_uint, vp],
             "qgemv_q4k_fused": [vp, vp, vp, ci, i64, i64, vp, ctypes.c_uint, vp],
@@ -167,6 +170,19 @@ def qgemv_iq3(W, grid, X, out=None, stream=None, flags=0):
     rc = load().qgemv_iq3_ex(W.data_ptr(), grid.data_ptr(), X.data_ptr(), out.data_ptr(), M, N, K, flags,
                              _stream(stream))
     _check("qgemv_iq3_ex" if flags else "qgemv_iq3", rc)
+    return out
+
+
+def qgemv_iq3xxs(W, grid, X, out=None, stream=None, flags=0):
+    """Y = X @ dequant(W)^T for an IQ3_XXS matrix (page 3 byte order, raw grid entries)."""
+    import torch
+    _req(grid, torch.uint8, "grid")
+    if grid.numel() != 1024:
+        raise ValueError("grid must hold 256 x 4 bytes")
+    X, out, M, N, K = _xy(W, X, out, 98)
+    rc = load().qgemv_iq3xxs_ex(W.data_ptr(), grid.data_ptr(), X.data_ptr(), out.data_ptr(), M, N, K, flags,
+                                _stream(stream))
+    _check("qgemv_iq3xxs_ex", rc)
     return out
 
 
@@ -343,6 +359,19 @@ def qdequant_iq3(W, grid, K, out=None, stream=None):
         out = torch.empty((N, K), dtype=torch.float32, device=W.device)
     _check("qdequant_iq3", load().qdequant_iq3(W.data_ptr(), grid.data_ptr(), out.data_ptr(), N, K,
                                                _stream(stream)))
+    return out
+
+
+def qdequant_iq3xxs(W, grid, K, out=None, stream=None):
+    """Test-only: fp32 [N, K] dequantisation of an IQ3_XXS matrix."""
+    import torch
+    _req(W, torch.uint8, "W")
+    _req(grid, torch.uint8, "grid")
+    N = W.numel() // (K // 256 * 98)
+    if out is None:
+        out = torch.empty((N, K), dtype=torch.float32, device=W.device)
+    _check("qdequant_iq3xxs", load().qdequant_iq3xxs(W.data_ptr(), grid.data_ptr(), out.data_ptr(), N, K,
+                                                     _stream(stream)))
     return out
 
 

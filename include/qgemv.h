@@ -105,6 +105,20 @@ QG_API int qgemv_iq3(const uint8_t* W, const uint8_t* grid, const float* X, floa
 QG_API int qgemv_iq3_ex(const uint8_t* W, const uint8_t* grid, const float* X, float* Y, int M, int64_t N, int64_t K,
                         unsigned flags, cudaStream_t stream);
 
+/* IQ3_XXS GEMV: the same 98-byte super-block in page 3's byte order and
+ * scale convention (llama.cpp's IQ3_XXS; page 3, the format table, Format
+ * and eff_np): fp16 d @0, 64 grid index bytes @2, eight u32 @66 (sign
+ * fields and implied eighth sign as qgemv_iq3, the 4-bit sub-scale s in
+ * bits 28-31); weight = d*(0.5+s)*0.5 * grid[idx][j] * sign, the grid
+ * entries used as they are (no halving).  The same fields in page 4's order
+ * give half these values.  Other arguments, paths and numerics as qgemv_iq3. */
+QG_API int qgemv_iq3xxs(const uint8_t* W, const uint8_t* grid, const float* X, float* Y, int M, int64_t N, int64_t K,
+                        cudaStream_t stream);
+
+/* qgemv_iq3xxs with launch flags (0 or QG_PREFETCH_WEIGHTS). */
+QG_API int qgemv_iq3xxs_ex(const uint8_t* W, const uint8_t* grid, const float* X, float* Y, int M, int64_t N,
+                           int64_t K, unsigned flags, cudaStream_t stream);
+
 /* Several Q4_K GEMVs that read the same X (in a decode step: q, k and v of a
  * layer read the attention-norm output; gate and up read the FFN-norm
  * output) in one launch: Y[i] = X * dequant(W[i])^T for i < count,
@@ -232,6 +246,11 @@ QG_API int qdequant_q4k(const uint8_t* W, float* out, int64_t N, int64_t K, cuda
 /* Test-only: dequantise an IQ3 matrix to fp32 out[N][K]; every value is
  * exact (at most 24 significant bits), hence bit-exact with page 4's decode. */
 QG_API int qdequant_iq3(const uint8_t* W, const uint8_t* grid, float* out, int64_t N, int64_t K, cudaStream_t stream);
+
+/* Test-only: dequantise an IQ3_XXS matrix (page 3 order) to fp32 out[N][K];
+ * exact like qdequant_iq3. */
+QG_API int qdequant_iq3xxs(const uint8_t* W, const uint8_t* grid, float* out, int64_t N, int64_t K,
+                           cudaStream_t stream);
 
 /* Synchronise `stream`, then return and clear the current device's status
  * word: QG_OK, QG_ETIMEOUT or QG_EBOUNDS (QG_ECUDA if the sync failed). */

@@ -65,6 +65,9 @@ def _load():
                                         ctypes.c_int]
         lib.oracle_gemv_iq3.argtypes = [u8p, u8p, f32p, ctypes.c_int, i64, i64p, i64, f64p,
                                         f64p, ctypes.c_int]
+        lib.oracle_dequant_iq3xxs.argtypes = [u8p, u8p, i64, i64, f32p]
+        lib.oracle_gemv_iq3xxs.argtypes = [u8p, u8p, f32p, ctypes.c_int, i64, i64p, i64, f64p,
+                                           f64p, ctypes.c_int]
         lib.oracle_max_threads.restype = ctypes.c_int
         _lib = lib
         return lib
@@ -127,13 +130,34 @@ def dequant_iq3(W: np.ndarray, grid: np.ndarray, K: int) -> np.ndarray:
     return out
 
 
+def dequant_iq3xxs(W: np.ndarray, grid: np.ndarray, K: int) -> np.ndarray:
+    """fp32 [N, K] weights of an IQ3_XXS matrix in page 3's byte order (d
+    first, eff = d*(0.5+s)*0.5 times the raw codebook entry and sign)."""
+    W = np.ascontiguousarray(W, dtype=np.uint8)
+    grid = np.ascontiguousarray(grid, dtype=np.uint8).reshape(256, 4)
+    N = _check_rows(W, K, IQ3_BYTES)
+    out = np.empty((N, K), dtype=np.float32)
+    _load().oracle_dequant_iq3xxs(_ptr(W, ctypes.c_uint8), _ptr(grid, ctypes.c_uint8), N, K,
+                                  _ptr(out, ctypes.c_float))
+    return out
+
+
+def iq3_to_iq3xxs(W: np.ndarray, K: int) -> np.ndarray:
+    """The same fields re-laid from page 4's order (indices, words, d) into
+    page 3's (d, indices, words): a byte permutation per block."""
+    W = np.ascontiguousarray(W, dtype=np.uint8)
+    N = _check_rows(W, K, IQ3_BYTES)
+    b = W.reshape(N, K // QK, IQ3_BYTES)
+    return np.concatenate([b[:, :, 96:98], b[:, :, 0:96]], axis=2).reshape(W.shape)
+
+
 def _gemv(fmt, W, grid, X, rows, nthreads):
     W = np.ascontiguousarray(W, dtype=np.uint8)
     X = np.ascontiguousarray(X, dtype=np.float32)
     if X.ndim == 1:
         X = X[None, :]
     M, K = X.shape
-    N = _check_rows(W, K, Q4K_BYTES if fmt == 0 else IQ3_BYTES)
+    N = _check_rows(W, K, Q4K_BYTES if fmt == 0 else IQ3_BYTES)  # fmt 1, 2: 98-byte blocks
     if rows is None:
         rows_arr = np.arange(N, dtype=np.int64)
     else:
@@ -151,9 +175,9 @@ def _gemv(fmt, W, grid, X, rows, nthreads):
                             _ptr(A, ctypes.c_double), nt)
     else:
         g = np.ascontiguousarray(grid, dtype=np.uint8).reshape(256, 4)
-        lib.oracle_gemv_iq3(_ptr(W, ctypes.c_uint8), _ptr(g, ctypes.c_uint8),
-                            _ptr(X, ctypes.c_float), M, K, _ptr(rows_arr, ctypes.c_int64), nr,
-                            _ptr(Y, ctypes.c_double), _ptr(A, ctypes.c_double), nt)
+        f = lib.oracle_gemv_iq3 if fmt == 1 else lib.oracle_gemv_iq3xxs
+        f(_ptr(W, ctypes.c_uint8), _ptr(g, ctypes.c_uint8), _ptr(X, ctypes.c_float), M, K,
+          _ptr(rows_arr, ctypes.c_int64), nr, _ptr(Y, ctypes.c_double), _ptr(A, ctypes.c_double), nt)
     return Y, A
 
 
@@ -165,6 +189,11 @@ def gemv_q4k(W, X, rows=None, nthreads=None):
 def gemv_iq3(W, grid, X, rows=None, nthreads=None):
     """(Y, A): fp64 y = X W^T and A = sum |w x| for the given rows of an IQ3 W."""
     return _gemv(1, W, grid, X, rows, nthreads)
+
+
+def gemv_iq3xxs(W, grid, X, rows=None, nthreads=None):
+    """(Y, A): fp64 y = X W^T and A = sum |w x| for the given rows of an IQ3_XXS W."""
+    return _gemv(2, W, grid, X, rows, nthreads)
 
 
 # ------------------------------------------------ decode-step prologues (fp64)

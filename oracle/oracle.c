@@ -13,6 +13,11 @@
  *   - IQ3:  page 4 "iq3_pack.py" (colibri fmt=5), module docstring (layout,
  *     value formula) and function decode (sign words, implied 8th sign,
  *     sub-scale), function grid (the x0.5 applied to the published table).
+ *   - IQ3_XXS: page 3 (llama.cpp's codebook formats as trainable students),
+ *     the format table (98 bytes, d at bytes 0-1, s the top 4 bits of the
+ *     uint32s at bytes 66-97, eff = d*(0.5+s)*0.5), the class Format /
+ *     eff_np (eff times v, v = codebook entry times sign) and the note that
+ *     IQ3_XXS stores 8 signs in 7 bits with an even count of negatives.
  *   - GEMV: page 1, model_forward / forward: matmul(out, x, W, n_in, n_out)
  *     computes out = W x with one output per row of W.
  *
@@ -152,6 +157,42 @@ void oracle_dequant_iq3_block(const uint8_t *blk, const uint8_t *grid, float *ou
     }
 }
 
+/* One IQ3_XXS block (98 bytes) -> 256 fp32 weights, page 3.  Bytes 0-1: fp16
+ * d; 2-65: one codebook index per 4 weights (the code bytes: everything but
+ * d and the sub-scales); 66-97: eight little-endian u32, one per 32-weight
+ * sub-block: bits 7l..7l+6 the signs of weights 8l..8l+6 (bit set =>
+ * negative), the eighth sign the XOR of those seven (an even count of
+ * negatives), bits 28-31 the sub-scale s.  eff = d*(0.5+s)*0.5 in fp32 (as
+ * ggml computes it), v = grid entry (raw, not halved) times the sign,
+ * weight = eff*v (exact in fp32: page 3 notes v*eff is exact). */
+void oracle_dequant_iq3xxs_block(const uint8_t *blk, const uint8_t *grid, float *out)
+{
+    float d = oracle_f16_to_f32(le16(blk + 0));
+    for (int ib = 0; ib < 8; ++ib) {
+        const uint8_t *idx = blk + 2 + 8 * ib;
+        uint32_t word = le32(blk + 66 + 4 * ib);
+        float s = (float)((word >> 28) & 0xF);
+        float eff = d * (0.5f + s) * 0.5f;
+        for (int l = 0; l < 4; ++l) {
+            uint32_t seven = (word >> (7 * l)) & 0x7F;
+            uint32_t par = 0;
+            for (int j = 0; j < 8; ++j) {
+                uint32_t neg;
+                if (j < 7) {
+                    neg = (seven >> j) & 1u;
+                    par ^= neg;
+                } else {
+                    neg = par;
+                }
+                int t = 8 * l + j;
+                float v = (float)grid[4 * idx[t / 4] + (t % 4)];
+                if (neg) v = -v;
+                out[32 * ib + t] = eff * v;
+            }
+        }
+    }
+}
+
 /* Whole rows: W is [N][K/256 blocks], out is [N][K] fp32. */
 void oracle_dequant_q4k(const uint8_t *W, int64_t N, int64_t K, float *out)
 {
@@ -169,10 +210,18 @@ void oracle_dequant_iq3(const uint8_t *W, const uint8_t *grid, int64_t N, int64_
             oracle_dequant_iq3_block(W + (n * nb + b) * IQ3_BYTES, grid, out + n * K + b * QK);
 }
 
+void oracle_dequant_iq3xxs(const uint8_t *W, const uint8_t *grid, int64_t N, int64_t K, float *out)
+{
+    int64_t nb = K / QK;
+    for (int64_t n = 0; n < N; ++n)
+        for (int64_t b = 0; b < nb; ++b)
+            oracle_dequant_iq3xxs_block(W + (n * nb + b) * IQ3_BYTES, grid, out + n * K + b * QK);
+}
+
 /* GEMV reference for selected rows.  Y[m][r] = sum_k (double)w[row][k] * (double)x[m][k],
  * summed in k order in fp64; A[m][r] = sum_k |w*x| in fp64 (the scale of the
  * tolerance).  rows == NULL means rows 0..nrows-1.  Y and A are [M][nrows].
- * fmt 0 = Q4_K, 1 = IQ3.  Rows are independent; with nthreads > 1 they are
+ * fmt 0 = Q4_K, 1 = IQ3 (page 4), 2 = IQ3_XXS (page 3).  Rows are independent; with nthreads > 1 they are
  * split across OpenMP threads (each row's sum is still sequential). */
 static void gemv_rows(int fmt, const uint8_t *W, const uint8_t *grid, const float *X,
                       int M, int64_t K, const int64_t *rows, int64_t nrows,
@@ -195,8 +244,10 @@ static void gemv_rows(int fmt, const uint8_t *W, const uint8_t *grid, const floa
             const uint8_t *blk = W + (row * nb + b) * bytes;
             if (fmt == 0)
                 oracle_dequant_q4k_block(blk, w);
-            else
+            else if (fmt == 1)
                 oracle_dequant_iq3_block(blk, grid, w);
+            else
+                oracle_dequant_iq3xxs_block(blk, grid, w);
             for (int m = 0; m < M; ++m) {
                 const float *x = X + (int64_t)m * K + b * QK;
                 double y = Y[(int64_t)m * nrows + r], a = A[(int64_t)m * nrows + r];
@@ -222,6 +273,12 @@ void oracle_gemv_iq3(const uint8_t *W, const uint8_t *grid, const float *X, int 
                      const int64_t *rows, int64_t nrows, double *Y, double *A, int nthreads)
 {
     gemv_rows(1, W, grid, X, M, K, rows, nrows, Y, A, nthreads);
+}
+
+void oracle_gemv_iq3xxs(const uint8_t *W, const uint8_t *grid, const float *X, int M, int64_t K,
+                        const int64_t *rows, int64_t nrows, double *Y, double *A, int nthreads)
+{
+    gemv_rows(2, W, grid, X, M, K, rows, nrows, Y, A, nthreads);
 }
 
 int oracle_max_threads(void)

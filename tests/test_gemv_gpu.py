@@ -393,3 +393,46 @@ def test_gemv_q4k_x_range(q, scale, M):
     y = q.qgemv_q4k(dev(W), dev(x)).cpu().numpy()
     assert np.isfinite(y).all()
     check_tol(y, Y, A, TAU_FMA, f"x scale {scale:g}, M={M}")
+
+
+# ------------------------------------------------------------ IQ3_XXS (page 3 order)
+@pytest.mark.parametrize("N,K", [(1, 256), (33, 2304), (40, 4096)])
+def test_dequant_iq3xxs_bit_exact(q, N, K):
+    W, grid = synth.gen_iq3(N, K, 300 + N)
+    W = oracle.iq3_to_iq3xxs(W, K)
+    ref = oracle.dequant_iq3xxs(W, grid, K)
+    got = q.qdequant_iq3xxs(dev(W), dev(grid), K).cpu().numpy()
+    assert np.array_equal(got.view(np.uint32), ref.view(np.uint32))
+
+
+def test_dequant_iq3xxs_handworked_block(q, golden):
+    from tests.test_oracle_pins import _iq3xxs_golden
+    grid, blk, vals = _iq3xxs_golden(golden)
+    got = q.qdequant_iq3xxs(dev(blk), dev(grid), 256).cpu().numpy()[0]
+    for ib, v in vals.items():
+        assert got[32 * ib:32 * ib + 32].tolist() == v
+
+
+@pytest.mark.parametrize("N,K", [(64, 2048), (100, 4096), (300, 2048), (33, 768), (57, 6144)])
+@pytest.mark.parametrize("M", [1, 2, 3, 8])
+def test_gemv_iq3xxs(q, N, K, M):
+    """Both decode paths (two-row half blocks for M <= 2, whole blocks for
+    M > 2) and the byte-addressed path (K/256 not a multiple of 8)."""
+    W, grid = synth.gen_iq3(N, K, 400 + N + K)
+    W = oracle.iq3_to_iq3xxs(W, K)
+    x = synth.gen_x(M, K, 401)
+    Y, A = oracle.gemv_iq3xxs(W, grid, x)
+    y = q.qgemv_iq3xxs(dev(W), dev(grid), dev(x)).cpu().numpy()
+    check_tol(y, Y, A, TAU_FMA, f"iq3xxs N={N} K={K} M={M}")
+
+
+def test_gemv_iq3xxs_full_size_sampled(q):
+    K, N = 8192, 28672
+    W, grid = synth.gen_iq3(N, K, 4)
+    W = oracle.iq3_to_iq3xxs(W, K)
+    x = synth.gen_x(1, K, 5)
+    rng = np.random.default_rng(3)
+    rows = np.unique(np.concatenate([[0, N - 1], rng.integers(0, N, 64)]))
+    Y, A = oracle.gemv_iq3xxs(W, grid, x, rows=rows)
+    y = q.qgemv_iq3xxs(dev(W), dev(grid), dev(x), flags=q.QG_PREFETCH_WEIGHTS).cpu().numpy()
+    check_tol(y[:, rows], Y, A, TAU_FMA, "iq3xxs full")

@@ -157,8 +157,8 @@ def test_q4k_weight_positions_distinct_per_nibble():
 
 
 # ------------------------------------------------------------------- IQ3
-def _iq3_golden(golden):
-    rows = golden("iq3_block_handworked.txt")
+def _iq3_golden(golden, name="iq3_block_handworked.txt"):
+    rows = golden(name)
     grid = np.full((256, 4), 4, np.uint8)
     subs, vals, d = {}, {}, None
     for r in rows:
@@ -407,3 +407,64 @@ def test_fused_gemv_reduces_to_the_plain_oracle():
     R = synth.gen_x(3, 33, 25)
     Yr, _ = oracle.fused_gemv_q4k(W, x, up=up, residual=R)
     assert np.array_equal(Yr, Ys + R.astype(np.float64))
+
+
+# ------------------------------------------------------------------ IQ3_XXS
+def _iq3xxs_golden(golden):
+    """The golden fields written in page 3's order: d, the 64 index bytes,
+    the eight words (built by hand here, not by a converter)."""
+    grid, p4blk, vals = _iq3_golden(golden, "iq3xxs_block_handworked.txt")
+    d16 = p4blk[96:98]
+    blk = np.concatenate([d16, p4blk[0:64], p4blk[64:96]]).astype(np.uint8)
+    return grid, blk, vals
+
+
+def test_iq3xxs_handworked_block(golden):
+    grid, blk, vals = _iq3xxs_golden(golden)
+    assert blk.size == 98 and blk[0:2].tolist() == [0x00, 0x3C]      # d first (page 3)
+    w = oracle.dequant_iq3xxs(blk[None, :], grid, 256)[0]
+    for ib, v in vals.items():
+        assert w[32 * ib:32 * ib + 32].tolist() == v, ib
+    for ib in range(4, 8):
+        assert w[32 * ib:32 * ib + 32].tolist() == vals[3]
+
+
+def test_iq3xxs_is_page4_reordered_and_doubled():
+    """Page 3's eff = d*(0.5+s)*0.5 times the raw entry versus page 4's
+    d*(0.5+code)*0.5 * entry*0.5: the same fields in the two byte orders
+    give values in a ratio of exactly 2."""
+    K = 768
+    W, grid = synth.gen_iq3(9, K, 31)
+    x3 = oracle.iq3_to_iq3xxs(W, K)
+    assert not np.array_equal(x3, W)
+    a = oracle.dequant_iq3(W, grid, K)
+    b = oracle.dequant_iq3xxs(x3, grid, K)
+    assert np.array_equal(b, 2.0 * a)
+    x = synth.gen_x(2, K, 32)
+    Ya, Aa = oracle.gemv_iq3(W, grid, x)
+    Yb, Ab = oracle.gemv_iq3xxs(x3, grid, x)
+    assert np.array_equal(Yb, 2.0 * Ya) and np.array_equal(Ab, 2.0 * Aa)
+
+
+def test_iq3xxs_field_positions():
+    """Bytes 0-1 scale the whole block; a byte in 2-65 moves one 4-weight
+    group; the top byte of the word at 66+4*ib changes only sub-block ib."""
+    K = 256
+    W, grid = synth.gen_iq3(1, K, 33)
+    W = oracle.iq3_to_iq3xxs(W, K)
+    base = oracle.dequant_iq3xxs(W, grid, K)[0]
+    v = W.copy()
+    v[0, 0:2] = np.array([0x3C00], "<u2").view(np.uint8)              # d = 1
+    v2 = v.copy()
+    v2[0, 0:2] = np.array([0x4000], "<u2").view(np.uint8)             # d = 2
+    assert np.array_equal(oracle.dequant_iq3xxs(v2, grid, K), 2.0 * oracle.dequant_iq3xxs(v, grid, K))
+    for t in (2, 17, 65):
+        w2 = W.copy()
+        w2[0, t] ^= 0x5A
+        diff = np.nonzero(oracle.dequant_iq3xxs(w2, grid, K)[0] != base)[0]
+        assert diff.size and diff.min() >= 4 * (t - 2) and diff.max() < 4 * (t - 2) + 4
+    for ib in (0, 5, 7):
+        w3 = W.copy()
+        w3[0, 66 + 4 * ib + 3] ^= 0x30                                  # bits 28-29: s
+        diff = np.nonzero(oracle.dequant_iq3xxs(w3, grid, K)[0] != base)[0]
+        assert diff.size and diff.min() >= 32 * ib and diff.max() < 32 * ib + 32
