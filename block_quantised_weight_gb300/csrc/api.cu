@@ -149,6 +149,32 @@ int qgemv_iq3xxs(const uint8_t* W, const uint8_t* grid, const float* X, float* Y
     return qgemv_iq3xxs_ex(W, grid, X, Y, M, N, K, 0u, stream);
 }
 
+static int64_t codebook_bytes(int format) {
+    return format == QG_CB_IQ4_NL || format == QG_CB_IQ4_XS ? 16 : 2048;
+}
+
+int qgemv_codebook(int format, const uint8_t* W, const void* codebook, const float* X, float* Y, int M, int64_t N,
+                   int64_t K, cudaStream_t stream) {
+    if (format < QG_CB_IQ4_NL || format > QG_CB_IQ2_XXS || !codebook) return QG_EINVAL;
+    const uint8_t* book = static_cast<const uint8_t*>(codebook);
+    int rc = check_gemv(W, nullptr, false, X, Y, M, N, K, qg::cb_unit_bytes(format));
+    if (rc != QG_OK) return rc;
+    if (!aligned16(book)) return QG_EALIGN;
+    if (overlap(Y, int64_t(M) * N * 4, book, codebook_bytes(format))) return QG_EALIAS;
+    return qg::launch_gemv_cb(format, W, book, X, Y, M, N, K, stream);
+}
+
+int qdequant_codebook(int format, const uint8_t* W, const void* codebook, float* out, int64_t N, int64_t K,
+                      cudaStream_t stream) {
+    if (format < QG_CB_IQ4_NL || format > QG_CB_IQ2_XXS || !codebook) return QG_EINVAL;
+    const uint8_t* book = static_cast<const uint8_t*>(codebook);
+    int rc = check_dequant(W, nullptr, false, out, N, K, qg::cb_unit_bytes(format));
+    if (rc != QG_OK) return rc;
+    if (!aligned16(book)) return QG_EALIGN;
+    if (overlap(out, N * K * 4, book, codebook_bytes(format))) return QG_EALIAS;
+    return qg::launch_dequant_cb(format, W, book, out, N, K, stream);
+}
+
 // Group checks: every matrix as a single GEMV, plus no Y[i] overlapping any
 // other matrix's W or Y.
 static int check_group(const uint8_t* const* W, float* const* Y, const int64_t* N, int count, const uint8_t* grid,

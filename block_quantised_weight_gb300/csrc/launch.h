@@ -23,6 +23,12 @@ int launch_gemv_iq3xxs(const uint8_t* W, const uint8_t* grid, const float* X, fl
 int launch_dequant_iq3xxs(const uint8_t* W, const uint8_t* grid, float* out, int64_t N, int64_t K, cudaStream_t s);
 int launch_group_iq3(const uint8_t* const* W, float* const* Y, const int64_t* N, int count, const uint8_t* grid,
                      const float* X, int M, int64_t K, cudaStream_t s, unsigned* status, unsigned flags);
+// page 3's codebook formats (QG_CB_*)
+int cb_unit_bytes(int format);
+int launch_gemv_cb(int format, const uint8_t* W, const void* book, const float* X, float* Y, int M, int64_t N,
+                   int64_t K, cudaStream_t s);
+int launch_dequant_cb(int format, const uint8_t* W, const void* book, float* out, int64_t N, int64_t K,
+                      cudaStream_t s);
 int launch_pass_q4k(const qg_stage* stages, int nstages, int M, unsigned* sync, cudaStream_t s, unsigned* status);
 int launch_dequant_q4k(const uint8_t* W, float* out, int64_t N, int64_t K, cudaStream_t s);
 int launch_dequant_iq3(const uint8_t* W, const uint8_t* grid, float* out, int64_t N, int64_t K, cudaStream_t s);

@@ -40,8 +40,10 @@ class QgFuse(ctypes.Structure):
                 ("residual", ctypes.c_void_p * 4)]
 
 QG_PREFETCH_WEIGHTS = 1
+QG_CB = {"iq4nl": 1, "iq4xs": 2, "iq3s": 3, "iq2xxs": 4}
+CB_UNIT_BYTES = {"iq4nl": 144, "iq4xs": 136, "iq3s": 110, "iq2xxs": 66}
 
-EXPORTS = ("qgemv_q4k", "qgemv_q4k_ex", "qgemv_q4k_group", "qgemv_q4k_fused", "qgemv_q4k_fused_group", "qgemv_q4k_pass", "qgemv_q4k_pass_noalloc", "qgemv_iq3", "qgemv_iq3_ex", "qgemv_iq3_group", "qgemv_iq3xxs", "qgemv_iq3xxs_ex", "qdequant_iq3xxs", "qgemm_q4k_batched", "qgemm_iq3_batched", "qdequant_q4k", "qdequant_iq3",
+EXPORTS = ("qgemv_q4k", "qgemv_q4k_ex", "qgemv_q4k_group", "qgemv_q4k_fused", "qgemv_q4k_fused_group", "qgemv_q4k_pass", "qgemv_q4k_pass_noalloc", "qgemv_iq3", "qgemv_iq3_ex", "qgemv_iq3_group", "qgemv_iq3xxs", "qgemv_iq3xxs_ex", "qdequant_iq3xxs", "qgemv_codebook", "qdequant_codebook", "qgemm_q4k_batched", "qgemm_iq3_batched", "qdequant_q4k", "qdequant_iq3",
            "qg_device_status", "qg_test_bounded_wait", "qg_strerror")
 
 
@@ -74,6 +76,8 @@ def load():
             "qgemv_iq3xxs": [vp, vp, vp, vp, ci, i64, i64, vp],
             "qgemv_iq3xxs_ex": [vp, vp, vp, vp, ci, i64, i64, ctypes.c_uint, vp],
             "qdequant_iq3xxs": [vp, vp, vp, i64, i64, vp],
+            "qgemv_codebook": [ci, vp, vp, vp, vp, ci, i64, i64, vp],
+            "qdequant_codebook": [ci, vp, vp, vp, i64, i64, vp],
             "qgemv_q4k_group": [vp, vp, vp, ci, vp, ci, i64, ctypes.c_uint, vp],
             "qgemv_iq3_group": [vp, vp, vp, ci, vp, vp, ci, i64, ctypes.c_uint, vp],
             "qgemv_q4k_fused": [vp, vp, vp, ci, i64, i64, vp, ctypes.c_uint, vp],
@@ -183,6 +187,29 @@ def qgemv_iq3xxs(W, grid, X, out=None, stream=None, flags=0):
     rc = load().qgemv_iq3xxs_ex(W.data_ptr(), grid.data_ptr(), X.data_ptr(), out.data_ptr(), M, N, K, flags,
                                 _stream(stream))
     _check("qgemv_iq3xxs_ex", rc)
+    return out
+
+
+def qgemv_codebook(fmt, W, codebook, X, out=None, stream=None):
+    """Y = X @ dequant(W)^T for page 3's codebook formats ("iq4nl", "iq4xs",
+    "iq3s", "iq2xxs"); codebook: int8 [16] or uint8 [512, 4] / [256, 8]."""
+    _req(codebook, codebook.dtype, "codebook")
+    X, out, M, N, K = _xy(W, X, out, CB_UNIT_BYTES[fmt])
+    rc = load().qgemv_codebook(QG_CB[fmt], W.data_ptr(), codebook.data_ptr(), X.data_ptr(), out.data_ptr(), M, N, K,
+                               _stream(stream))
+    _check("qgemv_codebook", rc)
+    return out
+
+
+def qdequant_codebook(fmt, W, codebook, K, out=None, stream=None):
+    """Test-only: fp32 [N, K] dequantisation of a codebook-format matrix."""
+    import torch
+    _req(W, torch.uint8, "W")
+    N = W.numel() // (K // 256 * CB_UNIT_BYTES[fmt])
+    if out is None:
+        out = torch.empty((N, K), dtype=torch.float32, device=W.device)
+    _check("qdequant_codebook", load().qdequant_codebook(QG_CB[fmt], W.data_ptr(), codebook.data_ptr(),
+                                                         out.data_ptr(), N, K, _stream(stream)))
     return out
 
 

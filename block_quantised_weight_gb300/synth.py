@@ -19,6 +19,14 @@ module docstring):
 * The IQ3 grid is 256 rows x 4 bytes drawn i.i.d. from the doubled-unit
   magnitudes {4, 12, 20, 28, 36, 44, 52, 62}.
 * Activations ``x`` are fp32 ``N(0, 1)``, shape ``[M, K]``.
+* Page 3's other codebook formats (block sizes, d at bytes 0-1, the rest of
+  the bytes uniform uint8, d ~ U(1e-3, 4e-3) rounded to fp16; the codebooks
+  are not printed on the pages, so they are drawn too):
+  IQ4_NL (18 bytes per 32 weights, eight blocks per 256) and IQ4_XS (136
+  bytes per 256) with a table of 16 distinct sorted int8 values drawn from
+  [-127, 127]; IQ3_S (110 bytes) with a 512 x 4 grid drawn from
+  {1, 3, ..., 15}; IQ2_XXS (66 bytes) with a 256 x 8 grid drawn from
+  {8, 24, 40}.  Draw order: codebook, the block bytes, d.
 
 Draw order for one Q4_K matrix: d, dmin, the 12 scale bytes, the 128 qs bytes,
 then x. For one IQ3 matrix: grid, the 96 index/word bytes, d, then x.
@@ -86,6 +94,41 @@ def gen_iq3(N: int, K: int, seed, grid_seed=None):
     blk[:, 0:96] = body
     blk[:, 96:98] = _fp16_bytes(d)
     return blk.reshape(N, -1), grid
+
+
+# Page 3's codebook formats: bytes per 256 weights, bytes per fp16 d field
+# (one per 32 weights for IQ4_NL, one per 256 otherwise).
+CB_UNIT_BYTES = {"iq4nl": 144, "iq4xs": 136, "iq3s": 110, "iq2xxs": 66}
+
+
+def gen_cb_table(fmt: str, seed) -> np.ndarray:
+    """Random codebook of a page-3 format: int8 [16] (IQ4), uint8 [512, 4]
+    (IQ3_S) or uint8 [256, 8] (IQ2_XXS)."""
+    rng = _rng(seed)
+    if fmt in ("iq4nl", "iq4xs"):
+        return np.sort(rng.choice(np.arange(-127, 128), 16, replace=False)).astype(np.int8)
+    if fmt == "iq3s":
+        return (2 * rng.integers(0, 8, (512, 4)) + 1).astype(np.uint8)
+    if fmt == "iq2xxs":
+        return np.array([8, 24, 40], dtype=np.uint8)[rng.integers(0, 3, (256, 8))]
+    raise ValueError(fmt)
+
+
+def gen_cb(fmt: str, N: int, K: int, seed):
+    """Random matrix of a page-3 codebook format: ``(W uint8 [N, K/256*B], table)``."""
+    if K % QK:
+        raise ValueError(f"K must be a multiple of {QK}, got {K}")
+    rng = _rng(seed)
+    table = gen_cb_table(fmt, rng)
+    units = N * (K // QK)
+    if fmt == "iq4nl":   # eight 18-byte blocks per 256 weights, each with its own d
+        nblk = 8 * units
+        blk = rng.integers(0, 256, (nblk, 18), dtype=np.uint8)
+        blk[:, 0:2] = _fp16_bytes(rng.uniform(1e-3, 4e-3, nblk))
+    else:
+        blk = rng.integers(0, 256, (units, CB_UNIT_BYTES[fmt]), dtype=np.uint8)
+        blk[:, 0:2] = _fp16_bytes(rng.uniform(1e-3, 4e-3, units))
+    return blk.reshape(N, -1), table
 
 
 def gen_x(M: int, K: int, seed) -> np.ndarray:

@@ -119,6 +119,46 @@ QG_API int qgemv_iq3xxs(const uint8_t* W, const uint8_t* grid, const float* X, f
 QG_API int qgemv_iq3xxs_ex(const uint8_t* W, const uint8_t* grid, const float* X, float* Y, int M, int64_t N,
                            int64_t K, unsigned flags, cudaStream_t stream);
 
+/* Page 3's other codebook formats (llama.cpp's codebook formats as
+ * trainable students: the format table, get_s, eff_np, encode).  Every one
+ * stores weight = eff * v with v = codebook entry * sign, d the block's
+ * fp16 scale at bytes 0-1; bytes per 256 weights and codebook (an input,
+ * since the pages do not print it):
+ *   QG_CB_IQ4_NL   144 (eight 18-byte blocks of 32 weights: d, then byte i =
+ *                  code of weight i | code of weight i+16 << 4); eff = d;
+ *                  codebook: 16 int8 values
+ *   QG_CB_IQ4_XS   136: d; u16 @2 = bits 4-5 of the eight 6-bit s (2 per
+ *                  sub-block); @4-7 their low nibbles (sub-block j: nibble j,
+ *                  low first); @8-135 the codes, 16 bytes per 32-weight
+ *                  sub-block packed as IQ4_NL; eff = d*(s-32); codebook as
+ *                  IQ4_NL (the code layout is not printed on the pages; this
+ *                  is the reading that shares IQ4_NL's packing)
+ *   QG_CB_IQ3_S    110: d; @2-65 low 8 bits of the 64 grid indices (one per
+ *                  4 weights); @66-73 their 9th bits (index i: bit i%8 of byte
+ *                  66+i/8); @74-105 one sign bit per weight (weight k: bit k%8
+ *                  of byte 74+k/8, set = negative); @106-109 the 4-bit s
+ *                  (sub-block j: nibble j, low first); eff = d*(1+2s);
+ *                  codebook: 512 x 4 bytes
+ *   QG_CB_IQ2_XXS  66: d; per 32-weight sub-block j two u32 at 2+8j: the grid
+ *                  indices of its four 8-weight groups (byte g), then the
+ *                  groups' 7-bit sign fields (bits 7g..7g+6, the eighth sign
+ *                  their parity: an even count of negatives) and s in bits
+ *                  28-31; eff = d*(0.5+s)*0.25; codebook: 256 x 8 bytes
+ * W [N][K/256 units], X [M][K], Y [M][N] as qgemv_q4k; 1 <= M <= 32;
+ * codebook device memory, 16-byte aligned.  fp32 FMA path, tolerance
+ * 1e-5 * sum|w*x|.  Errors as qgemv_q4k, plus QG_EINVAL for an unknown
+ * format. */
+#define QG_CB_IQ4_NL 1
+#define QG_CB_IQ4_XS 2
+#define QG_CB_IQ3_S 3
+#define QG_CB_IQ2_XXS 4
+QG_API int qgemv_codebook(int format, const uint8_t* W, const void* codebook, const float* X, float* Y, int M,
+                          int64_t N, int64_t K, cudaStream_t stream);
+
+/* Test-only: dequantise a codebook-format matrix to fp32 out[N][K] (exact). */
+QG_API int qdequant_codebook(int format, const uint8_t* W, const void* codebook, float* out, int64_t N, int64_t K,
+                             cudaStream_t stream);
+
 /* Several Q4_K GEMVs that read the same X (in a decode step: q, k and v of a
  * layer read the attention-norm output; gate and up read the FFN-norm
  * output) in one launch: Y[i] = X * dequant(W[i])^T for i < count,

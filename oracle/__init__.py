@@ -66,6 +66,9 @@ def _load():
         lib.oracle_gemv_iq3.argtypes = [u8p, u8p, f32p, ctypes.c_int, i64, i64p, i64, f64p,
                                         f64p, ctypes.c_int]
         lib.oracle_dequant_iq3xxs.argtypes = [u8p, u8p, i64, i64, f32p]
+        lib.oracle_dequant_cb.argtypes = [ctypes.c_int, u8p, u8p, i64, i64, f32p]
+        lib.oracle_gemv_cb.argtypes = [ctypes.c_int, u8p, u8p, f32p, ctypes.c_int, i64, i64p, i64, f64p,
+                                       f64p, ctypes.c_int]
         lib.oracle_gemv_iq3xxs.argtypes = [u8p, u8p, f32p, ctypes.c_int, i64, i64p, i64, f64p,
                                            f64p, ctypes.c_int]
         lib.oracle_max_threads.restype = ctypes.c_int
@@ -140,6 +143,53 @@ def dequant_iq3xxs(W: np.ndarray, grid: np.ndarray, K: int) -> np.ndarray:
     _load().oracle_dequant_iq3xxs(_ptr(W, ctypes.c_uint8), _ptr(grid, ctypes.c_uint8), N, K,
                                   _ptr(out, ctypes.c_float))
     return out
+
+
+# Page 3's other codebook formats: oracle.c format code, bytes per 256
+# weights, codebook shape (entries, width) and dtype.
+CB_FORMATS = {
+    "iq4nl": (3, 144, (16,), np.int8),
+    "iq4xs": (4, 136, (16,), np.int8),
+    "iq3s": (5, 110, (512, 4), np.uint8),
+    "iq2xxs": (6, 66, (256, 8), np.uint8),
+}
+
+
+def _cb_args(fmt, W, table, K):
+    code, ub, shape, dt = CB_FORMATS[fmt]
+    W = np.ascontiguousarray(W, dtype=np.uint8)
+    t = np.ascontiguousarray(table, dtype=dt).reshape(shape)
+    N = _check_rows(W, K, ub)
+    return code, W, t.view(np.uint8), N
+
+
+def dequant_cb(fmt: str, W: np.ndarray, table: np.ndarray, K: int) -> np.ndarray:
+    """fp32 [N, K] weights of a page-3 codebook format (iq4nl, iq4xs, iq3s, iq2xxs)."""
+    code, W, t, N = _cb_args(fmt, W, table, K)
+    out = np.empty((N, K), dtype=np.float32)
+    _load().oracle_dequant_cb(code, _ptr(W, ctypes.c_uint8), _ptr(t, ctypes.c_uint8), N, K,
+                              _ptr(out, ctypes.c_float))
+    return out
+
+
+def gemv_cb(fmt: str, W, table, X, rows=None, nthreads=None):
+    """(Y, A) of a page-3 codebook-format GEMV, fp64 as gemv_q4k."""
+    X = np.ascontiguousarray(X, dtype=np.float32)
+    if X.ndim == 1:
+        X = X[None, :]
+    M, K = X.shape
+    code, W, t, N = _cb_args(fmt, W, table, K)
+    rows_arr = np.arange(N, dtype=np.int64) if rows is None else np.ascontiguousarray(rows, dtype=np.int64)
+    if rows_arr.size and (rows_arr.min() < 0 or rows_arr.max() >= N):
+        raise ValueError("row index out of range")
+    nr = rows_arr.size
+    Y = np.empty((M, nr), dtype=np.float64)
+    A = np.empty((M, nr), dtype=np.float64)
+    nt = max_threads() if nthreads is None else int(nthreads)
+    _load().oracle_gemv_cb(code, _ptr(W, ctypes.c_uint8), _ptr(t, ctypes.c_uint8), _ptr(X, ctypes.c_float), M, K,
+                           _ptr(rows_arr, ctypes.c_int64), nr, _ptr(Y, ctypes.c_double),
+                           _ptr(A, ctypes.c_double), nt)
+    return Y, A
 
 
 def iq3_to_iq3xxs(W: np.ndarray, K: int) -> np.ndarray:

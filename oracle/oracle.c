@@ -18,6 +18,10 @@
  *     uint32s at bytes 66-97, eff = d*(0.5+s)*0.5), the class Format /
  *     eff_np (eff times v, v = codebook entry times sign) and the note that
  *     IQ3_XXS stores 8 signs in 7 bits with an even count of negatives.
+ *   - IQ4_NL, IQ4_XS, IQ3_S, IQ2_XXS: page 3, the format table (block and
+ *     sub-block sizes, eff, byte counts, where d and s sit), get_s (how s is
+ *     read), eff_np (eff = d, d*(s-32), d*(1+2s), d*(0.5+s)*0.25) and
+ *     encode (the code bytes of IQ4_NL, IQ3_S and IQ2_XXS).
  *   - GEMV: page 1, model_forward / forward: matmul(out, x, W, n_in, n_out)
  *     computes out = W x with one output per row of W.
  *
@@ -193,6 +197,132 @@ void oracle_dequant_iq3xxs_block(const uint8_t *blk, const uint8_t *grid, float 
     }
 }
 
+/* ---- page 3's other codebook formats, decoded per 256 weights ----------
+ * Every one stores weight = eff * v, v = (codebook entry) * (sign), d the
+ * block's fp16 scale at bytes 0-1 and s the sub-block scales; products are
+ * exact in fp32 (page 3: "v*eff is exact in fp32").  The codebooks are not
+ * printed on the pages; they are inputs: the IQ4 table as 16 signed bytes,
+ * the IQ3_S grid as 512 x 4 bytes, the IQ2_XXS grid as 256 x 8 bytes. */
+
+/* IQ4_NL: 32 weights in 18 bytes: d, then 16 bytes where byte i holds the
+ * code of weight i in its low nibble and of weight i+16 in its high nibble
+ * (page 3, encode: q[:16] | q[16:] << 4); eff = d; v = table[code].  One
+ * 256-weight unit is 8 consecutive blocks (144 bytes). */
+void oracle_dequant_iq4nl_unit(const uint8_t *u, const int8_t *table, float *out)
+{
+    for (int b = 0; b < 8; ++b) {
+        const uint8_t *blk = u + 18 * b;
+        float d = oracle_f16_to_f32(le16(blk));
+        for (int i = 0; i < 16; ++i) {
+            uint8_t q = blk[2 + i];
+            out[32 * b + i] = d * (float)table[q & 0xF];
+            out[32 * b + 16 + i] = d * (float)table[q >> 4];
+        }
+    }
+}
+
+/* IQ4_XS: 256 weights in 136 bytes: d at 0-1; s of sub-block j (6 bits) =
+ * nibble j of bytes 4-7 (low nibble first: page 3 get_s's _nibbles) plus
+ * bits 2j, 2j+1 of the little-endian u16 at bytes 2-3 as bits 4-5;
+ * eff = d * (s - 32); v = table[code].  The code bytes are bytes 8-135,
+ * 16 per 32-weight sub-block, packed as in IQ4_NL (low nibble weight i,
+ * high nibble weight i+16): the pages do not print IQ4_XS's code layout,
+ * this is the reading that shares IQ4_NL's codebook and packing. */
+void oracle_dequant_iq4xs_unit(const uint8_t *u, const int8_t *table, float *out)
+{
+    float d = oracle_f16_to_f32(le16(u));
+    uint16_t sh = le16(u + 2);
+    for (int j = 0; j < 8; ++j) {
+        int lo = (u[4 + j / 2] >> (4 * (j & 1))) & 0xF;
+        int hi = (sh >> (2 * j)) & 3;
+        int s = lo | (hi << 4);
+        float eff = d * (float)(s - 32);
+        const uint8_t *qs = u + 8 + 16 * j;
+        for (int i = 0; i < 16; ++i) {
+            out[32 * j + i] = eff * (float)table[qs[i] & 0xF];
+            out[32 * j + 16 + i] = eff * (float)table[qs[i] >> 4];
+        }
+    }
+}
+
+/* IQ3_S: 256 weights in 110 bytes: d; bytes 2-65 the low 8 bits of the 64
+ * grid indices (one per 4 weights); bytes 66-73 their 9th bits, index i at
+ * bit i%8 of byte 66+i/8 (packbits, little bit order); bytes 74-105 one
+ * sign bit per weight, weight k at bit k%8 of byte 74+k/8 (set = negative);
+ * bytes 106-109 the eight 4-bit s, sub-block j in nibble j (low first);
+ * eff = d * (1 + 2s); v = grid[index][k%4] * sign (page 3, encode, get_s). */
+void oracle_dequant_iq3s_unit(const uint8_t *u, const uint8_t *grid, float *out)
+{
+    float d = oracle_f16_to_f32(le16(u));
+    for (int j = 0; j < 8; ++j) {
+        int s = (u[106 + j / 2] >> (4 * (j & 1))) & 0xF;
+        float eff = d * (float)(1 + 2 * s);
+        for (int t = 0; t < 32; ++t) {
+            int k = 32 * j + t;
+            int gi = k / 4;
+            int idx = u[2 + gi] | (((u[66 + gi / 8] >> (gi % 8)) & 1) << 8);
+            float v = (float)grid[4 * idx + (k % 4)];
+            if ((u[74 + k / 8] >> (k % 8)) & 1) v = -v;
+            out[k] = eff * v;
+        }
+    }
+}
+
+/* IQ2_XXS: 256 weights in 66 bytes: d; then per 32-weight sub-block j two
+ * little-endian u32 at 2+8j: the first holds the grid indices of its four
+ * 8-weight groups (byte g), the second the groups' 7-bit sign fields at bits
+ * 7g..7g+6 (bit i set = weight i of the group negative; the eighth sign is
+ * their parity, an even count of negatives) and s in bits 28-31;
+ * eff = d * (0.5 + s) * 0.25; v = grid[index][i] * sign (page 3, encode,
+ * get_s, the even-sign note). */
+void oracle_dequant_iq2xxs_unit(const uint8_t *u, const uint8_t *grid, float *out)
+{
+    float d = oracle_f16_to_f32(le16(u));
+    for (int j = 0; j < 8; ++j) {
+        uint32_t aux0 = le32(u + 2 + 8 * j), aux1 = le32(u + 6 + 8 * j);
+        float s = (float)((aux1 >> 28) & 0xF);
+        float eff = d * (0.5f + s) * 0.25f;
+        for (int g = 0; g < 4; ++g) {
+            uint32_t idx = (aux0 >> (8 * g)) & 0xFF;
+            uint32_t seven = (aux1 >> (7 * g)) & 0x7F, par = 0;
+            for (int i = 0; i < 8; ++i) {
+                uint32_t neg;
+                if (i < 7) {
+                    neg = (seven >> i) & 1u;
+                    par ^= neg;
+                } else {
+                    neg = par;
+                }
+                float v = (float)grid[8 * idx + i];
+                if (neg) v = -v;
+                out[32 * j + 8 * g + i] = eff * v;
+            }
+        }
+    }
+}
+
+/* Bytes per 256-weight unit of the formats above (fmt 3..6). */
+static int64_t cb_unit_bytes(int fmt)
+{
+    return fmt == 3 ? 144 : fmt == 4 ? 136 : fmt == 5 ? 110 : 66;
+}
+
+static void cb_unit(int fmt, const uint8_t *u, const uint8_t *tab, float *out)
+{
+    if (fmt == 3) oracle_dequant_iq4nl_unit(u, (const int8_t *)tab, out);
+    else if (fmt == 4) oracle_dequant_iq4xs_unit(u, (const int8_t *)tab, out);
+    else if (fmt == 5) oracle_dequant_iq3s_unit(u, tab, out);
+    else oracle_dequant_iq2xxs_unit(u, tab, out);
+}
+
+void oracle_dequant_cb(int fmt, const uint8_t *W, const uint8_t *tab, int64_t N, int64_t K, float *out)
+{
+    int64_t nb = K / QK, ub = cb_unit_bytes(fmt);
+    for (int64_t n = 0; n < N; ++n)
+        for (int64_t b = 0; b < nb; ++b)
+            cb_unit(fmt, W + (n * nb + b) * ub, tab, out + n * K + b * QK);
+}
+
 /* Whole rows: W is [N][K/256 blocks], out is [N][K] fp32. */
 void oracle_dequant_q4k(const uint8_t *W, int64_t N, int64_t K, float *out)
 {
@@ -221,14 +351,15 @@ void oracle_dequant_iq3xxs(const uint8_t *W, const uint8_t *grid, int64_t N, int
 /* GEMV reference for selected rows.  Y[m][r] = sum_k (double)w[row][k] * (double)x[m][k],
  * summed in k order in fp64; A[m][r] = sum_k |w*x| in fp64 (the scale of the
  * tolerance).  rows == NULL means rows 0..nrows-1.  Y and A are [M][nrows].
- * fmt 0 = Q4_K, 1 = IQ3 (page 4), 2 = IQ3_XXS (page 3).  Rows are independent; with nthreads > 1 they are
+ * fmt 0 = Q4_K, 1 = IQ3 (page 4), 2 = IQ3_XXS, 3 = IQ4_NL, 4 = IQ4_XS,
+ * 5 = IQ3_S, 6 = IQ2_XXS (page 3; grid = the format's codebook).  Rows are independent; with nthreads > 1 they are
  * split across OpenMP threads (each row's sum is still sequential). */
 static void gemv_rows(int fmt, const uint8_t *W, const uint8_t *grid, const float *X,
                       int M, int64_t K, const int64_t *rows, int64_t nrows,
                       double *Y, double *A, int nthreads)
 {
     int64_t nb = K / QK;
-    int64_t bytes = fmt == 0 ? Q4K_BYTES : IQ3_BYTES;
+    int64_t bytes = fmt == 0 ? Q4K_BYTES : fmt <= 2 ? IQ3_BYTES : cb_unit_bytes(fmt);
 #ifdef _OPENMP
     if (nthreads < 1) nthreads = 1;
 #pragma omp parallel for schedule(dynamic, 1) num_threads(nthreads)
@@ -246,8 +377,10 @@ static void gemv_rows(int fmt, const uint8_t *W, const uint8_t *grid, const floa
                 oracle_dequant_q4k_block(blk, w);
             else if (fmt == 1)
                 oracle_dequant_iq3_block(blk, grid, w);
-            else
+            else if (fmt == 2)
                 oracle_dequant_iq3xxs_block(blk, grid, w);
+            else
+                cb_unit(fmt, blk, grid, w);
             for (int m = 0; m < M; ++m) {
                 const float *x = X + (int64_t)m * K + b * QK;
                 double y = Y[(int64_t)m * nrows + r], a = A[(int64_t)m * nrows + r];
@@ -279,6 +412,12 @@ void oracle_gemv_iq3xxs(const uint8_t *W, const uint8_t *grid, const float *X, i
                         const int64_t *rows, int64_t nrows, double *Y, double *A, int nthreads)
 {
     gemv_rows(2, W, grid, X, M, K, rows, nrows, Y, A, nthreads);
+}
+
+void oracle_gemv_cb(int fmt, const uint8_t *W, const uint8_t *tab, const float *X, int M, int64_t K,
+                    const int64_t *rows, int64_t nrows, double *Y, double *A, int nthreads)
+{
+    gemv_rows(fmt, W, tab, X, M, K, rows, nrows, Y, A, nthreads);
 }
 
 int oracle_max_threads(void)

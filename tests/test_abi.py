@@ -130,3 +130,14 @@ def test_fused_arguments_rejected_on_host(lib):
     f = qgemv.QgFuse()
     f.residual[0] = A + 0x3000000                             # matrix 0's residual is matrix 1's output
     assert lib.qgemv_q4k_fused_group(Wg, Yg, Ng, 2, X, 1, 256, ctypes.byref(f), 0, None) == qgemv.QG_EALIAS
+
+
+def test_codebook_arguments_rejected_on_host(lib):
+    W, X, Y, B = A, A + 0x10000000, A + 0x20000000, A + 0x30000000
+    assert lib.qgemv_codebook(0, W, B, X, Y, 1, 64, 256, None) == qgemv.QG_EINVAL
+    assert lib.qgemv_codebook(5, W, B, X, Y, 1, 64, 256, None) == qgemv.QG_EINVAL
+    assert lib.qgemv_codebook(1, W, None, X, Y, 1, 64, 256, None) == qgemv.QG_EINVAL
+    assert lib.qgemv_codebook(2, W, B + 4, X, Y, 1, 64, 256, None) == qgemv.QG_EALIGN
+    assert lib.qgemv_codebook(3, W, B, X, Y, 1, 64, 300, None) == qgemv.QG_EINVAL
+    assert lib.qgemv_codebook(4, W, Y + 16, X, Y, 1, 64, 256, None) == qgemv.QG_EALIAS
+    assert lib.qdequant_codebook(1, W, B, W + 16, 4, 256, None) == qgemv.QG_EALIAS

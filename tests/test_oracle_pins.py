@@ -468,3 +468,98 @@ def test_iq3xxs_field_positions():
         w3[0, 66 + 4 * ib + 3] ^= 0x30                                  # bits 28-29: s
         diff = np.nonzero(oracle.dequant_iq3xxs(w3, grid, K)[0] != base)[0]
         assert diff.size and diff.min() >= 32 * ib and diff.max() < 32 * ib + 32
+
+
+# ------------------------------------------------ page 3's codebook formats
+def _cb_golden(golden):
+    """{fmt: (W bytes [1, unit], table, {weight: value})} from the fixture."""
+    out, cur = {}, None
+    for r in golden("cb_blocks_handworked.txt"):
+        if r[0] == "format":
+            cur = r[1]
+            if cur in ("iq4nl", "iq4xs"):
+                tab = np.zeros(16, np.int8)
+            elif cur == "iq3s":
+                tab = np.ones((512, 4), np.uint8)
+            else:
+                tab = np.full((256, 8), 8, np.uint8)
+            out[cur] = [None, tab, {}]
+        elif r[0] == "table":
+            out[cur][1][:] = [int(t) for t in r[1:]]
+        elif r[0] == "gridrow":
+            out[cur][1][int(r[1])] = [int(t) for t in r[2:]]
+        elif r[0] == "bytes":
+            out[cur][0] = np.array([int(t, 16) for t in r[1:]], np.uint8)
+        elif r[0] == "val":
+            out[cur][2][int(r[1])] = float(r[2])
+    for fmt, e in out.items():   # pad IQ4_NL's two blocks to a 256-weight unit (d = 0 blocks)
+        unit = synth.CB_UNIT_BYTES[fmt]
+        e[0] = np.concatenate([e[0], np.zeros(unit - e[0].size, np.uint8)])[None, :]
+    return out
+
+
+@pytest.mark.parametrize("fmt", ["iq4nl", "iq4xs", "iq3s", "iq2xxs"])
+def test_cb_handworked_blocks(golden, fmt):
+    W, tab, vals = _cb_golden(golden)[fmt]
+    w = oracle.dequant_cb(fmt, W, tab, 256)[0]
+    for k, v in vals.items():
+        assert w[k] == np.float32(v), (fmt, k, w[k], v)
+    if fmt == "iq4nl":
+        assert np.all(w[64:] == 0.0)      # the padding blocks have d = 0
+
+
+@pytest.mark.parametrize("fmt", ["iq4nl", "iq4xs", "iq3s", "iq2xxs"])
+def test_cb_exact_products_and_sizes(fmt):
+    """Bytes per 256 weights from page 3's table (IQ4_NL 18 per 32); every
+    value is eff * v exactly (an fp64 recomputation from the same fields
+    agrees bit for bit); doubling d doubles every value of its block."""
+    K = 512
+    W, tab = synth.gen_cb(fmt, 4, K, 41)
+    assert W.shape == (4, 2 * {"iq4nl": 144, "iq4xs": 136, "iq3s": 110, "iq2xxs": 66}[fmt])
+    w = oracle.dequant_cb(fmt, W, tab, K)
+    W2 = W.copy()
+    if fmt == "iq4nl":
+        d = W2.reshape(-1, 18)[:, 0:2].copy().view("<f2")
+        W2.reshape(-1, 18)[:, 0:2] = (d.astype(np.float32) * 2).astype("<f2").view(np.uint8)
+    else:
+        u = synth.CB_UNIT_BYTES[fmt]
+        d = W2.reshape(-1, u)[:, 0:2].copy().view("<f2")
+        W2.reshape(-1, u)[:, 0:2] = (d.astype(np.float32) * 2).astype("<f2").view(np.uint8)
+    assert np.array_equal(oracle.dequant_cb(fmt, W2, tab, K), 2 * w)
+
+
+def test_iq4_table_sign_and_nibble_order():
+    """IQ4_NL: negating the table negates every value; swapping the nibbles
+    of every code byte swaps weights i and i+16 (page 3, encode)."""
+    W, tab = synth.gen_cb("iq4nl", 2, 256, 42)
+    w = oracle.dequant_cb("iq4nl", W, tab, 256)
+    assert np.array_equal(oracle.dequant_cb("iq4nl", W, (-tab.astype(np.int16)).clip(-127, 127).astype(np.int8), 256), -w)
+    Ws = W.copy().reshape(-1, 18)
+    Ws[:, 2:] = (Ws[:, 2:] >> 4) | (Ws[:, 2:] << 4)
+    ws = oracle.dequant_cb("iq4nl", Ws.reshape(W.shape), tab, 256).reshape(-1, 2, 16)
+    assert np.array_equal(ws[:, 0], w.reshape(-1, 2, 16)[:, 1]) and np.array_equal(ws[:, 1], w.reshape(-1, 2, 16)[:, 0])
+
+
+def test_cb_sign_parity_invariant():
+    """IQ2_XXS: every 8-weight group has an even number of negative values
+    (seven stored signs plus their parity); IQ3_S stores all 256 signs."""
+    W, tab = synth.gen_cb("iq2xxs", 16, 256, 43)
+    w = oracle.dequant_cb("iq2xxs", W, tab, 256).reshape(-1, 8)
+    assert np.all((w < 0).sum(axis=1) % 2 == 0)
+    W3, t3 = synth.gen_cb("iq3s", 16, 256, 44)
+    w3 = oracle.dequant_cb("iq3s", W3, t3, 256)
+    neg = np.unpackbits(W3.reshape(-1, 110)[:, 74:106], axis=1, bitorder="little").reshape(w3.shape)
+    assert np.array_equal(neg == 1, w3 < 0)
+
+
+@pytest.mark.parametrize("fmt", ["iq4nl", "iq4xs", "iq3s", "iq2xxs"])
+def test_cb_gemv_matches_fsum(fmt):
+    K = 512
+    W, tab = synth.gen_cb(fmt, 3, K, 45)
+    x = synth.gen_x(2, K, 46)
+    Y, A = oracle.gemv_cb(fmt, W, tab, x)
+    w = oracle.dequant_cb(fmt, W, tab, K).astype(np.float64)
+    for m in range(2):
+        for n in range(3):
+            prods = w[n] * x[m].astype(np.float64)
+            assert abs(Y[m, n] - math.fsum(prods)) <= K * 2.0 ** -53 * A[m, n]
