@@ -175,7 +175,7 @@ __device__ __forceinline__ int group_find(const Group& G, int64_t tile) {
     return i;
 }
 
-// Dynamic smem layout of gemv_kernel<F, MT, XS, RG> with `stages` stages;
+// Dynamic smem layout of gemv_kernel<F, MT, RG> with `stages` stages;
 // xh = F::kXH when x is staged with the weights, 0 when it is read from
 // global memory.
 __host__ __device__ inline Layout make_layout(bool iq3, int MT, int xh, int RG, int stages, int row_stride,
@@ -279,75 +279,6 @@ __device__ __forceinline__ void q4k_stage_x(float* xb, int64_t xstride, const fl
     }
 }
 
-// One Q4_K super-block (144 bytes at blk, smem) against MT tokens of x.
-// sx[m*8 + j] = sum of x over sub-block j for token m.
-// Nibbles become exact fp32 without any arithmetic: a nibble placed in the
-// low bits of an fp16 is the subnormal q*2^-24 (high nibbles left in place:
-// 16q*2^-24), which cvt.f32.f16 turns into an exact fp32; the powers of two
-// are folded into the sub-block scales.  PRMT pairs bytes (0,1) and (2,3) so
-// each pair meets x[kl..kl+1], x[kl+2..kl+3].
-template <int MT>
-__device__ __forceinline__ void q4k_block(const uint8_t* blk, const float* xb, int64_t xstride, const float* sx,
-                                          int M, float (&acc)[MT]) {
-    const uint4 h = *reinterpret_cast<const uint4*>(blk);
-    const float d = h2f(h.x), dmin = h2f(h.x >> 16);
-    uint32_t sc03, mn03, sc47, mn47;
-    q4k_scale_min_words(h.y, h.z, h.w, sc03, mn03, sc47, mn47);
-    float mt[MT];
-#pragma unroll
-    for (int m = 0; m < MT; ++m) mt[m] = 0.f;
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-        const float dmn = dmin * byte_f(j < 4 ? mn03 : mn47, j & 3);
-#pragma unroll
-        for (int m = 0; m < MT; ++m)
-            if (MT == 1 || m < M) mt[m] = fmaf(dmn, sx[m * 8 + j], mt[m]);
-    }
-#pragma unroll
-    for (int g = 0; g < 4; ++g) {
-        const uint32_t scw = g < 2 ? sc03 : sc47;
-        const float dl = d * byte_f(scw, (2 * g) & 3);
-        const float dh = d * byte_f(scw, (2 * g + 1) & 3) * 0.0625f;
-        f2 al[MT], ah[MT];
-#pragma unroll
-        for (int m = 0; m < MT; ++m) al[m] = ah[m] = f2{0.f, 0.f};
-#pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
-            const uint4 q = *reinterpret_cast<const uint4*>(blk + 16 + 32 * g + 16 * hh);
-            const uint32_t qv[4] = {q.x, q.y, q.z, q.w};
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const int kl = 64 * g + 16 * hh + 4 * e;  // weights kl..kl+3 (low), +32 (high)
-                const uint32_t lo4 = qv[e] & 0x0F0F0F0Fu, hi4 = qv[e] & 0xF0F0F0F0u;
-                const f2 l01 = h2_to_f2(prmt(lo4, 0u, 0x5140u));
-                const f2 l23 = h2_to_f2(prmt(lo4, 0u, 0x5342u));
-                const f2 h01 = h2_to_f2(prmt(hi4, 0u, 0x5140u));
-                const f2 h23 = h2_to_f2(prmt(hi4, 0u, 0x5342u));
-#pragma unroll
-                for (int m = 0; m < MT; ++m) {
-                    if (MT == 1 || m < M) {
-                        const float4 xl = *reinterpret_cast<const float4*>(xb + m * xstride + kl);
-                        const float4 xh = *reinterpret_cast<const float4*>(xb + m * xstride + kl + 32);
-                        ffma2(al[m], l01, f2{xl.x, xl.y});
-                        ffma2(al[m], l23, f2{xl.z, xl.w});
-                        ffma2(ah[m], h01, f2{xh.x, xh.y});
-                        ffma2(ah[m], h23, f2{xh.z, xh.w});
-                    }
-                }
-            }
-        }
-#pragma unroll
-        for (int m = 0; m < MT; ++m) {
-            if (MT == 1 || m < M) {
-                acc[m] = fmaf(dl * 16777216.f, al[m].x + al[m].y, acc[m]);     // 2^24
-                acc[m] = fmaf(dh * 16777216.f, ah[m].x + ah[m].y, acc[m]);     // dh has 1/16: 2^20 * 16
-            }
-        }
-    }
-#pragma unroll
-    for (int m = 0; m < MT; ++m) acc[m] -= mt[m];
-}
-
 // Half of one Q4_K super-block column for two rows (x pre-scaled by
 // q4k_stage_x with SCALE; half 1 of x XH floats after half 0).  Lane L of a warp takes rows L&15 and (L&15)+16 of the tile and
 // half h = L>>4 of the block (sub-blocks 4h..4h+3, weights 128h..128h+127),
@@ -436,32 +367,6 @@ __device__ __forceinline__ void q4k_half2(const uint8_t* blk, int rstride, int h
     }
 }
 
-// Load the IQ3 super-block at byte COL*98 of a 16-byte aligned row chunk in
-// smem and realign it: v[i] = block bytes F::kIdxOff + 4i.. (i < 24: the 64
-// index bytes and the eight sign/scale words, contiguous in both orders),
-// d = the fp16 at block byte F::kDOff.  Only this small step is
-// specialised per column; the decoder is shared.
-template <class F, int COL>
-__device__ __forceinline__ void iq3_load_block(const uint8_t* rowp, uint32_t (&v)[24], uint32_t& dbits) {
-    constexpr int S0 = COL * 98, A0 = S0 & ~15, OFF = S0 - A0;
-    uint32_t w[28];
-#pragma unroll
-    for (int i = 0; i < 7; ++i) {
-        const uint4 t = *reinterpret_cast<const uint4*>(rowp + A0 + 16 * i);
-        w[4 * i] = t.x;
-        w[4 * i + 1] = t.y;
-        w[4 * i + 2] = t.z;
-        w[4 * i + 3] = t.w;
-    }
-#pragma unroll
-    for (int i = 0; i < 24; ++i) {
-        const int P = OFF + F::kIdxOff + 4 * i;
-        v[i] = (P & 3) == 0 ? w[P >> 2] : __funnelshift_r(w[P >> 2], w[(P >> 2) + 1], 8 * (P & 3));
-    }
-    constexpr int PD = OFF + F::kDOff;
-    dbits = w[PD >> 2] >> (8 * (PD & 3));
-}
-
 // Sign word T of the sign field at bits 7l..7l+6 of sw (see kIQ3SignBytes);
 // lane4 = 4 * lane.
 __device__ __forceinline__ uint32_t iq3_signs(const uint8_t* sg, uint32_t sw, int l, uint32_t lane4) {
@@ -475,49 +380,6 @@ __device__ __forceinline__ uint32_t iq3_flip(uint32_t g, uint32_t T, int p) { re
 __device__ __forceinline__ uint2 iq3_grid(const uint8_t* tb, uint32_t w, int byte, uint32_t lane8) {
     const uint32_t off = prmt(w, lane8, 4u | (static_cast<uint32_t>(byte) << 4) | (5u << 8) | (5u << 12));
     return *reinterpret_cast<const uint2*>(tb + off);
-}
-
-// One IQ3 super-block (realigned: v, d) against MT tokens.
-// Each 4-weight group gathers its grid row from the lane-replicated fp16
-// table (exact magnitudes), flips signs in the fp16 domain with the masks of
-// the sign table (the implied eighth sign included), converts to fp32 and
-// FMAs.  The sub-block factor d*(0.5+code)*0.5 and the grid's 0.5 are
-// applied once per 32 weights (exact: at most 16 significant bits).
-template <int MT, class F>
-__device__ __forceinline__ void iq3_block(const uint32_t (&v)[24], uint32_t dbits, const uint8_t* tb, const uint8_t* sg,
-                                          uint32_t lane8, uint32_t lane4, const float* xb, int64_t xstride, int M,
-                                          float (&acc)[MT]) {
-    const float d = h2f(dbits);
-#pragma unroll
-    for (int ib = 0; ib < 8; ++ib) {
-        const uint32_t sw = v[16 + ib];
-        const float db = d * (static_cast<float>(sw >> 28) + 0.5f) * F::kDbScale;
-        f2 dot[MT];
-#pragma unroll
-        for (int m = 0; m < MT; ++m) dot[m] = f2{0.f, 0.f};
-#pragma unroll
-        for (int l = 0; l < 4; ++l) {
-            const uint32_t T = iq3_signs(sg, sw, l, lane4);
-#pragma unroll
-            for (int hf = 0; hf < 2; ++hf) {
-                const int PI = 8 * ib + 2 * l + hf;  // grid index byte of weights 8l+4hf..+3
-                const uint2 g = iq3_grid(tb, v[PI >> 2], PI & 3, lane8);
-                const f2 w01 = h2_to_f2(iq3_flip(g.x, T, 2 * hf));
-                const f2 w23 = h2_to_f2(iq3_flip(g.y, T, 2 * hf + 1));
-#pragma unroll
-                for (int m = 0; m < MT; ++m) {
-                    if (MT == 1 || m < M) {
-                        const float4 x = *reinterpret_cast<const float4*>(xb + m * xstride + 32 * ib + 8 * l + 4 * hf);
-                        ffma2(dot[m], w01, f2{x.x, x.y});
-                        ffma2(dot[m], w23, f2{x.z, x.w});
-                    }
-                }
-            }
-        }
-#pragma unroll
-        for (int m = 0; m < MT; ++m)
-            if (MT == 1 || m < M) acc[m] = fmaf(db, dot[m].x + dot[m].y, acc[m]);
-    }
 }
 
 // Half h of the IQ3 super-block of column COL from its 112-byte TMA box row
@@ -643,10 +505,10 @@ __device__ __forceinline__ void named_barrier_sync(int id) {
 
 // ------------------------------------------------------------ the kernel
 // Threads: RG*8 consumer warps, then one producer warp.
-// XS: x staged in shared memory with each unit (padded layout above) and
-// the two-row decode (lane L: rows L&15 and (L&15)+16, half L>>4 of each
-// block); otherwise x read from global memory and one row per lane.
-template <class F, int MT, bool XS, int RG, int MINB, int FUSE = 0>
+// x is staged in shared memory with each unit (Q4_K contiguous, IQ3 in the
+// padded layout above) and decoded two rows per lane (lane L: rows L&15 and
+// (L&15)+16, half L>>4 of each block).
+template <class F, int MT, int RG, int MINB, int FUSE = 0>
 __global__ void __launch_bounds__(RG * F::kCols * 32 + 32, MINB)
     gemv_kernel(const __grid_constant__ Group G, const __grid_constant__ TMaps T, const __grid_constant__ Fuse Fz,
                 const uint8_t* __restrict__ grid, const float* __restrict__ X, int M, int64_t K, int stages,
@@ -658,17 +520,17 @@ __global__ void __launch_bounds__(RG * F::kCols * 32 + 32, MINB)
     const int nb = static_cast<int>(K / 256);
     const int nchunks = (nb + F::kCols - 1) / F::kCols;
     const int64_t ntiles = G.tile0[G.count];
-    constexpr int XH = XS ? F::kXH : 0;  // floats from half 0 to half 1 of a staged x column
+    constexpr int XH = F::kXH;  // floats from half 0 to half 1 of a staged x column
     const Layout L = make_layout(F::kIQ3, MT, XH, RG, stages, F::kRowStride, F::kCols, FUSE);
-    static_assert(FUSE == 0 || (XS && !F::kIQ3), "fused prologues run on the staged Q4_K path");
+    static_assert(FUSE == 0 || !F::kIQ3, "fused prologues run on the Q4_K path");
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.full);
     uint64_t* empty = reinterpret_cast<uint64_t*>(smem + L.empty);
     float* sxw = reinterpret_cast<float*>(smem + L.sx);
     float* red = reinterpret_cast<float*>(smem + L.red);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     static_assert(F::kTMA, "weights arrive through the format's tensor map");
-    static_assert(!XS || F::kCols == 8, "one x box holds 8 columns");
-    static_assert(!XS || F::kIQ3 || RG == 1, "in-place x scaling needs one warp per column");
+    static_assert(F::kCols == 8, "one x box holds 8 columns");
+    static_assert(F::kIQ3 || RG == 1, "in-place x scaling needs one warp per column");
 
     // Programmatic dependent launch: let the next kernel in the stream get
     // scheduled now.  Without the weight-prefetch flag, wait for the previous
@@ -771,14 +633,14 @@ __global__ void __launch_bounds__(RG * F::kCols * 32 + 32, MINB)
                 const uint32_t aux = FUSE == 0 ? 0u : (kAuxTokens ? M : 1) * kc * 1024;
                 if (lane == 0)
                     mbar_arrive_expect_tx(&full[p.s],
-                                          kc * kBox + (XS ? M * (kXBox ? kXBoxBytes : kc * 1024) : 0) + aux);
+                                          kc * kBox + M * (kXBox ? kXBoxBytes : kc * 1024) + aux);
                 __syncwarp();
             }
             if (do_w && lane == 0)
                 for (int b = 0; b < kc; ++b)
                     tma_load_2d(st + b * kBox, &T.m[p.gi], ((p.c * F::kCols + b) * F::kBytes) & ~15,
                                 static_cast<int>(p.row0), &full[p.s], pol_w);
-            if (XS && do_x && lane < M) {
+            if (do_x && lane < M) {
                 if constexpr (kXBox)
                     tma_load_2d(st + L.xoff + lane * kXBoxBytes, &T.xm, 0,
                                 static_cast<int>((lane * K) / 128 + p.c * (2 * F::kCols)), &full[p.s], pol_x);
@@ -830,13 +692,11 @@ __global__ void __launch_bounds__(RG * F::kCols * 32 + 32, MINB)
     // ---------------- consumer warps
     if (prefetch) grid_dependency_wait();  // x and Y belong to the dependency chain
     const int rg = warp / F::kCols, cw = warp % F::kCols;
-    // XS: two rows per lane (acc2[j]: row (lane&15) + 16j, half lane>>4)
-    constexpr bool kHalf2 = XS;
-    float acc[MT];
+    // two rows per lane (acc2[j]: row (lane&15) + 16j, half lane>>4)
     float acc2[2][MT];
     float ss[MT];  // RMSNorm prologue: this lane's part of sum(x^2) over the tile's units
 #pragma unroll
-    for (int m = 0; m < MT; ++m) acc[m] = acc2[0][m] = acc2[1][m] = ss[m] = 0.f;
+    for (int m = 0; m < MT; ++m) acc2[0][m] = acc2[1][m] = ss[m] = 0.f;
     const uint32_t lane8 = static_cast<uint32_t>(lane) * 8u, lane4 = static_cast<uint32_t>(lane) * 4u;
     int64_t tile_count = 0;
 
@@ -856,28 +716,20 @@ __global__ void __launch_bounds__(RG * F::kCols * 32 + 32, MINB)
     for (int64_t u = 0; u < U; ++u) {
         const int kc = min(F::kCols, nb - c * F::kCols);
         const uint8_t* st = smem + L.stage0 + s * L.stage_bytes;
-        const int r = rg * kRows + lane;  // row within the tile
         mbar_wait_bounded(&full[s], phase, status);
 
         if (cw < kc) {
-            const int64_t b = static_cast<int64_t>(c) * F::kCols + cw;  // super-block column
-            const float* xb = XS ? reinterpret_cast<const float*>(st + L.xoff) + cw * 2 * XH : X + b * 256;
-            const int64_t xstride = XS ? F::kCols * 2 * XH : K;
+            const float* xb = reinterpret_cast<const float*>(st + L.xoff) + cw * 2 * XH;
+            const int64_t xstride = F::kCols * 2 * XH;
             if constexpr (!F::kIQ3) {
                 float* sxp = sxw + warp * MT * 8;
                 const float* ab = reinterpret_cast<const float*>(st + L.aoff) + cw * 256;
-                q4k_stage_x<MT, XS, XS ? XH : 128, FUSE>(const_cast<float*>(xb), xstride, ab, F::kCols * 256, sxp, ss,
-                                                         M, lane);
+                q4k_stage_x<MT, true, XH, FUSE>(const_cast<float*>(xb), xstride, ab, F::kCols * 256, sxp, ss, M, lane);
                 __syncwarp();
-                if constexpr (kHalf2) {
-                    const uint8_t* blk = st + cw * (kTileRows * F::kBytes) + (lane & 15) * F::kBytes;
-                    q4k_half2<MT, XH>(blk, 16 * F::kBytes, lane >> 4, xb, xstride, sxp, M, acc2);
-                    fence_proxy_async_smem();  // x was written: order it before the slot's next copy
-                } else {
-                    const uint8_t* blk = st + cw * (kTileRows * F::kBytes) + r * F::kBytes;
-                    if (r < rows) q4k_block<MT>(blk, xb, xstride, sxp, M, acc);
-                }
-            } else if constexpr (kHalf2) {
+                const uint8_t* blk = st + cw * (kTileRows * F::kBytes) + (lane & 15) * F::kBytes;
+                q4k_half2<MT, XH>(blk, 16 * F::kBytes, lane >> 4, xb, xstride, sxp, M, acc2);
+                fence_proxy_async_smem();  // x was written: order it before the slot's next copy
+            } else {
                 // two rows per lane, half a block each (TMA layout): rows
                 // rg*32 + (lane&15) and +16, half lane>>4
                 const int hl = lane >> 4;
@@ -899,26 +751,6 @@ __global__ void __launch_bounds__(RG * F::kCols * 32 + 32, MINB)
                 }
                 const uint8_t* tb = smem + L.table;
                 iq3_half2<MT, F>(vi, vs, dbits, tb, tb + kIQ3GridBytes, lane8, lane4, xb + XH * hl, xstride, M, acc2);
-            } else {
-                if (r < rows) {
-                    // block cw's box row, shifted so that rowp + (98*cw & ~15)
-                    // is the box row
-                    const uint8_t* rowp =
-                        st + cw * (kTileRows * F::kBoxBytes) + r * F::kBoxBytes - ((cw * F::kBytes) & ~15);
-                    const uint8_t* tb = smem + L.table;
-                    uint32_t v[24], dbits;
-                    switch (cw) {
-                        case 0: iq3_load_block<F, 0>(rowp, v, dbits); break;
-                        case 1: iq3_load_block<F, 1>(rowp, v, dbits); break;
-                        case 2: iq3_load_block<F, 2>(rowp, v, dbits); break;
-                        case 3: iq3_load_block<F, 3>(rowp, v, dbits); break;
-                        case 4: iq3_load_block<F, 4>(rowp, v, dbits); break;
-                        case 5: iq3_load_block<F, 5>(rowp, v, dbits); break;
-                        case 6: iq3_load_block<F, 6>(rowp, v, dbits); break;
-                        default: iq3_load_block<F, 7>(rowp, v, dbits); break;
-                    }
-                    iq3_block<MT, F>(v, dbits, tb, tb + kIQ3GridBytes, lane8, lane4, xb, xstride, M, acc);
-                }
             }
         }
         __syncwarp();
@@ -929,16 +761,11 @@ __global__ void __launch_bounds__(RG * F::kCols * 32 + 32, MINB)
             float* rb = red + (tile_count & 1) * (kWarps * MT * kRows);
 #pragma unroll
             for (int m = 0; m < MT; ++m) {
-                if constexpr (kHalf2) {
-                    // lanes L and L^16 hold the two halves of rows L&15 and (L&15)+16
-                    const float s0 = acc2[0][m] + __shfl_xor_sync(0xffffffffu, acc2[0][m], 16);
-                    const float s1 = acc2[1][m] + __shfl_xor_sync(0xffffffffu, acc2[1][m], 16);
-                    rb[(warp * MT + m) * kRows + lane] = lane < 16 ? s0 : s1;
-                    acc2[0][m] = acc2[1][m] = 0.f;
-                } else {
-                    rb[(warp * MT + m) * kRows + lane] = acc[m];
-                    acc[m] = 0.f;
-                }
+                // lanes L and L^16 hold the two halves of rows L&15 and (L&15)+16
+                const float s0 = acc2[0][m] + __shfl_xor_sync(0xffffffffu, acc2[0][m], 16);
+                const float s1 = acc2[1][m] + __shfl_xor_sync(0xffffffffu, acc2[1][m], 16);
+                rb[(warp * MT + m) * kRows + lane] = lane < 16 ? s0 : s1;
+                acc2[0][m] = acc2[1][m] = 0.f;
             }
             // RMSNorm prologue: each warp's sum of x^2 (its columns, all of
             // the tile's chunks) per token

@@ -25,21 +25,21 @@ inline int sm_count(int dev) {
     return cache[dev];
 }
 
-// Launch gemv_kernel<F, MT, XS, RG, MINB> over `count` matrices that
+// Launch gemv_kernel<F, MT, RG, MINB, FUSE> over `count` matrices that
 // share X (token offset m0 already applied to X; Y[i] + m0*N[i] here): MINB
 // CTAs per SM, as many pipeline stages as fit in the per-CTA share of shared
 // memory.
-template <class F, int MT, bool XS, int RG, int MINB, int FUSE = 0>
+template <class F, int MT, int RG, int MINB, int FUSE = 0>
 int launch_gemv(const uint8_t* const* W, float* const* Y, const int64_t* N, int count, int m0, const uint8_t* grid,
                 const float* X, int M, int64_t K, cudaStream_t s, unsigned* status, int dev, unsigned flags,
                 int csize = 1, const Fuse* fz = nullptr) {
     static bool attr_done[64];
     const int budget = std::min(kSmemPerCTA, kSmemPerSM / MINB - kSmemReserve);
-    const Layout L1 = make_layout(F::kIQ3, MT, XS ? F::kXH : 0, RG, 1, F::kRowStride, F::kCols, FUSE);
+    const Layout L1 = make_layout(F::kIQ3, MT, F::kXH, RG, 1, F::kRowStride, F::kCols, FUSE);
     const int stages = std::min(kMaxStages, (budget - L1.stage0) / L1.stage_bytes);
     if (stages < 2) return QG_EINVAL;
-    const Layout L = make_layout(F::kIQ3, MT, XS ? F::kXH : 0, RG, stages, F::kRowStride, F::kCols, FUSE);
-    auto kern = gemv_kernel<F, MT, XS, RG, MINB, FUSE>;
+    const Layout L = make_layout(F::kIQ3, MT, F::kXH, RG, stages, F::kRowStride, F::kCols, FUSE);
+    auto kern = gemv_kernel<F, MT, RG, MINB, FUSE>;
     if (!attr_done[dev]) {
         if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L.total) != cudaSuccess)
             return QG_ECUDA;
@@ -70,7 +70,7 @@ int launch_gemv(const uint8_t* const* W, float* const* Y, const int64_t* N, int 
             if (!encode_byte_rows(&T.m[i], W[i], pitch, static_cast<uint64_t>(N[i]), F::kBoxBytes, RG * kRows))
                 return QG_ECUDA;
     }
-    if (XS && F::kXH == kXHalf && !encode_x_halves(&T.xm, X, static_cast<uint64_t>(M) * static_cast<uint64_t>(K / 128))) return QG_ECUDA;
+    if (F::kXH == kXHalf && !encode_x_halves(&T.xm, X, static_cast<uint64_t>(M) * static_cast<uint64_t>(K / 128))) return QG_ECUDA;
     const int64_t ntiles = G.tile0[count];
     const int sms = sm_count(dev);
     if (sms <= 0) return QG_ECUDA;

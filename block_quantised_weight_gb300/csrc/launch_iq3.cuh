@@ -68,29 +68,29 @@ int launch_group_iq3_t(const uint8_t* const* W, float* const* Y, const int64_t* 
                        const float* X, int M, int64_t K, cudaStream_t s, unsigned* status, unsigned flags) {
     const int dev = current_device();
     if (dev < 0) return QG_ECUDA;
-    const bool aligned = (K / 256) % 8 == 0;
-    for (int m0 = 0; m0 < M; m0 += 8) {
-        const int mg = std::min(8, M - m0);
-        const float* Xg = X + static_cast<int64_t>(m0) * K;
-        int rc = QG_OK;
-        if (!aligned) {
-            const int sms = sm_count(dev);
-            if (sms <= 0) return QG_ECUDA;
-            for (int i = 0; i < count && rc == QG_OK; ++i) {
+    if ((K / 256) % 8 != 0) {
+        // rows not 16-byte aligned: the byte-addressed kernel, up to 8 tokens per pass
+        const int sms = sm_count(dev);
+        if (sms <= 0) return QG_ECUDA;
+        for (int m0 = 0; m0 < M; m0 += 8) {
+            const int mg = std::min(8, M - m0);
+            for (int i = 0; i < count; ++i) {
                 const int64_t blocks = std::min<int64_t>((N[i] + 7) / 8, static_cast<int64_t>(sms) * 8);
-                gemv_iq3_bytes_kernel<F><<<static_cast<int>(blocks), 256, 0, s>>>(W[i], grid, Xg, Y[i] + m0 * N[i], mg,
-                                                                                N[i], K);
-                rc = cudaGetLastError() == cudaSuccess ? QG_OK : QG_ECUDA;
+                gemv_iq3_bytes_kernel<F><<<static_cast<int>(blocks), 256, 0, s>>>(
+                    W[i], grid, X + static_cast<int64_t>(m0) * K, Y[i] + m0 * N[i], mg, N[i], K);
+                if (cudaGetLastError() != cudaSuccess) return QG_ECUDA;
             }
-        } else if (mg == 1) {
-            rc = launch_gemv<F, 1, true, 2, 1>(W, Y, N, count, m0, grid, Xg, mg, K, s, status, dev, flags);
-        } else if (mg == 2) {
-            rc = launch_gemv<F, 2, true, 1, 1>(W, Y, N, count, m0, grid, Xg, mg, K, s, status, dev, flags);
-        } else if (mg <= 4) {
-            rc = launch_gemv<F, 4, false, 1, 1>(W, Y, N, count, m0, grid, Xg, mg, K, s, status, dev, flags);
-        } else {
-            rc = launch_gemv<F, 8, false, 1, 1>(W, Y, N, count, m0, grid, Xg, mg, K, s, status, dev, flags);
         }
+        return QG_OK;
+    }
+    // groups of at most 2 tokens (the two-row decode with x staged): beyond
+    // two tokens its registers run out, and repeated 2-token passes over W
+    // beat a wider group
+    for (int m0 = 0; m0 < M; m0 += 2) {
+        const int mg = std::min(2, M - m0);
+        const float* Xg = X + static_cast<int64_t>(m0) * K;
+        const int rc = mg == 1 ? launch_gemv<F, 1, 2, 1>(W, Y, N, count, m0, grid, Xg, mg, K, s, status, dev, flags)
+                               : launch_gemv<F, 2, 1, 1>(W, Y, N, count, m0, grid, Xg, mg, K, s, status, dev, flags);
         if (rc != QG_OK) return rc;
     }
     return QG_OK;

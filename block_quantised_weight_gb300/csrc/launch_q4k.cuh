@@ -5,8 +5,10 @@
 
 namespace qg {
 
-// count matrices sharing X; M is split into groups of at most 8 tokens, each
-// group streaming W once.  FUSE != 0 (a prologue on x) needs M <= 4: the
+// count matrices sharing X; M is split into groups of at most 4 tokens, each
+// group streaming W once (an 8-token group needs more registers than the
+// two-row decode can keep: two 4-token passes over W are several times
+// faster than one 8-token pass).  FUSE != 0 (a prologue on x) needs M <= 4: the
 // staged-x kernels apply it.  fz may carry residuals with any FUSE.
 template <int FUSE>
 int launch_group_q4k_t(const uint8_t* const* W, float* const* Y, const int64_t* N, int count, const float* X, int M,
@@ -24,30 +26,25 @@ int launch_group_q4k_t(const uint8_t* const* W, float* const* Y, const int64_t* 
     // chunk gets its own CTA, the chunks of a tile forming one cluster.
     const int64_t nchunks = (K / 256 + kCols - 1) / kCols;
     const int csize = (nchunks > 1 && nchunks <= kMaxCluster && tiles * nchunks <= 2 * sms) ? static_cast<int>(nchunks) : 1;
-    for (int m0 = 0; m0 < M; m0 += 8) {
-        const int mg = std::min(8, M - m0);
+    for (int m0 = 0; m0 < M; m0 += 4) {
+        const int mg = std::min(4, M - m0);
         const float* Xg = X + static_cast<int64_t>(m0) * K;
         int rc;
         if (mg == 1 && csize > 1)
-            rc = launch_gemv<FmtQ4KT, 1, true, 1, 2, FUSE>(W, Y, N, count, m0, nullptr, Xg, mg, K, s, status, dev,
+            rc = launch_gemv<FmtQ4KT, 1, 1, 2, FUSE>(W, Y, N, count, m0, nullptr, Xg, mg, K, s, status, dev,
                                                            flags, csize, fz);
         else if (mg == 1 && few_tiles)  // one CTA per SM: a deeper ring prefetches every unit of a tile
-            rc = launch_gemv<FmtQ4KT, 1, true, 1, 1, FUSE>(W, Y, N, count, m0, nullptr, Xg, mg, K, s, status, dev,
+            rc = launch_gemv<FmtQ4KT, 1, 1, 1, FUSE>(W, Y, N, count, m0, nullptr, Xg, mg, K, s, status, dev,
                                                            flags, 1, fz);
         else if (mg == 1)
-            rc = launch_gemv<FmtQ4KT, 1, true, 1, 2, FUSE>(W, Y, N, count, m0, nullptr, Xg, mg, K, s, status, dev,
+            rc = launch_gemv<FmtQ4KT, 1, 1, 2, FUSE>(W, Y, N, count, m0, nullptr, Xg, mg, K, s, status, dev,
                                                            flags, 1, fz);
         else if (mg == 2)  // prologue operands double a stage's x area: one CTA per SM then
-            rc = launch_gemv<FmtQ4KT, 2, true, 1, FUSE == 0 ? 2 : 1, FUSE>(W, Y, N, count, m0, nullptr, Xg, mg, K, s,
+            rc = launch_gemv<FmtQ4KT, 2, 1, FUSE == 0 ? 2 : 1, FUSE>(W, Y, N, count, m0, nullptr, Xg, mg, K, s,
                                                                            status, dev, flags, 1, fz);
-        else if (mg <= 4)
-            rc = launch_gemv<FmtQ4KT, 4, true, 1, 1, FUSE>(W, Y, N, count, m0, nullptr, Xg, mg, K, s, status, dev,
-                                                           flags, 1, fz);
-        else if constexpr (FUSE == 0)
-            rc = launch_gemv<FmtQ4KT, 8, false, 1, 1>(W, Y, N, count, m0, nullptr, Xg, mg, K, s, status, dev, flags, 1,
-                                                      fz);
         else
-            rc = QG_EINVAL;
+            rc = launch_gemv<FmtQ4KT, 4, 1, 1, FUSE>(W, Y, N, count, m0, nullptr, Xg, mg, K, s, status, dev,
+                                                           flags, 1, fz);
         if (rc != QG_OK) return rc;
     }
     return QG_OK;

@@ -79,11 +79,11 @@ extern "C" {
  * model_forward's matmul (operation).
  * W: N*K/256*144 bytes.  X: M*K floats.  Y: M*N floats (output).
  * Numerics: |Y - exact| <= 1e-5 * sum_k |w*x| per element (fp32 FMA,
- * sub-block-factored sums).  M > 8 is processed in groups of 8 tokens, each
- * group streaming W once.  Range: for groups of up to 4 tokens the kernel
- * scales x by powers of two up to 2^88 in shared memory, so every |x| must
- * be below 2^40 (larger values give inf/NaN in Y); the same holds for
- * qgemv_q4k_group and qgemv_q4k_pass. */
+ * sub-block-factored sums).  M > 4 is processed in groups of 4 tokens, each
+ * group streaming W once.  Range: the kernel scales x by powers of two up to
+ * 2^88 in shared memory, so every |x| must be below 2^40 (larger values give
+ * inf/NaN in Y); the same holds for qgemv_q4k_group, qgemv_q4k_fused and
+ * qgemv_q4k_pass. */
 QG_API int qgemv_q4k(const uint8_t* W, const float* X, float* Y, int M, int64_t N, int64_t K, cudaStream_t stream);
 
 /* qgemv_q4k with launch flags (0 or QG_PREFETCH_WEIGHTS); other flag bits:
@@ -96,8 +96,9 @@ QG_API int qgemv_q4k_ex(const uint8_t* W, const float* X, float* Y, int M, int64
  * model_forward's matmul (operation).
  * grid: 256*4 bytes, the codebook in the published doubled units (the kernel
  * applies the 0.5 of page 4's grid()).  Other arguments as qgemv_q4k.
- * K/256 a multiple of 8 takes the bulk-copy path; other K take a slower
- * byte-addressed path with identical results. */
+ * K/256 a multiple of 8 takes the tensor-map path, M > 2 in groups of 2
+ * tokens, each group streaming W once; other K take a slower byte-addressed
+ * path (groups of 8 tokens) with the same numerics. */
 QG_API int qgemv_iq3(const uint8_t* W, const uint8_t* grid, const float* X, float* Y, int M, int64_t N, int64_t K,
               cudaStream_t stream);
 
