@@ -50,6 +50,10 @@ def workload_spec(name: str, M: int):
         "q4k_c0": ("q4k", 2048, 2048), "iq3_c2": ("iq3", 4096, 14336), "q4k_c3": ("q4k", 4096, 11008),
         "q4k_c4a": ("q4k", 8192, 28672), "q4k_c4b": ("q4k", 28672, 8192),
         "iq3_c4a": ("iq3", 8192, 28672), "iq3_c4b": ("iq3", 28672, 8192),
+        # page 3's formats at the IQ3 config's shape (not headline configs)
+        "iq3xxs_c2": ("iq3xxs", 4096, 14336), "iq4nl_c2": ("iq4nl", 4096, 14336),
+        "iq4xs_c2": ("iq4xs", 4096, 14336), "iq3s_c2": ("iq3s", 4096, 14336),
+        "iq2xxs_c2": ("iq2xxs", 4096, 14336),
     }
     fmt, K, N = table[name]
     return [(fmt, K, N)], f"{fmt.upper()} GEMV K={K} N={N} M={M}", M
@@ -68,8 +72,13 @@ def pass_groups(name, n, single):
     return groups
 
 
+UNIT_BYTES = {"q4k": Q4K_BYTES, "iq3": IQ3_BYTES, "iq3xxs": IQ3_BYTES, "iq4nl": 144, "iq4xs": 136, "iq3s": 110,
+              "iq2xxs": 66}
+CB_FORMATS = ("iq4nl", "iq4xs", "iq3s", "iq2xxs")
+
+
 def weight_bytes(fmt, K, N):
-    return N * (K // 256) * (Q4K_BYTES if fmt == "q4k" else IQ3_BYTES)
+    return N * (K // 256) * UNIT_BYTES[fmt]
 
 
 def gen_mats(name, mats, M):
@@ -88,8 +97,13 @@ def gen_mats(name, mats, M):
     rng = np.random.default_rng(seed)
     if fmt == "q4k":
         W, grid = synth.gen_q4k(N, K, rng), None
-    else:
+    elif fmt in CB_FORMATS:
+        W, grid = synth.gen_cb(fmt, N, K, rng)
+    else:  # IQ3 fields; the page-3 order is the same bytes with d moved first
         W, grid = synth.gen_iq3(N, K, rng)
+        if fmt == "iq3xxs":
+            b = W.reshape(N, K // 256, 98)
+            W = np.concatenate([b[:, :, 96:98], b[:, :, 0:96]], axis=2).reshape(N, -1)
     x = synth.gen_x(M, K, rng)
     out.append((fmt, K, N, W, grid, x))
     return out
@@ -323,8 +337,15 @@ def run_ours(args, rank, world, local_rank):
                 lst.append((lib.qgemm_q4k_batched, (Wp[0], xp, Yp[0], M, Ns[0], K), wb, algo, label))
             elif fmt == "q4k":
                 lst.append((lib.qgemv_q4k_ex, (Wp[0], xp, Yp[0], M, Ns[0], K, fl), wb, algo, label))
-            else:
+            elif fmt == "iq3" and M >= 16:
+                lst.append((lib.qgemm_iq3_batched, (Wp[0], gd.data_ptr(), xp, Yp[0], M, Ns[0], K), wb, algo, label))
+            elif fmt == "iq3":
                 lst.append((lib.qgemv_iq3_ex, (Wp[0], gd.data_ptr(), xp, Yp[0], M, Ns[0], K, fl), wb, algo, label))
+            elif fmt == "iq3xxs":
+                lst.append((lib.qgemv_iq3xxs_ex, (Wp[0], gd.data_ptr(), xp, Yp[0], M, Ns[0], K, fl), wb, algo, label))
+            else:
+                lst.append((lib.qgemv_codebook, (qgemv.QG_CB[fmt], Wp[0], gd.data_ptr(), xp, Yp[0], M, Ns[0], K), wb,
+                            algo, label))
             xo += M * K
         if args.mode == "pass" and args.workload == "tinyllama":
             # the whole pass as one persistent launch: stage i reads its x only
@@ -484,10 +505,15 @@ def run_ours(args, rank, world, local_rank):
     elif fused:
         kname = "qgemv_q4k_fused gemv_kernel<FmtQ4KT, FUSE>"
     elif mats[0][0] == "q4k":
-        kname = ("qgemm_q4k_batched gemm_q4k_tc_kernel (tcgen05)" if M >= 16 else
+        kname = ("qgemm_q4k_batched gemm_tc_kernel<Q4_K> (tcgen05)" if M >= 16 else
                  "qgemv_q4k gemv_kernel<FmtQ4KT>")
+    elif mats[0][0] == "iq3":
+        kname = ("qgemm_iq3_batched gemm_tc_kernel<IQ3> (tcgen05)" if M >= 16 else
+                 "qgemv_iq3 gemv_kernel<FmtIQ3T>")
+    elif mats[0][0] == "iq3xxs":
+        kname = "qgemv_iq3xxs gemv_kernel<FmtIQ3XXST>"
     else:
-        kname = "qgemv_iq3 gemv_kernel<FmtIQ3T>"
+        kname = f"qgemv_codebook gemv_cb_kernel<{mats[0][0].upper()}>"
     roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
             "frac": round(achieved / peak, 4), "traffic": profiled_traffic(args.workload, M),
             "peak_kind": f"of {peak_kind}", "kernel": kname, "launches_timed": n_launch,
@@ -558,8 +584,12 @@ def oracle_sample_rate(workload, M, budget_s, threads=None):
             t0 = time.perf_counter()
             if fmt == "q4k":
                 oracle.gemv_q4k(W[:nr], x, rows=rows, nthreads=nt)
-            else:
+            elif fmt == "iq3":
                 oracle.gemv_iq3(W[:nr], grid, x, rows=rows, nthreads=nt)
+            elif fmt == "iq3xxs":
+                oracle.gemv_iq3xxs(W[:nr], grid, x, rows=rows, nthreads=nt)
+            else:
+                oracle.gemv_cb(fmt, W[:nr], grid, x, rows=rows, nthreads=nt)
             t_used += time.perf_counter() - t0
             done_bytes += weight_bytes(fmt, K, nr)
             n += 1

@@ -70,9 +70,9 @@ constexpr int kOp0 = kRaw0 + 2 * kRawStage;         // 103424
 // lane L reading copy L & 7, so the 8 lanes of a quarter warp gather from 8
 // distinct bank groups whatever their rows (32 KB).
 constexpr int kGrid0 = kOp0 + 2 * kOpStage;
-constexpr int kSign0 = kGrid0 + 32768;              // IQ3: sign-mask word per 7-bit sign field (512 B)
+constexpr int kSign0 = kGrid0 + 32768;              // IQ3: sign-mask words, 8 copies (entry s7 of copy c at 8*s7 + c: 4 KB)
 constexpr int kSmemTotal = kGrid0;                  // 185344 (Q4_K)
-constexpr int kSmemTotalIQ3 = kSign0 + 512;
+constexpr int kSmemTotalIQ3 = kSign0 + 4096;
 constexpr int kTmemCols = 32;
 constexpr uint32_t kSBO = 16 * 128;                 // row-group stride in an operand stage
 constexpr uint32_t kLBO = 128;                      // k-chunk stride
@@ -211,35 +211,31 @@ __device__ __forceinline__ void dequant_half(const uint8_t* blk, uint8_t* opA, i
 }
 
 // IQ3: thread t, half `half` (sub-blocks 4*half .. +3) of tile row t, the
-// block starting `off` bytes into the box row.  Fields are read as 32-bit
-// words at the aligned address below and funnel-shifted into place.  Signs
-// are applied to packed bf16 pairs: sgn[s7] holds the eight signs of a
-// 7-bit field (the eighth its parity) with sign 2p at bit 15-p and sign
-// 2p+1 at bit 31-p, so (T << p) & 0x80008000 flips pair p.
-__device__ __forceinline__ void dequant_half_iq3(const uint8_t* row, int off, const float4* grid4,
-                                                 const uint32_t* sgn, uint8_t* opA, int t, int half) {
-    const uint8_t* base = row + (off & ~3);
-    const uint32_t sh = 8u * static_cast<uint32_t>(off & 3);
-    auto word = [&](int b) {  // block bytes b..b+3 (b a multiple of 4)
-        const uint32_t lo = *reinterpret_cast<const uint32_t*>(base + b);
-        const uint32_t hi = *reinterpret_cast<const uint32_t*>(base + b + 4);
-        return __funnelshift_r(lo, hi, sh);
-    };
-    const float d = h2f(word(96));
+// block of column COL starting (98*COL) mod 16 bytes into its 112-byte box
+// row: the fields come in as 16-byte loads (rows 112 = 7 x 16 bytes apart,
+// so 8 consecutive threads hit 8 distinct bank groups) realigned in
+// registers (iq3_load_half).  Signs are applied to packed bf16 pairs:
+// sgn[s7] holds the eight signs of a 7-bit field (the eighth its parity)
+// with sign 2p at bit 15-p and sign 2p+1 at bit 31-p, so (T << p) &
+// 0x80008000 flips pair p.
+template <int COL>
+__device__ __forceinline__ void dequant_half_iq3(const uint8_t* boxrow, const float4* grid4, const uint32_t* sgn,
+                                                 uint8_t* opA, int t, int half) {
+    uint32_t vi[8], vs[4], dbits;
+    iq3_load_half<FmtIQ3T, COL>(boxrow, half, vi, vs, dbits);
+    const float d = h2f(dbits);
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-        const int ib = 4 * half + j;
-        const uint32_t sw = word(64 + 4 * ib);
+        const uint32_t sw = vs[j];
         const float dbh = d * (static_cast<float>(sw >> 28) + 0.5f) * 0.25f;  // 0.5 * grid's 0.5
-        const uint32_t iw0 = word(8 * ib), iw1 = word(8 * ib + 4);
 #pragma unroll
         for (int l = 0; l < 4; ++l) {
-            const uint32_t T = sgn[(sw >> (7 * l)) & 0x7Fu];
+            const uint32_t T = sgn[8 * ((sw >> (7 * l)) & 0x7Fu) + (t & 7)];
             uint32_t packed[4];
 #pragma unroll
             for (int hf = 0; hf < 2; ++hf) {
-                const int pi = 2 * l + hf;  // index byte within the sub-block
-                const uint32_t idx = ((pi < 4 ? iw0 : iw1) >> (8 * (pi & 3))) & 0xFFu;
+                const int pi = 8 * j + 2 * l + hf;  // index byte within the half
+                const uint32_t idx = (vi[pi >> 2] >> (8 * (pi & 3))) & 0xFFu;
                 const float4 g = grid4[8 * idx + (t & 7)];
                 // |w| = grid * dbh exactly, rounded once to bf16; the sign bits of
                 // pairs 2hf and 2hf+1 come from T
@@ -294,8 +290,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         // signs of each 7-bit field: the seven stored ones and their parity
         // (page 4, decode), sign k at bit 15 - k/2 (k even) or 31 - k/2 (odd)
         uint32_t* sg = reinterpret_cast<uint32_t*>(smem + kSign0);
-        for (int i = threadIdx.x; i < 128; i += kThreads) {
-            const uint32_t s8 = static_cast<uint32_t>(i) | ((__popc(i) & 1u) << 7);
+        for (int i = threadIdx.x; i < 8 * 128; i += kThreads) {  // i = 8 * s7 + copy
+            const uint32_t s7 = static_cast<uint32_t>(i) >> 3;
+            const uint32_t s8 = s7 | ((__popc(s7) & 1u) << 7);
             uint32_t t = 0;
             for (int pr = 0; pr < 4; ++pr)
                 t |= (((s8 >> (2 * pr)) & 1u) << (15 - pr)) | (((s8 >> (2 * pr + 1)) & 1u) << (31 - pr));
@@ -387,8 +384,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_wait_bounded(&raw_full[s], static_cast<uint32_t>((i >> 1) & 1), status);
             if (i >= 1) mbar_wait_bounded(&op_empty[half], static_cast<uint32_t>((i - 1) & 1), status);
             if constexpr (IQ3)  // rows past N: TMA zero fill, unused
-                dequant_half_iq3(raw + t * kIQ3Box, (kb * 98) & 15, reinterpret_cast<const float4*>(smem + kGrid0),
-                                 reinterpret_cast<const uint32_t*>(smem + kSign0), opA, t, half);
+                switch (kb & 7) {  // the block's offset in its box: (98 * kb) mod 16
+#define QG_TC_IQ3(C)                                                                                          \
+    case C:                                                                                                  \
+        dequant_half_iq3<C>(raw + t * kIQ3Box, reinterpret_cast<const float4*>(smem + kGrid0),             \
+                            reinterpret_cast<const uint32_t*>(smem + kSign0), opA, t, half);                 \
+        break;
+                    QG_TC_IQ3(0) QG_TC_IQ3(1) QG_TC_IQ3(2) QG_TC_IQ3(3)
+                    QG_TC_IQ3(4) QG_TC_IQ3(5) QG_TC_IQ3(6) QG_TC_IQ3(7)
+#undef QG_TC_IQ3
+                }
             else
                 dequant_half(raw + t * kBlockBytes, opA, t, half);
             for (int c = t; c < M * 16; c += 128) {
