@@ -457,6 +457,44 @@ def run_ours(args, rank, world, local_rank):
     if status != 0:
         raise RuntimeError(f"device status {status}")
 
+    # dependent-launch floor of the step: the same chain of launches (same
+    # count, grids and x lengths) doing no weight work (qg_test_chain_step)
+    floor = None
+    if args.workload == "tinyllama" and args.mode in ("group", "fused"):
+        sms = torch.cuda.get_device_properties(dev).multi_processor_count
+        ybuf = torch.empty(2 * sms * 32 + 64, dtype=torch.float32, device=dev)
+        chain = []
+        for grp in groups:
+            K = host[grp[0]][1]
+            tiles = sum((host[i][2] + 31) // 32 for i in grp)
+            chain.append((K, min(tiles, 2 * sms)))
+        xs_len = max(K for K, _ in chain)
+        xf = torch.zeros(xs_len, dtype=torch.float32, device=dev)
+        gf = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gf, stream=stream):
+            cap = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+            for K, gx in chain:
+                rc = lib.qg_test_chain_step(xf.data_ptr(), ybuf.data_ptr(), K, gx, qgemv.QG_PREFETCH_WEIGHTS, cap)
+                if rc != 0:
+                    raise RuntimeError(f"chain step failed: {rc}")
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                gf.replay()
+        torch.cuda.synchronize(dev)
+        f0 = torch.cuda.Event(enable_timing=True)
+        f1 = torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            f0.record(stream)
+            for _ in range(args.steps):
+                gf.replay()
+            f1.record(stream)
+        torch.cuda.synchronize(dev)
+        floor_ms = f0.elapsed_time(f1) / args.steps
+        floor = {"ms_per_pass": round(floor_ms, 4), "launches": len(chain),
+                 "note": "the same chain of programmatic dependent launches (grids min(tiles, 2 x SMs), each "
+                         "reading its x) doing no weight work: the part of the step time that streaming and "
+                         "decoding inside this launch chain cannot remove"}
+
     # e2e: host x in, host y out, every step, through the same C-ABI calls
     xs_pin = torch.from_numpy(xs_host).pin_memory()
     ys_pin = torch.empty(ys_len, dtype=torch.float32).pin_memory()
@@ -490,6 +528,8 @@ def run_ours(args, rank, world, local_rank):
     value = world * step_wbytes * n_pass / (ms_total * 1e-3) / 1e9
     e2e_value = world * step_wbytes * n_pass / (ms_e2e * 1e-3) / 1e9
 
+    if floor:
+        floor["above_floor_ms_per_pass"] = round(ms_step - floor["ms_per_pass"], 4)
     peak, peak_kind = measured_peaks()
     # Dominant kernel (the only one in the timed region): algorithmic bytes per
     # launch / average launch duration, the duration taken from the timed
@@ -559,6 +599,7 @@ def run_ours(args, rank, world, local_rank):
                          "pinned host x -> device, graph of C-ABI launches, device y -> pinned host, every step")},
         "gpu_launches": len(flat) * args.steps * (1 if M <= 8 or M >= 16 else (M + 7) // 8),
         "mode": args.mode,
+        "latency_floor": floor,
         "roofline": roof,
         "clocks": clocks,
     }

@@ -358,6 +358,14 @@ int qg_test_bounded_wait(cudaStream_t stream) {
     return cudaGetLastError() == cudaSuccess ? QG_OK : QG_ECUDA;
 }
 
+int qg_test_chain_step(const float* X, float* Y, int64_t K, int grid, unsigned flags, cudaStream_t stream) {
+    if (!X || !Y || K <= 0 || K % 256 != 0 || K > (int64_t(1) << 31) || grid < 1 || grid > 65535) return QG_EINVAL;
+    if (flags & ~static_cast<unsigned>(QG_PREFETCH_WEIGHTS)) return QG_EINVAL;
+    if (!aligned16(X) || !aligned16(Y)) return QG_EALIGN;
+    if (overlap(Y, int64_t(grid) * 32 * 4, X, K * 4)) return QG_EALIAS;
+    return qg::launch_chain_step(X, Y, K, grid, flags, stream);
+}
+
 const char* qg_strerror(int status) {
     switch (status) {
         case QG_OK: return "ok";

@@ -29,6 +29,7 @@ int launch_gemv_cb(int format, const uint8_t* W, const void* book, const float* 
                    int64_t K, cudaStream_t s);
 int launch_dequant_cb(int format, const uint8_t* W, const void* book, float* out, int64_t N, int64_t K,
                       cudaStream_t s);
+int launch_chain_step(const float* X, float* Y, int64_t K, int grid, unsigned flags, cudaStream_t s);
 int launch_pass_q4k(const qg_stage* stages, int nstages, int M, unsigned* sync, cudaStream_t s, unsigned* status);
 int launch_dequant_q4k(const uint8_t* W, float* out, int64_t N, int64_t K, cudaStream_t s);
 int launch_dequant_iq3(const uint8_t* W, const uint8_t* grid, float* out, int64_t N, int64_t K, cudaStream_t s);

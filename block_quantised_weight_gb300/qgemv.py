@@ -44,7 +44,7 @@ QG_CB = {"iq4nl": 1, "iq4xs": 2, "iq3s": 3, "iq2xxs": 4}
 CB_UNIT_BYTES = {"iq4nl": 144, "iq4xs": 136, "iq3s": 110, "iq2xxs": 66}
 
 EXPORTS = ("qgemv_q4k", "qgemv_q4k_ex", "qgemv_q4k_group", "qgemv_q4k_fused", "qgemv_q4k_fused_group", "qgemv_q4k_pass", "qgemv_q4k_pass_noalloc", "qgemv_iq3", "qgemv_iq3_ex", "qgemv_iq3_group", "qgemv_iq3xxs", "qgemv_iq3xxs_ex", "qdequant_iq3xxs", "qgemv_codebook", "qdequant_codebook", "qgemm_q4k_batched", "qgemm_iq3_batched", "qdequant_q4k", "qdequant_iq3",
-           "qg_device_status", "qg_test_bounded_wait", "qg_strerror")
+           "qg_device_status", "qg_test_bounded_wait", "qg_test_chain_step", "qg_strerror")
 
 
 class QGError(RuntimeError):
@@ -90,6 +90,7 @@ def load():
             "qdequant_iq3": [vp, vp, vp, i64, i64, vp],
             "qg_device_status": [vp],
             "qg_test_bounded_wait": [vp],
+            "qg_test_chain_step": [vp, vp, i64, ci, ctypes.c_uint, vp],
             "qg_strerror": [ci],
         }
         for name, args in sigs.items():

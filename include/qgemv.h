@@ -303,6 +303,16 @@ QG_API int qg_device_status(cudaStream_t stream);
  * Never traps or hangs. */
 QG_API int qg_test_bounded_wait(cudaStream_t stream);
 
+/* Test-only measurement aid: one launch that does only what a GEMV of a
+ * decode step must do on the dependency chain: with QG_PREFETCH_WEIGHTS it
+ * is a programmatic dependent launch that lets the next launch start and
+ * waits for the previous one; then each of `grid` CTAs reads X[0..K) (fp32)
+ * and writes 32 floats of Y (Y holds grid*32 floats; caller-owned device
+ * memory, 16-byte aligned, not overlapping X).  A chain of these with the
+ * grids of a step's GEMVs measures the step's dependent-launch floor.  The
+ * pages have no counterpart. */
+QG_API int qg_test_chain_step(const float* X, float* Y, int64_t K, int grid, unsigned flags, cudaStream_t stream);
+
 /* Static description of a status code. */
 QG_API const char* qg_strerror(int status);
 

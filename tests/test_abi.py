@@ -141,3 +141,13 @@ def test_codebook_arguments_rejected_on_host(lib):
     assert lib.qgemv_codebook(3, W, B, X, Y, 1, 64, 300, None) == qgemv.QG_EINVAL
     assert lib.qgemv_codebook(4, W, Y + 16, X, Y, 1, 64, 256, None) == qgemv.QG_EALIAS
     assert lib.qdequant_codebook(1, W, B, W + 16, 4, 256, None) == qgemv.QG_EALIAS
+
+
+def test_chain_step_arguments_rejected_on_host(lib):
+    X, Y = A, A + 0x10000000
+    assert lib.qg_test_chain_step(None, Y, 2048, 80, 1, None) == qgemv.QG_EINVAL
+    assert lib.qg_test_chain_step(X, Y, 300, 80, 1, None) == qgemv.QG_EINVAL
+    assert lib.qg_test_chain_step(X, Y, 2048, 0, 1, None) == qgemv.QG_EINVAL
+    assert lib.qg_test_chain_step(X, Y, 2048, 80, 4, None) == qgemv.QG_EINVAL
+    assert lib.qg_test_chain_step(X + 4, Y, 2048, 80, 1, None) == qgemv.QG_EALIGN
+    assert lib.qg_test_chain_step(X, X + 4096, 2048, 80, 1, None) == qgemv.QG_EALIAS

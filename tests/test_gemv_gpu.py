@@ -436,3 +436,30 @@ def test_gemv_iq3xxs_full_size_sampled(q):
     Y, A = oracle.gemv_iq3xxs(W, grid, x, rows=rows)
     y = q.qgemv_iq3xxs(dev(W), dev(grid), dev(x), flags=q.QG_PREFETCH_WEIGHTS).cpu().numpy()
     check_tol(y[:, rows], Y, A, TAU_FMA, "iq3xxs full")
+
+
+def _probe_value(x):
+    """What one CTA of the probe writes: warp 0's share of sum(x), thread t
+    taking float4 groups t, t + 288, ... (288 threads per CTA)."""
+    g = x.double().reshape(-1, 4).sum(1)
+    return float(sum(g[t::288].sum() for t in range(32)))
+
+
+def test_chain_step_probe(q):
+    """qg_test_chain_step (the dependent-launch floor probe): every CTA writes
+    the same value (its first warp's share of sum(x)) into its 32 outputs,
+    with and without the programmatic dependent launch flag, in a chain that
+    reads the previous launch's output."""
+    import ctypes
+    lib = q.load()
+    K, grid = 2048, 80
+    x = torch.arange(K, dtype=torch.float32, device="cuda") / K
+    y = torch.zeros(grid * 32, dtype=torch.float32, device="cuda")
+    y2 = torch.zeros(grid * 32, dtype=torch.float32, device="cuda")
+    s = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    for flags in (0, q.QG_PREFETCH_WEIGHTS):
+        assert lib.qg_test_chain_step(x.data_ptr(), y.data_ptr(), K, grid, flags, s) == 0
+        assert lib.qg_test_chain_step(y.data_ptr(), y2.data_ptr(), K, grid, flags, s) == 0
+        torch.cuda.synchronize()
+        assert torch.allclose(y.double(), torch.full_like(y.double(), _probe_value(x)), rtol=1e-5)
+        assert torch.allclose(y2.double(), torch.full_like(y2.double(), _probe_value(y[:K])), rtol=1e-5)
