@@ -36,12 +36,12 @@ int launch_gemv(const uint8_t* const* W, float* const* Y, const int64_t* N, int 
     static bool attr_done[64];
     const int budget = std::min(kSmemPerCTA, kSmemPerSM / MINB - kSmemReserve);
     const Layout L1 = make_layout(F::kIQ3, MT, F::kXH, RG, 1, F::kRowStride, F::kCols, FUSE);
-    const int stages = std::min(kMaxStages, (budget - L1.stage0) / L1.stage_bytes);
-    if (stages < 2) return QG_EINVAL;
-    const Layout L = make_layout(F::kIQ3, MT, F::kXH, RG, stages, F::kRowStride, F::kCols, FUSE);
+    const int stages_fit = std::min(kMaxStages, (budget - L1.stage0) / L1.stage_bytes);
+    if (stages_fit < 2) return QG_EINVAL;
     auto kern = gemv_kernel<F, MT, RG, MINB, FUSE>;
     if (!attr_done[dev]) {
-        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L.total) != cudaSuccess)
+        const Layout Lmax = make_layout(F::kIQ3, MT, F::kXH, RG, stages_fit, F::kRowStride, F::kCols, FUSE);
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Lmax.total) != cudaSuccess)
             return QG_ECUDA;
         attr_done[dev] = true;
     }
@@ -78,6 +78,13 @@ int launch_gemv(const uint8_t* const* W, float* const* Y, const int64_t* N, int 
     // cluster (the caller checks that the grid fits one wave).
     const int grid_x = csize > 1 ? static_cast<int>(ntiles * csize)
                                  : static_cast<int>(std::min<int64_t>(ntiles, static_cast<int64_t>(sms) * MINB));
+    // A ring deeper than a CTA's units only takes shared memory from the CTAs
+    // of the next launch, which could otherwise become resident early and
+    // start their weight stream: at most one stage per unit.
+    const int64_t nch = (K / 256 + F::kCols - 1) / F::kCols;
+    const int64_t units = csize > 1 ? 1 : (ntiles + grid_x - 1) / grid_x * nch;
+    const int stages = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(stages_fit, units)));
+    const Layout L = make_layout(F::kIQ3, MT, F::kXH, RG, stages, F::kRowStride, F::kCols, FUSE);
     const int kflags = ((flags & QG_PREFETCH_WEIGHTS) ? kFlagPrefetchWeights : 0) |
                        (csize > 1 ? csize << kFlagClusterShift : 0);
     if (!(flags & QG_PREFETCH_WEIGHTS) && csize <= 1) {
