@@ -222,7 +222,10 @@ __device__ __forceinline__ float half_hi(uint32_t h) {
 }
 
 // SiLU (page 2 "Candle", Block::forward's silu): z * sigmoid(z).
-__device__ __forceinline__ float silu(float z) { return z / (1.f + expf(-z)); }
+// exp by the fast hardware path (__expf: relative error of a few ulp, far
+// inside the GEMV's 1e-5 tolerance); exp(-z) = inf for z << 0 gives z / inf
+// = -0, the limit.
+__device__ __forceinline__ float silu(float z) { return z / (1.f + __expf(-z)); }
 
 // Per-warp x preparation for one Q4_K super-block column (256 x values per
 // token; half 1, x[128..255], starts XH floats after half 0):
@@ -648,10 +651,11 @@ __global__ void __launch_bounds__(RG * F::kCols * 32 + 32, MINB)
                     bulk_g2s(st + L.xoff + lane * F::kCols * 1024,
                              X + lane * K + static_cast<int64_t>(p.c) * F::kCols * 256, kc * 1024, &full[p.s], pol_x);
             }
-            // prologue operand slices, laid out like x (they belong to the
-            // dependency chain, as x does)
+            // prologue operand slices, laid out like x: the RMSNorm weight is
+            // a model weight (it streams with W, before the dependency wait);
+            // the SwiGLU up operand belongs to the dependency chain, as x does
             if constexpr (FUSE == kFuseNorm) {
-                if (do_x && lane == 0)
+                if (do_w && lane == 0)
                     bulk_g2s(st + L.aoff, Fz.g + static_cast<int64_t>(p.c) * F::kCols * 256, kc * 1024, &full[p.s],
                              pol_x);
             } else if constexpr (FUSE == kFuseSwiGLU) {

@@ -60,8 +60,8 @@ extern "C" {
 #define QG_MAX_GROUP 4
 
 /* Launch flag for the *_ex entry points.  QG_PREFETCH_WEIGHTS promises that W
- * (and the IQ3 grid) are not written by the kernel that precedes this call in
- * the stream.  The GEMV is then launched as a programmatic dependent launch:
+ * (and the IQ3 grid, and a fused call's RMSNorm weight) are not written by
+ * the kernel that precedes this call in the stream.  The GEMV is then launched as a programmatic dependent launch:
  * it may start while the preceding kernel is still running and stream its
  * first weight tiles, and it waits for the preceding kernel to complete (all
  * its memory visible) before it reads X or writes Y.  Without the flag the
