@@ -59,20 +59,22 @@ constexpr int kBlockBytes = 144;
 constexpr int kThreads = 320;  // 8 dequant warps, producer, MMA
 constexpr int kRawW = kTileRows * kBlockBytes;     // 18432: TMA box 144 x 128 (IQ3: 112 x 128)
 constexpr int kIQ3Box = 112;
-constexpr int kRawX = 32 * 1024;                    // up to 32 tokens x 256 fp32
-constexpr int kRawStage = kRawW + kRawX;            // 51200
+constexpr int kMaxRaw = 6;                          // raw stages (W box + the unit's x, M KB)
 constexpr int kOpA = kTileRows * 128 * 2;           // 32768: 128 rows x 128 k bf16
 constexpr int kOpB = 32 * 128 * 2;                  // 8192: 32 tokens x 128 k bf16
 constexpr int kOpStage = kOpA + kOpB;               // 40960
-constexpr int kRaw0 = 1024;
-constexpr int kOp0 = kRaw0 + 2 * kRawStage;         // 103424
+// Shared memory: barriers, then the two operand stages, the IQ3 tables, and
+// the raw ring at the end: as many stages of kRawW + M * 1024 bytes as fit.
+constexpr int kOp0 = 1024;
 // IQ3: the grid as fp32, 8 copies: row i of copy c at (8i + c) * 16 bytes,
 // lane L reading copy L & 7, so the 8 lanes of a quarter warp gather from 8
 // distinct bank groups whatever their rows (32 KB).
 constexpr int kGrid0 = kOp0 + 2 * kOpStage;
 constexpr int kSign0 = kGrid0 + 32768;              // IQ3: sign-mask words, 8 copies (entry s7 of copy c at 8*s7 + c: 4 KB)
-constexpr int kSmemTotal = kGrid0;                  // 185344 (Q4_K)
-constexpr int kSmemTotalIQ3 = kSign0 + 4096;
+constexpr int kRaw0Q4K = kGrid0;                    // 82944
+constexpr int kRaw0IQ3 = kSign0 + 4096;              // 119808
+constexpr int kSmemMax = 232448;                     // 227 KB per CTA
+__host__ __device__ constexpr int raw_stage_bytes(int M) { return kRawW + M * 1024; }
 constexpr int kTmemCols = 32;
 constexpr uint32_t kSBO = 16 * 128;                 // row-group stride in an operand stage
 constexpr uint32_t kLBO = 128;                      // k-chunk stride
@@ -252,16 +254,18 @@ __device__ __forceinline__ void dequant_half_iq3(const uint8_t* boxrow, const fl
 template <bool IQ3>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
-                   const uint8_t* __restrict__ grid, float* __restrict__ Y, int M, int64_t N, int64_t K,
+                   const uint8_t* __restrict__ grid, float* __restrict__ Y, int M, int64_t N, int64_t K, int nraw,
                    unsigned* status) {
     extern __shared__ __align__(1024) uint8_t smem[];
-    uint64_t* raw_full = reinterpret_cast<uint64_t*>(smem);  // [2]
-    uint64_t* raw_empty = raw_full + 2;                       // [2]
-    uint64_t* op_full = raw_full + 4;                         // [2]
-    uint64_t* op_empty = raw_full + 6;                        // [2]
-    uint64_t* acc_full = raw_full + 8;
-    uint64_t* acc_empty = raw_full + 9;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + 128);
+    uint64_t* raw_full = reinterpret_cast<uint64_t*>(smem);  // [kMaxRaw]
+    uint64_t* raw_empty = raw_full + kMaxRaw;                 // [kMaxRaw]
+    uint64_t* op_full = raw_full + 2 * kMaxRaw;               // [2]
+    uint64_t* op_empty = op_full + 2;                         // [2]
+    uint64_t* acc_full = op_full + 4;
+    uint64_t* acc_empty = op_full + 5;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + 512);
+    const int raw0 = IQ3 ? kRaw0IQ3 : kRaw0Q4K;
+    const int rstage = raw_stage_bytes(M);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int nb = static_cast<int>(K / 256);
@@ -272,9 +276,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int nmma = M <= 16 ? 16 : 32;
 
     if (threadIdx.x == 0) {
-        for (int i = 0; i < 2; ++i) {
+        for (int i = 0; i < nraw; ++i) {
             mbar_init(&raw_full[i], 1);
             mbar_init(&raw_empty[i], 8);
+        }
+        for (int i = 0; i < 2; ++i) {
             mbar_init(&op_full[i], 4);
             mbar_init(&op_empty[i], 1);
         }
@@ -318,11 +324,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t bytes = kTileRows * kBoxBytes + M * 1024;
             for (int64_t u = u_begin; u < u_end; ++u) {
                 const int64_t i = u - u_begin;
-                const int s = static_cast<int>(i & 1);
-                if (i >= 2) mbar_wait_bounded(&raw_empty[s], static_cast<uint32_t>(((i >> 1) - 1) & 1), status);
+                const int s = static_cast<int>(i % nraw);
+                if (i >= nraw) mbar_wait_bounded(&raw_empty[s], static_cast<uint32_t>((i / nraw - 1) & 1), status);
                 const int64_t tile = u / nb;
                 const int kb = static_cast<int>(u % nb);
-                uint8_t* raw = smem + kRaw0 + s * kRawStage;
+                uint8_t* raw = smem + raw0 + s * rstage;
                 mbar_arrive_expect_tx(&raw_full[s], bytes);
                 const int bx = IQ3 ? (kb * 98) & ~15 : kb * kBlockBytes;  // x * 1 byte: 16-byte aligned
                 tma_load_2d(raw, &tmW, bx, static_cast<int>(tile * kTileRows), &raw_full[s], pol_w);
@@ -373,15 +379,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         int64_t seg = 0;
         for (int64_t u = u_begin; u < u_end; ++u) {
             const int64_t i = u - u_begin;
-            const int s = static_cast<int>(i & 1);
+            const int s = static_cast<int>(i % nraw);
             const int64_t tile = u / nb;
             const int kb = static_cast<int>(u % nb);
             const bool last = (u == u_end - 1) || kb == nb - 1;
             const int64_t row0 = tile * kTileRows;
             const int rows = static_cast<int>(min64(kTileRows, N - row0));
-            const uint8_t* raw = smem + kRaw0 + s * kRawStage;
+            const uint8_t* raw = smem + raw0 + s * rstage;
             const float* xr = reinterpret_cast<const float*>(raw + kRawW);
-            mbar_wait_bounded(&raw_full[s], static_cast<uint32_t>((i >> 1) & 1), status);
+            mbar_wait_bounded(&raw_full[s], static_cast<uint32_t>((i / nraw) & 1), status);
             if (i >= 1) mbar_wait_bounded(&op_empty[half], static_cast<uint32_t>((i - 1) & 1), status);
             if constexpr (IQ3)  // rows past N: TMA zero fill, unused
                 switch (kb & 7) {  // the block's offset in its box: (98 * kb) mod 16
@@ -449,9 +455,13 @@ int launch_tc(const uint8_t* W, const uint8_t* grid, const float* X, float* Y, i
     static bool attr_done[64];
     int dev = -1;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return QG_ECUDA;
-    const int smem = IQ3 ? tc::kSmemTotalIQ3 : tc::kSmemTotal;
+    // as many raw stages as fit (the x part of a stage is M KB)
+    const int raw0 = IQ3 ? tc::kRaw0IQ3 : tc::kRaw0Q4K;
+    const int nraw = std::min(tc::kMaxRaw, (tc::kSmemMax - raw0) / tc::raw_stage_bytes(M));
+    if (nraw < 2) return QG_EINVAL;
+    const int smem = raw0 + nraw * tc::raw_stage_bytes(M);
     if (!attr_done[dev]) {
-        if (cudaFuncSetAttribute(tc::gemm_tc_kernel<IQ3>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
+        if (cudaFuncSetAttribute(tc::gemm_tc_kernel<IQ3>, cudaFuncAttributeMaxDynamicSharedMemorySize, tc::kSmemMax) !=
             cudaSuccess)
             return QG_ECUDA;
         attr_done[dev] = true;
@@ -479,7 +489,7 @@ int launch_tc(const uint8_t* W, const uint8_t* grid, const float* X, float* Y, i
     if (cudaMemsetAsync(Y, 0, static_cast<size_t>(M) * N * sizeof(float), s) != cudaSuccess) return QG_ECUDA;
     const int64_t units = ((N + tc::kTileRows - 1) / tc::kTileRows) * (K / 256);
     const int gridx = static_cast<int>(std::min<int64_t>(units, sms));
-    tc::gemm_tc_kernel<IQ3><<<gridx, tc::kThreads, smem, s>>>(tmW, tmX, grid, Y, M, N, K, status);
+    tc::gemm_tc_kernel<IQ3><<<gridx, tc::kThreads, smem, s>>>(tmW, tmX, grid, Y, M, N, K, nraw, status);
     return cudaGetLastError() == cudaSuccess ? QG_OK : QG_ECUDA;
 }
 
