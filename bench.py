@@ -196,6 +196,24 @@ def profiled_traffic(workload, M):
     return None
 
 
+# ------------------------------------------------------------------ ranks
+def max_over_ranks(vals, world, device):
+    """Every rank's timings -> the slowest rank's, on every rank.  Replicas
+    share no data; this and a barrier are the only collectives."""
+    import torch
+    t = torch.tensor(vals, dtype=torch.float64, device=device)
+    if world > 1:
+        import torch.distributed as dist
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(v) for v in t]
+
+
+def job_throughput(world, bytes_per_step, steps, ms):
+    """Whole-job GB/s: every replica streams bytes_per_step per step, all in
+    the slowest rank's time."""
+    return world * bytes_per_step * steps / (ms * 1e-3) / 1e9
+
+
 # ------------------------------------------------------------------ our arm
 def fused_step_launches(lib, qgemv, host, dev, keep):
     """The TinyLlama-shaped decode step with its data flow on the device, every
@@ -518,15 +536,11 @@ def run_ours(args, rank, world, local_rank):
     torch.cuda.synchronize(dev)
     ms_e2e = e0.elapsed_time(e1)
 
-    # max over ranks
-    t = torch.tensor([ms_total, ms_e2e], dtype=torch.float64, device=dev)
-    if world > 1:
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    ms_total, ms_e2e = float(t[0]), float(t[1])
+    ms_total, ms_e2e = max_over_ranks([ms_total, ms_e2e], world, dev)
     n_pass = args.steps * passes_per_replay
     ms_step = ms_total / n_pass
-    value = world * step_wbytes * n_pass / (ms_total * 1e-3) / 1e9
-    e2e_value = world * step_wbytes * n_pass / (ms_e2e * 1e-3) / 1e9
+    value = job_throughput(world, step_wbytes, n_pass, ms_total)
+    e2e_value = job_throughput(world, step_wbytes, n_pass, ms_e2e)
 
     if floor:
         floor["above_floor_ms_per_pass"] = round(ms_step - floor["ms_per_pass"], 4)
