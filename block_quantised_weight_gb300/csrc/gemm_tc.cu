@@ -402,12 +402,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             else
                 dequant_half(raw + t * kBlockBytes, opA, t, half);
-            for (int c = t; c < M * 16; c += 128) {
-                const int m = c >> 4, j = c & 15;
-                const float4 a = *reinterpret_cast<const float4*>(xr + m * 256 + 128 * half + 8 * j);
-                const float4 b = *reinterpret_cast<const float4*>(xr + m * 256 + 128 * half + 8 * j + 4);
-                *reinterpret_cast<uint4*>(opB + op_off(m, j)) = make_uint4(
-                    pack_bf16(a.x, a.y), pack_bf16(a.z, a.w), pack_bf16(b.x, b.y), pack_bf16(b.z, b.w));
+            // x -> bf16 chunks (token m, k chunk j): the 8 lanes of a quarter
+            // warp take 8 consecutive tokens, whose chunks sit in distinct bank
+            // groups of the operand stage, and chunks j, j+1, ... whose fp32
+            // sources pair up on the row's bank groups: conflict-free stores,
+            // two-way loads (the least for 256 bytes)
+            {
+                const int r = t & 7, j = ((t >> 3) + r) & 15;  // 16 quarter warps: every chunk j once
+                for (int m = r; m < M; m += 8) {
+                    const float4 a = *reinterpret_cast<const float4*>(xr + m * 256 + 128 * half + 8 * j);
+                    const float4 b = *reinterpret_cast<const float4*>(xr + m * 256 + 128 * half + 8 * j + 4);
+                    *reinterpret_cast<uint4*>(opB + op_off(m, j)) = make_uint4(
+                        pack_bf16(a.x, a.y), pack_bf16(a.z, a.w), pack_bf16(b.x, b.y), pack_bf16(b.z, b.w));
+                }
             }
             fence_proxy_async_smem();  // generic-proxy stores -> visible to the tensor core
             __syncwarp();
