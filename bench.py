@@ -567,7 +567,8 @@ def run_ours(args, rank, world, local_rank):
     elif mats[0][0] == "iq3xxs":
         kname = "qgemv_iq3xxs gemv_kernel<FmtIQ3XXST>"
     else:
-        kname = f"qgemv_codebook gemv_cb_kernel<{mats[0][0].upper()}>"
+        kname = (f"qgemv_codebook gemv_cb_tma_kernel<{mats[0][0].upper()}>" if mats[0][0] in ("iq4nl", "iq4xs")
+                 else f"qgemv_codebook gemv_cb_kernel<{mats[0][0].upper()}>")
     roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
             "frac": round(achieved / peak, 4), "traffic": profiled_traffic(args.workload, M),
             "peak_kind": f"of {peak_kind}", "kernel": kname, "launches_timed": n_launch,

@@ -161,7 +161,9 @@ int qgemv_codebook(int format, const uint8_t* W, const void* codebook, const flo
     if (rc != QG_OK) return rc;
     if (!aligned16(book)) return QG_EALIGN;
     if (overlap(Y, int64_t(M) * N * 4, book, codebook_bytes(format))) return QG_EALIAS;
-    return qg::launch_gemv_cb(format, W, book, X, Y, M, N, K, stream);
+    unsigned* st = status_ptr();
+    if (!st) return QG_ECUDA;
+    return qg::launch_gemv_cb(format, W, book, X, Y, M, N, K, stream, st);
 }
 
 int qdequant_codebook(int format, const uint8_t* W, const void* codebook, float* out, int64_t N, int64_t K,

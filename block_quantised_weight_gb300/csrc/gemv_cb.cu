@@ -12,6 +12,8 @@
 // byte), those of kDepth sub-blocks per lane before any is decoded, to keep
 // enough bytes in flight.  Per row, the lanes' partial sums meet in a warp
 // shuffle.
+#include <type_traits>
+
 #include "launch_common.cuh"
 
 namespace qg {
@@ -134,6 +136,31 @@ __device__ __forceinline__ void decode_sub(const Raw& R, int64_t sb, const Table
     }
 }
 
+// IQ4_NL / IQ4_XS sub-block as the 32 table values v and the sub-block's
+// eff (weight = eff * v), for sums taken as eff * sum(v * x).
+template <int F>
+__device__ __forceinline__ void decode_sub_iq4_factored(const Raw& R, int64_t sb, const Table& T, float (&w)[32],
+                                                        float& eff) {
+    const int j = static_cast<int>(sb & 7);
+    if constexpr (F == kIQ4NL) {
+        eff = h2f(R.r[0]);
+    } else {
+        const uint32_t sh = R.r[0] >> 16, sl = R.r[1];
+        const int s = static_cast<int>(((sl >> (4 * j)) & 15u) | (((sh >> (2 * j)) & 3u) << 4));
+        eff = h2f(R.r[0]) * static_cast<float>(s - 32);
+    }
+    constexpr int C = F == kIQ4NL ? 1 : 2;  // first code word
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const uint32_t c = R.r[C + i];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            w[4 * i + e] = T.iq4[(c >> (8 * e)) & 15u];
+            w[16 + 4 * i + e] = T.iq4[(c >> (8 * e + 4)) & 15u];
+        }
+    }
+}
+
 template <int F>
 __device__ void load_table(const void* book, Table& T) {
     if constexpr (F == kIQ4NL || F == kIQ4XS) {
@@ -220,6 +247,282 @@ __global__ void __launch_bounds__(256) gemv_cb_kernel(const uint8_t* __restrict_
     }
 }
 
+// ------------------------------------------------------------ TMA-ring kernel
+// The same decode (used for IQ4_NL and IQ4_XS) fed like the Q4_K / IQ3 GEMV: a producer warp streams each
+// unit (32 rows x 8 columns of 256 weights) into a shared-memory ring with
+// one 2D tensor-map box per column (the column's bytes from their offset
+// rounded down to 16; every unit starts 16-byte aligned, as 8 columns of any
+// of these formats are a multiple of 16 bytes) and the unit's x slice with a
+// bulk copy; consumer warp w decodes column w, one row per lane, reading its
+// box row with 16-byte loads (box rows 144 or 80 bytes apart: 8 consecutive
+// lanes hit 8 distinct bank groups) and realigning it in registers.
+template <int F>
+struct Box {
+    static constexpr int kUB = unit_bytes(F);
+    static constexpr int kBox = F == kIQ2XXS ? 80 : 144;  // >= kUB + the largest in-box offset
+    static constexpr int kWords = kBox / 4;
+};
+
+// Fields of sub-block j of a unit held as words v (v[k] = unit bytes 4k..4k+3);
+// the positions of load_sub, every field at an even byte.
+template <int B>
+__device__ __forceinline__ uint32_t f16at(const uint32_t* v) {
+    return (v[B >> 2] >> (8 * (B & 3))) & 0xFFFFu;
+}
+template <int B>
+__device__ __forceinline__ uint32_t f32at(const uint32_t* v) {
+    return (B & 3) ? __funnelshift_r(v[B >> 2], v[(B >> 2) + 1], 8 * (B & 3)) : v[B >> 2];
+}
+template <int F, int J>
+__device__ __forceinline__ void raw_from_words(const uint32_t* v, Raw& R) {
+    if constexpr (F == kIQ4NL) {
+        R.r[0] = f16at<18 * J>(v);
+        R.r[1] = f32at<18 * J + 2>(v);
+        R.r[2] = f32at<18 * J + 6>(v);
+        R.r[3] = f32at<18 * J + 10>(v);
+        R.r[4] = f32at<18 * J + 14>(v);
+    } else if constexpr (F == kIQ4XS) {
+        R.r[0] = f32at<0>(v);
+        R.r[1] = f32at<4>(v);
+        R.r[2] = f32at<8 + 16 * J>(v);
+        R.r[3] = f32at<12 + 16 * J>(v);
+        R.r[4] = f32at<16 + 16 * J>(v);
+        R.r[5] = f32at<20 + 16 * J>(v);
+    } else if constexpr (F == kIQ3S) {
+        R.r[0] = f16at<0>(v) | (f16at<106 + 2 * (J >> 2)>(v) << 16);
+        R.r[1] = f32at<2 + 8 * J>(v);
+        R.r[2] = f32at<6 + 8 * J>(v);
+        R.r[3] = f16at<66 + (J & ~1)>(v);
+        R.r[4] = f32at<74 + 4 * J>(v);
+    } else {
+        R.r[0] = f16at<0>(v);
+        R.r[1] = f32at<2 + 8 * J>(v);
+        R.r[2] = f32at<6 + 8 * J>(v);
+    }
+}
+
+// One lane's row of one column (unit bytes OFF bytes into the box row)
+// against MT tokens of x (xs: the column's 256 x values of token 0; tokens
+// 2048 floats apart).
+template <int F, int MT, int OFF>
+__device__ __forceinline__ void cb_column(const uint8_t* boxrow, const float* xs, const Table& T, int M,
+                                          float (&acc)[MT]) {
+    constexpr int NW = Box<F>::kWords, W0 = OFF >> 2, SH = 8 * (OFF & 3);
+    uint32_t a[NW + 1];
+#pragma unroll
+    for (int i = 0; i < NW / 4; ++i) {
+        const uint4 t = *reinterpret_cast<const uint4*>(boxrow + 16 * i);
+        a[4 * i] = t.x; a[4 * i + 1] = t.y; a[4 * i + 2] = t.z; a[4 * i + 3] = t.w;
+    }
+    a[NW] = 0u;  // past the box: only ever the unused top bytes of the last word
+    constexpr int NV = (Box<F>::kUB + 3) / 4 + 1;
+    uint32_t v[NV];
+#pragma unroll
+    for (int k = 0; k < NV; ++k) {
+        const int i0 = W0 + k < NW ? W0 + k : NW, i1 = W0 + k + 1 < NW ? W0 + k + 1 : NW;
+        v[k] = SH ? __funnelshift_r(a[i0], a[i1], SH) : a[i0];
+    }
+    auto sub = [&](auto jc) {
+        constexpr int J = decltype(jc)::value;
+        Raw R;
+        raw_from_words<F, J>(v, R);
+        float w[32];
+        float eff = 1.f;
+        if constexpr (F == kIQ4NL || F == kIQ4XS)
+            decode_sub_iq4_factored<F>(R, J, T, w, eff);  // eff applied to the sub-block's sum
+        else
+            decode_sub<F>(R, J, T, w);
+#pragma unroll
+        for (int m = 0; m < MT; ++m) {
+            if (MT == 1 || m < M) {
+                const float4* xp = reinterpret_cast<const float4*>(xs + m * 2048 + 32 * J);
+                float s = 0.f;
+#pragma unroll
+                for (int q = 0; q < 8; ++q) {
+                    const float4 x = xp[q];
+                    s = fmaf(w[4 * q], x.x, s);
+                    s = fmaf(w[4 * q + 1], x.y, s);
+                    s = fmaf(w[4 * q + 2], x.z, s);
+                    s = fmaf(w[4 * q + 3], x.w, s);
+                }
+                acc[m] = fmaf(eff, s, acc[m]);
+            }
+        }
+    };
+    sub(std::integral_constant<int, 0>{});
+    sub(std::integral_constant<int, 1>{});
+    sub(std::integral_constant<int, 2>{});
+    sub(std::integral_constant<int, 3>{});
+    sub(std::integral_constant<int, 4>{});
+    sub(std::integral_constant<int, 5>{});
+    sub(std::integral_constant<int, 6>{});
+    sub(std::integral_constant<int, 7>{});
+}
+
+constexpr int kCbCols = 8;        // columns per unit = consumer warps
+constexpr int kCbMaxStages = 4;
+// Dynamic shared memory: barriers at 0, the codebook at 128, the warps'
+// row sums at 2176, the ring from 8192.
+constexpr int kCbTable0 = 128, kCbRed0 = kCbTable0 + 2048, kCbRing0 = 8192;
+static_assert(sizeof(Table) <= 2048, "codebook slot");
+__host__ __device__ constexpr int cb_stage_bytes(int F, int MT) {
+    return kCbCols * 32 * (F == kIQ2XXS ? 80 : 144) + MT * kCbCols * 1024;
+}
+
+template <int F, int MT, int MINB>
+__global__ void __launch_bounds__(kCbCols * 32 + 32, MINB)
+    gemv_cb_tma_kernel(const __grid_constant__ CUtensorMap tmW, const void* __restrict__ book,
+                       const float* __restrict__ X, float* __restrict__ Y, int M, int64_t N, int64_t K, int stages,
+                       unsigned* status) {
+    extern __shared__ __align__(1024) uint8_t smem[];
+    Table& T = *reinterpret_cast<Table*>(smem + kCbTable0);
+    float (*red)[MT][32] = reinterpret_cast<float (*)[MT][32]>(smem + kCbRed0);
+    static_assert(kCbRed0 + kCbCols * MT * 32 * 4 <= kCbRing0, "row-sum slot");
+    constexpr int kBox = Box<F>::kBox, kUB = Box<F>::kUB;
+    constexpr int kColBytes = 32 * kBox;
+    constexpr int kSB = cb_stage_bytes(F, MT);
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem);
+    uint64_t* empty = full + kCbMaxStages;
+    uint8_t* ring = smem + kCbRing0;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int nb = static_cast<int>(K / 256);
+    const int nchunks = (nb + kCbCols - 1) / kCbCols;
+    const int64_t ntiles = (N + 31) / 32;
+    const int64_t my_tiles = blockIdx.x < ntiles ? (ntiles - 1 - blockIdx.x) / gridDim.x + 1 : 0;
+    const int64_t U = my_tiles * nchunks;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < stages; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], kCbCols);
+        }
+        fence_mbar_init();
+    }
+    load_table<F>(book, T);
+    __syncthreads();
+
+    if (warp == kCbCols) {
+        // ---------------- producer
+        if (lane == 0) {
+            const uint64_t pol_w = policy_evict_first(), pol_x = policy_evict_last();
+            int s = 0, c = 0;
+            uint32_t round = 0;
+            int64_t tile = blockIdx.x;
+            for (int64_t u = 0; u < U; ++u) {
+                if (u >= stages) mbar_wait_bounded(&empty[s], (round - 1) & 1u, status);
+                const int kc = min(kCbCols, nb - c * kCbCols);
+                uint8_t* st = ring + s * kSB;
+                mbar_arrive_expect_tx(&full[s], kc * kColBytes + M * kc * 1024);
+                for (int b = 0; b < kc; ++b)
+                    tma_load_2d(st + b * kColBytes, &tmW, ((c * kCbCols + b) * kUB) & ~15,
+                                static_cast<int>(tile * 32), &full[s], pol_w);
+                for (int m = 0; m < M; ++m)
+                    bulk_g2s(st + kCbCols * kColBytes + m * kCbCols * 1024,
+                             X + m * K + static_cast<int64_t>(c) * kCbCols * 256, kc * 1024, &full[s], pol_x);
+                if (++s == stages) {
+                    s = 0;
+                    ++round;
+                }
+                if (++c == nchunks) {
+                    c = 0;
+                    tile += gridDim.x;
+                }
+            }
+        }
+        return;
+    }
+
+    // ---------------- consumers: warp = column, lane = row
+    float acc[MT];
+#pragma unroll
+    for (int m = 0; m < MT; ++m) acc[m] = 0.f;
+    int s = 0, c = 0;
+    uint32_t phase = 0;
+    int64_t tile = blockIdx.x;
+    for (int64_t u = 0; u < U; ++u) {
+        const int kc = min(kCbCols, nb - c * kCbCols);
+        const uint8_t* st = ring + s * kSB;
+        mbar_wait_bounded(&full[s], phase, status);
+        if (warp < kc) {
+            const uint8_t* boxrow = st + warp * kColBytes + lane * kBox;
+            const float* xs = reinterpret_cast<const float*>(st + kCbCols * kColBytes) + warp * 256;
+            // the column's offset in its box: (kUB * column) mod 16, and
+            // 8 * kUB is a multiple of 16
+            switch ((warp * kUB) & 15) {
+#define QG_CB_COL(O) \
+    case O: cb_column<F, MT, O>(boxrow, xs, T, M, acc); break;
+                QG_CB_COL(0) QG_CB_COL(2) QG_CB_COL(4) QG_CB_COL(6)
+                QG_CB_COL(8) QG_CB_COL(10) QG_CB_COL(12) QG_CB_COL(14)
+#undef QG_CB_COL
+                default: break;
+            }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[s]);
+        if (c == nchunks - 1) {
+#pragma unroll
+            for (int m = 0; m < MT; ++m) {
+                red[warp][m][lane] = acc[m];
+                acc[m] = 0.f;
+            }
+            named_barrier_sync<kCbCols * 32>(1);
+            for (int t = threadIdx.x; t < MT * 32; t += kCbCols * 32) {
+                const int m = t >> 5, r = t & 31;
+                const int64_t nn = tile * 32 + r;
+                if ((MT == 1 || m < M) && nn < N) {
+                    float v = 0.f;
+#pragma unroll
+                    for (int w = 0; w < kCbCols; ++w) v += red[w][m][r];
+                    Y[m * N + nn] = v;
+                }
+            }
+            named_barrier_sync<kCbCols * 32>(1);
+        }
+        if (++s == stages) {
+            s = 0;
+            phase ^= 1u;
+        }
+        if (++c == nchunks) {
+            c = 0;
+            tile += gridDim.x;
+        }
+    }
+}
+
+// The TMA path: the IQ4 formats (a 16-entry table lookup per weight), rows
+// whose pitch is a multiple of 16 bytes.  The grid formats (IQ3_S, IQ2_XXS)
+// stay on the direct-load kernel: their decode is a chain of dependent
+// table gathers per lane, which that kernel's 40 warps per SM (48 registers
+// a thread) hide better than this one's 16 (measured 2-3x faster there).
+inline bool tma_ok(int F, int64_t K) {
+    return (F == kIQ4NL || F == kIQ4XS) && ((K / 256) * unit_bytes(F)) % 16 == 0;
+}
+
+template <int F, int MT, int MINB>
+int launch_tma(const uint8_t* W, const void* book, const float* X, float* Y, int M, int64_t N, int64_t K,
+               cudaStream_t s, unsigned* status, int dev, int sms) {
+    static bool attr_done[64];
+    const int budget = std::min(kSmemPerCTA, kSmemPerSM / MINB - kSmemReserve) - kCbRing0;
+    const int stages = std::min(kCbMaxStages, budget / cb_stage_bytes(F, MT));
+    if (stages < 2) return QG_EINVAL;
+    auto kern = gemv_cb_tma_kernel<F, MT, MINB>;
+    if (!attr_done[dev]) {
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 std::min(kSmemPerCTA, kCbRing0 + kCbMaxStages * cb_stage_bytes(F, MT))) !=
+            cudaSuccess)
+            return QG_ECUDA;
+        attr_done[dev] = true;
+    }
+    CUtensorMap tm;
+    const uint64_t pitch = static_cast<uint64_t>(K / 256) * unit_bytes(F);
+    if (!encode_byte_rows(&tm, W, pitch, static_cast<uint64_t>(N), Box<F>::kBox, 32)) return QG_ECUDA;
+    const int64_t ntiles = (N + 31) / 32;
+    const int grid = static_cast<int>(std::min<int64_t>(ntiles, static_cast<int64_t>(sms) * MINB));
+    const int64_t units_per_cta = (ntiles + grid - 1) / grid * ((K / 256 + kCbCols - 1) / kCbCols);
+    const int st = static_cast<int>(std::min<int64_t>(stages, std::max<int64_t>(2, units_per_cta)));
+    kern<<<grid, kCbCols * 32 + 32, kCbRing0 + st * cb_stage_bytes(F, MT), s>>>(tm, book, X, Y, M, N, K, st, status);
+    return cudaGetLastError() == cudaSuccess ? QG_OK : QG_ECUDA;
+}
+
 // Test-only: every sub-block's 32 values (exact), one thread per sub-block.
 template <int F>
 __global__ void __launch_bounds__(256) dequant_cb_kernel(const uint8_t* __restrict__ W, const void* __restrict__ book,
@@ -241,11 +544,25 @@ __global__ void __launch_bounds__(256) dequant_cb_kernel(const uint8_t* __restri
 
 template <int F>
 int launch_t(const uint8_t* W, const void* book, const float* X, float* Y, int M, int64_t N, int64_t K,
-             cudaStream_t s) {
+             cudaStream_t s, unsigned* status) {
     const int dev = current_device();
     if (dev < 0) return QG_ECUDA;
     const int sms = sm_count(dev);
     if (sms <= 0) return QG_ECUDA;
+    if constexpr (F == kIQ4NL || F == kIQ4XS) {
+        if (tma_ok(F, K)) {
+            // groups of at most 4 tokens, each streaming W once
+            for (int m0 = 0; m0 < M; m0 += 4) {
+                const int mg = std::min(4, M - m0);
+                const float* Xg = X + static_cast<int64_t>(m0) * K;
+                float* Yg = Y + static_cast<int64_t>(m0) * N;
+                const int rc = mg == 1 ? launch_tma<F, 1, 2>(W, book, Xg, Yg, mg, N, K, s, status, dev, sms)
+                                       : launch_tma<F, 4, 1>(W, book, Xg, Yg, mg, N, K, s, status, dev, sms);
+                if (rc != QG_OK) return rc;
+            }
+            return QG_OK;
+        }
+    }
     const int blocks = static_cast<int>(std::min<int64_t>((N + 31) / 32, static_cast<int64_t>(sms) * 8));
     for (int m0 = 0; m0 < M; m0 += 8) {
         const int mg = std::min(8, M - m0);
@@ -274,12 +591,12 @@ int dequant_t(const uint8_t* W, const void* book, float* out, int64_t N, int64_t
 int cb_unit_bytes(int format) { return cb::unit_bytes(format); }
 
 int launch_gemv_cb(int format, const uint8_t* W, const void* book, const float* X, float* Y, int M, int64_t N,
-                   int64_t K, cudaStream_t s) {
+                   int64_t K, cudaStream_t s, unsigned* status) {
     switch (format) {
-        case QG_CB_IQ4_NL: return cb::launch_t<cb::kIQ4NL>(W, book, X, Y, M, N, K, s);
-        case QG_CB_IQ4_XS: return cb::launch_t<cb::kIQ4XS>(W, book, X, Y, M, N, K, s);
-        case QG_CB_IQ3_S: return cb::launch_t<cb::kIQ3S>(W, book, X, Y, M, N, K, s);
-        case QG_CB_IQ2_XXS: return cb::launch_t<cb::kIQ2XXS>(W, book, X, Y, M, N, K, s);
+        case QG_CB_IQ4_NL: return cb::launch_t<cb::kIQ4NL>(W, book, X, Y, M, N, K, s, status);
+        case QG_CB_IQ4_XS: return cb::launch_t<cb::kIQ4XS>(W, book, X, Y, M, N, K, s, status);
+        case QG_CB_IQ3_S: return cb::launch_t<cb::kIQ3S>(W, book, X, Y, M, N, K, s, status);
+        case QG_CB_IQ2_XXS: return cb::launch_t<cb::kIQ2XXS>(W, book, X, Y, M, N, K, s, status);
         default: return QG_EINVAL;
     }
 }

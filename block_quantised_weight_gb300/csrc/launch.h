@@ -26,7 +26,7 @@ int launch_group_iq3(const uint8_t* const* W, float* const* Y, const int64_t* N,
 // page 3's codebook formats (QG_CB_*)
 int cb_unit_bytes(int format);
 int launch_gemv_cb(int format, const uint8_t* W, const void* book, const float* X, float* Y, int M, int64_t N,
-                   int64_t K, cudaStream_t s);
+                   int64_t K, cudaStream_t s, unsigned* status);
 int launch_dequant_cb(int format, const uint8_t* W, const void* book, float* out, int64_t N, int64_t K,
                       cudaStream_t s);
 int launch_chain_step(const float* X, float* Y, int64_t K, int grid, unsigned flags, cudaStream_t s);
