@@ -173,23 +173,38 @@ def cudart():
     return None
 
 
-def kernel_source_hash():
+# Sources each kernel is built from (the library's translation unit for it
+# and everything that unit includes).
+_COMMON = ["common.cuh", "gemv_kernel.cuh", "launch.h", "tensor_map.h", "launch_common.cuh",
+           "../../include/qgemv.h"]
+KERNEL_SOURCES = {
+    "q4k": _COMMON + ["launch_q4k.cuh", "gemv_q4k.cu"],
+    "iq3": _COMMON + ["launch_iq3.cuh", "gemv_iq3.cu"],
+    "tc": ["common.cuh", "gemv_kernel.cuh", "launch.h", "tensor_map.h", "../../include/qgemv.h", "gemm_tc.cu"],
+    "cb": _COMMON + ["gemv_cb.cu"],
+}
+
+
+def kernel_source_hash(files=None):
+    """Hash of the given kernel sources (paths relative to csrc/), or of every
+    source in csrc/."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "block_quantised_weight_gb300", "csrc")
-    for f in sorted(os.listdir(csrc)):
-        if f.endswith((".cu", ".cuh", ".h")):
-            h.update(open(os.path.join(csrc, f), "rb").read())
+    if files is None:
+        files = sorted(f for f in os.listdir(csrc) if f.endswith((".cu", ".cuh", ".h")))
+    for f in files:
+        h.update(open(os.path.join(csrc, f), "rb").read())
     return h.hexdigest()[:16]
 
 
 def profiled_traffic(workload, M):
     """DRAM bytes per launch of the dominant kernel from a committed ncu summary,
-    only if the kernel sources are unchanged since it was taken."""
+    only if that kernel's sources are unchanged since it was taken."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         d = json.load(open(p))
         e = d.get(f"{workload}:M{M}")
-        if e and e.get("kernel_source_hash") == kernel_source_hash():
+        if e and e.get("kernel_source_hash") == kernel_source_hash(KERNEL_SOURCES[e["sources"]]):
             return e["dram_bytes_per_launch"]
     except Exception:
         pass
