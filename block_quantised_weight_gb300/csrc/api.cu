@@ -2,6 +2,7 @@
 //
 // Every argument is checked on the host before anything is launched; no
 // exception crosses this boundary and nothing here aborts the process.
+#include <atomic>
 #include <cstdint>
 #include <mutex>
 
@@ -15,17 +16,19 @@ namespace {
 // its device address (cudaGetSymbolAddress, cached per device), never the
 // host-side symbol.
 __device__ unsigned qg_status_word;
-unsigned* g_status_ptr[64];
+std::atomic<unsigned*> g_status_ptr[64];  // filled on first use; racing threads store the same value
 
 unsigned* status_ptr() {
     int dev = -1;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
-    if (!g_status_ptr[dev]) {
-        void* p = nullptr;
-        if (cudaGetSymbolAddress(&p, qg_status_word) != cudaSuccess) return nullptr;
-        g_status_ptr[dev] = static_cast<unsigned*>(p);
+    unsigned* p = g_status_ptr[dev].load(std::memory_order_relaxed);
+    if (!p) {
+        void* a = nullptr;
+        if (cudaGetSymbolAddress(&a, qg_status_word) != cudaSuccess) return nullptr;
+        p = static_cast<unsigned*>(a);
+        g_status_ptr[dev].store(p, std::memory_order_relaxed);
     }
-    return g_status_ptr[dev];
+    return p;
 }
 
 }  // namespace

@@ -46,6 +46,7 @@
 #include <cudaTypedefs.h>
 
 #include <algorithm>
+#include <atomic>
 
 #include "gemv_kernel.cuh"
 #include "launch.h"
@@ -459,7 +460,7 @@ template <bool IQ3>
 int launch_tc(const uint8_t* W, const uint8_t* grid, const float* X, float* Y, int M, int64_t N, int64_t K,
               cudaStream_t s, unsigned* status) {
     if (M < 16 || M > 32) return QG_EINVAL;
-    static bool attr_done[64];
+    static std::atomic<bool> attr_done[64];
     int dev = -1;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return QG_ECUDA;
     // as many raw stages as fit (the x part of a stage is M KB)
@@ -467,11 +468,11 @@ int launch_tc(const uint8_t* W, const uint8_t* grid, const float* X, float* Y, i
     const int nraw = std::min(tc::kMaxRaw, (tc::kSmemMax - raw0) / tc::raw_stage_bytes(M));
     if (nraw < 2) return QG_EINVAL;
     const int smem = raw0 + nraw * tc::raw_stage_bytes(M);
-    if (!attr_done[dev]) {
+    if (!attr_done[dev].load(std::memory_order_acquire)) {
         if (cudaFuncSetAttribute(tc::gemm_tc_kernel<IQ3>, cudaFuncAttributeMaxDynamicSharedMemorySize, tc::kSmemMax) !=
             cudaSuccess)
             return QG_ECUDA;
-        attr_done[dev] = true;
+        attr_done[dev].store(true, std::memory_order_release);
     }
     auto encode = tensor_map_encoder();
     if (!encode) return QG_ECUDA;

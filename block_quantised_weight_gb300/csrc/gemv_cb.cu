@@ -500,17 +500,17 @@ inline bool tma_ok(int F, int64_t K) {
 template <int F, int MT, int MINB>
 int launch_tma(const uint8_t* W, const void* book, const float* X, float* Y, int M, int64_t N, int64_t K,
                cudaStream_t s, unsigned* status, int dev, int sms) {
-    static bool attr_done[64];
+    static std::atomic<bool> attr_done[64];
     const int budget = std::min(kSmemPerCTA, kSmemPerSM / MINB - kSmemReserve) - kCbRing0;
     const int stages = std::min(kCbMaxStages, budget / cb_stage_bytes(F, MT));
     if (stages < 2) return QG_EINVAL;
     auto kern = gemv_cb_tma_kernel<F, MT, MINB>;
-    if (!attr_done[dev]) {
+    if (!attr_done[dev].load(std::memory_order_acquire)) {
         if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  std::min(kSmemPerCTA, kCbRing0 + kCbMaxStages * cb_stage_bytes(F, MT))) !=
             cudaSuccess)
             return QG_ECUDA;
-        attr_done[dev] = true;
+        attr_done[dev].store(true, std::memory_order_release);
     }
     CUtensorMap tm;
     const uint64_t pitch = static_cast<uint64_t>(K / 256) * unit_bytes(F);

@@ -221,27 +221,27 @@ namespace {
 
 template <int MT>
 int launch_pass_t(const pass::Plan& plan, int M, unsigned* sync, cudaStream_t s, unsigned* status, int dev) {
-    static bool attr_done[64];
-    static int occ_cache[64];
+    static std::atomic<bool> attr_done[64];
+    static std::atomic<int> occ_cache[64];
     const int budget = kSmemPerSM / 2 - kSmemReserve;
     const Layout L1 = make_layout(false, MT, FmtQ4K::kXH, 1, 1, FmtQ4K::kRowStride);
     int stages = std::min(kMaxStages, (budget - L1.stage0) / L1.stage_bytes);
     if (stages < 2) return QG_EINVAL;
     const Layout L = make_layout(false, MT, FmtQ4K::kXH, 1, stages, FmtQ4K::kRowStride);
     auto kern = pass::gemv_pass_kernel<MT>;
-    if (!attr_done[dev]) {
+    if (!attr_done[dev].load(std::memory_order_acquire)) {
         if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L.total) != cudaSuccess)
             return QG_ECUDA;
         int occ = 0;
         if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, kCols * 32 + 32, L.total) != cudaSuccess ||
             occ < 1)
             return QG_ECUDA;
-        occ_cache[dev] = occ;
-        attr_done[dev] = true;
+        occ_cache[dev].store(occ, std::memory_order_relaxed);
+        attr_done[dev].store(true, std::memory_order_release);  // publishes occ_cache[dev]
     }
     const int sms = sm_count(dev);
     if (sms <= 0) return QG_ECUDA;
-    const int grid = sms * std::min(occ_cache[dev], 2);
+    const int grid = sms * std::min(occ_cache[dev].load(std::memory_order_relaxed), 2);
     if (cudaMemsetAsync(sync, 0, sizeof(unsigned) * plan.nstages, s) != cudaSuccess) return QG_ECUDA;
     void* args[] = {const_cast<pass::Plan*>(&plan), &M, &sync, &stages, &status};
     if (cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(kern), dim3(grid), dim3(kCols * 32 + 32), args,

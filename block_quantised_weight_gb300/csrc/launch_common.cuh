@@ -1,6 +1,7 @@
 // Host-side helpers shared by the GEMV launchers.
 #pragma once
 #include <algorithm>
+#include <atomic>
 
 #include "gemv_kernel.cuh"
 #include "launch.h"
@@ -14,15 +15,17 @@ inline int current_device() {
     return dev;
 }
 
+// Per-device values computed on first use.  Host threads may race to fill a
+// slot; they all store the same value, and atomics keep that well defined.
 inline int sm_count(int dev) {
-    static int cache[64];
+    static std::atomic<int> cache[64];
     if (dev < 0 || dev >= 64) return 0;
-    if (cache[dev] == 0) {
-        int n = 0;
+    int n = cache[dev].load(std::memory_order_relaxed);
+    if (n == 0) {
         if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
-        cache[dev] = n;
+        cache[dev].store(n, std::memory_order_relaxed);
     }
-    return cache[dev];
+    return n;
 }
 
 // Launch gemv_kernel<F, MT, RG, MINB, FUSE> over `count` matrices that
@@ -33,17 +36,17 @@ template <class F, int MT, int RG, int MINB, int FUSE = 0>
 int launch_gemv(const uint8_t* const* W, float* const* Y, const int64_t* N, int count, int m0, const uint8_t* grid,
                 const float* X, int M, int64_t K, cudaStream_t s, unsigned* status, int dev, unsigned flags,
                 int csize = 1, const Fuse* fz = nullptr) {
-    static bool attr_done[64];
+    static std::atomic<bool> attr_done[64];
     const int budget = std::min(kSmemPerCTA, kSmemPerSM / MINB - kSmemReserve);
     const Layout L1 = make_layout(F::kIQ3, MT, F::kXH, RG, 1, F::kRowStride, F::kCols, FUSE);
     const int stages_fit = std::min(kMaxStages, (budget - L1.stage0) / L1.stage_bytes);
     if (stages_fit < 2) return QG_EINVAL;
     auto kern = gemv_kernel<F, MT, RG, MINB, FUSE>;
-    if (!attr_done[dev]) {
+    if (!attr_done[dev].load(std::memory_order_acquire)) {
         const Layout Lmax = make_layout(F::kIQ3, MT, F::kXH, RG, stages_fit, F::kRowStride, F::kCols, FUSE);
         if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Lmax.total) != cudaSuccess)
             return QG_ECUDA;
-        attr_done[dev] = true;
+        attr_done[dev].store(true, std::memory_order_release);
     }
     // prologue operands and residuals (token offset m0 applied like X, Y)
     Fuse Fz = {};

@@ -5,12 +5,14 @@
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <cstdint>
 
 namespace qg {
 
 inline PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::atomic<PFN_cuTensorMapEncodeTiled_v12000> cached{nullptr};  // racing threads store the same value
+    PFN_cuTensorMapEncodeTiled_v12000 fn = cached.load(std::memory_order_relaxed);
     if (!fn) {
         void* p = nullptr;
         cudaDriverEntryPointQueryResult q;
@@ -19,6 +21,7 @@ inline PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
             q != cudaDriverEntryPointSuccess)
             return nullptr;
         fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+        cached.store(fn, std::memory_order_relaxed);
     }
     return fn;
 }
