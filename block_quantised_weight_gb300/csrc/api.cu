@@ -49,11 +49,11 @@ unsigned* g_noalloc_ptr[64];
 // qg_noalloc_scratch.
 int noalloc_scratch(unsigned** out) {
     int dev = -1;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return QG_ECUDA;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return qg::cuda_fail(cudaGetLastError());
     std::lock_guard<std::mutex> lock(g_noalloc_mu);
     if (!g_noalloc_ptr[dev]) {
         void* p = nullptr;
-        if (cudaGetSymbolAddress(&p, qg_noalloc_scratch) != cudaSuccess || !p) return QG_ECUDA;
+        if (cudaGetSymbolAddress(&p, qg_noalloc_scratch) != cudaSuccess || !p) return qg::cuda_fail(cudaGetLastError());
         g_noalloc_ptr[dev] = static_cast<unsigned*>(p);
     }
     *out = g_noalloc_ptr[dev];
@@ -114,7 +114,7 @@ int qgemv_q4k_ex(const uint8_t* W, const float* X, float* Y, int M, int64_t N, i
     int rc = check_gemv(W, nullptr, false, X, Y, M, N, K, 144);
     if (rc != QG_OK) return rc;
     unsigned* st = status_ptr();
-    if (!st) return QG_ECUDA;
+    if (!st) return qg::cuda_fail(cudaGetLastError());
     return qg::launch_gemv_q4k(W, X, Y, M, N, K, stream, st, flags);
 }
 
@@ -128,7 +128,7 @@ int qgemv_iq3_ex(const uint8_t* W, const uint8_t* grid, const float* X, float* Y
     int rc = check_gemv(W, grid, true, X, Y, M, N, K, 98);
     if (rc != QG_OK) return rc;
     unsigned* st = status_ptr();
-    if (!st) return QG_ECUDA;
+    if (!st) return qg::cuda_fail(cudaGetLastError());
     return qg::launch_gemv_iq3(W, grid, X, Y, M, N, K, stream, st, flags);
 }
 
@@ -143,7 +143,7 @@ int qgemv_iq3xxs_ex(const uint8_t* W, const uint8_t* grid, const float* X, float
     int rc = check_gemv(W, grid, true, X, Y, M, N, K, 98);
     if (rc != QG_OK) return rc;
     unsigned* st = status_ptr();
-    if (!st) return QG_ECUDA;
+    if (!st) return qg::cuda_fail(cudaGetLastError());
     return qg::launch_gemv_iq3xxs(W, grid, X, Y, M, N, K, stream, st, flags);
 }
 
@@ -165,7 +165,7 @@ int qgemv_codebook(int format, const uint8_t* W, const void* codebook, const flo
     if (!aligned16(book)) return QG_EALIGN;
     if (overlap(Y, int64_t(M) * N * 4, book, codebook_bytes(format))) return QG_EALIAS;
     unsigned* st = status_ptr();
-    if (!st) return QG_ECUDA;
+    if (!st) return qg::cuda_fail(cudaGetLastError());
     return qg::launch_gemv_cb(format, W, book, X, Y, M, N, K, stream, st);
 }
 
@@ -205,7 +205,7 @@ int qgemv_q4k_group(const uint8_t* const* W, float* const* Y, const int64_t* N, 
     int rc = check_group(W, Y, N, count, nullptr, false, X, M, K, 144);
     if (rc != QG_OK) return rc;
     unsigned* st = status_ptr();
-    if (!st) return QG_ECUDA;
+    if (!st) return qg::cuda_fail(cudaGetLastError());
     return qg::launch_group_q4k(W, Y, N, count, X, M, K, stream, st, flags, nullptr);
 }
 
@@ -252,7 +252,7 @@ int qgemv_q4k_fused_group(const uint8_t* const* W, float* const* Y, const int64_
     rc = check_fuse(fuse, Y, N, count, M, K);
     if (rc != QG_OK) return rc;
     unsigned* st = status_ptr();
-    if (!st) return QG_ECUDA;
+    if (!st) return qg::cuda_fail(cudaGetLastError());
     const qg::Fuse z = to_fuse(fuse);
     return qg::launch_group_q4k_fused(W, Y, N, count, X, M, K, stream, st, flags, z);
 }
@@ -271,7 +271,7 @@ int qgemv_iq3_group(const uint8_t* const* W, float* const* Y, const int64_t* N, 
     int rc = check_group(W, Y, N, count, grid, true, X, M, K, 98);
     if (rc != QG_OK) return rc;
     unsigned* st = status_ptr();
-    if (!st) return QG_ECUDA;
+    if (!st) return qg::cuda_fail(cudaGetLastError());
     return qg::launch_group_iq3(W, Y, N, count, grid, X, M, K, stream, st, flags);
 }
 
@@ -288,7 +288,7 @@ int qgemv_q4k_pass(const qg_stage* stages, int nstages, int M, unsigned* sync, c
                 return QG_EALIAS;
     }
     unsigned* st = status_ptr();
-    if (!st) return QG_ECUDA;
+    if (!st) return qg::cuda_fail(cudaGetLastError());
     return qg::launch_pass_q4k(stages, nstages, M, sync, stream, st);
 }
 
@@ -301,7 +301,7 @@ int qgemv_q4k_pass_noalloc(const qg_stage* stages, int nstages, int M, cudaStrea
         if (rc != QG_OK) return rc;
     }
     unsigned* st = status_ptr();
-    if (!st) return QG_ECUDA;
+    if (!st) return qg::cuda_fail(cudaGetLastError());
     unsigned* scratch = nullptr;
     const int rc = noalloc_scratch(&scratch);
     if (rc != QG_OK) return rc;
@@ -313,7 +313,7 @@ int qgemm_q4k_batched(const uint8_t* W, const float* X, float* Y, int M, int64_t
     int rc = check_gemv(W, nullptr, false, X, Y, M, N, K, 144);
     if (rc != QG_OK) return rc;
     unsigned* st = status_ptr();
-    if (!st) return QG_ECUDA;
+    if (!st) return qg::cuda_fail(cudaGetLastError());
     if (M < 16) return qg::launch_gemv_q4k(W, X, Y, M, N, K, stream, st, 0u);
     return qg::launch_gemm_q4k_tc(W, X, Y, M, N, K, stream, st);
 }
@@ -323,7 +323,7 @@ int qgemm_iq3_batched(const uint8_t* W, const uint8_t* grid, const float* X, flo
     int rc = check_gemv(W, grid, true, X, Y, M, N, K, 98);
     if (rc != QG_OK) return rc;
     unsigned* st = status_ptr();
-    if (!st) return QG_ECUDA;
+    if (!st) return qg::cuda_fail(cudaGetLastError());
     if (M < 16 || (K / 256) % 8 != 0) return qg::launch_gemv_iq3(W, grid, X, Y, M, N, K, stream, st, 0u);
     return qg::launch_gemm_iq3_tc(W, grid, X, Y, M, N, K, stream, st);
 }
@@ -347,10 +347,10 @@ int qdequant_iq3xxs(const uint8_t* W, const uint8_t* grid, float* out, int64_t N
 }
 
 int qg_device_status(cudaStream_t stream) {
-    if (cudaStreamSynchronize(stream) != cudaSuccess) return QG_ECUDA;
+    if (cudaStreamSynchronize(stream) != cudaSuccess) return qg::cuda_fail(cudaGetLastError());
     unsigned v = 0, zero = 0;
-    if (cudaMemcpyFromSymbol(&v, qg_status_word, sizeof(v)) != cudaSuccess) return QG_ECUDA;
-    if (v != 0 && cudaMemcpyToSymbol(qg_status_word, &zero, sizeof(zero)) != cudaSuccess) return QG_ECUDA;
+    if (cudaMemcpyFromSymbol(&v, qg_status_word, sizeof(v)) != cudaSuccess) return qg::cuda_fail(cudaGetLastError());
+    if (v != 0 && cudaMemcpyToSymbol(qg_status_word, &zero, sizeof(zero)) != cudaSuccess) return qg::cuda_fail(cudaGetLastError());
     if (v & qg::kStatusTimeout) return QG_ETIMEOUT;
     if (v & qg::kStatusBounds) return QG_EBOUNDS;
     return QG_OK;
@@ -358,9 +358,9 @@ int qg_device_status(cudaStream_t stream) {
 
 int qg_test_bounded_wait(cudaStream_t stream) {
     unsigned* st = status_ptr();
-    if (!st) return QG_ECUDA;
+    if (!st) return qg::cuda_fail(cudaGetLastError());
     bounded_wait_probe<<<1, 32, 0, stream>>>(st);
-    return cudaGetLastError() == cudaSuccess ? QG_OK : QG_ECUDA;
+    return qg::launch_status();
 }
 
 int qg_test_chain_step(const float* X, float* Y, int64_t K, int grid, unsigned flags, cudaStream_t stream) {
@@ -370,6 +370,8 @@ int qg_test_chain_step(const float* X, float* Y, int64_t K, int grid, unsigned f
     if (overlap(Y, int64_t(grid) * 32 * 4, X, K * 4)) return QG_EALIAS;
     return qg::launch_chain_step(X, Y, K, grid, flags, stream);
 }
+
+int qg_last_cuda_error(void) { return qg::t_last_cuda_error; }
 
 const char* qg_strerror(int status) {
     switch (status) {

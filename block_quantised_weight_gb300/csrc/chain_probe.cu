@@ -34,8 +34,8 @@ int launch_chain_step(const float* X, float* Y, int64_t K, int grid, unsigned fl
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = (flags & QG_PREFETCH_WEIGHTS) ? 1 : 0;
-    if (cudaLaunchKernelEx(&cfg, chain_step_kernel, X, Y, K) != cudaSuccess) return QG_ECUDA;
-    return cudaGetLastError() == cudaSuccess ? QG_OK : QG_ECUDA;
+    if (cudaLaunchKernelEx(&cfg, chain_step_kernel, X, Y, K) != cudaSuccess) return qg::cuda_fail(cudaGetLastError());
+    return launch_status();
 }
 
 }  // namespace qg

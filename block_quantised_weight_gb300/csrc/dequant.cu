@@ -58,14 +58,14 @@ int launch_dequant_q4k(const uint8_t* W, float* out, int64_t N, int64_t K, cudaS
     const int64_t nblocks = N * (K / 256);
     const int64_t threads = nblocks * 4;
     dequant_q4k_kernel<<<static_cast<unsigned>((threads + 255) / 256), 256, 0, s>>>(W, out, nblocks);
-    return cudaGetLastError() == cudaSuccess ? QG_OK : QG_ECUDA;
+    return launch_status();
 }
 
 int launch_dequant_iq3(const uint8_t* W, const uint8_t* grid, float* out, int64_t N, int64_t K, cudaStream_t s) {
     const int64_t nblocks = N * (K / 256);
     const int64_t threads = nblocks * 8;
     dequant_iq3_kernel<FmtIQ3T><<<static_cast<unsigned>((threads + 255) / 256), 256, 0, s>>>(W, grid, out, nblocks);
-    return cudaGetLastError() == cudaSuccess ? QG_OK : QG_ECUDA;
+    return launch_status();
 }
 
 int launch_dequant_iq3xxs(const uint8_t* W, const uint8_t* grid, float* out, int64_t N, int64_t K, cudaStream_t s) {
@@ -73,7 +73,7 @@ int launch_dequant_iq3xxs(const uint8_t* W, const uint8_t* grid, float* out, int
     const int64_t threads = nblocks * 8;
     dequant_iq3_kernel<FmtIQ3XXST><<<static_cast<unsigned>((threads + 255) / 256), 256, 0, s>>>(W, grid, out,
                                                                                               nblocks);
-    return cudaGetLastError() == cudaSuccess ? QG_OK : QG_ECUDA;
+    return launch_status();
 }
 
 }  // namespace qg

@@ -462,7 +462,7 @@ int launch_tc(const uint8_t* W, const uint8_t* grid, const float* X, float* Y, i
     if (M < 16 || M > 32) return QG_EINVAL;
     static std::atomic<bool> attr_done[64];
     int dev = -1;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return QG_ECUDA;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return qg::cuda_fail(cudaGetLastError());
     // as many raw stages as fit (the x part of a stage is M KB)
     const int raw0 = IQ3 ? tc::kRaw0IQ3 : tc::kRaw0Q4K;
     const int nraw = std::min(tc::kMaxRaw, (tc::kSmemMax - raw0) / tc::raw_stage_bytes(M));
@@ -471,16 +471,16 @@ int launch_tc(const uint8_t* W, const uint8_t* grid, const float* X, float* Y, i
     if (!attr_done[dev].load(std::memory_order_acquire)) {
         if (cudaFuncSetAttribute(tc::gemm_tc_kernel<IQ3>, cudaFuncAttributeMaxDynamicSharedMemorySize, tc::kSmemMax) !=
             cudaSuccess)
-            return QG_ECUDA;
+            return qg::cuda_fail(cudaGetLastError());
         attr_done[dev].store(true, std::memory_order_release);
     }
     auto encode = tensor_map_encoder();
-    if (!encode) return QG_ECUDA;
+    if (!encode) return qg::cuda_fail(cudaGetLastError());
     const uint64_t pitch = static_cast<uint64_t>(K / 256) * (IQ3 ? 98 : tc::kBlockBytes);
     CUtensorMap tmW, tmX;
     if (!encode_byte_rows(&tmW, W, pitch, static_cast<uint64_t>(N), IQ3 ? tc::kIQ3Box : tc::kBlockBytes,
                           tc::kTileRows))
-        return QG_ECUDA;
+        return qg::cuda_fail(cudaGetLastError());
     {
         const cuuint64_t gdim[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(M)};
         const cuuint64_t gstride[1] = {static_cast<cuuint64_t>(K) * 4};
@@ -489,16 +489,16 @@ int launch_tc(const uint8_t* W, const uint8_t* grid, const float* X, float* Y, i
         if (encode(&tmX, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float*>(X), gdim, gstride, box, estr,
                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-            return QG_ECUDA;
+            return qg::cuda_fail(cudaGetLastError());
     }
     int sms = 0;
     if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0)
-        return QG_ECUDA;
-    if (cudaMemsetAsync(Y, 0, static_cast<size_t>(M) * N * sizeof(float), s) != cudaSuccess) return QG_ECUDA;
+        return qg::cuda_fail(cudaGetLastError());
+    if (cudaMemsetAsync(Y, 0, static_cast<size_t>(M) * N * sizeof(float), s) != cudaSuccess) return qg::cuda_fail(cudaGetLastError());
     const int64_t units = ((N + tc::kTileRows - 1) / tc::kTileRows) * (K / 256);
     const int gridx = static_cast<int>(std::min<int64_t>(units, sms));
     tc::gemm_tc_kernel<IQ3><<<gridx, tc::kThreads, smem, s>>>(tmW, tmX, grid, Y, M, N, K, nraw, status);
-    return cudaGetLastError() == cudaSuccess ? QG_OK : QG_ECUDA;
+    return launch_status();
 }
 
 }  // namespace

@@ -509,18 +509,18 @@ int launch_tma(const uint8_t* W, const void* book, const float* X, float* Y, int
         if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  std::min(kSmemPerCTA, kCbRing0 + kCbMaxStages * cb_stage_bytes(F, MT))) !=
             cudaSuccess)
-            return QG_ECUDA;
+            return qg::cuda_fail(cudaGetLastError());
         attr_done[dev].store(true, std::memory_order_release);
     }
     CUtensorMap tm;
     const uint64_t pitch = static_cast<uint64_t>(K / 256) * unit_bytes(F);
-    if (!encode_byte_rows(&tm, W, pitch, static_cast<uint64_t>(N), Box<F>::kBox, 32)) return QG_ECUDA;
+    if (!encode_byte_rows(&tm, W, pitch, static_cast<uint64_t>(N), Box<F>::kBox, 32)) return qg::cuda_fail(cudaGetLastError());
     const int64_t ntiles = (N + 31) / 32;
     const int grid = static_cast<int>(std::min<int64_t>(ntiles, static_cast<int64_t>(sms) * MINB));
     const int64_t units_per_cta = (ntiles + grid - 1) / grid * ((K / 256 + kCbCols - 1) / kCbCols);
     const int st = static_cast<int>(std::min<int64_t>(stages, std::max<int64_t>(2, units_per_cta)));
     kern<<<grid, kCbCols * 32 + 32, kCbRing0 + st * cb_stage_bytes(F, MT), s>>>(tm, book, X, Y, M, N, K, st, status);
-    return cudaGetLastError() == cudaSuccess ? QG_OK : QG_ECUDA;
+    return launch_status();
 }
 
 // Test-only: every sub-block's 32 values (exact), one thread per sub-block.
@@ -546,9 +546,9 @@ template <int F>
 int launch_t(const uint8_t* W, const void* book, const float* X, float* Y, int M, int64_t N, int64_t K,
              cudaStream_t s, unsigned* status) {
     const int dev = current_device();
-    if (dev < 0) return QG_ECUDA;
+    if (dev < 0) return qg::cuda_fail(cudaGetLastError());
     const int sms = sm_count(dev);
-    if (sms <= 0) return QG_ECUDA;
+    if (sms <= 0) return qg::cuda_fail(cudaGetLastError());
     if constexpr (F == kIQ4NL || F == kIQ4XS) {
         if (tma_ok(F, K)) {
             // groups of at most 4 tokens, each streaming W once
@@ -574,7 +574,7 @@ int launch_t(const uint8_t* W, const void* book, const float* X, float* Y, int M
             gemv_cb_kernel<F, 4><<<blocks, 256, 0, s>>>(W, book, Xg, Yg, mg, N, K);
         else
             gemv_cb_kernel<F, 8><<<blocks, 256, 0, s>>>(W, book, Xg, Yg, mg, N, K);
-        if (cudaGetLastError() != cudaSuccess) return QG_ECUDA;
+        if (cudaGetLastError() != cudaSuccess) return qg::cuda_fail(cudaGetLastError());
     }
     return QG_OK;
 }
@@ -583,7 +583,7 @@ template <int F>
 int dequant_t(const uint8_t* W, const void* book, float* out, int64_t N, int64_t K, cudaStream_t s) {
     const int64_t threads = N * (K / 32);
     dequant_cb_kernel<F><<<static_cast<unsigned>((threads + 255) / 256), 256, 0, s>>>(W, book, out, N, K);
-    return cudaGetLastError() == cudaSuccess ? QG_OK : QG_ECUDA;
+    return launch_status();
 }
 
 }  // namespace cb

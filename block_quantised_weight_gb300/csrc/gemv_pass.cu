@@ -231,30 +231,30 @@ int launch_pass_t(const pass::Plan& plan, int M, unsigned* sync, cudaStream_t s,
     auto kern = pass::gemv_pass_kernel<MT>;
     if (!attr_done[dev].load(std::memory_order_acquire)) {
         if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L.total) != cudaSuccess)
-            return QG_ECUDA;
+            return qg::cuda_fail(cudaGetLastError());
         int occ = 0;
         if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, kCols * 32 + 32, L.total) != cudaSuccess ||
             occ < 1)
-            return QG_ECUDA;
+            return qg::cuda_fail(cudaGetLastError());
         occ_cache[dev].store(occ, std::memory_order_relaxed);
         attr_done[dev].store(true, std::memory_order_release);  // publishes occ_cache[dev]
     }
     const int sms = sm_count(dev);
-    if (sms <= 0) return QG_ECUDA;
+    if (sms <= 0) return qg::cuda_fail(cudaGetLastError());
     const int grid = sms * std::min(occ_cache[dev].load(std::memory_order_relaxed), 2);
-    if (cudaMemsetAsync(sync, 0, sizeof(unsigned) * plan.nstages, s) != cudaSuccess) return QG_ECUDA;
+    if (cudaMemsetAsync(sync, 0, sizeof(unsigned) * plan.nstages, s) != cudaSuccess) return qg::cuda_fail(cudaGetLastError());
     void* args[] = {const_cast<pass::Plan*>(&plan), &M, &sync, &stages, &status};
     if (cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(kern), dim3(grid), dim3(kCols * 32 + 32), args,
                                     L.total, s) != cudaSuccess)
-        return QG_ECUDA;
-    return cudaGetLastError() == cudaSuccess ? QG_OK : QG_ECUDA;
+        return qg::cuda_fail(cudaGetLastError());
+    return launch_status();
 }
 
 }  // namespace
 
 int launch_pass_q4k(const qg_stage* stages, int nstages, int M, unsigned* sync, cudaStream_t s, unsigned* status) {
     const int dev = current_device();
-    if (dev < 0) return QG_ECUDA;
+    if (dev < 0) return qg::cuda_fail(cudaGetLastError());
     thread_local pass::Plan plan;  // ~16 KB, kept off the stack; copied into the launch's parameters
     plan.nstages = nstages;
     for (int i = 0; i < nstages; ++i) {

@@ -8,6 +8,19 @@
 
 namespace qg {
 
+// The CUDA error behind the calling host thread's last QG_ECUDA (0 when the
+// failing step was not a CUDA runtime call, e.g. a tensor-map encoding).
+inline thread_local int t_last_cuda_error = 0;
+inline int cuda_fail(cudaError_t e) {
+    t_last_cuda_error = static_cast<int>(e);
+    return QG_ECUDA;
+}
+// Status of the launch just made on this thread: QG_OK or QG_ECUDA (recorded).
+inline int launch_status() {
+    const cudaError_t e = cudaGetLastError();
+    return e == cudaSuccess ? QG_OK : cuda_fail(e);
+}
+
 int launch_gemv_q4k(const uint8_t* W, const float* X, float* Y, int M, int64_t N, int64_t K, cudaStream_t s,
                     unsigned* status, unsigned flags);
 int launch_gemv_iq3(const uint8_t* W, const uint8_t* grid, const float* X, float* Y, int M, int64_t N, int64_t K,

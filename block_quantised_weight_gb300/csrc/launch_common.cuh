@@ -45,7 +45,7 @@ int launch_gemv(const uint8_t* const* W, float* const* Y, const int64_t* N, int 
     if (!attr_done[dev].load(std::memory_order_acquire)) {
         const Layout Lmax = make_layout(F::kIQ3, MT, F::kXH, RG, stages_fit, F::kRowStride, F::kCols, FUSE);
         if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Lmax.total) != cudaSuccess)
-            return QG_ECUDA;
+            return qg::cuda_fail(cudaGetLastError());
         attr_done[dev].store(true, std::memory_order_release);
     }
     // prologue operands and residuals (token offset m0 applied like X, Y)
@@ -71,12 +71,12 @@ int launch_gemv(const uint8_t* const* W, float* const* Y, const int64_t* N, int 
         const uint64_t pitch = static_cast<uint64_t>(K / 256) * F::kBytes;
         for (int i = 0; i < count; ++i)
             if (!encode_byte_rows(&T.m[i], W[i], pitch, static_cast<uint64_t>(N[i]), F::kBoxBytes, RG * kRows))
-                return QG_ECUDA;
+                return qg::cuda_fail(cudaGetLastError());
     }
-    if (F::kXH == kXHalf && !encode_x_halves(&T.xm, X, static_cast<uint64_t>(M) * static_cast<uint64_t>(K / 128))) return QG_ECUDA;
+    if (F::kXH == kXHalf && !encode_x_halves(&T.xm, X, static_cast<uint64_t>(M) * static_cast<uint64_t>(K / 128))) return qg::cuda_fail(cudaGetLastError());
     const int64_t ntiles = G.tile0[count];
     const int sms = sm_count(dev);
-    if (sms <= 0) return QG_ECUDA;
+    if (sms <= 0) return qg::cuda_fail(cudaGetLastError());
     // csize > 1: one CTA per (tile, K chunk), the chunks of a tile in one
     // cluster (the caller checks that the grid fits one wave).
     const int grid_x = csize > 1 ? static_cast<int>(ntiles * csize)
@@ -92,7 +92,7 @@ int launch_gemv(const uint8_t* const* W, float* const* Y, const int64_t* N, int 
                        (csize > 1 ? csize << kFlagClusterShift : 0);
     if (!(flags & QG_PREFETCH_WEIGHTS) && csize <= 1) {
         kern<<<grid_x, RG * F::kCols * 32 + 32, L.total, s>>>(G, T, Fz, grid, X, M, K, stages, status, kflags);
-        return cudaGetLastError() == cudaSuccess ? QG_OK : QG_ECUDA;
+        return launch_status();
     }
     // programmatic dependent launch (this grid may start before the previous
     // kernel in the stream finishes; the kernel waits before reading x) and/or
@@ -119,8 +119,8 @@ int launch_gemv(const uint8_t* const* W, float* const* Y, const int64_t* N, int 
     cfg.attrs = attr;
     cfg.numAttrs = na;
     if (cudaLaunchKernelEx(&cfg, kern, G, T, Fz, grid, X, M, K, stages, status, kflags) != cudaSuccess)
-        return QG_ECUDA;
-    return cudaGetLastError() == cudaSuccess ? QG_OK : QG_ECUDA;
+        return qg::cuda_fail(cudaGetLastError());
+    return launch_status();
 }
 
 }  // namespace qg

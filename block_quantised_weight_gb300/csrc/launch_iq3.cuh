@@ -67,18 +67,18 @@ template <class F>
 int launch_group_iq3_t(const uint8_t* const* W, float* const* Y, const int64_t* N, int count, const uint8_t* grid,
                        const float* X, int M, int64_t K, cudaStream_t s, unsigned* status, unsigned flags) {
     const int dev = current_device();
-    if (dev < 0) return QG_ECUDA;
+    if (dev < 0) return qg::cuda_fail(cudaGetLastError());
     if ((K / 256) % 8 != 0) {
         // rows not 16-byte aligned: the byte-addressed kernel, up to 8 tokens per pass
         const int sms = sm_count(dev);
-        if (sms <= 0) return QG_ECUDA;
+        if (sms <= 0) return qg::cuda_fail(cudaGetLastError());
         for (int m0 = 0; m0 < M; m0 += 8) {
             const int mg = std::min(8, M - m0);
             for (int i = 0; i < count; ++i) {
                 const int64_t blocks = std::min<int64_t>((N[i] + 7) / 8, static_cast<int64_t>(sms) * 8);
                 gemv_iq3_bytes_kernel<F><<<static_cast<int>(blocks), 256, 0, s>>>(
                     W[i], grid, X + static_cast<int64_t>(m0) * K, Y[i] + m0 * N[i], mg, N[i], K);
-                if (cudaGetLastError() != cudaSuccess) return QG_ECUDA;
+                if (cudaGetLastError() != cudaSuccess) return qg::cuda_fail(cudaGetLastError());
             }
         }
         return QG_OK;

@@ -14,7 +14,7 @@ template <int FUSE>
 int launch_group_q4k_t(const uint8_t* const* W, float* const* Y, const int64_t* N, int count, const float* X, int M,
                        int64_t K, cudaStream_t s, unsigned* status, unsigned flags, const Fuse* fz) {
     const int dev = current_device();
-    if (dev < 0) return QG_ECUDA;
+    if (dev < 0) return qg::cuda_fail(cudaGetLastError());
     if (FUSE != 0 && M > 4) return QG_EINVAL;
     // Launches with at most one 32-row tile per SM are latency-bound: run them
     // one CTA per SM with the deepest ring that fits.

@@ -11,6 +11,15 @@
 namespace qg {
 
 inline PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+    // The encoder is a driver call and needs a context current on this host
+    // thread; the runtime binds one lazily, so a thread whose first CUDA call
+    // is ours (cudaGetDevice does not bind) would fail.  A runtime no-op that
+    // initialises binds the device's primary context, once per thread.
+    static thread_local bool bound = false;
+    if (!bound) {
+        if (cudaFree(nullptr) != cudaSuccess) return nullptr;
+        bound = true;
+    }
     static std::atomic<PFN_cuTensorMapEncodeTiled_v12000> cached{nullptr};  // racing threads store the same value
     PFN_cuTensorMapEncodeTiled_v12000 fn = cached.load(std::memory_order_relaxed);
     if (!fn) {

@@ -44,13 +44,15 @@ QG_CB = {"iq4nl": 1, "iq4xs": 2, "iq3s": 3, "iq2xxs": 4}
 CB_UNIT_BYTES = {"iq4nl": 144, "iq4xs": 136, "iq3s": 110, "iq2xxs": 66}
 
 EXPORTS = ("qgemv_q4k", "qgemv_q4k_ex", "qgemv_q4k_group", "qgemv_q4k_fused", "qgemv_q4k_fused_group", "qgemv_q4k_pass", "qgemv_q4k_pass_noalloc", "qgemv_iq3", "qgemv_iq3_ex", "qgemv_iq3_group", "qgemv_iq3xxs", "qgemv_iq3xxs_ex", "qdequant_iq3xxs", "qgemv_codebook", "qdequant_codebook", "qgemm_q4k_batched", "qgemm_iq3_batched", "qdequant_q4k", "qdequant_iq3",
-           "qg_device_status", "qg_test_bounded_wait", "qg_test_chain_step", "qg_strerror")
+           "qg_device_status", "qg_test_bounded_wait", "qg_test_chain_step", "qg_strerror", "qg_last_cuda_error")
 
 
 class QGError(RuntimeError):
-    def __init__(self, fn: str, code: int):
+    def __init__(self, fn: str, code: int, cuda_error: int = 0):
         self.code = code
-        super().__init__(f"{fn} failed: {code} ({strerror(code)})")
+        self.cuda_error = cuda_error
+        extra = f"; cudaError {cuda_error}" if code == QG_ECUDA and cuda_error else ""
+        super().__init__(f"{fn} failed: {code} ({strerror(code)}{extra})")
 
 
 def library_path() -> str:
@@ -92,6 +94,7 @@ def load():
             "qg_test_bounded_wait": [vp],
             "qg_test_chain_step": [vp, vp, i64, ci, ctypes.c_uint, vp],
             "qg_strerror": [ci],
+            "qg_last_cuda_error": [],
         }
         for name, args in sigs.items():
             f = getattr(lib, name)
@@ -117,7 +120,8 @@ def _stream(stream):
 
 def _check(fn, rc):
     if rc != QG_OK:
-        raise QGError(fn, rc)
+        # the CUDA error behind a QG_ECUDA, recorded for this host thread
+        raise QGError(fn, rc, int(load().qg_last_cuda_error()) if rc == QG_ECUDA else 0)
 
 
 def _req(t, dtype, name):

@@ -266,7 +266,10 @@ QG_API int qgemv_q4k_pass_noalloc(const qg_stage* stages, int nstages, int M, cu
  * (tolerance 1e-5 * sum|w*x|); M >= 16 dequantises W tiles to bf16 (round to
  * nearest even) in shared memory and multiplies on the tcgen05 tensor cores
  * with fp32 accumulation in tensor memory, X also rounded to bf16
- * (tolerance 4e-3 * sum|w*x|). */
+ * (tolerance 4e-3 * sum|w*x|).  On this path Y is zeroed on `stream` and the
+ * row sums of K ranges that different CTAs share are added into it with fp32
+ * atomics, so repeated calls may differ in the last bits (the FMA paths are
+ * deterministic). */
 QG_API int qgemm_q4k_batched(const uint8_t* W, const float* X, float* Y, int M, int64_t N, int64_t K, cudaStream_t stream);
 
 /* Batched IQ3 GEMM for decode batches, 1 <= M <= 32.  Same operation,
@@ -274,8 +277,9 @@ QG_API int qgemm_q4k_batched(const uint8_t* W, const float* X, float* Y, int M, 
  * dequantises W tiles to bf16 (round to nearest even; every IQ3 value is
  * exact in fp32 first, page 4 "iq3_pack.py", decode) in shared memory and
  * multiplies on the tcgen05 tensor cores with fp32 accumulation in tensor
- * memory, X also rounded to bf16 (tolerance 4e-3 * sum|w*x|); otherwise the
- * fp32 FMA path of qgemv_iq3 (1e-5 * sum|w*x|). */
+ * memory, X also rounded to bf16 (tolerance 4e-3 * sum|w*x|; fp32 atomics
+ * as in qgemm_q4k_batched, so not bit-reproducible); otherwise the fp32 FMA
+ * path of qgemv_iq3 (1e-5 * sum|w*x|). */
 QG_API int qgemm_iq3_batched(const uint8_t* W, const uint8_t* grid, const float* X, float* Y, int M, int64_t N,
                              int64_t K, cudaStream_t stream);
 
@@ -315,6 +319,12 @@ QG_API int qg_test_chain_step(const float* X, float* Y, int64_t K, int grid, uns
 
 /* Static description of a status code. */
 QG_API const char* qg_strerror(int status);
+
+/* The cudaError_t of the CUDA runtime call behind the calling host thread's
+ * most recent QG_ECUDA (0 if that failure was not a runtime call, e.g. a
+ * tensor-map encoding; 0 before any).  Per host thread; other status codes
+ * leave it unchanged. */
+QG_API int qg_last_cuda_error(void);
 
 #ifdef __cplusplus
 }

@@ -463,3 +463,52 @@ def test_chain_step_probe(q):
         torch.cuda.synchronize()
         assert torch.allclose(y.double(), torch.full_like(y.double(), _probe_value(x)), rtol=1e-5)
         assert torch.allclose(y2.double(), torch.full_like(y2.double(), _probe_value(y[:K])), rtol=1e-5)
+
+
+def test_concurrent_host_threads(q):
+    """Eight host threads calling four entry points at once, each on its own
+    stream (the binding releases the GIL for the C call), get the results of
+    the same calls made one at a time.  A thread whose first CUDA call is the
+    library's must work too: the tensor-map encoder is a driver call that
+    needs the runtime's context bound to the thread."""
+    import threading
+    K, N = 2048, 300
+    Wq = dev(synth.gen_q4k(N, K, 11))
+    Wi_np, grid_np = synth.gen_iq3(N, K, 12)
+    Wi, grid = dev(Wi_np), dev(grid_np)
+    Wc_np, tab_np = synth.gen_cb("iq4nl", N, K, 13)
+    Wc, tab = dev(Wc_np), dev(tab_np)
+    x1 = dev(synth.gen_x(1, K, 14))
+    x16 = dev(synth.gen_x(16, K, 15))
+    calls = [lambda s: q.qgemv_q4k(Wq, x1, stream=s),
+             lambda s: q.qgemv_iq3(Wi, grid, x1, stream=s),
+             lambda s: q.qgemv_codebook("iq4nl", Wc, tab, x1, stream=s),
+             lambda s: q.qgemm_q4k_batched(Wq, x16, stream=s)]
+    ref = []
+    for c in calls:
+        ref.append(c(None).cpu())
+    torch.cuda.synchronize()
+    outs, errs = [None] * 8, []
+
+    def run(i):
+        try:
+            s = torch.cuda.Stream()
+            y = calls[i % 4](s)
+            s.synchronize()
+            outs[i] = y.cpu()
+        except Exception as e:  # reported below
+            errs.append(e)
+
+    ts = [threading.Thread(target=run, args=(i,)) for i in range(8)]
+    for t in ts:
+        t.start()
+    for t in ts:
+        t.join()
+    assert not errs, errs
+    for i, y in enumerate(outs):
+        r = ref[i % 4]
+        if i % 4 == 3:  # tcgen05 path: split tiles meet in fp32 atomics, summation order varies
+            assert torch.allclose(y, r, rtol=1e-5, atol=1e-6 * float(r.abs().max())), i
+        else:           # FMA paths: deterministic
+            assert torch.equal(y, r), i
+    assert q.qg_device_status() == 0
