@@ -222,10 +222,11 @@ __device__ __forceinline__ float half_hi(uint32_t h) {
 }
 
 // SiLU (page 2 "Candle", Block::forward's silu): z * sigmoid(z).
-// exp by the fast hardware path (__expf: relative error of a few ulp, far
-// inside the GEMV's 1e-5 tolerance); exp(-z) = inf for z << 0 gives z / inf
-// = -0, the limit.
-__device__ __forceinline__ float silu(float z) { return z / (1.f + __expf(-z)); }
+// exp and the division by the fast hardware paths (__expf, __fdividef:
+// relative errors of a few ulp, far inside the GEMV's 1e-5 tolerance); for
+// z << 0 the denominator passes 2^126 or overflows and __fdividef gives 0,
+// the limit (the true value is below 1e-36 in size there).
+__device__ __forceinline__ float silu(float z) { return __fdividef(z, 1.f + __expf(-z)); }
 
 // Per-warp x preparation for one Q4_K super-block column (256 x values per
 // token; half 1, x[128..255], starts XH floats after half 0):
@@ -717,9 +718,20 @@ __global__ void __launch_bounds__(RG * F::kCols * 32 + 32, MINB)
         rows = static_cast<int>(min64(kTileRows, Ni - row0));
     };
     if (U > 0) load_tile();
+    // Residual epilogue of the prologue kernels (FUSE != 0): the thread that
+    // finishes (token m, row rr) of a tile (thread m * 32 + rr of the tile's
+    // finishing CTA) loads its residual when the tile starts, so the load's
+    // latency hides behind the decode.  (FUSE = 0 kernels, which also serve
+    // the plain GEMV, read it in the epilogue and keep the register.)
+    static_assert(MT * kTileRows <= kConsumerThreads, "one finishing thread per output");
+    float rpre = 0.f;
     for (int64_t u = 0; u < U; ++u) {
         const int kc = min(F::kCols, nb - c * F::kCols);
         const uint8_t* st = smem + L.stage0 + s * L.stage_bytes;
+        if (FUSE != 0 && c == crank && Fz.R[gi] && crank == 0 && threadIdx.x < MT * kTileRows) {
+            const int m = threadIdx.x / kTileRows, rr = threadIdx.x % kTileRows;
+            if ((MT == 1 || m < M) && rr < rows) rpre = Fz.R[gi][m * Ni + row0 + rr];
+        }
         mbar_wait_bounded(&full[s], phase, status);
 
         if (cw < kc) {
@@ -787,9 +799,9 @@ __global__ void __launch_bounds__(RG * F::kCols * 32 + 32, MINB)
             named_barrier_sync<kConsumerThreads>(1);
             // finished row sum -> output: times 1/rms(x) of the token, plus the residual
             auto finish = [&](int m, int rr, float sum, float sumsq) {
-                if constexpr (FUSE == kFuseNorm) sum *= 1.f / sqrtf(sumsq / static_cast<float>(K) + Fz.eps);
+                if constexpr (FUSE == kFuseNorm) sum *= rsqrtf(sumsq / static_cast<float>(K) + Fz.eps);
                 const int64_t o = m * Ni + row0 + rr;
-                if (Fz.R[gi]) sum += Fz.R[gi][o];
+                if (Fz.R[gi]) sum += FUSE != 0 ? rpre : Fz.R[gi][o];  // prologue kernels: loaded at the tile's start
                 G.Y[gi][o] = sum;
             };
             if (clus) {
