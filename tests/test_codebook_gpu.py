@@ -82,3 +82,25 @@ def test_gemv_full_size_sampled(q, fmt):
     y = q.qgemv_codebook(fmt, dev(W), dev(tab), dev(x)).cpu().numpy()
     check(y[:, rows], Y, A, f"{fmt} full")
     assert np.isfinite(y).all()
+
+
+@pytest.mark.parametrize("fmt", FORMATS)
+def test_extreme_scales(q, fmt):
+    """Every fp16 d field set to an extreme finite value (smallest subnormal,
+    smallest normal, 1, 65504), |x| up to 1e3: bit-exact dequantisation and
+    the GEMV within tolerance, on the shape each kernel takes (K = 2048)."""
+    N, K = 64, 2048
+    W, tab = synth.gen_cb(fmt, N, K, 800)
+    ext = np.array([0x0001, 0x0400, 0x3C00, 0x7BFF], dtype=np.uint16)
+    rng = np.random.default_rng(801)
+    step = 18 if fmt == "iq4nl" else synth.CB_UNIT_BYTES[fmt]
+    flat = W.reshape(-1, step)
+    flat[:, 0:2] = ext[rng.integers(0, 4, len(flat))].view(np.uint8).reshape(-1, 2)
+    x = (synth.gen_x(1, K, 802) * 1e3).astype(np.float32)
+    ref = oracle.dequant_cb(fmt, W, tab, K)
+    got = q.qdequant_codebook(fmt, dev(W), dev(tab), K).cpu().numpy()
+    assert np.array_equal(got.view(np.uint32), ref.view(np.uint32))
+    Y, A = oracle.gemv_cb(fmt, W, tab, x)
+    y = q.qgemv_codebook(fmt, dev(W), dev(tab), dev(x)).cpu().numpy()
+    check(y, Y, A, f"{fmt} extreme scales")
+    assert np.isfinite(y).all()

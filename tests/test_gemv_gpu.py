@@ -512,3 +512,50 @@ def test_concurrent_host_threads(q):
         else:           # FMA paths: deterministic
             assert torch.equal(y, r), i
     assert q.qg_device_status() == 0
+
+
+# fp16 scale fields at the ends of their range: the smallest subnormal, the
+# smallest normal, 1, and the largest finite value (65504).
+_EXTREME_F16 = np.array([0x0001, 0x0400, 0x3C00, 0x7BFF], dtype=np.uint16)
+
+
+@pytest.mark.parametrize("M", [1, 4, 16])
+def test_q4k_extreme_scales(q, M):
+    """Q4_K blocks whose d and dmin take the extreme finite fp16 values, with
+    |x| up to 1e3: dequantisation stays bit-exact and the GEMV (including the
+    x pre-scaling by 2^76..2^88 of the nibble trick, and the tcgen05 path at
+    M = 16) within its tolerance."""
+    N, K = 96, 1024
+    W = synth.gen_q4k(N, K, 31)
+    blk = W.reshape(-1, 144)
+    rng = np.random.default_rng(32)
+    blk[:, 0:2] = _EXTREME_F16[rng.integers(0, 4, len(blk))].view(np.uint8).reshape(-1, 2)
+    blk[:, 2:4] = _EXTREME_F16[rng.integers(0, 4, len(blk))].view(np.uint8).reshape(-1, 2)
+    x = (synth.gen_x(M, K, 33) * 1e3).astype(np.float32)
+    ref = oracle.dequant_q4k(W, K)
+    got = q.qdequant_q4k(dev(W), K).cpu().numpy()
+    assert np.array_equal(got.view(np.uint32), ref.view(np.uint32))
+    Y, A = oracle.gemv_q4k(W, x)
+    y = q.qgemm_q4k_batched(dev(W), dev(x)).cpu().numpy()
+    check_tol(y, Y, A, 4e-3 if M >= 16 else TAU_FMA, f"q4k extreme scales M={M}")
+    assert np.isfinite(y).all()
+
+
+@pytest.mark.parametrize("M", [1, 2, 16])
+def test_iq3_extreme_scales(q, M):
+    """IQ3 super-blocks whose d takes the extreme finite fp16 values, |x| up
+    to 1e3: bit-exact dequantisation, GEMV within tolerance (FMA path, and
+    the tcgen05 path at M = 16)."""
+    N, K = 96, 2048
+    W, grid = synth.gen_iq3(N, K, 41)
+    blk = W.reshape(-1, 98)
+    rng = np.random.default_rng(42)
+    blk[:, 96:98] = _EXTREME_F16[rng.integers(0, 4, len(blk))].view(np.uint8).reshape(-1, 2)
+    x = (synth.gen_x(M, K, 43) * 1e3).astype(np.float32)
+    ref = oracle.dequant_iq3(W, grid, K)
+    got = q.qdequant_iq3(dev(W), dev(grid), K).cpu().numpy()
+    assert np.array_equal(got.view(np.uint32), ref.view(np.uint32))
+    Y, A = oracle.gemv_iq3(W, grid, x)
+    y = q.qgemm_iq3_batched(dev(W), dev(grid), dev(x)).cpu().numpy()
+    check_tol(y, Y, A, 4e-3 if M >= 16 else TAU_FMA, f"iq3 extreme scales M={M}")
+    assert np.isfinite(y).all()
