@@ -718,18 +718,18 @@ __global__ void __launch_bounds__(RG * F::kCols * 32 + 32, MINB)
         rows = static_cast<int>(min64(kTileRows, Ni - row0));
     };
     if (U > 0) load_tile();
-    // Residual epilogue of the prologue kernels (FUSE != 0) and the one-token
-    // kernels: the thread that finishes (token m, row rr) of a tile (thread
-    // m * 32 + rr of the tile's finishing CTA) loads its residual when the
-    // tile starts, so the load's latency hides behind the decode.  (The
-    // multi-token FUSE = 0 kernels read it in the epilogue: one more live
-    // register spills there.)
+    // Residual epilogue of the prologue kernels (FUSE != 0): the thread that
+    // finishes (token m, row rr) of a tile (thread m * 32 + rr of the tile's
+    // finishing CTA) loads its residual when the tile starts, so the load's
+    // latency hides behind the decode.  The FUSE = 0 kernels, which also run
+    // the plain GEMV, read it in the epilogue: the extra live register costs
+    // the large one-token GEMV 1.5-2 % and spills in the two-token kernel.
     static_assert(MT * kTileRows <= kConsumerThreads, "one finishing thread per output");
     float rpre = 0.f;
     for (int64_t u = 0; u < U; ++u) {
         const int kc = min(F::kCols, nb - c * F::kCols);
         const uint8_t* st = smem + L.stage0 + s * L.stage_bytes;
-        if ((FUSE != 0 || (MT == 1 && !F::kIQ3)) && c == crank && Fz.R[gi] && crank == 0 && threadIdx.x < MT * kTileRows) {
+        if (FUSE != 0 && c == crank && Fz.R[gi] && crank == 0 && threadIdx.x < MT * kTileRows) {
             const int m = threadIdx.x / kTileRows, rr = threadIdx.x % kTileRows;
             if ((MT == 1 || m < M) && rr < rows) rpre = Fz.R[gi][m * Ni + row0 + rr];
         }
@@ -802,7 +802,7 @@ __global__ void __launch_bounds__(RG * F::kCols * 32 + 32, MINB)
             auto finish = [&](int m, int rr, float sum, float sumsq) {
                 if constexpr (FUSE == kFuseNorm) sum *= rsqrtf(sumsq / static_cast<float>(K) + Fz.eps);
                 const int64_t o = m * Ni + row0 + rr;
-                if (Fz.R[gi]) sum += (FUSE != 0 || (MT == 1 && !F::kIQ3)) ? rpre : Fz.R[gi][o];  // loaded at the tile's start
+                if (Fz.R[gi]) sum += FUSE != 0 ? rpre : Fz.R[gi][o];  // prologue kernels: loaded at the tile's start
                 G.Y[gi][o] = sum;
             };
             if (clus) {
