@@ -35,7 +35,12 @@
  * abort, throw or trap.  Argument errors are detected on the host before any
  * launch.  Faults detected inside a kernel (a bounded wait that gave up) are
  * latched in a per-device status word; qg_device_status reports and clears
- * it.
+ * it.  After QG_ECUDA, qg_last_cuda_error gives the CUDA error behind it.
+ *
+ * Threads: every entry point may be called from several host threads at
+ * once (each on its own stream, or ordered by the caller); the library's
+ * per-device set-up is done once and shared.  The device is the calling
+ * thread's current CUDA device.
  */
 #ifndef QGEMV_H
 #define QGEMV_H
