@@ -574,7 +574,7 @@ int launch_t(const uint8_t* W, const void* book, const float* X, float* Y, int M
             gemv_cb_kernel<F, 4><<<blocks, 256, 0, s>>>(W, book, Xg, Yg, mg, N, K);
         else
             gemv_cb_kernel<F, 8><<<blocks, 256, 0, s>>>(W, book, Xg, Yg, mg, N, K);
-        if (cudaGetLastError() != cudaSuccess) return qg::cuda_fail(cudaGetLastError());
+        if (const cudaError_t e = cudaGetLastError(); e != cudaSuccess) return qg::cuda_fail(e);
     }
     return QG_OK;
 }

@@ -78,7 +78,7 @@ int launch_group_iq3_t(const uint8_t* const* W, float* const* Y, const int64_t* 
                 const int64_t blocks = std::min<int64_t>((N[i] + 7) / 8, static_cast<int64_t>(sms) * 8);
                 gemv_iq3_bytes_kernel<F><<<static_cast<int>(blocks), 256, 0, s>>>(
                     W[i], grid, X + static_cast<int64_t>(m0) * K, Y[i] + m0 * N[i], mg, N[i], K);
-                if (cudaGetLastError() != cudaSuccess) return qg::cuda_fail(cudaGetLastError());
+                if (const cudaError_t e = cudaGetLastError(); e != cudaSuccess) return qg::cuda_fail(e);
             }
         }
         return QG_OK;
