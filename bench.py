@@ -229,6 +229,23 @@ def job_throughput(world, bytes_per_step, steps, ms):
     return world * bytes_per_step * steps / (ms * 1e-3) / 1e9
 
 
+def kernel_launches(lib, fn, a, M):
+    """Kernels of ours that one C-ABI call launches: the FMA paths split M
+    into token groups (Q4_K and the IQ4 codebook formats 4, IQ3 2, the other
+    codebook formats 8), each a launch; the tcgen05 path (M >= 16) and the
+    persistent pass are one launch."""
+    if fn in (lib.qgemm_q4k_batched, lib.qgemm_iq3_batched) and M >= 16:
+        return 1
+    if fn in (lib.qgemv_q4k_ex, lib.qgemv_q4k_group, lib.qgemv_q4k_fused, lib.qgemv_q4k_fused_group,
+              lib.qgemm_q4k_batched):
+        return (M + 3) // 4
+    if fn in (lib.qgemv_iq3_ex, lib.qgemv_iq3_group, lib.qgemv_iq3xxs_ex, lib.qgemm_iq3_batched):
+        return (M + 1) // 2  # rows a multiple of 16 bytes (every workload here)
+    if fn == lib.qgemv_codebook:
+        return (M + 3) // 4 if a[0] in (1, 2) else (M + 7) // 8
+    return 1
+
+
 # ------------------------------------------------------------------ our arm
 def fused_step_launches(lib, qgemv, host, dev, keep):
     """The TinyLlama-shaped decode step with its data flow on the device, every
@@ -621,13 +638,14 @@ def run_ours(args, rank, world, local_rank):
                               "programmatic dependent launch: each GEMV streams its first weight tiles while "
                               "the previous one finishes and waits for it before reading x")},
         "tokens_per_s_equiv": round(world * 1000.0 / ms_step, 1),
+        "gemv_per_s": round(world * len(mats) * 1000.0 / ms_step, 1),
         "pct_of_hbm_peak": round(100 * value / world / peak, 1),
         "e2e": {"value": round(e2e_value, 1), "unit": "GB/s", "h2d_bytes_per_step": int(xs_host.nbytes),
                 "d2h_bytes_per_step": int(4 * ys_len),
                 "note": ("pinned host x (the embedding row) -> device, graph of C-ABI launches, device logits -> "
                          "pinned host, every step" if fused else
                          "pinned host x -> device, graph of C-ABI launches, device y -> pinned host, every step")},
-        "gpu_launches": len(flat) * args.steps * (1 if M <= 8 or M >= 16 else (M + 7) // 8),
+        "gpu_launches": sum(kernel_launches(lib, fn, a, M) for fn, a, _wb, _ab, _lb in flat) * args.steps,
         "mode": args.mode,
         "latency_floor": floor,
         "roofline": roof,
