@@ -195,7 +195,8 @@ QG_API int qgemv_iq3_group(const uint8_t* const* W, float* const* Y, const int64
  * fp32, which may be exactly Y[i] (in-place add) but must not otherwise
  * overlap any Y.  At most one of norm_weight and up; with either, M <= 4.
  * Numerics: |Y - exact| <= 1e-5 * sum_k |w*h| per element (h exact), plus
- * the fp32 rounding of the residual add. */
+ * the fp32 rounding of the residual add; 1/sqrt, exp and the SiLU division
+ * use the fast hardware paths (a few ulp each). */
 typedef struct qg_fuse {
     const float* norm_weight;
     float norm_eps;                      /* >= 0, finite */
