@@ -57,7 +57,7 @@ def test_handworked_blocks_on_gpu(q, golden, fmt):
 
 @pytest.mark.parametrize("fmt", FORMATS)
 @pytest.mark.parametrize("N,K", [(64, 2048), (100, 768), (257, 4096), (65, 3072), (40, 6144)])
-@pytest.mark.parametrize("M", [1, 3, 8, 13])
+@pytest.mark.parametrize("M", [1, 3, 8, 13, 32])
 def test_gemv(q, fmt, N, K, M):
     """IQ4_NL and IQ4_XS rows that are a multiple of 16 bytes take the
     TMA-fed kernel (K = 768, 2048, 3072, 4096, 6144; 768 and 3072 with a
