@@ -231,7 +231,7 @@ def job_throughput(world, bytes_per_step, steps, ms):
 
 def kernel_launches(lib, fn, a, M):
     """Kernels of ours that one C-ABI call launches: the FMA paths split M
-    into token groups (Q4_K and the IQ4 codebook formats 4, IQ3 2, the other
+    into token groups (Q4_K, IQ3 and the IQ4 codebook formats 4, the other
     codebook formats 8), each a launch; the tcgen05 path (M >= 16) and the
     persistent pass are one launch."""
     if fn in (lib.qgemm_q4k_batched, lib.qgemm_iq3_batched) and M >= 16:
@@ -240,7 +240,7 @@ def kernel_launches(lib, fn, a, M):
               lib.qgemm_q4k_batched):
         return (M + 3) // 4
     if fn in (lib.qgemv_iq3_ex, lib.qgemv_iq3_group, lib.qgemv_iq3xxs_ex, lib.qgemm_iq3_batched):
-        return (M + 1) // 2  # rows a multiple of 16 bytes (every workload here)
+        return (M + 3) // 4  # rows a multiple of 16 bytes (every workload here)
     if fn == lib.qgemv_codebook:
         return (M + 3) // 4 if a[0] in (1, 2) else (M + 7) // 8
     return 1

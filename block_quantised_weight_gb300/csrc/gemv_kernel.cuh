@@ -110,12 +110,14 @@ struct FmtIQ3XXST : FmtIQ3T {
 // IQ3 tables in smem, shared by all consumer warps.
 // Grid: lane-replicated so every gather is conflict-free: for grid row i,
 // lane L reads the 8 bytes at 256*i + 8*L (fp16 magnitudes 0,1 then 2,3).
-// Signs: for each 7-bit sign field s7 one word T with the eight signs s8 (the
-// eighth = parity of the seven) placed so that (T << p) & 0x80008000 is the
-// sign mask of fp16 pair p (weights 2p, 2p+1): sign 2p at bit 15-p, sign
-// 2p+1 at bit 31-p.  Lane replicated: lane L reads word 32*s7 + L.
+// Signs: for each 7-bit sign field s7 two words (T0, T1) with the eight
+// signs s8 (the eighth = parity of the seven) placed so that
+// (T[p >> 1] << (p & 1)) & 0x80008000 is the sign mask of fp16 pair p
+// (weights 2p, 2p+1): in word p >> 1, sign 2p at bit 15 - (p & 1) and sign
+// 2p+1 at bit 31 - (p & 1).  Replicated per half-warp lane: lane L reads the
+// 8 bytes at 128*s7 + 8*(L & 15).
 constexpr int kIQ3GridBytes = 256 * 32 * 8;
-constexpr int kIQ3SignBytes = 128 * 32 * 4;
+constexpr int kIQ3SignBytes = 128 * 16 * 8;
 constexpr int kIQ3TableBytes = kIQ3GridBytes + kIQ3SignBytes;
 
 
@@ -371,14 +373,15 @@ __device__ __forceinline__ void q4k_half2(const uint8_t* blk, int rstride, int h
     }
 }
 
-// Sign word T of the sign field at bits 7l..7l+6 of sw (see kIQ3SignBytes);
-// lane4 = 4 * lane.
-__device__ __forceinline__ uint32_t iq3_signs(const uint8_t* sg, uint32_t sw, int l, uint32_t lane4) {
+// Sign words (T0, T1) of the sign field at bits 7l..7l+6 of sw (see
+// kIQ3SignBytes); lane_s = 8 * (lane & 15).
+__device__ __forceinline__ uint2 iq3_signs(const uint8_t* sg, uint32_t sw, int l, uint32_t lane_s) {
     const uint32_t off = (l == 0 ? (sw << 7) : (sw >> (7 * l - 7))) & 0x3F80u;
-    return *reinterpret_cast<const uint32_t*>(sg + (off | lane4));
+    return *reinterpret_cast<const uint2*>(sg + (off | lane_s));
 }
-// fp16 pair p of the grid row, sign flipped by sign word T.
-__device__ __forceinline__ uint32_t iq3_flip(uint32_t g, uint32_t T, int p) { return g ^ ((T << p) & 0x80008000u); }
+// An fp16 pair of the grid row, sign flipped by sign word t shifted by q:
+// pair p takes word p >> 1 and q = p & 1.
+__device__ __forceinline__ uint32_t iq3_flip(uint32_t g, uint32_t t, int q) { return g ^ ((t << q) & 0x80008000u); }
 
 // Grid row of the index byte `byte` of word w: 8 bytes (two fp16 pairs).
 __device__ __forceinline__ uint2 iq3_grid(const uint8_t* tb, uint32_t w, int byte, uint32_t lane8) {
@@ -420,11 +423,18 @@ __device__ __forceinline__ void iq3_load_half(const uint8_t* boxrow, int h, uint
 // block + 128h.
 template <int MT, class F>
 __device__ __forceinline__ void iq3_half2(const uint32_t (&vi)[2][8], const uint32_t (&vs)[2][4], const uint32_t (&dbits)[2],
-                                          const uint8_t* tb, const uint8_t* sg, uint32_t lane8, uint32_t lane4,
+                                          const uint8_t* tb, const uint8_t* sg, uint32_t lane8, uint32_t lane_s,
                                           const float* xq, int64_t xstride, int M, float (&acc)[2][MT]) {
-    float d[2];
+    // sub-block factor d*(0.5+code)*kDbScale = fma(1 + code/16, 16 d', -15.5 d')
+    // with d' = d*kDbScale: 1 + code/16 is the float with the code as the
+    // top four mantissa bits; every term is exact, so is the result
+    float d16[2], d155[2];
 #pragma unroll
-    for (int r = 0; r < 2; ++r) d[r] = h2f(dbits[r]);
+    for (int r = 0; r < 2; ++r) {
+        const float d = h2f(dbits[r]);
+        d16[r] = d * (16.f * F::kDbScale);
+        d155[r] = d * (15.5f * F::kDbScale);
+    }
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
         f2 dot[2][MT];
@@ -434,9 +444,9 @@ __device__ __forceinline__ void iq3_half2(const uint32_t (&vi)[2][8], const uint
             for (int m = 0; m < MT; ++m) dot[r][m] = f2{0.f, 0.f};
 #pragma unroll
         for (int l = 0; l < 4; ++l) {
-            uint32_t T[2];
+            uint2 T[2];
 #pragma unroll
-            for (int r = 0; r < 2; ++r) T[r] = iq3_signs(sg, vs[r][j], l, lane4);
+            for (int r = 0; r < 2; ++r) T[r] = iq3_signs(sg, vs[r][j], l, lane_s);
 #pragma unroll
             for (int hf = 0; hf < 2; ++hf) {
                 const int PI = 8 * j + 2 * l + hf;  // index byte within the half
@@ -447,8 +457,9 @@ __device__ __forceinline__ void iq3_half2(const uint32_t (&vi)[2][8], const uint
 #pragma unroll
                 for (int r = 0; r < 2; ++r) {
                     const uint2 g = iq3_grid(tb, vi[r][PI >> 2], PI & 3, lane8);
-                    const f2 w01 = h2_to_f2(iq3_flip(g.x, T[r], 2 * hf));
-                    const f2 w23 = h2_to_f2(iq3_flip(g.y, T[r], 2 * hf + 1));
+                    const uint32_t t = hf ? T[r].y : T[r].x;
+                    const f2 w01 = h2_to_f2(iq3_flip(g.x, t, 0));
+                    const f2 w23 = h2_to_f2(iq3_flip(g.y, t, 1));
 #pragma unroll
                     for (int m = 0; m < MT; ++m) {
                         if (MT == 1 || m < M) {
@@ -461,7 +472,8 @@ __device__ __forceinline__ void iq3_half2(const uint32_t (&vi)[2][8], const uint
         }
 #pragma unroll
         for (int r = 0; r < 2; ++r) {
-            const float db = d[r] * (static_cast<float>(vs[r][j] >> 28) + 0.5f) * F::kDbScale;
+            const float f = __uint_as_float(((vs[r][j] >> 9) & 0x00780000u) | 0x3F800000u);
+            const float db = fmaf(f, d16[r], -d155[r]);
 #pragma unroll
             for (int m = 0; m < MT; ++m)
                 if (MT == 1 || m < M) acc[r][m] = fmaf(db, dot[r][m].x + dot[r][m].y, acc[r][m]);
@@ -565,12 +577,15 @@ __global__ void __launch_bounds__(RG * F::kCols * 32 + 32, MINB)
         // decode); sign k goes to bit 15 (k even) or 31 (k odd) of pair k/2
         uint32_t* sgt = reinterpret_cast<uint32_t*>(smem + L.table + kIQ3GridBytes);
         for (int i = threadIdx.x; i < 128 * 32; i += blockDim.x) {
-            const uint32_t s7 = static_cast<uint32_t>(i) >> 5;
+            const uint32_t s7 = static_cast<uint32_t>(i) >> 5;  // 32 words per field: 16 copies of (T0, T1)
             const uint32_t s8 = s7 | ((__popc(s7) & 1u) << 7);
+            const int half = i & 1;  // word T0 (pairs 0, 1) or T1 (pairs 2, 3)
             uint32_t t = 0;
 #pragma unroll
-            for (int pr = 0; pr < 4; ++pr)
-                t |= (((s8 >> (2 * pr)) & 1u) << (15 - pr)) | (((s8 >> (2 * pr + 1)) & 1u) << (31 - pr));
+            for (int q = 0; q < 2; ++q) {
+                const int pr = 2 * half + q;
+                t |= (((s8 >> (2 * pr)) & 1u) << (15 - q)) | (((s8 >> (2 * pr + 1)) & 1u) << (31 - q));
+            }
             sgt[i] = t;
         }
     }
@@ -702,7 +717,7 @@ __global__ void __launch_bounds__(RG * F::kCols * 32 + 32, MINB)
     float ss[MT];  // RMSNorm prologue: this lane's part of sum(x^2) over the tile's units
 #pragma unroll
     for (int m = 0; m < MT; ++m) acc2[0][m] = acc2[1][m] = ss[m] = 0.f;
-    const uint32_t lane8 = static_cast<uint32_t>(lane) * 8u, lane4 = static_cast<uint32_t>(lane) * 4u;
+    const uint32_t lane8 = static_cast<uint32_t>(lane) * 8u, lane_s = static_cast<uint32_t>(lane & 15) * 8u;
     int64_t tile_count = 0;
 
     int s = 0, c = crank;
@@ -767,7 +782,7 @@ __global__ void __launch_bounds__(RG * F::kCols * 32 + 32, MINB)
 #undef QG_IQ3_HALF
                 }
                 const uint8_t* tb = smem + L.table;
-                iq3_half2<MT, F>(vi, vs, dbits, tb, tb + kIQ3GridBytes, lane8, lane4, xb + XH * hl, xstride, M, acc2);
+                iq3_half2<MT, F>(vi, vs, dbits, tb, tb + kIQ3GridBytes, lane8, lane_s, xb + XH * hl, xstride, M, acc2);
             }
         }
         __syncwarp();

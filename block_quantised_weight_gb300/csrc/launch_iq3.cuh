@@ -83,14 +83,15 @@ int launch_group_iq3_t(const uint8_t* const* W, float* const* Y, const int64_t* 
         }
         return QG_OK;
     }
-    // groups of at most 2 tokens (the two-row decode with x staged): beyond
-    // two tokens its registers run out, and repeated 2-token passes over W
-    // beat a wider group
-    for (int m0 = 0; m0 < M; m0 += 2) {
-        const int mg = std::min(2, M - m0);
+    // groups of at most 4 tokens (the two-row decode with x staged; beyond
+    // one token, one 32-row tile per CTA, so that two stages of the group's
+    // x fit beside the tables)
+    for (int m0 = 0; m0 < M; m0 += 4) {
+        const int mg = std::min(4, M - m0);
         const float* Xg = X + static_cast<int64_t>(m0) * K;
-        const int rc = mg == 1 ? launch_gemv<F, 1, 2, 1>(W, Y, N, count, m0, grid, Xg, mg, K, s, status, dev, flags)
-                               : launch_gemv<F, 2, 1, 1>(W, Y, N, count, m0, grid, Xg, mg, K, s, status, dev, flags);
+        const int rc = mg == 1   ? launch_gemv<F, 1, 2, 1>(W, Y, N, count, m0, grid, Xg, mg, K, s, status, dev, flags)
+                       : mg == 2 ? launch_gemv<F, 2, 1, 1>(W, Y, N, count, m0, grid, Xg, mg, K, s, status, dev, flags)
+                                 : launch_gemv<F, 4, 1, 1>(W, Y, N, count, m0, grid, Xg, mg, K, s, status, dev, flags);
         if (rc != QG_OK) return rc;
     }
     return QG_OK;

@@ -101,7 +101,7 @@ QG_API int qgemv_q4k_ex(const uint8_t* W, const float* X, float* Y, int M, int64
  * model_forward's matmul (operation).
  * grid: 256*4 bytes, the codebook in the published doubled units (the kernel
  * applies the 0.5 of page 4's grid()).  Other arguments as qgemv_q4k.
- * K/256 a multiple of 8 takes the tensor-map path, M > 2 in groups of 2
+ * K/256 a multiple of 8 takes the tensor-map path, M > 4 in groups of 4
  * tokens, each group streaming W once; other K take a slower byte-addressed
  * path (groups of 8 tokens) with the same numerics. */
 QG_API int qgemv_iq3(const uint8_t* W, const uint8_t* grid, const float* X, float* Y, int M, int64_t N, int64_t K,

@@ -26,8 +26,8 @@ def test_kernel_launches_follow_the_token_groups():
     assert kl(lib, lib.qgemm_q4k_batched, (), 8) == 2
     assert kl(lib, lib.qgemm_q4k_batched, (), 16) == 1
     assert kl(lib, lib.qgemv_q4k_fused_group, (), 3) == 1
-    # IQ3: groups of 2 tokens
-    assert [kl(lib, lib.qgemv_iq3_group, (), m) for m in (1, 2, 3, 8)] == [1, 1, 2, 4]
+    # IQ3: groups of 4 tokens
+    assert [kl(lib, lib.qgemv_iq3_group, (), m) for m in (1, 2, 3, 5, 8)] == [1, 1, 1, 2, 2]
     assert kl(lib, lib.qgemm_iq3_batched, (), 32) == 1
     # codebook formats: IQ4 (ids 1, 2) groups of 4, grid formats groups of 8
     assert kl(lib, lib.qgemv_codebook, (1,), 5) == 2
