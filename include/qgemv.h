@@ -262,7 +262,7 @@ QG_API int qgemv_q4k_pass(const qg_stage* stages, int nstages, int M, unsigned* 
  * All calls on a device share the one array, so calls that overlap on the
  * GPU (other streams, other host threads) race and give wrong results:
  * order them on one stream or synchronise between them.
- * The paper has no counterpart: this entry point exists only for callers
+ * The pages have no counterpart: this entry point exists only for callers
  * that cannot allocate. */
 #define QG_NOALLOC_SCRATCH_WORDS 96
 QG_API int qgemv_q4k_pass_noalloc(const qg_stage* stages, int nstages, int M, cudaStream_t stream);
