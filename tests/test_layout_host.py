@@ -1,0 +1,83 @@
+"""Shared-memory layouts of the GEMV kernels, checked on the host.
+
+tests/layout_probe.cu prints, for every configuration the launchers can
+choose, the layout that launch_gemv derives.  The checks are the rules the
+copies into that memory depend on: mbarriers 8-byte aligned, every
+tensor-map (TMA) destination and bulk-copy destination on a 128-byte
+boundary, at least two ring stages inside the per-CTA limit, and each
+super-block inside the box that carries it (an IQ3 block of 98 bytes starts
+0..14 bytes into its 112-byte box, since the box's x coordinate is the
+block's byte offset rounded down to 16).
+"""
+import json
+import os
+import shutil
+import subprocess
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+CSRC = os.path.join(ROOT, "block_quantised_weight_gb300", "csrc")
+
+
+@pytest.fixture(scope="module")
+def layouts(tmp_path_factory):
+    nvcc = shutil.which("nvcc") or "/usr/local/cuda/bin/nvcc"
+    if not os.path.exists(nvcc):
+        pytest.skip("nvcc not found")
+    exe = str(tmp_path_factory.mktemp("layout") / "layout_probe")
+    subprocess.run([nvcc, "-std=c++17", "-gencode", "arch=compute_103a,code=sm_103a", "-I", CSRC,
+                    "-I", os.path.join(ROOT, "include"), os.path.join(ROOT, "tests", "layout_probe.cu"), "-o", exe],
+                   check=True, capture_output=True, timeout=300)
+    out = subprocess.run([exe], check=True, capture_output=True, text=True, timeout=60).stdout
+    return [json.loads(line) for line in out.splitlines() if line.strip()]
+
+
+def test_every_configuration_is_listed(layouts):
+    got = {(c["fmt"], c["MT"], c["RG"], c["MINB"], c["fuse"]) for c in layouts}
+    assert ("q4k", 1, 1, 2, 0) in got and ("q4k", 4, 1, 1, 2) in got
+    assert {("iq3", 1, 2, 1, 0), ("iq3", 2, 1, 1, 0), ("iq3", 4, 1, 1, 0)} <= got
+    assert len(got) == len(layouts) == 18
+
+
+def test_ring_fits_with_at_least_two_stages(layouts):
+    for c in layouts:
+        assert 2 <= c["stages"] <= c["max_stages"], c
+        assert c["total"] <= c["budget"] <= c["smem_per_cta"], c
+        assert c["total"] == c["stage0"] + c["stages"] * c["stage_bytes"], c
+
+
+def test_barriers_and_copy_destinations_aligned(layouts):
+    for c in layouts:
+        # one full and one empty mbarrier per stage, 8 bytes each, before sx
+        assert c["full"] % 8 == 0 and c["empty"] % 8 == 0, c
+        assert c["empty"] >= c["full"] + 8 * c["max_stages"], c
+        assert c["sx"] >= c["empty"] + 8 * c["max_stages"], c
+        for k in ("sx", "red", "cred", "ss", "table", "stage0", "stage_bytes", "xoff", "aoff"):
+            assert c[k] % 128 == 0, (k, c)
+        # weight boxes: one per block column at st + b * tile_rows * box_bytes
+        assert (c["tile_rows"] * c["box_bytes"]) % 128 == 0, c
+        assert c["xoff"] >= c["cols"] * c["tile_rows"] * c["box_bytes"], c
+        # x: per token a padded 2D box (IQ3) or one 1 KB-per-column bulk copy (Q4_K)
+        x_per_token = c["x_box_bytes"] if c["xh"] == 132 else c["cols"] * 1024
+        assert x_per_token % 128 == 0, c
+        assert c["aoff"] - c["xoff"] >= c["MT"] * x_per_token, c
+        # prologue operands: the RMSNorm weight once, the SwiGLU up operand per token
+        extra = {0: 0, 1: c["cols"] * 1024, 2: c["MT"] * c["cols"] * 1024}[c["fuse"]]
+        assert c["stage_bytes"] - c["aoff"] == extra, c
+
+
+def test_tables_sit_between_reductions_and_ring(layouts):
+    for c in layouts:
+        iq3 = c["fmt"].startswith("iq3")
+        assert c["stage0"] - c["table"] == (256 * 32 * 8 + 128 * 16 * 8 if iq3 else 0), c
+        assert c["table"] >= c["ss"], c
+
+
+def test_every_block_lies_inside_its_box(layouts):
+    for c in layouts:
+        for col in range(64):  # the block's offset modulo 16 repeats every 8 columns
+            start = col * c["block_bytes"]
+            box_x = start & ~15  # the tensor-map x coordinate: a multiple of 16 bytes
+            assert box_x % 16 == 0
+            assert start - box_x + c["block_bytes"] <= c["box_bytes"], (c["fmt"], col)
