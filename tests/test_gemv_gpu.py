@@ -292,11 +292,12 @@ def test_q4k_group_with_prefetch_flag(q):
 
 
 @pytest.mark.parametrize("K", [2048, 768])
-def test_iq3_group_matches_single_calls(q, K):
+@pytest.mark.parametrize("M", [1, 2, 4, 5])
+def test_iq3_group_matches_single_calls(q, K, M):
     grid = synth.gen_iq3_grid(3)
     Ws = [dev(synth.gen_iq3(N, K, 80 + i, grid_seed=3)[0]) for i, N in enumerate((100, 64, 33))]
     g = dev(grid)
-    x = dev(synth.gen_x(2, K, 13))
+    x = dev(synth.gen_x(M, K, 13))
     ys = q.qgemv_iq3_group(Ws, g, x)
     for W, y in zip(Ws, ys):
         assert torch.equal(y, q.qgemv_iq3(W, g, x))
