@@ -478,21 +478,27 @@ def run_ours(args, rank, world, local_rank):
     if sampler:
         sampler.start()
         time.sleep(0.3)
-    if world > 1:
-        dist.barrier()
-    torch.cuda.synchronize(dev)
-    t0 = torch.cuda.Event(enable_timing=True)
-    t1 = torch.cuda.Event(enable_timing=True)
-    with torch.cuda.stream(stream):
-        t0.record(stream)
-        for _ in range(args.steps):
-            g.replay()
-        t1.record(stream)
-    torch.cuda.synchronize(dev)
-    if world > 1:
-        dist.barrier()
-    clocks = sampler.stop() if sampler else None
-    ms_total = t0.elapsed_time(t1)
+    # REPEATS timed regions of exactly `steps` steps, each bracketed by a
+    # barrier and a device synchronisation; the slowest rank's time of each,
+    # and the median region is reported
+    region_ms = []
+    for _ in range(REPEATS):
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            t0.record(stream)
+            for _ in range(args.steps):
+                g.replay()
+            t1.record(stream)
+        torch.cuda.synchronize(dev)
+        if world > 1:
+            dist.barrier()
+        region_ms.append(t0.elapsed_time(t1))
+    region_ms = max_over_ranks(region_ms, world, dev)
+    ms_total = statistics.median(region_ms)
     durs = None
     if per_launch_ok:
         try:
@@ -568,7 +574,12 @@ def run_ours(args, rank, world, local_rank):
     torch.cuda.synchronize(dev)
     ms_e2e = e0.elapsed_time(e1)
 
-    ms_total, ms_e2e = max_over_ranks([ms_total, ms_e2e], world, dev)
+    ms_e2e = max_over_ranks([ms_e2e], world, dev)[0]
+    # the single-matrix configurations at M=1, measured in the same run (one GPU)
+    per_config = None
+    if world == 1 and args.workload == "tinyllama" and args.mode == "group" and not args.no_per_config:
+        per_config = measure_configs(lib, qgemv, dev, stream, l2)
+    clocks = sampler.stop() if sampler else None
     n_pass = args.steps * passes_per_replay
     ms_step = ms_total / n_pass
     value = job_throughput(world, step_wbytes, n_pass, ms_total)
@@ -587,20 +598,20 @@ def run_ours(args, rank, world, local_rank):
     avg_launch_ms = ms_total / n_launch
     achieved = (algo / len(flat)) / (avg_launch_ms * 1e-3) / 1e9
     if args.mode == "pass" and args.workload == "tinyllama":
-        kname = "qgemv_q4k_pass gemv_pass_kernel"
+        kname = "qgemv_q4k_pass qg_gemv_pass_kernel"
     elif fused:
-        kname = "qgemv_q4k_fused gemv_kernel<FmtQ4KT, FUSE>"
+        kname = "qgemv_q4k_fused qg_gemv_kernel<FmtQ4KT, FUSE>"
     elif mats[0][0] == "q4k":
-        kname = ("qgemm_q4k_batched gemm_tc_kernel<Q4_K> (tcgen05)" if M >= 16 else
-                 "qgemv_q4k gemv_kernel<FmtQ4KT>")
+        kname = ("qgemm_q4k_batched qg_gemm_tc_kernel<Q4_K> (tcgen05)" if M >= 16 else
+                 "qgemv_q4k qg_gemv_kernel<FmtQ4KT>")
     elif mats[0][0] == "iq3":
-        kname = ("qgemm_iq3_batched gemm_tc_kernel<IQ3> (tcgen05)" if M >= 16 else
-                 "qgemv_iq3 gemv_kernel<FmtIQ3T>")
+        kname = ("qgemm_iq3_batched qg_gemm_tc_kernel<IQ3> (tcgen05)" if M >= 16 else
+                 "qgemv_iq3 qg_gemv_kernel<FmtIQ3T>")
     elif mats[0][0] == "iq3xxs":
-        kname = "qgemv_iq3xxs gemv_kernel<FmtIQ3XXST>"
+        kname = "qgemv_iq3xxs qg_gemv_kernel<FmtIQ3XXST>"
     else:
-        kname = (f"qgemv_codebook gemv_cb_tma_kernel<{mats[0][0].upper()}>" if mats[0][0] in ("iq4nl", "iq4xs")
-                 else f"qgemv_codebook gemv_cb_kernel<{mats[0][0].upper()}>")
+        kname = (f"qgemv_codebook qg_gemv_cb_tma_kernel<{mats[0][0].upper()}>" if mats[0][0] in ("iq4nl", "iq4xs")
+                 else f"qgemv_codebook qg_gemv_cb_kernel<{mats[0][0].upper()}>")
     roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
             "frac": round(achieved / peak, 4), "traffic": profiled_traffic(args.workload, M),
             "peak_kind": f"of {peak_kind}", "kernel": kname, "launches_timed": n_launch,
@@ -645,12 +656,90 @@ def run_ours(args, rank, world, local_rank):
                 "note": ("pinned host x (the embedding row) -> device, graph of C-ABI launches, device logits -> "
                          "pinned host, every step" if fused else
                          "pinned host x -> device, graph of C-ABI launches, device y -> pinned host, every step")},
+        "repeats": {"n": REPEATS, "statistic": "median",
+                    "ms_per_step_each": [round(r / n_pass, 4) for r in region_ms]},
         "gpu_launches": sum(kernel_launches(lib, fn, a, M) for fn, a, _wb, _ab, _lb in flat) * args.steps,
         "mode": args.mode,
         "latency_floor": floor,
         "roofline": roof,
+        "per_config": per_config,
         "clocks": clocks,
     }
+
+
+# ------------------------------------------------------------------ per-config block
+REPEATS = 5
+PER_CONFIG = ("q4k_c0", "iq3_c2", "q4k_c4a", "q4k_c4b", "iq3_c4a", "iq3_c4b")
+
+
+def measure_configs(lib, qgemv, dev, stream, l2, min_region_ms=200.0):
+    """The single-matrix M=1 configurations, each timed as REPEATS regions of
+    at least min_region_ms (a CUDA graph of launches rotating over weight
+    copies that together exceed 2x L2, replayed), median region reported."""
+    import numpy as np
+    import torch
+    peak, peak_kind = measured_peaks()
+    out = []
+    for name in PER_CONFIG:
+        mats, desc, M = workload_spec(name, 1)
+        fmt, K, N = mats[0]
+        host = gen_mats(name, mats, 1)
+        wb = weight_bytes(fmt, K, N)
+        copies = int(np.ceil(2 * l2 / wb)) + 1 if wb < 2 * l2 else 1
+        _f, _K, _N, W, grid, x = host[0]
+        xd = torch.from_numpy(np.ascontiguousarray(x)).to(dev)
+        yd = torch.empty((1, N), dtype=torch.float32, device=dev)
+        gd = torch.from_numpy(grid).to(dev) if grid is not None else None
+        Wds = [torch.from_numpy(W).to(dev) for _ in range(copies)]
+        fl = qgemv.QG_PREFETCH_WEIGHTS
+
+        def launch(Wd, s):
+            if fmt == "q4k":
+                return lib.qgemv_q4k_ex(Wd.data_ptr(), xd.data_ptr(), yd.data_ptr(), 1, N, K, fl, s)
+            return lib.qgemv_iq3_ex(Wd.data_ptr(), gd.data_ptr(), xd.data_ptr(), yd.data_ptr(), 1, N, K, fl, s)
+
+        per_graph = max(copies, 64 // copies * copies)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            cap = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+            for i in range(per_graph):
+                if launch(Wds[i % copies], cap) != 0:
+                    raise RuntimeError(f"{name}: capture launch failed")
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                g.replay()
+        torch.cuda.synchronize(dev)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            g.replay()
+            e1.record(stream)
+        torch.cuda.synchronize(dev)
+        replays = max(1, int(np.ceil(min_region_ms / max(e0.elapsed_time(e1), 1e-3))))
+        regions = []
+        for _ in range(REPEATS):
+            torch.cuda.synchronize(dev)
+            with torch.cuda.stream(stream):
+                e0.record(stream)
+                for _ in range(replays):
+                    g.replay()
+                e1.record(stream)
+            torch.cuda.synchronize(dev)
+            regions.append(e0.elapsed_time(e1))
+        status = qgemv.qg_device_status()
+        if status != 0:
+            raise RuntimeError(f"{name}: device status {status}")
+        ms = statistics.median(regions) / (replays * per_graph)
+        gbps = wb / (ms * 1e-3) / 1e9
+        out.append({"workload": desc, "fmt": fmt, "K": K, "N": N, "M": 1, "ms": round(ms, 5),
+                    "GBps": round(gbps, 1), "roofline_frac": round(gbps / peak, 4),
+                    "peak": peak, "peak_kind": f"of {peak_kind}",
+                    "tokens_per_s_equiv": round(1000.0 / ms, 1), "gemv_per_s": round(1000.0 / ms, 1),
+                    "launches_per_region": replays * per_graph,
+                    "region_ms_each": [round(r, 2) for r in regions], "weight_copies": copies})
+        del Wds, g
+        torch.cuda.empty_cache()
+    return out
 
 
 # ------------------------------------------------------------------ oracle arm
@@ -727,6 +816,8 @@ def main():
     ap.add_argument("--M", type=int, default=1)
     ap.add_argument("--cpu-baseline-s", type=float, default=12.0)
     ap.add_argument("--no-prefetch", action="store_true", help="plain stream-ordered launches")
+    ap.add_argument("--no-per-config", action="store_true",
+                    help="skip the single-matrix M=1 configurations measured after the decode pass")
     ap.add_argument("--mode", choices=["pass", "group", "single", "fused"], default="group",
                     help="decode pass as one persistent launch (pass), one launch per q/k/v or gate/up group "
                          "(group), one launch per matrix (single), or the decode step with fused RMSNorm / "

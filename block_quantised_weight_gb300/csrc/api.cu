@@ -39,6 +39,8 @@ unsigned* status_ptr() {
 // host code `qg_noalloc_scratch` is a host-side stand-in for the symbol, not
 // a device address: kernels get the address from cudaGetSymbolAddress.
 static __device__ __align__(256) unsigned qg_noalloc_scratch[QG_NOALLOC_SCRATCH_WORDS];
+// A pass's plan holds QG_MAX_PASS_STAGES stages: the scratch never admits more.
+static_assert(QG_NOALLOC_SCRATCH_WORDS <= QG_MAX_PASS_STAGES, "no-allocation scratch larger than a pass's plan");
 
 namespace {
 
@@ -94,7 +96,7 @@ int check_dequant(const uint8_t* W, const uint8_t* grid, bool need_grid, const f
 }
 
 // Test-only: an mbarrier nobody arrives on; the bounded wait must give up.
-__global__ void bounded_wait_probe(unsigned* status) {
+__global__ void qg_bounded_wait_probe(unsigned* status) {
     __shared__ uint64_t bar;
     if (threadIdx.x == 0) {
         qg::mbar_init(&bar, 1);
@@ -295,6 +297,7 @@ int qgemv_q4k_pass(const qg_stage* stages, int nstages, int M, unsigned* sync, c
 int qgemv_q4k_pass_noalloc(const qg_stage* stages, int nstages, int M, cudaStream_t stream) {
     if (!stages || nstages < 1 || M < 1 || M > 4) return QG_EINVAL;
     if (nstages > QG_NOALLOC_SCRATCH_WORDS) return QG_ESCRATCH;
+    if (nstages > QG_MAX_PASS_STAGES) return QG_EINVAL;  // unreachable while the static_assert holds
     for (int i = 0; i < nstages; ++i) {
         const qg_stage& q = stages[i];
         const int rc = check_group(q.W, const_cast<float* const*>(q.Y), q.N, q.count, nullptr, false, q.X, M, q.K, 144);
@@ -359,7 +362,7 @@ int qg_device_status(cudaStream_t stream) {
 int qg_test_bounded_wait(cudaStream_t stream) {
     unsigned* st = status_ptr();
     if (!st) return qg::cuda_fail(cudaGetLastError());
-    bounded_wait_probe<<<1, 32, 0, stream>>>(st);
+    qg_bounded_wait_probe<<<1, 32, 0, stream>>>(st);
     return qg::launch_status();
 }
 

@@ -1,5 +1,5 @@
 // Test-only: the dependent-launch floor of a decode step.  One launch of
-// chain_step_kernel does what every GEMV of the step must do on the
+// qg_chain_step_kernel does what every GEMV of the step must do on the
 // dependency chain and nothing else: let the next launch start
 // (griddepcontrol.launch_dependents), wait for the previous one
 // (griddepcontrol.wait), read the activation vector x and write 32 outputs
@@ -10,7 +10,7 @@
 
 namespace qg {
 
-__global__ void __launch_bounds__(288) chain_step_kernel(const float* __restrict__ X, float* __restrict__ Y,
+__global__ void __launch_bounds__(288) qg_chain_step_kernel(const float* __restrict__ X, float* __restrict__ Y,
                                                          int64_t K) {
     grid_launch_dependents();
     grid_dependency_wait();
@@ -34,7 +34,7 @@ int launch_chain_step(const float* X, float* Y, int64_t K, int grid, unsigned fl
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = (flags & QG_PREFETCH_WEIGHTS) ? 1 : 0;
-    if (cudaLaunchKernelEx(&cfg, chain_step_kernel, X, Y, K) != cudaSuccess) return qg::cuda_fail(cudaGetLastError());
+    if (cudaLaunchKernelEx(&cfg, qg_chain_step_kernel, X, Y, K) != cudaSuccess) return qg::cuda_fail(cudaGetLastError());
     return launch_status();
 }
 

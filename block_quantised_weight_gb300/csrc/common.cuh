@@ -158,6 +158,19 @@ __device__ __forceinline__ void fadd2(f2& a, f2 b) {
         : "f"(b.x), "f"(b.y));
 }
 
+// Packed fp32x2 multiply (round to nearest, subnormals kept).
+__device__ __forceinline__ f2 fmul2(f2 a, f2 b) {
+    f2 r;
+    asm("{\n\t.reg .b64 ra, rb;\n\t"
+        "mov.b64 ra, {%2, %3};\n\t"
+        "mov.b64 rb, {%4, %5};\n\t"
+        "mul.rn.f32x2 ra, ra, rb;\n\t"
+        "mov.b64 {%0, %1}, ra;\n\t}"
+        : "=f"(r.x), "=f"(r.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+    return r;
+}
+
 // Both fp16 halves of a 32-bit register -> fp32 (exact).
 __device__ __forceinline__ f2 h2_to_f2(uint32_t h) {
     f2 r;

@@ -6,7 +6,7 @@ namespace qg {
 // ------------------------------------------------ test-only dequantisation
 // Bit-exact with the pages' fp32 evaluation order: the products and the
 // difference are rounded separately (no FMA contraction).
-__global__ void dequant_q4k_kernel(const uint8_t* __restrict__ W, float* __restrict__ out, int64_t nblocks) {
+__global__ void qg_dequant_q4k_kernel(const uint8_t* __restrict__ W, float* __restrict__ out, int64_t nblocks) {
     const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;  // (block, group g)
     if (i >= nblocks * 4) return;
     const int64_t bi = i >> 2;
@@ -30,7 +30,7 @@ __global__ void dequant_q4k_kernel(const uint8_t* __restrict__ W, float* __restr
 // Both IQ3 orders (FmtIQ3T: page 4; FmtIQ3XXST: page 3): every value has at
 // most 24 significant bits, so any evaluation order gives the exact value.
 template <class F>
-__global__ void dequant_iq3_kernel(const uint8_t* __restrict__ W, const uint8_t* __restrict__ grid,
+__global__ void qg_dequant_iq3_kernel(const uint8_t* __restrict__ W, const uint8_t* __restrict__ grid,
                                    float* __restrict__ out, int64_t nblocks) {
     const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;  // (block, sub-block)
     if (i >= nblocks * 8) return;
@@ -57,21 +57,21 @@ __global__ void dequant_iq3_kernel(const uint8_t* __restrict__ W, const uint8_t*
 int launch_dequant_q4k(const uint8_t* W, float* out, int64_t N, int64_t K, cudaStream_t s) {
     const int64_t nblocks = N * (K / 256);
     const int64_t threads = nblocks * 4;
-    dequant_q4k_kernel<<<static_cast<unsigned>((threads + 255) / 256), 256, 0, s>>>(W, out, nblocks);
+    qg_dequant_q4k_kernel<<<static_cast<unsigned>((threads + 255) / 256), 256, 0, s>>>(W, out, nblocks);
     return launch_status();
 }
 
 int launch_dequant_iq3(const uint8_t* W, const uint8_t* grid, float* out, int64_t N, int64_t K, cudaStream_t s) {
     const int64_t nblocks = N * (K / 256);
     const int64_t threads = nblocks * 8;
-    dequant_iq3_kernel<FmtIQ3T><<<static_cast<unsigned>((threads + 255) / 256), 256, 0, s>>>(W, grid, out, nblocks);
+    qg_dequant_iq3_kernel<FmtIQ3T><<<static_cast<unsigned>((threads + 255) / 256), 256, 0, s>>>(W, grid, out, nblocks);
     return launch_status();
 }
 
 int launch_dequant_iq3xxs(const uint8_t* W, const uint8_t* grid, float* out, int64_t N, int64_t K, cudaStream_t s) {
     const int64_t nblocks = N * (K / 256);
     const int64_t threads = nblocks * 8;
-    dequant_iq3_kernel<FmtIQ3XXST><<<static_cast<unsigned>((threads + 255) / 256), 256, 0, s>>>(W, grid, out,
+    qg_dequant_iq3_kernel<FmtIQ3XXST><<<static_cast<unsigned>((threads + 255) / 256), 256, 0, s>>>(W, grid, out,
                                                                                               nblocks);
     return launch_status();
 }

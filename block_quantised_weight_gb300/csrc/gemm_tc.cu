@@ -254,7 +254,7 @@ __device__ __forceinline__ void dequant_half_iq3(const uint8_t* boxrow, const fl
 
 template <bool IQ3>
 __global__ void __launch_bounds__(kThreads, 1)
-    gemm_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
+    qg_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
                    const uint8_t* __restrict__ grid, float* __restrict__ Y, int M, int64_t N, int64_t K, int nraw,
                    unsigned* status) {
     extern __shared__ __align__(1024) uint8_t smem[];
@@ -469,7 +469,7 @@ int launch_tc(const uint8_t* W, const uint8_t* grid, const float* X, float* Y, i
     if (nraw < 2) return QG_EINVAL;
     const int smem = raw0 + nraw * tc::raw_stage_bytes(M);
     if (!attr_done[dev].load(std::memory_order_acquire)) {
-        if (cudaFuncSetAttribute(tc::gemm_tc_kernel<IQ3>, cudaFuncAttributeMaxDynamicSharedMemorySize, tc::kSmemMax) !=
+        if (cudaFuncSetAttribute(tc::qg_gemm_tc_kernel<IQ3>, cudaFuncAttributeMaxDynamicSharedMemorySize, tc::kSmemMax) !=
             cudaSuccess)
             return qg::cuda_fail(cudaGetLastError());
         attr_done[dev].store(true, std::memory_order_release);
@@ -497,7 +497,7 @@ int launch_tc(const uint8_t* W, const uint8_t* grid, const float* X, float* Y, i
     if (cudaMemsetAsync(Y, 0, static_cast<size_t>(M) * N * sizeof(float), s) != cudaSuccess) return qg::cuda_fail(cudaGetLastError());
     const int64_t units = ((N + tc::kTileRows - 1) / tc::kTileRows) * (K / 256);
     const int gridx = static_cast<int>(std::min<int64_t>(units, sms));
-    tc::gemm_tc_kernel<IQ3><<<gridx, tc::kThreads, smem, s>>>(tmW, tmX, grid, Y, M, N, K, nraw, status);
+    tc::qg_gemm_tc_kernel<IQ3><<<gridx, tc::kThreads, smem, s>>>(tmW, tmX, grid, Y, M, N, K, nraw, status);
     return launch_status();
 }
 

@@ -182,7 +182,7 @@ constexpr int kDepth = 4;  // consecutive sub-blocks a lane loads before decodin
 // warp-wide broadcasts and each lane reads a contiguous stretch of its row.
 // The 8 warps' partial sums meet in shared memory.
 template <int F, int MT>
-__global__ void __launch_bounds__(256) gemv_cb_kernel(const uint8_t* __restrict__ W, const void* __restrict__ book,
+__global__ void __launch_bounds__(256) qg_gemv_cb_kernel(const uint8_t* __restrict__ W, const void* __restrict__ book,
                                                       const float* __restrict__ X, float* __restrict__ Y, int M,
                                                       int64_t N, int64_t K) {
     __shared__ Table T;
@@ -371,7 +371,7 @@ __host__ __device__ constexpr int cb_stage_bytes(int F, int MT) {
 
 template <int F, int MT, int MINB>
 __global__ void __launch_bounds__(kCbCols * 32 + 32, MINB)
-    gemv_cb_tma_kernel(const __grid_constant__ CUtensorMap tmW, const void* __restrict__ book,
+    qg_gemv_cb_tma_kernel(const __grid_constant__ CUtensorMap tmW, const void* __restrict__ book,
                        const float* __restrict__ X, float* __restrict__ Y, int M, int64_t N, int64_t K, int stages,
                        unsigned* status) {
     extern __shared__ __align__(1024) uint8_t smem[];
@@ -504,7 +504,7 @@ int launch_tma(const uint8_t* W, const void* book, const float* X, float* Y, int
     const int budget = std::min(kSmemPerCTA, kSmemPerSM / MINB - kSmemReserve) - kCbRing0;
     const int stages = std::min(kCbMaxStages, budget / cb_stage_bytes(F, MT));
     if (stages < 2) return QG_EINVAL;
-    auto kern = gemv_cb_tma_kernel<F, MT, MINB>;
+    auto kern = qg_gemv_cb_tma_kernel<F, MT, MINB>;
     if (!attr_done[dev].load(std::memory_order_acquire)) {
         if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  std::min(kSmemPerCTA, kCbRing0 + kCbMaxStages * cb_stage_bytes(F, MT))) !=
@@ -525,7 +525,7 @@ int launch_tma(const uint8_t* W, const void* book, const float* X, float* Y, int
 
 // Test-only: every sub-block's 32 values (exact), one thread per sub-block.
 template <int F>
-__global__ void __launch_bounds__(256) dequant_cb_kernel(const uint8_t* __restrict__ W, const void* __restrict__ book,
+__global__ void __launch_bounds__(256) qg_dequant_cb_kernel(const uint8_t* __restrict__ W, const void* __restrict__ book,
                                                          float* __restrict__ out, int64_t N, int64_t K) {
     __shared__ Table T;
     load_table<F>(book, T);
@@ -569,11 +569,11 @@ int launch_t(const uint8_t* W, const void* book, const float* X, float* Y, int M
         const float* Xg = X + static_cast<int64_t>(m0) * K;
         float* Yg = Y + static_cast<int64_t>(m0) * N;
         if (mg == 1)
-            gemv_cb_kernel<F, 1><<<blocks, 256, 0, s>>>(W, book, Xg, Yg, mg, N, K);
+            qg_gemv_cb_kernel<F, 1><<<blocks, 256, 0, s>>>(W, book, Xg, Yg, mg, N, K);
         else if (mg <= 4)
-            gemv_cb_kernel<F, 4><<<blocks, 256, 0, s>>>(W, book, Xg, Yg, mg, N, K);
+            qg_gemv_cb_kernel<F, 4><<<blocks, 256, 0, s>>>(W, book, Xg, Yg, mg, N, K);
         else
-            gemv_cb_kernel<F, 8><<<blocks, 256, 0, s>>>(W, book, Xg, Yg, mg, N, K);
+            qg_gemv_cb_kernel<F, 8><<<blocks, 256, 0, s>>>(W, book, Xg, Yg, mg, N, K);
         if (const cudaError_t e = cudaGetLastError(); e != cudaSuccess) return qg::cuda_fail(e);
     }
     return QG_OK;
@@ -582,7 +582,7 @@ int launch_t(const uint8_t* W, const void* book, const float* X, float* Y, int M
 template <int F>
 int dequant_t(const uint8_t* W, const void* book, float* out, int64_t N, int64_t K, cudaStream_t s) {
     const int64_t threads = N * (K / 32);
-    dequant_cb_kernel<F><<<static_cast<unsigned>((threads + 255) / 256), 256, 0, s>>>(W, book, out, N, K);
+    qg_dequant_cb_kernel<F><<<static_cast<unsigned>((threads + 255) / 256), 256, 0, s>>>(W, book, out, N, K);
     return launch_status();
 }
 

@@ -1,32 +1,45 @@
 // Fused-dequantisation GEMV over block-quantised weights, fp32 FMA path.
 //
-//   Y[m][n] = sum_k w[n][k] * X[m][k],   m < MT <= 8 tokens per launch
+//   Y[m][n] = sum_k w[n][k] * X[m][k],   m < MT <= 4 tokens per launch
 //
-// w is never materialised: each consumer thread decodes one 256-weight
-// super-block in registers and dots it with x.  Formats:
+// w is never materialised: it is decoded in registers from the block bytes
+// and dotted with x.  Formats:
 //   Q4_K  page 1 "Rewriting picoLM in Python", dequantize_q4_K
-//   IQ3   page 4 "iq3_pack.py" (fmt=5), module docstring and decode
+//   IQ3   page 4 "iq3_pack.py" (fmt=5), module docstring and decode, and
+//         page 3's IQ3_XXS byte order of the same fields
 //
-// CTA = RG row groups x 8 consumer warps + 1 producer warp.
-//   * A tile is RG*32 consecutive rows; the CTA walks the tile's K range in
-//     chunks of 8 super-block columns ("units").
-//   * The producer warp posts, per unit, one cp.async.bulk per row (the row's
-//     8 blocks are contiguous in HBM) into a padded smem slot, plus one copy
-//     per token of the matching x slice, on the stage's `full` mbarrier.  It
-//     reuses a stage once all consumer warps have arrived on its `empty`
-//     mbarrier: no CTA-wide barrier in the steady state.
-//   * Consumer warp (rg, c): lane r decodes block (row rg*32 + r, column c).
-//     The 8 lanes of a quarter-warp read 8 different rows: the smem row
-//     stride is an odd multiple of 16 bytes, so the 16-byte loads are
-//     conflict-free; all 32 lanes read the same x (broadcast).
+// CTA = RG row groups x 8 consumer warps + 1 producer warp; a tile is RG*32
+// consecutive rows, walked in units of 8 super-block columns.
+//   * The producer warp posts, per unit, one 2D tensor-map TMA
+//     (cp.async.bulk.tensor) per super-block column, a [tile rows][box] box
+//     of that column's blocks, plus the x slice of each token (Q4_K: one bulk
+//     copy per token, contiguous; IQ3: one tensor-map box per token in a
+//     padded layout), all completing on the stage's `full` mbarrier.  It
+//     reuses a stage once every consumer warp has arrived on its `empty`
+//     mbarrier: no CTA-wide barrier in the steady state.  With the
+//     weight-prefetch flag the weights of the first stages are posted before
+//     the programmatic-dependent-launch wait, x after it.
+//   * Consumer warp (rg, c) takes block column c.  Lane L decodes two rows,
+//     L&15 and (L&15)+16 of its row group, half L>>4 of each block (128
+//     weights), so every x load serves two rows; the halves of a row meet in
+//     one shuffle when the tile ends.  Box rows of 144 B (Q4_K) or 112 B
+//     (IQ3) are odd multiples of 16 bytes, so eight lanes loading eight rows
+//     with 16-byte loads hit eight distinct bank groups.
 //   * Per-row partial sums stay in registers across a tile's units and are
 //     reduced over the 8 column warps through a double-buffered smem array
-//     once per tile (one named barrier among the consumers).
+//     once per tile (one named barrier among the consumers), or across a
+//     cluster's CTAs through DSMEM when the tile's K is split over a cluster.
 //
-// Q4_K arithmetic: for sub-block j,
-//   sum_l (d*sc_j*q_l - dmin*mn_j) * x_l = (d*sc_j) * sum_l q_l*x_l - (dmin*mn_j) * sum_l x_l
-// and sum_l x_l is computed once per (column, token) by the warp, shared by
-// its 32 rows.
+// Q4_K arithmetic, sub-block j (a = d*sc_j, b = dmin*mn_j, c the integer in
+// [0, 15] nearest b/a; see q4k_offset):
+//   sum_l (a*q_l - b) * x_l = a * sum_l (q_l - c) * x_l - (b - a*c) * sum_l x_l
+// sum_l x_l is computed once per (column, token) by the warp, shared by its
+// 32 rows; q_l - c is formed exactly while each nibble is an fp32 subnormal
+// against x pre-scaled by powers of two.  IQ3: magnitudes gathered from a
+// lane-replicated fp16 grid table, signs from a sign-mask table, the
+// sub-block factor d*(0.5+code) applied per sub-block.  Slices of x outside
+// the directly handled range are rescaled by a power of two (see
+// q4k_stage_x and iq3_stage_x).
 #pragma once
 #include <cuda_fp16.h>
 
@@ -109,13 +122,15 @@ struct FmtIQ3XXST : FmtIQ3T {
 
 // IQ3 tables in smem, shared by all consumer warps.
 // Grid: lane-replicated so every gather is conflict-free: for grid row i,
-// lane L reads the 8 bytes at 256*i + 8*L (fp16 magnitudes 0,1 then 2,3).
-// Signs: for each 7-bit sign field s7 two words (T0, T1) with the eight
-// signs s8 (the eighth = parity of the seven) placed so that
-// (T[p >> 1] << (p & 1)) & 0x80008000 is the sign mask of fp16 pair p
-// (weights 2p, 2p+1): in word p >> 1, sign 2p at bit 15 - (p & 1) and sign
-// 2p+1 at bit 31 - (p & 1).  Replicated per half-warp lane: lane L reads the
-// 8 bytes at 128*s7 + 8*(L & 15).
+// lane L reads the 8 bytes at 256*i + 8*L, the row's four bytes laid out as
+// [g0, 0, g1, 0] [g2, 0, g3, 0].  Signs: for each 7-bit sign field s7 two
+// words of sign bytes, [s0 s1 s2 s3] [s4 s5 s6 s7] with s_k = 0x80 when
+// weight k is negative (the eighth sign: the parity of the seven, page 4
+// decode).  One byte permute of a grid word and a sign word then gives an
+// fp32 with the sign of weight k at bit 31 and its grid byte at bits 0-7:
+// the exact value +-g * 2^-149, which q4k-style pre-scaled x (2^88) turns
+// into a normal product.  Replicated per half-warp lane: lane L reads the 8
+// bytes at 128*s7 + 8*(L & 15).
 constexpr int kIQ3GridBytes = 256 * 32 * 8;
 constexpr int kIQ3SignBytes = 128 * 16 * 8;
 constexpr int kIQ3TableBytes = kIQ3GridBytes + kIQ3SignBytes;
@@ -177,7 +192,7 @@ __device__ __forceinline__ int group_find(const Group& G, int64_t tile) {
     return i;
 }
 
-// Dynamic smem layout of gemv_kernel<F, MT, RG> with `stages` stages;
+// Dynamic smem layout of qg_gemv_kernel<F, MT, RG> with `stages` stages;
 // xh = F::kXH when x is staged with the weights, 0 when it is read from
 // global memory.
 __host__ __device__ inline Layout make_layout(bool iq3, int MT, int xh, int RG, int stages, int row_stride,
@@ -230,22 +245,34 @@ __device__ __forceinline__ float half_hi(uint32_t h) {
 // the limit (the true value is below 1e-36 in size there).
 __device__ __forceinline__ float silu(float z) { return __fdividef(z, 1.f + __expf(-z)); }
 
+// Range of the staged x slices that q4k_half2 takes as they are: the
+// largest |x| of a token's 256-value slice in [2^-24, 2^39).  Products of a
+// nibble (at most 15) with x are then normal fp32 numbers after the 2^76..2^88
+// pre-scaling below, and no pre-scaled value overflows.  A slice outside
+// that range (but finite) is first multiplied by 2^-e, e the exponent of its
+// largest |x| clamped to [-100, 100], and the column's partial sums by 2^e
+// afterwards: every finite x is handled, only the cost differs.
+constexpr uint32_t kXExpLo = 127 - 24, kXExpHi = 127 + 39;  // biased exponents
+
 // Per-warp x preparation for one Q4_K super-block column (256 x values per
 // token; half 1, x[128..255], starts XH floats after half 0):
 // sx[m*8 + j] = sum of x over sub-block j (the dmin*mn term's factor), and
-// with SCALE the x values (in smem) are scaled in place by 2^(88-c),
-// c = 4*(high nibble) + 8*(odd byte), the bit offsets at which q4k_half2
-// finds each nibble.  The scaling is exact for |x| < 2^40; larger values
-// overflow to inf.  With FUSE the prologue (kFuseNorm: x * g, sum of x^2
-// into ss; kFuseSwiGLU: silu(x) * up) is applied first, reading g or up at
-// ab (+ m * astride), laid out like x; sx and the scaling see the result.
-// Callers that write x in smem must fence it against the next bulk copy
-// into the same slot.
-template <int MT, bool SCALE, int XH, int FUSE = 0>
-__device__ __forceinline__ void q4k_stage_x(float* xb, int64_t xstride, const float* ab, int64_t astride, float* sx,
-                                            float (&ss)[MT], int M, int lane) {
+// the x values (in smem) are scaled in place by 2^(88-c), c = 4*(high
+// nibble) + 8*(odd byte), the bit offsets at which q4k_half2 finds each
+// nibble.  A token whose slice lies outside the range above is also scaled
+// by 2^-e first (sx too); e2[m] = 2^e then (1 otherwise), and the return
+// value, the same in every lane, says whether any token was.  With FUSE the
+// prologue (kFuseNorm: x * g, sum of x^2 into ss; kFuseSwiGLU: silu(x) * up)
+// is applied first, reading g or up at ab (+ m * astride), laid out like x;
+// the range test, sx and the scaling see the result.  Callers must fence
+// the written x against the next bulk copy into the same slot.
+template <int MT, int XH, int FUSE = 0>
+__device__ __forceinline__ bool q4k_stage_x(float* xb, int64_t xstride, const float* ab, int64_t astride, float* sx,
+                                            float (&ss)[MT], float (&e2)[MT], int M, int lane) {
+    bool rescaled = false;
 #pragma unroll
     for (int m = 0; m < MT; ++m) {
+        e2[m] = 1.f;
         if (MT == 1 || m < M) {
             const int off = (lane >> 4) * XH + ((lane >> 2) & 3) * 32 + (lane & 3) * 8;
             float* xp = xb + m * xstride + off;
@@ -267,56 +294,122 @@ __device__ __forceinline__ void q4k_stage_x(float* xb, int64_t xstride, const fl
                 a = make_float4(silu(a.x) * ua.x, silu(a.y) * ua.y, silu(a.z) * ua.z, silu(a.w) * ua.w);
                 b = make_float4(silu(b.x) * ub.x, silu(b.y) * ub.y, silu(b.z) * ub.z, silu(b.w) * ub.w);
             }
+            // largest |x| of the slice (fmaxf passes over NaN; an all-NaN lane
+            // reads as the largest value and takes the rescaled path, whose
+            // result is NaN as it must be)
+            const float mx = fmaxf(fmaxf(fmaxf(fabsf(a.x), fabsf(a.y)), fmaxf(fabsf(a.z), fabsf(a.w))),
+                                   fmaxf(fmaxf(fabsf(b.x), fabsf(b.y)), fmaxf(fabsf(b.z), fabsf(b.w))));
+            const uint32_t top = __reduce_max_sync(0xffffffffu, __float_as_uint(mx));
+            const uint32_t be = top >> 23;
+            if (top != 0u && (be < kXExpLo || be >= kXExpHi)) {  // the same in every lane
+                const int e = min(max(static_cast<int>(be) - 127, -100), 100);
+                const float s = __uint_as_float(static_cast<uint32_t>(127 - e) << 23);
+                a = make_float4(a.x * s, a.y * s, a.z * s, a.w * s);
+                b = make_float4(b.x * s, b.y * s, b.z * s, b.w * s);
+                e2[m] = __uint_as_float(static_cast<uint32_t>(127 + e) << 23);
+                rescaled = true;
+            }
             float sm = ((a.x + a.y) + (a.z + a.w)) + ((b.x + b.y) + (b.z + b.w));
             sm += __shfl_xor_sync(0xffffffffu, sm, 1);
             sm += __shfl_xor_sync(0xffffffffu, sm, 2);
             if ((lane & 3) == 0) sx[m * 8 + (lane >> 2)] = sm;
-            if constexpr (SCALE) {
-                const float se = ((lane >> 2) & 1) ? 0x1p84f : 0x1p88f;   // even byte
-                const float so = se * 0x1p-8f;                            // odd byte
-                a = make_float4(a.x * se, a.y * so, a.z * se, a.w * so);
-                b = make_float4(b.x * se, b.y * so, b.z * se, b.w * so);
-            }
-            if constexpr (SCALE || FUSE != 0) {
-                *reinterpret_cast<float4*>(xp) = a;
-                *reinterpret_cast<float4*>(xp + 4) = b;
-            }
+            const float se = ((lane >> 2) & 1) ? 0x1p84f : 0x1p88f;  // even byte
+            const float so = se * 0x1p-8f;                           // odd byte
+            a = make_float4(a.x * se, a.y * so, a.z * se, a.w * so);
+            b = make_float4(b.x * se, b.y * so, b.z * se, b.w * so);
+            *reinterpret_cast<float4*>(xp) = a;
+            *reinterpret_cast<float4*>(xp + 4) = b;
         }
     }
+    return rescaled;
+}
+
+// Offset of a Q4_K sub-block with scale a = d*sc and min b = dmin*mn: the
+// integer c in [0, 15] nearest b/a.  For any integer c
+//   sum_l (a*q_l - b)*x_l = a * sum_l (q_l - c)*x_l - (b - a*c) * sum_l x_l,
+// and with the nearest one every term on the right is at most twice the
+// |w*x| of its weight (|b - a*c| <= a/2, and |a*(q - c)| <= 2|a*q - b| for
+// q != c), so the factored sum keeps the accuracy of the per-weight one even
+// where d*sc*q and dmin*mn cancel.  b - a*c is exact in fp32 whenever c > 0
+// (both products are exact and their exponents are close).  a = 0 gives an
+// infinite or NaN quotient: fmaxf drops the NaN and the clamp takes the rest.
+__device__ __forceinline__ float q4k_offset(float a, float b) {
+    return fminf(fmaxf(rintf(__fdividef(b, a)), 0.f), 15.f);
 }
 
 // Half of one Q4_K super-block column for two rows (x pre-scaled by
-// q4k_stage_x with SCALE; half 1 of x XH floats after half 0).  Lane L of a warp takes rows L&15 and (L&15)+16 of the tile and
-// half h = L>>4 of the block (sub-blocks 4h..4h+3, weights 128h..128h+127),
-// so every x load serves two rows; the two halves of a row meet with one
-// shuffle at the end of the tile.  blk: the row-(L&15) block in smem;
-// rstride: bytes from a row to the row 16 below.  The min term
-// dmin*mn*sum(x) is taken first, then the scaled sub-block sums.
-template <int MT, int XH>
+// q4k_stage_x; half 1 of x XH floats after half 0).  Lane L of a warp takes
+// rows L&15 and (L&15)+16 of the tile and half h = L>>4 of the block
+// (sub-blocks 4h..4h+3, weights 128h..128h+127), so every x load serves two
+// rows; the two halves of a row meet with one shuffle at the end of the
+// tile.  blk: the row-(L&15) block in smem; rstride: bytes from a row to the
+// row 16 below.  Per sub-block the offset c above is taken off every nibble
+// while it is still an fp32 subnormal (q*2^-149 - c*2^-149 is exact), the
+// min term is (b - a*c) * sum(x), then the scaled sum of (q - c)*x.  With
+// RESCALE the column's sums are formed apart and multiplied by e2[m] (the
+// 2^e of a token whose slice q4k_stage_x rescaled) before they join acc.
+template <int MT, int XH, bool RESCALE>
 __device__ __forceinline__ void q4k_half2(const uint8_t* blk, int rstride, int h, const float* xb, int64_t xstride,
-                                          const float* sx, int M, float (&acc)[2][MT]) {
-    float d61[2];
-    uint32_t scw[2];
+                                          const float* sx, int M, const float (&e2)[MT], float (&acc)[2][MT]) {
+    if constexpr (RESCALE && MT > 1) {
+        // the rare rescaled column: one token at a time, which needs far fewer
+        // registers than the MT-token decode and its separate column sums
+#pragma unroll
+        for (int m = 0; m < MT; ++m) {
+            if (m < M) {
+                float a1[2][1] = {{acc[0][m]}, {acc[1][m]}};
+                const float e1[1] = {e2[m]};
+                q4k_half2<1, XH, true>(blk, rstride, h, xb + m * xstride, xstride, sx + m * 8, 1, e1, a1);
+                acc[0][m] = a1[0][0];
+                acc[1][m] = a1[1][0];
+            }
+        }
+        return;
+    }
+    float dd[2], dm[2];
+    uint32_t scw[2], mnw[2];
 #pragma unroll
     for (int j = 0; j < 2; ++j) {
         const uint4 hd = *reinterpret_cast<const uint4*>(blk + j * rstride);
-        d61[j] = h2f(hd.x) * 0x1p61f;
-        const float dmin = h2f(hd.x >> 16);
+        dd[j] = h2f(hd.x);
+        dm[j] = h2f(hd.x >> 16);
         // scales / mins of sub-blocks 4h..4h+3 (page 1 packing: j >= 4 straddles)
         scw[j] = h ? ((hd.w & 0x0F0F0F0Fu) | ((hd.y >> 2) & 0x30303030u)) : (hd.y & 0x3F3F3F3Fu);
-        const uint32_t mnw = h ? (((hd.w >> 4) & 0x0F0F0F0Fu) | ((hd.z >> 2) & 0x30303030u)) : (hd.z & 0x3F3F3F3Fu);
+        mnw[j] = h ? (((hd.w >> 4) & 0x0F0F0F0Fu) | ((hd.z >> 2) & 0x30303030u)) : (hd.z & 0x3F3F3F3Fu);
+    }
+    float part[2][MT];
+    float (&tgt)[2][MT] = RESCALE ? part : acc;
+    if constexpr (RESCALE) {
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            const float dmn = dmin * byte_f(mnw, k);
+        for (int j = 0; j < 2; ++j)
 #pragma unroll
-            for (int m = 0; m < MT; ++m)
-                if (MT == 1 || m < M) acc[j][m] = fmaf(-dmn, sx[m * 8 + 4 * h + k], acc[j][m]);
-        }
+            for (int m = 0; m < MT; ++m) part[j][m] = 0.f;
     }
     const uint8_t* qb = blk + 16 + 64 * h;
     const float* xq = xb + XH * h;
 #pragma unroll
     for (int g = 0; g < 2; ++g) {
+        // sub-blocks 4h+2g (low nibbles) and 4h+2g+1 (high nibbles) of each row
+        float al61[2], ah61[2];  // a * 2^61 (the pre-scaling of x is 2^-61 in the products)
+        f2 ol[2], oh[2];         // -c at the subnormal scales of the nibbles' bit offsets
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            const float a0 = dd[j] * byte_f(scw[j], 2 * g), a1 = dd[j] * byte_f(scw[j], 2 * g + 1);
+            const float b0 = dm[j] * byte_f(mnw[j], 2 * g), b1 = dm[j] * byte_f(mnw[j], 2 * g + 1);
+            const float c0 = q4k_offset(a0, b0), c1 = q4k_offset(a1, b1);
+            const float r0 = fmaf(-a0, c0, b0), r1 = fmaf(-a1, c1, b1);
+#pragma unroll
+            for (int m = 0; m < MT; ++m) {
+                if (MT == 1 || m < M) {
+                    tgt[j][m] = fmaf(-r0, sx[m * 8 + 4 * h + 2 * g], tgt[j][m]);
+                    tgt[j][m] = fmaf(-r1, sx[m * 8 + 4 * h + 2 * g + 1], tgt[j][m]);
+                }
+            }
+            al61[j] = a0 * 0x1p61f;
+            ah61[j] = a1 * 0x1p61f;
+            ol[j] = fmul2(f2{c0, c0}, f2{-0x1p-149f, -0x1p-141f});
+            oh[j] = fmul2(f2{c1, c1}, f2{-0x1p-145f, -0x1p-137f});
+        }
         f2 al[2][MT], ah[2][MT];
 #pragma unroll
         for (int j = 0; j < 2; ++j)
@@ -342,10 +435,15 @@ __device__ __forceinline__ void q4k_half2(const uint8_t* blk, int rstride, int h
                 for (int j = 0; j < 2; ++j) {
                     const uint32_t v = e == 0 ? q[j].x : e == 1 ? q[j].y : e == 2 ? q[j].z : q[j].w;
                     const uint32_t u = v >> 16;
-                    const f2 l01{__uint_as_float(v & 0xFu), __uint_as_float(v & 0xF00u)};
-                    const f2 l23{__uint_as_float(u & 0xFu), __uint_as_float(u & 0xF00u)};
-                    const f2 h01{__uint_as_float(v & 0xF0u), __uint_as_float(v & 0xF000u)};
-                    const f2 h23{__uint_as_float(u & 0xF0u), __uint_as_float(u & 0xF000u)};
+                    // each nibble in place as an fp32 subnormal, then q - c
+                    f2 l01{__uint_as_float(v & 0xFu), __uint_as_float(v & 0xF00u)};
+                    f2 l23{__uint_as_float(u & 0xFu), __uint_as_float(u & 0xF00u)};
+                    f2 h01{__uint_as_float(v & 0xF0u), __uint_as_float(v & 0xF000u)};
+                    f2 h23{__uint_as_float(u & 0xF0u), __uint_as_float(u & 0xF000u)};
+                    fadd2(l01, ol[j]);
+                    fadd2(l23, ol[j]);
+                    fadd2(h01, oh[j]);
+                    fadd2(h23, oh[j]);
 #pragma unroll
                     for (int m = 0; m < MT; ++m) {
                         if (MT == 1 || m < M) {
@@ -360,33 +458,42 @@ __device__ __forceinline__ void q4k_half2(const uint8_t* blk, int rstride, int h
         }
 #pragma unroll
         for (int j = 0; j < 2; ++j) {
-            const float dl = d61[j] * byte_f(scw[j], 2 * g);
-            const float dh = d61[j] * byte_f(scw[j], 2 * g + 1);
 #pragma unroll
             for (int m = 0; m < MT; ++m) {
                 if (MT == 1 || m < M) {
-                    acc[j][m] = fmaf(dl, al[j][m].x + al[j][m].y, acc[j][m]);
-                    acc[j][m] = fmaf(dh, ah[j][m].x + ah[j][m].y, acc[j][m]);
+                    tgt[j][m] = fmaf(al61[j], al[j][m].x + al[j][m].y, tgt[j][m]);
+                    tgt[j][m] = fmaf(ah61[j], ah[j][m].x + ah[j][m].y, tgt[j][m]);
                 }
             }
         }
     }
+    if constexpr (RESCALE) {
+#pragma unroll
+        for (int j = 0; j < 2; ++j)
+#pragma unroll
+            for (int m = 0; m < MT; ++m)
+                if (MT == 1 || m < M) acc[j][m] = fmaf(part[j][m], e2[m], acc[j][m]);
+    }
 }
 
-// Sign words (T0, T1) of the sign field at bits 7l..7l+6 of sw (see
+// Sign words (S0, S1) of the sign field at bits 7l..7l+6 of sw (see
 // kIQ3SignBytes); lane_s = 8 * (lane & 15).
 __device__ __forceinline__ uint2 iq3_signs(const uint8_t* sg, uint32_t sw, int l, uint32_t lane_s) {
     const uint32_t off = (l == 0 ? (sw << 7) : (sw >> (7 * l - 7))) & 0x3F80u;
     return *reinterpret_cast<const uint2*>(sg + (off | lane_s));
 }
-// An fp16 pair of the grid row, sign flipped by sign word t shifted by q:
-// pair p takes word p >> 1 and q = p & 1.
-__device__ __forceinline__ uint32_t iq3_flip(uint32_t g, uint32_t t, int q) { return g ^ ((t << q) & 0x80008000u); }
 
-// Grid row of the index byte `byte` of word w: 8 bytes (two fp16 pairs).
+// Grid row of the index byte `byte` of word w: 8 bytes [g0,0,g1,0][g2,0,g3,0].
 __device__ __forceinline__ uint2 iq3_grid(const uint8_t* tb, uint32_t w, int byte, uint32_t lane8) {
     const uint32_t off = prmt(w, lane8, 4u | (static_cast<uint32_t>(byte) << 4) | (5u << 8) | (5u << 12));
     return *reinterpret_cast<const uint2*>(tb + off);
+}
+
+// Signed grid value as an fp32 subnormal: byte P of grid word g (P = 0 or 2;
+// bytes 1 and 3 of g are zero) at bits 0-7, sign byte K of s at bits 24-31.
+template <int P, int K>
+__device__ __forceinline__ float iq3_val(uint32_t g, uint32_t s) {
+    return __uint_as_float(prmt(g, s, static_cast<uint32_t>(P) | (1u << 4) | (1u << 8) | ((4u + K) << 12)));
 }
 
 // Half h of the IQ3 super-block of column COL from its 112-byte TMA box row
@@ -420,20 +527,47 @@ __device__ __forceinline__ void iq3_load_half(const uint8_t* boxrow, int h, uint
 
 // Two rows (r, r+16), half h of an IQ3 super-block each, against MT tokens:
 // the layout of q4k_half2 (one x load serves both rows).  xq = x of the
-// block + 128h.
-template <int MT, class F>
+// block + 128h, pre-scaled by 2^88 (iq3_stage_x).  Each weight is one byte
+// permute (iq3_val: grid byte and sign as an fp32 subnormal) and half a
+// packed FMA; the sub-block factor d*(0.5+code)*kDbScale*2^61 undoes the
+// scaling.  With RESCALE the column's sums are formed apart and multiplied
+// by e2[m] (a token whose slice iq3_stage_x rescaled) before they join acc.
+template <int MT, class F, bool RESCALE>
 __device__ __forceinline__ void iq3_half2(const uint32_t (&vi)[2][8], const uint32_t (&vs)[2][4], const uint32_t (&dbits)[2],
                                           const uint8_t* tb, const uint8_t* sg, uint32_t lane8, uint32_t lane_s,
-                                          const float* xq, int64_t xstride, int M, float (&acc)[2][MT]) {
-    // sub-block factor d*(0.5+code)*kDbScale = fma(1 + code/16, 16 d', -15.5 d')
-    // with d' = d*kDbScale: 1 + code/16 is the float with the code as the
-    // top four mantissa bits; every term is exact, so is the result
+                                          const float* xq, int64_t xstride, int M, const float (&e2)[MT],
+                                          float (&acc)[2][MT]) {
+    if constexpr (RESCALE && MT > 1) {
+        // the rare rescaled column: one token at a time (fewer registers)
+#pragma unroll
+        for (int m = 0; m < MT; ++m) {
+            if (m < M) {
+                float a1[2][1] = {{acc[0][m]}, {acc[1][m]}};
+                const float e1[1] = {e2[m]};
+                iq3_half2<1, F, true>(vi, vs, dbits, tb, sg, lane8, lane_s, xq + m * xstride, xstride, 1, e1, a1);
+                acc[0][m] = a1[0][0];
+                acc[1][m] = a1[1][0];
+            }
+        }
+        return;
+    }
+    float part[2][MT];
+    float (&tgt)[2][MT] = RESCALE ? part : acc;
+    if constexpr (RESCALE) {
+#pragma unroll
+        for (int r = 0; r < 2; ++r)
+#pragma unroll
+            for (int m = 0; m < MT; ++m) part[r][m] = 0.f;
+    }
+    // sub-block factor d*(0.5+code)*kDbScale*2^61 = fma(1 + code/16, 16 d', -15.5 d')
+    // with d' = d*kDbScale*2^61: 1 + code/16 is the float with the code as
+    // the top four mantissa bits; every term is exact, so is the result
     float d16[2], d155[2];
 #pragma unroll
     for (int r = 0; r < 2; ++r) {
         const float d = h2f(dbits[r]);
-        d16[r] = d * (16.f * F::kDbScale);
-        d155[r] = d * (15.5f * F::kDbScale);
+        d16[r] = d * (16.f * F::kDbScale * 0x1p61f);
+        d155[r] = d * (15.5f * F::kDbScale * 0x1p61f);
     }
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
@@ -457,9 +591,9 @@ __device__ __forceinline__ void iq3_half2(const uint32_t (&vi)[2][8], const uint
 #pragma unroll
                 for (int r = 0; r < 2; ++r) {
                     const uint2 g = iq3_grid(tb, vi[r][PI >> 2], PI & 3, lane8);
-                    const uint32_t t = hf ? T[r].y : T[r].x;
-                    const f2 w01 = h2_to_f2(iq3_flip(g.x, t, 0));
-                    const f2 w23 = h2_to_f2(iq3_flip(g.y, t, 1));
+                    const uint32_t t = hf ? T[r].y : T[r].x;  // signs of weights 4hf..4hf+3 of the field
+                    const f2 w01{iq3_val<0, 0>(g.x, t), iq3_val<2, 1>(g.x, t)};
+                    const f2 w23{iq3_val<0, 2>(g.y, t), iq3_val<2, 3>(g.y, t)};
 #pragma unroll
                     for (int m = 0; m < MT; ++m) {
                         if (MT == 1 || m < M) {
@@ -476,9 +610,54 @@ __device__ __forceinline__ void iq3_half2(const uint32_t (&vi)[2][8], const uint
             const float db = fmaf(f, d16[r], -d155[r]);
 #pragma unroll
             for (int m = 0; m < MT; ++m)
-                if (MT == 1 || m < M) acc[r][m] = fmaf(db, dot[r][m].x + dot[r][m].y, acc[r][m]);
+                if (MT == 1 || m < M) tgt[r][m] = fmaf(db, dot[r][m].x + dot[r][m].y, tgt[r][m]);
         }
     }
+    if constexpr (RESCALE) {
+#pragma unroll
+        for (int r = 0; r < 2; ++r)
+#pragma unroll
+            for (int m = 0; m < MT; ++m)
+                if (MT == 1 || m < M) acc[r][m] = fmaf(part[r][m], e2[m], acc[r][m]);
+    }
+}
+
+// Per-warp x preparation for one IQ3 column (the warp's own copy, 256
+// values per token, halves XH floats apart): every value scaled in place by
+// 2^88, so that a grid byte held as an fp32 subnormal (g * 2^-149) times x
+// is a normal number.  A token whose largest |x| lies outside [2^-24, 2^39)
+// (the range of q4k_stage_x) is first scaled by 2^-e as well, e the exponent
+// of its largest |x| clamped to [-100, 100]; e2[m] = 2^e then (1 otherwise),
+// and the return value, the same in every lane, says whether any token was.
+// Callers must fence the written x against the next copy into the slot.
+template <int MT, int XH>
+__device__ __forceinline__ bool iq3_stage_x(float* xb, int64_t xstride, int M, int lane, float (&e2)[MT]) {
+    bool rescaled = false;
+#pragma unroll
+    for (int m = 0; m < MT; ++m) {
+        e2[m] = 1.f;
+        if (MT == 1 || m < M) {
+            float* xp = xb + m * xstride + (lane >> 4) * XH + (lane & 15) * 8;
+            float4 a = *reinterpret_cast<const float4*>(xp);
+            float4 b = *reinterpret_cast<const float4*>(xp + 4);
+            const float mx = fmaxf(fmaxf(fmaxf(fabsf(a.x), fabsf(a.y)), fmaxf(fabsf(a.z), fabsf(a.w))),
+                                   fmaxf(fmaxf(fabsf(b.x), fabsf(b.y)), fmaxf(fabsf(b.z), fabsf(b.w))));
+            const uint32_t top = __reduce_max_sync(0xffffffffu, __float_as_uint(mx));
+            const uint32_t be = top >> 23;
+            if (top != 0u && (be < kXExpLo || be >= kXExpHi)) {  // the same in every lane
+                const int e = min(max(static_cast<int>(be) - 127, -100), 100);
+                const float s = __uint_as_float(static_cast<uint32_t>(127 - e) << 23);
+                a = make_float4(a.x * s, a.y * s, a.z * s, a.w * s);
+                b = make_float4(b.x * s, b.y * s, b.z * s, b.w * s);
+                e2[m] = __uint_as_float(static_cast<uint32_t>(127 + e) << 23);
+                rescaled = true;
+            }
+            constexpr float k88 = 0x1p88f;
+            *reinterpret_cast<float4*>(xp) = make_float4(a.x * k88, a.y * k88, a.z * k88, a.w * k88);
+            *reinterpret_cast<float4*>(xp + 4) = make_float4(b.x * k88, b.y * k88, b.z * k88, b.w * k88);
+        }
+    }
+    return rescaled;
 }
 
 __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
@@ -518,6 +697,9 @@ template <int N>
 __device__ __forceinline__ void named_barrier_sync(int id) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "n"(N) : "memory");
 }
+__device__ __forceinline__ void named_barrier_sync_n(int id, int n) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
 
 // ------------------------------------------------------------ the kernel
 // Threads: RG*8 consumer warps, then one producer warp.
@@ -526,7 +708,7 @@ __device__ __forceinline__ void named_barrier_sync(int id) {
 // (L&15)+16, half L>>4 of each block).
 template <class F, int MT, int RG, int MINB, int FUSE = 0>
 __global__ void __launch_bounds__(RG * F::kCols * 32 + 32, MINB)
-    gemv_kernel(const __grid_constant__ Group G, const __grid_constant__ TMaps T, const __grid_constant__ Fuse Fz,
+    qg_gemv_kernel(const __grid_constant__ Group G, const __grid_constant__ TMaps T, const __grid_constant__ Fuse Fz,
                 const uint8_t* __restrict__ grid, const float* __restrict__ X, int M, int64_t K, int stages,
                 unsigned* status, int flags) {
     constexpr int kWarps = RG * F::kCols;          // consumer warps
@@ -563,30 +745,21 @@ __global__ void __launch_bounds__(RG * F::kCols * 32 + 32, MINB)
         fence_mbar_init();
     }
     if constexpr (F::kIQ3) {
-        // fp16 copies of the doubled-unit magnitudes (exact: bytes < 2048)
+        // grid rows as bytes [g0, 0, g1, 0] [g2, 0, g3, 0], 32 lane copies
         uint32_t* tbl = reinterpret_cast<uint32_t*>(smem + L.table);
         for (int i = threadIdx.x; i < 256 * 32; i += blockDim.x) {
-            const int row = i >> 5;
-            const uint32_t g = *reinterpret_cast<const uint32_t*>(grid + 4 * row);
-            const __half2 a = __floats2half2_rn(byte_f(g, 0), byte_f(g, 1));
-            const __half2 b = __floats2half2_rn(byte_f(g, 2), byte_f(g, 3));
-            tbl[2 * i] = *reinterpret_cast<const uint32_t*>(&a);
-            tbl[2 * i + 1] = *reinterpret_cast<const uint32_t*>(&b);
+            const uint32_t g = *reinterpret_cast<const uint32_t*>(grid + 4 * (i >> 5));
+            tbl[2 * i] = (g & 0xFFu) | ((g & 0xFF00u) << 8);
+            tbl[2 * i + 1] = ((g >> 16) & 0xFFu) | ((g >> 8) & 0xFF0000u);
         }
-        // sign masks: s8 = the seven stored signs + their parity (page 4,
-        // decode); sign k goes to bit 15 (k even) or 31 (k odd) of pair k/2
+        // sign bytes: s8 = the seven stored signs + their parity (page 4,
+        // decode); word h holds weights 4h..4h+3, 0x80 in byte k if negative
         uint32_t* sgt = reinterpret_cast<uint32_t*>(smem + L.table + kIQ3GridBytes);
         for (int i = threadIdx.x; i < 128 * 32; i += blockDim.x) {
-            const uint32_t s7 = static_cast<uint32_t>(i) >> 5;  // 32 words per field: 16 copies of (T0, T1)
+            const uint32_t s7 = static_cast<uint32_t>(i) >> 5;  // 32 words per field: 16 copies of (S0, S1)
             const uint32_t s8 = s7 | ((__popc(s7) & 1u) << 7);
-            const int half = i & 1;  // word T0 (pairs 0, 1) or T1 (pairs 2, 3)
-            uint32_t t = 0;
-#pragma unroll
-            for (int q = 0; q < 2; ++q) {
-                const int pr = 2 * half + q;
-                t |= (((s8 >> (2 * pr)) & 1u) << (15 - q)) | (((s8 >> (2 * pr + 1)) & 1u) << (31 - q));
-            }
-            sgt[i] = t;
+            const uint32_t nib = (s8 >> (4 * (i & 1))) & 15u;
+            sgt[i] = ((nib & 1u) << 7) | ((nib & 2u) << 14) | ((nib & 4u) << 21) | ((nib & 8u) << 28);
         }
     }
     __syncthreads();
@@ -756,10 +929,15 @@ __global__ void __launch_bounds__(RG * F::kCols * 32 + 32, MINB)
             if constexpr (!F::kIQ3) {
                 float* sxp = sxw + warp * MT * 8;
                 const float* ab = reinterpret_cast<const float*>(st + L.aoff) + cw * 256;
-                q4k_stage_x<MT, true, XH, FUSE>(const_cast<float*>(xb), xstride, ab, F::kCols * 256, sxp, ss, M, lane);
+                float e2[MT];
+                const bool rescaled =
+                    q4k_stage_x<MT, XH, FUSE>(const_cast<float*>(xb), xstride, ab, F::kCols * 256, sxp, ss, e2, M, lane);
                 __syncwarp();
                 const uint8_t* blk = st + cw * (kTileRows * F::kBytes) + (lane & 15) * F::kBytes;
-                q4k_half2<MT, XH>(blk, 16 * F::kBytes, lane >> 4, xb, xstride, sxp, M, acc2);
+                if (rescaled)  // x outside the direct range (rare; the same in every lane)
+                    q4k_half2<MT, XH, true>(blk, 16 * F::kBytes, lane >> 4, xb, xstride, sxp, M, e2, acc2);
+                else
+                    q4k_half2<MT, XH, false>(blk, 16 * F::kBytes, lane >> 4, xb, xstride, sxp, M, e2, acc2);
                 fence_proxy_async_smem();  // x was written: order it before the slot's next copy
             } else {
                 // two rows per lane, half a block each (TMA layout): rows
@@ -782,7 +960,41 @@ __global__ void __launch_bounds__(RG * F::kCols * 32 + 32, MINB)
 #undef QG_IQ3_HALF
                 }
                 const uint8_t* tb = smem + L.table;
-                iq3_half2<MT, F>(vi, vs, dbits, tb, tb + kIQ3GridBytes, lane8, lane_s, xb + XH * hl, xstride, M, acc2);
+                float e2[MT];
+                bool rescaled;
+                if constexpr (RG == 1) {
+                    rescaled = iq3_stage_x<MT, XH>(const_cast<float*>(xb), xstride, M, lane, e2);
+                    __syncwarp();
+                } else {
+                    // the column's x is shared by its RG warps: row group 0
+                    // scales it and publishes the rescale factors (slots
+                    // alternate with the unit, so a slot is rewritten only
+                    // after both warps passed the next unit's barrier), then
+                    // the column's warps meet on a named barrier
+                    float* ef = reinterpret_cast<float*>(smem + L.ss) + ((u & 1) * F::kCols + cw) * MT;
+                    if (rg == 0) {
+                        rescaled = iq3_stage_x<MT, XH>(const_cast<float*>(xb), xstride, M, lane, e2);
+                        if (lane == 0)
+#pragma unroll
+                            for (int m = 0; m < MT; ++m) ef[m] = e2[m];  // the same in every lane
+                    }
+                    named_barrier_sync_n(2 + cw, RG * 32);
+                    if (rg != 0) {
+                        rescaled = false;
+#pragma unroll
+                        for (int m = 0; m < MT; ++m) {
+                            e2[m] = ef[m];
+                            rescaled |= e2[m] != 1.f;
+                        }
+                    }
+                }
+                if (rescaled)  // rare; the same in every lane
+                    iq3_half2<MT, F, true>(vi, vs, dbits, tb, tb + kIQ3GridBytes, lane8, lane_s, xb + XH * hl, xstride,
+                                           M, e2, acc2);
+                else
+                    iq3_half2<MT, F, false>(vi, vs, dbits, tb, tb + kIQ3GridBytes, lane8, lane_s, xb + XH * hl,
+                                            xstride, M, e2, acc2);
+                fence_proxy_async_smem();  // x was written: order it before the slot's next copy
             }
         }
         __syncwarp();

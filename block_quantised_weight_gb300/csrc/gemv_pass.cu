@@ -5,7 +5,7 @@
 // q/k/v read the attention-norm output, gate/up the FFN-norm output), and
 // stage s+1 may read what stage s wrote.  One cooperative launch (all CTAs
 // resident) walks every stage with the same producer/consumer pipeline as
-// gemv_kernel; between stages a grid-wide completion count replaces the
+// qg_gemv_kernel; between stages a grid-wide completion count replaces the
 // kernel boundary:
 //   * each CTA, after writing its last Y of stage s (named barrier among its
 //     consumers, then __threadfence), adds 1 to sync[s];
@@ -43,22 +43,48 @@ __device__ __forceinline__ uint32_t ld_acquire(const unsigned* p) {
     return v;
 }
 
+__device__ __forceinline__ uint32_t ld_volatile(const unsigned* p) {
+    uint32_t v;
+    asm volatile("ld.volatile.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
 // Bounded wait until *p >= target.  Returns false (timeout bit set) on expiry.
-__device__ __forceinline__ bool wait_count(const unsigned* p, uint32_t target, unsigned* status) {
+// Fails fast, without waiting, once this CTA has given up on an earlier
+// count (gave_up) or once the status word carries a timeout that it did not
+// carry when the kernel started (status0): a pass whose counts were reset
+// under it (an overlapping call on the shared no-allocation scratch) would
+// otherwise wait the full limit at every later stage.  Skipping a count wait
+// only lets x be copied early; every copy still completes before use.
+__device__ __forceinline__ bool wait_count(const unsigned* p, uint32_t target, unsigned* status, uint32_t status0,
+                                           bool& gave_up) {
     if (ld_acquire(p) >= target) return true;
+    if (gave_up) return false;
     const uint64_t t0 = globaltimer_ns();
     for (uint32_t i = 1;; ++i) {
         __nanosleep(64);
         if (ld_acquire(p) >= target) return true;
-        if ((i & 15u) == 0 && globaltimer_ns() - t0 > kWaitLimitNs) break;
+        if ((i & 15u) == 0) {
+            if (globaltimer_ns() - t0 > kWaitLimitNs) break;
+            if ((ld_volatile(status) & ~status0 & kStatusTimeout) != 0u) {  // someone else timed out meanwhile
+                gave_up = true;
+                return false;
+            }
+        }
     }
     atomicOr(status, kStatusTimeout);
+    gave_up = true;
     return false;
 }
 
+// CTAs per SM: two for one and two tokens; a 4-token stage (32 rows of
+// blocks plus 4 x 8 KB of x, 69 KB) needs one CTA per SM to keep two stages.
 template <int MT>
-__global__ void __launch_bounds__(kCols * 32 + 32, 2)
-    gemv_pass_kernel(const __grid_constant__ Plan P, int M, unsigned* sync, int stages, unsigned* status) {
+constexpr int pass_ctas_per_sm() { return MT == 4 ? 1 : 2; }
+
+template <int MT>
+__global__ void __launch_bounds__(kCols * 32 + 32, pass_ctas_per_sm<MT>())
+    qg_gemv_pass_kernel(const __grid_constant__ Plan P, int M, unsigned* sync, int stages, unsigned* status) {
     using F = FmtQ4K;
     constexpr int kWarps = kCols;  // one row group
     constexpr int kConsumerThreads = kWarps * 32;
@@ -88,6 +114,8 @@ __global__ void __launch_bounds__(kCols * 32 + 32, 2)
         uint32_t round = 0;   // completed passes over the ring
         int64_t posted = 0;   // units posted so far (all stages)
         int def_s[kMaxStages], def_c[kMaxStages];
+        const uint32_t status0 = ld_volatile(status);  // timeouts already reported before this launch
+        bool gave_up = false;
         for (int si = 0; si < P.nstages; ++si) {
             const Stage& S = P.st[si];
             const int64_t pitch = static_cast<int64_t>(S.nb) * F::kBytes;
@@ -95,7 +123,7 @@ __global__ void __launch_bounds__(kCols * 32 + 32, 2)
             bool deferring = si > 0;
             int ndef = 0;
             auto release_x = [&]() {
-                if (lane == 0) wait_count(&sync[si - 1], gridDim.x, status);
+                if (lane == 0) wait_count(&sync[si - 1], gridDim.x, status, status0, gave_up);
                 __syncwarp();
                 asm volatile("fence.proxy.async.global;" ::: "memory");
                 for (int k = 0; k < ndef; ++k) {
@@ -166,13 +194,17 @@ __global__ void __launch_bounds__(kCols * 32 + 32, 2)
                         const float* xb = reinterpret_cast<const float*>(st + L.xoff) + cw * 256;
                         constexpr int64_t xstride = kCols * 256;
                         float* sxp = sxw + warp * MT * 8;
-                        float ssq[MT];  // unused: no prologue here
-                        q4k_stage_x<MT, true, 128>(const_cast<float*>(xb), xstride, nullptr, 0, sxp, ssq, M, lane);
+                        float ssq[MT], e2[MT];  // ssq unused: no prologue here
+                        const bool rescaled =
+                            q4k_stage_x<MT, 128>(const_cast<float*>(xb), xstride, nullptr, 0, sxp, ssq, e2, M, lane);
                         __syncwarp();
                         // two rows per lane, half a block each (same arithmetic as the
                         // single-launch GEMV; rows past the tile end are discarded)
-                        q4k_half2<MT, 128>(st + (lane & 15) * F::kRowStride + cw * F::kBytes, 16 * F::kRowStride, lane >> 4,
-                                      xb, xstride, sxp, M, acc);
+                        const uint8_t* blk = st + (lane & 15) * F::kRowStride + cw * F::kBytes;
+                        if (rescaled)
+                            q4k_half2<MT, 128, true>(blk, 16 * F::kRowStride, lane >> 4, xb, xstride, sxp, M, e2, acc);
+                        else
+                            q4k_half2<MT, 128, false>(blk, 16 * F::kRowStride, lane >> 4, xb, xstride, sxp, M, e2, acc);
                         fence_proxy_async_smem();  // x was written: order it before the slot's next copy
                     }
                     __syncwarp();
@@ -223,12 +255,13 @@ template <int MT>
 int launch_pass_t(const pass::Plan& plan, int M, unsigned* sync, cudaStream_t s, unsigned* status, int dev) {
     static std::atomic<bool> attr_done[64];
     static std::atomic<int> occ_cache[64];
-    const int budget = kSmemPerSM / 2 - kSmemReserve;
+    constexpr int kCtas = pass::pass_ctas_per_sm<MT>();
+    const int budget = std::min(kSmemPerCTA, kSmemPerSM / kCtas - kSmemReserve);
     const Layout L1 = make_layout(false, MT, FmtQ4K::kXH, 1, 1, FmtQ4K::kRowStride);
     int stages = std::min(kMaxStages, (budget - L1.stage0) / L1.stage_bytes);
     if (stages < 2) return QG_EINVAL;
     const Layout L = make_layout(false, MT, FmtQ4K::kXH, 1, stages, FmtQ4K::kRowStride);
-    auto kern = pass::gemv_pass_kernel<MT>;
+    auto kern = pass::qg_gemv_pass_kernel<MT>;
     if (!attr_done[dev].load(std::memory_order_acquire)) {
         if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L.total) != cudaSuccess)
             return qg::cuda_fail(cudaGetLastError());
@@ -241,7 +274,7 @@ int launch_pass_t(const pass::Plan& plan, int M, unsigned* sync, cudaStream_t s,
     }
     const int sms = sm_count(dev);
     if (sms <= 0) return qg::cuda_fail(cudaGetLastError());
-    const int grid = sms * std::min(occ_cache[dev].load(std::memory_order_relaxed), 2);
+    const int grid = sms * std::min(occ_cache[dev].load(std::memory_order_relaxed), kCtas);
     if (cudaMemsetAsync(sync, 0, sizeof(unsigned) * plan.nstages, s) != cudaSuccess) return qg::cuda_fail(cudaGetLastError());
     void* args[] = {const_cast<pass::Plan*>(&plan), &M, &sync, &stages, &status};
     if (cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(kern), dim3(grid), dim3(kCols * 32 + 32), args,

@@ -28,7 +28,7 @@ inline int sm_count(int dev) {
     return n;
 }
 
-// Launch gemv_kernel<F, MT, RG, MINB, FUSE> over `count` matrices that
+// Launch qg_gemv_kernel<F, MT, RG, MINB, FUSE> over `count` matrices that
 // share X (token offset m0 already applied to X; Y[i] + m0*N[i] here): MINB
 // CTAs per SM, as many pipeline stages as fit in the per-CTA share of shared
 // memory.
@@ -41,7 +41,7 @@ int launch_gemv(const uint8_t* const* W, float* const* Y, const int64_t* N, int 
     const Layout L1 = make_layout(F::kIQ3, MT, F::kXH, RG, 1, F::kRowStride, F::kCols, FUSE);
     const int stages_fit = std::min(kMaxStages, (budget - L1.stage0) / L1.stage_bytes);
     if (stages_fit < 2) return QG_EINVAL;
-    auto kern = gemv_kernel<F, MT, RG, MINB, FUSE>;
+    auto kern = qg_gemv_kernel<F, MT, RG, MINB, FUSE>;
     if (!attr_done[dev].load(std::memory_order_acquire)) {
         const Layout Lmax = make_layout(F::kIQ3, MT, F::kXH, RG, stages_fit, F::kRowStride, F::kCols, FUSE);
         if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Lmax.total) != cudaSuccess)

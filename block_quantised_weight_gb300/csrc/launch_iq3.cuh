@@ -15,7 +15,7 @@ namespace qg {
 // staged in smem.  Correct for every K % 256 == 0; not tuned.
 template <class F>
 __global__ void __launch_bounds__(256)
-    gemv_iq3_bytes_kernel(const uint8_t* __restrict__ W, const uint8_t* __restrict__ grid, const float* __restrict__ X,
+    qg_gemv_iq3_bytes_kernel(const uint8_t* __restrict__ W, const uint8_t* __restrict__ grid, const float* __restrict__ X,
                           float* __restrict__ Y, int M, int64_t N, int64_t K) {
     __shared__ uint32_t g[256];
     for (int i = threadIdx.x; i < 256; i += blockDim.x) g[i] = *reinterpret_cast<const uint32_t*>(grid + 4 * i);
@@ -76,7 +76,7 @@ int launch_group_iq3_t(const uint8_t* const* W, float* const* Y, const int64_t* 
             const int mg = std::min(8, M - m0);
             for (int i = 0; i < count; ++i) {
                 const int64_t blocks = std::min<int64_t>((N[i] + 7) / 8, static_cast<int64_t>(sms) * 8);
-                gemv_iq3_bytes_kernel<F><<<static_cast<int>(blocks), 256, 0, s>>>(
+                qg_gemv_iq3_bytes_kernel<F><<<static_cast<int>(blocks), 256, 0, s>>>(
                     W[i], grid, X + static_cast<int64_t>(m0) * K, Y[i] + m0 * N[i], mg, N[i], K);
                 if (const cudaError_t e = cudaGetLastError(); e != cudaSuccess) return qg::cuda_fail(e);
             }

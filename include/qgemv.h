@@ -83,11 +83,16 @@ extern "C" {
  * Page 1 "Rewriting picoLM in Python", dequantize_q4_K (format) and
  * model_forward's matmul (operation).
  * W: N*K/256*144 bytes.  X: M*K floats.  Y: M*N floats (output).
- * Numerics: |Y - exact| <= 1e-5 * sum_k |w*x| per element (fp32 FMA,
- * sub-block-factored sums).  M > 4 is processed in groups of 4 tokens, each
- * group streaming W once.  Range: the kernel scales x by powers of two up to
- * 2^88 in shared memory, so every |x| must be below 2^40 (larger values give
- * inf/NaN in Y); the same holds for qgemv_q4k_group, qgemv_q4k_fused and
+ * Numerics: |Y - exact| <= 1e-5 * sum_k |w*x| per element (fp32 FMA).
+ * Each 32-weight sub-block is summed as a*sum((q - c)*x) - (b - a*c)*sum(x),
+ * a = d*sc, b = dmin*mn, c the integer in [0, 15] nearest b/a, so sub-blocks
+ * whose d*sc*q and dmin*mn cancel keep that accuracy (a row of zero weights
+ * gives exactly 0).  Range: every finite x; slices of 256 x values whose
+ * largest |x| lies outside [2^-24, 2^39) take a slower rescaled decode (a
+ * power of two in, its inverse out), so the outputs are only limited by
+ * fp32 itself.  M > 4 is processed in groups of 4 tokens, each group
+ * streaming W once.  The same holds for qgemv_q4k_group, qgemv_q4k_fused
+ * (its RMSNorm prologue sums x^2 in fp32: |x| below 2^63) and
  * qgemv_q4k_pass. */
 QG_API int qgemv_q4k(const uint8_t* W, const float* X, float* Y, int M, int64_t N, int64_t K, cudaStream_t stream);
 
@@ -103,7 +108,11 @@ QG_API int qgemv_q4k_ex(const uint8_t* W, const float* X, float* Y, int M, int64
  * applies the 0.5 of page 4's grid()).  Other arguments as qgemv_q4k.
  * K/256 a multiple of 8 takes the tensor-map path, M > 4 in groups of 4
  * tokens, each group streaming W once; other K take a slower byte-addressed
- * path (groups of 8 tokens) with the same numerics. */
+ * path (groups of 8 tokens) with the same numerics.  Range: the tensor-map
+ * path takes every finite x (columns whose largest |x| lies outside
+ * [2^-60, 2^60) are rescaled by a power of two); the byte-addressed path
+ * multiplies x as given, so there |x| must stay within [2^-100, 2^100]
+ * for the tolerance to hold. */
 QG_API int qgemv_iq3(const uint8_t* W, const uint8_t* grid, const float* X, float* Y, int M, int64_t N, int64_t K,
               cudaStream_t stream);
 
@@ -152,8 +161,9 @@ QG_API int qgemv_iq3xxs_ex(const uint8_t* W, const uint8_t* grid, const float* X
  *                  28-31; eff = d*(0.5+s)*0.25; codebook: 256 x 8 bytes
  * W [N][K/256 units], X [M][K], Y [M][N] as qgemv_q4k; 1 <= M <= 32;
  * codebook device memory, 16-byte aligned.  fp32 FMA path, tolerance
- * 1e-5 * sum|w*x|.  Errors as qgemv_q4k, plus QG_EINVAL for an unknown
- * format. */
+ * 1e-5 * sum|w*x| for |x| within [2^-100, 2^100] (x is multiplied as given,
+ * so products must stay normal fp32 numbers).  Errors as qgemv_q4k, plus
+ * QG_EINVAL for an unknown format. */
 #define QG_CB_IQ4_NL 1
 #define QG_CB_IQ4_XS 2
 #define QG_CB_IQ3_S 3
@@ -260,8 +270,15 @@ QG_API int qgemv_q4k_pass(const qg_stage* stages, int nstages, int M, unsigned* 
  * allocating library routine.  Each call zeroes the counts it uses on the
  * stream before its launch (the array keeps the previous call's contents).
  * All calls on a device share the one array, so calls that overlap on the
- * GPU (other streams, other host threads) race and give wrong results:
- * order them on one stream or synchronise between them.
+ * GPU (other streams, other host threads) race: one call can zero the
+ * counts another is still using, so they give wrong results and may also
+ * end in QG_ETIMEOUT (reported by qg_device_status) after a count wait gives
+ * up; once one has, the call's remaining count waits return at once, so the
+ * call still ends within about one wait limit (2 s).  Order such calls on
+ * one stream or synchronise between them.
+ * The scratch address is cached per device for the life of the process: do
+ * not call the library again on a device after cudaDeviceReset (the same
+ * holds for every entry point, which caches the status word's address).
  * The pages have no counterpart: this entry point exists only for callers
  * that cannot allocate. */
 #define QG_NOALLOC_SCRATCH_WORDS 96
@@ -272,7 +289,8 @@ QG_API int qgemv_q4k_pass_noalloc(const qg_stage* stages, int nstages, int M, cu
  * (tolerance 1e-5 * sum|w*x|); M >= 16 dequantises W tiles to bf16 (round to
  * nearest even) in shared memory and multiplies on the tcgen05 tensor cores
  * with fp32 accumulation in tensor memory, X also rounded to bf16
- * (tolerance 4e-3 * sum|w*x|).  On this path Y is zeroed on `stream` and the
+ * (tolerance 4e-3 * sum|w*x|, for |x| within [2^-100, 2^100]: bf16 keeps
+ * fp32's exponent range but not its subnormals).  On this path Y is zeroed on `stream` and the
  * row sums of K ranges that different CTAs share are added into it with fp32
  * atomics, so repeated calls may differ in the last bits (the FMA paths are
  * deterministic). */

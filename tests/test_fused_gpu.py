@@ -126,46 +126,74 @@ def test_group_residual_per_matrix(q):
 
 def test_decode_step_chain(q):
     """Two layers of a small decode step, every GEMV fused and reading the
-    previous GEMV's output on the device (programmatic dependent launches,
-    no host synchronisation in between): q/k/v (attention RMSNorm) -> o
+    previous GEMV's output on the device: q/k/v (attention RMSNorm) -> o
     (x = q, standing in for attention; residual in place) -> gate/up (FFN
     RMSNorm) -> down (SwiGLU, residual in place) -> output (final RMSNorm).
-    Device-side snapshots record what each stage read and wrote; every stage
-    is then checked against the oracle on the inputs the GPU gave it."""
+    The chain of programmatic dependent launches (no host synchronisation in
+    between) equals, bit for bit, the same chain with the host waiting after
+    every launch; and every stage, given the oracle's own chain of inputs
+    (the fp32 of the oracle's previous outputs), matches the oracle."""
     D, F, KV, V = 512, 1024, 128, 600
     rng = np.random.default_rng(77)
-    x = dev(synth.gen_x(1, D, 30))
-    fl = q.QG_PREFETCH_WEIGHTS
-    stages = []  # (name, [W], oracle kwargs with device snapshots, [output snapshots], residual?)
+    x0 = synth.gen_x(1, D, 30)
+    layers = []
     for layer in range(2):
         Wq, Wk, Wv, Wo = (synth.gen_q4k(n, D, 7000 + 10 * layer + i) for i, n in enumerate((D, KV, KV, D)))
         Wg, Wu = (synth.gen_q4k(F, D, 7100 + 10 * layer + i) for i in range(2))
         Wd = synth.gen_q4k(D, F, 7200 + layer)
         ga, gf = (rng.standard_normal(D).astype(np.float32) for _ in range(2))
-        x_in = x.clone()
-        qv, kv, vv = q.qgemv_q4k_fused_group([dev(Wq), dev(Wk), dev(Wv)], x, norm_weight=dev(ga), eps=1e-5,
-                                             flags=fl)
-        stages.append((f"{layer} qkv", [Wq, Wk, Wv], dict(X=x_in, norm_weight=ga, eps=1e-5),
-                       [qv.clone(), kv.clone(), vv.clone()], False))
-        x_before = x.clone()
-        q.qgemv_q4k_fused(dev(Wo), qv, out=x, residual=x, flags=fl)
-        stages.append((f"{layer} o", [Wo], dict(X=qv.clone(), residual=x_before), [x.clone()], True))
-        x_mid = x.clone()
-        gt, upv = q.qgemv_q4k_fused_group([dev(Wg), dev(Wu)], x, norm_weight=dev(gf), eps=1e-5, flags=fl)
-        stages.append((f"{layer} gate/up", [Wg, Wu], dict(X=x_mid, norm_weight=gf, eps=1e-5),
-                       [gt.clone(), upv.clone()], False))
-        q.qgemv_q4k_fused(dev(Wd), gt, out=x, up=upv, residual=x, flags=fl)
-        stages.append((f"{layer} down", [Wd], dict(X=gt.clone(), up=upv.clone(), residual=x_mid.clone()),
-                       [x.clone()], True))
+        layers.append((Wq, Wk, Wv, Wo, Wg, Wu, Wd, ga, gf))
     Wout = synth.gen_q4k(V, D, 7300)
     gn = rng.standard_normal(D).astype(np.float32)
-    x_fin = x.clone()
-    logits = q.qgemv_q4k_fused(dev(Wout), x, norm_weight=dev(gn), eps=1e-5, flags=fl)
-    stages.append(("output", [Wout], dict(X=x_fin, norm_weight=gn, eps=1e-5), [logits], False))
+
+    def gpu_chain(fl, wait):
+        x = dev(x0)
+        outs = []
+        for Wq, Wk, Wv, Wo, Wg, Wu, Wd, ga, gf in layers:
+            qv, kv, vv = q.qgemv_q4k_fused_group([dev(Wq), dev(Wk), dev(Wv)], x, norm_weight=dev(ga), eps=1e-5,
+                                                 flags=fl)
+            wait()
+            q.qgemv_q4k_fused(dev(Wo), qv, out=x, residual=x, flags=fl)
+            wait()
+            x_mid = x.clone()
+            gt, upv = q.qgemv_q4k_fused_group([dev(Wg), dev(Wu)], x, norm_weight=dev(gf), eps=1e-5, flags=fl)
+            wait()
+            q.qgemv_q4k_fused(dev(Wd), gt, out=x, up=upv, residual=x, flags=fl)
+            wait()
+            outs += [qv, kv, vv, x_mid, gt, upv, x.clone()]
+        outs.append(q.qgemv_q4k_fused(dev(Wout), x, norm_weight=dev(gn), eps=1e-5, flags=fl))
+        torch.cuda.synchronize()
+        return outs
+
+    chained = gpu_chain(q.QG_PREFETCH_WEIGHTS, lambda: None)
+    stepped = gpu_chain(0, torch.cuda.synchronize)
+    for a, b in zip(chained, stepped):
+        assert torch.equal(a, b)
     assert q.qg_device_status() == 0
-    for name, Ws, kw, outs, res in stages:
-        kw = {k: (v.cpu().numpy() if isinstance(v, torch.Tensor) else v) for k, v in kw.items()}
-        X = kw.pop("X")
-        for W, o in zip(Ws, outs):
-            Y, A = oracle.fused_gemv_q4k(W, X, **kw)
-            check(o.cpu().numpy(), Y, A, res=res, what=name)
+
+    # every stage on the oracle's chain of inputs
+    def f32(Y):
+        return np.asarray(Y, dtype=np.float32)
+
+    x = x0
+    for layer, (Wq, Wk, Wv, Wo, Wg, Wu, Wd, ga, gf) in enumerate(layers):
+        outs = q.qgemv_q4k_fused_group([dev(Wq), dev(Wk), dev(Wv)], dev(x), norm_weight=dev(ga), eps=1e-5)
+        refs = [oracle.fused_gemv_q4k(W, x, norm_weight=ga, eps=1e-5) for W in (Wq, Wk, Wv)]
+        for o, (Y, A) in zip(outs, refs):
+            check(o.cpu().numpy(), Y, A, what=f"{layer} qkv")
+        qv = f32(refs[0][0])
+        Y, A = oracle.fused_gemv_q4k(Wo, qv, residual=x)
+        check(q.qgemv_q4k_fused(dev(Wo), dev(qv), residual=dev(x)).cpu().numpy(), Y, A, res=True, what=f"{layer} o")
+        x = f32(Y)
+        outs = q.qgemv_q4k_fused_group([dev(Wg), dev(Wu)], dev(x), norm_weight=dev(gf), eps=1e-5)
+        refs = [oracle.fused_gemv_q4k(W, x, norm_weight=gf, eps=1e-5) for W in (Wg, Wu)]
+        for o, (Y, A) in zip(outs, refs):
+            check(o.cpu().numpy(), Y, A, what=f"{layer} gate/up")
+        gt, upv = f32(refs[0][0]), f32(refs[1][0])
+        Y, A = oracle.fused_gemv_q4k(Wd, gt, up=upv, residual=x)
+        check(q.qgemv_q4k_fused(dev(Wd), dev(gt), up=dev(upv), residual=dev(x)).cpu().numpy(), Y, A, res=True,
+              what=f"{layer} down")
+        x = f32(Y)
+    Y, A = oracle.fused_gemv_q4k(Wout, x, norm_weight=gn, eps=1e-5)
+    check(q.qgemv_q4k_fused(dev(Wout), dev(x), norm_weight=dev(gn), eps=1e-5).cpu().numpy(), Y, A, what="output")
+    assert q.qg_device_status() == 0
