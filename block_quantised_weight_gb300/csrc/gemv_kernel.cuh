@@ -392,23 +392,35 @@ __device__ __forceinline__ void q4k_half2(const uint8_t* blk, int rstride, int h
         // sub-blocks 4h+2g (low nibbles) and 4h+2g+1 (high nibbles) of each row
         float al61[2], ah61[2];  // a * 2^61 (the pre-scaling of x is 2^-61 in the products)
         f2 ol[2], oh[2];         // -c at the subnormal scales of the nibbles' bit offsets
+        // the two rows' scale arithmetic as packed pairs (row 0, row 1)
+        const f2 dd2{dd[0], dd[1]}, dm2{dm[0], dm[1]};
+        const f2 a0 = fmul2(dd2, f2{byte_f(scw[0], 2 * g), byte_f(scw[1], 2 * g)});
+        const f2 a1 = fmul2(dd2, f2{byte_f(scw[0], 2 * g + 1), byte_f(scw[1], 2 * g + 1)});
+        const f2 b0 = fmul2(dm2, f2{byte_f(mnw[0], 2 * g), byte_f(mnw[1], 2 * g)});
+        const f2 b1 = fmul2(dm2, f2{byte_f(mnw[0], 2 * g + 1), byte_f(mnw[1], 2 * g + 1)});
+        const f2 c0{q4k_offset(a0.x, b0.x), q4k_offset(a0.y, b0.y)};
+        const f2 c1{q4k_offset(a1.x, b1.x), q4k_offset(a1.y, b1.y)};
+        f2 r0 = b0, r1 = b1;  // b - a*c, exact where it matters
+        ffma2(r0, f2{-a0.x, -a0.y}, c0);
+        ffma2(r1, f2{-a1.x, -a1.y}, c1);
+        const f2 al2 = fmul2(a0, f2{0x1p61f, 0x1p61f}), ah2 = fmul2(a1, f2{0x1p61f, 0x1p61f});
+        al61[0] = al2.x;
+        al61[1] = al2.y;
+        ah61[0] = ah2.x;
+        ah61[1] = ah2.y;
+        ol[0] = fmul2(f2{c0.x, c0.x}, f2{-0x1p-149f, -0x1p-141f});
+        ol[1] = fmul2(f2{c0.y, c0.y}, f2{-0x1p-149f, -0x1p-141f});
+        oh[0] = fmul2(f2{c1.x, c1.x}, f2{-0x1p-145f, -0x1p-137f});
+        oh[1] = fmul2(f2{c1.y, c1.y}, f2{-0x1p-145f, -0x1p-137f});
 #pragma unroll
-        for (int j = 0; j < 2; ++j) {
-            const float a0 = dd[j] * byte_f(scw[j], 2 * g), a1 = dd[j] * byte_f(scw[j], 2 * g + 1);
-            const float b0 = dm[j] * byte_f(mnw[j], 2 * g), b1 = dm[j] * byte_f(mnw[j], 2 * g + 1);
-            const float c0 = q4k_offset(a0, b0), c1 = q4k_offset(a1, b1);
-            const float r0 = fmaf(-a0, c0, b0), r1 = fmaf(-a1, c1, b1);
-#pragma unroll
-            for (int m = 0; m < MT; ++m) {
-                if (MT == 1 || m < M) {
-                    tgt[j][m] = fmaf(-r0, sx[m * 8 + 4 * h + 2 * g], tgt[j][m]);
-                    tgt[j][m] = fmaf(-r1, sx[m * 8 + 4 * h + 2 * g + 1], tgt[j][m]);
-                }
+        for (int m = 0; m < MT; ++m) {
+            if (MT == 1 || m < M) {
+                const float s0 = sx[m * 8 + 4 * h + 2 * g], s1 = sx[m * 8 + 4 * h + 2 * g + 1];
+                tgt[0][m] = fmaf(-r0.x, s0, tgt[0][m]);
+                tgt[0][m] = fmaf(-r1.x, s1, tgt[0][m]);
+                tgt[1][m] = fmaf(-r0.y, s0, tgt[1][m]);
+                tgt[1][m] = fmaf(-r1.y, s1, tgt[1][m]);
             }
-            al61[j] = a0 * 0x1p61f;
-            ah61[j] = a1 * 0x1p61f;
-            ol[j] = fmul2(f2{c0, c0}, f2{-0x1p-149f, -0x1p-141f});
-            oh[j] = fmul2(f2{c1, c1}, f2{-0x1p-145f, -0x1p-137f});
         }
         f2 al[2][MT], ah[2][MT];
 #pragma unroll
@@ -988,12 +1000,12 @@ __global__ void __launch_bounds__(RG * F::kCols * 32 + 32, MINB)
                         }
                     }
                 }
+                const uint8_t* sg = tb + kIQ3GridBytes;
+                const float* xq = xb + XH * hl;
                 if (rescaled)  // rare; the same in every lane
-                    iq3_half2<MT, F, true>(vi, vs, dbits, tb, tb + kIQ3GridBytes, lane8, lane_s, xb + XH * hl, xstride,
-                                           M, e2, acc2);
+                    iq3_half2<MT, F, true>(vi, vs, dbits, tb, sg, lane8, lane_s, xq, xstride, M, e2, acc2);
                 else
-                    iq3_half2<MT, F, false>(vi, vs, dbits, tb, tb + kIQ3GridBytes, lane8, lane_s, xb + XH * hl,
-                                            xstride, M, e2, acc2);
+                    iq3_half2<MT, F, false>(vi, vs, dbits, tb, sg, lane8, lane_s, xq, xstride, M, e2, acc2);
                 fence_proxy_async_smem();  // x was written: order it before the slot's next copy
             }
         }

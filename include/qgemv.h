@@ -110,7 +110,7 @@ QG_API int qgemv_q4k_ex(const uint8_t* W, const float* X, float* Y, int M, int64
  * tokens, each group streaming W once; other K take a slower byte-addressed
  * path (groups of 8 tokens) with the same numerics.  Range: the tensor-map
  * path takes every finite x (columns whose largest |x| lies outside
- * [2^-60, 2^60) are rescaled by a power of two); the byte-addressed path
+ * [2^-24, 2^39) are rescaled by a power of two); the byte-addressed path
  * multiplies x as given, so there |x| must stay within [2^-100, 2^100]
  * for the tolerance to hold. */
 QG_API int qgemv_iq3(const uint8_t* W, const uint8_t* grid, const float* X, float* Y, int M, int64_t N, int64_t K,

@@ -113,6 +113,18 @@ def test_gemv_iq3_small(q, N, K, M):
     check_tol(y, Y, A, TAU_FMA, f"iq3 N={N} K={K} M={M}")
 
 
+@pytest.mark.parametrize("M", [1, 2, 4, 8])
+def test_gemv_iq3_grid_bytes_above_127(q, M):
+    """Grid bytes anywhere in 0..255 against the oracle."""
+    N, K = 300, 4096
+    W, _ = synth.gen_iq3(N, K, 21)
+    grid = np.random.default_rng(22).integers(0, 256, (256, 4), dtype=np.uint8)
+    x = synth.gen_x(M, K, 23)
+    Y, A = oracle.gemv_iq3(W, grid, x)
+    y = q.qgemv_iq3(dev(W), dev(grid), dev(x)).cpu().numpy()
+    check_tol(y, Y, A, TAU_FMA, f"iq3 grid bytes >= 128 M={M}")
+
+
 @pytest.mark.parametrize("M", [13, 32])
 def test_gemv_iq3_many_tokens(q, M):
     N, K = 45, 2048
@@ -482,8 +494,9 @@ def test_gemv_q4k_x_mixed_ranges(q):
 @pytest.mark.parametrize("scale", X_SCALES)
 @pytest.mark.parametrize("M", [1, 2, 4])
 def test_gemv_iq3_x_range(q, scale, M):
-    """The IQ3 decode takes columns whose largest |x| is in [2^-60, 2^60) as
-    they are and rescales the others by a power of two."""
+    """The IQ3 decode takes columns whose largest |x| is in [2^-24, 2^39) as
+    they are (x pre-scaled by 2^88 against grid bytes held as fp32
+    subnormals) and rescales the others by a power of two."""
     N, K = 96, 2048
     W, grid = synth.gen_iq3(N, K, 35)
     x = (synth.gen_x(M, K, 36) * np.float32(scale)).astype(np.float32)

@@ -158,9 +158,30 @@ def test_onehot_iq3(q, order, N, K, group):
     sweep(lambda x: fn(Wg, gg, x), Wd, K, group, what=f"iq3 {order} N={N} K={K} group={group}")
 
 
+@pytest.mark.parametrize("order", ["page4", "iq3xxs"])
+@pytest.mark.parametrize("group", [1, 2, 32])
+def test_onehot_iq3_grid_bytes_above_127(q, order, group):
+    """A grid with bytes of 128 and more (the format allows any byte; the
+    published grids stay below 64): each byte lands whole in the low byte
+    of its fp32 subnormal."""
+    N, K = 70, 2048
+    W, _ = synth.gen_iq3(N, K, 11)
+    grid = np.random.default_rng(12).integers(0, 256, (256, 4), dtype=np.uint8)
+    grid[0, 0] = 255
+    if order == "page4":
+        Wd = oracle.dequant_iq3(W, grid, K)
+        fn = q.qgemv_iq3
+    else:
+        W = oracle.iq3_to_iq3xxs(W, K)
+        Wd = oracle.dequant_iq3xxs(W, grid, K)
+        fn = q.qgemv_iq3xxs
+    Wg, gg = dev(W), dev(grid)
+    sweep(lambda x: fn(Wg, gg, x), Wd, K, group, what=f"iq3 {order} grid bytes >= 128, group={group}")
+
+
 @pytest.mark.parametrize("value", [2.0 ** 70, 2.0 ** -90])
 def test_onehot_iq3_rescaled_x(q, value):
-    """x outside [2^-60, 2^60): the IQ3 decode rescales the column."""
+    """x outside [2^-24, 2^39): the IQ3 decode rescales the column."""
     N, K = 70, 2048
     W, grid = synth.gen_iq3(N, K, 5)
     Wd = oracle.dequant_iq3(W, grid, K)
