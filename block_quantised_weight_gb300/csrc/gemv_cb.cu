@@ -301,12 +301,12 @@ __device__ __forceinline__ void raw_from_words(const uint32_t* v, Raw& R) {
     }
 }
 
-// One lane's row of one column (unit bytes OFF bytes into the box row)
-// against MT tokens of x (xs: the column's 256 x values of token 0; tokens
-// 2048 floats apart).
-template <int F, int MT, int OFF>
-__device__ __forceinline__ void cb_column(const uint8_t* boxrow, const float* xs, const Table& T, int M,
-                                          float (&acc)[MT]) {
+// One lane's row of one column, unit bytes OFF bytes into the box row, as
+// NV aligned words (v[k] = unit bytes 4k..4k+3).
+template <int F>
+constexpr int row_words() { return (Box<F>::kUB + 3) / 4 + 1; }
+template <int F, int OFF>
+__device__ __forceinline__ void load_row_words(const uint8_t* boxrow, uint32_t (&v)[row_words<F>()]) {
     constexpr int NW = Box<F>::kWords, W0 = OFF >> 2, SH = 8 * (OFF & 3);
     uint32_t a[NW + 1];
 #pragma unroll
@@ -315,23 +315,25 @@ __device__ __forceinline__ void cb_column(const uint8_t* boxrow, const float* xs
         a[4 * i] = t.x; a[4 * i + 1] = t.y; a[4 * i + 2] = t.z; a[4 * i + 3] = t.w;
     }
     a[NW] = 0u;  // past the box: only ever the unused top bytes of the last word
-    constexpr int NV = (Box<F>::kUB + 3) / 4 + 1;
-    uint32_t v[NV];
 #pragma unroll
-    for (int k = 0; k < NV; ++k) {
+    for (int k = 0; k < row_words<F>(); ++k) {
         const int i0 = W0 + k < NW ? W0 + k : NW, i1 = W0 + k + 1 < NW ? W0 + k + 1 : NW;
         v[k] = SH ? __funnelshift_r(a[i0], a[i1], SH) : a[i0];
     }
+}
+
+// IQ4_NL / IQ4_XS: one lane's row of one column against MT tokens of x (xs:
+// the column's 256 x values of token 0; tokens 2048 floats apart).
+template <int F, int MT>
+__device__ __forceinline__ void cb_iq4_column(const uint32_t (&v)[row_words<F>()], const float* xs, const Table& T,
+                                              int M, float (&acc)[MT]) {
     auto sub = [&](auto jc) {
         constexpr int J = decltype(jc)::value;
         Raw R;
         raw_from_words<F, J>(v, R);
         float w[32];
         float eff = 1.f;
-        if constexpr (F == kIQ4NL || F == kIQ4XS)
-            decode_sub_iq4_factored<F>(R, J, T, w, eff);  // eff applied to the sub-block's sum
-        else
-            decode_sub<F>(R, J, T, w);
+        decode_sub_iq4_factored<F>(R, J, T, w, eff);  // eff applied to the sub-block's sum
 #pragma unroll
         for (int m = 0; m < MT; ++m) {
             if (MT == 1 || m < M) {
@@ -359,12 +361,234 @@ __device__ __forceinline__ void cb_column(const uint8_t* boxrow, const float* xs
     sub(std::integral_constant<int, 7>{});
 }
 
+// ------------------------------------------------ grid formats on the ring
+// IQ3_S and IQ2_XXS decode as the IQ3 GEMV does: the codebook's rows are
+// expanded with zero bytes, so that one byte permute per weight puts the
+// grid byte at bits 0-7 and its sign byte (0x80 when negative) at bits
+// 24-31 of an fp32: the exact subnormal +-g * 2^-149, against x pre-scaled
+// by 2^88 (cb_stage_x); the sub-block's eff * 2^61 undoes the scaling.
+//   IQ3_S    entry i (4 weights) -> [g0,0,g1,0][g2,0,g3,0]          512 x 8 bytes
+//   IQ2_XXS  entry i (8 weights) -> [g0,0,g1,0] ... [g6,0,g7,0]     256 x 16 bytes,
+//            then the sign bytes of each 7-bit field (the eighth sign
+//            its parity: an even count of negatives)                128 x 8 bytes
+constexpr int kGridTabBytes = 5120;
+
+// Sign bytes of four sign bits: bit k of nib -> bit 8k+7 (one multiply
+// places bit k at k, k+7, k+14, k+21 and k+28, which never collide).
+__device__ __forceinline__ uint32_t sign_bytes(uint32_t nib) { return (nib * 0x10204081u) & 0x80808080u; }
+
+// [b0, 0, b1, 0] of the low two bytes of w
+__device__ __forceinline__ uint32_t spread2(uint32_t w) { return (w & 0xFFu) | ((w & 0xFF00u) << 8); }
+
+// Loads the codebook; returns true (the same in every thread of the CTA)
+// when every codebook byte is below 128.  Then the table keeps the
+// codebook's own rows (IQ3_S 512 x 4 bytes, IQ2_XXS 256 x 8 bytes, half
+// the bytes per gather) and the permute takes the zero bytes from the
+// sign-replicate of the grid byte itself (its top bit is 0); otherwise the
+// rows are expanded as above.
+template <int F>
+__device__ bool load_grid_table(const void* book, uint8_t* gt) {
+    const uint32_t* w = static_cast<const uint32_t*>(book);
+    uint32_t high = 0;
+    for (int i = threadIdx.x; i < 512; i += blockDim.x) high |= w[i];  // both formats: 2 KB
+    const bool compact = __syncthreads_or((high & 0x80808080u) != 0u) == 0;
+    if (compact) {
+        uint32_t* t = reinterpret_cast<uint32_t*>(gt);
+        for (int i = threadIdx.x; i < 512; i += blockDim.x) t[i] = w[i];
+        if constexpr (F == kIQ2XXS) {
+            uint2* sg = reinterpret_cast<uint2*>(gt + 4096);
+            for (int i = threadIdx.x; i < 128; i += blockDim.x) {
+                const uint32_t s8 = static_cast<uint32_t>(i) | ((__popc(i) & 1u) << 7);
+                sg[i] = make_uint2(sign_bytes(s8 & 15u), sign_bytes(s8 >> 4));
+            }
+        }
+        return true;
+    }
+    if constexpr (F == kIQ3S) {
+        const uint32_t* t = static_cast<const uint32_t*>(book);
+        uint2* e = reinterpret_cast<uint2*>(gt);
+        for (int i = threadIdx.x; i < 512; i += blockDim.x) e[i] = make_uint2(spread2(t[i]), spread2(t[i] >> 16));
+    } else {
+        const uint2* t = static_cast<const uint2*>(book);
+        uint4* e = reinterpret_cast<uint4*>(gt);
+        for (int i = threadIdx.x; i < 256; i += blockDim.x) {
+            const uint2 g = t[i];
+            e[i] = make_uint4(spread2(g.x), spread2(g.x >> 16), spread2(g.y), spread2(g.y >> 16));
+        }
+        uint2* sg = reinterpret_cast<uint2*>(gt + 4096);
+        for (int i = threadIdx.x; i < 128; i += blockDim.x) {
+            const uint32_t s8 = static_cast<uint32_t>(i) | ((__popc(i) & 1u) << 7);
+            sg[i] = make_uint2(sign_bytes(s8 & 15u), sign_bytes(s8 >> 4));
+        }
+    }
+    return false;
+}
+
+// Signed grid value: byte P (0 or 2) of the expanded word g, sign byte K of s.
+template <int P, int K>
+__device__ __forceinline__ float grid_val(uint32_t g, uint32_t s) {
+    return __uint_as_float(prmt(g, s, static_cast<uint32_t>(P) | (1u << 4) | (1u << 8) | ((4u + K) << 12)));
+}
+// The same from a compact row word (bytes below 128): byte P at bits 0-7,
+// bits 8-23 the replicated top bit of byte P (0), sign byte K at 24-31.
+template <int P, int K>
+__device__ __forceinline__ float grid_val_c(uint32_t g, uint32_t s) {
+    constexpr uint32_t rep = 8u | P;
+    return __uint_as_float(prmt(g, s, static_cast<uint32_t>(P) | (rep << 4) | (rep << 8) | ((4u + K) << 12)));
+}
+
+// IQ3_S / IQ2_XXS: one lane's row of one column against MT tokens of x
+// (pre-scaled by 2^88; tokens 2048 floats apart).  With RESCALE the
+// column's sums are formed apart and multiplied by e2[m] before they join
+// acc (a token whose column cb_stage_x rescaled).
+template <int F, int MT, bool RESCALE, bool COMPACT>
+__device__ __forceinline__ void cb_grid_column(const uint32_t (&v)[row_words<F>()], const float* xs,
+                                               const uint8_t* gt, int M, const float (&e2)[MT], float (&acc)[MT]) {
+    if constexpr (RESCALE && MT > 1) {
+#pragma unroll
+        for (int m = 0; m < MT; ++m) {
+            if (m < M) {
+                float a1[1] = {acc[m]};
+                const float e1[1] = {e2[m]};
+                cb_grid_column<F, 1, true, COMPACT>(v, xs + m * 2048, gt, 1, e1, a1);
+                acc[m] = a1[0];
+            }
+        }
+        return;
+    }
+    float part[MT];
+    float (&tgt)[MT] = RESCALE ? part : acc;
+    if constexpr (RESCALE) {
+#pragma unroll
+        for (int m = 0; m < MT; ++m) part[m] = 0.f;
+    }
+    // four weights: expanded words ga = [g0,0,g1,0], gb = [g2,0,g3,0], or
+    // (COMPACT) one word ga = [g0 g1 g2 g3]
+    auto four = [&](uint32_t ga, uint32_t gb, uint32_t sgn, const float* xq, f2 (&dot)[MT]) {
+        f2 w01, w23;
+        if constexpr (COMPACT) {
+            w01 = f2{grid_val_c<0, 0>(ga, sgn), grid_val_c<1, 1>(ga, sgn)};
+            w23 = f2{grid_val_c<2, 2>(ga, sgn), grid_val_c<3, 3>(ga, sgn)};
+        } else {
+            w01 = f2{grid_val<0, 0>(ga, sgn), grid_val<2, 1>(ga, sgn)};
+            w23 = f2{grid_val<0, 2>(gb, sgn), grid_val<2, 3>(gb, sgn)};
+        }
+#pragma unroll
+        for (int m = 0; m < MT; ++m) {
+            if (MT == 1 || m < M) {
+                const float4 x = *reinterpret_cast<const float4*>(xq + m * 2048);
+                ffma2(dot[m], w01, f2{x.x, x.y});
+                ffma2(dot[m], w23, f2{x.z, x.w});
+            }
+        }
+    };
+    auto sub = [&](auto jc) {
+        constexpr int J = decltype(jc)::value;
+        Raw R;
+        raw_from_words<F, J>(v, R);
+        f2 dot[MT];
+#pragma unroll
+        for (int m = 0; m < MT; ++m) dot[m] = f2{0.f, 0.f};
+        float eff61;
+        if constexpr (F == kIQ3S) {
+            // eff = d*(1+2s); 9-bit indices (low byte + one high bit); one sign bit per weight
+            const uint32_t sc = (R.r[0] >> (16 + 4 * (J & 3))) & 15u;
+            eff61 = h2f(R.r[0]) * static_cast<float>(1u + 2u * sc) * 0x1p61f;
+            const uint32_t qh = (R.r[3] >> (8 * (J & 1))) & 0xFFu, sg = R.r[4];
+#pragma unroll
+            for (int g = 0; g < 8; ++g) {
+                const uint32_t idx = (((g < 4 ? R.r[1] : R.r[2]) >> (8 * (g & 3))) & 0xFFu) | (((qh >> g) & 1u) << 8);
+                const uint32_t sgn = sign_bytes((sg >> (4 * g)) & 15u);
+                if constexpr (COMPACT) {
+                    four(reinterpret_cast<const uint32_t*>(gt)[idx], 0u, sgn, xs + 32 * J + 4 * g, dot);
+                } else {
+                    const uint2 ge = reinterpret_cast<const uint2*>(gt)[idx];
+                    four(ge.x, ge.y, sgn, xs + 32 * J + 4 * g, dot);
+                }
+            }
+        } else {
+            // eff = d*(0.5+s)*0.25; four 8-weight groups, each a grid index byte and a 7-bit sign field
+            const uint32_t aux0 = R.r[1], aux1 = R.r[2];
+            eff61 = h2f(R.r[0]) * (0.5f + static_cast<float>(aux1 >> 28)) * (0.25f * 0x1p61f);
+            const uint2* sgt = reinterpret_cast<const uint2*>(gt + 4096);
+#pragma unroll
+            for (int g = 0; g < 4; ++g) {
+                const uint32_t idx = (aux0 >> (8 * g)) & 0xFFu;
+                const uint2 sgn = sgt[(aux1 >> (7 * g)) & 0x7Fu];
+                if constexpr (COMPACT) {
+                    const uint2 ge = reinterpret_cast<const uint2*>(gt)[idx];
+                    four(ge.x, 0u, sgn.x, xs + 32 * J + 8 * g, dot);
+                    four(ge.y, 0u, sgn.y, xs + 32 * J + 8 * g + 4, dot);
+                } else {
+                    const uint4 ge = reinterpret_cast<const uint4*>(gt)[idx];
+                    four(ge.x, ge.y, sgn.x, xs + 32 * J + 8 * g, dot);
+                    four(ge.z, ge.w, sgn.y, xs + 32 * J + 8 * g + 4, dot);
+                }
+            }
+        }
+#pragma unroll
+        for (int m = 0; m < MT; ++m)
+            if (MT == 1 || m < M) tgt[m] = fmaf(eff61, dot[m].x + dot[m].y, tgt[m]);
+    };
+    sub(std::integral_constant<int, 0>{});
+    sub(std::integral_constant<int, 1>{});
+    sub(std::integral_constant<int, 2>{});
+    sub(std::integral_constant<int, 3>{});
+    sub(std::integral_constant<int, 4>{});
+    sub(std::integral_constant<int, 5>{});
+    sub(std::integral_constant<int, 6>{});
+    sub(std::integral_constant<int, 7>{});
+    if constexpr (RESCALE) {
+#pragma unroll
+        for (int m = 0; m < MT; ++m)
+            if (MT == 1 || m < M) acc[m] = fmaf(part[m], e2[m], acc[m]);
+    }
+}
+
+// Per-warp x preparation of one column (256 values per token, tokens 2048
+// floats apart) for the grid formats: scaled in place by 2^88; a token
+// whose largest |x| lies outside [2^-24, 2^39) is also scaled by 2^-e (e
+// the exponent of its largest |x|, clamped to [-100, 100]), e2[m] = 2^e
+// then (1 otherwise), and the return value, the same in every lane, says
+// whether any token was.  Callers fence the written x before the slot's
+// next copy.
+template <int MT>
+__device__ __forceinline__ bool cb_stage_x(float* xs, int M, int lane, float (&e2)[MT]) {
+    bool rescaled = false;
+#pragma unroll
+    for (int m = 0; m < MT; ++m) {
+        e2[m] = 1.f;
+        if (MT == 1 || m < M) {
+            float* xp = xs + m * 2048 + lane * 8;
+            float4 a = *reinterpret_cast<const float4*>(xp);
+            float4 b = *reinterpret_cast<const float4*>(xp + 4);
+            const float mx = fmaxf(fmaxf(fmaxf(fabsf(a.x), fabsf(a.y)), fmaxf(fabsf(a.z), fabsf(a.w))),
+                                   fmaxf(fmaxf(fabsf(b.x), fabsf(b.y)), fmaxf(fabsf(b.z), fabsf(b.w))));
+            const uint32_t top = __reduce_max_sync(0xffffffffu, __float_as_uint(mx));
+            const uint32_t be = top >> 23;
+            if (top != 0u && (be < kXExpLo || be >= kXExpHi)) {  // the same in every lane
+                const int e = min(max(static_cast<int>(be) - 127, -100), 100);
+                const float sc = __uint_as_float(static_cast<uint32_t>(127 - e) << 23);
+                a = make_float4(a.x * sc, a.y * sc, a.z * sc, a.w * sc);
+                b = make_float4(b.x * sc, b.y * sc, b.z * sc, b.w * sc);
+                e2[m] = __uint_as_float(static_cast<uint32_t>(127 + e) << 23);
+                rescaled = true;
+            }
+            constexpr float k88 = 0x1p88f;
+            *reinterpret_cast<float4*>(xp) = make_float4(a.x * k88, a.y * k88, a.z * k88, a.w * k88);
+            *reinterpret_cast<float4*>(xp + 4) = make_float4(b.x * k88, b.y * k88, b.z * k88, b.w * k88);
+        }
+    }
+    return rescaled;
+}
+
 constexpr int kCbCols = 8;        // columns per unit = consumer warps
 constexpr int kCbMaxStages = 4;
-// Dynamic shared memory: barriers at 0, the codebook at 128, the warps'
-// row sums at 2176, the ring from 8192.
-constexpr int kCbTable0 = 128, kCbRed0 = kCbTable0 + 2048, kCbRing0 = 8192;
-static_assert(sizeof(Table) <= 2048, "codebook slot");
+// Dynamic shared memory: barriers at 0, the codebook at 128 (IQ4: the 16
+// table values; grid formats: their tables), the warps' row sums after it,
+// the ring from 10240.
+constexpr int kCbTable0 = 128, kCbRed0 = kCbTable0 + kGridTabBytes, kCbRing0 = 10240;
+static_assert(sizeof(Table) <= kGridTabBytes, "codebook slot");
 __host__ __device__ constexpr int cb_stage_bytes(int F, int MT) {
     return kCbCols * 32 * (F == kIQ2XXS ? 80 : 144) + MT * kCbCols * 1024;
 }
@@ -397,7 +621,12 @@ __global__ void __launch_bounds__(kCbCols * 32 + 32, MINB)
         }
         fence_mbar_init();
     }
-    load_table<F>(book, T);
+    constexpr bool kGrid = F == kIQ3S || F == kIQ2XXS;
+    bool compact = false;  // grid formats: codebook bytes all below 128 (the same in every thread)
+    if constexpr (kGrid)
+        compact = load_grid_table<F>(book, smem + kCbTable0);
+    else
+        load_table<F>(book, T);
     __syncthreads();
 
     if (warp == kCbCols) {
@@ -444,16 +673,36 @@ __global__ void __launch_bounds__(kCbCols * 32 + 32, MINB)
         mbar_wait_bounded(&full[s], phase, status);
         if (warp < kc) {
             const uint8_t* boxrow = st + warp * kColBytes + lane * kBox;
-            const float* xs = reinterpret_cast<const float*>(st + kCbCols * kColBytes) + warp * 256;
+            float* xs = reinterpret_cast<float*>(const_cast<uint8_t*>(st) + kCbCols * kColBytes) + warp * 256;
             // the column's offset in its box: (kUB * column) mod 16, and
             // 8 * kUB is a multiple of 16
+            uint32_t v[row_words<F>()];
             switch ((warp * kUB) & 15) {
 #define QG_CB_COL(O) \
-    case O: cb_column<F, MT, O>(boxrow, xs, T, M, acc); break;
+    case O: load_row_words<F, O>(boxrow, v); break;
                 QG_CB_COL(0) QG_CB_COL(2) QG_CB_COL(4) QG_CB_COL(6)
                 QG_CB_COL(8) QG_CB_COL(10) QG_CB_COL(12) QG_CB_COL(14)
 #undef QG_CB_COL
                 default: break;
+            }
+            if constexpr (kGrid) {
+                float e2[MT];
+                const bool rescaled = cb_stage_x<MT>(xs, M, lane, e2);
+                __syncwarp();
+                const uint8_t* gt = smem + kCbTable0;
+                if (rescaled) {  // rare; the same in every lane
+                    if (compact)
+                        cb_grid_column<F, MT, true, true>(v, xs, gt, M, e2, acc);
+                    else
+                        cb_grid_column<F, MT, true, false>(v, xs, gt, M, e2, acc);
+                } else if (compact) {
+                    cb_grid_column<F, MT, false, true>(v, xs, gt, M, e2, acc);
+                } else {
+                    cb_grid_column<F, MT, false, false>(v, xs, gt, M, e2, acc);
+                }
+                fence_proxy_async_smem();  // x was written: order it before the slot's next copy
+            } else {
+                cb_iq4_column<F, MT>(v, xs, T, M, acc);
             }
         }
         __syncwarp();
@@ -488,14 +737,10 @@ __global__ void __launch_bounds__(kCbCols * 32 + 32, MINB)
     }
 }
 
-// The TMA path: the IQ4 formats (a 16-entry table lookup per weight), rows
-// whose pitch is a multiple of 16 bytes.  The grid formats (IQ3_S, IQ2_XXS)
-// stay on the direct-load kernel: their decode is a chain of dependent
-// table gathers per lane, which that kernel's 40 warps per SM (48 registers
-// a thread) hide better than this one's 16 (measured 2-3x faster there).
-inline bool tma_ok(int F, int64_t K) {
-    return (F == kIQ4NL || F == kIQ4XS) && ((K / 256) * unit_bytes(F)) % 16 == 0;
-}
+// The TMA path: every format whose rows are a multiple of 16 bytes (IQ4_NL
+// always; IQ4_XS for even K/256; IQ3_S and IQ2_XXS for K/256 a multiple of
+// 8).  Other rows take the direct-load kernel.
+inline bool tma_ok(int F, int64_t K) { return ((K / 256) * unit_bytes(F)) % 16 == 0; }
 
 template <int F, int MT, int MINB>
 int launch_tma(const uint8_t* W, const void* book, const float* X, float* Y, int M, int64_t N, int64_t K,
@@ -549,7 +794,7 @@ int launch_t(const uint8_t* W, const void* book, const float* X, float* Y, int M
     if (dev < 0) return qg::cuda_fail(cudaGetLastError());
     const int sms = sm_count(dev);
     if (sms <= 0) return qg::cuda_fail(cudaGetLastError());
-    if constexpr (F == kIQ4NL || F == kIQ4XS) {
+    {
         if (tma_ok(F, K)) {
             // groups of at most 4 tokens, each streaming W once
             for (int m0 = 0; m0 < M; m0 += 4) {

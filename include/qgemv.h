@@ -161,9 +161,14 @@ QG_API int qgemv_iq3xxs_ex(const uint8_t* W, const uint8_t* grid, const float* X
  *                  28-31; eff = d*(0.5+s)*0.25; codebook: 256 x 8 bytes
  * W [N][K/256 units], X [M][K], Y [M][N] as qgemv_q4k; 1 <= M <= 32;
  * codebook device memory, 16-byte aligned.  fp32 FMA path, tolerance
- * 1e-5 * sum|w*x| for |x| within [2^-100, 2^100] (x is multiplied as given,
- * so products must stay normal fp32 numbers).  Errors as qgemv_q4k, plus
- * QG_EINVAL for an unknown format. */
+ * 1e-5 * sum|w*x|.  Rows that are a multiple of 16 bytes (IQ4_NL always,
+ * IQ4_XS for even K/256, IQ3_S and IQ2_XXS for K/256 a multiple of 8)
+ * stream through tensor-map copies; the others are read directly.  Range
+ * of x: IQ3_S and IQ2_XXS on the tensor-map path take every finite x
+ * (columns whose largest |x| lies outside [2^-24, 2^39) are rescaled by a
+ * power of two); otherwise x is multiplied as given and |x| must stay
+ * within [2^-100, 2^100].  Errors as qgemv_q4k, plus QG_EINVAL for an
+ * unknown format. */
 #define QG_CB_IQ4_NL 1
 #define QG_CB_IQ4_XS 2
 #define QG_CB_IQ3_S 3

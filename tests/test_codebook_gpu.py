@@ -104,3 +104,56 @@ def test_extreme_scales(q, fmt):
     y = q.qgemv_codebook(fmt, dev(W), dev(tab), dev(x)).cpu().numpy()
     check(y, Y, A, f"{fmt} extreme scales")
     assert np.isfinite(y).all()
+
+
+@pytest.mark.parametrize("fmt", ["iq3s", "iq2xxs"])
+@pytest.mark.parametrize("scale", [2.0 ** -100, 2.0 ** -30, 1.0, 2.0 ** 45, 2.0 ** 110])
+@pytest.mark.parametrize("M", [1, 4])
+def test_grid_formats_x_range(q, fmt, scale, M):
+    """The grid formats on the TMA ring hold each weight as an fp32
+    subnormal against x pre-scaled by 2^88; columns whose largest |x| lies
+    outside [2^-24, 2^39) are rescaled by a power of two, so every finite x
+    meets the tolerance (K = 2048 and 4096: 16-byte rows, the ring)."""
+    for N, K in ((70, 2048), (33, 4096)):
+        W, tab = synth.gen_cb(fmt, N, K, 600 + N)
+        x = (synth.gen_x(M, K, 601) * np.float32(scale)).astype(np.float32)
+        Y, A = oracle.gemv_cb(fmt, W, tab, x)
+        y = q.qgemv_codebook(fmt, dev(W), dev(tab), dev(x)).cpu().numpy()
+        assert np.isfinite(y).all()
+        check(y, Y, A, f"{fmt} x scale {scale:g} N={N} K={K} M={M}")
+
+
+@pytest.mark.parametrize("fmt", ["iq3s", "iq2xxs"])
+def test_grid_formats_full_size_sampled(q, fmt):
+    """The page-3 grid formats at the IQ3 workload's shape (K=4096,
+    N=14336), sampled rows, through the TMA ring."""
+    N, K = 14336, 4096
+    W, tab = synth.gen_cb(fmt, N, K, 700)
+    x = synth.gen_x(1, K, 701)
+    rows = np.unique(np.concatenate([[0, N - 1], np.random.default_rng(5).integers(0, N, 96)]))
+    Y, A = oracle.gemv_cb(fmt, W, tab, x, rows=rows)
+    y = q.qgemv_codebook(fmt, dev(W), dev(tab), dev(x)).cpu().numpy()
+    check(y[:, rows], Y, A, f"{fmt} full size")
+
+
+@pytest.mark.parametrize("fmt", ["iq3s", "iq2xxs"])
+@pytest.mark.parametrize("M", [1, 3])
+def test_grid_formats_codebook_bytes_above_127(q, fmt, M):
+    """Codebooks with bytes of 128 and more (the published grids stay far
+    below) take the expanded table rows: against the oracle, and bit-exact
+    through one-hot x."""
+    N, K = 70, 2048
+    W, tab0 = synth.gen_cb(fmt, N, K, 800)
+    rng = np.random.default_rng(801)
+    tab = rng.integers(0, 256, tab0.shape, dtype=np.uint8)
+    tab.reshape(-1)[0] = 255
+    x = synth.gen_x(M, K, 802)
+    Y, A = oracle.gemv_cb(fmt, W, tab, x)
+    Wg, tg = dev(W), dev(tab)
+    check(q.qgemv_codebook(fmt, Wg, tg, dev(x)).cpu().numpy(), Y, A, f"{fmt} codebook bytes >= 128 M={M}")
+    Wd = oracle.dequant_cb(fmt, W, tab, K)
+    ks = 256 * ((7 * np.arange(32)) % (K // 256)) + 8 * np.arange(32)
+    xo = np.zeros((32, K), np.float32)
+    xo[np.arange(32), ks] = 1.0
+    y = q.qgemv_codebook(fmt, Wg, tg, dev(xo)).cpu().numpy()
+    assert np.array_equal(y, Wd[:, ks].T), fmt
