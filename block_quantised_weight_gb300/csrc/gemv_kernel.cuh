@@ -79,6 +79,7 @@ struct FmtQ4K {
     static constexpr int kBytes = 144;
     static constexpr int kCols = qg::kCols;
     static constexpr int kRowStride = kCols * 144 + 16;  // 1168 = 73 * 16 (odd)
+    static constexpr int kWPC = 1;                         // consumer warps per column
     static constexpr bool kIQ3 = false;
     static constexpr bool kTMA = false;
     static constexpr int kBoxBytes = 0;
@@ -89,12 +90,21 @@ struct FmtQ4KTc {
     static constexpr int kBytes = 144;
     static constexpr int kCols = C;
     static constexpr int kRowStride = C * 144;  // bytes per tile row per unit (C boxes of 144 B)
+    static constexpr int kWPC = 1;              // consumer warps per column
     static constexpr bool kIQ3 = false;
     static constexpr bool kTMA = true;
     static constexpr int kBoxBytes = 144;
     static constexpr int kXH = 128;  // x staged contiguously (one bulk copy per token)
 };
 using FmtQ4KT = FmtQ4KTc<kCols>;
+// The same stage layout with two consumer warps per column, one per half of
+// each block (lane L: rows L&15 and (L&15)+16, sub-block pair L>>4 of the
+// warp's half): 16 warps per unit, for launches that leave SMs with at most
+// one tile.  The SM's issue rate still bounds a unit's decode; the gain is in
+// the prologue work of the fused kernels, which the 16 warps share.
+struct FmtQ4KT2 : FmtQ4KTc<kCols> {
+    static constexpr int kWPC = 2;
+};
 // IQ3 block layouts (98 bytes, same fields, two orders):
 //   FmtIQ3T    page 4 "iq3_pack.py": 64 index bytes @0, eight u32 @64, fp16 d
 //              @96; value = d*(0.5+code)*0.5 * grid*0.5 * sign
@@ -106,6 +116,7 @@ struct FmtIQ3T {
     static constexpr int kBytes = 98;
     static constexpr int kCols = qg::kCols;
     static constexpr int kRowStride = kCols * 112;  // bytes per tile row per unit (kCols boxes of 112 B)
+    static constexpr int kWPC = 1;                  // consumer warps per column
     static constexpr bool kIQ3 = true;
     static constexpr bool kTMA = true;
     static constexpr int kBoxBytes = 112;
@@ -196,9 +207,9 @@ __device__ __forceinline__ int group_find(const Group& G, int64_t tile) {
 // xh = F::kXH when x is staged with the weights, 0 when it is read from
 // global memory.
 __host__ __device__ inline Layout make_layout(bool iq3, int MT, int xh, int RG, int stages, int row_stride,
-                                              int cols = kCols, int fuse = 0) {
+                                              int cols = kCols, int fuse = 0, int wpc = 1) {
     Layout L;
-    const int warps = RG * cols;
+    const int warps = RG * cols * wpc;
     L.full = 0;
     L.empty = 8 * kMaxStages;
     L.sx = 128;
@@ -324,6 +335,54 @@ __device__ __forceinline__ bool q4k_stage_x(float* xb, int64_t xstride, const fl
     return rescaled;
 }
 
+// q4k_stage_x for one half of a column, when two warps share the column
+// (FmtQ4KT2): xh = the half's 128 x values of token 0 (token m at
+// xh + m*xstride), ah likewise for the prologue operand; lane L takes
+// x[32*(L>>3) + 4*(L&7) .. +3], sub-block 4h + (L>>3), and writes its sum to
+// sx[m*8 + 4h + (L>>3)].  The range test covers the half's 128 values.
+template <int MT, int FUSE = 0>
+__device__ __forceinline__ bool q4k_stage_x_half(float* xh, int64_t xstride, const float* ah, int64_t astride,
+                                                 float* sx, int h, float (&ss)[MT], float (&e2)[MT], int M,
+                                                 int lane) {
+    bool rescaled = false;
+    const int off = (lane >> 3) * 32 + (lane & 7) * 4;
+#pragma unroll
+    for (int m = 0; m < MT; ++m) {
+        e2[m] = 1.f;
+        if (MT == 1 || m < M) {
+            float* xp = xh + m * xstride + off;
+            float4 a = *reinterpret_cast<const float4*>(xp);
+            if constexpr (FUSE == kFuseNorm) {
+                ss[m] = fmaf(a.x, a.x, fmaf(a.y, a.y, fmaf(a.z, a.z, fmaf(a.w, a.w, ss[m]))));
+                const float4 ga = *reinterpret_cast<const float4*>(ah + off);
+                a = make_float4(a.x * ga.x, a.y * ga.y, a.z * ga.z, a.w * ga.w);
+            } else if constexpr (FUSE == kFuseSwiGLU) {
+                const float4 ua = *reinterpret_cast<const float4*>(ah + m * astride + off);
+                a = make_float4(silu(a.x) * ua.x, silu(a.y) * ua.y, silu(a.z) * ua.z, silu(a.w) * ua.w);
+            }
+            const float mx = fmaxf(fmaxf(fabsf(a.x), fabsf(a.y)), fmaxf(fabsf(a.z), fabsf(a.w)));
+            const uint32_t top = __reduce_max_sync(0xffffffffu, __float_as_uint(mx));
+            const uint32_t be = top >> 23;
+            if (top != 0u && (be < kXExpLo || be >= kXExpHi)) {  // the same in every lane
+                const int e = min(max(static_cast<int>(be) - 127, -100), 100);
+                const float sc = __uint_as_float(static_cast<uint32_t>(127 - e) << 23);
+                a = make_float4(a.x * sc, a.y * sc, a.z * sc, a.w * sc);
+                e2[m] = __uint_as_float(static_cast<uint32_t>(127 + e) << 23);
+                rescaled = true;
+            }
+            float sm = (a.x + a.y) + (a.z + a.w);
+            sm += __shfl_xor_sync(0xffffffffu, sm, 1);
+            sm += __shfl_xor_sync(0xffffffffu, sm, 2);
+            sm += __shfl_xor_sync(0xffffffffu, sm, 4);
+            if ((lane & 7) == 0) sx[m * 8 + 4 * h + (lane >> 3)] = sm;
+            const float se = ((lane >> 3) & 1) ? 0x1p84f : 0x1p88f;  // even byte of the sub-block's nibbles
+            const float so = se * 0x1p-8f;                           // odd byte
+            *reinterpret_cast<float4*>(xp) = make_float4(a.x * se, a.y * so, a.z * se, a.w * so);
+        }
+    }
+    return rescaled;
+}
+
 // Offset of a Q4_K sub-block with scale a = d*sc and min b = dmin*mn: the
 // integer c in [0, 15] nearest b/a.  For any integer c
 //   sum_l (a*q_l - b)*x_l = a * sum_l (q_l - c)*x_l - (b - a*c) * sum_l x_l,
@@ -348,9 +407,14 @@ __device__ __forceinline__ float q4k_offset(float a, float b) {
 // min term is (b - a*c) * sum(x), then the scaled sum of (q - c)*x.  With
 // RESCALE the column's sums are formed apart and multiplied by e2[m] (the
 // 2^e of a token whose slice q4k_stage_x rescaled) before they join acc.
-template <int MT, int XH, bool RESCALE>
+//
+// NG = 2 takes both sub-block pairs of the half (g = 0, 1); NG = 1 only the
+// pair g = g1 (sub-blocks 4h+2g1 and 4h+2g1+1), for kernels whose two lanes
+// L and L^16 split a half between them (FmtQ4KT2).
+template <int MT, int XH, bool RESCALE, int NG = 2>
 __device__ __forceinline__ void q4k_half2(const uint8_t* blk, int rstride, int h, const float* xb, int64_t xstride,
-                                          const float* sx, int M, const float (&e2)[MT], float (&acc)[2][MT]) {
+                                          const float* sx, int M, const float (&e2)[MT], float (&acc)[2][MT],
+                                          int g1 = 0) {
     if constexpr (RESCALE && MT > 1) {
         // the rare rescaled column: one token at a time, which needs far fewer
         // registers than the MT-token decode and its separate column sums
@@ -359,7 +423,7 @@ __device__ __forceinline__ void q4k_half2(const uint8_t* blk, int rstride, int h
             if (m < M) {
                 float a1[2][1] = {{acc[0][m]}, {acc[1][m]}};
                 const float e1[1] = {e2[m]};
-                q4k_half2<1, XH, true>(blk, rstride, h, xb + m * xstride, xstride, sx + m * 8, 1, e1, a1);
+                q4k_half2<1, XH, true, NG>(blk, rstride, h, xb + m * xstride, xstride, sx + m * 8, 1, e1, a1, g1);
                 acc[0][m] = a1[0][0];
                 acc[1][m] = a1[1][0];
             }
@@ -388,7 +452,8 @@ __device__ __forceinline__ void q4k_half2(const uint8_t* blk, int rstride, int h
     const uint8_t* qb = blk + 16 + 64 * h;
     const float* xq = xb + XH * h;
 #pragma unroll
-    for (int g = 0; g < 2; ++g) {
+    for (int gi = 0; gi < NG; ++gi) {
+        const int g = NG == 2 ? gi : g1;
         // sub-blocks 4h+2g (low nibbles) and 4h+2g+1 (high nibbles) of each row
         float al61[2], ah61[2];  // a * 2^61 (the pre-scaling of x is 2^-61 in the products)
         f2 ol[2], oh[2];         // -c at the subnormal scales of the nibbles' bit offsets
@@ -719,11 +784,12 @@ __device__ __forceinline__ void named_barrier_sync_n(int id, int n) {
 // padded layout above) and decoded two rows per lane (lane L: rows L&15 and
 // (L&15)+16, half L>>4 of each block).
 template <class F, int MT, int RG, int MINB, int FUSE = 0>
-__global__ void __launch_bounds__(RG * F::kCols * 32 + 32, MINB)
+__global__ void __launch_bounds__(RG * F::kCols * F::kWPC * 32 + 32, MINB)
     qg_gemv_kernel(const __grid_constant__ Group G, const __grid_constant__ TMaps T, const __grid_constant__ Fuse Fz,
                 const uint8_t* __restrict__ grid, const float* __restrict__ X, int M, int64_t K, int stages,
                 unsigned* status, int flags) {
-    constexpr int kWarps = RG * F::kCols;          // consumer warps
+    constexpr int kRGWarps = F::kCols * F::kWPC;   // consumer warps per row group
+    constexpr int kWarps = RG * kRGWarps;          // consumer warps
     constexpr int kConsumerThreads = kWarps * 32;
     constexpr int kTileRows = RG * kRows;
     extern __shared__ __align__(128) uint8_t smem[];
@@ -731,8 +797,9 @@ __global__ void __launch_bounds__(RG * F::kCols * 32 + 32, MINB)
     const int nchunks = (nb + F::kCols - 1) / F::kCols;
     const int64_t ntiles = G.tile0[G.count];
     constexpr int XH = F::kXH;  // floats from half 0 to half 1 of a staged x column
-    const Layout L = make_layout(F::kIQ3, MT, XH, RG, stages, F::kRowStride, F::kCols, FUSE);
+    const Layout L = make_layout(F::kIQ3, MT, XH, RG, stages, F::kRowStride, F::kCols, FUSE, F::kWPC);
     static_assert(FUSE == 0 || !F::kIQ3, "fused prologues run on the Q4_K path");
+    static_assert(F::kWPC == 1 || (F::kWPC == 2 && !F::kIQ3 && RG == 1), "two warps per column: Q4_K, one row group");
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.full);
     uint64_t* empty = reinterpret_cast<uint64_t*>(smem + L.empty);
     float* sxw = reinterpret_cast<float*>(smem + L.sx);
@@ -896,7 +963,8 @@ __global__ void __launch_bounds__(RG * F::kCols * 32 + 32, MINB)
 
     // ---------------- consumer warps
     if (prefetch) grid_dependency_wait();  // x and Y belong to the dependency chain
-    const int rg = warp / F::kCols, cw = warp % F::kCols;
+    const int rg = warp / kRGWarps, cw = warp % F::kCols;
+    const int hw = (warp / F::kCols) % F::kWPC;  // FmtQ4KT2: the warp's half of its column
     // two rows per lane (acc2[j]: row (lane&15) + 16j, half lane>>4)
     float acc2[2][MT];
     float ss[MT];  // RMSNorm prologue: this lane's part of sum(x^2) over the tile's units
@@ -938,7 +1006,22 @@ __global__ void __launch_bounds__(RG * F::kCols * 32 + 32, MINB)
         if (cw < kc) {
             const float* xb = reinterpret_cast<const float*>(st + L.xoff) + cw * 2 * XH;
             const int64_t xstride = F::kCols * 2 * XH;
-            if constexpr (!F::kIQ3) {
+            if constexpr (!F::kIQ3 && F::kWPC == 2) {
+                // half hw of the column: its x (128 values per token), then
+                // sub-block pair lane>>4 of the half for rows lane&15 and +16
+                float* sxp = sxw + warp * MT * 8;
+                const float* ab = reinterpret_cast<const float*>(st + L.aoff) + cw * 256 + hw * 128;
+                float e2[MT];
+                const bool rescaled = q4k_stage_x_half<MT, FUSE>(const_cast<float*>(xb) + hw * XH, xstride, ab,
+                                                                 F::kCols * 256, sxp, hw, ss, e2, M, lane);
+                __syncwarp();
+                const uint8_t* blk = st + cw * (kTileRows * F::kBytes) + (lane & 15) * F::kBytes;
+                if (rescaled)  // x outside the direct range (rare; the same in every lane)
+                    q4k_half2<MT, XH, true, 1>(blk, 16 * F::kBytes, hw, xb, xstride, sxp, M, e2, acc2, lane >> 4);
+                else
+                    q4k_half2<MT, XH, false, 1>(blk, 16 * F::kBytes, hw, xb, xstride, sxp, M, e2, acc2, lane >> 4);
+                fence_proxy_async_smem();  // x was written: order it before the slot's next copy
+            } else if constexpr (!F::kIQ3) {
                 float* sxp = sxw + warp * MT * 8;
                 const float* ab = reinterpret_cast<const float*>(st + L.aoff) + cw * 256;
                 float e2[MT];
@@ -1017,7 +1100,8 @@ __global__ void __launch_bounds__(RG * F::kCols * 32 + 32, MINB)
             float* rb = red + (tile_count & 1) * (kWarps * MT * kRows);
 #pragma unroll
             for (int m = 0; m < MT; ++m) {
-                // lanes L and L^16 hold the two halves of rows L&15 and (L&15)+16
+                // lanes L and L^16 hold the two halves (FmtQ4KT2: the two
+                // sub-block pairs of the warp's half) of rows L&15 and (L&15)+16
                 const float s0 = acc2[0][m] + __shfl_xor_sync(0xffffffffu, acc2[0][m], 16);
                 const float s1 = acc2[1][m] + __shfl_xor_sync(0xffffffffu, acc2[1][m], 16);
                 rb[(warp * MT + m) * kRows + lane] = lane < 16 ? s0 : s1;
@@ -1057,7 +1141,7 @@ __global__ void __launch_bounds__(RG * F::kCols * 32 + 32, MINB)
                     const int g = rr / kRows, ln = rr % kRows;
                     float sum = 0.f;
 #pragma unroll
-                    for (int w = 0; w < F::kCols; ++w) sum += rb[((g * F::kCols + w) * MT + m) * kRows + ln];
+                    for (int w = 0; w < kRGWarps; ++w) sum += rb[((g * kRGWarps + w) * MT + m) * kRows + ln];
                     st_cluster_f32(cred + crank * MT * kTileRows + t, 0, sum);
                 }
                 if (FUSE == kFuseNorm && threadIdx.x < MT) {
@@ -1087,7 +1171,7 @@ __global__ void __launch_bounds__(RG * F::kCols * 32 + 32, MINB)
                     if ((MT == 1 || m < M) && rr < rows) {
                         float sum = 0.f, sq = 0.f;
 #pragma unroll
-                        for (int w = 0; w < F::kCols; ++w) sum += rb[((g * F::kCols + w) * MT + m) * kRows + ln];
+                        for (int w = 0; w < kRGWarps; ++w) sum += rb[((g * kRGWarps + w) * MT + m) * kRows + ln];
                         if (FUSE == kFuseNorm)
                             for (int w = 0; w < kWarps; ++w) sq += ssw[w * MT + m];
                         finish(m, rr, sum, sq);

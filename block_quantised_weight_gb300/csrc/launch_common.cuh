@@ -37,13 +37,14 @@ int launch_gemv(const uint8_t* const* W, float* const* Y, const int64_t* N, int 
                 const float* X, int M, int64_t K, cudaStream_t s, unsigned* status, int dev, unsigned flags,
                 int csize = 1, const Fuse* fz = nullptr) {
     static std::atomic<bool> attr_done[64];
+    constexpr int kThreads = RG * F::kCols * F::kWPC * 32 + 32;  // consumer warps + the producer
     const int budget = std::min(kSmemPerCTA, kSmemPerSM / MINB - kSmemReserve);
-    const Layout L1 = make_layout(F::kIQ3, MT, F::kXH, RG, 1, F::kRowStride, F::kCols, FUSE);
+    const Layout L1 = make_layout(F::kIQ3, MT, F::kXH, RG, 1, F::kRowStride, F::kCols, FUSE, F::kWPC);
     const int stages_fit = std::min(kMaxStages, (budget - L1.stage0) / L1.stage_bytes);
     if (stages_fit < 2) return QG_EINVAL;
     auto kern = qg_gemv_kernel<F, MT, RG, MINB, FUSE>;
     if (!attr_done[dev].load(std::memory_order_acquire)) {
-        const Layout Lmax = make_layout(F::kIQ3, MT, F::kXH, RG, stages_fit, F::kRowStride, F::kCols, FUSE);
+        const Layout Lmax = make_layout(F::kIQ3, MT, F::kXH, RG, stages_fit, F::kRowStride, F::kCols, FUSE, F::kWPC);
         if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Lmax.total) != cudaSuccess)
             return qg::cuda_fail(cudaGetLastError());
         attr_done[dev].store(true, std::memory_order_release);
@@ -87,11 +88,11 @@ int launch_gemv(const uint8_t* const* W, float* const* Y, const int64_t* N, int 
     const int64_t nch = (K / 256 + F::kCols - 1) / F::kCols;
     const int64_t units = csize > 1 ? 1 : (ntiles + grid_x - 1) / grid_x * nch;
     const int stages = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(stages_fit, units)));
-    const Layout L = make_layout(F::kIQ3, MT, F::kXH, RG, stages, F::kRowStride, F::kCols, FUSE);
+    const Layout L = make_layout(F::kIQ3, MT, F::kXH, RG, stages, F::kRowStride, F::kCols, FUSE, F::kWPC);
     const int kflags = ((flags & QG_PREFETCH_WEIGHTS) ? kFlagPrefetchWeights : 0) |
                        (csize > 1 ? csize << kFlagClusterShift : 0);
     if (!(flags & QG_PREFETCH_WEIGHTS) && csize <= 1) {
-        kern<<<grid_x, RG * F::kCols * 32 + 32, L.total, s>>>(G, T, Fz, grid, X, M, K, stages, status, kflags);
+        kern<<<grid_x, kThreads, L.total, s>>>(G, T, Fz, grid, X, M, K, stages, status, kflags);
         return launch_status();
     }
     // programmatic dependent launch (this grid may start before the previous
@@ -99,7 +100,7 @@ int launch_gemv(const uint8_t* const* W, float* const* Y, const int64_t* N, int 
     // a cluster launch
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid_x);
-    cfg.blockDim = dim3(RG * F::kCols * 32 + 32);
+    cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = L.total;
     cfg.stream = s;
     cudaLaunchAttribute attr[2];

@@ -17,7 +17,9 @@ int launch_group_q4k_t(const uint8_t* const* W, float* const* Y, const int64_t* 
     if (dev < 0) return qg::cuda_fail(cudaGetLastError());
     if (FUSE != 0 && M > 4) return QG_EINVAL;
     // Launches with at most one 32-row tile per SM are latency-bound: run them
-    // one CTA per SM with the deepest ring that fits.
+    // one CTA per SM.  A unit's decode is bound by the SM's issue rate either
+    // way, but the prologue kernels (RMSNorm, SwiGLU) measure faster with 16
+    // consumer warps, two per column (FmtQ4KT2).
     int64_t tiles = 0;
     for (int i = 0; i < count; ++i) tiles += (N[i] + kRows - 1) / kRows;
     const int sms = sm_count(dev);
@@ -33,6 +35,9 @@ int launch_group_q4k_t(const uint8_t* const* W, float* const* Y, const int64_t* 
         if (mg == 1 && csize > 1)
             rc = launch_gemv<FmtQ4KT, 1, 1, 2, FUSE>(W, Y, N, count, m0, nullptr, Xg, mg, K, s, status, dev,
                                                            flags, csize, fz);
+        else if (mg == 1 && few_tiles && FUSE != 0)  // prologue kernels: two warps per column stage x in parallel
+            rc = launch_gemv<FmtQ4KT2, 1, 1, 1, FUSE>(W, Y, N, count, m0, nullptr, Xg, mg, K, s, status, dev,
+                                                            flags, 1, fz);
         else if (mg == 1 && few_tiles)  // one CTA per SM: a deeper ring prefetches every unit of a tile
             rc = launch_gemv<FmtQ4KT, 1, 1, 1, FUSE>(W, Y, N, count, m0, nullptr, Xg, mg, K, s, status, dev,
                                                            flags, 1, fz);
