@@ -161,17 +161,19 @@ __device__ __forceinline__ void decode_sub_iq4_factored(const Raw& R, int64_t sb
     }
 }
 
+// Codebook -> shared memory, by threads tid = 0..nt-1 (the whole CTA by
+// default).
 template <int F>
-__device__ void load_table(const void* book, Table& T) {
+__device__ void load_table(const void* book, Table& T, int tid = threadIdx.x, int nt = blockDim.x) {
     if constexpr (F == kIQ4NL || F == kIQ4XS) {
         const int8_t* t = static_cast<const int8_t*>(book);
-        for (int i = threadIdx.x; i < 16; i += blockDim.x) T.iq4[i] = static_cast<float>(t[i]);
+        for (int i = tid; i < 16; i += nt) T.iq4[i] = static_cast<float>(t[i]);
     } else if constexpr (F == kIQ3S) {
         const uint32_t* t = static_cast<const uint32_t*>(book);
-        for (int i = threadIdx.x; i < 512; i += blockDim.x) T.iq3s[i] = t[i];
+        for (int i = tid; i < 512; i += nt) T.iq3s[i] = t[i];
     } else {
         const uint2* t = static_cast<const uint2*>(book);
-        for (int i = threadIdx.x; i < 256; i += blockDim.x) T.iq2[i] = t[i];
+        for (int i = tid; i < 256; i += nt) T.iq2[i] = t[i];
     }
 }
 
@@ -386,18 +388,34 @@ __device__ __forceinline__ uint32_t spread2(uint32_t w) { return (w & 0xFFu) | (
 // the bytes per gather) and the permute takes the zero bytes from the
 // sign-replicate of the grid byte itself (its top bit is 0); otherwise the
 // rows are expanded as above.
+// Nonzero in every participating thread when pred is nonzero in any of
+// the nt threads (a multiple of 32) that meet on named barrier id.
+__device__ __forceinline__ bool named_barrier_or(int id, int nt, bool pred) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 p, %1, 0;\n\t"
+        "barrier.cta.red.or.pred q, %2, %3, p;\n\t"
+        "selp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r) : "r"(static_cast<uint32_t>(pred)), "r"(id), "r"(nt) : "memory");
+    return r != 0u;
+}
+
+// Threads tid = 0..nt-1, all of which call it, meeting on named barrier
+// bar (nt a multiple of 32); the caller synchronises them again before the
+// table is read.
 template <int F>
-__device__ bool load_grid_table(const void* book, uint8_t* gt) {
+__device__ bool load_grid_table(const void* book, uint8_t* gt, int tid, int nt, int bar) {
     const uint32_t* w = static_cast<const uint32_t*>(book);
     uint32_t high = 0;
-    for (int i = threadIdx.x; i < 512; i += blockDim.x) high |= w[i];  // both formats: 2 KB
-    const bool compact = __syncthreads_or((high & 0x80808080u) != 0u) == 0;
+    for (int i = tid; i < 512; i += nt) high |= w[i];  // both formats: 2 KB
+    const bool compact = !named_barrier_or(bar, nt, (high & 0x80808080u) != 0u);
     if (compact) {
         uint32_t* t = reinterpret_cast<uint32_t*>(gt);
-        for (int i = threadIdx.x; i < 512; i += blockDim.x) t[i] = w[i];
+        for (int i = tid; i < 512; i += nt) t[i] = w[i];
         if constexpr (F == kIQ2XXS) {
             uint2* sg = reinterpret_cast<uint2*>(gt + 4096);
-            for (int i = threadIdx.x; i < 128; i += blockDim.x) {
+            for (int i = tid; i < 128; i += nt) {
                 const uint32_t s8 = static_cast<uint32_t>(i) | ((__popc(i) & 1u) << 7);
                 sg[i] = make_uint2(sign_bytes(s8 & 15u), sign_bytes(s8 >> 4));
             }
@@ -407,16 +425,16 @@ __device__ bool load_grid_table(const void* book, uint8_t* gt) {
     if constexpr (F == kIQ3S) {
         const uint32_t* t = static_cast<const uint32_t*>(book);
         uint2* e = reinterpret_cast<uint2*>(gt);
-        for (int i = threadIdx.x; i < 512; i += blockDim.x) e[i] = make_uint2(spread2(t[i]), spread2(t[i] >> 16));
+        for (int i = tid; i < 512; i += nt) e[i] = make_uint2(spread2(t[i]), spread2(t[i] >> 16));
     } else {
         const uint2* t = static_cast<const uint2*>(book);
         uint4* e = reinterpret_cast<uint4*>(gt);
-        for (int i = threadIdx.x; i < 256; i += blockDim.x) {
+        for (int i = tid; i < 256; i += nt) {
             const uint2 g = t[i];
             e[i] = make_uint4(spread2(g.x), spread2(g.x >> 16), spread2(g.y), spread2(g.y >> 16));
         }
         uint2* sg = reinterpret_cast<uint2*>(gt + 4096);
-        for (int i = threadIdx.x; i < 128; i += blockDim.x) {
+        for (int i = tid; i < 128; i += nt) {
             const uint32_t s8 = static_cast<uint32_t>(i) | ((__popc(i) & 1u) << 7);
             sg[i] = make_uint2(sign_bytes(s8 & 15u), sign_bytes(s8 >> 4));
         }
@@ -495,9 +513,16 @@ __device__ __forceinline__ void cb_grid_column(const uint32_t (&v)[row_words<F>(
             const uint32_t sc = (R.r[0] >> (16 + 4 * (J & 3))) & 15u;
             eff61 = h2f(R.r[0]) * static_cast<float>(1u + 2u * sc) * 0x1p61f;
             const uint32_t qh = (R.r[3] >> (8 * (J & 1))) & 0xFFu, sg = R.r[4];
+            // the ninth index bits, bit k of each half of qh moved to bit 0
+            // of byte k (no two shifted copies overlap), so that one byte
+            // permute per group joins an index's two bytes: [low, high, 0, 0]
+            const uint32_t hb[2] = {((qh & 15u) * 0x00204081u) & 0x01010101u, ((qh >> 4) * 0x00204081u) & 0x01010101u};
 #pragma unroll
             for (int g = 0; g < 8; ++g) {
-                const uint32_t idx = (((g < 4 ? R.r[1] : R.r[2]) >> (8 * (g & 3))) & 0xFFu) | (((qh >> g) & 1u) << 8);
+                constexpr uint32_t kZero = 0xCu;  // replicate bit 7 of byte 0 of hb (clear): a zero byte
+                const uint32_t idx = prmt(g < 4 ? R.r[1] : R.r[2], hb[g >> 2],
+                                          static_cast<uint32_t>(g & 3) | ((4u + (g & 3)) << 4) | (kZero << 8) |
+                                              (kZero << 12));
                 const uint32_t sgn = sign_bytes((sg >> (4 * g)) & 15u);
                 if constexpr (COMPACT) {
                     four(reinterpret_cast<const uint32_t*>(gt)[idx], 0u, sgn, xs + 32 * J + 4 * g, dot);
@@ -622,13 +647,11 @@ __global__ void __launch_bounds__(kCbCols * 32 + 32, MINB)
         fence_mbar_init();
     }
     constexpr bool kGrid = F == kIQ3S || F == kIQ2XXS;
-    bool compact = false;  // grid formats: codebook bytes all below 128 (the same in every thread)
-    if constexpr (kGrid)
-        compact = load_grid_table<F>(book, smem + kCbTable0);
-    else
-        load_table<F>(book, T);
-    __syncthreads();
+    __syncthreads();  // the barriers are initialised
 
+    // The producer starts the weight stream at once; the consumer warps
+    // build the codebook table meanwhile (named barriers 2 and 3 among
+    // them), so its global loads overlap the first copies.
     if (warp == kCbCols) {
         // ---------------- producer
         if (lane == 0) {
@@ -661,6 +684,12 @@ __global__ void __launch_bounds__(kCbCols * 32 + 32, MINB)
     }
 
     // ---------------- consumers: warp = column, lane = row
+    bool compact = false;  // grid formats: codebook bytes all below 128 (the same in every consumer)
+    if constexpr (kGrid)
+        compact = load_grid_table<F>(book, smem + kCbTable0, threadIdx.x, kCbCols * 32, 3);
+    else
+        load_table<F>(book, T, threadIdx.x, kCbCols * 32);
+    named_barrier_sync<kCbCols * 32>(2);
     float acc[MT];
 #pragma unroll
     for (int m = 0; m < MT; ++m) acc[m] = 0.f;
