@@ -98,6 +98,27 @@ def test_large_activations_and_extreme_silu(q):
     check(q.qgemv_q4k_fused(dev(W), dev(x), norm_weight=dev(g), eps=1e-6).cpu().numpy(), Y, A, what="norm scale")
 
 
+@pytest.mark.parametrize("N", [96, 9728])   # few tiles: two warps per column; 304 tiles: one warp per column
+@pytest.mark.parametrize("scale", [2.0 ** 50, 2.0 ** -40])
+def test_prologue_output_outside_direct_range(q, N, scale):
+    """The prologue's output (x * g before 1/rms, silu(gate) * up) far
+    outside [2^-24, 2^39): the staged column is rescaled by a power of two
+    and its sums scaled back, in both fused kernels."""
+    K = 2048
+    W = synth.gen_q4k(N, K, 5000 + N)
+    x = synth.gen_x(1, K, 18) * scale
+    g = synth.gen_x(1, K, 19)[0]
+    Y, A = oracle.fused_gemv_q4k(W, x, norm_weight=g, eps=0.0)
+    y = q.qgemv_q4k_fused(dev(W), dev(x), norm_weight=dev(g), eps=0.0)
+    check(y.cpu().numpy(), Y, A, what=f"rmsnorm N={N} x*{scale:g}")
+    gate = synth.gen_x(1, K, 20)
+    up = synth.gen_x(1, K, 21) * scale
+    Y, A = oracle.fused_gemv_q4k(W, gate, up=up)
+    y = q.qgemv_q4k_fused(dev(W), dev(gate), up=dev(up))
+    check(y.cpu().numpy(), Y, A, what=f"swiglu N={N} up*{scale:g}")
+    assert q.qg_device_status() == q.QG_OK
+
+
 @pytest.mark.parametrize("flags", [0, 1])
 def test_group_rmsnorm_qkv(q, flags):
     """q/k/v of one TinyLlama-shaped layer (2048 -> 2048, 256, 256) with the
