@@ -236,8 +236,10 @@ __global__ void __launch_bounds__(kCols * 32 + 32, pass_ctas_per_sm<MT>())
                     }
                 }
             }
-            // this CTA's part of stage si is written: publish it
-            __threadfence();
+            // this CTA's part of stage si is written: publish it.  The barrier
+            // orders every consumer's Y stores before thread 0's gpu-scope
+            // fence, which releases them (cumulatively) ahead of the count; a
+            // fence in each storing thread as well is not needed.
             named_barrier_sync<kConsumerThreads>(1);
             if (threadIdx.x == 0) {
                 __threadfence();
