@@ -249,7 +249,12 @@ typedef struct qg_stage {
  * cooperative launch.  Stage s reads its X only after every stage < s has
  * written all of its Y, so X of a stage may be any Y of an earlier stage;
  * the weights of later stages stream while earlier stages finish.
- * Results are identical to qgemv_q4k_group per stage.  1 <= M <= 4,
+ * Each stage meets the same tolerance as qgemv_q4k_group.  Results are
+ * identical to it bit for bit where the grouped launch also decodes a
+ * tile's K chunks in one CTA (one 32-row tile per CTA and one K chunk, or
+ * more tiles than the SMs can each take one of); where it splits a tile's K
+ * chunks over a cluster (few tiles, 2 to 8 chunks) the partial sums meet in
+ * another order.  1 <= M <= 4,
  * 1 <= nstages <= QG_MAX_PASS_STAGES.  `stages` is a host array.
  * sync: caller-owned device memory of at least 4*nstages bytes (4-byte
  * aligned) used for the stage completion counts; the call zeroes it on the
