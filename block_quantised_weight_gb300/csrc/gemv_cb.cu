@@ -374,6 +374,11 @@ __device__ __forceinline__ void cb_iq4_column(const uint32_t (&v)[row_words<F>()
 //            then the sign bytes of each 7-bit field (the eighth sign
 //            its parity: an even count of negatives)                128 x 8 bytes
 constexpr int kGridTabBytes = 5120;
+// Compact tables are kept in kGridCopies copies, entry i of copy c at
+// i * kGridCopies + c, lane L reading copy L & 7: the 32 rows' random
+// lookups then meet at most 4 to a copy instead of 32 to one table (a
+// capture counted 4.7 wavefronts per lookup with one copy).
+constexpr int kGridCopies = 8;
 
 // Sign bytes of four sign bits: bit k of nib -> bit 8k+7 (one multiply
 // places bit k at k, k+7, k+14, k+21 and k+28, which never collide).
@@ -411,12 +416,17 @@ __device__ bool load_grid_table(const void* book, uint8_t* gt, int tid, int nt, 
     for (int i = tid; i < 512; i += nt) high |= w[i];  // both formats: 2 KB
     const bool compact = !named_barrier_or(bar, nt, (high & 0x80808080u) != 0u);
     if (compact) {
-        uint32_t* t = reinterpret_cast<uint32_t*>(gt);
-        for (int i = tid; i < 512; i += nt) t[i] = w[i];
-        if constexpr (F == kIQ2XXS) {
-            uint2* sg = reinterpret_cast<uint2*>(gt + 4096);
-            for (int i = tid; i < 128; i += nt) {
-                const uint32_t s8 = static_cast<uint32_t>(i) | ((__popc(i) & 1u) << 7);
+        if constexpr (F == kIQ3S) {
+            uint32_t* t = reinterpret_cast<uint32_t*>(gt);
+            for (int i = tid; i < 512 * kGridCopies; i += nt) t[i] = w[i / kGridCopies];
+        } else {
+            uint2* t = reinterpret_cast<uint2*>(gt);
+            const uint2* w2 = static_cast<const uint2*>(book);
+            for (int i = tid; i < 256 * kGridCopies; i += nt) t[i] = w2[i / kGridCopies];
+            uint2* sg = reinterpret_cast<uint2*>(gt + 256 * 8 * kGridCopies);
+            for (int i = tid; i < 128 * kGridCopies; i += nt) {
+                const uint32_t s7 = static_cast<uint32_t>(i / kGridCopies);
+                const uint32_t s8 = s7 | ((__popc(s7) & 1u) << 7);
                 sg[i] = make_uint2(sign_bytes(s8 & 15u), sign_bytes(s8 >> 4));
             }
         }
@@ -461,14 +471,15 @@ __device__ __forceinline__ float grid_val_c(uint32_t g, uint32_t s) {
 // acc (a token whose column cb_stage_x rescaled).
 template <int F, int MT, bool RESCALE, bool COMPACT>
 __device__ __forceinline__ void cb_grid_column(const uint32_t (&v)[row_words<F>()], const float* xs,
-                                               const uint8_t* gt, int M, const float (&e2)[MT], float (&acc)[MT]) {
+                                               const uint8_t* gt, int M, const float (&e2)[MT], float (&acc)[MT],
+                                               uint32_t lc) {
     if constexpr (RESCALE && MT > 1) {
 #pragma unroll
         for (int m = 0; m < MT; ++m) {
             if (m < M) {
                 float a1[1] = {acc[m]};
                 const float e1[1] = {e2[m]};
-                cb_grid_column<F, 1, true, COMPACT>(v, xs + m * 2048, gt, 1, e1, a1);
+                cb_grid_column<F, 1, true, COMPACT>(v, xs + m * 2048, gt, 1, e1, a1, lc);
                 acc[m] = a1[0];
             }
         }
@@ -525,7 +536,7 @@ __device__ __forceinline__ void cb_grid_column(const uint32_t (&v)[row_words<F>(
                                               (kZero << 12));
                 const uint32_t sgn = sign_bytes((sg >> (4 * g)) & 15u);
                 if constexpr (COMPACT) {
-                    four(reinterpret_cast<const uint32_t*>(gt)[idx], 0u, sgn, xs + 32 * J + 4 * g, dot);
+                    four(reinterpret_cast<const uint32_t*>(gt)[idx * kGridCopies + lc], 0u, sgn, xs + 32 * J + 4 * g, dot);
                 } else {
                     const uint2 ge = reinterpret_cast<const uint2*>(gt)[idx];
                     four(ge.x, ge.y, sgn, xs + 32 * J + 4 * g, dot);
@@ -535,13 +546,14 @@ __device__ __forceinline__ void cb_grid_column(const uint32_t (&v)[row_words<F>(
             // eff = d*(0.5+s)*0.25; four 8-weight groups, each a grid index byte and a 7-bit sign field
             const uint32_t aux0 = R.r[1], aux1 = R.r[2];
             eff61 = h2f(R.r[0]) * (0.5f + static_cast<float>(aux1 >> 28)) * (0.25f * 0x1p61f);
-            const uint2* sgt = reinterpret_cast<const uint2*>(gt + 4096);
+            const uint2* sgt = reinterpret_cast<const uint2*>(gt + (COMPACT ? 256 * 8 * kGridCopies : 4096));
 #pragma unroll
             for (int g = 0; g < 4; ++g) {
                 const uint32_t idx = (aux0 >> (8 * g)) & 0xFFu;
-                const uint2 sgn = sgt[(aux1 >> (7 * g)) & 0x7Fu];
+                const uint32_t s7 = (aux1 >> (7 * g)) & 0x7Fu;
+                const uint2 sgn = COMPACT ? sgt[s7 * kGridCopies + lc] : sgt[s7];
                 if constexpr (COMPACT) {
-                    const uint2 ge = reinterpret_cast<const uint2*>(gt)[idx];
+                    const uint2 ge = reinterpret_cast<const uint2*>(gt)[idx * kGridCopies + lc];
                     four(ge.x, 0u, sgn.x, xs + 32 * J + 8 * g, dot);
                     four(ge.y, 0u, sgn.y, xs + 32 * J + 8 * g + 4, dot);
                 } else {
@@ -612,8 +624,17 @@ constexpr int kCbMaxStages = 4;
 // Dynamic shared memory: barriers at 0, the codebook at 128 (IQ4: the 16
 // table values; grid formats: their tables), the warps' row sums after it,
 // the ring from 10240.
-constexpr int kCbTable0 = 128, kCbRed0 = kCbTable0 + kGridTabBytes, kCbRing0 = 10240;
+constexpr int kCbTable0 = 128;
 static_assert(sizeof(Table) <= kGridTabBytes, "codebook slot");
+// The codebook region: IQ4's Table or an expanded grid table (at most
+// kGridTabBytes), or a compact grid table in kGridCopies copies (IQ2_XXS
+// with its sign table); then the row sums (up to 4 tokens), then the ring.
+__host__ __device__ constexpr int cb_table_bytes(int F) {
+    return F == kIQ3S ? 512 * 4 * kGridCopies : F == kIQ2XXS ? (256 + 128) * 8 * kGridCopies : kGridTabBytes;
+}
+__host__ __device__ constexpr int cb_red0(int F) { return kCbTable0 + cb_table_bytes(F); }
+__host__ __device__ constexpr int cb_ring0(int F) { return (cb_red0(F) + kCbCols * 4 * 32 * 4 + 1023) / 1024 * 1024; }
+static_assert(cb_table_bytes(kIQ3S) >= kGridTabBytes && cb_table_bytes(kIQ2XXS) >= kGridTabBytes, "expanded tables fit");
 __host__ __device__ constexpr int cb_stage_bytes(int F, int MT) {
     return kCbCols * 32 * (F == kIQ2XXS ? 80 : 144) + MT * kCbCols * 1024;
 }
@@ -625,14 +646,14 @@ __global__ void __launch_bounds__(kCbCols * 32 + 32, MINB)
                        unsigned* status) {
     extern __shared__ __align__(1024) uint8_t smem[];
     Table& T = *reinterpret_cast<Table*>(smem + kCbTable0);
-    float (*red)[MT][32] = reinterpret_cast<float (*)[MT][32]>(smem + kCbRed0);
-    static_assert(kCbRed0 + kCbCols * MT * 32 * 4 <= kCbRing0, "row-sum slot");
+    float (*red)[MT][32] = reinterpret_cast<float (*)[MT][32]>(smem + cb_red0(F));
+    static_assert(MT <= 4 && cb_red0(F) + kCbCols * MT * 32 * 4 <= cb_ring0(F), "row-sum slot");
     constexpr int kBox = Box<F>::kBox, kUB = Box<F>::kUB;
     constexpr int kColBytes = 32 * kBox;
     constexpr int kSB = cb_stage_bytes(F, MT);
     uint64_t* full = reinterpret_cast<uint64_t*>(smem);
     uint64_t* empty = full + kCbMaxStages;
-    uint8_t* ring = smem + kCbRing0;
+    uint8_t* ring = smem + cb_ring0(F);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int nb = static_cast<int>(K / 256);
     const int nchunks = (nb + kCbCols - 1) / kCbCols;
@@ -721,13 +742,13 @@ __global__ void __launch_bounds__(kCbCols * 32 + 32, MINB)
                 const uint8_t* gt = smem + kCbTable0;
                 if (rescaled) {  // rare; the same in every lane
                     if (compact)
-                        cb_grid_column<F, MT, true, true>(v, xs, gt, M, e2, acc);
+                        cb_grid_column<F, MT, true, true>(v, xs, gt, M, e2, acc, lane & 7);
                     else
-                        cb_grid_column<F, MT, true, false>(v, xs, gt, M, e2, acc);
+                        cb_grid_column<F, MT, true, false>(v, xs, gt, M, e2, acc, lane & 7);
                 } else if (compact) {
-                    cb_grid_column<F, MT, false, true>(v, xs, gt, M, e2, acc);
+                    cb_grid_column<F, MT, false, true>(v, xs, gt, M, e2, acc, lane & 7);
                 } else {
-                    cb_grid_column<F, MT, false, false>(v, xs, gt, M, e2, acc);
+                    cb_grid_column<F, MT, false, false>(v, xs, gt, M, e2, acc, lane & 7);
                 }
                 fence_proxy_async_smem();  // x was written: order it before the slot's next copy
             } else {
@@ -775,13 +796,13 @@ template <int F, int MT, int MINB>
 int launch_tma(const uint8_t* W, const void* book, const float* X, float* Y, int M, int64_t N, int64_t K,
                cudaStream_t s, unsigned* status, int dev, int sms) {
     static std::atomic<bool> attr_done[64];
-    const int budget = std::min(kSmemPerCTA, kSmemPerSM / MINB - kSmemReserve) - kCbRing0;
+    const int budget = std::min(kSmemPerCTA, kSmemPerSM / MINB - kSmemReserve) - cb_ring0(F);
     const int stages = std::min(kCbMaxStages, budget / cb_stage_bytes(F, MT));
     if (stages < 2) return QG_EINVAL;
     auto kern = qg_gemv_cb_tma_kernel<F, MT, MINB>;
     if (!attr_done[dev].load(std::memory_order_acquire)) {
         if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 std::min(kSmemPerCTA, kCbRing0 + kCbMaxStages * cb_stage_bytes(F, MT))) !=
+                                 std::min(kSmemPerCTA, cb_ring0(F) + kCbMaxStages * cb_stage_bytes(F, MT))) !=
             cudaSuccess)
             return qg::cuda_fail(cudaGetLastError());
         attr_done[dev].store(true, std::memory_order_release);
@@ -793,7 +814,7 @@ int launch_tma(const uint8_t* W, const void* book, const float* X, float* Y, int
     const int grid = static_cast<int>(std::min<int64_t>(ntiles, static_cast<int64_t>(sms) * MINB));
     const int64_t units_per_cta = (ntiles + grid - 1) / grid * ((K / 256 + kCbCols - 1) / kCbCols);
     const int st = static_cast<int>(std::min<int64_t>(stages, std::max<int64_t>(2, units_per_cta)));
-    kern<<<grid, kCbCols * 32 + 32, kCbRing0 + st * cb_stage_bytes(F, MT), s>>>(tm, book, X, Y, M, N, K, st, status);
+    kern<<<grid, kCbCols * 32 + 32, cb_ring0(F) + st * cb_stage_bytes(F, MT), s>>>(tm, book, X, Y, M, N, K, st, status);
     return launch_status();
 }
 
