@@ -387,12 +387,6 @@ __device__ __forceinline__ uint32_t sign_bytes(uint32_t nib) { return (nib * 0x1
 // [b0, 0, b1, 0] of the low two bytes of w
 __device__ __forceinline__ uint32_t spread2(uint32_t w) { return (w & 0xFFu) | ((w & 0xFF00u) << 8); }
 
-// Loads the codebook; returns true (the same in every thread of the CTA)
-// when every codebook byte is below 128.  Then the table keeps the
-// codebook's own rows (IQ3_S 512 x 4 bytes, IQ2_XXS 256 x 8 bytes, half
-// the bytes per gather) and the permute takes the zero bytes from the
-// sign-replicate of the grid byte itself (its top bit is 0); otherwise the
-// rows are expanded as above.
 // Nonzero in every participating thread when pred is nonzero in any of
 // the nt threads (a multiple of 32) that meet on named barrier id.
 __device__ __forceinline__ bool named_barrier_or(int id, int nt, bool pred) {
@@ -406,7 +400,13 @@ __device__ __forceinline__ bool named_barrier_or(int id, int nt, bool pred) {
     return r != 0u;
 }
 
-// Threads tid = 0..nt-1, all of which call it, meeting on named barrier
+// Loads the codebook; returns true (the same in every calling thread) when
+// every codebook byte is below 128.  Then the table keeps the codebook's
+// own rows (IQ3_S 512 x 4 bytes, IQ2_XXS 256 x 8 bytes, half the bytes per
+// gather) in kGridCopies lane copies, IQ2_XXS's sign table after them, and
+// the permute takes the zero bytes from the sign-replicate of the grid byte
+// itself (its top bit is 0); otherwise the rows are expanded as above, one
+// copy.  Threads tid = 0..nt-1, all of which call it, meet on named barrier
 // bar (nt a multiple of 32); the caller synchronises them again before the
 // table is read.
 template <int F>
