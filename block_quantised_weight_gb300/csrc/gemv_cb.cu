@@ -3,15 +3,21 @@
 // format table, get_s, eff_np and encode).  weight = eff * v, v = codebook
 // entry * sign; every value is exact in fp32.
 //
-// One lane per row (32 rows per CTA), the 8 warps of a CTA on eighths of K;
-// the codebook sits in shared
-// memory (IQ4: 16 fp32 values, which occupy 16 distinct banks, so any
-// gather is conflict-free; IQ3_S: 512 x 4 bytes; IQ2_XXS: 256 x 8 bytes);
-// x is read through the read-only cache (shared by all rows).  Block fields
-// are read with 16-bit loads (every field of these layouts starts at an even
-// byte), those of kDepth sub-blocks per lane before any is decoded, to keep
-// enough bytes in flight.  Per row, the lanes' partial sums meet in a warp
-// shuffle.
+// Two kernels, one lane per row (32-row tiles):
+//   * qg_gemv_cb_tma_kernel, every format whose rows are a multiple of 16
+//     bytes: a producer warp streams one tensor-map box per 256-weight
+//     column and the x slices into a ring; consumer warp w decodes column w
+//     of each 8-column unit, and the 8 warps' row sums meet in shared
+//     memory once per tile.  IQ4_NL / IQ4_XS look each code up in a 16-entry
+//     fp32 table (16 distinct banks: conflict-free); IQ3_S / IQ2_XXS join
+//     grid and sign bytes with one byte permute per weight, from compact
+//     grid tables in lane copies (or zero-interleaved rows when a codebook
+//     byte is 128 or more).  The consumers build the tables while the
+//     producer's first copies are in flight.
+//   * qg_gemv_cb_kernel, the other rows: the 8 warps of a CTA on eighths of
+//     K read the block fields directly with 16-bit loads (every field of
+//     these layouts starts at an even byte), those of kDepth sub-blocks per
+//     lane before any is decoded; x through the read-only cache.
 #include <type_traits>
 
 #include "launch_common.cuh"

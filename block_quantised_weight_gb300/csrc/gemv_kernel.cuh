@@ -8,8 +8,9 @@
 //   IQ3   page 4 "iq3_pack.py" (fmt=5), module docstring and decode, and
 //         page 3's IQ3_XXS byte order of the same fields
 //
-// CTA = RG row groups x 8 consumer warps + 1 producer warp; a tile is RG*32
-// consecutive rows, walked in units of 8 super-block columns.
+// CTA = RG row groups x 8 consumer warps + 1 producer warp (FmtQ4KT2: 16
+// consumer warps, two per column); a tile is RG*32 consecutive rows, walked
+// in units of 8 super-block columns.
 //   * The producer warp posts, per unit, one 2D tensor-map TMA
 //     (cp.async.bulk.tensor) per super-block column, a [tile rows][box] box
 //     of that column's blocks, plus the x slice of each token (Q4_K: one bulk
@@ -22,7 +23,8 @@
 //   * Consumer warp (rg, c) takes block column c.  Lane L decodes two rows,
 //     L&15 and (L&15)+16 of its row group, half L>>4 of each block (128
 //     weights), so every x load serves two rows; the halves of a row meet in
-//     one shuffle when the tile ends.  Box rows of 144 B (Q4_K) or 112 B
+//     one shuffle when the tile ends.  FmtQ4KT2 gives each half of a column
+//     its own warp (lane L: sub-block pair L>>4 of the warp's half).  Box rows of 144 B (Q4_K) or 112 B
 //     (IQ3) are odd multiples of 16 bytes, so eight lanes loading eight rows
 //     with 16-byte loads hit eight distinct bank groups.
 //   * Per-row partial sums stay in registers across a tile's units and are
@@ -35,11 +37,12 @@
 //   sum_l (a*q_l - b) * x_l = a * sum_l (q_l - c) * x_l - (b - a*c) * sum_l x_l
 // sum_l x_l is computed once per (column, token) by the warp, shared by its
 // 32 rows; q_l - c is formed exactly while each nibble is an fp32 subnormal
-// against x pre-scaled by powers of two.  IQ3: magnitudes gathered from a
-// lane-replicated fp16 grid table, signs from a sign-mask table, the
-// sub-block factor d*(0.5+code) applied per sub-block.  Slices of x outside
-// the directly handled range are rescaled by a power of two (see
-// q4k_stage_x and iq3_stage_x).
+// against x pre-scaled by powers of two.  IQ3: one byte permute per weight
+// joins a grid byte (from a lane-replicated table of zero-interleaved grid
+// rows) and a sign byte (from a table of the 128 sign fields) into the fp32
+// subnormal +-g * 2^-149; the sub-block factor d*(0.5+code) is applied per
+// sub-block.  Slices of x outside the directly handled range are rescaled
+// by a power of two (see q4k_stage_x and iq3_stage_x).
 #pragma once
 #include <cuda_fp16.h>
 
