@@ -36,8 +36,9 @@ def layouts(tmp_path_factory):
 def test_every_configuration_is_listed(layouts):
     got = {(c["fmt"], c["MT"], c["RG"], c["MINB"], c["fuse"]) for c in layouts}
     assert ("q4k", 1, 1, 2, 0) in got and ("q4k", 4, 1, 1, 2) in got
+    assert {("q4k2", 1, 1, 1, 1), ("q4k2", 1, 1, 1, 2)} <= got
     assert {("iq3", 1, 2, 1, 0), ("iq3", 2, 1, 1, 0), ("iq3", 4, 1, 1, 0)} <= got
-    assert len(got) == len(layouts) == 18
+    assert len(got) == len(layouts) == 20
 
 
 def test_ring_fits_with_at_least_two_stages(layouts):
@@ -65,6 +66,17 @@ def test_barriers_and_copy_destinations_aligned(layouts):
         # prologue operands: the RMSNorm weight once, the SwiGLU up operand per token
         extra = {0: 0, 1: c["cols"] * 1024, 2: c["MT"] * c["cols"] * 1024}[c["fuse"]]
         assert c["stage_bytes"] - c["aoff"] == extra, c
+
+
+def test_per_warp_arrays_hold_every_consumer_warp(layouts):
+    """Each consumer warp owns MT x 8 sub-block sums of x, two tile
+    parities of MT x 32 row sums and two of MT sums of x^2: with two warps
+    per column (q4k2) there are 16 warps, not 8."""
+    for c in layouts:
+        w, mt = c["warps"], c["MT"]
+        assert c["red"] - c["sx"] >= w * mt * 8 * 4, c
+        assert c["cred"] - c["red"] >= 2 * w * mt * 32 * 4, c
+        assert c["table"] - c["ss"] >= 2 * w * mt * 4, c
 
 
 def test_tables_sit_between_reductions_and_ring(layouts):
