@@ -178,7 +178,7 @@ def cudart():
 _COMMON = ["common.cuh", "gemv_kernel.cuh", "launch.h", "tensor_map.h", "launch_common.cuh",
            "../../include/qgemv.h"]
 KERNEL_SOURCES = {
-    "q4k": _COMMON + ["launch_q4k.cuh", "gemv_q4k.cu"],
+    "q4k": _COMMON + ["launch_q4k.cuh", "gemv_q4k8.cuh", "gemv_q4k.cu"],
     "iq3": _COMMON + ["launch_iq3.cuh", "gemv_iq3.cu"],
     "tc": ["common.cuh", "gemv_kernel.cuh", "launch.h", "tensor_map.h", "../../include/qgemv.h", "gemm_tc.cu"],
     "cb": _COMMON + ["gemv_cb.cu"],

@@ -1,15 +1,16 @@
 // Q4_K GEMV dispatch (fp32 FMA path), shared by the plain and the fused
 // translation units.  Kernel: gemv_kernel.cuh.
 #pragma once
+#include "gemv_q4k8.cuh"
 #include "launch_common.cuh"
 
 namespace qg {
 
-// count matrices sharing X; M is split into groups of at most 4 tokens, each
-// group streaming W once (an 8-token group needs more registers than the
-// two-row decode can keep: two 4-token passes over W are several times
-// faster than one 8-token pass).  FUSE != 0 (a prologue on x) needs M <= 4: the
-// staged-x kernels apply it.  fz may carry residuals with any FUSE.
+// count matrices sharing X; M is split into token groups, each streaming W
+// once: groups of 5 to 8 tokens run the 8-warp kernel of gemv_q4k8.cuh
+// (no prologue, no residual), the rest groups of at most 4.  FUSE != 0 (a
+// prologue on x) needs M <= 4: the staged-x kernels apply it.  fz may carry
+// residuals with any FUSE.
 template <int FUSE>
 int launch_group_q4k_t(const uint8_t* const* W, float* const* Y, const int64_t* N, int count, const float* X, int M,
                        int64_t K, cudaStream_t s, unsigned* status, unsigned flags, const Fuse* fz) {
@@ -28,9 +29,19 @@ int launch_group_q4k_t(const uint8_t* const* W, float* const* Y, const int64_t* 
     // chunk gets its own CTA, the chunks of a tile forming one cluster.
     const int64_t nchunks = (K / 256 + kCols - 1) / kCols;
     const int csize = (nchunks > 1 && nchunks <= kMaxCluster && tiles * nchunks <= 2 * sms) ? static_cast<int>(nchunks) : 1;
-    for (int m0 = 0; m0 < M; m0 += 4) {
-        const int mg = std::min(4, M - m0);
+    bool residual = false;
+    if (fz)
+        for (int i = 0; i < count; ++i) residual = residual || fz->R[i] != nullptr;
+    for (int m0 = 0; m0 < M;) {
         const float* Xg = X + static_cast<int64_t>(m0) * K;
+        if (FUSE == 0 && !residual && M - m0 >= 5) {  // 5 to 8 tokens in one pass
+            const int mg = std::min(8, M - m0);
+            const int rc = launch_gemv8(W, Y, N, count, m0, Xg, mg, K, s, status, dev, flags);
+            if (rc != QG_OK) return rc;
+            m0 += mg;
+            continue;
+        }
+        const int mg = std::min(4, M - m0);
         int rc;
         if (mg == 1 && csize > 1)
             rc = launch_gemv<FmtQ4KT, 1, 1, 2, FUSE>(W, Y, N, count, m0, nullptr, Xg, mg, K, s, status, dev,
@@ -51,6 +62,7 @@ int launch_group_q4k_t(const uint8_t* const* W, float* const* Y, const int64_t* 
             rc = launch_gemv<FmtQ4KT, 4, 1, 1, FUSE>(W, Y, N, count, m0, nullptr, Xg, mg, K, s, status, dev,
                                                            flags, 1, fz);
         if (rc != QG_OK) return rc;
+        m0 += mg;
     }
     return QG_OK;
 }
