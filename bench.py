@@ -617,6 +617,23 @@ def run_ours(args, rank, world, local_rank):
             "peak_kind": f"of {peak_kind}", "kernel": kname, "launches_timed": n_launch,
             "avg_launch_us": round(1e3 * avg_launch_ms, 3), "algorithmic_bytes_per_launch": round(algo / len(flat)),
             "durations": "CUDA events on the launch stream around the timed region / launches in it"}
+    # 2 <= M <= 15 on the fp32 FMA path: the arithmetic (2*M flops per weight)
+    # can take longer than the weight stream, so the roofline is the lower of
+    # the two ceilings; the fp32 peak is the SMs' FMA lanes (128 per SM, 2
+    # flops each) at the largest SM clock sampled during the run
+    fma_path = fused or mats[0][0] not in ("q4k", "iq3") or M < 16
+    if fma_path and 2 <= M <= 15:
+        sms = torch.cuda.get_device_properties(dev).multi_processor_count
+        mhz = (clocks or {}).get("sm_max_mhz") or 2070.0
+        fp32_peak = sms * 128 * 2 * mhz * 1e6 / 1e12  # TFLOP/s
+        flops = 2.0 * M * sum(K * N for _f, K, N in mats)  # per step
+        tflops = flops / (ms_step * 1e-3) / 1e12
+        if flops / (fp32_peak * 1e12) > step_wbytes / (peak * 1e9):  # the arithmetic takes longer
+            hbm_view = {k: roof[k] for k in ("achieved", "peak", "unit", "frac", "peak_kind")}
+            roof.update({"bound": "alu", "achieved": round(tflops, 2), "peak": round(fp32_peak, 1), "unit": "TFLOP/s",
+                         "frac": round(tflops / fp32_peak, 4),
+                         "peak_kind": f"of nominal ({sms} SMs x 128 fp32 FMA lanes x 2 flop at {mhz:.0f} MHz)",
+                         "hbm_view": hbm_view})
     if durs:
         kern_ms = sum(durs)
         by_shape = {}
