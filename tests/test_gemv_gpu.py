@@ -81,7 +81,7 @@ Q4K_SHAPES = [(1, 256), (31, 256), (33, 512), (100, 2304), (64, 2048), (257, 409
 
 
 @pytest.mark.parametrize("N,K", Q4K_SHAPES)
-@pytest.mark.parametrize("M", [1, 2, 3, 4, 8])
+@pytest.mark.parametrize("M", [1, 2, 3, 4, 5, 7, 8])   # 5-8: one pass of the 8-token kernel
 def test_gemv_q4k_small(q, N, K, M):
     W = synth.gen_q4k(N, K, 7 * N + K)
     x = synth.gen_x(M, K, 3 + M)
@@ -253,8 +253,8 @@ def test_binding_raises_on_bad_arguments(q):
 
 
 # ------------------------------------------------------------ dependent launch
-@pytest.mark.parametrize("fmt", ["q4k", "iq3"])
-def test_prefetch_flag_dependency_chain(q, fmt):
+@pytest.mark.parametrize("fmt,M", [("q4k", 1), ("iq3", 1), ("q4k", 8)])   # q4k 8: the one-pass 8-token kernel
+def test_prefetch_flag_dependency_chain(q, fmt, M):
     """x_{i+1} = y_i through six square GEMVs issued back to back on one stream.
     With QG_PREFETCH_WEIGHTS each launch may start before its predecessor ends;
     the results must equal the plain stream-ordered launches bit for bit and
@@ -267,7 +267,7 @@ def test_prefetch_flag_dependency_chain(q, fmt):
         else:
             W, grid = synth.gen_iq3(N, K, 400 + i)
             mats.append((dev(W), dev(grid)))
-    x0 = dev(synth.gen_x(1, K, 7))
+    x0 = dev(synth.gen_x(M, K, 7))
 
     def chain(flags):
         xs = [x0]
@@ -286,7 +286,7 @@ def test_prefetch_flag_dependency_chain(q, fmt):
         assert torch.equal(a, b)
     # each stage on the oracle's own chain of inputs (fp32 of the oracle's
     # previous output / 32), with and without the flag
-    xin = x0.cpu().numpy().reshape(1, K)
+    xin = x0.cpu().numpy().reshape(M, K)
     for i, (W, g) in enumerate(mats):
         Wh = W.cpu().numpy()
         if fmt == "q4k":
