@@ -323,17 +323,27 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint64_t pol_x = policy_evict_last();
             constexpr int kBoxBytes = IQ3 ? kIQ3Box : kBlockBytes;
             const uint32_t bytes = kTileRows * kBoxBytes + M * 1024;
+            // (stage, phase, tile, k-block) kept incrementally: a 64-bit
+            // division per unit costs a good fraction of a unit's time
+            int s = 0;
+            uint32_t round = 0;  // completed passes over the raw ring
+            int64_t tile = u_begin / nb;
+            int kb = static_cast<int>(u_begin % nb);
             for (int64_t u = u_begin; u < u_end; ++u) {
-                const int64_t i = u - u_begin;
-                const int s = static_cast<int>(i % nraw);
-                if (i >= nraw) mbar_wait_bounded(&raw_empty[s], static_cast<uint32_t>((i / nraw - 1) & 1), status);
-                const int64_t tile = u / nb;
-                const int kb = static_cast<int>(u % nb);
+                if (u - u_begin >= nraw) mbar_wait_bounded(&raw_empty[s], (round - 1) & 1u, status);
                 uint8_t* raw = smem + raw0 + s * rstage;
                 mbar_arrive_expect_tx(&raw_full[s], bytes);
                 const int bx = IQ3 ? (kb * 98) & ~15 : kb * kBlockBytes;  // x * 1 byte: 16-byte aligned
                 tma_load_2d(raw, &tmW, bx, static_cast<int>(tile * kTileRows), &raw_full[s], pol_w);
                 tma_load_2d(raw + kRawW, &tmX, kb * 256, 0, &raw_full[s], pol_x);
+                if (++s == nraw) {
+                    s = 0;
+                    ++round;
+                }
+                if (++kb == nb) {
+                    kb = 0;
+                    ++tile;
+                }
             }
         }
         __syncwarp();
@@ -341,9 +351,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ---------------- MMA issuer
         const uint32_t idesc = instr_desc(kTileRows, nmma);
         int64_t seg = 0;
-        for (int64_t u = u_begin; u < u_end; ++u) {
+        int kb = static_cast<int>(u_begin % nb);  // advanced at the end of each unit (no division per unit)
+        for (int64_t u = u_begin; u < u_end; ++u, kb = kb + 1 == nb ? 0 : kb + 1) {
             const int64_t i = u - u_begin;
-            const int kb = static_cast<int>(u % nb);
             const bool first = (u == u_begin) || kb == 0;
             const bool last = (u == u_end - 1) || kb == nb - 1;
             for (int half = 0; half < 2; ++half) {
@@ -378,17 +388,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint8_t* opA = smem + kOp0 + half * kOpStage;
         uint8_t* opB = opA + kOpA;
         int64_t seg = 0;
+        // (raw stage, its phase, tile, k-block) kept incrementally
+        int s = 0;
+        uint32_t rphase = 0;
+        int64_t tile = u_begin / nb;
+        int kb = static_cast<int>(u_begin % nb);
         for (int64_t u = u_begin; u < u_end; ++u) {
             const int64_t i = u - u_begin;
-            const int s = static_cast<int>(i % nraw);
-            const int64_t tile = u / nb;
-            const int kb = static_cast<int>(u % nb);
             const bool last = (u == u_end - 1) || kb == nb - 1;
             const int64_t row0 = tile * kTileRows;
             const int rows = static_cast<int>(min64(kTileRows, N - row0));
             const uint8_t* raw = smem + raw0 + s * rstage;
             const float* xr = reinterpret_cast<const float*>(raw + kRawW);
-            mbar_wait_bounded(&raw_full[s], static_cast<uint32_t>((i / nraw) & 1), status);
+            mbar_wait_bounded(&raw_full[s], rphase, status);
             if (i >= 1) mbar_wait_bounded(&op_empty[half], static_cast<uint32_t>((i - 1) & 1), status);
             if constexpr (IQ3)  // rows past N: TMA zero fill, unused
                 switch (kb & 7) {  // the block's offset in its box: (98 * kb) mod 16
@@ -439,6 +451,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (lane == 0) arrive(acc_empty);
             }
             if (last) ++seg;
+            if (++s == nraw) {
+                s = 0;
+                rphase ^= 1u;
+            }
+            if (++kb == nb) {
+                kb = 0;
+                ++tile;
+            }
         }
     }
     __syncthreads();
