@@ -12,22 +12,30 @@
 // on the MMA's M=128 side, tokens on its N=16/32 side).
 //
 // CTA roles (320 threads):
-//   warps 0-7  dequantise W and X into the operand stages: warps 0-3 the
-//              first 128 k of each unit, warps 4-7 the second (thread =
-//              tile row); warps 0-3 then drain the accumulator (tcgen05.ld,
-//              warp w reads TMEM lanes 32w..32w+31) into Y;
+//   warps 0-7  dequantise W into tensor memory and X into shared memory:
+//              warps 0-3 the first 128 k of each unit, warps 4-7 the second
+//              (thread = tile row = TMEM lane); warps 0-3 then drain the
+//              accumulator (tcgen05.ld, warp w reads TMEM lanes 32w..32w+31)
+//              into Y;
 //   warp 8     producer: one 2D tensor-map TMA per unit for the 128 rows x
 //              block column of W (Q4_K: 144 bytes; IQ3: the 112 bytes from
 //              the block's offset rounded down to 16, the block starting
-//              0..14 bytes in) and one for the x slice (fp32), into a
-//              double-buffered raw stage;
+//              0..14 bytes in) and one for the x slice (fp32), into a ring of
+//              raw stages;
 //   warp 9     allocates tensor memory; lane 0 issues the MMAs and commits
 //              them to mbarriers.
 // Work: units (tile, k-block) in row-major order, split evenly over the grid
 // (stream-K); a CTA's run over one tile is a "segment" whose partial sums are
 // added into Y (zeroed first) with fp32 atomics.  Each unit is dequantised
-// in two halves of 128 k into two operand stages, in parallel, and the MMAs
-// of one unit overlap the dequantisation of the next raw stage.
+// in two halves of 128 k, in parallel.  The MMA takes its W operand (A, 128
+// rows x 16 k per instruction) from tensor memory, written with tcgen05.st,
+// and x (B) from shared memory.  Both are double-buffered per half, and so
+// is the accumulator, so the dequantisation of one unit overlaps the MMAs
+// of the one before, and a segment's drain the next segment's MMAs.
+//
+// Tensor memory (512 columns): A of half h, buffer b at columns 64 (2h + b)
+// (row = lane, k pairs as bf16x2 per column, k ascending); the accumulators
+// at 256 and 288 (D[row][token], fp32, 32 columns each).
 //
 // Exact weights: with the fp16 magic h = 1024 + q, one fp16 FMA gives
 // h*sc - 1024*sc = q*sc exactly (at most 945: the fused product is rounded
@@ -37,10 +45,10 @@
 // *0.25) is exact in fp32 (the grid's 0.5 folded into the sub-block factor),
 // so bf16 rounds the pages' exact value once.
 //
-// Operand layout (no swizzle, K-major): 8-row x 16-byte core matrices; in a
-// half stage core (row group i, k chunk j) sits at ((i * 16) + j) * 128
-// bytes, row r of the core at +16 r: adjacent k chunks 128 bytes apart,
-// adjacent row groups 2048 bytes apart.
+// x operand layout (K-major, 128-byte swizzle): for half h, buffer b, two
+// 4 KB atoms (k 0-63 and 64-127 of the half) of 32 token rows x 128 bytes;
+// the 16-byte chunk j of row r sits at position j ^ (r mod 8), so eight
+// rows' chunks j fall in eight distinct bank groups.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cudaTypedefs.h>
@@ -61,34 +69,36 @@ constexpr int kThreads = 320;  // 8 dequant warps, producer, MMA
 constexpr int kRawW = kTileRows * kBlockBytes;     // 18432: TMA box 144 x 128 (IQ3: 112 x 128)
 constexpr int kIQ3Box = 112;
 constexpr int kMaxRaw = 6;                          // raw stages (W box + the unit's x, M KB)
-constexpr int kOpA = kTileRows * 128 * 2;           // 32768: 128 rows x 128 k bf16
-constexpr int kOpB = 32 * 128 * 2;                  // 8192: 32 tokens x 128 k bf16
-constexpr int kOpStage = kOpA + kOpB;               // 40960
-// Shared memory: barriers, then the two operand stages, the IQ3 tables, and
-// the raw ring at the end: as many stages of kRawW + M * 1024 bytes as fit.
-constexpr int kOp0 = 1024;
+// Shared memory: barriers, the four x stages, the IQ3 tables, and the raw
+// ring at the end: as many stages of kRawW + M * 1024 bytes as fit.
+constexpr int kB0 = 1024;
+constexpr int kBStage = 2 * 32 * 128;               // 8192: two 64-k atoms of 32 token rows
 // IQ3: the grid as fp32, 8 copies: row i of copy c at (8i + c) * 16 bytes,
 // lane L reading copy L & 7, so the 8 lanes of a quarter warp gather from 8
 // distinct bank groups whatever their rows (32 KB).
-constexpr int kGrid0 = kOp0 + 2 * kOpStage;
+constexpr int kGrid0 = kB0 + 4 * kBStage;           // 33792
 constexpr int kSign0 = kGrid0 + 32768;              // IQ3: sign-mask words, 8 copies (entry s7 of copy c at 8*s7 + c: 4 KB)
-constexpr int kRaw0Q4K = kGrid0;                    // 82944
-constexpr int kRaw0IQ3 = kSign0 + 4096;              // 119808
+constexpr int kRaw0Q4K = kGrid0;                    // 33792
+constexpr int kRaw0IQ3 = kSign0 + 4096;             // 70656
 constexpr int kSmemMax = 232448;                     // 227 KB per CTA
 __host__ __device__ constexpr int raw_stage_bytes(int M) { return kRawW + M * 1024; }
-constexpr int kTmemCols = 32;
-constexpr uint32_t kSBO = 16 * 128;                 // row-group stride in an operand stage
-constexpr uint32_t kLBO = 128;                      // k-chunk stride
+constexpr int kTmemCols = 512;
+constexpr uint32_t kTmA = 0;                        // A of half h, buffer b at kTmA + 64 (2h + b)
+constexpr uint32_t kTmD = 256;                      // accumulator p at kTmD + 32 p
+constexpr uint32_t kSBO = 8 * 128;                  // 8-row group stride in an x atom
 
-// smem descriptor for tcgen05.mma: start address, leading (k) and stride
-// (row group) byte offsets, descriptor version 1, no swizzle.
-__device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+// smem descriptor for tcgen05.mma, K-major with the 128-byte swizzle: start
+// address, leading byte offset (unused by this layout: 16), stride byte
+// offset between 8-row groups, descriptor version 1, base offset 0 (every
+// atom starts on a 1024-byte boundary), swizzle mode 2 (128 bytes).
+__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t sbo) {
     uint64_t d = 0;
     d |= static_cast<uint64_t>((saddr >> 4) & 0x3FFFu);
-    d |= static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16;
+    d |= static_cast<uint64_t>(1) << 16;
     d |= static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32;
     d |= static_cast<uint64_t>(1) << 46;  // version
-    return d;  // base offset 0, layout type 0 (no swizzle)
+    d |= static_cast<uint64_t>(2) << 61;  // 128-byte swizzle
+    return d;
 }
 
 // instruction descriptor, kind::f16: D fp32, A and B bf16, both K-major.
@@ -97,12 +107,13 @@ __host__ __device__ constexpr uint32_t instr_desc(int m, int n) {
            (static_cast<uint32_t>(m >> 4) << 24);
 }
 
-__device__ __forceinline__ void mma_bf16(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
-                                         uint32_t accumulate) {
+// D (+)= A B^T with A (128 rows x 16 k, bf16) in tensor memory at tmem_a.
+__device__ __forceinline__ void mma_bf16_ta(uint32_t tmem_d, uint32_t tmem_a, uint64_t bdesc, uint32_t idesc,
+                                            uint32_t accumulate) {
     asm volatile(
         "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
-        ::"r"(tmem_d), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate) : "memory");
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}"
+        ::"r"(tmem_d), "r"(tmem_a), "l"(bdesc), "r"(idesc), "r"(accumulate) : "memory");
 }
 
 __device__ __forceinline__ void mma_commit(uint64_t* bar) {
@@ -139,9 +150,24 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
     for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
 
-// Offset of the 16-byte chunk (row, k chunk j < 16) in a half operand stage.
-__device__ __forceinline__ uint32_t op_off(int row, int j) {
-    return static_cast<uint32_t>((((row >> 3) * 16) + j) * 128 + (row & 7) * 16);
+// 32 32-bit columns of this warp's 32 TMEM lanes (lane = thread), from registers.
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&w)[32]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+        "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+        "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};"
+        ::"r"(taddr), "r"(w[0]), "r"(w[1]), "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7]),
+          "r"(w[8]), "r"(w[9]), "r"(w[10]), "r"(w[11]), "r"(w[12]), "r"(w[13]), "r"(w[14]), "r"(w[15]),
+          "r"(w[16]), "r"(w[17]), "r"(w[18]), "r"(w[19]), "r"(w[20]), "r"(w[21]), "r"(w[22]), "r"(w[23]),
+          "r"(w[24]), "r"(w[25]), "r"(w[26]), "r"(w[27]), "r"(w[28]), "r"(w[29]), "r"(w[30]), "r"(w[31])
+        : "memory");
+}
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+// Offset of the 16-byte chunk (token row m, k chunk j < 16 of the half) in an
+// x stage: atom j / 8, row m at 128 m, chunk position (j mod 8) ^ (m mod 8).
+__device__ __forceinline__ uint32_t x_off(int m, int j) {
+    return static_cast<uint32_t>((j >> 3) * 4096 + m * 128 + (((j & 7) ^ (m & 7)) << 4));
 }
 
 __device__ __forceinline__ uint32_t hfma2_u32(uint32_t a, uint32_t b, uint32_t c) {
@@ -169,9 +195,9 @@ __device__ __forceinline__ uint32_t half2_bits(float a) {
     return *reinterpret_cast<const uint32_t*>(&h);
 }
 
-// Thread t: half `half` (k 128*half .. +127) of the W tile row t -> 16 chunks
-// of 8 bf16 in the operand stage.
-__device__ __forceinline__ void dequant_half(const uint8_t* blk, uint8_t* opA, int t, int half) {
+// Thread t: half `half` (k 128*half .. +127) of the W tile row t -> 64 bf16
+// pairs in this thread's TMEM lane, columns ta .. ta + 63 (column c: k 2c, 2c+1).
+__device__ __forceinline__ void dequant_half(const uint8_t* blk, uint32_t ta, int half) {
     const uint4 h = *reinterpret_cast<const uint4*>(blk);
     const uint32_t dbits = h.x & 0xFFFFu;
     const float dmin = h2f(h.x >> 16);
@@ -181,6 +207,7 @@ __device__ __forceinline__ void dequant_half(const uint8_t* blk, uint8_t* opA, i
 #pragma unroll
     for (int gg = 0; gg < 2; ++gg) {
         const int g = 2 * half + gg;
+        uint32_t w[32];  // k 64gg .. 64gg + 63 of the half: 8 chunks of 4 columns
         const float sl = byte_f(scw, 2 * gg), sh = byte_f(scw, 2 * gg + 1);
         const float ml = -(dmin * byte_f(mnw, 2 * gg)), mh = -(dmin * byte_f(mnw, 2 * gg + 1));
         // (1024+q)*sl - 1024*sl = q*sl; (1024+16q)*(sh/16) - 64*sh = q*sh (all exact in fp16)
@@ -203,13 +230,17 @@ __device__ __forceinline__ void dequant_half(const uint8_t* blk, uint8_t* opA, i
                 hi[2 * e] = pack_bf16(mfma_lo(dbits, B, mh), mfma_lo(dbits, D, mh));
                 hi[2 * e + 1] = pack_bf16(mfma_hi(dbits, B, mh), mfma_hi(dbits, D, mh));
             }
-            // low nibbles: k' = 64gg + 16hh + 0..15; high: k' + 32 (k' within the half)
-            const int jl = 8 * gg + 2 * hh, jh = 8 * gg + 4 + 2 * hh;
-            *reinterpret_cast<uint4*>(opA + op_off(t, jl)) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
-            *reinterpret_cast<uint4*>(opA + op_off(t, jl + 1)) = make_uint4(lo[4], lo[5], lo[6], lo[7]);
-            *reinterpret_cast<uint4*>(opA + op_off(t, jh)) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-            *reinterpret_cast<uint4*>(opA + op_off(t, jh + 1)) = make_uint4(hi[4], hi[5], hi[6], hi[7]);
+            // low nibbles: k' = 16hh + 0..15 (chunks 2hh, 2hh+1 of the 64); high: k' + 32
+            const int jl = 2 * hh, jh = 4 + 2 * hh;
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                w[4 * jl + e] = lo[e];
+                w[4 * jl + 4 + e] = lo[4 + e];
+                w[4 * jh + e] = hi[e];
+                w[4 * jh + 4 + e] = hi[4 + e];
+            }
         }
+        tmem_st32(ta + 32 * gg, w);
     }
 }
 
@@ -223,10 +254,11 @@ __device__ __forceinline__ void dequant_half(const uint8_t* blk, uint8_t* opA, i
 // 0x80008000 flips pair p.
 template <int COL>
 __device__ __forceinline__ void dequant_half_iq3(const uint8_t* boxrow, const float4* grid4, const uint32_t* sgn,
-                                                 uint8_t* opA, int t, int half) {
+                                                 uint32_t ta, int t, int half) {
     uint32_t vi[8], vs[4], dbits;
     iq3_load_half<FmtIQ3T, COL>(boxrow, half, vi, vs, dbits);
     const float d = h2f(dbits);
+    uint32_t w[32];  // two sub-blocks: 8 chunks of 4 columns
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
         const uint32_t sw = vs[j];
@@ -245,10 +277,11 @@ __device__ __forceinline__ void dequant_half_iq3(const uint8_t* boxrow, const fl
                 packed[2 * hf] = pack_bf16(g.x * dbh, g.y * dbh) ^ ((T << (2 * hf)) & 0x80008000u);
                 packed[2 * hf + 1] = pack_bf16(g.z * dbh, g.w * dbh) ^ ((T << (2 * hf + 1)) & 0x80008000u);
             }
-            // weights 32j + 8l .. +7 of the half: chunk 4j + l
-            *reinterpret_cast<uint4*>(opA + op_off(t, 4 * j + l)) =
-                make_uint4(packed[0], packed[1], packed[2], packed[3]);
+            // weights 32j + 8l .. +7 of the half: columns 16j + 4l .. +3
+#pragma unroll
+            for (int e = 0; e < 4; ++e) w[16 * (j & 1) + 4 * l + e] = packed[e];
         }
+        if (j & 1) tmem_st32(ta + 32 * (j >> 1), w);
     }
 }
 
@@ -260,10 +293,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     extern __shared__ __align__(1024) uint8_t smem[];
     uint64_t* raw_full = reinterpret_cast<uint64_t*>(smem);  // [kMaxRaw]
     uint64_t* raw_empty = raw_full + kMaxRaw;                 // [kMaxRaw]
-    uint64_t* op_full = raw_full + 2 * kMaxRaw;               // [2]
-    uint64_t* op_empty = op_full + 2;                         // [2]
-    uint64_t* acc_full = op_full + 4;
-    uint64_t* acc_empty = op_full + 5;
+    uint64_t* op_full = raw_full + 2 * kMaxRaw;               // [half][buffer]
+    uint64_t* op_empty = op_full + 4;                         // [half][buffer]
+    uint64_t* acc_full = op_full + 8;                         // [2]
+    uint64_t* acc_empty = op_full + 10;                       // [2]
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + 512);
     const int raw0 = IQ3 ? kRaw0IQ3 : kRaw0Q4K;
     const int rstage = raw_stage_bytes(M);
@@ -275,20 +308,32 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int64_t u_begin = U * blockIdx.x / gridDim.x;
     const int64_t u_end = U * (blockIdx.x + 1) / gridDim.x;
     const int nmma = M <= 16 ? 16 : 32;
+    // the swizzled x stages need a 1024-byte aligned base (all threads see the
+    // same address: the CTA leaves before any barrier or TMEM use)
+    if ((smem_u32(smem) & 1023u) != 0) {
+        if (threadIdx.x == 0) atomicOr(status, kStatusBounds);
+        return;
+    }
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < nraw; ++i) {
             mbar_init(&raw_full[i], 1);
             mbar_init(&raw_empty[i], 8);
         }
-        for (int i = 0; i < 2; ++i) {
+        for (int i = 0; i < 4; ++i) {
             mbar_init(&op_full[i], 4);
             mbar_init(&op_empty[i], 1);
         }
-        mbar_init(acc_full, 1);
-        mbar_init(acc_empty, 4);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&acc_full[i], 1);
+            mbar_init(&acc_empty[i], 4);
+        }
         fence_mbar_init();
     }
+    // x stages: token rows past M stay zero (the MMA reads 16 or 32 rows)
+    for (int i = threadIdx.x; i < 4 * kBStage / 16; i += kThreads)
+        reinterpret_cast<uint4*>(smem + kB0)[i] = make_uint4(0u, 0u, 0u, 0u);
+    fence_proxy_async_smem();
     if constexpr (IQ3) {
         // the grid bytes (doubled units) as fp32, one float4 per row
         float* g = reinterpret_cast<float*>(smem + kGrid0);
@@ -354,39 +399,45 @@ __global__ void __launch_bounds__(kThreads, 1)
         int kb = static_cast<int>(u_begin % nb);  // advanced at the end of each unit (no division per unit)
         for (int64_t u = u_begin; u < u_end; ++u, kb = kb + 1 == nb ? 0 : kb + 1) {
             const int64_t i = u - u_begin;
+            const int b = static_cast<int>(i & 1);
             const bool first = (u == u_begin) || kb == 0;
             const bool last = (u == u_end - 1) || kb == nb - 1;
-            for (int half = 0; half < 2; ++half) {
-                const int o = half;  // operand stage o holds half o of every unit
-                mbar_wait_bounded(&op_full[o], static_cast<uint32_t>(i & 1), status);
-                if (first && half == 0 && seg > 0)
-                    mbar_wait_bounded(acc_empty, static_cast<uint32_t>((seg - 1) & 1), status);
-                tc_fence_after();
-                if (lane == 0) {
-                    const uint32_t a0 = smem_u32(smem + kOp0 + o * kOpStage);
-                    const uint32_t b0 = a0 + kOpA;
+            const uint32_t td = tmem + kTmD + 32u * static_cast<uint32_t>(seg & 1);
+            // both halves, then the unit's 16 MMAs in one straight run (a
+            // branch between two MMAs doubles their issue cost)
+            mbar_wait_bounded(&op_full[b], static_cast<uint32_t>((i >> 1) & 1), status);
+            mbar_wait_bounded(&op_full[2 + b], static_cast<uint32_t>((i >> 1) & 1), status);
+            if (first && seg >= 2)  // segment seg - 2 drained from this accumulator
+                mbar_wait_bounded(&acc_empty[seg & 1], static_cast<uint32_t>(((seg >> 1) - 1) & 1), status);
+            tc_fence_after();
+            if (lane == 0) {
+                const uint32_t acc0 = first ? 0u : 1u;
 #pragma unroll
-                    for (int ks = 0; ks < 8; ++ks) {
-                        const uint64_t ad = smem_desc(a0 + 256 * ks, kLBO, kSBO);
-                        const uint64_t bd = smem_desc(b0 + 256 * ks, kLBO, kSBO);
-                        mma_bf16(tmem, ad, bd, idesc, (first && half == 0 && ks == 0) ? 0u : 1u);
+                for (int h = 0; h < 2; ++h) {
+                    const uint32_t ta = tmem + kTmA + 64u * static_cast<uint32_t>(2 * h + b);
+                    const uint32_t b0 = smem_u32(smem + kB0 + (2 * h + b) * kBStage);
+#pragma unroll
+                    for (int ks = 0; ks < 8; ++ks) {  // k 16 ks .. +15 of the half
+                        const uint64_t bd = smem_desc_sw128(b0 + 4096 * (ks >> 2) + 32 * (ks & 3), kSBO);
+                        mma_bf16_ta(td, ta + 8 * ks, bd, idesc, (h == 0 && ks == 0) ? acc0 : 1u);
                     }
-                    mma_commit(&op_empty[o]);
-                    if (last && half == 1) mma_commit(acc_full);
                 }
-                __syncwarp();
+                mma_commit(&op_empty[b]);
+                mma_commit(&op_empty[2 + b]);
+                if (last) mma_commit(&acc_full[seg & 1]);
             }
+            __syncwarp();
             if (last) ++seg;
         }
-        // the last segment's accumulator must be drained before TMEM is freed
-        if (seg > 0) mbar_wait_bounded(acc_empty, static_cast<uint32_t>((seg - 1) & 1), status);
+        // the last segments' accumulators must be drained before TMEM is freed
+        for (int64_t q = seg >= 2 ? seg - 2 : 0; q < seg; ++q)
+            mbar_wait_bounded(&acc_empty[q & 1], static_cast<uint32_t>((q >> 1) & 1), status);
     } else {
         // ---------------- dequant (warps 0-7) + epilogue (warps 0-3)
         const int half = warp >> 2;         // which 128 k of the unit
-        const int t = threadIdx.x & 127;    // tile row
-        const int hw = warp & 3;            // warp within the half
-        uint8_t* opA = smem + kOp0 + half * kOpStage;
-        uint8_t* opB = opA + kOpA;
+        const int t = threadIdx.x & 127;    // tile row = TMEM lane
+        const int hw = warp & 3;            // TMEM lanes 32 hw .. 32 hw + 31
+        const uint32_t tl = static_cast<uint32_t>(32 * hw) << 16;
         int64_t seg = 0;
         // (raw stage, its phase, tile, k-block) kept incrementally
         int s = 0;
@@ -400,55 +451,60 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int rows = static_cast<int>(min64(kTileRows, N - row0));
             const uint8_t* raw = smem + raw0 + s * rstage;
             const float* xr = reinterpret_cast<const float*>(raw + kRawW);
+            const int b = static_cast<int>(i & 1);
             mbar_wait_bounded(&raw_full[s], rphase, status);
-            if (i >= 1) mbar_wait_bounded(&op_empty[half], static_cast<uint32_t>((i - 1) & 1), status);
+            // buffer b of this half was last read by the MMAs of unit i - 2
+            if (i >= 2) mbar_wait_bounded(&op_empty[2 * half + b], static_cast<uint32_t>(((i >> 1) - 1) & 1), status);
+            tc_fence_after();
+            const uint32_t ta = tmem + tl + kTmA + 64u * static_cast<uint32_t>(2 * half + b);
             if constexpr (IQ3)  // rows past N: TMA zero fill, unused
                 switch (kb & 7) {  // the block's offset in its box: (98 * kb) mod 16
 #define QG_TC_IQ3(C)                                                                                          \
     case C:                                                                                                  \
         dequant_half_iq3<C>(raw + t * kIQ3Box, reinterpret_cast<const float4*>(smem + kGrid0),             \
-                            reinterpret_cast<const uint32_t*>(smem + kSign0), opA, t, half);                 \
+                            reinterpret_cast<const uint32_t*>(smem + kSign0), ta, t, half);                  \
         break;
                     QG_TC_IQ3(0) QG_TC_IQ3(1) QG_TC_IQ3(2) QG_TC_IQ3(3)
                     QG_TC_IQ3(4) QG_TC_IQ3(5) QG_TC_IQ3(6) QG_TC_IQ3(7)
 #undef QG_TC_IQ3
                 }
             else
-                dequant_half(raw + t * kBlockBytes, opA, t, half);
-            // x -> bf16 chunks (token m, k chunk j): the 8 lanes of a quarter
-            // warp take 8 consecutive tokens, whose chunks sit in distinct bank
-            // groups of the operand stage, and chunks j, j+1, ... whose fp32
-            // sources pair up on the row's bank groups: conflict-free stores,
-            // two-way loads (the least for 256 bytes)
+                dequant_half(raw + t * kBlockBytes, ta, half);
+            // x -> bf16 chunks (token m = c / 16, k chunk j = c mod 16 of the
+            // half): a quarter warp takes one token's 8 consecutive chunks,
+            // stored to 8 distinct bank groups; two-way loads
             {
-                const int r = t & 7, j = ((t >> 3) + r) & 15;  // 16 quarter warps: every chunk j once
-                for (int m = r; m < M; m += 8) {
+                uint8_t* xs = smem + kB0 + (2 * half + b) * kBStage;
+                for (int c = t; c < M * 16; c += 128) {
+                    const int m = c >> 4, j = c & 15;
                     const float4 a = *reinterpret_cast<const float4*>(xr + m * 256 + 128 * half + 8 * j);
-                    const float4 b = *reinterpret_cast<const float4*>(xr + m * 256 + 128 * half + 8 * j + 4);
-                    *reinterpret_cast<uint4*>(opB + op_off(m, j)) = make_uint4(
-                        pack_bf16(a.x, a.y), pack_bf16(a.z, a.w), pack_bf16(b.x, b.y), pack_bf16(b.z, b.w));
+                    const float4 q = *reinterpret_cast<const float4*>(xr + m * 256 + 128 * half + 8 * j + 4);
+                    *reinterpret_cast<uint4*>(xs + x_off(m, j)) = make_uint4(
+                        pack_bf16(a.x, a.y), pack_bf16(a.z, a.w), pack_bf16(q.x, q.y), pack_bf16(q.z, q.w));
                 }
             }
-            fence_proxy_async_smem();  // generic-proxy stores -> visible to the tensor core
+            tmem_wait_st();            // W in tensor memory
+            fence_proxy_async_smem();  // x: generic-proxy stores -> visible to the tensor core
+            tc_fence_before();
             __syncwarp();
             if (lane == 0) {
-                arrive(&op_full[half]);
+                arrive(&op_full[2 * half + b]);
                 arrive(&raw_empty[s]);
             }
             if (last && half == 0) {
-                mbar_wait_bounded(acc_full, static_cast<uint32_t>(seg & 1), status);
+                mbar_wait_bounded(&acc_full[seg & 1], static_cast<uint32_t>((seg >> 1) & 1), status);
                 tc_fence_after();
                 float v[32];
-                tmem_ld32(tmem + (static_cast<uint32_t>(32 * hw) << 16), v);
+                tmem_ld32(tmem + tl + kTmD + 32u * static_cast<uint32_t>(seg & 1), v);
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) arrive(&acc_empty[seg & 1]);
                 if (t < rows) {
                     const int64_t row = row0 + t;
 #pragma unroll
                     for (int m = 0; m < 32; ++m)
                         if (m < M) atomicAdd(&Y[m * N + row], v[m]);
                 }
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) arrive(acc_empty);
             }
             if (last) ++seg;
             if (++s == nraw) {
@@ -467,6 +523,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols) : "memory");
     }
 }
+
 
 }  // namespace tc
 
