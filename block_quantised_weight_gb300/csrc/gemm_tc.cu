@@ -1,15 +1,18 @@
-// Batched Q4_K / IQ3 GEMM on the tcgen05 tensor cores (16 <= M <= 32 tokens).
+// Batched Q4_K and IQ3 GEMM on the tcgen05 tensor cores.
 //
 //   Y[m][n] = sum_k w[n][k] * X[m][k]
 //
-// Only here the path is a dense contraction: a 128-row tile of W is
-// dequantised (page 1 "Rewriting picoLM in Python", dequantize_q4_K:
-// (d*sc)*q - dmin*mn; page 4 "iq3_pack.py", decode:
-// d*(0.5+code)*0.5 * grid*0.5 * sign) into shared memory as bf16 (round to
-// nearest even); X
-// is rounded to bf16 likewise; tcgen05.mma (kind::f16, bf16 x bf16, fp32
-// accumulation in tensor memory) computes D[row][token] = W_tile X^T (W rows
-// on the MMA's M=128 side, tokens on its N=16/32 side).
+// Two kernels, one CTA layout.  W rows sit on the MMA's M=128 side, tokens
+// on its N=16/32 side (tcgen05.mma kind::f16, bf16 x bf16, fp32
+// accumulation in tensor memory).
+//   qg_gemm_tc_kernel (Q4_K, 16 <= M <= 32): a 128-row tile of W is
+//     dequantised (page 1 "Rewriting picoLM in Python", dequantize_q4_K:
+//     (d*sc)*q - dmin*mn) exactly in fp32 and rounded once to bf16 (to
+//     nearest even); X is rounded to bf16 likewise.
+//   qg_gemm_tc_iq3x_kernel<XP> (IQ3): the signed grid bytes enter the MMA
+//     exactly and each sub-block factor is applied after it (see there); x
+//     in XP bf16 parts (XP = 3 from 5 to 10 tokens: exact products; XP = 1
+//     from 16 tokens).
 //
 // CTA roles (320 threads):
 //   warps 0-7  dequantise W into tensor memory and X into shared memory:
@@ -34,16 +37,14 @@
 // of the one before, and a segment's drain the next segment's MMAs.
 //
 // Tensor memory (512 columns): A of half h, buffer b at columns 64 (2h + b)
-// (row = lane, k pairs as bf16x2 per column, k ascending); the accumulators
-// at 256 and 288 (D[row][token], fp32, 32 columns each).
+// (row = lane, k pairs as bf16x2 per column, k ascending); the Q4_K
+// accumulators at 256 and 288 (D[row][token], fp32, 32 columns each), the
+// IQ3 sub-block sums at 256 + 128 h + 32 j.
 //
-// Exact weights: with the fp16 magic h = 1024 + q, one fp16 FMA gives
+// Exact Q4_K weights: with the fp16 magic h = 1024 + q, one fp16 FMA gives
 // h*sc - 1024*sc = q*sc exactly (at most 945: the fused product is rounded
 // once and the result is representable); a mixed f16 x f16 + f32 FMA then
 // gives d*(q*sc) - dmin*mn with a single rounding, the pages' fp32 value.
-// IQ3 values have at most 24 significant bits: (grid byte) * (d*(0.5+code)
-// *0.25) is exact in fp32 (the grid's 0.5 folded into the sub-block factor),
-// so bf16 rounds the pages' exact value once.
 //
 // x operand layout (K-major, 128-byte swizzle): for half h, buffer b, two
 // 4 KB atoms (k 0-63 and 64-127 of the half) of 32 token rows x 128 bytes;
@@ -66,20 +67,14 @@ namespace tc {
 constexpr int kTileRows = 128;
 constexpr int kBlockBytes = 144;
 constexpr int kThreads = 320;  // 8 dequant warps, producer, MMA
-constexpr int kRawW = kTileRows * kBlockBytes;     // 18432: TMA box 144 x 128 (IQ3: 112 x 128)
+constexpr int kRawW = kTileRows * kBlockBytes;     // 18432: TMA box 144 x 128 (IQ3: 112 x 128, x after 18432 too)
 constexpr int kIQ3Box = 112;
 constexpr int kMaxRaw = 6;                          // raw stages (W box + the unit's x, M KB)
-// Shared memory: barriers, the four x stages, the IQ3 tables, and the raw
+// Shared memory: barriers, the four x stages, (IQ3) the tables, and the raw
 // ring at the end: as many stages of kRawW + M * 1024 bytes as fit.
 constexpr int kB0 = 1024;
 constexpr int kBStage = 2 * 32 * 128;               // 8192: two 64-k atoms of 32 token rows
-// IQ3: the grid as fp32, 8 copies: row i of copy c at (8i + c) * 16 bytes,
-// lane L reading copy L & 7, so the 8 lanes of a quarter warp gather from 8
-// distinct bank groups whatever their rows (32 KB).
-constexpr int kGrid0 = kB0 + 4 * kBStage;           // 33792
-constexpr int kSign0 = kGrid0 + 32768;              // IQ3: sign-mask words, 8 copies (entry s7 of copy c at 8*s7 + c: 4 KB)
-constexpr int kRaw0Q4K = kGrid0;                    // 33792
-constexpr int kRaw0IQ3 = kSign0 + 4096;             // 70656
+constexpr int kRaw0Q4K = kB0 + 4 * kBStage;         // 33792
 constexpr int kSmemMax = 232448;                     // 227 KB per CTA
 __host__ __device__ constexpr int raw_stage_bytes(int M) { return kRawW + M * 1024; }
 constexpr int kTmemCols = 512;
@@ -244,48 +239,6 @@ __device__ __forceinline__ void dequant_half(const uint8_t* blk, uint32_t ta, in
     }
 }
 
-// IQ3: thread t, half `half` (sub-blocks 4*half .. +3) of tile row t, the
-// block of column COL starting (98*COL) mod 16 bytes into its 112-byte box
-// row: the fields come in as 16-byte loads (rows 112 = 7 x 16 bytes apart,
-// so 8 consecutive threads hit 8 distinct bank groups) realigned in
-// registers (iq3_load_half).  Signs are applied to packed bf16 pairs:
-// sgn[s7] holds the eight signs of a 7-bit field (the eighth its parity)
-// with sign 2p at bit 15-p and sign 2p+1 at bit 31-p, so (T << p) &
-// 0x80008000 flips pair p.
-template <int COL>
-__device__ __forceinline__ void dequant_half_iq3(const uint8_t* boxrow, const float4* grid4, const uint32_t* sgn,
-                                                 uint32_t ta, int t, int half) {
-    uint32_t vi[8], vs[4], dbits;
-    iq3_load_half<FmtIQ3T, COL>(boxrow, half, vi, vs, dbits);
-    const float d = h2f(dbits);
-    uint32_t w[32];  // two sub-blocks: 8 chunks of 4 columns
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-        const uint32_t sw = vs[j];
-        const float dbh = d * (static_cast<float>(sw >> 28) + 0.5f) * 0.25f;  // 0.5 * grid's 0.5
-#pragma unroll
-        for (int l = 0; l < 4; ++l) {
-            const uint32_t T = sgn[8 * ((sw >> (7 * l)) & 0x7Fu) + (t & 7)];
-            uint32_t packed[4];
-#pragma unroll
-            for (int hf = 0; hf < 2; ++hf) {
-                const int pi = 8 * j + 2 * l + hf;  // index byte within the half
-                const uint32_t idx = (vi[pi >> 2] >> (8 * (pi & 3))) & 0xFFu;
-                const float4 g = grid4[8 * idx + (t & 7)];
-                // |w| = grid * dbh exactly, rounded once to bf16; the sign bits of
-                // pairs 2hf and 2hf+1 come from T
-                packed[2 * hf] = pack_bf16(g.x * dbh, g.y * dbh) ^ ((T << (2 * hf)) & 0x80008000u);
-                packed[2 * hf + 1] = pack_bf16(g.z * dbh, g.w * dbh) ^ ((T << (2 * hf + 1)) & 0x80008000u);
-            }
-            // weights 32j + 8l .. +7 of the half: columns 16j + 4l .. +3
-#pragma unroll
-            for (int e = 0; e < 4; ++e) w[16 * (j & 1) + 4 * l + e] = packed[e];
-        }
-        if (j & 1) tmem_st32(ta + 32 * (j >> 1), w);
-    }
-}
-
-template <bool IQ3>
 __global__ void __launch_bounds__(kThreads, 1)
     qg_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
                    const uint8_t* __restrict__ grid, float* __restrict__ Y, int M, int64_t N, int64_t K, int nraw,
@@ -298,7 +251,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t* acc_full = op_full + 8;                         // [2]
     uint64_t* acc_empty = op_full + 10;                       // [2]
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + 512);
-    const int raw0 = IQ3 ? kRaw0IQ3 : kRaw0Q4K;
+    const int raw0 = kRaw0Q4K;
     const int rstage = raw_stage_bytes(M);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -334,23 +287,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int i = threadIdx.x; i < 4 * kBStage / 16; i += kThreads)
         reinterpret_cast<uint4*>(smem + kB0)[i] = make_uint4(0u, 0u, 0u, 0u);
     fence_proxy_async_smem();
-    if constexpr (IQ3) {
-        // the grid bytes (doubled units) as fp32, one float4 per row
-        float* g = reinterpret_cast<float*>(smem + kGrid0);
-        for (int i = threadIdx.x; i < 8 * 1024; i += kThreads)  // i = (row * 8 + copy) * 4 + j
-            g[i] = static_cast<float>(grid[(i >> 5) * 4 + (i & 3)]);
-        // signs of each 7-bit field: the seven stored ones and their parity
-        // (page 4, decode), sign k at bit 15 - k/2 (k even) or 31 - k/2 (odd)
-        uint32_t* sg = reinterpret_cast<uint32_t*>(smem + kSign0);
-        for (int i = threadIdx.x; i < 8 * 128; i += kThreads) {  // i = 8 * s7 + copy
-            const uint32_t s7 = static_cast<uint32_t>(i) >> 3;
-            const uint32_t s8 = s7 | ((__popc(s7) & 1u) << 7);
-            uint32_t t = 0;
-            for (int pr = 0; pr < 4; ++pr)
-                t |= (((s8 >> (2 * pr)) & 1u) << (15 - pr)) | (((s8 >> (2 * pr + 1)) & 1u) << (31 - pr));
-            sg[i] = t;
-        }
-    }
     if (warp == 9) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
                      ::"r"(smem_u32(tmem_slot)), "r"(kTmemCols) : "memory");
@@ -366,8 +302,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) {
             const uint64_t pol_w = policy_evict_first();
             const uint64_t pol_x = policy_evict_last();
-            constexpr int kBoxBytes = IQ3 ? kIQ3Box : kBlockBytes;
-            const uint32_t bytes = kTileRows * kBoxBytes + M * 1024;
+            const uint32_t bytes = kTileRows * kBlockBytes + M * 1024;
             // (stage, phase, tile, k-block) kept incrementally: a 64-bit
             // division per unit costs a good fraction of a unit's time
             int s = 0;
@@ -378,8 +313,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (u - u_begin >= nraw) mbar_wait_bounded(&raw_empty[s], (round - 1) & 1u, status);
                 uint8_t* raw = smem + raw0 + s * rstage;
                 mbar_arrive_expect_tx(&raw_full[s], bytes);
-                const int bx = IQ3 ? (kb * 98) & ~15 : kb * kBlockBytes;  // x * 1 byte: 16-byte aligned
-                tma_load_2d(raw, &tmW, bx, static_cast<int>(tile * kTileRows), &raw_full[s], pol_w);
+                tma_load_2d(raw, &tmW, kb * kBlockBytes, static_cast<int>(tile * kTileRows), &raw_full[s], pol_w);
                 tma_load_2d(raw + kRawW, &tmX, kb * 256, 0, &raw_full[s], pol_x);
                 if (++s == nraw) {
                     s = 0;
@@ -457,19 +391,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (i >= 2) mbar_wait_bounded(&op_empty[2 * half + b], static_cast<uint32_t>(((i >> 1) - 1) & 1), status);
             tc_fence_after();
             const uint32_t ta = tmem + tl + kTmA + 64u * static_cast<uint32_t>(2 * half + b);
-            if constexpr (IQ3)  // rows past N: TMA zero fill, unused
-                switch (kb & 7) {  // the block's offset in its box: (98 * kb) mod 16
-#define QG_TC_IQ3(C)                                                                                          \
-    case C:                                                                                                  \
-        dequant_half_iq3<C>(raw + t * kIQ3Box, reinterpret_cast<const float4*>(smem + kGrid0),             \
-                            reinterpret_cast<const uint32_t*>(smem + kSign0), ta, t, half);                  \
-        break;
-                    QG_TC_IQ3(0) QG_TC_IQ3(1) QG_TC_IQ3(2) QG_TC_IQ3(3)
-                    QG_TC_IQ3(4) QG_TC_IQ3(5) QG_TC_IQ3(6) QG_TC_IQ3(7)
-#undef QG_TC_IQ3
-                }
-            else
-                dequant_half(raw + t * kBlockBytes, ta, half);
+            dequant_half(raw + t * kBlockBytes, ta, half);
             // x -> bf16 chunks (token m = c / 16, k chunk j = c mod 16 of the
             // half): a quarter warp takes one token's 8 consecutive chunks,
             // stored to 8 distinct bank groups; two-way loads
@@ -525,6 +447,310 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 
+
+// ------------------------------------------------ IQ3: sub-block factors after the MMA
+// IQ3 (page 4 "iq3_pack.py", decode): w = d*(0.5+code)*0.5 * grid*0.5 *
+// sign = f_j * (+-g), with g a grid byte and f_j = d*(0.5+code)*0.25 the
+// factor of sub-block j.  The MMA takes the signed grid bytes (integers
+// below 256: exact in bf16) and x as XP bf16 parts: XP = 3 splits each x
+// exactly (x = hi + mid + lo, each part rounding the remainder of the one
+// before), so every product is exact and only the fp32 accumulation rounds;
+// XP = 1 rounds x to bf16.  Each (row, sub-block, token part) accumulates in
+// its own TMEM column, and the dequantising warps add f_j * (sum of the
+// parts) into registers, a unit behind the MMAs.
+constexpr int kGridX0 = kB0 + 4 * kBStage;       // 33792: grid rows as two bf16 pairs, 8 copies (16 KB)
+constexpr int kSignX0 = kGridX0 + 16384;         // 50176: sign words, 8 copies (4 KB)
+constexpr int kRaw0X = kSignX0 + 4096;           // 54272
+constexpr uint32_t kTmDX = 256;                  // D of half h at 256 + 128 h, sub-block j at + 32 j
+
+template <int XP>
+__global__ void __launch_bounds__(kThreads, 1)
+    qg_gemm_tc_iq3x_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
+                           const uint8_t* __restrict__ grid, float* __restrict__ Y, int M, int64_t N, int64_t K,
+                           int nraw, unsigned* status) {
+    static_assert(XP == 1 || XP == 3, "x parts");
+    constexpr int MT = 32 / XP;  // tokens at most: XP * M columns of D per sub-block
+    extern __shared__ __align__(1024) uint8_t smem[];
+    uint64_t* raw_full = reinterpret_cast<uint64_t*>(smem);  // [kMaxRaw]
+    uint64_t* raw_empty = raw_full + kMaxRaw;                 // [kMaxRaw]
+    uint64_t* op_full = raw_full + 2 * kMaxRaw;               // [half][buffer]
+    uint64_t* op_empty = op_full + 4;                         // [half][buffer]
+    uint64_t* d_full = op_full + 8;                           // [half]
+    uint64_t* d_empty = op_full + 10;                         // [half]
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + 512);
+    const int rstage = raw_stage_bytes(M);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int nb = static_cast<int>(K / 256);
+    const int64_t ntiles = (N + kTileRows - 1) / kTileRows;
+    const int64_t U = ntiles * nb;
+    const int64_t u_begin = U * blockIdx.x / gridDim.x;
+    const int64_t u_end = U * (blockIdx.x + 1) / gridDim.x;
+    const int ncol = XP * M <= 16 ? 16 : 32;
+    // the swizzled x stages need a 1024-byte aligned base (all threads see the
+    // same address: the CTA leaves before any barrier or TMEM use)
+    if ((smem_u32(smem) & 1023u) != 0) {
+        if (threadIdx.x == 0) atomicOr(status, kStatusBounds);
+        return;
+    }
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < nraw; ++i) {
+            mbar_init(&raw_full[i], 1);
+            mbar_init(&raw_empty[i], 8);
+        }
+        for (int i = 0; i < 4; ++i) {
+            mbar_init(&op_full[i], 4);
+            mbar_init(&op_empty[i], 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&d_full[i], 1);
+            mbar_init(&d_empty[i], 4);
+        }
+        fence_mbar_init();
+    }
+    // x stages: token rows past XP * M stay zero (the MMA reads 16 or 32 rows)
+    for (int i = threadIdx.x; i < 4 * kBStage / 16; i += kThreads)
+        reinterpret_cast<uint4*>(smem + kB0)[i] = make_uint4(0u, 0u, 0u, 0u);
+    fence_proxy_async_smem();
+    {
+        // grid row r as bf16 pairs (bytes 0,1) (bytes 2,3), 8 copies: row r of copy c at 8 (8 r + c) bytes
+        uint2* g2 = reinterpret_cast<uint2*>(smem + kGridX0);
+        for (int i = threadIdx.x; i < 256 * 8; i += kThreads) {
+            const uint8_t* gr = grid + (i >> 3) * 4;
+            g2[i] = make_uint2(pack_bf16(gr[0], gr[1]), pack_bf16(gr[2], gr[3]));
+        }
+        // signs of each 7-bit field: the seven stored ones and their parity
+        // (page 4, decode), sign k at bit 15 - k/2 (k even) or 31 - k/2 (odd)
+        uint32_t* sg = reinterpret_cast<uint32_t*>(smem + kSignX0);
+        for (int i = threadIdx.x; i < 8 * 128; i += kThreads) {  // i = 8 * s7 + copy
+            const uint32_t s7 = static_cast<uint32_t>(i) >> 3;
+            const uint32_t s8 = s7 | ((__popc(s7) & 1u) << 7);
+            uint32_t t = 0;
+            for (int pr = 0; pr < 4; ++pr)
+                t |= (((s8 >> (2 * pr)) & 1u) << (15 - pr)) | (((s8 >> (2 * pr + 1)) & 1u) << (31 - pr));
+            sg[i] = t;
+        }
+    }
+    if (warp == 9) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
+                     ::"r"(smem_u32(tmem_slot)), "r"(kTmemCols) : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 8) {
+        // ---------------- producer (one thread issues the tensor copies)
+        if (lane == 0) {
+            const uint64_t pol_w = policy_evict_first();
+            const uint64_t pol_x = policy_evict_last();
+            const uint32_t bytes = kTileRows * kIQ3Box + M * 1024;
+            int s = 0;
+            uint32_t round = 0;  // completed passes over the raw ring
+            int64_t tile = u_begin / nb;
+            int kb = static_cast<int>(u_begin % nb);
+            for (int64_t u = u_begin; u < u_end; ++u) {
+                if (u - u_begin >= nraw) mbar_wait_bounded(&raw_empty[s], (round - 1) & 1u, status);
+                uint8_t* raw = smem + kRaw0X + s * rstage;
+                mbar_arrive_expect_tx(&raw_full[s], bytes);
+                tma_load_2d(raw, &tmW, (kb * 98) & ~15, static_cast<int>(tile * kTileRows), &raw_full[s], pol_w);
+                tma_load_2d(raw + kRawW, &tmX, kb * 256, 0, &raw_full[s], pol_x);
+                if (++s == nraw) {
+                    s = 0;
+                    ++round;
+                }
+                if (++kb == nb) {
+                    kb = 0;
+                    ++tile;
+                }
+            }
+        }
+        __syncwarp();
+    } else if (warp == 9) {
+        // ---------------- MMA issuer: per unit both halves, 16 MMAs in one run
+        const uint32_t idesc = instr_desc(kTileRows, ncol);
+        for (int64_t i = 0; i < u_end - u_begin; ++i) {
+            const int b = static_cast<int>(i & 1);
+            mbar_wait_bounded(&op_full[b], static_cast<uint32_t>((i >> 1) & 1), status);
+            mbar_wait_bounded(&op_full[2 + b], static_cast<uint32_t>((i >> 1) & 1), status);
+            if (i >= 1) {  // the previous unit's sums read out of D
+                mbar_wait_bounded(&d_empty[0], static_cast<uint32_t>((i - 1) & 1), status);
+                mbar_wait_bounded(&d_empty[1], static_cast<uint32_t>((i - 1) & 1), status);
+            }
+            tc_fence_after();
+            if (lane == 0) {
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const uint32_t ta = tmem + kTmA + 64u * static_cast<uint32_t>(2 * h + b);
+                    const uint32_t td = tmem + kTmDX + 128u * static_cast<uint32_t>(h);
+                    const uint32_t b0 = smem_u32(smem + kB0 + (2 * h + b) * kBStage);
+#pragma unroll
+                    for (int ks = 0; ks < 8; ++ks) {  // sub-block ks / 2 of the half: two MMAs of 16 k
+                        const uint64_t bd = smem_desc_sw128(b0 + 4096 * (ks >> 2) + 32 * (ks & 3), kSBO);
+                        mma_bf16_ta(td + 32 * (ks >> 1), ta + 8 * ks, bd, idesc, static_cast<uint32_t>(ks & 1));
+                    }
+                }
+                mma_commit(&op_empty[b]);
+                mma_commit(&op_empty[2 + b]);
+                mma_commit(&d_full[0]);
+                mma_commit(&d_full[1]);
+            }
+            __syncwarp();
+        }
+    } else {
+        // ---------------- dequant (warps 0-7: half = warp / 4, thread = tile row = TMEM lane)
+        const int half = warp >> 2;
+        const int t = threadIdx.x & 127;
+        const uint32_t tl = static_cast<uint32_t>(32 * (warp & 3)) << 16;
+        const uint2* g2 = reinterpret_cast<const uint2*>(smem + kGridX0);
+        const uint32_t* sgn = reinterpret_cast<const uint32_t*>(smem + kSignX0);
+        float acc[MT];
+#pragma unroll
+        for (int m = 0; m < MT; ++m) acc[m] = 0.f;
+        float fp[4] = {0.f, 0.f, 0.f, 0.f};  // the previous unit's sub-block factors
+        int64_t prow0 = 0;
+        int prows = 0;
+        bool plast = false;
+        // the previous unit's sums: f_j * (sum of the parts) into acc; at a
+        // segment's end acc goes into Y
+        auto drain = [&](int64_t ip) {
+            mbar_wait_bounded(&d_full[half], static_cast<uint32_t>(ip & 1), status);
+            tc_fence_after();
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                float v[32];
+                tmem_ld32(tmem + tl + kTmDX + 128u * static_cast<uint32_t>(half) + 32u * j, v);
+                if (j == 3) {
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) arrive(&d_empty[half]);
+                }
+#pragma unroll
+                for (int m = 0; m < MT; ++m) {
+                    const float sm = XP == 1 ? v[m] : v[3 * m] + (v[3 * m + 1] + v[3 * m + 2]);
+                    acc[m] = fmaf(fp[j], sm, acc[m]);
+                }
+            }
+            if (plast) {
+                if (t < prows) {
+                    const int64_t row = prow0 + t;
+#pragma unroll
+                    for (int m = 0; m < MT; ++m)
+                        if (m < M) atomicAdd(&Y[m * N + row], acc[m]);
+                }
+#pragma unroll
+                for (int m = 0; m < MT; ++m) acc[m] = 0.f;
+            }
+        };
+        int s = 0;
+        uint32_t rphase = 0;
+        int64_t tile = u_begin / nb;
+        int kb = static_cast<int>(u_begin % nb);
+        for (int64_t u = u_begin; u < u_end; ++u) {
+            const int64_t i = u - u_begin;
+            const int b = static_cast<int>(i & 1);
+            const bool last = (u == u_end - 1) || kb == nb - 1;
+            const int64_t row0 = tile * kTileRows;
+            const int rows = static_cast<int>(min64(kTileRows, N - row0));
+            const uint8_t* raw = smem + kRaw0X + s * rstage;
+            const float* xr = reinterpret_cast<const float*>(raw + kRawW);
+            mbar_wait_bounded(&raw_full[s], rphase, status);
+            // buffer b of this half was last read by the MMAs of unit i - 2
+            if (i >= 2) mbar_wait_bounded(&op_empty[2 * half + b], static_cast<uint32_t>(((i >> 1) - 1) & 1), status);
+            tc_fence_after();
+            uint32_t vi[8], vs[4], dbits;
+            switch (kb & 7) {  // the block's offset in its box: (98 * kb) mod 16
+#define QG_TC_IQ3X(C) \
+    case C: iq3_load_half<FmtIQ3T, C>(raw + t * kIQ3Box, half, vi, vs, dbits); break;
+                QG_TC_IQ3X(0) QG_TC_IQ3X(1) QG_TC_IQ3X(2) QG_TC_IQ3X(3)
+                QG_TC_IQ3X(4) QG_TC_IQ3X(5) QG_TC_IQ3X(6) QG_TC_IQ3X(7)
+#undef QG_TC_IQ3X
+            }
+            const float d = h2f(dbits);
+            float f[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) f[j] = d * (static_cast<float>(vs[j] >> 28) + 0.5f) * 0.25f;
+            // the signed grid bytes as bf16, sub-block j at columns 16 j .. 16 j + 15
+            const uint32_t ta = tmem + tl + kTmA + 64u * static_cast<uint32_t>(2 * half + b);
+#pragma unroll
+            for (int jp = 0; jp < 2; ++jp) {
+                uint32_t w[32];
+#pragma unroll
+                for (int jj = 0; jj < 2; ++jj) {
+                    const int j = 2 * jp + jj;
+                    const uint32_t sw = vs[j];
+#pragma unroll
+                    for (int l = 0; l < 4; ++l) {
+                        const uint32_t T = sgn[8 * ((sw >> (7 * l)) & 0x7Fu) + (t & 7)];
+#pragma unroll
+                        for (int hf = 0; hf < 2; ++hf) {
+                            const int pi = 8 * j + 2 * l + hf;  // index byte within the half
+                            const uint32_t idx = (vi[pi >> 2] >> (8 * (pi & 3))) & 0xFFu;
+                            const uint2 g = g2[8 * idx + (t & 7)];
+                            w[16 * jj + 4 * l + 2 * hf] = g.x ^ ((T << (2 * hf)) & 0x80008000u);
+                            w[16 * jj + 4 * l + 2 * hf + 1] = g.y ^ ((T << (2 * hf + 1)) & 0x80008000u);
+                        }
+                    }
+                }
+                tmem_st32(ta + 32 * jp, w);
+            }
+            // x -> XP bf16 parts, part p of token m in row XP m + p
+            {
+                uint8_t* xs = smem + kB0 + (2 * half + b) * kBStage;
+                for (int c = t; c < M * 16; c += 128) {
+                    const int m = c >> 4, j = c & 15;
+                    const float4 a = *reinterpret_cast<const float4*>(xr + m * 256 + 128 * half + 8 * j);
+                    const float4 q = *reinterpret_cast<const float4*>(xr + m * 256 + 128 * half + 8 * j + 4);
+                    float v[8] = {a.x, a.y, a.z, a.w, q.x, q.y, q.z, q.w};
+#pragma unroll
+                    for (int p = 0; p < XP; ++p) {
+                        uint32_t w4[4];
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            w4[e] = pack_bf16(v[2 * e], v[2 * e + 1]);
+                            // the remainder is exact in fp32 (Sterbenz)
+                            v[2 * e] -= __uint_as_float(w4[e] << 16);
+                            v[2 * e + 1] -= __uint_as_float(w4[e] & 0xFFFF0000u);
+                        }
+                        *reinterpret_cast<uint4*>(xs + x_off(XP * m + p, j)) = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+                    }
+                }
+            }
+            tmem_wait_st();            // W in tensor memory
+            fence_proxy_async_smem();  // x: generic-proxy stores -> visible to the tensor core
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) {
+                arrive(&op_full[2 * half + b]);
+                arrive(&raw_empty[s]);
+            }
+            if (i >= 1) drain(i - 1);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) fp[j] = f[j];
+            plast = last;
+            prow0 = row0;
+            prows = rows;
+            if (++s == nraw) {
+                s = 0;
+                rphase ^= 1u;
+            }
+            if (++kb == nb) {
+                kb = 0;
+                ++tile;
+            }
+        }
+        if (u_end > u_begin) drain(u_end - u_begin - 1);
+    }
+    __syncthreads();
+    if (warp == 9) {
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols) : "memory");
+    }
+}
+
 }  // namespace tc
 
 
@@ -532,22 +758,25 @@ namespace {
 
 // Both formats: W viewed as [N rows][pitch bytes] with a box of one block
 // column (Q4_K 144 bytes; IQ3 112 bytes) x 128 rows; X [M][K] fp32 with a
-// box of 256 k x M tokens.
-template <bool IQ3>
+// box of 256 k x M tokens.  KIND 0: Q4_K (bf16 weights, 16 <= M <= 32);
+// KIND 1 / 3: IQ3 with the sub-block factors after the MMA and x in 1 / 3
+// bf16 parts (KIND * M <= 32).
+template <int KIND>
 int launch_tc(const uint8_t* W, const uint8_t* grid, const float* X, float* Y, int M, int64_t N, int64_t K,
               cudaStream_t s, unsigned* status) {
-    if (M < 16 || M > 32) return QG_EINVAL;
+    constexpr bool IQ3 = KIND != 0;
+    if (KIND == 0 ? (M < 16 || M > 32) : (M < 1 || KIND * M > 32)) return QG_EINVAL;
     static std::atomic<bool> attr_done[64];
     int dev = -1;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return qg::cuda_fail(cudaGetLastError());
+    auto kern = KIND == 0 ? tc::qg_gemm_tc_kernel : tc::qg_gemm_tc_iq3x_kernel<KIND == 0 ? 1 : KIND>;
     // as many raw stages as fit (the x part of a stage is M KB)
-    const int raw0 = IQ3 ? tc::kRaw0IQ3 : tc::kRaw0Q4K;
+    const int raw0 = IQ3 ? tc::kRaw0X : tc::kRaw0Q4K;
     const int nraw = std::min(tc::kMaxRaw, (tc::kSmemMax - raw0) / tc::raw_stage_bytes(M));
     if (nraw < 2) return QG_EINVAL;
     const int smem = raw0 + nraw * tc::raw_stage_bytes(M);
     if (!attr_done[dev].load(std::memory_order_acquire)) {
-        if (cudaFuncSetAttribute(tc::qg_gemm_tc_kernel<IQ3>, cudaFuncAttributeMaxDynamicSharedMemorySize, tc::kSmemMax) !=
-            cudaSuccess)
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, tc::kSmemMax) != cudaSuccess)
             return qg::cuda_fail(cudaGetLastError());
         attr_done[dev].store(true, std::memory_order_release);
     }
@@ -574,7 +803,7 @@ int launch_tc(const uint8_t* W, const uint8_t* grid, const float* X, float* Y, i
     if (cudaMemsetAsync(Y, 0, static_cast<size_t>(M) * N * sizeof(float), s) != cudaSuccess) return qg::cuda_fail(cudaGetLastError());
     const int64_t units = ((N + tc::kTileRows - 1) / tc::kTileRows) * (K / 256);
     const int gridx = static_cast<int>(std::min<int64_t>(units, sms));
-    tc::qg_gemm_tc_kernel<IQ3><<<gridx, tc::kThreads, smem, s>>>(tmW, tmX, grid, Y, M, N, K, nraw, status);
+    kern<<<gridx, tc::kThreads, smem, s>>>(tmW, tmX, grid, Y, M, N, K, nraw, status);
     return launch_status();
 }
 
@@ -582,14 +811,21 @@ int launch_tc(const uint8_t* W, const uint8_t* grid, const float* X, float* Y, i
 
 int launch_gemm_q4k_tc(const uint8_t* W, const float* X, float* Y, int M, int64_t N, int64_t K, cudaStream_t s,
                        unsigned* status) {
-    return launch_tc<false>(W, nullptr, X, Y, M, N, K, s, status);
+    return launch_tc<0>(W, nullptr, X, Y, M, N, K, s, status);
 }
 
 // IQ3 needs 16-byte aligned rows (K/256 a multiple of 8) for its tensor map.
 int launch_gemm_iq3_tc(const uint8_t* W, const uint8_t* grid, const float* X, float* Y, int M, int64_t N, int64_t K,
                        cudaStream_t s, unsigned* status) {
     if ((K / 256) % 8 != 0) return QG_EINVAL;
-    return launch_tc<true>(W, grid, X, Y, M, N, K, s, status);
+    return launch_tc<1>(W, grid, X, Y, M, N, K, s, status);
+}
+
+// IQ3, 1 <= M <= 10, x in three bf16 parts: every product exact, fp32 sums.
+int launch_gemm_iq3_tc3(const uint8_t* W, const uint8_t* grid, const float* X, float* Y, int M, int64_t N, int64_t K,
+                        cudaStream_t s, unsigned* status) {
+    if ((K / 256) % 8 != 0) return QG_EINVAL;
+    return launch_tc<3>(W, grid, X, Y, M, N, K, s, status);
 }
 
 }  // namespace qg

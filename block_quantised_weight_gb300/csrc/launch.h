@@ -46,10 +46,16 @@ int launch_chain_step(const float* X, float* Y, int64_t K, int grid, unsigned fl
 int launch_pass_q4k(const qg_stage* stages, int nstages, int M, unsigned* sync, cudaStream_t s, unsigned* status);
 int launch_dequant_q4k(const uint8_t* W, float* out, int64_t N, int64_t K, cudaStream_t s);
 int launch_dequant_iq3(const uint8_t* W, const uint8_t* grid, float* out, int64_t N, int64_t K, cudaStream_t s);
-// tcgen05 bf16 path, 16 <= M <= 32
+// tcgen05 paths, 16 <= M <= 32: Q4_K weights rounded to bf16; IQ3 weights
+// exact (signed grid bytes, sub-block factors applied after the MMA), x
+// rounded to bf16
 int launch_gemm_q4k_tc(const uint8_t* W, const float* X, float* Y, int M, int64_t N, int64_t K, cudaStream_t s,
                        unsigned* status);
 int launch_gemm_iq3_tc(const uint8_t* W, const uint8_t* grid, const float* X, float* Y, int M, int64_t N, int64_t K,
                        cudaStream_t s, unsigned* status);
+// tcgen05 IQ3 with x split exactly into three bf16 parts, 1 <= M <= 10:
+// exact products, fp32 accumulation (the fp32 FMA path's bar)
+int launch_gemm_iq3_tc3(const uint8_t* W, const uint8_t* grid, const float* X, float* Y, int M, int64_t N, int64_t K,
+                        cudaStream_t s, unsigned* status);
 
 }  // namespace qg

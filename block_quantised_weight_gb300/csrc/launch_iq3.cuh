@@ -1,8 +1,10 @@
-// IQ3 GEMV dispatch (fp32 FMA path) for both block orders (page 4's and
-// page 3's IQ3_XXS), shared by their translation units.  Kernel:
-// gemv_kernel.cuh; rows whose byte offsets are not 16-byte aligned take the
-// byte-addressed kernel below.
+// IQ3 GEMV dispatch for both block orders (page 4's and page 3's IQ3_XXS),
+// shared by their translation units.  Kernel: gemv_kernel.cuh (fp32 FMA);
+// rows whose byte offsets are not 16-byte aligned take the byte-addressed
+// kernel below; page 4's order from 5 tokens the tcgen05 kernel of
+// gemm_tc.cu with x in three exact bf16 parts.
 #pragma once
+#include <type_traits>
 #include "launch_common.cuh"
 
 namespace qg {
@@ -82,6 +84,24 @@ int launch_group_iq3_t(const uint8_t* const* W, float* const* Y, const int64_t* 
             }
         }
         return QG_OK;
+    }
+    if constexpr (std::is_same<F, FmtIQ3T>::value) {
+        if (M >= 5) {
+            // 5 or more tokens: the tensor cores, x split exactly into three
+            // bf16 parts (gemm_tc.cu), in ceil(M / 10) balanced token groups
+            // of 5 to 10, one pass over W each
+            const int ng = (M + 9) / 10;
+            for (int g = 0; g < ng; ++g) {
+                const int m0 = M * g / ng, m1 = M * (g + 1) / ng;
+                for (int i = 0; i < count; ++i) {
+                    const int rc = launch_gemm_iq3_tc3(W[i], grid, X + static_cast<int64_t>(m0) * K,
+                                                       Y[i] + static_cast<int64_t>(m0) * N[i], m1 - m0, N[i], K, s,
+                                                       status);
+                    if (rc != QG_OK) return rc;
+                }
+            }
+            return QG_OK;
+        }
     }
     // groups of at most 4 tokens (the two-row decode with x staged; beyond
     // one token, one 32-row tile per CTA, so that two stages of the group's

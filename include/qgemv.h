@@ -101,18 +101,23 @@ QG_API int qgemv_q4k(const uint8_t* W, const float* X, float* Y, int M, int64_t 
 QG_API int qgemv_q4k_ex(const uint8_t* W, const float* X, float* Y, int M, int64_t N, int64_t K, unsigned flags,
                         cudaStream_t stream);
 
-/* IQ3 (98-byte super-block) GEMV, fp32 FMA path, 1 <= M <= 32.
+/* IQ3 (98-byte super-block) GEMV, 1 <= M <= 32, within 1e-5 * sum|w*x|.
  * Page 4 "iq3_pack.py", module docstring and decode (format); page 1
  * model_forward's matmul (operation).
  * grid: 256*4 bytes, the codebook in the published doubled units (the kernel
  * applies the 0.5 of page 4's grid()).  Other arguments as qgemv_q4k.
- * K/256 a multiple of 8 takes the tensor-map path, M > 4 in groups of 4
- * tokens, each group streaming W once; other K take a slower byte-addressed
- * path (groups of 8 tokens) with the same numerics.  Range: the tensor-map
- * path takes every finite x (columns whose largest |x| lies outside
- * [2^-24, 2^39) are rescaled by a power of two); the byte-addressed path
- * multiplies x as given, so there |x| must stay within [2^-100, 2^100]
- * for the tolerance to hold. */
+ * K/256 a multiple of 8: M <= 4 takes the fp32 FMA tensor-map path; M >= 5
+ * the tcgen05 tensor cores in groups of 5 to 10 tokens, each streaming W
+ * once: the signed grid bytes enter the MMA exactly (bf16), x split exactly
+ * into three bf16 parts, so every product is exact and the sums are fp32 in
+ * tensor memory, each sub-block factor applied afterwards.  There Y is
+ * zeroed on `stream` and row sums that different CTAs share are added with
+ * fp32 atomics, so repeated calls may differ in the last bits.  Other K
+ * take a slower byte-addressed fp32 path (groups of 8 tokens).  Range: the
+ * FMA tensor-map path takes every finite x (columns whose largest |x| lies
+ * outside [2^-24, 2^39) are rescaled by a power of two); the tensor-core and
+ * byte-addressed paths multiply x as given, so there |x| must stay within
+ * [2^-100, 2^100] for the tolerance to hold. */
 QG_API int qgemv_iq3(const uint8_t* W, const uint8_t* grid, const float* X, float* Y, int M, int64_t N, int64_t K,
               cudaStream_t stream);
 
@@ -191,7 +196,9 @@ QG_API int qdequant_codebook(int format, const uint8_t* W, const void* codebook,
 QG_API int qgemv_q4k_group(const uint8_t* const* W, float* const* Y, const int64_t* N, int count, const float* X,
                            int M, int64_t K, unsigned flags, cudaStream_t stream);
 
-/* IQ3 counterpart of qgemv_q4k_group; one grid for all matrices. */
+/* IQ3 counterpart of qgemv_q4k_group; one grid for all matrices.  From 5
+ * tokens (the tensor-core path of qgemv_iq3) each matrix is its own launch
+ * and results match separate calls up to the order of the fp32 atomics. */
 QG_API int qgemv_iq3_group(const uint8_t* const* W, float* const* Y, const int64_t* N, int count,
                            const uint8_t* grid, const float* X, int M, int64_t K, unsigned flags,
                            cudaStream_t stream);
@@ -307,13 +314,13 @@ QG_API int qgemv_q4k_pass_noalloc(const qg_stage* stages, int nstages, int M, cu
 QG_API int qgemm_q4k_batched(const uint8_t* W, const float* X, float* Y, int M, int64_t N, int64_t K, cudaStream_t stream);
 
 /* Batched IQ3 GEMM for decode batches, 1 <= M <= 32.  Same operation,
- * layouts and grid as qgemv_iq3.  M >= 16 with K/256 a multiple of 8
- * dequantises W tiles to bf16 (round to nearest even; every IQ3 value is
- * exact in fp32 first, page 4 "iq3_pack.py", decode) in shared memory and
- * multiplies on the tcgen05 tensor cores with fp32 accumulation in tensor
- * memory, X also rounded to bf16 (tolerance 4e-3 * sum|w*x|; fp32 atomics
- * as in qgemm_q4k_batched, so not bit-reproducible); otherwise the fp32 FMA
- * path of qgemv_iq3 (1e-5 * sum|w*x|). */
+ * layouts and grid as qgemv_iq3.  M >= 16 with K/256 a multiple of 8 runs
+ * on the tcgen05 tensor cores with the weights exact: the signed grid bytes
+ * in bf16, each sub-block factor d*(0.5+code)*0.25 (page 4 "iq3_pack.py",
+ * decode) applied in fp32 to the sub-block's sums afterwards, X rounded to
+ * bf16 (tolerance 4e-3 * sum|w*x|; fp32 atomics as in qgemm_q4k_batched, so
+ * not bit-reproducible); otherwise the paths of qgemv_iq3 (1e-5 *
+ * sum|w*x|). */
 QG_API int qgemm_iq3_batched(const uint8_t* W, const uint8_t* grid, const float* X, float* Y, int M, int64_t N,
                              int64_t K, cudaStream_t stream);
 

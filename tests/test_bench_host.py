@@ -21,14 +21,20 @@ def _fake_lib():
 def test_kernel_launches_follow_the_token_groups():
     lib = _fake_lib()
     kl = bench.kernel_launches
-    # Q4_K FMA path: groups of 4 tokens; tcgen05 from 16 tokens: one launch
-    assert [kl(lib, lib.qgemv_q4k_ex, (), m) for m in (1, 4, 5, 8, 13)] == [1, 1, 2, 2, 4]
-    assert kl(lib, lib.qgemm_q4k_batched, (), 8) == 2
+    # Q4_K FMA path: 5 to 8 remaining tokens in one 8-token pass, otherwise
+    # groups of at most 4; tcgen05 from 16 tokens: one launch
+    assert [kl(lib, lib.qgemv_q4k_ex, (), m) for m in (1, 4, 5, 8, 9, 12, 13)] == [1, 1, 1, 1, 2, 2, 2]
+    assert kl(lib, lib.qgemm_q4k_batched, (), 8) == 1
     assert kl(lib, lib.qgemm_q4k_batched, (), 16) == 1
     assert kl(lib, lib.qgemv_q4k_fused_group, (), 3) == 1
-    # IQ3: groups of 4 tokens
-    assert [kl(lib, lib.qgemv_iq3_group, (), m) for m in (1, 2, 3, 5, 8)] == [1, 1, 1, 2, 2]
+    assert kl(lib, lib.qgemv_q4k_fused, (), 8) == 2
+    # IQ3: groups of 4 tokens up to 4; from 5, tcgen05 per matrix and group of <= 10
+    grp = (None, None, None, 3)
+    assert [kl(lib, lib.qgemv_iq3_group, grp, m) for m in (1, 2, 3, 4, 5, 8, 13)] == [1, 1, 1, 1, 3, 3, 6]
+    assert [kl(lib, lib.qgemv_iq3_ex, (), m) for m in (4, 5, 10, 11, 15)] == [1, 1, 1, 2, 2]
+    assert kl(lib, lib.qgemm_iq3_batched, (), 8) == 1
     assert kl(lib, lib.qgemm_iq3_batched, (), 32) == 1
+    assert kl(lib, lib.qgemv_iq3xxs_ex, (), 8) == 2
     # codebook formats: IQ4 (ids 1, 2) groups of 4, grid formats groups of 8
     assert kl(lib, lib.qgemv_codebook, (1,), 5) == 2
     assert kl(lib, lib.qgemv_codebook, (3,), 5) == 1

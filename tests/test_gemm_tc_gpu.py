@@ -1,9 +1,12 @@
 """GPU parity of qgemm_q4k_batched against the oracle.
 
-M >= 16 runs the tcgen05 path: W tiles dequantised and rounded to bf16 (RN),
-X rounded to bf16, fp32 accumulation.  Each product carries at most
+M >= 16 runs the tcgen05 path: Q4_K tiles dequantised and rounded to bf16
+(RN), X rounded to bf16, fp32 accumulation.  Each product carries at most
 (1 + 2^-9)^2 - 1 < 3.91e-3 relative error, so |y - y_ref| <= 4e-3 * sum|w*x|.
-M < 16 runs the fp32 FMA path (1e-5).
+IQ3 keeps its weights exact (signed grid bytes in the MMA, the sub-block
+factor applied in fp32 after it), so only the bf16 rounding of X counts
+and the same bar holds with room to spare.  M < 16 runs the fp32 FMA path
+(1e-5).
 """
 import numpy as np
 import pytest

@@ -336,13 +336,20 @@ def test_q4k_group_with_prefetch_flag(q):
 @pytest.mark.parametrize("K", [2048, 768])
 @pytest.mark.parametrize("M", [1, 2, 4, 5])
 def test_iq3_group_matches_single_calls(q, K, M):
+    """Bit-identical on the FMA paths; from 5 tokens with K/256 a multiple
+    of 8 (the tensor-core path) split rows meet in fp32 atomics, so the two
+    agree to the order of those additions."""
     grid = synth.gen_iq3_grid(3)
     Ws = [dev(synth.gen_iq3(N, K, 80 + i, grid_seed=3)[0]) for i, N in enumerate((100, 64, 33))]
     g = dev(grid)
     x = dev(synth.gen_x(M, K, 13))
     ys = q.qgemv_iq3_group(Ws, g, x)
     for W, y in zip(Ws, ys):
-        assert torch.equal(y, q.qgemv_iq3(W, g, x))
+        r = q.qgemv_iq3(W, g, x)
+        if M >= 5 and (K // 256) % 8 == 0:
+            assert torch.allclose(y, r, rtol=0, atol=1e-6 * float(r.abs().max()))
+        else:
+            assert torch.equal(y, r)
 
 
 # ------------------------------------------------------------ persistent pass
