@@ -458,9 +458,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 // XP = 1 rounds x to bf16.  Each (row, sub-block, token part) accumulates in
 // its own TMEM column, and the dequantising warps add f_j * (sum of the
 // parts) into registers, a unit behind the MMAs.
-constexpr int kGridX0 = kB0 + 4 * kBStage;       // 33792: grid rows as two bf16 pairs, 8 copies (16 KB)
-constexpr int kSignX0 = kGridX0 + 16384;         // 50176: sign words, 8 copies (4 KB)
-constexpr int kRaw0X = kSignX0 + 4096;           // 54272
+// the grid in 16 copies: a half warp's 8-byte gathers (lane L reads copy
+// L mod 16) fall in 16 distinct bank pairs whatever the grid rows
+constexpr int kGridX0 = kB0 + 4 * kBStage;       // 33792: grid rows as two bf16 pairs, 16 copies (32 KB)
+constexpr int kSignX0 = kGridX0 + 32768;         // 66560: sign words, 8 copies (4 KB)
+constexpr int kRaw0X = kSignX0 + 4096;           // 70656
 constexpr uint32_t kTmDX = 256;                  // D of half h at 256 + 128 h, sub-block j at + 32 j
 
 template <int XP>
@@ -514,10 +516,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         reinterpret_cast<uint4*>(smem + kB0)[i] = make_uint4(0u, 0u, 0u, 0u);
     fence_proxy_async_smem();
     {
-        // grid row r as bf16 pairs (bytes 0,1) (bytes 2,3), 8 copies: row r of copy c at 8 (8 r + c) bytes
+        // grid row r as bf16 pairs (bytes 0,1) (bytes 2,3), 16 copies: row r of copy c at 8 (16 r + c) bytes
         uint2* g2 = reinterpret_cast<uint2*>(smem + kGridX0);
-        for (int i = threadIdx.x; i < 256 * 8; i += kThreads) {
-            const uint8_t* gr = grid + (i >> 3) * 4;
+        for (int i = threadIdx.x; i < 256 * 16; i += kThreads) {
+            const uint8_t* gr = grid + (i >> 4) * 4;
             g2[i] = make_uint2(pack_bf16(gr[0], gr[1]), pack_bf16(gr[2], gr[3]));
         }
         // signs of each 7-bit field: the seven stored ones and their parity
@@ -689,7 +691,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         for (int hf = 0; hf < 2; ++hf) {
                             const int pi = 8 * j + 2 * l + hf;  // index byte within the half
                             const uint32_t idx = (vi[pi >> 2] >> (8 * (pi & 3))) & 0xFFu;
-                            const uint2 g = g2[8 * idx + (t & 7)];
+                            const uint2 g = g2[16 * idx + (t & 15)];
                             w[16 * jj + 4 * l + 2 * hf] = g.x ^ ((T << (2 * hf)) & 0x80008000u);
                             w[16 * jj + 4 * l + 2 * hf + 1] = g.y ^ ((T << (2 * hf + 1)) & 0x80008000u);
                         }
