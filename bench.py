@@ -178,7 +178,7 @@ def cudart():
 _COMMON = ["common.cuh", "gemv_kernel.cuh", "launch.h", "tensor_map.h", "launch_common.cuh",
            "../../include/qgemv.h"]
 KERNEL_SOURCES = {
-    "q4k": _COMMON + ["launch_q4k.cuh", "gemv_q4k8.cuh", "gemv_q4k.cu"],
+    "q4k": _COMMON + ["launch_q4k.cuh", "gemv_q4k.cu"],
     "iq3": _COMMON + ["launch_iq3.cuh", "gemv_iq3.cu"],
     "tc": ["common.cuh", "gemv_kernel.cuh", "launch.h", "tensor_map.h", "../../include/qgemv.h", "gemm_tc.cu"],
     "cb": _COMMON + ["gemv_cb.cu"],
@@ -229,33 +229,23 @@ def job_throughput(world, bytes_per_step, steps, ms):
     return world * bytes_per_step * steps / (ms * 1e-3) / 1e9
 
 
-def q4k_token_groups(M, eight=True):
-    """Token groups of the Q4_K FMA dispatch: 5 to 8 remaining tokens in one
-    8-token pass (no prologue, no residual), otherwise at most 4."""
-    n = m0 = 0
-    while m0 < M:
-        m0 += min(8, M - m0) if eight and M - m0 >= 5 else min(4, M - m0)
-        n += 1
-    return n
-
-
 def kernel_launches(lib, fn, a, M):
     """Kernels of ours that one C-ABI call launches: the FMA paths split M
-    into token groups (Q4_K up to 8 or 4, IQ3 and the IQ4 codebook formats
-    4, the other codebook formats 8), each a launch; the tcgen05 path
-    (M >= 16) and the persistent pass are one launch; IQ3 from 5 tokens below
-    16 (rows a multiple of 16 bytes, every workload here) one tcgen05 launch
-    per matrix and group of at most 10 tokens."""
+    into token groups (Q4_K, IQ3 and the IQ4 codebook formats 4, the other
+    codebook formats 8), each a launch; the batched tcgen05 path (M >= 16)
+    and the persistent pass are one launch; Q4_K (without prologue or
+    residual) and IQ3 (rows a multiple of 16 bytes, every workload here)
+    from 5 tokens below 16 one tcgen05 launch per matrix and group of at most
+    10 tokens."""
     if fn in (lib.qgemm_q4k_batched, lib.qgemm_iq3_batched) and M >= 16:
         return 1
-    if fn in (lib.qgemv_iq3_ex, lib.qgemm_iq3_batched) and M >= 5:
+    if fn in (lib.qgemv_q4k_ex, lib.qgemm_q4k_batched, lib.qgemv_iq3_ex, lib.qgemm_iq3_batched) and M >= 5:
         return (M + 9) // 10
-    if fn == lib.qgemv_iq3_group and M >= 5:
+    if fn in (lib.qgemv_q4k_group, lib.qgemv_iq3_group) and M >= 5:
         return a[3] * ((M + 9) // 10)
-    if fn in (lib.qgemv_q4k_ex, lib.qgemv_q4k_group, lib.qgemm_q4k_batched):
-        return q4k_token_groups(M)
-    if fn in (lib.qgemv_q4k_fused, lib.qgemv_q4k_fused_group):
-        return q4k_token_groups(M, eight=False)
+    if fn in (lib.qgemv_q4k_ex, lib.qgemv_q4k_group, lib.qgemv_q4k_fused, lib.qgemv_q4k_fused_group,
+              lib.qgemm_q4k_batched):
+        return (M + 3) // 4
     if fn in (lib.qgemv_iq3_ex, lib.qgemv_iq3_group, lib.qgemv_iq3xxs_ex, lib.qgemm_iq3_batched):
         return (M + 3) // 4  # rows a multiple of 16 bytes (every workload here)
     if fn == lib.qgemv_codebook:
@@ -619,11 +609,12 @@ def run_ours(args, rank, world, local_rank):
     elif fused:
         kname = "qgemv_q4k_fused qg_gemv_kernel<FmtQ4KT, FUSE>"
     elif mats[0][0] == "q4k":
-        kname = ("qgemm_q4k_batched qg_gemm_tc_kernel<Q4_K> (tcgen05)" if M >= 16 else
+        kname = ("qgemm_q4k_batched qg_gemm_tc_kernel (tcgen05, bf16 weights)" if M >= 16 else
+                 "qgemv_q4k qg_gemm_tc_x_kernel<Q4_K, 3> (tcgen05, x in three bf16 parts)" if M >= 5 else
                  "qgemv_q4k qg_gemv_kernel<FmtQ4KT>")
     elif mats[0][0] == "iq3":
-        kname = ("qgemm_iq3_batched qg_gemm_tc_iq3x_kernel<1> (tcgen05)" if M >= 16 else
-                 "qgemv_iq3 qg_gemm_tc_iq3x_kernel<3> (tcgen05, x in three bf16 parts)" if M >= 5 else
+        kname = ("qgemm_iq3_batched qg_gemm_tc_x_kernel<IQ3, 1> (tcgen05)" if M >= 16 else
+                 "qgemv_iq3 qg_gemm_tc_x_kernel<IQ3, 3> (tcgen05, x in three bf16 parts)" if M >= 5 else
                  "qgemv_iq3 qg_gemv_kernel<FmtIQ3T>")
     elif mats[0][0] == "iq3xxs":
         kname = "qgemv_iq3xxs qg_gemv_kernel<FmtIQ3XXST>"
@@ -639,8 +630,7 @@ def run_ours(args, rank, world, local_rank):
     # can take longer than the weight stream, so the roofline is the lower of
     # the two ceilings; the fp32 peak is the SMs' FMA lanes (128 per SM, 2
     # flops each) at the largest SM clock sampled during the run
-    fma_path = (fused or mats[0][0] not in ("q4k", "iq3") or (mats[0][0] == "q4k" and M < 16)
-                or (mats[0][0] == "iq3" and M < 5))
+    fma_path = fused or mats[0][0] not in ("q4k", "iq3") or M < 5
     if fma_path and 2 <= M <= 15:
         sms = torch.cuda.get_device_properties(dev).multi_processor_count
         mhz = (clocks or {}).get("sm_max_mhz") or 2070.0

@@ -448,30 +448,47 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 
 
-// ------------------------------------------------ IQ3: sub-block factors after the MMA
-// IQ3 (page 4 "iq3_pack.py", decode): w = d*(0.5+code)*0.5 * grid*0.5 *
-// sign = f_j * (+-g), with g a grid byte and f_j = d*(0.5+code)*0.25 the
-// factor of sub-block j.  The MMA takes the signed grid bytes (integers
-// below 256: exact in bf16) and x as XP bf16 parts: XP = 3 splits each x
-// exactly (x = hi + mid + lo, each part rounding the remainder of the one
-// before), so every product is exact and only the fp32 accumulation rounds;
-// XP = 1 rounds x to bf16.  Each (row, sub-block, token part) accumulates in
-// its own TMEM column, and the dequantising warps add f_j * (sum of the
-// parts) into registers, a unit behind the MMAs.
-// the grid in 16 copies: a half warp's 8-byte gathers (lane L reads copy
-// L mod 16) fall in 16 distinct bank pairs whatever the grid rows
-constexpr int kGridX0 = kB0 + 4 * kBStage;       // 33792: grid rows as two bf16 pairs, 16 copies (32 KB)
-constexpr int kSignX0 = kGridX0 + 32768;         // 66560: sign words, 8 copies (4 KB)
-constexpr int kRaw0X = kSignX0 + 4096;           // 70656
+// ------------------------------------ sub-block factors after the MMA
+// Both formats write each weight as a small integer times a per-sub-block
+// factor, and the MMA takes the integers, which bf16 holds exactly:
+//   IQ3 (page 4 "iq3_pack.py", decode): w = d*(0.5+code)*0.5 * grid*0.5 *
+//     sign = f_j * (+-g), g a grid byte, f_j = d*(0.5+code)*0.25;
+//   Q4_K (page 1 "Rewriting picoLM in Python", dequantize_q4_K): w =
+//     a*q - b with a = d*sc, b = dmin*mn of sub-block j; with the offset c
+//     of q4k_offset (the integer nearest b/a) w = a*(q - c) - r, r = b - a*c,
+//     and every term of a*sum((q-c)*x) - r*sum(x) is at most twice |w*x| of
+//     its weight, so cancelling weights keep their accuracy.
+// x enters as XP bf16 parts: XP = 3 splits each x exactly (x = hi + mid +
+// lo, each part rounding the remainder of the one before), so every product
+// is exact and only the fp32 sums round; XP = 1 rounds x to bf16.  Each
+// (row, sub-block, token part) accumulates in its own TMEM column; the
+// dequantising warps then add f_j * S (IQ3) or a_j * S - r_j * X_j (Q4_K; S
+// the sum of the parts, X_j the sub-block's sum of x as the MMA saw it)
+// into registers, a unit behind the MMAs.
+// IQ3 grid in 16 copies: a half warp's 8-byte gathers (lane L reads copy
+// L mod 16) fall in 16 distinct bank pairs whatever the grid rows.
+constexpr int kGridX0 = kB0 + 4 * kBStage;       // 33792: IQ3 grid rows as two bf16 pairs, 16 copies (32 KB)
+constexpr int kSignX0 = kGridX0 + 32768;         // 66560: IQ3 sign words, 8 copies (4 KB)
+constexpr int kRaw0X3 = kSignX0 + 4096;          // 70656: IQ3 raw ring
+constexpr int kXSum0 = kB0 + 4 * kBStage;        // 33792: Q4_K x sums [half][3 slots][4 sub-blocks][32 tokens]
+constexpr int kRaw0XQ = kXSum0 + 2 * 3 * 4 * 32 * 4;  // 36864: Q4_K raw ring
 constexpr uint32_t kTmDX = 256;                  // D of half h at 256 + 128 h, sub-block j at + 32 j
 
-template <int XP>
+__device__ __forceinline__ uint32_t bf16x2_sub(uint32_t a, uint32_t b) {
+    uint32_t r;
+    asm("sub.rn.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+    return r;
+}
+
+template <bool Q4K, int XP>
 __global__ void __launch_bounds__(kThreads, 1)
-    qg_gemm_tc_iq3x_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
-                           const uint8_t* __restrict__ grid, float* __restrict__ Y, int M, int64_t N, int64_t K,
-                           int nraw, unsigned* status) {
+    qg_gemm_tc_x_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
+                        const uint8_t* __restrict__ grid, float* __restrict__ Y, int M, int64_t N, int64_t K,
+                        int nraw, unsigned* status) {
     static_assert(XP == 1 || XP == 3, "x parts");
     constexpr int MT = 32 / XP;  // tokens at most: XP * M columns of D per sub-block
+    constexpr int kRaw0 = Q4K ? kRaw0XQ : kRaw0X3;
+    constexpr int kBox = Q4K ? kBlockBytes : kIQ3Box;
     extern __shared__ __align__(1024) uint8_t smem[];
     uint64_t* raw_full = reinterpret_cast<uint64_t*>(smem);  // [kMaxRaw]
     uint64_t* raw_empty = raw_full + kMaxRaw;                 // [kMaxRaw]
@@ -515,7 +532,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int i = threadIdx.x; i < 4 * kBStage / 16; i += kThreads)
         reinterpret_cast<uint4*>(smem + kB0)[i] = make_uint4(0u, 0u, 0u, 0u);
     fence_proxy_async_smem();
-    {
+    if constexpr (!Q4K) {
         // grid row r as bf16 pairs (bytes 0,1) (bytes 2,3), 16 copies: row r of copy c at 8 (16 r + c) bytes
         uint2* g2 = reinterpret_cast<uint2*>(smem + kGridX0);
         for (int i = threadIdx.x; i < 256 * 16; i += kThreads) {
@@ -549,16 +566,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) {
             const uint64_t pol_w = policy_evict_first();
             const uint64_t pol_x = policy_evict_last();
-            const uint32_t bytes = kTileRows * kIQ3Box + M * 1024;
+            const uint32_t bytes = kTileRows * kBox + M * 1024;
             int s = 0;
             uint32_t round = 0;  // completed passes over the raw ring
             int64_t tile = u_begin / nb;
             int kb = static_cast<int>(u_begin % nb);
             for (int64_t u = u_begin; u < u_end; ++u) {
                 if (u - u_begin >= nraw) mbar_wait_bounded(&raw_empty[s], (round - 1) & 1u, status);
-                uint8_t* raw = smem + kRaw0X + s * rstage;
+                uint8_t* raw = smem + kRaw0 + s * rstage;
                 mbar_arrive_expect_tx(&raw_full[s], bytes);
-                tma_load_2d(raw, &tmW, (kb * 98) & ~15, static_cast<int>(tile * kTileRows), &raw_full[s], pol_w);
+                const int bx = Q4K ? kb * kBlockBytes : (kb * 98) & ~15;  // x * 1 byte: 16-byte aligned
+                tma_load_2d(raw, &tmW, bx, static_cast<int>(tile * kTileRows), &raw_full[s], pol_w);
                 tma_load_2d(raw + kRawW, &tmX, kb * 256, 0, &raw_full[s], pol_x);
                 if (++s == nraw) {
                     s = 0;
@@ -607,20 +625,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int half = warp >> 2;
         const int t = threadIdx.x & 127;
         const uint32_t tl = static_cast<uint32_t>(32 * (warp & 3)) << 16;
-        const uint2* g2 = reinterpret_cast<const uint2*>(smem + kGridX0);
-        const uint32_t* sgn = reinterpret_cast<const uint32_t*>(smem + kSignX0);
+        float* xsum = reinterpret_cast<float*>(smem + kXSum0) + half * (3 * 4 * 32);  // Q4_K: [slot][sub-block][token]
         float acc[MT];
 #pragma unroll
         for (int m = 0; m < MT; ++m) acc[m] = 0.f;
-        float fp[4] = {0.f, 0.f, 0.f, 0.f};  // the previous unit's sub-block factors
+        float fp[4] = {0.f, 0.f, 0.f, 0.f};  // the previous unit's sub-block factors (IQ3 f, Q4_K a)
+        float rp[4] = {0.f, 0.f, 0.f, 0.f};  // and Q4_K offsets' remainders r
         int64_t prow0 = 0;
         int prows = 0;
         bool plast = false;
-        // the previous unit's sums: f_j * (sum of the parts) into acc; at a
-        // segment's end acc goes into Y
+        // the previous unit's sums into acc; at a segment's end acc goes into Y
         auto drain = [&](int64_t ip) {
             mbar_wait_bounded(&d_full[half], static_cast<uint32_t>(ip & 1), status);
             tc_fence_after();
+            const float* xs = xsum + static_cast<int>(ip % 3) * (4 * 32);
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
                 float v[32];
@@ -634,6 +652,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int m = 0; m < MT; ++m) {
                     const float sm = XP == 1 ? v[m] : v[3 * m] + (v[3 * m + 1] + v[3 * m + 2]);
                     acc[m] = fmaf(fp[j], sm, acc[m]);
+                    if constexpr (Q4K) acc[m] = fmaf(-rp[j], xs[j * 32 + m], acc[m]);
                 }
             }
             if (plast) {
@@ -657,67 +676,123 @@ __global__ void __launch_bounds__(kThreads, 1)
             const bool last = (u == u_end - 1) || kb == nb - 1;
             const int64_t row0 = tile * kTileRows;
             const int rows = static_cast<int>(min64(kTileRows, N - row0));
-            const uint8_t* raw = smem + kRaw0X + s * rstage;
+            const uint8_t* raw = smem + kRaw0 + s * rstage;
             const float* xr = reinterpret_cast<const float*>(raw + kRawW);
             mbar_wait_bounded(&raw_full[s], rphase, status);
             // buffer b of this half was last read by the MMAs of unit i - 2
             if (i >= 2) mbar_wait_bounded(&op_empty[2 * half + b], static_cast<uint32_t>(((i >> 1) - 1) & 1), status);
             tc_fence_after();
-            uint32_t vi[8], vs[4], dbits;
-            switch (kb & 7) {  // the block's offset in its box: (98 * kb) mod 16
+            const uint32_t ta = tmem + tl + kTmA + 64u * static_cast<uint32_t>(2 * half + b);
+            float f[4], r[4];
+            if constexpr (Q4K) {
+                // row t's sub-blocks 4 half .. 4 half + 3: a = d*sc, b = dmin*mn, offset c, r = b - a*c
+                const uint8_t* blk = raw + t * kBlockBytes;
+                const uint4 hd = *reinterpret_cast<const uint4*>(blk);
+                const float d = h2f(hd.x), dmin = h2f(hd.x >> 16);
+                uint32_t sc03, mn03, sc47, mn47;
+                q4k_scale_min_words(hd.y, hd.z, hd.w, sc03, mn03, sc47, mn47);
+                const uint32_t scw = half == 0 ? sc03 : sc47, mnw = half == 0 ? mn03 : mn47;
+                uint32_t cneg[4];  // bf16 pairs of 128 + c
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const float a = d * byte_f(scw, j), bb = dmin * byte_f(mnw, j);
+                    const float c = q4k_offset(a, bb);
+                    f[j] = a;
+                    r[j] = bb - a * c;
+                    cneg[j] = (0x4300u | static_cast<uint32_t>(c)) * 0x10001u;
+                }
+                // q - c as bf16: a byte permute puts q next to 0x43 (bf16 128 + q),
+                // and one bf16x2 subtraction takes 128 + c off, both exact
+#pragma unroll
+                for (int gg = 0; gg < 2; ++gg) {  // sub-blocks 2gg (low nibbles) and 2gg + 1 (high)
+                    const uint4 q0 = *reinterpret_cast<const uint4*>(blk + 16 + 64 * half + 32 * gg);
+                    const uint4 q1 = *reinterpret_cast<const uint4*>(blk + 16 + 64 * half + 32 * gg + 16);
+                    const uint32_t qv[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
+                    uint32_t w[32];  // k 64gg .. 64gg + 63 of the half
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        const uint32_t L = qv[e] & 0x0F0F0F0Fu, H = (qv[e] >> 4) & 0x0F0F0F0Fu;
+                        w[2 * e] = bf16x2_sub(prmt(L, 0x43434343u, 0x4140u), cneg[2 * gg]);
+                        w[2 * e + 1] = bf16x2_sub(prmt(L, 0x43434343u, 0x4342u), cneg[2 * gg]);
+                        w[16 + 2 * e] = bf16x2_sub(prmt(H, 0x43434343u, 0x4140u), cneg[2 * gg + 1]);
+                        w[16 + 2 * e + 1] = bf16x2_sub(prmt(H, 0x43434343u, 0x4342u), cneg[2 * gg + 1]);
+                    }
+                    tmem_st32(ta + 32 * gg, w);
+                }
+            } else {
+                const uint2* g2 = reinterpret_cast<const uint2*>(smem + kGridX0);
+                const uint32_t* sgn = reinterpret_cast<const uint32_t*>(smem + kSignX0);
+                uint32_t vi[8], vs[4], dbits;
+                switch (kb & 7) {  // the block's offset in its box: (98 * kb) mod 16
 #define QG_TC_IQ3X(C) \
     case C: iq3_load_half<FmtIQ3T, C>(raw + t * kIQ3Box, half, vi, vs, dbits); break;
-                QG_TC_IQ3X(0) QG_TC_IQ3X(1) QG_TC_IQ3X(2) QG_TC_IQ3X(3)
-                QG_TC_IQ3X(4) QG_TC_IQ3X(5) QG_TC_IQ3X(6) QG_TC_IQ3X(7)
+                    QG_TC_IQ3X(0) QG_TC_IQ3X(1) QG_TC_IQ3X(2) QG_TC_IQ3X(3)
+                    QG_TC_IQ3X(4) QG_TC_IQ3X(5) QG_TC_IQ3X(6) QG_TC_IQ3X(7)
 #undef QG_TC_IQ3X
-            }
-            const float d = h2f(dbits);
-            float f[4];
+                }
+                const float d = h2f(dbits);
 #pragma unroll
-            for (int j = 0; j < 4; ++j) f[j] = d * (static_cast<float>(vs[j] >> 28) + 0.5f) * 0.25f;
-            // the signed grid bytes as bf16, sub-block j at columns 16 j .. 16 j + 15
-            const uint32_t ta = tmem + tl + kTmA + 64u * static_cast<uint32_t>(2 * half + b);
+                for (int j = 0; j < 4; ++j) {
+                    f[j] = d * (static_cast<float>(vs[j] >> 28) + 0.5f) * 0.25f;
+                    r[j] = 0.f;
+                }
+                // the signed grid bytes as bf16, sub-block j at columns 16 j .. 16 j + 15
 #pragma unroll
-            for (int jp = 0; jp < 2; ++jp) {
-                uint32_t w[32];
+                for (int jp = 0; jp < 2; ++jp) {
+                    uint32_t w[32];
 #pragma unroll
-                for (int jj = 0; jj < 2; ++jj) {
-                    const int j = 2 * jp + jj;
-                    const uint32_t sw = vs[j];
+                    for (int jj = 0; jj < 2; ++jj) {
+                        const int j = 2 * jp + jj;
+                        const uint32_t sw = vs[j];
 #pragma unroll
-                    for (int l = 0; l < 4; ++l) {
-                        const uint32_t T = sgn[8 * ((sw >> (7 * l)) & 0x7Fu) + (t & 7)];
+                        for (int l = 0; l < 4; ++l) {
+                            const uint32_t T = sgn[8 * ((sw >> (7 * l)) & 0x7Fu) + (t & 7)];
 #pragma unroll
-                        for (int hf = 0; hf < 2; ++hf) {
-                            const int pi = 8 * j + 2 * l + hf;  // index byte within the half
-                            const uint32_t idx = (vi[pi >> 2] >> (8 * (pi & 3))) & 0xFFu;
-                            const uint2 g = g2[16 * idx + (t & 15)];
-                            w[16 * jj + 4 * l + 2 * hf] = g.x ^ ((T << (2 * hf)) & 0x80008000u);
-                            w[16 * jj + 4 * l + 2 * hf + 1] = g.y ^ ((T << (2 * hf + 1)) & 0x80008000u);
+                            for (int hf = 0; hf < 2; ++hf) {
+                                const int pi = 8 * j + 2 * l + hf;  // index byte within the half
+                                const uint32_t idx = (vi[pi >> 2] >> (8 * (pi & 3))) & 0xFFu;
+                                const uint2 g = g2[16 * idx + (t & 15)];
+                                w[16 * jj + 4 * l + 2 * hf] = g.x ^ ((T << (2 * hf)) & 0x80008000u);
+                                w[16 * jj + 4 * l + 2 * hf + 1] = g.y ^ ((T << (2 * hf + 1)) & 0x80008000u);
+                            }
                         }
                     }
+                    tmem_st32(ta + 32 * jp, w);
                 }
-                tmem_st32(ta + 32 * jp, w);
             }
-            // x -> XP bf16 parts, part p of token m in row XP m + p
+            // x -> XP bf16 parts, part p of token m in row XP m + p; Q4_K also
+            // the sums of x as the MMA sees it per (token, sub-block): the four
+            // chunks of a sub-block are four consecutive lanes
             {
                 uint8_t* xs = smem + kB0 + (2 * half + b) * kBStage;
-                for (int c = t; c < M * 16; c += 128) {
-                    const int m = c >> 4, j = c & 15;
-                    const float4 a = *reinterpret_cast<const float4*>(xr + m * 256 + 128 * half + 8 * j);
-                    const float4 q = *reinterpret_cast<const float4*>(xr + m * 256 + 128 * half + 8 * j + 4);
-                    float v[8] = {a.x, a.y, a.z, a.w, q.x, q.y, q.z, q.w};
+                float* xsw = xsum + static_cast<int>(i % 3) * (4 * 32);
+                for (int n = 0; n < (M * 16 + 127) / 128; ++n) {  // the same trip count in every lane
+                    const int c = t + 128 * n, m = c >> 4, j = c & 15;
+                    float part = 0.f;
+                    if (m < M) {
+                        const float4 a = *reinterpret_cast<const float4*>(xr + m * 256 + 128 * half + 8 * j);
+                        const float4 q = *reinterpret_cast<const float4*>(xr + m * 256 + 128 * half + 8 * j + 4);
+                        float v[8] = {a.x, a.y, a.z, a.w, q.x, q.y, q.z, q.w};
+                        if constexpr (Q4K && XP == 3) part = ((v[0] + v[1]) + (v[2] + v[3])) + ((v[4] + v[5]) + (v[6] + v[7]));
 #pragma unroll
-                    for (int p = 0; p < XP; ++p) {
-                        uint32_t w4[4];
+                        for (int p = 0; p < XP; ++p) {
+                            uint32_t w4[4];
 #pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            w4[e] = pack_bf16(v[2 * e], v[2 * e + 1]);
-                            // the remainder is exact in fp32 (Sterbenz)
-                            v[2 * e] -= __uint_as_float(w4[e] << 16);
-                            v[2 * e + 1] -= __uint_as_float(w4[e] & 0xFFFF0000u);
+                            for (int e = 0; e < 4; ++e) {
+                                w4[e] = pack_bf16(v[2 * e], v[2 * e + 1]);
+                                const float lo = __uint_as_float(w4[e] << 16), hi = __uint_as_float(w4[e] & 0xFFFF0000u);
+                                if constexpr (Q4K && XP == 1) part += lo + hi;
+                                // the remainder is exact in fp32 (Sterbenz)
+                                v[2 * e] -= lo;
+                                v[2 * e + 1] -= hi;
+                            }
+                            *reinterpret_cast<uint4*>(xs + x_off(XP * m + p, j)) = make_uint4(w4[0], w4[1], w4[2], w4[3]);
                         }
-                        *reinterpret_cast<uint4*>(xs + x_off(XP * m + p, j)) = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+                    }
+                    if constexpr (Q4K) {
+                        part += __shfl_xor_sync(0xffffffffu, part, 1);
+                        part += __shfl_xor_sync(0xffffffffu, part, 2);
+                        if (m < M && (j & 3) == 0) xsw[(j >> 2) * 32 + m] = part;
                     }
                 }
             }
@@ -729,9 +804,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                 arrive(&op_full[2 * half + b]);
                 arrive(&raw_empty[s]);
             }
+            // Q4_K: this unit's x sums for the whole half (three slots: a thread
+            // rewrites slot (i + 1) mod 3 only after every thread of the half
+            // passed this barrier, that is, left the drain of unit i - 2)
+            if constexpr (Q4K) named_barrier_sync<128>(1 + half);
             if (i >= 1) drain(i - 1);
 #pragma unroll
-            for (int j = 0; j < 4; ++j) fp[j] = f[j];
+            for (int j = 0; j < 4; ++j) {
+                fp[j] = f[j];
+                rp[j] = r[j];
+            }
             plast = last;
             prow0 = row0;
             prows = rows;
@@ -760,20 +842,20 @@ namespace {
 
 // Both formats: W viewed as [N rows][pitch bytes] with a box of one block
 // column (Q4_K 144 bytes; IQ3 112 bytes) x 128 rows; X [M][K] fp32 with a
-// box of 256 k x M tokens.  KIND 0: Q4_K (bf16 weights, 16 <= M <= 32);
-// KIND 1 / 3: IQ3 with the sub-block factors after the MMA and x in 1 / 3
-// bf16 parts (KIND * M <= 32).
-template <int KIND>
+// box of 256 k x M tokens.  FMT 0: Q4_K with weights rounded to bf16
+// (qg_gemm_tc_kernel, 16 <= M <= 32); FMT 1 / 2: IQ3 / Q4_K with the
+// sub-block factors after the MMA and x in XP bf16 parts (XP * M <= 32).
+template <int FMT, int XP>
 int launch_tc(const uint8_t* W, const uint8_t* grid, const float* X, float* Y, int M, int64_t N, int64_t K,
               cudaStream_t s, unsigned* status) {
-    constexpr bool IQ3 = KIND != 0;
-    if (KIND == 0 ? (M < 16 || M > 32) : (M < 1 || KIND * M > 32)) return QG_EINVAL;
+    constexpr bool IQ3 = FMT == 1;
+    if (FMT == 0 ? (M < 16 || M > 32) : (M < 1 || XP * M > 32)) return QG_EINVAL;
     static std::atomic<bool> attr_done[64];
     int dev = -1;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return qg::cuda_fail(cudaGetLastError());
-    auto kern = KIND == 0 ? tc::qg_gemm_tc_kernel : tc::qg_gemm_tc_iq3x_kernel<KIND == 0 ? 1 : KIND>;
+    auto kern = FMT == 0 ? tc::qg_gemm_tc_kernel : tc::qg_gemm_tc_x_kernel<FMT == 2, XP>;
     // as many raw stages as fit (the x part of a stage is M KB)
-    const int raw0 = IQ3 ? tc::kRaw0X : tc::kRaw0Q4K;
+    const int raw0 = FMT == 0 ? tc::kRaw0Q4K : IQ3 ? tc::kRaw0X3 : tc::kRaw0XQ;
     const int nraw = std::min(tc::kMaxRaw, (tc::kSmemMax - raw0) / tc::raw_stage_bytes(M));
     if (nraw < 2) return QG_EINVAL;
     const int smem = raw0 + nraw * tc::raw_stage_bytes(M);
@@ -813,21 +895,28 @@ int launch_tc(const uint8_t* W, const uint8_t* grid, const float* X, float* Y, i
 
 int launch_gemm_q4k_tc(const uint8_t* W, const float* X, float* Y, int M, int64_t N, int64_t K, cudaStream_t s,
                        unsigned* status) {
-    return launch_tc<0>(W, nullptr, X, Y, M, N, K, s, status);
+    return launch_tc<0, 1>(W, nullptr, X, Y, M, N, K, s, status);
 }
 
 // IQ3 needs 16-byte aligned rows (K/256 a multiple of 8) for its tensor map.
 int launch_gemm_iq3_tc(const uint8_t* W, const uint8_t* grid, const float* X, float* Y, int M, int64_t N, int64_t K,
                        cudaStream_t s, unsigned* status) {
     if ((K / 256) % 8 != 0) return QG_EINVAL;
-    return launch_tc<1>(W, grid, X, Y, M, N, K, s, status);
+    return launch_tc<1, 1>(W, grid, X, Y, M, N, K, s, status);
 }
 
 // IQ3, 1 <= M <= 10, x in three bf16 parts: every product exact, fp32 sums.
 int launch_gemm_iq3_tc3(const uint8_t* W, const uint8_t* grid, const float* X, float* Y, int M, int64_t N, int64_t K,
                         cudaStream_t s, unsigned* status) {
     if ((K / 256) % 8 != 0) return QG_EINVAL;
-    return launch_tc<3>(W, grid, X, Y, M, N, K, s, status);
+    return launch_tc<1, 3>(W, grid, X, Y, M, N, K, s, status);
+}
+
+// Q4_K, 1 <= M <= 10, x in three bf16 parts: every product exact, fp32 sums,
+// the offset factoring of the FMA path.
+int launch_gemm_q4k_tc3(const uint8_t* W, const float* X, float* Y, int M, int64_t N, int64_t K, cudaStream_t s,
+                        unsigned* status) {
+    return launch_tc<2, 3>(W, nullptr, X, Y, M, N, K, s, status);
 }
 
 }  // namespace qg

@@ -57,5 +57,9 @@ int launch_gemm_iq3_tc(const uint8_t* W, const uint8_t* grid, const float* X, fl
 // exact products, fp32 accumulation (the fp32 FMA path's bar)
 int launch_gemm_iq3_tc3(const uint8_t* W, const uint8_t* grid, const float* X, float* Y, int M, int64_t N, int64_t K,
                         cudaStream_t s, unsigned* status);
+// tcgen05 Q4_K the same way, 1 <= M <= 10: A = q - c (the offset of the FMA
+// path's exact factoring), a * sum - r * sum(x) per sub-block afterwards
+int launch_gemm_q4k_tc3(const uint8_t* W, const float* X, float* Y, int M, int64_t N, int64_t K, cudaStream_t s,
+                        unsigned* status);
 
 }  // namespace qg

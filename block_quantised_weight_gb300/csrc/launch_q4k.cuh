@@ -1,16 +1,16 @@
 // Q4_K GEMV dispatch (fp32 FMA path), shared by the plain and the fused
 // translation units.  Kernel: gemv_kernel.cuh.
 #pragma once
-#include "gemv_q4k8.cuh"
 #include "launch_common.cuh"
 
 namespace qg {
 
 // count matrices sharing X; M is split into token groups, each streaming W
-// once: groups of 5 to 8 tokens run the 8-warp kernel of gemv_q4k8.cuh
-// (no prologue, no residual), the rest groups of at most 4.  FUSE != 0 (a
-// prologue on x) needs M <= 4: the staged-x kernels apply it.  fz may carry
-// residuals with any FUSE.
+// once: from 5 tokens without prologue or residual the tcgen05 kernel of
+// gemm_tc.cu (groups of 5 to 10, x in three exact bf16 parts, the FMA
+// path's offset factoring), otherwise groups of at most 4 on the fp32 FMA
+// kernels.  FUSE != 0 (a prologue on x) needs M <= 4: the staged-x kernels
+// apply it.  fz may carry residuals with any FUSE.
 template <int FUSE>
 int launch_group_q4k_t(const uint8_t* const* W, float* const* Y, const int64_t* N, int count, const float* X, int M,
                        int64_t K, cudaStream_t s, unsigned* status, unsigned flags, const Fuse* fz) {
@@ -32,15 +32,23 @@ int launch_group_q4k_t(const uint8_t* const* W, float* const* Y, const int64_t* 
     bool residual = false;
     if (fz)
         for (int i = 0; i < count; ++i) residual = residual || fz->R[i] != nullptr;
+    if (FUSE == 0 && !residual && M >= 5) {
+        // 5 or more tokens: the tensor cores, x split exactly into three bf16
+        // parts (gemm_tc.cu), in ceil(M / 10) balanced token groups of 5 to
+        // 10, one pass over W each
+        const int ng = (M + 9) / 10;
+        for (int g = 0; g < ng; ++g) {
+            const int m0 = M * g / ng, m1 = M * (g + 1) / ng;
+            for (int i = 0; i < count; ++i) {
+                const int rc = launch_gemm_q4k_tc3(W[i], X + static_cast<int64_t>(m0) * K,
+                                                   Y[i] + static_cast<int64_t>(m0) * N[i], m1 - m0, N[i], K, s, status);
+                if (rc != QG_OK) return rc;
+            }
+        }
+        return QG_OK;
+    }
     for (int m0 = 0; m0 < M;) {
         const float* Xg = X + static_cast<int64_t>(m0) * K;
-        if (FUSE == 0 && !residual && M - m0 >= 5) {  // 5 to 8 tokens in one pass
-            const int mg = std::min(8, M - m0);
-            const int rc = launch_gemv8(W, Y, N, count, m0, Xg, mg, K, s, status, dev, flags);
-            if (rc != QG_OK) return rc;
-            m0 += mg;
-            continue;
-        }
         const int mg = std::min(4, M - m0);
         int rc;
         if (mg == 1 && csize > 1)

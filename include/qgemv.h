@@ -79,21 +79,27 @@ extern "C" {
 #define QG_API
 #endif
 
-/* Q4_K GEMV, fp32 FMA path, 1 <= M <= 32.
+/* Q4_K GEMV, 1 <= M <= 32.
  * Page 1 "Rewriting picoLM in Python", dequantize_q4_K (format) and
  * model_forward's matmul (operation).
  * W: N*K/256*144 bytes.  X: M*K floats.  Y: M*N floats (output).
- * Numerics: |Y - exact| <= 1e-5 * sum_k |w*x| per element (fp32 FMA).
+ * Numerics: |Y - exact| <= 1e-5 * sum_k |w*x| per element.
  * Each 32-weight sub-block is summed as a*sum((q - c)*x) - (b - a*c)*sum(x),
  * a = d*sc, b = dmin*mn, c the integer in [0, 15] nearest b/a, so sub-blocks
  * whose d*sc*q and dmin*mn cancel keep that accuracy (a row of zero weights
- * gives exactly 0).  Range: every finite x; slices of 256 x values whose
- * largest |x| lies outside [2^-24, 2^39) take a slower rescaled decode (a
- * power of two in, its inverse out), so the outputs are only limited by
- * fp32 itself.  M > 4 is processed in groups of 4 tokens, each group
- * streaming W once.  The same holds for qgemv_q4k_group, qgemv_q4k_fused
- * (its RMSNorm prologue sums x^2 in fp32: |x| below 2^63) and
- * qgemv_q4k_pass. */
+ * gives exactly 0).  Up to 4 tokens: the fp32 FMA path; range: every finite
+ * x (slices of 256 x values whose largest |x| lies outside [2^-24, 2^39)
+ * take a slower rescaled decode, a power of two in, its inverse out), so the
+ * outputs are only limited by fp32 itself.  From 5 tokens: the tcgen05
+ * tensor cores in groups of 5 to 10 tokens, each streaming W once, with the
+ * same factoring: q - c enters the MMA exactly (bf16) and x split exactly
+ * into three bf16 parts, so every product is exact and the sums are fp32 in
+ * tensor memory; there x is multiplied as given (|x| within [2^-100,
+ * 2^100]), Y is zeroed on `stream` and row sums that different CTAs share
+ * are added with fp32 atomics, so repeated calls may differ in the last
+ * bits.  The same holds for qgemv_q4k_group; qgemv_q4k_fused (its RMSNorm
+ * prologue sums x^2 in fp32: |x| below 2^63) and qgemv_q4k_pass keep the
+ * FMA path. */
 QG_API int qgemv_q4k(const uint8_t* W, const float* X, float* Y, int M, int64_t N, int64_t K, cudaStream_t stream);
 
 /* qgemv_q4k with launch flags (0 or QG_PREFETCH_WEIGHTS); other flag bits:
@@ -190,7 +196,9 @@ QG_API int qdequant_codebook(int format, const uint8_t* W, const void* codebook,
  * output) in one launch: Y[i] = X * dequant(W[i])^T for i < count,
  * 1 <= count <= QG_MAX_GROUP.  W, Y and N are HOST arrays holding device
  * pointers and row counts; Y[i] is [M][N[i]].  Same K for every matrix.
- * Results are identical to count separate qgemv_q4k_ex calls.  Page 1
+ * Results are identical to count separate qgemv_q4k_ex calls (from 5
+ * tokens, the tensor-core path, each matrix is its own launch and the two
+ * agree up to the order of the fp32 atomics).  Page 1
  * "Rewriting picoLM in Python", model_forward (the q/k/v and gate/up
  * matmuls of one layer consume the same normalised activation). */
 QG_API int qgemv_q4k_group(const uint8_t* const* W, float* const* Y, const int64_t* N, int count, const float* X,
@@ -302,14 +310,14 @@ QG_API int qgemv_q4k_pass(const qg_stage* stages, int nstages, int M, unsigned* 
 QG_API int qgemv_q4k_pass_noalloc(const qg_stage* stages, int nstages, int M, cudaStream_t stream);
 
 /* Batched Q4_K GEMM for decode batches, 1 <= M <= 32.
- * Same operation and layouts as qgemv_q4k.  M < 16 runs the fp32 FMA path
- * (tolerance 1e-5 * sum|w*x|); M >= 16 dequantises W tiles to bf16 (round to
+ * Same operation and layouts as qgemv_q4k.  M < 16 runs the paths of
+ * qgemv_q4k (tolerance 1e-5 * sum|w*x|); M >= 16 dequantises W tiles to bf16 (round to
  * nearest even) in shared memory and multiplies on the tcgen05 tensor cores
  * with fp32 accumulation in tensor memory, X also rounded to bf16
  * (tolerance 4e-3 * sum|w*x|, for |x| within [2^-100, 2^100]: bf16 keeps
  * fp32's exponent range but not its subnormals).  On this path Y is zeroed on `stream` and the
  * row sums of K ranges that different CTAs share are added into it with fp32
- * atomics, so repeated calls may differ in the last bits (the FMA paths are
+ * atomics, so repeated calls may differ in the last bits (the FMA path is
  * deterministic). */
 QG_API int qgemm_q4k_batched(const uint8_t* W, const float* X, float* Y, int M, int64_t N, int64_t K, cudaStream_t stream);
 

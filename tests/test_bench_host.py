@@ -21,9 +21,10 @@ def _fake_lib():
 def test_kernel_launches_follow_the_token_groups():
     lib = _fake_lib()
     kl = bench.kernel_launches
-    # Q4_K FMA path: 5 to 8 remaining tokens in one 8-token pass, otherwise
-    # groups of at most 4; tcgen05 from 16 tokens: one launch
-    assert [kl(lib, lib.qgemv_q4k_ex, (), m) for m in (1, 4, 5, 8, 9, 12, 13)] == [1, 1, 1, 1, 2, 2, 2]
+    # Q4_K: groups of at most 4 tokens up to 4; from 5 (no prologue or
+    # residual) tcgen05 per matrix and group of <= 10; batched from 16: one launch
+    assert [kl(lib, lib.qgemv_q4k_ex, (), m) for m in (1, 4, 5, 8, 10, 11, 15)] == [1, 1, 1, 1, 1, 2, 2]
+    assert [kl(lib, lib.qgemv_q4k_group, (None, None, None, 3), m) for m in (3, 5, 13)] == [1, 3, 6]
     assert kl(lib, lib.qgemm_q4k_batched, (), 8) == 1
     assert kl(lib, lib.qgemm_q4k_batched, (), 16) == 1
     assert kl(lib, lib.qgemv_q4k_fused_group, (), 3) == 1

@@ -81,7 +81,7 @@ Q4K_SHAPES = [(1, 256), (31, 256), (33, 512), (100, 2304), (64, 2048), (257, 409
 
 
 @pytest.mark.parametrize("N,K", Q4K_SHAPES)
-@pytest.mark.parametrize("M", [1, 2, 3, 4, 5, 7, 8])   # 5-8: one pass of the 8-token kernel
+@pytest.mark.parametrize("M", [1, 2, 3, 4, 5, 7, 8])   # 5-8: the tensor cores, x in three bf16 parts
 def test_gemv_q4k_small(q, N, K, M):
     W = synth.gen_q4k(N, K, 7 * N + K)
     x = synth.gen_x(M, K, 3 + M)
@@ -253,12 +253,14 @@ def test_binding_raises_on_bad_arguments(q):
 
 
 # ------------------------------------------------------------ dependent launch
-@pytest.mark.parametrize("fmt,M", [("q4k", 1), ("iq3", 1), ("q4k", 8)])   # q4k 8: the one-pass 8-token kernel
+@pytest.mark.parametrize("fmt,M", [("q4k", 1), ("iq3", 1), ("q4k", 4), ("q4k", 8)])   # q4k 8: tensor cores
 def test_prefetch_flag_dependency_chain(q, fmt, M):
     """x_{i+1} = y_i through six square GEMVs issued back to back on one stream.
     With QG_PREFETCH_WEIGHTS each launch may start before its predecessor ends;
     the results must equal the plain stream-ordered launches bit for bit and
-    match the oracle stage by stage."""
+    match the oracle stage by stage.  From 5 tokens the tensor-core path runs
+    (the flag changes nothing there) and its split rows meet in fp32 atomics,
+    so the two chains agree to the order of those additions."""
     K = N = 2048
     mats = []
     for i in range(6):
@@ -283,7 +285,10 @@ def test_prefetch_flag_dependency_chain(q, fmt, M):
     plain = chain(0)
     fast = chain(q.QG_PREFETCH_WEIGHTS)
     for a, b in zip(plain, fast):
-        assert torch.equal(a, b)
+        if M >= 5:
+            assert torch.allclose(a, b, rtol=0, atol=1e-6 * float(a.abs().max()))
+        else:
+            assert torch.equal(a, b)
     # each stage on the oracle's own chain of inputs (fp32 of the oracle's
     # previous output / 32), with and without the flag
     xin = x0.cpu().numpy().reshape(M, K)
@@ -312,13 +317,18 @@ def test_prefetch_flag_rejects_unknown_bits(q):
 @pytest.mark.parametrize("M", [1, 3, 9])
 def test_q4k_group_matches_single_calls(q, M):
     """q, k, v of one TinyLlama layer (2048x2048, 256x2048, 256x2048) in one
-    launch, reading the same x: identical to three separate launches."""
+    launch, reading the same x: identical to three separate launches (from 5
+    tokens, the tensor-core path, up to the order of its fp32 atomics)."""
     K = 2048
     Ws = [dev(synth.gen_q4k(N, K, 50 + N + i)) for i, N in enumerate((2048, 256, 256))]
     x = dev(synth.gen_x(M, K, 11))
     ys = q.qgemv_q4k_group(Ws, x)
     for W, y in zip(Ws, ys):
-        assert torch.equal(y, q.qgemv_q4k(W, x))
+        r = q.qgemv_q4k(W, x)
+        if M >= 5:
+            assert torch.allclose(y, r, rtol=0, atol=1e-6 * float(r.abs().max()))
+        else:
+            assert torch.equal(y, r)
         Y, A = oracle.gemv_q4k(W.cpu().numpy(), x.cpu().numpy(), rows=np.arange(0, W.numel() // 1152, 7))
         check_tol(y.cpu().numpy()[:, ::7], Y, A, TAU_FMA, "group")
 

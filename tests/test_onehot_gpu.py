@@ -95,7 +95,7 @@ Q4K_SHAPES = [(70, 4096), (2048, 18432), (9728, 4096)]
 
 
 @pytest.mark.parametrize("N,K", Q4K_SHAPES)
-@pytest.mark.parametrize("group", [1, 6, 32])   # token groups of 1; 6 in one 8-token pass; four of 8
+@pytest.mark.parametrize("group", [1, 6, 32])   # token groups of 1; 6 and 32 (4 x 8) on the tensor cores
 def test_onehot_q4k(q, N, K, group):
     W = synth.gen_q4k(N, K, N + K)
     Wd = oracle.dequant_q4k(W, K)
@@ -104,7 +104,7 @@ def test_onehot_q4k(q, N, K, group):
 
 
 @pytest.mark.parametrize("value", [2.0 ** 60, 2.0 ** -100])
-@pytest.mark.parametrize("group", [1, 4, 8])   # 8: the one-pass 8-token kernel
+@pytest.mark.parametrize("group", [1, 4, 8])   # 8: the tensor cores (x in three bf16 parts)
 def test_onehot_q4k_rescaled_x(q, value, group):
     """x far outside [2^-24, 2^39): the column is rescaled by 2^-e and its sums by 2^e."""
     N, K = 70, 2048
