@@ -480,13 +480,16 @@ __device__ __forceinline__ uint32_t bf16x2_sub(uint32_t a, uint32_t b) {
     return r;
 }
 
-template <bool Q4K, int XP>
+// MT: the tokens a launch may carry (XP * MT <= 32 columns of D per
+// sub-block), a compile-time bound so that the per-unit sums touch only
+// those columns.
+template <bool Q4K, int XP, int MT>
 __global__ void __launch_bounds__(kThreads, 1)
     qg_gemm_tc_x_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
                         const uint8_t* __restrict__ grid, float* __restrict__ Y, int M, int64_t N, int64_t K,
                         int nraw, unsigned* status) {
     static_assert(XP == 1 || XP == 3, "x parts");
-    constexpr int MT = 32 / XP;  // tokens at most: XP * M columns of D per sub-block
+    static_assert(XP * MT <= 32 && MT % 2 == 0, "tokens per launch");
     constexpr int kRaw0 = Q4K ? kRaw0XQ : kRaw0X3;
     constexpr int kBox = Q4K ? kBlockBytes : kIQ3Box;
     extern __shared__ __align__(1024) uint8_t smem[];
@@ -649,10 +652,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (lane == 0) arrive(&d_empty[half]);
                 }
 #pragma unroll
-                for (int m = 0; m < MT; ++m) {
-                    const float sm = XP == 1 ? v[m] : v[3 * m] + (v[3 * m + 1] + v[3 * m + 2]);
-                    acc[m] = fmaf(fp[j], sm, acc[m]);
-                    if constexpr (Q4K) acc[m] = fmaf(-rp[j], xs[j * 32 + m], acc[m]);
+                for (int m = 0; m < MT; m += 2) {
+                    const float s0 = XP == 1 ? v[m] : v[3 * m] + (v[3 * m + 1] + v[3 * m + 2]);
+                    const float s1 = XP == 1 ? v[m + 1] : v[3 * m + 3] + (v[3 * m + 4] + v[3 * m + 5]);
+                    acc[m] = fmaf(fp[j], s0, acc[m]);
+                    acc[m + 1] = fmaf(fp[j], s1, acc[m + 1]);
+                    if constexpr (Q4K) {
+                        const float2 xx = *reinterpret_cast<const float2*>(xs + j * 32 + m);
+                        acc[m] = fmaf(-rp[j], xx.x, acc[m]);
+                        acc[m + 1] = fmaf(-rp[j], xx.y, acc[m + 1]);
+                    }
                 }
             }
             if (plast) {
@@ -850,19 +859,25 @@ int launch_tc(const uint8_t* W, const uint8_t* grid, const float* X, float* Y, i
               cudaStream_t s, unsigned* status) {
     constexpr bool IQ3 = FMT == 1;
     if (FMT == 0 ? (M < 16 || M > 32) : (M < 1 || XP * M > 32)) return QG_EINVAL;
-    static std::atomic<bool> attr_done[64];
+    static std::atomic<bool> attr_done[2][64];
     int dev = -1;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return qg::cuda_fail(cudaGetLastError());
-    auto kern = FMT == 0 ? tc::qg_gemm_tc_kernel : tc::qg_gemm_tc_x_kernel<FMT == 2, XP>;
+    // the factored kernel with the smaller token bound that holds M
+    constexpr int kMT0 = XP == 3 ? 8 : 16, kMT1 = 32 / XP / 2 * 2;
+    const bool small = M <= kMT0;
+    auto kern = FMT == 0 ? tc::qg_gemm_tc_kernel
+                : small  ? tc::qg_gemm_tc_x_kernel<FMT == 2, XP, kMT0>
+                         : tc::qg_gemm_tc_x_kernel<FMT == 2, XP, kMT1>;
+    std::atomic<bool>& attr = attr_done[small ? 0 : 1][dev];
     // as many raw stages as fit (the x part of a stage is M KB)
     const int raw0 = FMT == 0 ? tc::kRaw0Q4K : IQ3 ? tc::kRaw0X3 : tc::kRaw0XQ;
     const int nraw = std::min(tc::kMaxRaw, (tc::kSmemMax - raw0) / tc::raw_stage_bytes(M));
     if (nraw < 2) return QG_EINVAL;
     const int smem = raw0 + nraw * tc::raw_stage_bytes(M);
-    if (!attr_done[dev].load(std::memory_order_acquire)) {
+    if (!attr.load(std::memory_order_acquire)) {
         if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, tc::kSmemMax) != cudaSuccess)
             return qg::cuda_fail(cudaGetLastError());
-        attr_done[dev].store(true, std::memory_order_release);
+        attr.store(true, std::memory_order_release);
     }
     auto encode = tensor_map_encoder();
     if (!encode) return qg::cuda_fail(cudaGetLastError());
