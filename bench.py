@@ -180,7 +180,8 @@ _COMMON = ["common.cuh", "gemv_kernel.cuh", "launch.h", "tensor_map.h", "launch_
 KERNEL_SOURCES = {
     "q4k": _COMMON + ["launch_q4k.cuh", "gemv_q4k.cu"],
     "iq3": _COMMON + ["launch_iq3.cuh", "gemv_iq3.cu"],
-    "tc": ["common.cuh", "gemv_kernel.cuh", "launch.h", "tensor_map.h", "../../include/qgemv.h", "gemm_tc.cu"],
+    "tc": ["common.cuh", "gemv_kernel.cuh", "launch.h", "tensor_map.h", "../../include/qgemv.h", "gemm_tc.cu",
+           "launch_q4k.cuh", "launch_iq3.cuh"],
     "cb": _COMMON + ["gemv_cb.cu"],
 }
 

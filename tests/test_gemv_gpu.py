@@ -473,6 +473,26 @@ def test_gemv_q4k_x_range(q, scale, M):
     check_tol(y, Y, A, TAU_FMA, f"x scale {scale:g}, M={M}")
 
 
+@pytest.mark.parametrize("scale", [2.0 ** -100, 2.0 ** -60, 1.0, 2.0 ** 60, 2.0 ** 100])
+@pytest.mark.parametrize("fmt", ["q4k", "iq3"])
+def test_gemv_x_range_tensor_cores(q, fmt, scale):
+    """From 5 tokens both formats run on the tensor cores with x split into
+    three bf16 parts and multiplied as given: the stated range |x| within
+    [2^-100, 2^100] meets the fp32 bar."""
+    N, K, M = 96, 2048, 8
+    x = (synth.gen_x(M, K, 40) * np.float32(scale)).astype(np.float32)
+    if fmt == "q4k":
+        W = synth.gen_q4k(N, K, 41)
+        Y, A = oracle.gemv_q4k(W, x)
+        y = q.qgemv_q4k(dev(W), dev(x)).cpu().numpy()
+    else:
+        W, grid = synth.gen_iq3(N, K, 42)
+        Y, A = oracle.gemv_iq3(W, grid, x)
+        y = q.qgemv_iq3(dev(W), dev(grid), dev(x)).cpu().numpy()
+    assert np.isfinite(y).all()
+    check_tol(y, Y, A, TAU_FMA, f"{fmt} tensor cores x scale {scale:g}")
+
+
 @pytest.mark.parametrize("M", [1, 4])
 def test_gemv_subnormal_x(q, M):
     """x entirely subnormal (|x| < 2^-137) against blocks with d near 2^15:
