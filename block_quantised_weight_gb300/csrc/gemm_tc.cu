@@ -9,17 +9,20 @@
 //     dequantised (page 1 "Rewriting picoLM in Python", dequantize_q4_K:
 //     (d*sc)*q - dmin*mn) exactly in fp32 and rounded once to bf16 (to
 //     nearest even); X is rounded to bf16 likewise.
-//   qg_gemm_tc_iq3x_kernel<XP> (IQ3): the signed grid bytes enter the MMA
-//     exactly and each sub-block factor is applied after it (see there); x
-//     in XP bf16 parts (XP = 3 from 5 to 10 tokens: exact products; XP = 1
-//     from 16 tokens).
+//   qg_gemm_tc_x_kernel<Q4K, XP, MT> (Q4_K from 5 to 15 tokens, IQ3 from 5
+//     tokens): each weight's small integer (Q4_K q - c, IQ3 the signed grid
+//     byte) enters the MMA exactly and the sub-block factors are applied
+//     after it (see there); x in XP bf16 parts (XP = 3 up to 10 tokens per
+//     launch: exact products, the fp32 bar; XP = 1 from 16 tokens).
 //
 // CTA roles (320 threads):
 //   warps 0-7  dequantise W into tensor memory and X into shared memory:
 //              warps 0-3 the first 128 k of each unit, warps 4-7 the second
-//              (thread = tile row = TMEM lane); warps 0-3 then drain the
-//              accumulator (tcgen05.ld, warp w reads TMEM lanes 32w..32w+31)
-//              into Y;
+//              (thread = tile row = TMEM lane); then read the sums back
+//              (tcgen05.ld, warp w reads TMEM lanes 32 (w mod 4) ..): in
+//              qg_gemm_tc_kernel warps 0-3 drain the accumulator into Y per
+//              segment, in the factored kernel each half's warps take their
+//              sub-blocks' sums every unit;
 //   warp 8     producer: one 2D tensor-map TMA per unit for the 128 rows x
 //              block column of W (Q4_K: 144 bytes; IQ3: the 112 bytes from
 //              the block's offset rounded down to 16, the block starting
@@ -37,9 +40,9 @@
 // of the one before, and a segment's drain the next segment's MMAs.
 //
 // Tensor memory (512 columns): A of half h, buffer b at columns 64 (2h + b)
-// (row = lane, k pairs as bf16x2 per column, k ascending); the Q4_K
-// accumulators at 256 and 288 (D[row][token], fp32, 32 columns each), the
-// IQ3 sub-block sums at 256 + 128 h + 32 j.
+// (row = lane, k pairs as bf16x2 per column, k ascending); the accumulators
+// of qg_gemm_tc_kernel at 256 and 288 (D[row][token], fp32, 32 columns
+// each), the factored kernel's sub-block sums at 256 + 128 h + 32 j.
 //
 // Exact Q4_K weights: with the fp16 magic h = 1024 + q, one fp16 FMA gives
 // h*sc - 1024*sc = q*sc exactly (at most 945: the fused product is rounded
@@ -70,8 +73,9 @@ constexpr int kThreads = 320;  // 8 dequant warps, producer, MMA
 constexpr int kRawW = kTileRows * kBlockBytes;     // 18432: TMA box 144 x 128 (IQ3: 112 x 128, x after 18432 too)
 constexpr int kIQ3Box = 112;
 constexpr int kMaxRaw = 6;                          // raw stages (W box + the unit's x, M KB)
-// Shared memory: barriers, the four x stages, (IQ3) the tables, and the raw
-// ring at the end: as many stages of kRawW + M * 1024 bytes as fit.
+// Shared memory: barriers, the four x stages, (factored kernel) the IQ3
+// tables or the Q4_K x sums, and the raw ring at the end: as many stages of
+// kRawW + M * 1024 bytes as fit.
 constexpr int kB0 = 1024;
 constexpr int kBStage = 2 * 32 * 128;               // 8192: two 64-k atoms of 32 token rows
 constexpr int kRaw0Q4K = kB0 + 4 * kBStage;         // 33792
