@@ -8,6 +8,10 @@ boundary, at least two ring stages inside the per-CTA limit, and each
 super-block inside the box that carries it (an IQ3 block of 98 bytes starts
 0..14 bytes into its 112-byte box, since the box's x coordinate is the
 block's byte offset rounded down to 16).
+
+tests/tc_layout_probe.cu does the same for the tcgen05 kernels of
+gemm_tc.cu: every token count their launchers accept, with the ring rule of
+launch_tc.
 """
 import json
 import os
@@ -93,3 +97,44 @@ def test_every_block_lies_inside_its_box(layouts):
             box_x = start & ~15  # the tensor-map x coordinate: a multiple of 16 bytes
             assert box_x % 16 == 0
             assert start - box_x + c["block_bytes"] <= c["box_bytes"], (c["fmt"], col)
+
+
+@pytest.fixture(scope="module")
+def tc_layouts(tmp_path_factory):
+    nvcc = shutil.which("nvcc") or "/usr/local/cuda/bin/nvcc"
+    if not os.path.exists(nvcc):
+        pytest.skip("nvcc not found")
+    exe = str(tmp_path_factory.mktemp("tc_layout") / "tc_layout_probe")
+    subprocess.run([nvcc, "-std=c++17", "-gencode", "arch=compute_103a,code=sm_103a", "-I", CSRC,
+                    "-I", os.path.join(ROOT, "include"), os.path.join(ROOT, "tests", "tc_layout_probe.cu"), "-o", exe],
+                   check=True, capture_output=True, timeout=300)
+    out = subprocess.run([exe], check=True, capture_output=True, text=True, timeout=60).stdout
+    return [json.loads(line) for line in out.splitlines() if line.strip()]
+
+
+def test_tc_every_token_count_is_listed(tc_layouts):
+    got = {(c["fmt"], c["xp"], c["M"]) for c in tc_layouts}
+    assert got == ({(0, 1, m) for m in range(16, 33)} | {(1, 1, m) for m in range(16, 33)}
+                   | {(1, 3, m) for m in range(1, 11)} | {(2, 3, m) for m in range(1, 11)})
+
+
+def test_tc_rings_fit_and_align(tc_layouts):
+    """At least two raw stages within the per-CTA limit; the raw ring, each
+    stage and its x part (a TMA destination) on 1024-byte boundaries; the x
+    stages (swizzled MMA operands) on 1024-byte boundaries; nothing below the
+    ring reaches into it; the W box inside the stage's W part."""
+    for c in tc_layouts:
+        assert 2 <= c["nraw"] and c["smem"] <= c["smem_max"], c
+        assert c["raw0"] % 1024 == 0 and c["stage"] % 1024 == 0 and c["raw_w"] % 1024 == 0, c
+        assert c["below"] <= c["raw0"], c
+        assert c["b0"] % 1024 == 0 and c["b_stage"] % 1024 == 0 and c["b0"] + 4 * c["b_stage"] <= c["below"], c
+        assert c["box_bytes"] * c["tile_rows"] <= c["raw_w"], c
+
+
+def test_tc_operands_and_tensor_memory(tc_layouts):
+    """x rows (token parts) fit a 32-row atom and the MMA's N; the mbarriers
+    end below the TMEM address slot; every TMEM column used is allocated."""
+    for c in tc_layouts:
+        assert c["x_rows"] <= 32 and c["x_rows"] <= c["ncol"] and c["ncol"] in (16, 32), c
+        assert c["barrier_bytes"] <= c["tmem_slot"], c
+        assert c["tmem_end"] <= c["tmem_cols"] == 512, c
