@@ -228,7 +228,9 @@ def group_arrays(Ws, Ys, Ns):
 
 
 def qgemv_q4k_group(Ws, X, outs=None, stream=None, flags=0):
-    """[X @ dequant(W_i)^T for W_i in Ws] in one launch (all W_i share K)."""
+    """[X @ dequant(W_i)^T for W_i in Ws] (all W_i share K): one launch per token
+    group of up to 4 on the FMA path; from 5 tokens one tensor-core launch per
+    matrix and group of up to 10."""
     import torch
     Xv = X.view(1, -1) if X.dim() == 1 else X
     M, K = Xv.shape
@@ -353,7 +355,8 @@ def qgemv_q4k_pass_noalloc(stages, M=1, stream=None):
 
 
 def qgemm_q4k_batched(W, X, out=None, stream=None):
-    """Batched Q4_K GEMM: M < 16 on the fp32 FMA path, M >= 16 on tcgen05 (bf16 operands)."""
+    """Batched Q4_K GEMM: M < 16 as qgemv_q4k (fp32 FMA path up to 4 tokens, tensor
+    cores with exact products from 5), M >= 16 on tcgen05 with bf16 weights."""
     X, out, M, N, K = _xy(W, X, out, 144)
     _check("qgemm_q4k_batched", load().qgemm_q4k_batched(W.data_ptr(), X.data_ptr(), out.data_ptr(), M, N, K,
                                                          _stream(stream)))
@@ -361,7 +364,9 @@ def qgemm_q4k_batched(W, X, out=None, stream=None):
 
 
 def qgemm_iq3_batched(W, grid, X, out=None, stream=None):
-    """Batched IQ3 GEMM: M >= 16 (K/256 a multiple of 8) on tcgen05 (bf16 operands), else the FMA path."""
+    """Batched IQ3 GEMM: with K/256 a multiple of 8, from 5 tokens on tcgen05 with the
+    weights exact (x in three bf16 parts below 16 tokens, rounded to bf16 from
+    16); otherwise the fp32 FMA path."""
     import torch
     _req(grid, torch.uint8, "grid")
     X, out, M, N, K = _xy(W, X, out, 98)
